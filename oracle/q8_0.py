@@ -1,0 +1,55 @@
+"""Q8_0 block quantisation for the oracle -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg may import this module.  It shares no code with the CUDA path.
+
+The Q8_0 weight format is named (never defined) on the minfer page "Qwen2 /
+Qwen2.5 Architecture Support", section 3 (the tied output matmul "is a
+n_vocab x n_embd Q4_0/Q8_0 matmul") and section 6 (quant support).  The
+reading used here, in float32 as the quantising side decides it:
+
+* a block is 32 consecutive elements along the input (K) dimension of one
+  weight row;
+* ``amax = max |x|`` over the block, ``d = amax / 127`` (float32 division);
+* ``q = clamp(round_half_away_from_zero(x / d), -127, 127)`` with a true
+  float32 division by the unrounded ``d``; ``q = 0`` where ``d == 0``;
+* the stored scale is ``float16(d)`` (round to nearest even);
+* dequantised value ``= float32(scale) * q`` (exact in float32: an 11-bit
+  significand times a 7-bit integer).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+QK = 32
+
+
+def quantize_q8_0(w: np.ndarray):
+    """Quantise a float16 matrix ``[rows, K]`` (K a multiple of 32).
+
+    Returns ``(q, d)``: ``q`` int8 ``[rows, K]`` and ``d`` float16
+    ``[rows, K // 32]``.
+    """
+    w = np.asarray(w)
+    rows, k = w.shape
+    if k % QK:
+        raise ValueError(f"K={k} is not a multiple of {QK}")
+    x = w.astype(np.float32).reshape(rows, k // QK, QK)
+    amax = np.max(np.abs(x), axis=2)                       # float32
+    d = (amax / np.float32(127.0)).astype(np.float32)      # float32 division
+    safe = np.where(d == 0, np.float32(1.0), d)[:, :, None]
+    v = (x / safe).astype(np.float32)                      # float32 division
+    # Round half away from zero: |v| <= 127.0001, so |v| + 0.5 is exact in
+    # float32 and its floor is the rounded magnitude.
+    r = np.sign(v) * np.floor(np.abs(v) + np.float32(0.5))
+    r = np.clip(r, -127, 127)
+    r = np.where((d == 0)[:, :, None], 0, r)
+    q = r.astype(np.int8).reshape(rows, k)
+    return q, d.astype(np.float16)
+
+
+def dequantize_q8_0(q: np.ndarray, d: np.ndarray) -> np.ndarray:
+    """Exact dequantisation to float64: ``float(scale) * q`` per block."""
+    rows, k = q.shape
+    scale = d.astype(np.float64)[:, :, None]
+    return (scale * q.reshape(rows, k // QK, QK).astype(np.float64)).reshape(rows, k)
