@@ -1,0 +1,216 @@
+/*
+ * qwen2.h -- C ABI of libqwen2: a single-GPU (GB300, sm_103a) forward of the
+ * Qwen2 / Qwen2.5 dense decoder.
+ *
+ * The forward each call runs is the layer of the minfer page "Qwen2 /
+ * Qwen2.5 Architecture Support", section 1:
+ *
+ *   h - RMSNorm - WQ/WK/WV matmuls + bias - RoPE(Q, K) - KV store
+ *     - GQA attention (Q K^T scale -> softmax -> V) - WO matmul - + residual
+ *     - RMSNorm - gate/up matmuls - SiLU(gate) * up - down matmul - + residual
+ *
+ * repeated n_layer times, then the final RMSNorm and the tied LM head
+ * (W_lm = E; Module 7 -- Qwen2 / Qwen2.5, section 7.3; nnterp encyclopedia
+ * qwen2, "The readout is the plain projection") and a greedy argmax taken on
+ * the device (Module 7 section 7.3, performance note: GPU argmax avoids
+ * reading back the 151936 logits each step).
+ *
+ * Conventions for every entry point:
+ *  - Return value: QWEN2_OK (0) or one of the QWEN2_E_* codes below.  On an
+ *    argument, position or support error nothing has been enqueued on the
+ *    stream and no output or cache slot has been written;
+ *    qwen2_last_error() holds a message.
+ *  - "host" pointers are ordinary CPU memory; they are read before the call
+ *    returns and may be reused at once.  Output pointers (logits, ids,
+ *    hidden) may be device memory or host memory: the library copies through
+ *    the unified address space.  If any output pointer is host memory the
+ *    call synchronises the stream before it returns; otherwise it does not
+ *    block the host.
+ *  - `stream` is a cudaStream_t passed as void* (NULL: the legacy default
+ *    stream).  All device work of a call is ordered on that stream.
+ *  - A context is single-threaded: no two calls on one context may run at
+ *    the same time.
+ */
+#ifndef QWEN2_H
+#define QWEN2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- error codes --------------------------------------------------------- */
+#define QWEN2_OK                 0
+#define QWEN2_E_ARG              1  /* null pointer, token outside [0, vocab), bad count or sequence id */
+#define QWEN2_E_POS              2  /* a position outside [0, n_ctx): a hard error, never truncation
+                                       (minfer page section 6: positions[i] < n_ctx is enforced with a
+                                       hard Err in the KV-store arm; section 7 item 5) */
+#define QWEN2_E_UNSUPPORTED      3  /* a config this build does not implement (e.g. head_dim != 64) */
+#define QWEN2_E_OOM              4  /* device allocation failed */
+#define QWEN2_E_CUDA             5  /* a CUDA runtime call failed */
+#define QWEN2_E_DEVICE_GUARD     6  /* a kernel's own guard tripped (found at qwen2_synchronize) */
+
+/* ---- weight storage formats -------------------------------------------- */
+#define QWEN2_WEIGHTS_F16        0  /* f16 linear weights and LM head, f32 biases and norm weights
+                                       (Module 7 section 7.4) */
+#define QWEN2_WEIGHTS_Q8_0       1  /* the seven linear weights and the tied embedding / LM head held as
+                                       Q8_0 blocks: 32 int8 values along K plus one f16 scale per block;
+                                       quantised by the library from the f16 weights given to create */
+
+/* ---- prefill arithmetic -------------------------------------------------- */
+#define QWEN2_PREFILL_F32        0  /* f32 activations, f32 accumulation on CUDA cores */
+#define QWEN2_PREFILL_TENSOR     1  /* tensor-core (tcgen05) GEMMs on f16 operands with f32 accumulation;
+                                       residual, norm statistics, softmax and the KV cache stay f32 */
+
+/* ---- flags ------------------------------------------------------------- */
+#define QWEN2_FLAG_NO_FUSE_QKV   0x1u  /* separate norm, Q, K and V products and epilogue kernels instead of
+                                          the fused QKV kernel (minfer page section 3, MINFER_NO_FUSE_QKV);
+                                          results are bit-identical either way */
+#define QWEN2_FLAG_NO_FUSE_FFN   0x2u  /* separate norm, gate, up and SiLU*up kernels (MINFER_NO_FUSE_FFN) */
+#define QWEN2_FLAG_NO_GRAPH      0x4u  /* launch decode kernels one by one, without a CUDA graph */
+#define QWEN2_FLAG_NO_MEGAKERNEL 0x8u  /* decode with one kernel per step of the layer instead of the
+                                          persistent single-launch decode kernel */
+
+typedef struct qwen2_config {
+    int32_t n_layer;        /* num_hidden_layers (24 on Qwen2.5-0.5B) */
+    int32_t hidden;         /* hidden_size H (896); must be n_head * head_dim and a multiple of 128 */
+    int32_t n_head;         /* num_attention_heads (14) */
+    int32_t n_kv_head;      /* num_key_value_heads (2); must divide n_head, n_head/n_kv_head <= 8 */
+    int32_t head_dim;       /* H / n_head (64); this build supports 64 */
+    int32_t intermediate;   /* intermediate_size I (4864); a multiple of 128 */
+    int32_t vocab;          /* vocab_size V (151936) */
+    float   rms_eps;        /* rms_norm_eps (1e-6) */
+    double  rope_theta;     /* rope_theta (1e6) */
+    int32_t weight_format;  /* QWEN2_WEIGHTS_* */
+    int32_t prefill_mode;   /* QWEN2_PREFILL_* */
+    int32_t n_ctx;          /* KV positions per sequence; positions must lie in [0, n_ctx) */
+    int32_t max_seqs;       /* number of sequence slots (KV caches) */
+    int32_t max_tokens;     /* most rows one qwen2_prefill call may carry (sum over its sequences) */
+    uint32_t flags;         /* QWEN2_FLAG_* */
+} qwen2_config;
+
+/* One decoder layer, host memory, HF layout [out_features][in_features]
+ * (Module 7 Lab 7; nnterp "Printout").  f16 values are IEEE binary16 bit
+ * patterns (uint16_t). */
+typedef struct qwen2_layer_weights {
+    const uint16_t *wq;   /* [n_head*head_dim][H]      q_proj.weight */
+    const uint16_t *wk;   /* [n_kv_head*head_dim][H]   k_proj.weight */
+    const uint16_t *wv;   /* [n_kv_head*head_dim][H]   v_proj.weight */
+    const uint16_t *wo;   /* [H][n_head*head_dim]      o_proj.weight (no bias) */
+    const uint16_t *wg;   /* [I][H]                    mlp.gate_proj.weight */
+    const uint16_t *wu;   /* [I][H]                    mlp.up_proj.weight */
+    const uint16_t *wd;   /* [H][I]                    mlp.down_proj.weight */
+    const float *bq;      /* [n_head*head_dim]         q_proj.bias */
+    const float *bk;      /* [n_kv_head*head_dim]      k_proj.bias */
+    const float *bv;      /* [n_kv_head*head_dim]      v_proj.bias */
+    const float *attn_norm;  /* [H] input_layernorm.weight */
+    const float *ffn_norm;   /* [H] post_attention_layernorm.weight */
+} qwen2_layer_weights;
+
+typedef struct qwen2_weights {
+    const uint16_t *embed;             /* [V][H] embed_tokens.weight; also the LM head (tied) */
+    const float *final_norm;           /* [H] model.norm.weight */
+    const qwen2_layer_weights *layers; /* [n_layer] */
+} qwen2_weights;
+
+typedef struct qwen2_ctx qwen2_ctx;
+
+/* Create a context on the current CUDA device: validate `cfg`, pack and
+ * upload the weights (the library keeps its own device copies; the host
+ * arrays may be freed after the call), allocate the zeroed KV cache of
+ * max_seqs sequences, the workspace and the RoPE table.  Synchronous.
+ * Errors: QWEN2_E_ARG (null pointers, non-positive sizes), QWEN2_E_UNSUPPORTED
+ * (head_dim != 64, H != n_head*head_dim, H or I not a multiple of 128,
+ * n_head % n_kv_head != 0, group > 8), QWEN2_E_OOM, QWEN2_E_CUDA.
+ * On success *out receives the context; on failure *out is set to NULL and
+ * qwen2_last_error(NULL) describes the failure. */
+int qwen2_create(const qwen2_config *cfg, const qwen2_weights *weights, qwen2_ctx **out);
+
+/* Free every device buffer of the context (synchronises the device first).
+ * NULL is accepted. */
+void qwen2_destroy(qwen2_ctx *ctx);
+
+/* Message of the last failed call on `ctx` ("" if none); with ctx == NULL,
+ * the calling thread's last qwen2_create failure.  The string stays valid
+ * until the next call on the same context (or thread). */
+const char *qwen2_last_error(const qwen2_ctx *ctx);
+
+/* The KV cache as caller-visible device memory: *base receives a device
+ * pointer to f32 [max_seqs][n_layer][2][n_kv_head][n_ctx][head_dim]
+ * (index 0 of the third axis holds rotated keys, 1 values; slot = position),
+ * contiguous row-major; dims[0..5] receive those six sizes.  The memory is
+ * owned by the context; the caller may read or write it between calls, in
+ * stream order (e.g. to save and restore a conversation). */
+int qwen2_kv_cache(qwen2_ctx *ctx, float **base, int64_t dims[6]);
+
+/* Prefill: run the rows of n_seq sequences through the forward, storing
+ * every row's key and value at its position in its sequence's cache.
+ *   seq_ids   host int32 [n_seq], distinct, each in [0, max_seqs)
+ *   n_tokens  host int32 [n_seq], each >= n_out; their sum <= max_tokens
+ *   tokens    host int32 [sum n_tokens], sequence after sequence, in [0, V)
+ *   positions host int32 [sum n_tokens], in [0, n_ctx)
+ *   n_out     rows per sequence that reach the LM head: the last n_out rows
+ *             of each sequence (minfer page, section 3, "G3 tail-row
+ *             optimization": the other rows are cut before the last layer's
+ *             attention output, since only the kept rows' results are used)
+ *   logits    nullable; f32 [n_seq*n_out][V]
+ *   ids       nullable; int32 [n_seq*n_out], the lowest index of each row's
+ *             maximum logit
+ * A row at position p attends to cache slots 0..p of its sequence; all
+ * rows of a call are stored before any row attends. */
+int qwen2_prefill(qwen2_ctx *ctx, int32_t n_seq, const int32_t *seq_ids,
+                  const int32_t *n_tokens, const int32_t *tokens,
+                  const int32_t *positions, int32_t n_out,
+                  float *logits, int32_t *ids, void *stream);
+
+/* One decode step: one row for each of n_seq sequences.
+ *   seq_ids, tokens, positions  host int32 [n_seq]
+ *   logits  nullable; f32 [n_seq][V]
+ *   ids     nullable; int32 [n_seq] greedy ids */
+int qwen2_decode_step(qwen2_ctx *ctx, int32_t n_seq, const int32_t *seq_ids,
+                      const int32_t *tokens, const int32_t *positions,
+                      float *logits, int32_t *ids, void *stream);
+
+/* n_steps greedy decode steps without a host round trip per step: step 0
+ * feeds first_tokens at start_positions, each later step feeds the previous
+ * step's ids at the next position (positions are data, minfer page section
+ * 6).  ids: int32 [n_steps][n_seq].  Fails with QWEN2_E_POS (nothing run)
+ * if any start_position + n_steps > n_ctx. */
+int qwen2_decode_steps(qwen2_ctx *ctx, int32_t n_seq, const int32_t *seq_ids,
+                       const int32_t *first_tokens, const int32_t *start_positions,
+                       int32_t n_steps, int32_t *ids, void *stream);
+
+/* Copy the final-norm output rows (the input of the LM head,
+ * "final_norm_output" in the nnterp names) of the last prefill or decode
+ * step into dst: f32 [rows][H], rows <= n_seq*n_out of that call.  Device or
+ * host dst. */
+int qwen2_final_hidden(qwen2_ctx *ctx, float *dst, int32_t rows, void *stream);
+
+/* Synchronise `stream` and report any device-side guard that tripped since
+ * the last check (QWEN2_E_DEVICE_GUARD, with the guard's code in the
+ * message); clears the guard word. */
+int qwen2_synchronize(qwen2_ctx *ctx, void *stream);
+
+/* Bytes of packed weights resident on the device (linear weights, LM head,
+ * biases, norm weights and, for Q8_0, scales), with 256-byte alignment
+ * padding between tensors. */
+int64_t qwen2_weight_bytes(const qwen2_ctx *ctx);
+
+/* Bytes one sequence's KV cache takes: n_layer * 2 * n_kv_head * n_ctx *
+ * head_dim * 4 (24 KB per position on Qwen2.5-0.5B, minfer page section 6). */
+int64_t qwen2_kv_bytes_per_seq(const qwen2_config *cfg);
+
+/* Host-only Q8_0 quantisation of an f16 matrix [rows][k] (k a multiple of
+ * 32), as the library's packer does it: blocks of 32 along k;
+ * d = max|x| / 127 in f32; q = clamp(round-half-away(x / d), -127, 127)
+ * (q = 0 where d = 0); the stored scale is f16(d), round to nearest even.
+ * q: int8 [rows][k]; d: f16 bits [rows][k/32].  Needs no GPU.  The format
+ * is named, not defined, on the minfer page (sections 3 and 6). */
+int qwen2_quantize_q8_0(const uint16_t *w, int64_t rows, int64_t k, int8_t *q, uint16_t *d);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QWEN2_H */

@@ -1,0 +1,497 @@
+// The C ABI of libqwen2: argument validation, context set-up (weight
+// packing, KV cache, workspace, RoPE table), decode CUDA graphs, and the
+// prefill / decode entry points declared in include/qwen2.h.
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <set>
+#include <string>
+#include <vector>
+
+#include "ctx.h"
+#include "prefill.h"
+
+using namespace qwen2;
+
+struct qwen2_ctx {
+    Ctx c;
+};
+
+namespace {
+
+thread_local std::string g_create_error;
+
+int fail(Ctx* c, int code, const std::string& msg) {
+    if (c) c->last_error = msg;
+    else g_create_error = msg;
+    return code;
+}
+
+int cuda_fail(Ctx* c, cudaError_t e, const char* what) {
+    return fail(c, QWEN2_E_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+#define Q2_CHECK(c, call)                                  \
+    do {                                                   \
+        cudaError_t e_ = (call);                           \
+        if (e_ != cudaSuccess) return cuda_fail(c, e_, #call); \
+    } while (0)
+
+bool is_device_ptr(const void* p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
+template <class T>
+int dev_alloc(Ctx& c, T** p, size_t count, bool zero = true) {
+    void* v = nullptr;
+    const size_t bytes = std::max<size_t>(count, 1) * sizeof(T);
+    if (cudaMalloc(&v, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return QWEN2_E_OOM;
+    }
+    if (zero && cudaMemset(v, 0, bytes) != cudaSuccess) {
+        cudaFree(v);
+        return QWEN2_E_CUDA;
+    }
+    c.allocs.push_back(v);
+    *p = static_cast<T*>(v);
+    return QWEN2_OK;
+}
+
+int validate_config(const qwen2_config* g, std::string& msg) {
+    if (g->n_layer < 1 || g->hidden < 1 || g->n_head < 1 || g->n_kv_head < 1 || g->head_dim < 1 ||
+        g->intermediate < 1 || g->vocab < 2 || g->n_ctx < 1 || g->max_seqs < 1 || g->max_tokens < 1) {
+        msg = "config sizes must be positive";
+        return QWEN2_E_ARG;
+    }
+    if (!(g->rms_eps >= 0.f) || !(g->rope_theta > 0.0)) {
+        msg = "rms_eps must be >= 0 and rope_theta > 0";
+        return QWEN2_E_ARG;
+    }
+    if (g->head_dim != 64) {
+        msg = "head_dim " + std::to_string(g->head_dim) + " is not supported (64 only)";
+        return QWEN2_E_UNSUPPORTED;
+    }
+    if (g->hidden != g->n_head * g->head_dim) {
+        msg = "hidden must equal n_head * head_dim";
+        return QWEN2_E_UNSUPPORTED;
+    }
+    if (g->hidden % 128 || g->intermediate % 128) {
+        msg = "hidden and intermediate must be multiples of 128";
+        return QWEN2_E_UNSUPPORTED;
+    }
+    if (g->n_head % g->n_kv_head || g->n_head / g->n_kv_head > 8) {
+        msg = "n_head must be a multiple of n_kv_head with at most 8 query heads per kv head";
+        return QWEN2_E_UNSUPPORTED;
+    }
+    if (g->weight_format != QWEN2_WEIGHTS_F16) {
+        msg = "weight_format " + std::to_string(g->weight_format) + " is not supported by this build";
+        return QWEN2_E_UNSUPPORTED;
+    }
+    if (g->prefill_mode != QWEN2_PREFILL_F32) {
+        msg = "prefill_mode " + std::to_string(g->prefill_mode) + " is not supported by this build";
+        return QWEN2_E_UNSUPPORTED;
+    }
+    if ((int64_t)g->vocab * g->hidden > INT32_MAX * 8LL) {
+        msg = "vocab * hidden too large";
+        return QWEN2_E_UNSUPPORTED;
+    }
+    return QWEN2_OK;
+}
+
+int validate_weights(const qwen2_config* g, const qwen2_weights* w, std::string& msg) {
+    if (!w->embed || !w->final_norm || !w->layers) {
+        msg = "null weight pointer";
+        return QWEN2_E_ARG;
+    }
+    for (int l = 0; l < g->n_layer; ++l) {
+        const qwen2_layer_weights& L = w->layers[l];
+        if (!L.wq || !L.wk || !L.wv || !L.wo || !L.wg || !L.wu || !L.wd || !L.bq || !L.bk || !L.bv ||
+            !L.attn_norm || !L.ffn_norm) {
+            msg = "null weight pointer in layer " + std::to_string(l);
+            return QWEN2_E_ARG;
+        }
+    }
+    return QWEN2_OK;
+}
+
+int setup_workspace(Ctx& c) {
+    const qwen2_config& g = c.cfg;
+    const int H = g.hidden, I = g.intermediate, nq = g.n_head * g.head_dim;
+    const int R = std::max(g.max_tokens, g.max_seqs);
+    const int S = g.max_seqs;
+    c.max_rows = R;
+    Workspace& w = c.ws;
+    w.att_max_chunks = (g.n_ctx + 63) / 64;
+    w.am_blocks = c.n_sm * 2;
+    int r = QWEN2_OK;
+    auto A = [&](auto** p, size_t n) {
+        if (r == QWEN2_OK) r = dev_alloc(c, p, n);
+    };
+    A(&w.x, (size_t)R * H);
+    A(&w.xn, (size_t)R * H);
+    A(&w.q, (size_t)R * nq);
+    A(&w.o, (size_t)R * nq);
+    A(&w.mlp, (size_t)R * I);
+    A(&w.raw, (size_t)S * std::max(c.nqkv, 2 * I));
+    A(&w.att_part, (size_t)S * g.n_head * w.att_max_chunks * (g.head_dim + 2));
+    A(&w.att_count, (size_t)S * g.n_kv_head);
+    A(&w.am_val, (size_t)w.am_blocks * 8);
+    A(&w.am_idx, (size_t)w.am_blocks * 8);
+    A(&w.am_count, 1);
+    A(&w.hidden, (size_t)R * H);
+    A(&w.logits, (size_t)S * g.vocab);
+    A(&w.rows_tok, R);
+    A(&w.rows_pos, R);
+    A(&w.rows_slot, R);
+    A(&w.keep_rows, R);
+    A(&w.keep_pos, R);
+    A(&w.keep_slot, R);
+    A(&w.blk, (size_t)4 * R);
+    A(&w.x2, (size_t)R * H);
+    A(&w.q2, (size_t)R * nq);
+    A(&w.ids, R);
+    A(&c.ds.tok, S);
+    A(&c.ds.pos, S);
+    A(&c.ds.slot, S);
+    A(&c.ds.step, 1);
+    A(&c.ds.ids_hist, (size_t)kIdsHist * S);
+    A(&c.err, 1);
+    return r;
+}
+
+// Sequence ids distinct and in range.
+int check_seq_ids(Ctx& c, int n_seq, const int32_t* seq_ids) {
+    std::set<int> seen;
+    for (int i = 0; i < n_seq; ++i) {
+        if (seq_ids[i] < 0 || seq_ids[i] >= c.cfg.max_seqs)
+            return fail(&c, QWEN2_E_ARG, "sequence id " + std::to_string(seq_ids[i]) + " outside [0, max_seqs)");
+        if (!seen.insert(seq_ids[i]).second)
+            return fail(&c, QWEN2_E_ARG, "sequence id " + std::to_string(seq_ids[i]) + " repeated");
+    }
+    return QWEN2_OK;
+}
+
+int check_tokens(Ctx& c, int n, const int32_t* tokens) {
+    for (int i = 0; i < n; ++i)
+        if (tokens[i] < 0 || tokens[i] >= c.cfg.vocab)
+            return fail(&c, QWEN2_E_ARG, "token " + std::to_string(tokens[i]) + " outside [0, vocab)");
+    return QWEN2_OK;
+}
+
+int check_positions(Ctx& c, int n, const int32_t* pos, int extra) {
+    for (int i = 0; i < n; ++i)
+        if (pos[i] < 0 || (int64_t)pos[i] + extra > c.cfg.n_ctx - 1)
+            return fail(&c, QWEN2_E_POS, "position " + std::to_string(pos[i]) +
+                                             (extra ? " + " + std::to_string(extra) : std::string()) +
+                                             " outside [0, n_ctx=" + std::to_string(c.cfg.n_ctx) + ")");
+    return QWEN2_OK;
+}
+
+int get_graph(Ctx& c, int B, bool want_logits, cudaGraphExec_t* out) {
+    const int key = B | (want_logits ? 1 << 16 : 0);
+    auto it = c.graphs.find(key);
+    if (it != c.graphs.end()) {
+        *out = it->second;
+        return QWEN2_OK;
+    }
+    cudaGraph_t graph = nullptr;
+    Q2_CHECK(&c, cudaStreamBeginCapture(c.cap_stream, cudaStreamCaptureModeThreadLocal));
+    cudaError_t e = enqueue_decode_step(c, B, want_logits, c.cap_stream);
+    cudaError_t e2 = cudaStreamEndCapture(c.cap_stream, &graph);
+    if (e != cudaSuccess) return cuda_fail(&c, e, "decode step capture");
+    if (e2 != cudaSuccess) return cuda_fail(&c, e2, "cudaStreamEndCapture");
+    cudaGraphExec_t exec = nullptr;
+    e = cudaGraphInstantiate(&exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess) return cuda_fail(&c, e, "cudaGraphInstantiate");
+    c.graphs[key] = exec;
+    *out = exec;
+    return QWEN2_OK;
+}
+
+int run_decode_step(Ctx& c, int B, bool want_logits, cudaStream_t st) {
+    if (c.cfg.flags & QWEN2_FLAG_NO_GRAPH) {
+        cudaError_t e = enqueue_decode_step(c, B, want_logits, st);
+        if (e != cudaSuccess) return cuda_fail(&c, e, "decode step launch");
+        return QWEN2_OK;
+    }
+    cudaGraphExec_t exec;
+    int r = get_graph(c, B, want_logits, &exec);
+    if (r != QWEN2_OK) return r;
+    Q2_CHECK(&c, cudaGraphLaunch(exec, st));
+    return QWEN2_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int qwen2_create(const qwen2_config* cfg, const qwen2_weights* weights, qwen2_ctx** out) {
+    g_create_error.clear();
+    if (!out) return fail(nullptr, QWEN2_E_ARG, "out is NULL");
+    *out = nullptr;
+    if (!cfg || !weights) return fail(nullptr, QWEN2_E_ARG, "cfg or weights is NULL");
+    std::string msg;
+    int r = validate_config(cfg, msg);
+    if (r == QWEN2_OK) r = validate_weights(cfg, weights, msg);
+    if (r != QWEN2_OK) return fail(nullptr, r, msg);
+
+    qwen2_ctx* h = new qwen2_ctx();
+    Ctx& c = h->c;
+    c.cfg = *cfg;
+    auto bail = [&](int code, const std::string& m) {
+        g_create_error = m;
+        qwen2_destroy(h);
+        return code;
+    };
+    if (cudaGetDevice(&c.device) != cudaSuccess) return bail(QWEN2_E_CUDA, "no CUDA device");
+    if (cudaDeviceGetAttribute(&c.n_sm, cudaDevAttrMultiProcessorCount, c.device) != cudaSuccess)
+        return bail(QWEN2_E_CUDA, "cannot read the SM count");
+    r = pack_weights(c, weights, msg);
+    if (r != QWEN2_OK) return bail(r, msg);
+    r = build_rope_table(c, msg);
+    if (r != QWEN2_OK) return bail(r, msg);
+    c.kv_floats = (size_t)cfg->max_seqs * qwen2_kv_bytes_per_seq(cfg) / 4;
+    r = dev_alloc(c, &c.kv, c.kv_floats);
+    if (r != QWEN2_OK) return bail(r, "KV cache allocation of " + std::to_string(c.kv_floats * 4) + " bytes failed");
+    r = setup_workspace(c);
+    if (r != QWEN2_OK) return bail(r, "workspace allocation failed");
+    int max_smem = 0;
+    cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, c.device);
+    if (decode_set_smem_limits(max_smem) != cudaSuccess || prefill_set_smem_limits() != cudaSuccess)
+        return bail(QWEN2_E_CUDA, "cannot set kernel shared-memory limits");
+    if (cudaStreamCreateWithFlags(&c.cap_stream, cudaStreamNonBlocking) != cudaSuccess)
+        return bail(QWEN2_E_CUDA, "cannot create the capture stream");
+    if (cudaDeviceSynchronize() != cudaSuccess) return bail(QWEN2_E_CUDA, "set-up failed on the device");
+    *out = h;
+    return QWEN2_OK;
+}
+
+void qwen2_destroy(qwen2_ctx* h) {
+    if (!h) return;
+    Ctx& c = h->c;
+    cudaDeviceSynchronize();
+    for (auto& kv : c.graphs) cudaGraphExecDestroy(kv.second);
+    if (c.cap_stream) cudaStreamDestroy(c.cap_stream);
+    for (void* p : c.allocs) cudaFree(p);
+    if (c.ws.out_logits) cudaFree(c.ws.out_logits);
+    if (c.rope) cudaFree(c.rope);
+    if (c.wblob) cudaFree(c.wblob);
+    cudaGetLastError();
+    delete h;
+}
+
+const char* qwen2_last_error(const qwen2_ctx* h) {
+    return h ? h->c.last_error.c_str() : g_create_error.c_str();
+}
+
+int qwen2_kv_cache(qwen2_ctx* h, float** base, int64_t dims[6]) {
+    if (!h || !base || !dims) return h ? fail(&h->c, QWEN2_E_ARG, "null argument") : QWEN2_E_ARG;
+    const qwen2_config& g = h->c.cfg;
+    *base = h->c.kv;
+    dims[0] = g.max_seqs;
+    dims[1] = g.n_layer;
+    dims[2] = 2;
+    dims[3] = g.n_kv_head;
+    dims[4] = g.n_ctx;
+    dims[5] = g.head_dim;
+    return QWEN2_OK;
+}
+
+int qwen2_prefill(qwen2_ctx* h, int32_t n_seq, const int32_t* seq_ids, const int32_t* n_tokens,
+                  const int32_t* tokens, const int32_t* positions, int32_t n_out, float* logits, int32_t* ids,
+                  void* stream) {
+    if (!h) return QWEN2_E_ARG;
+    Ctx& c = h->c;
+    c.last_error.clear();
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (n_seq < 1 || n_seq > c.cfg.max_seqs) return fail(&c, QWEN2_E_ARG, "n_seq outside [1, max_seqs]");
+    if (!seq_ids || !n_tokens || !tokens || !positions) return fail(&c, QWEN2_E_ARG, "null input pointer");
+    if (n_out < 1) return fail(&c, QWEN2_E_ARG, "n_out must be >= 1");
+    int r = check_seq_ids(c, n_seq, seq_ids);
+    if (r) return r;
+    int64_t total = 0;
+    for (int s = 0; s < n_seq; ++s) {
+        if (n_tokens[s] < n_out) return fail(&c, QWEN2_E_ARG, "a sequence has fewer than n_out tokens");
+        total += n_tokens[s];
+    }
+    if (total > c.cfg.max_tokens) return fail(&c, QWEN2_E_ARG, "more rows than max_tokens");
+    const int rows = (int)total;
+    if ((r = check_tokens(c, rows, tokens))) return r;
+    if ((r = check_positions(c, rows, positions, 0))) return r;
+
+    // Row plan: per-row slot, kept rows, attention query blocks.
+    std::vector<int> slot(rows), keep, plan;
+    std::vector<int> b0, bn, kb0, kbn;
+    int off = 0;
+    for (int s = 0; s < n_seq; ++s) {
+        const int n = n_tokens[s];
+        for (int i = 0; i < n; ++i) slot[off + i] = seq_ids[s];
+        for (int i = 0; i < n; i += kPrefillQB) {
+            b0.push_back(off + i);
+            bn.push_back(std::min(kPrefillQB, n - i));
+        }
+        const int k0 = (int)keep.size();
+        for (int i = n - n_out; i < n; ++i) keep.push_back(off + i);
+        for (int i = 0; i < n_out; i += kPrefillQB) {
+            kb0.push_back(k0 + i);
+            kbn.push_back(std::min(kPrefillQB, n_out - i));
+        }
+        off += n;
+    }
+    const int n_keep = (int)keep.size();
+    plan.insert(plan.end(), b0.begin(), b0.end());
+    plan.insert(plan.end(), bn.begin(), bn.end());
+    plan.insert(plan.end(), kb0.begin(), kb0.end());
+    plan.insert(plan.end(), kbn.begin(), kbn.end());
+    Workspace& w = c.ws;
+    Q2_CHECK(&c, cudaMemcpyAsync(w.rows_tok, tokens, rows * 4, cudaMemcpyHostToDevice, st));
+    Q2_CHECK(&c, cudaMemcpyAsync(w.rows_pos, positions, rows * 4, cudaMemcpyHostToDevice, st));
+    Q2_CHECK(&c, cudaMemcpyAsync(w.rows_slot, slot.data(), rows * 4, cudaMemcpyHostToDevice, st));
+    Q2_CHECK(&c, cudaMemcpyAsync(w.keep_rows, keep.data(), n_keep * 4, cudaMemcpyHostToDevice, st));
+    Q2_CHECK(&c, cudaMemcpyAsync(w.blk, plan.data(), plan.size() * 4, cudaMemcpyHostToDevice, st));
+    PrefillPlan pp;
+    const int nb = (int)b0.size(), nkb = (int)kb0.size();
+    pp.blk_row0 = w.blk;
+    pp.blk_nrows = w.blk + nb;
+    pp.n_blk = nb;
+    pp.kblk_row0 = w.blk + 2 * nb;
+    pp.kblk_nrows = w.blk + 2 * nb + nkb;
+    pp.n_kblk = nkb;
+
+    const bool logits_dev = logits && is_device_ptr(logits);
+    const bool ids_dev = ids && is_device_ptr(ids);
+    float* lg = logits_dev ? logits : nullptr;
+    if (logits && !logits_dev) {
+        if (w.out_logits_rows < (size_t)n_keep) {
+            if (w.out_logits) cudaFree(w.out_logits);
+            w.out_logits = nullptr;
+            w.out_logits_rows = 0;
+            if (cudaMalloc(&w.out_logits, (size_t)n_keep * c.cfg.vocab * 4) != cudaSuccess) {
+                cudaGetLastError();
+                w.out_logits = nullptr;
+                return fail(&c, QWEN2_E_OOM, "logits staging allocation failed");
+            }
+            w.out_logits_rows = n_keep;
+        }
+        lg = w.out_logits;
+    }
+    cudaError_t e = enqueue_prefill(c, rows, n_keep, pp, lg, ids ? (ids_dev ? ids : w.ids) : nullptr, st);
+    if (e != cudaSuccess) return cuda_fail(&c, e, "prefill launch");
+    if (logits && !logits_dev)
+        Q2_CHECK(&c, cudaMemcpyAsync(logits, lg, (size_t)n_keep * c.cfg.vocab * 4, cudaMemcpyDeviceToHost, st));
+    if (ids && !ids_dev) Q2_CHECK(&c, cudaMemcpyAsync(ids, w.ids, n_keep * 4, cudaMemcpyDeviceToHost, st));
+    c.last_rows_out = n_keep;
+    if ((logits && !logits_dev) || (ids && !ids_dev)) Q2_CHECK(&c, cudaStreamSynchronize(st));
+    return QWEN2_OK;
+}
+
+int qwen2_decode_step(qwen2_ctx* h, int32_t n_seq, const int32_t* seq_ids, const int32_t* tokens,
+                      const int32_t* positions, float* logits, int32_t* ids, void* stream) {
+    if (!h) return QWEN2_E_ARG;
+    Ctx& c = h->c;
+    c.last_error.clear();
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (n_seq < 1 || n_seq > c.cfg.max_seqs) return fail(&c, QWEN2_E_ARG, "n_seq outside [1, max_seqs]");
+    if (n_seq > 8) return fail(&c, QWEN2_E_UNSUPPORTED, "more than 8 sequences per decode step");
+    if (!seq_ids || !tokens || !positions) return fail(&c, QWEN2_E_ARG, "null input pointer");
+    int r = check_seq_ids(c, n_seq, seq_ids);
+    if (r) return r;
+    if ((r = check_tokens(c, n_seq, tokens))) return r;
+    if ((r = check_positions(c, n_seq, positions, 0))) return r;
+    DecodeState& d = c.ds;
+    Q2_CHECK(&c, cudaMemcpyAsync(d.tok, tokens, n_seq * 4, cudaMemcpyHostToDevice, st));
+    Q2_CHECK(&c, cudaMemcpyAsync(d.pos, positions, n_seq * 4, cudaMemcpyHostToDevice, st));
+    Q2_CHECK(&c, cudaMemcpyAsync(d.slot, seq_ids, n_seq * 4, cudaMemcpyHostToDevice, st));
+    Q2_CHECK(&c, cudaMemsetAsync(d.step, 0, 4, st));
+    if ((r = run_decode_step(c, n_seq, logits != nullptr, st))) return r;
+    const bool host_out = (logits && !is_device_ptr(logits)) || (ids && !is_device_ptr(ids));
+    if (logits)
+        Q2_CHECK(&c, cudaMemcpyAsync(logits, c.ws.logits, (size_t)n_seq * c.cfg.vocab * 4, cudaMemcpyDefault, st));
+    if (ids) Q2_CHECK(&c, cudaMemcpyAsync(ids, d.ids_hist, n_seq * 4, cudaMemcpyDefault, st));
+    c.last_rows_out = n_seq;
+    if (host_out) Q2_CHECK(&c, cudaStreamSynchronize(st));
+    return QWEN2_OK;
+}
+
+int qwen2_decode_steps(qwen2_ctx* h, int32_t n_seq, const int32_t* seq_ids, const int32_t* first_tokens,
+                       const int32_t* start_positions, int32_t n_steps, int32_t* ids, void* stream) {
+    if (!h) return QWEN2_E_ARG;
+    Ctx& c = h->c;
+    c.last_error.clear();
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (n_seq < 1 || n_seq > c.cfg.max_seqs) return fail(&c, QWEN2_E_ARG, "n_seq outside [1, max_seqs]");
+    if (n_seq > 8) return fail(&c, QWEN2_E_UNSUPPORTED, "more than 8 sequences per decode step");
+    if (!seq_ids || !first_tokens || !start_positions || !ids) return fail(&c, QWEN2_E_ARG, "null pointer");
+    if (n_steps < 1) return fail(&c, QWEN2_E_ARG, "n_steps must be >= 1");
+    int r = check_seq_ids(c, n_seq, seq_ids);
+    if (r) return r;
+    if ((r = check_tokens(c, n_seq, first_tokens))) return r;
+    if ((r = check_positions(c, n_seq, start_positions, n_steps - 1))) return r;
+    DecodeState& d = c.ds;
+    Q2_CHECK(&c, cudaMemcpyAsync(d.tok, first_tokens, n_seq * 4, cudaMemcpyHostToDevice, st));
+    Q2_CHECK(&c, cudaMemcpyAsync(d.pos, start_positions, n_seq * 4, cudaMemcpyHostToDevice, st));
+    Q2_CHECK(&c, cudaMemcpyAsync(d.slot, seq_ids, n_seq * 4, cudaMemcpyHostToDevice, st));
+    Q2_CHECK(&c, cudaMemsetAsync(d.step, 0, 4, st));
+    const bool host_out = !is_device_ptr(ids);
+    for (int s0 = 0; s0 < n_steps; s0 += kIdsHist) {
+        const int n = std::min(kIdsHist, n_steps - s0);
+        for (int s = 0; s < n; ++s)
+            if ((r = run_decode_step(c, n_seq, false, st))) return r;
+        Q2_CHECK(&c, cudaMemcpy2DAsync(ids + (size_t)s0 * n_seq, n_seq * 4, d.ids_hist, c.cfg.max_seqs * 4,
+                                       n_seq * 4, n, cudaMemcpyDefault, st));
+    }
+    c.last_rows_out = n_seq;
+    if (host_out) Q2_CHECK(&c, cudaStreamSynchronize(st));
+    return QWEN2_OK;
+}
+
+int qwen2_final_hidden(qwen2_ctx* h, float* dst, int32_t rows, void* stream) {
+    if (!h) return QWEN2_E_ARG;
+    Ctx& c = h->c;
+    if (!dst || rows < 1 || rows > c.last_rows_out)
+        return fail(&c, QWEN2_E_ARG, "rows outside [1, rows of the last call]");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    Q2_CHECK(&c, cudaMemcpyAsync(dst, c.ws.hidden, (size_t)rows * c.cfg.hidden * 4, cudaMemcpyDefault, st));
+    if (!is_device_ptr(dst)) Q2_CHECK(&c, cudaStreamSynchronize(st));
+    return QWEN2_OK;
+}
+
+int qwen2_synchronize(qwen2_ctx* h, void* stream) {
+    if (!h) return QWEN2_E_ARG;
+    Ctx& c = h->c;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    Q2_CHECK(&c, cudaStreamSynchronize(st));
+    int word = 0;
+    Q2_CHECK(&c, cudaMemcpy(&word, c.err, 4, cudaMemcpyDeviceToHost));
+    if (word) {
+        Q2_CHECK(&c, cudaMemset(c.err, 0, 4));
+        static const char* names[] = {"none", "position outside [0, n_ctx)", "token outside [0, vocab)",
+                                      "unexpected shape", "bounded wait timed out"};
+        const char* nm = word > 0 && word < 5 ? names[word] : "unknown";
+        return fail(&c, QWEN2_E_DEVICE_GUARD, std::string("device guard ") + std::to_string(word) + ": " + nm);
+    }
+    return QWEN2_OK;
+}
+
+int64_t qwen2_weight_bytes(const qwen2_ctx* h) { return h ? (int64_t)h->c.wbytes : 0; }
+
+int64_t qwen2_kv_bytes_per_seq(const qwen2_config* g) {
+    if (!g) return 0;
+    return (int64_t)g->n_layer * 2 * g->n_kv_head * g->n_ctx * g->head_dim * 4;
+}
+
+int qwen2_quantize_q8_0(const uint16_t* w, int64_t rows, int64_t k, int8_t* q, uint16_t* d) {
+    if (!w || !q || !d || rows < 0 || k <= 0 || k % 32) return QWEN2_E_ARG;
+    quantize_q8_0_host(w, rows, k, q, d);
+    return QWEN2_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,122 @@
+// Internal state of a libqwen2 context and the launchers the C ABI drives.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <map>
+#include <string>
+#include <vector>
+
+#include "../../include/qwen2.h"
+
+namespace qwen2 {
+
+// One linear weight in device memory.  f16: `w` is [rows][k] halves.
+// Q8_0: `q` is int8 [rows][k] and `d` the f16 scales [rows][k/32].
+struct DevMat {
+    const __half* w = nullptr;
+    const int8_t* q = nullptr;
+    const __half* d = nullptr;
+    int rows = 0, k = 0;
+};
+
+// Packed layer.  Row orders (chosen so that an output pair an epilogue needs
+// sits on adjacent rows):
+//  wqkv: [(nh + 2 nkv) hd][H]; head slot s (q heads, then k, then v) holds
+//        rows (s*hd + 2i, s*hd + 2i + 1) = original rows (s*hd + i,
+//        s*hd + i + hd/2): the two halves a NeoX rotation pairs;
+//  wgu:  [2I][H]; rows (2j, 2j+1) = (gate_proj row j, up_proj row j);
+//  wo [H][nh hd] and wd [H][I] keep the HF order.
+struct DevLayer {
+    DevMat wqkv, wo, wgu, wd;
+    const float* bqkv = nullptr;       // permuted like wqkv's rows
+    const float* attn_norm = nullptr;
+    const float* ffn_norm = nullptr;
+};
+
+struct Workspace {
+    float* x = nullptr;        // [rows][H] residual stream
+    float* xn = nullptr;       // [rows][max(H, I)] normed rows (unfused / prefill)
+    float* q = nullptr;        // [rows][nh*hd] rotated queries
+    float* o = nullptr;        // [rows][nh*hd] attention output (premix)
+    float* mlp = nullptr;      // [rows][I] SiLU(gate) * up
+    float* raw = nullptr;      // [max_seqs][max(NQKV, 2I)] unfused raw products
+    float* att_part = nullptr; // decode split-K partials [max_seqs][nh][chunks][2+hd]
+    int* att_count = nullptr;  // decode split-K arrival counters [max_seqs][nkv]
+    float* am_val = nullptr;   // LM-head per-block argmax values [blocks][8]
+    int* am_idx = nullptr;     // LM-head per-block argmax indices [blocks][8]
+    int* am_count = nullptr;   // LM-head arrival counter
+    float* hidden = nullptr;   // [rows_out][H] final_norm_output
+    float* logits = nullptr;   // [max_seqs][V] decode logits staging
+    int* rows_tok = nullptr;   // prefill: per-row token
+    int* rows_pos = nullptr;   // prefill: per-row position
+    int* rows_slot = nullptr;  // prefill: per-row sequence slot
+    int* keep_rows = nullptr;  // prefill: indices of the rows kept for the LM head
+    int* keep_pos = nullptr;   // prefill: positions of the kept rows
+    int* keep_slot = nullptr;  // prefill: slots of the kept rows
+    int* blk = nullptr;        // prefill: attention query-block plan (4 arrays)
+    float* x2 = nullptr;       // [rows][H] kept rows of the residual (tail cut)
+    float* q2 = nullptr;       // [rows][nh*hd] kept rows of q (tail cut)
+    __half* xn_h = nullptr;    // [rows][max(H, I)] f16 operand rows (tensor prefill)
+    int* ids = nullptr;        // [rows] prefill ids staging
+    float* out_logits = nullptr; // [rows_out][V] staging when the caller's logits are host memory
+    size_t out_logits_rows = 0;
+    int att_max_chunks = 0;
+    int am_blocks = 0;
+};
+
+// Static device state the decode CUDA graphs read (their pointers are baked
+// into the graphs).
+constexpr int kIdsHist = 512;
+struct DecodeState {
+    int* tok = nullptr;      // [max_seqs] token fed this step
+    int* pos = nullptr;      // [max_seqs] position of this step
+    int* slot = nullptr;     // [max_seqs] KV slot (sequence id)
+    int* step = nullptr;     // [1] index of the step within a decode_steps run
+    int* ids_hist = nullptr; // [kIdsHist][max_seqs] ids per step
+};
+
+struct Ctx {
+    qwen2_config cfg{};
+    int device = 0;
+    int n_sm = 0;
+    int nqkv = 0;                 // (nh + 2 nkv) * hd
+    void* wblob = nullptr;        // all packed weights, one allocation
+    size_t wbytes = 0;
+    std::vector<DevLayer> layers;
+    DevMat embed;                 // [V][H]; also the LM head
+    const float* final_norm = nullptr;
+    float* kv = nullptr;          // [max_seqs][L][2][nkv][n_ctx][hd]
+    size_t kv_floats = 0;
+    float2* rope = nullptr;       // [n_ctx][hd/2] (cos, sin), from double on the host
+    int* err = nullptr;           // device guard word
+    Workspace ws;
+    DecodeState ds;
+    int max_rows = 0;             // rows the prefill workspace holds
+    int last_rows_out = 0;        // rows of the last call's final_norm_output
+    cudaStream_t cap_stream = nullptr;
+    std::map<int, cudaGraphExec_t> graphs;   // key: B | (want_logits << 16)
+    std::vector<void*> allocs;    // device buffers freed at destroy
+    std::string last_error;
+};
+
+// ---- decode.cu ---------------------------------------------------------------
+// Enqueue one decode step for the first B slots of DecodeState on `st`
+// (B <= 8).  Logits go to ws.logits when want_logits.
+cudaError_t enqueue_decode_step(Ctx& c, int B, bool want_logits, cudaStream_t st);
+
+// LM head + argmax over `B` rows of `xin` (f32 [B][H]); writes the hidden
+// rows (ws.hidden), optional logits [B][V] and ids [B].  `decode` selects the
+// decode-state update (next token, position advance, ids history; B <= 8).
+cudaError_t enqueue_lm_head(Ctx& c, const float* xin, int B, float* logits, int* ids, bool decode,
+                            cudaStream_t st);
+cudaError_t decode_set_smem_limits(int max_bytes);
+
+// ---- pack.cu -------------------------------------------------------------------
+int pack_weights(Ctx& c, const qwen2_weights* w, std::string& err);
+void quantize_q8_0_host(const uint16_t* w, int64_t rows, int64_t k, int8_t* q, uint16_t* d);
+int build_rope_table(Ctx& c, std::string& err);
+
+}  // namespace qwen2

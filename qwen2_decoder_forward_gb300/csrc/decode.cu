@@ -1,0 +1,632 @@
+// Decode kernels (one row per sequence, B <= 8 rows per launch):
+// embedding gather, fused RMSNorm + QKV + bias + NeoX RoPE + KV store,
+// split-K GQA attention with an in-kernel combine, o_proj / down GEMV with
+// the residual add, fused RMSNorm + gate/up + SiLU*up, and the LM head fused
+// with a two-stage block argmax.  Also the unfused variants the
+// QWEN2_FLAG_NO_FUSE_* flags select.
+#include "ctx.h"
+#include "rowdot.cuh"
+
+namespace qwen2 {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kAttCh = 64;       // positions per attention split
+constexpr int kMaxGroup = 8;     // query heads per kv head the attention kernel holds
+constexpr int kHd = 64;
+
+struct StepArgs {
+    const int* tok;
+    const int* pos;
+    const int* slot;
+    int B;
+    float* x;
+    float* q;
+    float* o;
+    float* mlp;
+    float* kv;
+    const float2* rope;
+    int* err;
+    int H, nh, nkv, I, V, n_ctx, L;
+    float eps;
+};
+
+__device__ __forceinline__ float* kv_ptr(const StepArgs& a, int slot, int layer, int which, int g, int p) {
+    return a.kv + ((((size_t)slot * a.L + layer) * 2 + which) * a.nkv + g) * (size_t)a.n_ctx * kHd +
+           (size_t)p * kHd;
+}
+
+// ---------------------------------------------------------------------------
+// Embedding gather: x[b] = E[tok[b]] (nnterp "token_embeddings").
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) k_embed_f16(StepArgs a, const __half* __restrict__ E) {
+    const int b = blockIdx.x;
+    int t = a.tok[b];
+    if (t < 0 || t >= a.V) {
+        if (threadIdx.x == 0) raise_guard(a.err, kGuardToken);
+        t = 0;
+    }
+    const __half* row = E + (size_t)t * a.H;
+    for (int j = threadIdx.x; j < a.H; j += blockDim.x) a.x[(size_t)b * a.H + j] = __half2float(row[j]);
+}
+
+// ---------------------------------------------------------------------------
+// Epilogue of a Q/K/V row pair (packed rows 2t, 2t+1 = elements i and
+// i + hd/2 of head slot s): bias, NeoX rotation for q and k, then q to the
+// query buffer, k and v to the cache slot of the row's position.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void qkv_pair_epilogue(const StepArgs& a, int layer, int pair, int b, float d0,
+                                                  float d1, const float* __restrict__ bias) {
+    const int r0 = 2 * pair;
+    const int s = r0 / kHd;
+    const int i = (r0 % kHd) >> 1;
+    const int p = a.pos[b];
+    if (p < 0 || p >= a.n_ctx) {
+        raise_guard(a.err, kGuardPosition);
+        return;
+    }
+    const float v0 = d0 + bias[r0];
+    const float v1 = d1 + bias[r0 + 1];
+    if (s < a.nh + a.nkv) {
+        float ra, rb;
+        rope_pair(v0, v1, a.rope[(size_t)p * (kHd / 2) + i], ra, rb);
+        if (s < a.nh) {
+            float* qr = a.q + (size_t)b * a.nh * kHd + s * kHd;
+            qr[i] = ra;
+            qr[i + kHd / 2] = rb;
+        } else {
+            float* kr = kv_ptr(a, a.slot[b], layer, 0, s - a.nh, p);
+            kr[i] = ra;
+            kr[i + kHd / 2] = rb;
+        }
+    } else {
+        float* vr = kv_ptr(a, a.slot[b], layer, 1, s - a.nh - a.nkv, p);
+        vr[i] = v0;
+        vr[i + kHd / 2] = v1;
+    }
+}
+
+// Fused RMSNorm + stacked QKV GEMV + bias + RoPE + KV store.  One warp per
+// row pair; grid-stride over the (nh + 2 nkv) hd / 2 pairs.
+template <int NB>
+__global__ void __launch_bounds__(kThreads) k_qkv_fused(StepArgs a, int layer, const __half* __restrict__ W,
+                                                        const float* __restrict__ bias,
+                                                        const float* __restrict__ norm_w, int npairs) {
+    extern __shared__ __align__(16) float smem[];
+    float* xs = smem;              // [NB][H]
+    float* red = smem + NB * a.H;  // [kWarps]
+    norm_rows_to_smem<NB>(a.x, a.B, a.H, norm_w, a.eps, xs, a.H, red);
+    const int warp = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    for (int t = warp; t < npairs; t += gridDim.x * kWarps) {
+        const __half* rows[2] = {W + (size_t)(2 * t) * a.H, W + (size_t)(2 * t + 1) * a.H};
+        float acc[2][NB];
+        warp_rows_dot<NB, 2>(rows, a.H, xs, a.H, acc);
+        if (lane == 0) {
+#pragma unroll
+            for (int b = 0; b < NB; ++b)
+                if (b < a.B) qkv_pair_epilogue(a, layer, t, b, acc[0][b], acc[1][b], bias);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Unfused pieces (QWEN2_FLAG_NO_FUSE_QKV / _FFN): RMSNorm to a buffer, a
+// plain GEMV over a row range, the QKV epilogue and SiLU*up as kernels of
+// their own.  They share the norm, row-dot and epilogue routines with the
+// fused kernels, so both paths produce the same bits.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) k_rmsnorm_rows(const float* __restrict__ x, int H,
+                                                           const float* __restrict__ w, float eps,
+                                                           float* __restrict__ out) {
+    __shared__ float red[kWarps];
+    const int b = blockIdx.x;
+    const float* xr = x + (size_t)b * H;
+    float ss = 0.f;
+    for (int j = threadIdx.x; j < H; j += blockDim.x) {
+        const float v = xr[j];
+        ss = fmaf(v, v, ss);
+    }
+    const float s = rms_scale(block_sum(ss, red), H, eps);
+    for (int j = threadIdx.x; j < H; j += blockDim.x)
+        out[(size_t)b * H + j] = __fmul_rn(__fmul_rn(xr[j], s), w[j]);
+}
+
+// out[b][k] = W[r0 + stride*k] . xin[b] for k < n (n even); row pairs per
+// warp.
+template <int NB>
+__global__ void __launch_bounds__(kThreads) k_gemv_rows(const __half* __restrict__ W, int K, int r0, int stride,
+                                                        int n, const float* __restrict__ xin, int B,
+                                                        float* __restrict__ out, int ldo) {
+    extern __shared__ __align__(16) float smem[];
+    float* xs = smem;
+    for (int b = 0; b < NB; ++b)
+        for (int j = threadIdx.x; j < K; j += blockDim.x) xs[b * K + j] = b < B ? xin[(size_t)b * K + j] : 0.f;
+    __syncthreads();
+    const int warp = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    for (int t = warp; 2 * t < n; t += gridDim.x * kWarps) {
+        const __half* rows[2] = {W + (size_t)(r0 + stride * 2 * t) * K,
+                                 W + (size_t)(r0 + stride * (2 * t + 1)) * K};
+        float acc[2][NB];
+        warp_rows_dot<NB, 2>(rows, K, xs, K, acc);
+        if (lane == 0)
+            for (int b = 0; b < NB && b < B; ++b) {
+                out[(size_t)b * ldo + 2 * t] = acc[0][b];
+                out[(size_t)b * ldo + 2 * t + 1] = acc[1][b];
+            }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) k_qkv_epilogue(StepArgs a, int layer, const float* __restrict__ raw,
+                                                           int nqkv, const float* __restrict__ bias) {
+    const int b = blockIdx.y;
+    const int pair = blockIdx.x * blockDim.x + threadIdx.x;
+    if (pair * 2 >= nqkv || b >= a.B) return;
+    qkv_pair_epilogue(a, layer, pair, b, raw[(size_t)b * nqkv + 2 * pair], raw[(size_t)b * nqkv + 2 * pair + 1],
+                      bias);
+}
+
+// raw[b] holds gate products in [0, I) and up products in [I, 2I).
+__global__ void __launch_bounds__(kThreads) k_swiglu(const float* __restrict__ raw, int I, int B,
+                                                     float* __restrict__ mlp) {
+    const int b = blockIdx.y;
+    const int j = blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= I || b >= B) return;
+    const float g = raw[(size_t)b * 2 * I + j];
+    const float u = raw[(size_t)b * 2 * I + I + j];
+    mlp[(size_t)b * I + j] = silu_f(g) * u;
+}
+
+// ---------------------------------------------------------------------------
+// Split-K GQA decode attention.  Block (g, c, b) takes positions
+// [c*64, min(c*64+64, p+1)) of kv head g for row b and all `group` query
+// heads that read g (each K/V element is read once per group).  It writes
+// the partial (max, sum, acc[64]) per head; the last block of (b, g) to
+// finish merges the partials in chunk order and writes the head outputs.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) k_attn_decode(StepArgs a, int layer, float* __restrict__ part,
+                                                          int* __restrict__ count, int max_chunks) {
+    __shared__ float q_s[kMaxGroup][kHd];
+    __shared__ float k_s[kAttCh][kHd + 1];
+    __shared__ __align__(16) float v_s[kAttCh][kHd];
+    __shared__ float p_s[kMaxGroup][kAttCh];
+    __shared__ float m_s[kMaxGroup], l_s[kMaxGroup];
+    __shared__ int last_s;
+    const int g = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
+    const int group = a.nh / a.nkv;
+    const int p = a.pos[b];
+    if (p < 0 || p >= a.n_ctx) {
+        if (threadIdx.x == 0 && g == 0 && c == 0) raise_guard(a.err, kGuardPosition);
+        return;
+    }
+    const int n_pos = p + 1;
+    const int n_chunks = (n_pos + kAttCh - 1) / kAttCh;
+    const int j0 = c * kAttCh;
+    if (j0 >= n_pos) return;
+    const int nj = min(kAttCh, n_pos - j0);
+    const int slot = a.slot[b];
+    const int tid = threadIdx.x;
+
+    for (int e = tid; e < group * kHd; e += kThreads)
+        q_s[e / kHd][e % kHd] = a.q[(size_t)b * a.nh * kHd + (size_t)g * group * kHd + e];
+    const float* kb = kv_ptr(a, slot, layer, 0, g, j0);
+    const float* vb = kv_ptr(a, slot, layer, 1, g, j0);
+    for (int e = tid; e < nj * (kHd / 4); e += kThreads) {
+        const int j = e / (kHd / 4), d4 = (e % (kHd / 4)) * 4;
+        const float4 kk = __ldcg(reinterpret_cast<const float4*>(kb + (size_t)j * kHd + d4));
+        const float4 vv = __ldcg(reinterpret_cast<const float4*>(vb + (size_t)j * kHd + d4));
+        k_s[j][d4] = kk.x;
+        k_s[j][d4 + 1] = kk.y;
+        k_s[j][d4 + 2] = kk.z;
+        k_s[j][d4 + 3] = kk.w;
+        *reinterpret_cast<float4*>(&v_s[j][d4]) = vv;
+    }
+    __syncthreads();
+
+    // Scores q_h . k_j / sqrt(hd); hd = 64, so the scale 0.125 is exact.
+    const float scale = 0.125f;
+    for (int e = tid; e < group * kAttCh; e += kThreads) {
+        const int h = e / kAttCh, j = e % kAttCh;
+        float s = -INFINITY;
+        if (j < nj) {
+            float acc = 0.f;
+#pragma unroll 16
+            for (int d = 0; d < kHd; ++d) acc = fmaf(q_s[h][d], k_s[j][d], acc);
+            s = acc * scale;
+        }
+        p_s[h][j] = s;
+    }
+    __syncthreads();
+
+    // Per head: max, exponentials, sum (one warp per head).
+    const int warp = tid >> 5, lane = tid & 31;
+    for (int h = warp; h < group; h += kWarps) {
+        const float s0 = p_s[h][lane], s1 = p_s[h][lane + 32];
+        const float m = warp_max(fmaxf(s0, s1));
+        const float e0 = expf(s0 - m), e1 = expf(s1 - m);
+        p_s[h][lane] = e0;
+        p_s[h][lane + 32] = e1;
+        const float l = warp_sum(e0 + e1);
+        if (lane == 0) {
+            m_s[h] = m;
+            l_s[h] = l;
+        }
+    }
+    __syncthreads();
+
+    // acc[h][d] = sum_j e_j v_j[d]
+    const int stride = kHd + 2;
+    for (int e = tid; e < group * kHd; e += kThreads) {
+        const int h = e / kHd, d = e % kHd;
+        float acc = 0.f;
+        for (int j = 0; j < nj; ++j) acc = fmaf(p_s[h][j], v_s[j][d], acc);
+        float* pr = part + (((size_t)b * a.nh + g * group + h) * max_chunks + c) * stride;
+        pr[2 + d] = acc;
+        if (d == 0) {
+            pr[0] = m_s[h];
+            pr[1] = l_s[h];
+        }
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const int prev = atomicAdd(&count[b * a.nkv + g], 1);
+        last_s = (prev == n_chunks - 1);
+    }
+    __syncthreads();
+    if (!last_s) return;
+    __threadfence();
+    // Merge the chunks in order: M = max m_c, L = sum e^(m_c - M) l_c,
+    // o = sum e^(m_c - M) acc_c / L.
+    for (int e = tid; e < group * kHd; e += kThreads) {
+        const int h = e / kHd, d = e % kHd;
+        const float* ph = part + (((size_t)b * a.nh + g * group + h) * max_chunks) * stride;
+        float M = -INFINITY;
+        for (int cc = 0; cc < n_chunks; ++cc) M = fmaxf(M, __ldcg(ph + (size_t)cc * stride));
+        float L = 0.f, O = 0.f;
+        for (int cc = 0; cc < n_chunks; ++cc) {
+            const float w = expf(__ldcg(ph + (size_t)cc * stride) - M);
+            L = fmaf(w, __ldcg(ph + (size_t)cc * stride + 1), L);
+            O = fmaf(w, __ldcg(ph + (size_t)cc * stride + 2 + d), O);
+        }
+        a.o[(size_t)b * a.nh * kHd + (size_t)(g * group + h) * kHd + d] = O / L;
+    }
+    if (tid == 0) count[b * a.nkv + g] = 0;
+}
+
+// ---------------------------------------------------------------------------
+// y[b] += W . xin[b] over all rows of W (o_proj, down): the residual add.
+// ---------------------------------------------------------------------------
+template <int NB>
+__global__ void __launch_bounds__(kThreads) k_gemv_residual(const __half* __restrict__ W, int N, int K,
+                                                            const float* __restrict__ xin, int B,
+                                                            float* __restrict__ y) {
+    extern __shared__ __align__(16) float smem[];
+    float* xs = smem;
+    for (int b = 0; b < NB; ++b)
+        for (int j = threadIdx.x; j < K; j += blockDim.x) xs[b * K + j] = b < B ? xin[(size_t)b * K + j] : 0.f;
+    __syncthreads();
+    const int warp = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    for (int t = warp; 2 * t < N; t += gridDim.x * kWarps) {
+        const int r = 2 * t;
+        const __half* rows[2] = {W + (size_t)r * K, W + (size_t)(r + 1) * K};
+        float acc[2][NB];
+        warp_rows_dot<NB, 2>(rows, K, xs, K, acc);
+        if (lane == 0)
+            for (int b = 0; b < NB && b < B; ++b) {
+                y[(size_t)b * N + r] += acc[0][b];
+                y[(size_t)b * N + r + 1] += acc[1][b];
+            }
+    }
+}
+
+// Fused RMSNorm + gate/up GEMV + SiLU(gate) * up.  Packed rows (2j, 2j+1)
+// are (gate j, up j).
+template <int NB>
+__global__ void __launch_bounds__(kThreads) k_gateup_fused(StepArgs a, const __half* __restrict__ W,
+                                                           const float* __restrict__ norm_w) {
+    extern __shared__ __align__(16) float smem[];
+    float* xs = smem;
+    float* red = smem + NB * a.H;
+    norm_rows_to_smem<NB>(a.x, a.B, a.H, norm_w, a.eps, xs, a.H, red);
+    const int warp = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    for (int j = warp; j < a.I; j += gridDim.x * kWarps) {
+        const __half* rows[2] = {W + (size_t)(2 * j) * a.H, W + (size_t)(2 * j + 1) * a.H};
+        float acc[2][NB];
+        warp_rows_dot<NB, 2>(rows, a.H, xs, a.H, acc);
+        if (lane == 0)
+            for (int b = 0; b < NB && b < a.B; ++b) a.mlp[(size_t)b * a.I + j] = silu_f(acc[0][b]) * acc[1][b];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Final RMSNorm + tied LM head + argmax.  Block k takes the vocabulary rows
+// [k*span, (k+1)*span); each warp keeps its best (value, lowest index) per
+// row b; the block writes its pair, and the last block to finish merges all
+// pairs (stage 2) and writes the id.  In decode mode the id also becomes the
+// next step's token, the position advances, and the id is recorded in the
+// step history.
+// ---------------------------------------------------------------------------
+struct LmArgs {
+    const float* xin;  // [B][H]
+    const float* norm_w;
+    const __half* E;
+    int B, H, V, span;
+    float eps;
+    float* logits;  // nullable [B][V]
+    float* hidden;  // [B][H]
+    float* am_val;  // [gridDim][8]
+    int* am_idx;
+    int* count;
+    int* ids;  // nullable [B]
+    int decode;
+    int* tok;
+    int* pos;
+    int* step;
+    int* ids_hist;
+    int hist_stride;
+    int* err;
+};
+
+template <int NB>
+__global__ void __launch_bounds__(kThreads) k_lm_head(LmArgs a) {
+    extern __shared__ __align__(16) float smem[];
+    float* xs = smem;
+    float* red = smem + NB * a.H;
+    __shared__ float wv_s[kWarps][NB];
+    __shared__ int wi_s[kWarps][NB];
+    __shared__ int last_s;
+    norm_rows_to_smem<NB>(a.xin, a.B, a.H, a.norm_w, a.eps, xs, a.H, red);
+    if (blockIdx.x == 0)
+        for (int b = 0; b < a.B; ++b)
+            for (int j = threadIdx.x; j < a.H; j += blockDim.x) a.hidden[(size_t)b * a.H + j] = xs[b * a.H + j];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r_begin = blockIdx.x * a.span;
+    const int r_end = min(a.V, r_begin + a.span);
+    float best_v[NB];
+    int best_i[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        best_v[b] = -INFINITY;
+        best_i[b] = 0x7fffffff;
+    }
+    for (int r = r_begin + 2 * warp; r < r_end; r += 2 * kWarps) {
+        const bool two = r + 1 < r_end;
+        const __half* rows[2] = {a.E + (size_t)r * a.H, a.E + (size_t)(two ? r + 1 : r) * a.H};
+        float acc[2][NB];
+        warp_rows_dot<NB, 2>(rows, a.H, xs, a.H, acc);
+        if (lane == 0) {
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                if (b >= a.B) continue;
+                if (a.logits) {
+                    a.logits[(size_t)b * a.V + r] = acc[0][b];
+                    if (two) a.logits[(size_t)b * a.V + r + 1] = acc[1][b];
+                }
+                argmax_merge(best_v[b], best_i[b], acc[0][b], r);
+                if (two) argmax_merge(best_v[b], best_i[b], acc[1][b], r + 1);
+            }
+        }
+    }
+    if (lane == 0)
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            wv_s[warp][b] = best_v[b];
+            wi_s[warp][b] = best_i[b];
+        }
+    __syncthreads();
+    if (threadIdx.x < NB) {
+        const int b = threadIdx.x;
+        float v = wv_s[0][b];
+        int i = wi_s[0][b];
+        for (int w = 1; w < kWarps; ++w) argmax_merge(v, i, wv_s[w][b], wi_s[w][b]);
+        a.am_val[blockIdx.x * 8 + b] = v;
+        a.am_idx[blockIdx.x * 8 + b] = i;
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last_s = (atomicAdd(a.count, 1) == (int)gridDim.x - 1);
+    __syncthreads();
+    if (!last_s) return;
+    __threadfence();
+    // Stage 2: warp b merges the per-block pairs of row b.
+    if (warp < a.B && warp < NB) {
+        const int b = warp;
+        float v = -INFINITY;
+        int i = 0x7fffffff;
+        for (int k = lane; k < (int)gridDim.x; k += 32)
+            argmax_merge(v, i, __ldcg(a.am_val + k * 8 + b), __ldcg(a.am_idx + k * 8 + b));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+            argmax_merge(v, i, ov, oi);
+        }
+        if (lane == 0) {
+            if (i < 0 || i >= a.V) {
+                raise_guard(a.err, kGuardShape);
+                i = 0;
+            }
+            if (a.ids) a.ids[b] = i;
+            if (a.decode) {
+                a.ids_hist[(size_t)(*a.step % kIdsHist) * a.hist_stride + b] = i;
+                a.tok[b] = i;
+                a.pos[b] = a.pos[b] + 1;
+            }
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        *a.count = 0;
+        if (a.decode) *a.step = *a.step + 1;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Launchers.
+// ---------------------------------------------------------------------------
+namespace {
+
+StepArgs make_step_args(Ctx& c, int B, const int* tok, const int* pos, const int* slot, float* x) {
+    StepArgs a;
+    a.tok = tok;
+    a.pos = pos;
+    a.slot = slot;
+    a.B = B;
+    a.x = x;
+    a.q = c.ws.q;
+    a.o = c.ws.o;
+    a.mlp = c.ws.mlp;
+    a.kv = c.kv;
+    a.rope = c.rope;
+    a.err = c.err;
+    a.H = c.cfg.hidden;
+    a.nh = c.cfg.n_head;
+    a.nkv = c.cfg.n_kv_head;
+    a.I = c.cfg.intermediate;
+    a.V = c.cfg.vocab;
+    a.n_ctx = c.cfg.n_ctx;
+    a.L = c.cfg.n_layer;
+    a.eps = c.cfg.rms_eps;
+    return a;
+}
+
+int blocks_for(int warps_needed, int cap) {
+    int b = (warps_needed + kWarps - 1) / kWarps;
+    return b < 1 ? 1 : (b > cap ? cap : b);
+}
+
+template <int NB>
+cudaError_t layer_step(Ctx& c, const StepArgs& a, int l, cudaStream_t st) {
+    const DevLayer& L = c.layers[l];
+    const int H = c.cfg.hidden, I = c.cfg.intermediate, nq = c.cfg.n_head * kHd;
+    const int cap = c.n_sm * 8;
+    const bool fuse_qkv = !(c.cfg.flags & QWEN2_FLAG_NO_FUSE_QKV);
+    const bool fuse_ffn = !(c.cfg.flags & QWEN2_FLAG_NO_FUSE_FFN);
+    if (fuse_qkv) {
+        const int np = c.nqkv / 2;
+        k_qkv_fused<NB><<<blocks_for(np, cap), kThreads, (NB * H + kWarps) * 4, st>>>(a, l, L.wqkv.w, L.bqkv,
+                                                                                      L.attn_norm, np);
+    } else {
+        k_rmsnorm_rows<<<a.B, kThreads, 0, st>>>(a.x, H, L.attn_norm, a.eps, c.ws.xn);
+        const int nkvd = c.cfg.n_kv_head * kHd;
+        const int r0s[3] = {0, nq, nq + nkvd}, ns[3] = {nq, nkvd, nkvd};
+        for (int part = 0; part < 3; ++part)
+            k_gemv_rows<NB><<<blocks_for(ns[part] / 2, cap), kThreads, NB * H * 4, st>>>(
+                L.wqkv.w, H, r0s[part], 1, ns[part], c.ws.xn, a.B, c.ws.raw + r0s[part], c.nqkv);
+        k_qkv_epilogue<<<dim3((c.nqkv / 2 + kThreads - 1) / kThreads, a.B), kThreads, 0, st>>>(a, l, c.ws.raw,
+                                                                                             c.nqkv, L.bqkv);
+    }
+    k_attn_decode<<<dim3(c.cfg.n_kv_head, c.ws.att_max_chunks, a.B), kThreads, 0, st>>>(
+        a, l, c.ws.att_part, c.ws.att_count, c.ws.att_max_chunks);
+    k_gemv_residual<NB><<<blocks_for(H / 2, cap), kThreads, NB * nq * 4, st>>>(L.wo.w, H, nq, c.ws.o, a.B, a.x);
+    if (fuse_ffn) {
+        k_gateup_fused<NB><<<blocks_for(I, cap), kThreads, (NB * H + kWarps) * 4, st>>>(a, L.wgu.w, L.ffn_norm);
+    } else {
+        k_rmsnorm_rows<<<a.B, kThreads, 0, st>>>(a.x, H, L.ffn_norm, a.eps, c.ws.xn);
+        // Gate rows (even packed rows) and up rows (odd) as two products.
+        k_gemv_rows<NB><<<blocks_for(I / 2, cap), kThreads, NB * H * 4, st>>>(L.wgu.w, H, 0, 2, I, c.ws.xn, a.B,
+                                                                              c.ws.raw, 2 * I);
+        k_gemv_rows<NB><<<blocks_for(I / 2, cap), kThreads, NB * H * 4, st>>>(L.wgu.w, H, 1, 2, I, c.ws.xn, a.B,
+                                                                              c.ws.raw + I, 2 * I);
+        k_swiglu<<<dim3((I + kThreads - 1) / kThreads, a.B), kThreads, 0, st>>>(c.ws.raw, I, a.B, c.ws.mlp);
+    }
+    k_gemv_residual<NB><<<blocks_for(H / 2, cap), kThreads, NB * I * 4, st>>>(L.wd.w, H, I, c.ws.mlp, a.B, a.x);
+    return cudaGetLastError();
+}
+
+template <int NB>
+cudaError_t lm_head_nb(Ctx& c, const float* xin, int B, float* logits, int* ids, float* hidden, bool decode,
+                       cudaStream_t st) {
+    LmArgs la;
+    la.xin = xin;
+    la.norm_w = c.final_norm;
+    la.E = c.embed.w;
+    la.B = B;
+    la.H = c.cfg.hidden;
+    la.V = c.cfg.vocab;
+    la.eps = c.cfg.rms_eps;
+    const int grid = c.ws.am_blocks;
+    int span = (la.V + grid - 1) / grid;
+    span = (span + 1) & ~1;
+    la.span = span;
+    la.logits = logits;
+    la.hidden = hidden;
+    la.am_val = c.ws.am_val;
+    la.am_idx = c.ws.am_idx;
+    la.count = c.ws.am_count;
+    la.ids = ids;
+    la.decode = decode ? 1 : 0;
+    la.tok = c.ds.tok;
+    la.pos = c.ds.pos;
+    la.step = c.ds.step;
+    la.ids_hist = c.ds.ids_hist;
+    la.hist_stride = c.cfg.max_seqs;
+    la.err = c.err;
+    k_lm_head<NB><<<grid, kThreads, (NB * la.H + kWarps) * 4, st>>>(la);
+    return cudaGetLastError();
+}
+
+template <int NB>
+cudaError_t decode_nb(Ctx& c, int B, bool want_logits, cudaStream_t st) {
+    StepArgs a = make_step_args(c, B, c.ds.tok, c.ds.pos, c.ds.slot, c.ws.x);
+    k_embed_f16<<<B, kThreads, 0, st>>>(a, c.embed.w);
+    for (int l = 0; l < c.cfg.n_layer; ++l) {
+        cudaError_t e = layer_step<NB>(c, a, l, st);
+        if (e != cudaSuccess) return e;
+    }
+    return lm_head_nb<NB>(c, c.ws.x, B, want_logits ? c.ws.logits : nullptr, nullptr, c.ws.hidden, true, st);
+}
+
+}  // namespace
+
+cudaError_t enqueue_lm_head(Ctx& c, const float* xin, int B, float* logits, int* ids, bool decode,
+                            cudaStream_t st) {
+    if (decode && B > 8) return cudaErrorInvalidValue;
+    const int H = c.cfg.hidden;
+    const size_t V = (size_t)c.cfg.vocab;
+    for (int b0 = 0; b0 < B; b0 += 8) {
+        const int nb = B - b0 < 8 ? B - b0 : 8;
+        const float* xg = xin + (size_t)b0 * H;
+        float* lg = logits ? logits + (size_t)b0 * V : nullptr;
+        int* ig = ids ? ids + b0 : nullptr;
+        float* hg = c.ws.hidden + (size_t)b0 * H;
+        cudaError_t e;
+        if (nb <= 1) e = lm_head_nb<1>(c, xg, nb, lg, ig, hg, decode, st);
+        else if (nb <= 2) e = lm_head_nb<2>(c, xg, nb, lg, ig, hg, decode, st);
+        else if (nb <= 4) e = lm_head_nb<4>(c, xg, nb, lg, ig, hg, decode, st);
+        else e = lm_head_nb<8>(c, xg, nb, lg, ig, hg, decode, st);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t enqueue_decode_step(Ctx& c, int B, bool want_logits, cudaStream_t st) {
+    if (B <= 1) return decode_nb<1>(c, B, want_logits, st);
+    if (B <= 2) return decode_nb<2>(c, B, want_logits, st);
+    if (B <= 4) return decode_nb<4>(c, B, want_logits, st);
+    if (B <= 8) return decode_nb<8>(c, B, want_logits, st);
+    return cudaErrorInvalidValue;
+}
+
+// Dynamic shared-memory opt-in for the templated kernels (once at create).
+cudaError_t decode_set_smem_limits(int max_bytes) {
+    cudaError_t e = cudaSuccess;
+#define Q2_SMEM(kern) \
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_bytes);
+#define Q2_SMEM_NB(NB)           \
+    Q2_SMEM(k_qkv_fused<NB>)     \
+    Q2_SMEM(k_gemv_rows<NB>)     \
+    Q2_SMEM(k_gemv_residual<NB>) \
+    Q2_SMEM(k_gateup_fused<NB>)  \
+    Q2_SMEM(k_lm_head<NB>)
+    Q2_SMEM_NB(1) Q2_SMEM_NB(2) Q2_SMEM_NB(4) Q2_SMEM_NB(8)
+#undef Q2_SMEM_NB
+#undef Q2_SMEM
+    return e;
+}
+
+}  // namespace qwen2

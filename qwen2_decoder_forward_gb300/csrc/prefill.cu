@@ -1,0 +1,361 @@
+// Prefill on CUDA cores with f32 activations: per-row embedding gather and
+// RMSNorm, a tiled f32 x f16 GEMM whose epilogues carry the QKV bias + NeoX
+// RoPE + KV store, the residual add, or SiLU(gate) * up; a flash-style
+// causal GQA attention over the KV cache; the tail-row cut (minfer "Qwen2 /
+// Qwen2.5 Architecture Support", section 3, "G3 tail-row optimization"); and
+// the LM head on the kept rows.
+#include "prefill.h"
+#include "rowdot.cuh"
+
+namespace qwen2 {
+
+namespace {
+
+constexpr int kT = 256;
+constexpr int kHd = 64;
+
+__global__ void __launch_bounds__(kT) k_embed_rows(const int* __restrict__ tok, int V, int H,
+                                                   const __half* __restrict__ E, float* __restrict__ x,
+                                                   int* err) {
+    const int r = blockIdx.x;
+    int t = tok[r];
+    if (t < 0 || t >= V) {
+        if (threadIdx.x == 0) raise_guard(err, kGuardToken);
+        t = 0;
+    }
+    for (int j = threadIdx.x; j < H; j += blockDim.x) x[(size_t)r * H + j] = __half2float(E[(size_t)t * H + j]);
+}
+
+// out[r] = RMSNorm(x[r]) * w.
+__global__ void __launch_bounds__(kT) k_norm_rows(const float* __restrict__ x, int H, const float* __restrict__ w,
+                                                  float eps, float* __restrict__ out) {
+    __shared__ float red[kT / 32];
+    const int r = blockIdx.x;
+    const float* xr = x + (size_t)r * H;
+    float ss = 0.f;
+    for (int j = threadIdx.x; j < H; j += blockDim.x) {
+        const float v = xr[j];
+        ss = fmaf(v, v, ss);
+    }
+    const float s = rms_scale(block_sum(ss, red), H, eps);
+    for (int j = threadIdx.x; j < H; j += blockDim.x) out[(size_t)r * H + j] = __fmul_rn(__fmul_rn(xr[j], s), w[j]);
+}
+
+// ---------------------------------------------------------------------------
+// C[M][N] = A[M][K] . W[N][K]^T, A f32 row-major, W f16 (packed rows).
+// 128 x 128 tile, K step 16, 256 threads; thread (ty, tx) owns rows
+// ty + 16 i and columns tx + 16 j (i, j < 8).
+// ---------------------------------------------------------------------------
+constexpr int GBM = 128, GBN = 128, GBK = 16;
+
+__device__ __forceinline__ void epilogue_store(const PrefillEpi& e, int m, int n, float v, float v_next_col) {
+    const int H = e.H;
+    switch (e.kind) {
+    case kEpiResidual:
+        e.x[(size_t)m * H + n] += v;
+        break;
+    case kEpiSwiGLU:
+        // Even column 2j holds gate j, column 2j+1 up j.
+        if ((n & 1) == 0) e.mlp[(size_t)m * e.I + (n >> 1)] = silu_f(v) * v_next_col;
+        break;
+    case kEpiQKV: {
+        if (n & 1) break;
+        const int s = n / kHd, i = (n % kHd) >> 1;
+        const int p = e.pos[m];
+        if (p < 0 || p >= e.n_ctx) {
+            raise_guard(e.err, kGuardPosition);
+            break;
+        }
+        const float v0 = v + e.bias[n], v1 = v_next_col + e.bias[n + 1];
+        const size_t head_stride = (size_t)e.n_ctx * kHd;
+        const size_t cache0 = ((size_t)e.slot[m] * e.L + e.layer) * 2 * e.nkv;
+        if (s < e.nh + e.nkv) {
+            float ra, rb;
+            rope_pair(v0, v1, e.rope[(size_t)p * (kHd / 2) + i], ra, rb);
+            if (s < e.nh) {
+                float* qr = e.q + (size_t)m * e.nh * kHd + s * kHd;
+                qr[i] = ra;
+                qr[i + kHd / 2] = rb;
+            } else {
+                float* kr = e.kv + (cache0 + (s - e.nh)) * head_stride + (size_t)p * kHd;
+                kr[i] = ra;
+                kr[i + kHd / 2] = rb;
+            }
+        } else {
+            float* vr = e.kv + (cache0 + e.nkv + (s - e.nh - e.nkv)) * head_stride + (size_t)p * kHd;
+            vr[i] = v0;
+            vr[i + kHd / 2] = v1;
+        }
+        break;
+    }
+    }
+}
+
+__global__ void __launch_bounds__(kT) k_gemm_f32(const float* __restrict__ A, const __half* __restrict__ W, int M,
+                                                 int N, int K, PrefillEpi e) {
+    __shared__ float As[GBK][GBM + 1];
+    __shared__ float Ws[GBK][GBN + 1];
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    const int m0 = blockIdx.y * GBM, n0 = blockIdx.x * GBN;
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    for (int k0 = 0; k0 < K; k0 += GBK) {
+        // A tile: 128 rows x 16 k = 512 float4.
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const int idx = tid + t * kT;
+            const int r = idx >> 2, k4 = (idx & 3) * 4;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (m0 + r < M) v = *reinterpret_cast<const float4*>(A + (size_t)(m0 + r) * K + k0 + k4);
+            As[k4][r] = v.x;
+            As[k4 + 1][r] = v.y;
+            As[k4 + 2][r] = v.z;
+            As[k4 + 3][r] = v.w;
+        }
+        {
+            // W tile: 128 rows x 16 k halves = 256 x 8 halves.
+            const int r = tid >> 1, k8 = (tid & 1) * 8;
+            uint4 w = make_uint4(0, 0, 0, 0);
+            if (n0 + r < N) w = ld_stream_v4(W + (size_t)(n0 + r) * K + k0 + k8);
+            float2 f;
+            f = h2_to_f2(w.x); Ws[k8 + 0][r] = f.x; Ws[k8 + 1][r] = f.y;
+            f = h2_to_f2(w.y); Ws[k8 + 2][r] = f.x; Ws[k8 + 3][r] = f.y;
+            f = h2_to_f2(w.z); Ws[k8 + 4][r] = f.x; Ws[k8 + 5][r] = f.y;
+            f = h2_to_f2(w.w); Ws[k8 + 6][r] = f.x; Ws[k8 + 7][r] = f.y;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < GBK; ++kk) {
+            float av[8], bv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) av[i] = As[kk][ty + 16 * i];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) bv[j] = Ws[kk][tx + 16 * j];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+    // Columns 2j and 2j+1 sit in lanes tx and tx+1 (tx even): pass the odd
+    // column's value down one lane for the pair epilogues.
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float nxt = __shfl_down_sync(0xffffffffu, acc[i][j], 1);
+            const int m = m0 + ty + 16 * i, n = n0 + tx + 16 * j;
+            if (m < M && n < N) epilogue_store(e, m, n, acc[i][j], nxt);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Causal GQA attention for prefill rows.  Block (g, blk) takes up to 16
+// rows of one sequence and, for each of their `group` query heads that read
+// kv head g, runs an online softmax over key chunks of 64 positions from 0
+// to the block's largest position; a row at position p sees keys 0..p.
+// ---------------------------------------------------------------------------
+constexpr int kQB = kPrefillQB;
+constexpr int kMaxG = 8;
+constexpr int kVecPerWarp = kQB * kMaxG / (kT / 32);
+constexpr int kAttnSmem = (kQB * kMaxG * kHd + 64 * (kHd + 1) + 64 * kHd) * 4;
+
+__global__ void __launch_bounds__(kT) k_attn_prefill(PrefillAttnArgs a, int layer) {
+    extern __shared__ __align__(16) float sm[];
+    float* q_s = sm;                       // [kQB*kMaxG][64]
+    float* v_s = q_s + kQB * kMaxG * kHd;  // [64][64]
+    float* k_s = v_s + 64 * kHd;           // [64][65]
+    const int g = blockIdx.x, blk = blockIdx.y;
+    const int r0 = a.blk_row0[blk], nr = a.blk_nrows[blk];
+    const int group = a.nh / a.nkv;
+    const int nv = nr * group;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int slot = a.slot[r0];
+    int pmax = 0;
+    for (int r = 0; r < nr; ++r) pmax = max(pmax, a.pos[r0 + r]);
+    for (int e = tid; e < nv * kHd; e += kT) {
+        const int v = e / kHd, d = e % kHd;
+        const int ri = v / group, h = v % group;
+        q_s[e] = a.q[(size_t)(r0 + ri) * a.nh * kHd + (size_t)(g * group + h) * kHd + d];
+    }
+    float m_[kVecPerWarp], l_[kVecPerWarp], o0[kVecPerWarp], o1[kVecPerWarp];
+    int p_[kVecPerWarp];
+#pragma unroll
+    for (int t = 0; t < kVecPerWarp; ++t) {
+        m_[t] = -INFINITY;
+        l_[t] = 0.f;
+        o0[t] = 0.f;
+        o1[t] = 0.f;
+        const int v = warp + 8 * t;
+        p_[t] = v < nv ? a.pos[r0 + v / group] : -1;
+    }
+    const size_t head_stride = (size_t)a.n_ctx * kHd;
+    const size_t cache0 = ((size_t)slot * a.L + layer) * 2 * a.nkv;
+    const float* kbase = a.kv + (cache0 + g) * head_stride;
+    const float* vbase = a.kv + (cache0 + a.nkv + g) * head_stride;
+    for (int j0 = 0; j0 <= pmax; j0 += 64) {
+        const int nj = min(64, pmax + 1 - j0);
+        __syncthreads();
+        for (int e = tid; e < nj * (kHd / 4); e += kT) {
+            const int j = e / (kHd / 4), d4 = (e % (kHd / 4)) * 4;
+            const float4 kk = __ldcg(reinterpret_cast<const float4*>(kbase + (size_t)(j0 + j) * kHd + d4));
+            const float4 vv = __ldcg(reinterpret_cast<const float4*>(vbase + (size_t)(j0 + j) * kHd + d4));
+            float* kr = k_s + j * (kHd + 1) + d4;
+            kr[0] = kk.x;
+            kr[1] = kk.y;
+            kr[2] = kk.z;
+            kr[3] = kk.w;
+            *reinterpret_cast<float4*>(v_s + j * kHd + d4) = vv;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int t = 0; t < kVecPerWarp; ++t) {
+            const int v = warp + 8 * t;
+            if (v >= nv || j0 > p_[t]) continue;
+            const float* qv = q_s + v * kHd;
+            float s0 = 0.f, s1 = 0.f;
+            const bool ok0 = lane < nj && j0 + lane <= p_[t];
+            const bool ok1 = lane + 32 < nj && j0 + lane + 32 <= p_[t];
+#pragma unroll 16
+            for (int d = 0; d < kHd; ++d) {
+                const float qd = qv[d];
+                s0 = fmaf(qd, k_s[lane * (kHd + 1) + d], s0);
+                s1 = fmaf(qd, k_s[(lane + 32) * (kHd + 1) + d], s1);
+            }
+            s0 = ok0 ? s0 * 0.125f : -INFINITY;
+            s1 = ok1 ? s1 * 0.125f : -INFINITY;
+            const float cm = warp_max(fmaxf(s0, s1));
+            const float mn = fmaxf(m_[t], cm);
+            const float corr = expf(m_[t] - mn);
+            const float e0 = expf(s0 - mn), e1 = expf(s1 - mn);
+            l_[t] = fmaf(l_[t], corr, warp_sum(e0 + e1));
+            float a0 = o0[t] * corr, a1 = o1[t] * corr;
+            for (int jj = 0; jj < 32; ++jj) {
+                const float pj = __shfl_sync(0xffffffffu, e0, jj);
+                a0 = fmaf(pj, v_s[jj * kHd + lane], a0);
+                a1 = fmaf(pj, v_s[jj * kHd + lane + 32], a1);
+            }
+            for (int jj = 0; jj < 32; ++jj) {
+                const float pj = __shfl_sync(0xffffffffu, e1, jj);
+                a0 = fmaf(pj, v_s[(jj + 32) * kHd + lane], a0);
+                a1 = fmaf(pj, v_s[(jj + 32) * kHd + lane + 32], a1);
+            }
+            o0[t] = a0;
+            o1[t] = a1;
+            m_[t] = mn;
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < kVecPerWarp; ++t) {
+        const int v = warp + 8 * t;
+        if (v >= nv) continue;
+        const int ri = v / group, h = v % group;
+        float* orow = a.o + (size_t)(r0 + ri) * a.nh * kHd + (size_t)(g * group + h) * kHd;
+        orow[lane] = o0[t] / l_[t];
+        orow[lane + 32] = o1[t] / l_[t];
+    }
+}
+
+__global__ void k_gather_rows(const float* __restrict__ src, int width, const int* __restrict__ idx,
+                              float* __restrict__ dst) {
+    const int r = blockIdx.x;
+    const float* s = src + (size_t)idx[r] * width;
+    for (int j = threadIdx.x; j < width; j += blockDim.x) dst[(size_t)r * width + j] = s[j];
+}
+
+__global__ void k_gather_int(const int* __restrict__ src, const int* __restrict__ idx, int n,
+                             int* __restrict__ dst) {
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r < n) dst[r] = src[idx[r]];
+}
+
+PrefillEpi base_epi(Ctx& c, int layer, const int* pos, const int* slot, float* x, float* q) {
+    PrefillEpi e{};
+    e.H = c.cfg.hidden;
+    e.I = c.cfg.intermediate;
+    e.nh = c.cfg.n_head;
+    e.nkv = c.cfg.n_kv_head;
+    e.n_ctx = c.cfg.n_ctx;
+    e.L = c.cfg.n_layer;
+    e.layer = layer;
+    e.x = x;
+    e.q = q;
+    e.mlp = c.ws.mlp;
+    e.kv = c.kv;
+    e.rope = c.rope;
+    e.pos = pos;
+    e.slot = slot;
+    e.err = c.err;
+    return e;
+}
+
+dim3 gemm_grid(int M, int N) { return dim3((N + GBN - 1) / GBN, (M + GBM - 1) / GBM); }
+
+}  // namespace
+
+cudaError_t prefill_set_smem_limits() {
+    return cudaFuncSetAttribute(k_attn_prefill, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
+}
+
+cudaError_t enqueue_prefill(Ctx& c, int rows, int n_keep, const PrefillPlan& plan, float* logits_dev,
+                            int* ids_dev, cudaStream_t st) {
+    const qwen2_config& g = c.cfg;
+    const int H = g.hidden, I = g.intermediate, nq = g.n_head * kHd;
+    Workspace& w = c.ws;
+    k_embed_rows<<<rows, kT, 0, st>>>(w.rows_tok, g.vocab, H, c.embed.w, w.x, c.err);
+    float* x = w.x;
+    float* q = w.q;
+    const int* pos = w.rows_pos;
+    const int* slot = w.rows_slot;
+    int cur = rows;
+    for (int l = 0; l < g.n_layer; ++l) {
+        const DevLayer& L = c.layers[l];
+        const bool last = l == g.n_layer - 1;
+        PrefillEpi e = base_epi(c, l, pos, slot, x, q);
+        // RMSNorm, stacked QKV product + bias + RoPE + KV store (all rows).
+        k_norm_rows<<<cur, kT, 0, st>>>(x, H, L.attn_norm, g.rms_eps, w.xn);
+        e.kind = kEpiQKV;
+        e.bias = L.bqkv;
+        k_gemm_f32<<<gemm_grid(cur, c.nqkv), kT, 0, st>>>(w.xn, L.wqkv.w, cur, c.nqkv, H, e);
+        const int* blk_row0 = plan.blk_row0;
+        const int* blk_nrows = plan.blk_nrows;
+        int n_blk = plan.n_blk;
+        if (last && n_keep < cur) {
+            // Tail cut: only the kept rows go on to attention, o_proj, FFN, head.
+            k_gather_rows<<<n_keep, kT, 0, st>>>(x, H, w.keep_rows, w.x2);
+            k_gather_rows<<<n_keep, kT, 0, st>>>(q, nq, w.keep_rows, w.q2);
+            k_gather_int<<<(n_keep + 255) / 256, 256, 0, st>>>(w.rows_pos, w.keep_rows, n_keep, w.keep_pos);
+            k_gather_int<<<(n_keep + 255) / 256, 256, 0, st>>>(w.rows_slot, w.keep_rows, n_keep, w.keep_slot);
+            x = w.x2;
+            q = w.q2;
+            pos = w.keep_pos;
+            slot = w.keep_slot;
+            cur = n_keep;
+            blk_row0 = plan.kblk_row0;
+            blk_nrows = plan.kblk_nrows;
+            n_blk = plan.n_kblk;
+            e = base_epi(c, l, pos, slot, x, q);
+        }
+        PrefillAttnArgs aa{q, w.o, c.kv, pos, slot, blk_row0, blk_nrows, g.n_head, g.n_kv_head, g.n_ctx, g.n_layer};
+        k_attn_prefill<<<dim3(g.n_kv_head, n_blk), kT, kAttnSmem, st>>>(aa, l);
+        // o_proj + residual.
+        e.kind = kEpiResidual;
+        k_gemm_f32<<<gemm_grid(cur, H), kT, 0, st>>>(w.o, L.wo.w, cur, H, nq, e);
+        // RMSNorm, gate/up + SiLU * up, down + residual.
+        k_norm_rows<<<cur, kT, 0, st>>>(x, H, L.ffn_norm, g.rms_eps, w.xn);
+        e.kind = kEpiSwiGLU;
+        k_gemm_f32<<<gemm_grid(cur, 2 * I), kT, 0, st>>>(w.xn, L.wgu.w, cur, 2 * I, H, e);
+        e.kind = kEpiResidual;
+        k_gemm_f32<<<gemm_grid(cur, H), kT, 0, st>>>(w.mlp, L.wd.w, cur, H, I, e);
+        cudaError_t err = cudaGetLastError();
+        if (err != cudaSuccess) return err;
+    }
+    return enqueue_lm_head(c, x, n_keep, logits_dev, ids_dev, false, st);
+}
+
+}  // namespace qwen2

@@ -1,0 +1,59 @@
+// Shared declarations of the prefill kernels (CUDA-core and tensor-core).
+#pragma once
+
+#include "ctx.h"
+
+namespace qwen2 {
+
+enum EpiKind : int { kEpiQKV = 0, kEpiResidual = 1, kEpiSwiGLU = 2 };
+
+// What a GEMM epilogue does with output element (m, n) of a layer's product.
+//  kEpiQKV:      n indexes the packed Q/K/V rows; pairs (n, n+1) get the
+//                bias, the NeoX rotation (q, k) and go to q / the KV cache
+//  kEpiResidual: x[m][n] += value
+//  kEpiSwiGLU:   pairs (gate j, up j) -> mlp[m][j] = SiLU(gate) * up
+// Optional f16 copies (q_h, mlp_h) feed the tensor-core path.
+struct PrefillEpi {
+    int kind;
+    int H, I, nh, nkv, n_ctx, L, layer;
+    float* x;
+    float* q;
+    __half* q_h;
+    float* mlp;
+    __half* mlp_h;
+    float* kv;
+    const float2* rope;
+    const float* bias;
+    const int* pos;
+    const int* slot;
+    int* err;
+};
+
+struct PrefillAttnArgs {
+    const float* q;         // [rows][nh*64] rotated queries
+    float* o;               // [rows][nh*64] head outputs
+    const float* kv;
+    const int* pos;
+    const int* slot;
+    const int* blk_row0;    // query blocks: first row and row count, one sequence each
+    const int* blk_nrows;
+    int nh, nkv, n_ctx, L;
+};
+
+// Device copies of the per-call row plan (built on the host).
+struct PrefillPlan {
+    const int* blk_row0;
+    const int* blk_nrows;
+    int n_blk;
+    const int* kblk_row0;   // blocks over the kept rows (after the tail cut)
+    const int* kblk_nrows;
+    int n_kblk;
+};
+
+constexpr int kPrefillQB = 16;   // query rows per attention block
+
+cudaError_t enqueue_prefill(Ctx& c, int rows, int n_keep, const PrefillPlan& plan, float* logits_dev,
+                            int* ids_dev, cudaStream_t st);
+cudaError_t prefill_set_smem_limits();
+
+}  // namespace qwen2

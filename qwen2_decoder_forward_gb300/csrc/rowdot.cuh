@@ -1,0 +1,92 @@
+// The canonical weight-row dot product every f16 GEMV kernel of libqwen2 uses.
+//
+// A row of K f16 weights is read as K/8 chunks of 16 bytes; lane l of the
+// warp takes chunks l, l+32, l+64, ... in that order, adds each chunk's eight
+// products into its own f32 partial (dot8_f16, element order), and the 32
+// partials are summed by the xor butterfly of warp_sum (lane 0's value).
+// Because the lane assignment depends on the row alone, a row's result does
+// not depend on which rows share the warp, on the number of activation
+// vectors, or on which kernel computes it: fused and unfused paths, batch 1
+// and batch B, all round alike.
+#pragma once
+
+#include "common.cuh"
+
+namespace qwen2 {
+
+// Dot products of R weight rows with NB activation vectors held in shared
+// memory (xs + nb*ldx, 16-byte aligned, K floats each).  Loads of all R rows
+// are issued together, U chunks per lane per row at a time.  acc[r][nb] is
+// valid in lane 0.
+template <int NB, int R, int U = 8>
+__device__ __forceinline__ void warp_rows_dot(const __half* const (&rows)[R], int K,
+                                              const float* xs, int ldx, float (&acc)[R][NB]) {
+    const int lane = threadIdx.x & 31;
+    const int kc = K >> 3;
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) acc[r][nb] = 0.f;
+    for (int i0 = 0; i0 * 32 < kc; i0 += U) {
+        uint4 wv[R][U];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int c = lane + 32 * (i0 + u);
+                wv[r][u] = c < kc ? ld_stream_v4(rows[r] + (size_t)c * 8) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int c = lane + 32 * (i0 + u);
+            if (c < kc) {
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int nb = 0; nb < NB; ++nb)
+                        acc[r][nb] = dot8_f16(wv[r][u], xs + nb * ldx + c * 8, acc[r][nb]);
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) acc[r][nb] = warp_sum(acc[r][nb]);
+}
+
+// RMSNorm of NB rows into shared memory: xs[b][j] = (x[b][j] * s_b) * w[j]
+// with s_b = rms_scale(sum_j x[b][j]^2).  Rows b >= B are zero-filled.  The
+// sum of squares is accumulated per thread in index order (stride
+// blockDim.x) and reduced by block_sum; every normalising kernel runs with
+// 256 threads so the statistic rounds alike everywhere.
+template <int NB>
+__device__ __forceinline__ void norm_rows_to_smem(const float* __restrict__ x, int B, int H,
+                                                  const float* __restrict__ w, float eps,
+                                                  float* xs, int ldx, float* red) {
+#pragma unroll 1
+    for (int b = 0; b < NB; ++b) {
+        if (b >= B) {
+            for (int j = threadIdx.x; j < H; j += blockDim.x) xs[b * ldx + j] = 0.f;
+            continue;
+        }
+        const float* xr = x + (size_t)b * H;
+        float ss = 0.f;
+        for (int j = threadIdx.x; j < H; j += blockDim.x) {
+            const float v = xr[j];
+            ss = fmaf(v, v, ss);
+        }
+        const float s = rms_scale(block_sum(ss, red), H, eps);
+        for (int j = threadIdx.x; j < H; j += blockDim.x)
+            xs[b * ldx + j] = __fmul_rn(__fmul_rn(xr[j], s), w[j]);
+    }
+    __syncthreads();
+}
+
+// NeoX rotation of the pair (a, b) = (x_i, x_{i+hd/2}) by (cos, sin):
+// a' = a cos - b sin, b' = b cos + a sin.
+__device__ __forceinline__ void rope_pair(float a, float b, float2 cs, float& ra, float& rb) {
+    ra = fmaf(a, cs.x, -__fmul_rn(b, cs.y));
+    rb = fmaf(b, cs.x, __fmul_rn(a, cs.y));
+}
+
+}  // namespace qwen2

@@ -1,0 +1,98 @@
+"""The C ABI library without a GPU: it loads, exports every symbol the
+header declares, validates configs before touching the device, and its Q8_0
+packer matches the oracle's quantiser byte for byte."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from conftest import ROOT
+
+q2 = pytest.importorskip("qwen2_decoder_forward_gb300")
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(q2.LIB_PATH):
+        from qwen2_decoder_forward_gb300 import build
+        build.build()
+    return q2.lib()
+
+
+def header_symbols():
+    src = open(os.path.join(ROOT, "include", "qwen2.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return set(re.findall(r"\b(qwen2_[a-z0-9_]+)\s*\(", src))
+
+
+def test_every_declared_symbol_is_exported(L):
+    syms = header_symbols()
+    assert syms == set(q2.EXPORTS)
+    for s in syms:
+        assert hasattr(L, s), s
+
+
+def test_kv_bytes_per_position_matches_page_figure(L):
+    s = synth.SHAPES["qwen2.5-0.5b"]
+    assert q2.kv_bytes_per_seq(s, 1) == 24 * 1024
+    assert q2.kv_bytes_per_seq(s, 4096) == 96 * 2**20
+
+
+def _create(L, **over):
+    s = synth.SHAPES["toy"]
+    cfg = q2._Config(s.n_layer, s.hidden, s.n_head, s.n_kv_head, s.head_dim, s.intermediate, s.vocab,
+                     s.rms_eps, s.rope_theta, 0, 0, 64, 1, 16, 0)
+    for k, v in over.items():
+        setattr(cfg, k, v)
+    dummy = np.zeros(16, dtype=np.float32)
+    layers = (q2._LayerWeights * max(cfg.n_layer, 1))()
+    for i in range(len(layers)):
+        for f, _ in q2._LayerWeights._fields_:
+            setattr(layers[i], f, dummy.ctypes.data)
+    w = q2._Weights(dummy.ctypes.data, dummy.ctypes.data, layers)
+    h = ctypes.c_void_p()
+    rc = L.qwen2_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h))
+    return rc, L.qwen2_last_error(None).decode(), h
+
+
+@pytest.mark.parametrize("over,code", [
+    ({"head_dim": 128, "hidden": 512}, q2.QWEN2_E_UNSUPPORTED),
+    ({"hidden": 320}, q2.QWEN2_E_UNSUPPORTED),
+    ({"intermediate": 1000}, q2.QWEN2_E_UNSUPPORTED),
+    ({"n_kv_head": 3}, q2.QWEN2_E_UNSUPPORTED),
+    ({"n_ctx": 0}, q2.QWEN2_E_ARG),
+    ({"vocab": 1}, q2.QWEN2_E_ARG),
+])
+def test_create_rejects_bad_configs_without_a_device(L, over, code):
+    rc, msg, h = _create(L, **over)
+    assert rc == code and msg
+    assert not h.value
+
+
+def test_null_arguments_are_rejected(L):
+    h = ctypes.c_void_p()
+    assert L.qwen2_create(None, None, ctypes.byref(h)) == q2.QWEN2_E_ARG
+    assert L.qwen2_create(None, None, None) == q2.QWEN2_E_ARG
+
+
+def test_q8_0_packer_matches_oracle_bytes(L):
+    rng = np.random.default_rng(0)
+    w = (0.02 * rng.standard_normal((96, 256))).astype(np.float16)
+    w[3, :32] = 0                       # an all-zero block
+    w[5, 40] = np.float16(-1.5)         # a block dominated by one value
+    w[7, 64:96] = np.float16(0.25)      # a constant block
+    q_lib, d_lib = q2.quantize_q8_0(w)
+    q_orc, d_orc = oracle.quantize_q8_0(w)
+    np.testing.assert_array_equal(q_lib, q_orc)
+    np.testing.assert_array_equal(d_lib.view(np.uint16), d_orc.view(np.uint16))
+
+
+def test_q8_0_packer_rejects_ragged_k(L):
+    w = np.zeros((2, 48), dtype=np.float16)
+    q = np.empty((2, 48), dtype=np.int8)
+    d = np.empty((2, 2), dtype=np.uint16)
+    assert L.qwen2_quantize_q8_0(w.ctypes.data, 2, 48, q.ctypes.data, d.ctypes.data) == q2.QWEN2_E_ARG
