@@ -1,0 +1,271 @@
+"""Benchmark of the Qwen2 decoder forward on GB300 (one JSON line on stdout).
+
+Default workload: Qwen2.5-0.5B-shaped model (24 layers, hidden 896, 14/2
+heads, vocab 151936, tied head), seeded synthetic f16 weights, batch 1: a
+128-token prompt is prefilled once (untimed), then each timed step is one
+greedy generation of 256 tokens at positions 128..383 through
+qwen2_decode_steps (one CUDA-graph replay per token, ids fed back on the
+device).  The weights (988 MB) exceed the 129 MB L2, so no flush is needed
+between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--workload NAME]
+
+Under torchrun (N > 1) every rank runs an independent replica (the forward
+has no exchange step); value = tokens of all ranks / max rank time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "decode tokens/s (batch 1 and 32) and prefill tok/s; % of HBM/tensor roofline"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu, self.proc, self.lines = gpu, None, []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def decode_bytes_per_token(shape, positions) -> float:
+    """Algorithmic HBM bytes of one batch-1 decode token at position p:
+    f16 weights once + f32 biases and norms + the embedding row + the KV
+    read of positions 0..p and the KV write of position p."""
+    H, I, V, L = shape.hidden, shape.intermediate, shape.vocab, shape.n_layer
+    nq, nkv = shape.n_head * shape.head_dim, shape.n_kv_head * shape.head_dim
+    w = 2 * (V * H + L * ((nq + 2 * nkv) * H + H * nq + 2 * I * H + H * I))
+    small = 4 * (L * (nq + 2 * nkv + 2 * H) + H) + 2 * H
+    kv_pos = L * 2 * nkv * 4
+    p = np.asarray(positions, dtype=np.float64)
+    return float(np.mean(w + small + kv_pos * (p + 2)))
+
+
+def cpu_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("internal_api") == "openblas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    return len(os.sched_getaffinity(0))
+
+
+def oracle_decode_rate(shape, weights, prompt, n_tokens: int, budget_s: float = 15.0):
+    """The oracle's greedy decode tokens/s on the host cores: prefill the
+    prompt (untimed), then time decode steps until n_tokens or the budget."""
+    import oracle
+    orc = oracle.build_oracle(shape, weights, 4096)
+    cache = orc.new_cache()
+    pre = orc.prefill(cache, prompt)
+    tok = int(pre["ids"][0])
+    t0 = time.perf_counter()
+    done = 0
+    while done < n_tokens and (done == 0 or time.perf_counter() - t0 < budget_s):
+        r = orc.forward(cache, [tok], [len(prompt) + done])
+        tok = int(r["ids"][0])
+        done += 1
+    dt = time.perf_counter() - t0
+    return done / dt, done, dt
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="0.5b-decode-b1")
+    args = ap.parse_args()
+    wl = synth.WORKLOADS[args.workload]
+    shape = synth.SHAPES[wl.shape]
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    config = {"workload": f"{wl.name}: {shape.name} shape, batch {wl.n_seq}, prompt {wl.prompt_len}, "
+                          f"{wl.decode_steps} greedy decode steps per timed step, f16 weights, f32 KV, "
+                          f"n_ctx {wl.n_ctx}",
+              "global_batch": wl.n_seq * world, "seq_len": wl.prompt_len + wl.decode_steps,
+              "parallelism": f"replicas x{world}",
+              "l2": "weights (988 MB) exceed L2 (129 MB): no flush between steps"}
+    weights = synth.make_weights(shape, wl.weight_seed)
+    prompt = wl.prompts(shape.vocab)[0]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        n = max(1, args.steps)
+        rate, done, dt = oracle_decode_rate(shape, weights, prompt, 4 * n, budget_s=20.0)
+        cores = cpu_threads()
+        line = {"impl": "reference", "metric": METRIC, "value": rate, "unit": "tokens/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1e3 / rate, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded random weights)",
+                "config": config,
+                "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                 "sample": f"{done} greedy decode tokens after a {len(prompt)}-token prefill"},
+                "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    import qwen2_decoder_forward_gb300 as q2
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    n_steps = wl.decode_steps
+    model = q2.Qwen2Model(shape, weights, n_ctx=wl.n_ctx, max_seqs=1, max_tokens=len(prompt))
+    _, ids = model.prefill([0], [prompt])
+    first = int(ids[0])
+    p0 = len(prompt)
+    out = torch.empty((n_steps, 1), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        model.decode_steps([0], [first], [p0], n_steps, ids_out=out)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    model.synchronize()
+
+    def barrier():
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    with ClockSampler(local) as clocks:
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms = start.elapsed_time(end)
+    if dist:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    model.synchronize()
+    tokens = args.steps * n_steps * world
+    value = tokens / (ms / 1e3)
+    ms_per_step = ms / args.steps
+
+    # End to end through the public API with host buffers: host token and
+    # position inputs, ids read back into host memory each step.
+    host_ids = np.empty((n_steps, 1), dtype=np.int32)
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        model.decode_steps([0], [first], [p0], n_steps, ids_out=host_ids)
+    t1 = time.perf_counter()
+    e2e_s = t1 - t0
+    if dist:
+        t = torch.tensor([e2e_s], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e = {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": 3 * 4,
+           "d2h_bytes_per_step": int(host_ids.nbytes)}
+
+    hbm, tflops, src = peaks()
+    bytes_tok = decode_bytes_per_token(shape, np.arange(p0, p0 + n_steps))
+    per_token_s = (ms / 1e3) / (args.steps * n_steps)
+    achieved = bytes_tok / per_token_s / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "traffic": None, "kernel": "one decode token (the whole step, all kernels of the graph)",
+                "peak_source": src, "bytes_per_launch": bytes_tok}
+    launches_per_token = 2 + shape.n_layer * 5
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32 activations, f16 weights",
+            "data": "synthetic (seeded random weights of the Qwen2.5-0.5B shape, uniform-random tokens)",
+            "config": config, "clocks": clocks.summary(), "e2e": e2e, "roofline": roofline,
+            "gpu_launches": launches_per_token * n_steps * args.steps}
+    if rank == 0:
+        rate, done, dt = oracle_decode_rate(shape, weights, prompt, 64, budget_s=15.0)
+        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+                                "sample": f"{done} greedy decode tokens after a {len(prompt)}-token prefill"}
+        print(json.dumps(line), flush=True)
+    model.close()
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,167 @@
+"""GPU parity of the CUDA path against the oracle on shapes the oracle runs
+in seconds (toy, ragged, multi-head), element by element, plus the path's
+invariants: fused == unfused and graph == no-graph bit for bit, batch
+invariance, the position error, and KV save / restore."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from parity import (check_free_running, check_hidden, check_kv, check_logits_ids)
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def q2():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import qwen2_decoder_forward_gb300 as m
+    from qwen2_decoder_forward_gb300 import build
+    build.build()
+    return m
+
+
+def run_oracle(shape, w, prompts, n_steps, n_ctx, n_out=1):
+    orc = oracle.build_oracle(shape, w, n_ctx)
+    out = []
+    for p in prompts:
+        cache = orc.new_cache()
+        pre = orc.forward(cache, p, np.arange(len(p)), n_out=n_out)
+        dec = orc.greedy_decode(cache, int(pre["ids"][-1]), len(p), n_steps)
+        out.append((pre, dec, cache))
+    return orc, out
+
+
+@pytest.mark.parametrize("shape_name", ["toy", "ragged", "toy-mha"])
+def test_prefill_and_teacher_forced_decode(q2, shape_name):
+    shape = synth.SHAPES[shape_name]
+    w = synth.make_weights(shape, 0)
+    n_ctx, n_steps = 160, 16
+    prompts = [synth.make_tokens(shape.vocab, 37, 7), synth.make_tokens(shape.vocab, 70, 8)]
+    _, ref = run_oracle(shape, w, prompts, n_steps, n_ctx, n_out=2)
+    with q2.Qwen2Model(shape, w, n_ctx=n_ctx, max_seqs=2, max_tokens=128) as m:
+        logits, ids = m.prefill([0, 1], prompts, n_out=2)
+        hid = m.final_hidden(4).cpu().numpy()
+        lg, ig = logits.cpu().numpy(), ids.cpu().numpy()
+        for s in range(2):
+            pre = ref[s][0]
+            check_logits_ids(lg[2 * s:2 * s + 2], ig[2 * s:2 * s + 2], pre["logits"], f"prefill seq {s}")
+            check_hidden(hid[2 * s:2 * s + 2], pre["final_norm_output"], f"prefill seq {s}")
+        # Teacher-forced batch decode: both sequences each step, fed the
+        # oracle's ids.
+        toks = [int(ref[s][0]["ids"][-1]) for s in range(2)]
+        for step in range(n_steps):
+            pos = [len(prompts[0]) + step, len(prompts[1]) + step]
+            lgt, idt = m.decode_step([0, 1], toks, pos)
+            lgt, idt = lgt.cpu().numpy(), idt.cpu().numpy()
+            hid = m.final_hidden(2).cpu().numpy()
+            for s in range(2):
+                dec = ref[s][1]
+                check_logits_ids(lgt[s:s + 1], idt[s:s + 1], dec["logits"][step:step + 1], f"step {step} seq {s}")
+                check_hidden(hid[s:s + 1], dec["final_norm_output"][step:step + 1], f"step {step} seq {s}")
+            toks = [int(ref[s][1]["ids"][step]) for s in range(2)]
+        kv = m.kv_cache().cpu().numpy()
+        m.synchronize()
+        for s in range(2):
+            check_kv(kv[s], ref[s][2], np.arange(len(prompts[s]) + n_steps), f"seq {s}")
+
+
+def test_free_running_decode_steps_matches_oracle(q2):
+    shape = synth.SHAPES["toy"]
+    w = synth.make_weights(shape, 0)
+    prompt = synth.make_tokens(shape.vocab, 16, 1001)
+    _, ref = run_oracle(shape, w, [prompt], 16, 64)
+    pre, dec, _ = ref[0]
+    with q2.Qwen2Model(shape, w, n_ctx=64, max_seqs=1, max_tokens=16) as m:
+        _, ids = m.prefill([0], [prompt])
+        assert int(ids[0]) == int(pre["ids"][0])
+        out = m.decode_steps([0], [int(ids[0])], [16], 16).cpu().numpy()[:, 0]
+        # Host output buffer path (the call synchronises).
+        host = np.zeros((16, 1), dtype=np.int32)
+        m.decode_steps([0], [int(ids[0])], [16], 16, ids_out=host)
+        m.synchronize()
+    assert check_free_running(out, dec["ids"], dec["logits"], "toy greedy") == 16
+    np.testing.assert_array_equal(host[:, 0], out)
+
+
+@pytest.mark.parametrize("flags", ["fuse", "graph"])
+def test_variants_are_bit_identical(q2, flags):
+    shape = synth.SHAPES["ragged"]
+    w = synth.make_weights(shape, 1)
+    prompt = synth.make_tokens(shape.vocab, 40, 9)
+    variants = ([0, q2.FLAG_NO_FUSE_QKV | q2.FLAG_NO_FUSE_FFN, q2.FLAG_NO_FUSE_QKV, q2.FLAG_NO_FUSE_FFN]
+                if flags == "fuse" else [0, q2.FLAG_NO_GRAPH])
+    outs = []
+    for f in variants:
+        with q2.Qwen2Model(shape, w, n_ctx=96, max_seqs=1, max_tokens=64, flags=f) as m:
+            m.prefill([0], [prompt])
+            rows = []
+            tok = 5
+            for s in range(6):
+                lg, ids = m.decode_step([0], [tok], [40 + s])
+                rows.append(lg.cpu().numpy().copy())
+                tok = int(ids[0])
+            outs.append(np.stack(rows))
+    for o in outs[1:]:
+        assert np.array_equal(o.view(np.uint32), outs[0].view(np.uint32))
+
+
+def test_batch_invariance(q2):
+    """A sequence's decode row gives the same bits alone or in a batch."""
+    shape = synth.SHAPES["toy"]
+    w = synth.make_weights(shape, 2)
+    prompts = [synth.make_tokens(shape.vocab, n, 20 + n) for n in (5, 9, 13)]
+    with q2.Qwen2Model(shape, w, n_ctx=64, max_seqs=3, max_tokens=32) as m:
+        m.prefill([0, 1, 2], prompts)
+        kv0 = m.kv_cache().clone()
+        lb, _ = m.decode_step([0, 1, 2], [1, 2, 3], [5, 9, 13])
+        lb = lb.cpu().numpy()
+        m.kv_cache().copy_(kv0)
+        for s in range(3):
+            ls, _ = m.decode_step([s], [s + 1], [[5, 9, 13][s]])
+            assert np.array_equal(ls.cpu().numpy()[0].view(np.uint32), lb[s].view(np.uint32))
+
+
+def test_position_outside_n_ctx_is_an_error_and_writes_nothing(q2):
+    shape = synth.SHAPES["toy"]
+    w = synth.make_weights(shape, 0)
+    with q2.Qwen2Model(shape, w, n_ctx=32, max_seqs=1, max_tokens=8) as m:
+        m.prefill([0], [[1, 2, 3]])
+        before = m.kv_cache().clone()
+        with pytest.raises(q2.Qwen2Error) as e:
+            m.decode_step([0], [4], [32])
+        assert e.value.code == q2.QWEN2_E_POS
+        with pytest.raises(q2.Qwen2Error) as e:
+            m.decode_steps([0], [4], [30], 3)
+        assert e.value.code == q2.QWEN2_E_POS
+        with pytest.raises(q2.Qwen2Error) as e:
+            m.prefill([0], [[1, 2]], positions=[[31, 32]])
+        assert e.value.code == q2.QWEN2_E_POS
+        with pytest.raises(q2.Qwen2Error) as e:
+            m.decode_step([0], [shape.vocab], [3])
+        assert e.value.code == q2.QWEN2_E_ARG
+        m.synchronize()
+        assert torch.equal(m.kv_cache(), before)
+        m.decode_steps([0], [4], [29], 3)      # the last allowed position
+        m.synchronize()
+
+
+def test_kv_cache_save_and_restore(q2):
+    """Decode, save the caller-visible cache, destroy, recreate, restore and
+    continue: the ids equal an uninterrupted run."""
+    shape = synth.SHAPES["toy"]
+    w = synth.make_weights(shape, 3)
+    prompt = synth.make_tokens(shape.vocab, 12, 30)
+    with q2.Qwen2Model(shape, w, n_ctx=64, max_seqs=1, max_tokens=16) as m:
+        _, ids = m.prefill([0], [prompt])
+        full = m.decode_steps([0], [int(ids[0])], [12], 20).cpu().numpy()[:, 0]
+    with q2.Qwen2Model(shape, w, n_ctx=64, max_seqs=1, max_tokens=16) as m:
+        _, ids = m.prefill([0], [prompt])
+        first = m.decode_steps([0], [int(ids[0])], [12], 10).cpu().numpy()[:, 0]
+        saved = m.kv_cache().cpu().clone()
+    with q2.Qwen2Model(shape, w, n_ctx=64, max_seqs=1, max_tokens=16) as m:
+        m.kv_cache().copy_(saved.cuda())
+        rest = m.decode_steps([0], [int(first[-1])], [22], 10).cpu().numpy()[:, 0]
+        m.synchronize()
+    np.testing.assert_array_equal(np.concatenate([first, rest]), full)
