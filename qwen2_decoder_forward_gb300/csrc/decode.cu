@@ -612,11 +612,21 @@ cudaError_t enqueue_decode_step(Ctx& c, int B, bool want_logits, cudaStream_t st
     return cudaErrorInvalidValue;
 }
 
-// Dynamic shared-memory opt-in for the templated kernels (once at create).
+// Dynamic shared-memory opt-in for the templated kernels (once at create):
+// each may use the device's opt-in maximum less its static shared memory.
+template <class K>
+static cudaError_t allow_smem(K kern, int max_bytes) {
+    cudaFuncAttributes at;
+    cudaError_t e = cudaFuncGetAttributes(&at, kern);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                max_bytes - (int)at.sharedSizeBytes);
+}
+
 cudaError_t decode_set_smem_limits(int max_bytes) {
     cudaError_t e = cudaSuccess;
 #define Q2_SMEM(kern) \
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_bytes);
+    if (e == cudaSuccess) e = allow_smem(kern, max_bytes);
 #define Q2_SMEM_NB(NB)           \
     Q2_SMEM(k_qkv_fused<NB>)     \
     Q2_SMEM(k_gemv_rows<NB>)     \
