@@ -147,6 +147,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="0.5b-decode-b1")
+    ap.add_argument("--tokens-per-step", type=int, default=0,
+                    help="override the decode tokens of one timed step (profiling runs only)")
+    ap.add_argument("--skip-cpu-baseline", action="store_true", help="profiling runs: no oracle timing")
+    ap.add_argument("--flags", type=int, default=0, help="QWEN2_FLAG_* bits for the context")
     args = ap.parse_args()
     wl = synth.WORKLOADS[args.workload]
     shape = synth.SHAPES[wl.shape]
@@ -188,8 +192,8 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
-    n_steps = wl.decode_steps
-    model = q2.Qwen2Model(shape, weights, n_ctx=wl.n_ctx, max_seqs=1, max_tokens=len(prompt))
+    n_steps = args.tokens_per_step or wl.decode_steps
+    model = q2.Qwen2Model(shape, weights, n_ctx=wl.n_ctx, max_seqs=1, max_tokens=len(prompt), flags=args.flags)
     _, ids = model.prefill([0], [prompt])
     first = int(ids[0])
     p0 = len(prompt)
@@ -257,10 +261,11 @@ def main():
             "data": "synthetic (seeded random weights of the Qwen2.5-0.5B shape, uniform-random tokens)",
             "config": config, "clocks": clocks.summary(), "e2e": e2e, "roofline": roofline,
             "gpu_launches": launches_per_token * n_steps * args.steps}
-    if rank == 0:
+    if rank == 0 and not args.skip_cpu_baseline:
         rate, done, dt = oracle_decode_rate(shape, weights, prompt, 64, budget_s=15.0)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
                                 "sample": f"{done} greedy decode tokens after a {len(prompt)}-token prefill"}
+    if rank == 0:
         print(json.dumps(line), flush=True)
     model.close()
     if dist:
