@@ -10,6 +10,7 @@
 #include <vector>
 
 #include "ctx.h"
+#include "persistent.h"
 #include "prefill.h"
 
 using namespace qwen2;
@@ -194,8 +195,18 @@ int check_positions(Ctx& c, int n, const int32_t* pos, int extra) {
     return QWEN2_OK;
 }
 
+bool use_persistent(const Ctx& c, int B) {
+    const uint32_t off = QWEN2_FLAG_NO_MEGAKERNEL | QWEN2_FLAG_NO_FUSE_QKV | QWEN2_FLAG_NO_FUSE_FFN;
+    return B == 1 && c.pers.ok && !(c.cfg.flags & off);
+}
+
+cudaError_t enqueue_step(Ctx& c, int B, bool want_logits, cudaStream_t st) {
+    if (use_persistent(c, B)) return enqueue_decode_persistent(c, want_logits, st);
+    return enqueue_decode_step(c, B, want_logits, st);
+}
+
 int get_graph(Ctx& c, int B, bool want_logits, cudaGraphExec_t* out) {
-    const int key = B | (want_logits ? 1 << 16 : 0);
+    const int key = B | (want_logits ? 1 << 16 : 0) | (use_persistent(c, B) ? 1 << 17 : 0);
     auto it = c.graphs.find(key);
     if (it != c.graphs.end()) {
         *out = it->second;
@@ -203,7 +214,7 @@ int get_graph(Ctx& c, int B, bool want_logits, cudaGraphExec_t* out) {
     }
     cudaGraph_t graph = nullptr;
     Q2_CHECK(&c, cudaStreamBeginCapture(c.cap_stream, cudaStreamCaptureModeThreadLocal));
-    cudaError_t e = enqueue_decode_step(c, B, want_logits, c.cap_stream);
+    cudaError_t e = enqueue_step(c, B, want_logits, c.cap_stream);
     cudaError_t e2 = cudaStreamEndCapture(c.cap_stream, &graph);
     if (e != cudaSuccess) return cuda_fail(&c, e, "decode step capture");
     if (e2 != cudaSuccess) return cuda_fail(&c, e2, "cudaStreamEndCapture");
@@ -218,7 +229,7 @@ int get_graph(Ctx& c, int B, bool want_logits, cudaGraphExec_t* out) {
 
 int run_decode_step(Ctx& c, int B, bool want_logits, cudaStream_t st) {
     if (c.cfg.flags & QWEN2_FLAG_NO_GRAPH) {
-        cudaError_t e = enqueue_decode_step(c, B, want_logits, st);
+        cudaError_t e = enqueue_step(c, B, want_logits, st);
         if (e != cudaSuccess) return cuda_fail(&c, e, "decode step launch");
         return QWEN2_OK;
     }
@@ -267,6 +278,7 @@ int qwen2_create(const qwen2_config* cfg, const qwen2_weights* weights, qwen2_ct
     cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, c.device);
     if (decode_set_smem_limits(max_smem) != cudaSuccess || prefill_set_smem_limits() != cudaSuccess)
         return bail(QWEN2_E_CUDA, "cannot set kernel shared-memory limits");
+    if (persistent_setup(c) != cudaSuccess) return bail(QWEN2_E_CUDA, "persistent decode kernel set-up failed");
     if (cudaStreamCreateWithFlags(&c.cap_stream, cudaStreamNonBlocking) != cudaSuccess)
         return bail(QWEN2_E_CUDA, "cannot create the capture stream");
     if (cudaDeviceSynchronize() != cudaSuccess) return bail(QWEN2_E_CUDA, "set-up failed on the device");

@@ -1,0 +1,88 @@
+// Decode attention arithmetic shared by the per-step attention kernel and the
+// persistent decode kernel, so both produce the same bits.
+//
+// GQA (nnterp encyclopedia qwen2, "Grouped-query attention"): kv head g
+// serves query heads g*group .. g*group + group - 1; scores are
+// q . k / sqrt(64) over keys 0..p (full causal, no window).  Keys are taken
+// in chunks of 64 positions; each chunk yields, per query head, the running
+// maximum m, the sum l of e^(s - m) and acc[d] = sum e^(s - m) v[d]; chunks
+// are merged in chunk order.
+#pragma once
+
+#include "common.cuh"
+
+namespace qwen2 {
+
+constexpr int kHd = 64;        // head_dim this build supports
+constexpr int kAttCh = 64;     // keys per chunk
+constexpr int kMaxGroup = 8;   // query heads per kv head
+constexpr int kPartStride = kHd + 2;  // one partial: m, l, acc[64]
+
+struct AttnSmem {
+    float q[kMaxGroup][kHd];
+    float k[kAttCh][kHd + 1];   // padded: lanes read different keys
+    float v[kAttCh][kHd];
+    float p[kMaxGroup][kAttCh];
+    float m[kMaxGroup];
+    float l[kMaxGroup];
+};
+
+// One chunk of nj <= 64 keys (k, v, q already in `sm`) for `group` query
+// heads, computed by a 256-thread group; emit(h, d, acc, m, l) once per
+// output element.
+template <class S, class Emit>
+__device__ __forceinline__ void attn_chunk(AttnSmem& sm, int group, int nj, Emit emit) {
+    const int tid = threadIdx.x;
+    // Scores q_h . k_j / sqrt(hd); hd = 64 makes the scale 0.125 exact.
+    for (int e = tid; e < group * kAttCh; e += 256) {
+        const int h = e / kAttCh, j = e % kAttCh;
+        float s = -INFINITY;
+        if (j < nj) {
+            float acc = 0.f;
+#pragma unroll 16
+            for (int d = 0; d < kHd; ++d) acc = fmaf(sm.q[h][d], sm.k[j][d], acc);
+            s = acc * 0.125f;
+        }
+        sm.p[h][j] = s;
+    }
+    S::sync();
+    // Per head (one warp each): max, exponentials, sum.
+    const int warp = tid >> 5, lane = tid & 31;
+    for (int h = warp; h < group; h += 8) {
+        const float s0 = sm.p[h][lane], s1 = sm.p[h][lane + 32];
+        const float m = warp_max(fmaxf(s0, s1));
+        const float e0 = expf(s0 - m), e1 = expf(s1 - m);
+        sm.p[h][lane] = e0;
+        sm.p[h][lane + 32] = e1;
+        const float l = warp_sum(e0 + e1);
+        if (lane == 0) {
+            sm.m[h] = m;
+            sm.l[h] = l;
+        }
+    }
+    S::sync();
+    for (int e = tid; e < group * kHd; e += 256) {
+        const int h = e / kHd, d = e % kHd;
+        float acc = 0.f;
+        for (int j = 0; j < nj; ++j) acc = fmaf(sm.p[h][j], sm.v[j][d], acc);
+        emit(h, d, acc, sm.m[h], sm.l[h]);
+    }
+}
+
+// Merge of n chunk partials for element d of one head:
+// M = max m_c, L = sum e^(m_c - M) l_c, o = sum e^(m_c - M) acc_c[d] / L.
+// get(c, i) returns field i of chunk c's partial (0: m, 1: l, 2 + d: acc).
+template <class Get>
+__device__ __forceinline__ float attn_merge(int n, int d, Get get) {
+    float M = -INFINITY;
+    for (int c = 0; c < n; ++c) M = fmaxf(M, get(c, 0));
+    float L = 0.f, O = 0.f;
+    for (int c = 0; c < n; ++c) {
+        const float w = expf(get(c, 0) - M);
+        L = fmaf(w, get(c, 1), L);
+        O = fmaf(w, get(c, 2 + d), O);
+    }
+    return O / L;
+}
+
+}  // namespace qwen2

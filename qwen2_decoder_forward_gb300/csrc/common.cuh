@@ -64,24 +64,34 @@ __device__ __forceinline__ float warp_max(float v) {
     return v;
 }
 
-// Block-wide sum with a fixed reduction order; `red` is shared scratch of at
-// least blockDim.x/32 floats.  Every thread receives the result.
+// Thread-group barriers.  Kernels whose 256 threads are the whole block use
+// SyncBlock; the persistent decode kernel's 256 compute threads (warps 0-7,
+// beside a producer warp) use named barrier 1.
+struct SyncBlock {
+    __device__ __forceinline__ static void sync() { __syncthreads(); }
+};
+struct SyncCompute {
+    __device__ __forceinline__ static void sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+};
+
+// Sum over a 256-thread group with a fixed reduction order; `red` is shared
+// scratch of at least 8 floats.  Every thread of the group gets the result.
+template <class S = SyncBlock>
 __device__ __forceinline__ float block_sum(float v, float* red) {
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    const int nw = blockDim.x >> 5;
     v = warp_sum(v);
-    __syncthreads();
+    S::sync();
     if (lane == 0) red[wid] = v;
-    __syncthreads();
+    S::sync();
     float t = 0.f;
     if (wid == 0) {
-        t = lane < nw ? red[lane] : 0.f;
+        t = lane < 8 ? red[lane] : 0.f;
         t = warp_sum(t);
         if (lane == 0) red[0] = t;
     }
-    __syncthreads();
+    S::sync();
     t = red[0];
-    __syncthreads();
+    S::sync();
     return t;
 }
 

@@ -78,6 +78,25 @@ struct DecodeState {
     int* ids_hist = nullptr; // [kIdsHist][max_seqs] ids per step
 };
 
+// Per-layer weight pointers the persistent decode kernel reads.
+struct PersistLayer {
+    const __half *wqkv, *wo, *wgu, *wd;
+    const float *bqkv, *attn_norm, *ffn_norm;
+};
+
+// State of the persistent batch-1 decode kernel.
+struct PersistState {
+    bool ok = false;                  // the kernel fits this shape and device
+    int grid = 0;                     // one CTA per SM
+    size_t smem = 0;                  // dynamic shared memory per CTA
+    int rows_h = 0, rows_i = 0;       // weight rows per ring stage (K = H, K = I)
+    int act_floats = 0;               // activation / attention scratch floats
+    int max_chunks = 0;               // attention chunks of 64 keys at n_ctx
+    PersistLayer* layers = nullptr;   // [n_layer] on the device
+    unsigned long long* pk = nullptr; // activation packets (value + epoch)
+    unsigned* epoch = nullptr;        // launches so far (never reset)
+};
+
 struct Ctx {
     qwen2_config cfg{};
     int device = 0;
@@ -94,6 +113,7 @@ struct Ctx {
     int* err = nullptr;           // device guard word
     Workspace ws;
     DecodeState ds;
+    PersistState pers;
     int max_rows = 0;             // rows the prefill workspace holds
     int last_rows_out = 0;        // rows of the last call's final_norm_output
     cudaStream_t cap_stream = nullptr;

@@ -4,6 +4,7 @@
 // the residual add, fused RMSNorm + gate/up + SiLU*up, and the LM head fused
 // with a two-stage block argmax.  Also the unfused variants the
 // QWEN2_FLAG_NO_FUSE_* flags select.
+#include "attn.cuh"
 #include "ctx.h"
 #include "rowdot.cuh"
 
@@ -11,9 +12,6 @@ namespace qwen2 {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kAttCh = 64;       // positions per attention split
-constexpr int kMaxGroup = 8;     // query heads per kv head the attention kernel holds
-constexpr int kHd = 64;
 
 struct StepArgs {
     const int* tok;
@@ -187,11 +185,7 @@ __global__ void __launch_bounds__(kThreads) k_swiglu(const float* __restrict__ r
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads) k_attn_decode(StepArgs a, int layer, float* __restrict__ part,
                                                           int* __restrict__ count, int max_chunks) {
-    __shared__ float q_s[kMaxGroup][kHd];
-    __shared__ float k_s[kAttCh][kHd + 1];
-    __shared__ __align__(16) float v_s[kAttCh][kHd];
-    __shared__ float p_s[kMaxGroup][kAttCh];
-    __shared__ float m_s[kMaxGroup], l_s[kMaxGroup];
+    __shared__ __align__(16) AttnSmem sm;
     __shared__ int last_s;
     const int g = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
     const int group = a.nh / a.nkv;
@@ -209,65 +203,28 @@ __global__ void __launch_bounds__(kThreads) k_attn_decode(StepArgs a, int layer,
     const int tid = threadIdx.x;
 
     for (int e = tid; e < group * kHd; e += kThreads)
-        q_s[e / kHd][e % kHd] = a.q[(size_t)b * a.nh * kHd + (size_t)g * group * kHd + e];
+        sm.q[e / kHd][e % kHd] = a.q[(size_t)b * a.nh * kHd + (size_t)g * group * kHd + e];
     const float* kb = kv_ptr(a, slot, layer, 0, g, j0);
     const float* vb = kv_ptr(a, slot, layer, 1, g, j0);
     for (int e = tid; e < nj * (kHd / 4); e += kThreads) {
         const int j = e / (kHd / 4), d4 = (e % (kHd / 4)) * 4;
         const float4 kk = __ldcg(reinterpret_cast<const float4*>(kb + (size_t)j * kHd + d4));
         const float4 vv = __ldcg(reinterpret_cast<const float4*>(vb + (size_t)j * kHd + d4));
-        k_s[j][d4] = kk.x;
-        k_s[j][d4 + 1] = kk.y;
-        k_s[j][d4 + 2] = kk.z;
-        k_s[j][d4 + 3] = kk.w;
-        *reinterpret_cast<float4*>(&v_s[j][d4]) = vv;
+        sm.k[j][d4] = kk.x;
+        sm.k[j][d4 + 1] = kk.y;
+        sm.k[j][d4 + 2] = kk.z;
+        sm.k[j][d4 + 3] = kk.w;
+        *reinterpret_cast<float4*>(&sm.v[j][d4]) = vv;
     }
     __syncthreads();
-
-    // Scores q_h . k_j / sqrt(hd); hd = 64, so the scale 0.125 is exact.
-    const float scale = 0.125f;
-    for (int e = tid; e < group * kAttCh; e += kThreads) {
-        const int h = e / kAttCh, j = e % kAttCh;
-        float s = -INFINITY;
-        if (j < nj) {
-            float acc = 0.f;
-#pragma unroll 16
-            for (int d = 0; d < kHd; ++d) acc = fmaf(q_s[h][d], k_s[j][d], acc);
-            s = acc * scale;
-        }
-        p_s[h][j] = s;
-    }
-    __syncthreads();
-
-    // Per head: max, exponentials, sum (one warp per head).
-    const int warp = tid >> 5, lane = tid & 31;
-    for (int h = warp; h < group; h += kWarps) {
-        const float s0 = p_s[h][lane], s1 = p_s[h][lane + 32];
-        const float m = warp_max(fmaxf(s0, s1));
-        const float e0 = expf(s0 - m), e1 = expf(s1 - m);
-        p_s[h][lane] = e0;
-        p_s[h][lane + 32] = e1;
-        const float l = warp_sum(e0 + e1);
-        if (lane == 0) {
-            m_s[h] = m;
-            l_s[h] = l;
-        }
-    }
-    __syncthreads();
-
-    // acc[h][d] = sum_j e_j v_j[d]
-    const int stride = kHd + 2;
-    for (int e = tid; e < group * kHd; e += kThreads) {
-        const int h = e / kHd, d = e % kHd;
-        float acc = 0.f;
-        for (int j = 0; j < nj; ++j) acc = fmaf(p_s[h][j], v_s[j][d], acc);
-        float* pr = part + (((size_t)b * a.nh + g * group + h) * max_chunks + c) * stride;
+    attn_chunk<SyncBlock>(sm, group, nj, [&](int h, int d, float acc, float m, float l) {
+        float* pr = part + (((size_t)b * a.nh + g * group + h) * max_chunks + c) * kPartStride;
         pr[2 + d] = acc;
         if (d == 0) {
-            pr[0] = m_s[h];
-            pr[1] = l_s[h];
+            pr[0] = m;
+            pr[1] = l;
         }
-    }
+    });
     __threadfence();
     __syncthreads();
     if (tid == 0) {
@@ -277,20 +234,12 @@ __global__ void __launch_bounds__(kThreads) k_attn_decode(StepArgs a, int layer,
     __syncthreads();
     if (!last_s) return;
     __threadfence();
-    // Merge the chunks in order: M = max m_c, L = sum e^(m_c - M) l_c,
-    // o = sum e^(m_c - M) acc_c / L.
+    // The last block of (b, g) merges the chunks in order.
     for (int e = tid; e < group * kHd; e += kThreads) {
         const int h = e / kHd, d = e % kHd;
-        const float* ph = part + (((size_t)b * a.nh + g * group + h) * max_chunks) * stride;
-        float M = -INFINITY;
-        for (int cc = 0; cc < n_chunks; ++cc) M = fmaxf(M, __ldcg(ph + (size_t)cc * stride));
-        float L = 0.f, O = 0.f;
-        for (int cc = 0; cc < n_chunks; ++cc) {
-            const float w = expf(__ldcg(ph + (size_t)cc * stride) - M);
-            L = fmaf(w, __ldcg(ph + (size_t)cc * stride + 1), L);
-            O = fmaf(w, __ldcg(ph + (size_t)cc * stride + 2 + d), O);
-        }
-        a.o[(size_t)b * a.nh * kHd + (size_t)(g * group + h) * kHd + d] = O / L;
+        const float* ph = part + (((size_t)b * a.nh + g * group + h) * max_chunks) * kPartStride;
+        a.o[(size_t)b * a.nh * kHd + (size_t)(g * group + h) * kHd + d] =
+            attn_merge(n_chunks, d, [&](int cc, int i) { return __ldcg(ph + (size_t)cc * kPartStride + i); });
     }
     if (tid == 0) count[b * a.nkv + g] = 0;
 }

@@ -1,0 +1,579 @@
+// Persistent single-launch decode step for one sequence (batch 1).
+//
+// One CTA per SM, all resident (cooperative launch).  Each CTA owns a fixed
+// slice of every weight matrix: the Q/K/V, o_proj and gate/up row pairs and
+// the down_proj and LM-head rows, split evenly over the CTAs.  A producer
+// warp streams the CTA's slices, in the order they are used, through a ring
+// of shared-memory stages with bulk (TMA) copies and mbarriers; the weights
+// do not depend on the activations, so the stream runs ahead of the compute
+// and never waits for a data dependency.  Eight compute warps run the steps
+// of the layer (minfer "Qwen2 / Qwen2.5 Architecture Support", section 1)
+// and exchange activation vectors through global "packets": 64-bit words
+// holding a float and the launch's epoch, written and read with single-copy
+// atomic 64-bit accesses, so a reader that sees the current epoch has the
+// value -- one L2 round trip per dependency, no grid barrier.
+//
+// Per layer the dependencies are x -> Q/K/V (norm needs all of x), q/k/v ->
+// attention, attention partials -> o_proj (the chunk merge is recomputed by
+// every CTA), x -> gate/up (norm), SiLU(gate)*up -> down.  The arithmetic
+// is the per-step kernels' own (rowdot.cuh, attn.cuh), so the logits are
+// bit-identical to the multi-kernel path.
+//
+// Every wait is bounded: a wait that gives up raises kGuardTimeout, and the
+// CTA stops issuing copies, waits for the ones in flight and returns.
+#include "attn.cuh"
+#include "ctx.h"
+#include "persistent.h"
+#include "rowdot.cuh"
+
+namespace qwen2 {
+
+namespace {
+
+constexpr int kCompute = 256;
+constexpr int kThreads = 288;             // 8 compute warps + 1 producer warp
+constexpr unsigned long long kWaitNs = 2000000000ull;  // a wait gives up after 2 s
+
+typedef unsigned long long u64;
+
+__device__ __forceinline__ u64 now_ns() {
+    u64 t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(u64* b, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(u64* b, unsigned parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ void mbar_arrive(u64* b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(u64* b, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, u64* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+// Bounded mbarrier wait; gives up after kWaitNs or when `abort` is set.
+__device__ __forceinline__ bool mbar_wait(u64* b, unsigned parity, volatile int* abort) {
+    if (mbar_try_wait(b, parity)) return true;
+    const u64 t0 = now_ns();
+    while (now_ns() - t0 < kWaitNs) {
+        if (mbar_try_wait(b, parity)) return true;
+        if (abort && *abort) return false;
+    }
+    return false;
+}
+
+// Named-barrier OR over the 256 compute threads.
+__device__ __forceinline__ bool compute_any(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, 256, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void pk_put(u64* p, float v, unsigned ep) {
+    const u64 w = ((u64)ep << 32) | (u64)__float_as_uint(v);
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+__device__ __forceinline__ u64 pk_raw(const u64* p) {
+    u64 w;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+    return w;
+}
+
+// Reader of packets of one epoch; after a failed wait it returns 0 at once
+// and the thread's `failed` flag stays set.
+struct PkReader {
+    unsigned ep;
+    bool failed = false;
+    __device__ __forceinline__ float get(const u64* p) {
+        if (failed) return 0.f;
+        u64 w = pk_raw(p);
+        if ((unsigned)(w >> 32) == ep) return __uint_as_float((unsigned)w);
+        const u64 t0 = now_ns();
+        while ((unsigned)(w >> 32) != ep) {
+            if (now_ns() - t0 > kWaitNs) {
+                failed = true;
+                return 0.f;
+            }
+            __nanosleep(32);
+            w = pk_raw(p);
+        }
+        return __uint_as_float((unsigned)w);
+    }
+};
+
+__device__ __forceinline__ int split(int n, int c, int G) { return (int)(((long long)n * c) / G); }
+
+}  // namespace
+
+// Packet buffer layout per layer (offsets in packets).
+struct PkLayout {
+    int qkv, x1, m, x2, att, per_layer;
+    __host__ __device__ PkLayout(int nqkv, int H, int I, int nh, int max_chunks) {
+        qkv = 0;
+        x1 = nqkv;
+        m = x1 + H;
+        x2 = m + I;
+        att = x2 + H;
+        per_layer = att + nh * max_chunks * kPartStride;
+    }
+};
+
+__global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char* ring = smem;
+    u64* full = reinterpret_cast<u64*>(smem + a.stages * kPersistStage);
+    u64* empty = full + a.stages;
+    float* red = reinterpret_cast<float*>(empty + a.stages);
+    int* misc = reinterpret_cast<int*>(red + 8);  // [0] abort
+    volatile int* abort = misc;
+    float* act = reinterpret_cast<float*>(smem + a.stages * kPersistStage + 256);
+    float* xr = act + a.act_floats;  // raw x [H]
+    AttnSmem& at = *reinterpret_cast<AttnSmem*>(act);
+    float* xs = act;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x, G = gridDim.x;
+    const int H = a.H, I = a.I, V = a.V, L = a.L, nh = a.nh, nkv = a.nkv;
+    const int group = nh / nkv;
+    const int np = a.nqkv / 2;
+    const int rpc_h = a.rows_h, rpc_i = a.rows_i;
+
+    if (tid == 0) {
+        for (int s = 0; s < a.stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kCompute / 32);
+        }
+        misc[0] = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    const unsigned ep = *a.epoch + 1;
+    const int p = a.pos[0], t = a.tok[0], slot = a.slot[0];
+    if (p < 0 || p >= a.n_ctx || t < 0 || t >= V || slot < 0 || slot >= a.max_seqs) {
+        if (tid == 0 && c == 0) raise_guard(a.err, (p < 0 || p >= a.n_ctx) ? kGuardPosition : kGuardToken);
+        return;
+    }
+    const int n_chunks = (p + 1 + kAttCh - 1) / kAttCh;
+    const PkLayout lay(a.nqkv, H, I, nh, a.max_chunks);
+
+    // ------------------------------------------------------------------
+    // Producer: one lane streams this CTA's weight slices into the ring.
+    // ------------------------------------------------------------------
+    if (warp == kCompute / 32) {
+        if (lane != 0) return;
+        int it = 0;
+        bool ok = true;
+        auto issue = [&](const __half* W, int K, int r0, int r1, int rpc) {
+            for (int r = r0; ok && r < r1; r += rpc) {
+                const int n = min(rpc, r1 - r);
+                const int s = it % a.stages;
+                const unsigned k = it / a.stages;
+                if (k > 0 && !mbar_wait(&empty[s], (k - 1) & 1, abort)) {
+                    ok = false;
+                    break;
+                }
+                const unsigned bytes = (unsigned)n * K * 2;
+                mbar_expect_tx(&full[s], bytes);
+                bulk_g2s(ring + (size_t)s * kPersistStage, W + (size_t)r * K, bytes, &full[s]);
+                ++it;
+            }
+        };
+        for (int l = 0; l < L && ok; ++l) {
+            const PersistLayer& Lw = a.layers[l];
+            issue(Lw.wqkv, H, 2 * split(np, c, G), 2 * split(np, c + 1, G), rpc_h);
+            issue(Lw.wo, H, 2 * split(H / 2, c, G), 2 * split(H / 2, c + 1, G), rpc_h);
+            issue(Lw.wgu, H, 2 * split(I, c, G), 2 * split(I, c + 1, G), rpc_h);
+            issue(Lw.wd, I, split(H, c, G), split(H, c + 1, G), rpc_i);
+        }
+        if (ok) issue(a.E, H, split(V, c, G), split(V, c + 1, G), rpc_h);
+        // Wait for every copy still in flight before leaving.
+        for (int j = max(0, it - a.stages); j < it; ++j) mbar_wait(&full[j % a.stages], (j / a.stages) & 1, nullptr);
+        if (!ok && c == 0) raise_guard(a.err, kGuardTimeout);
+        return;
+    }
+
+    // ------------------------------------------------------------------
+    // Compute warps.
+    // ------------------------------------------------------------------
+    PkReader rd{ep};
+    int it = 0;
+    bool dead = false;
+    // Consume this CTA's chunks of one matrix slice in order: fn(stage, row0, n).
+    auto consume = [&](int r0, int r1, int rpc, auto&& fn) {
+        for (int r = r0; !dead && r < r1; r += rpc) {
+            const int n = min(rpc, r1 - r);
+            const int s = it % a.stages;
+            const unsigned k = it / a.stages;
+            const bool ok = mbar_wait(&full[s], k & 1, abort);
+            if (compute_any(!ok)) {
+                dead = true;
+                break;
+            }
+            fn(reinterpret_cast<const __half*>(ring + (size_t)s * kPersistStage), r, n);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+            ++it;
+        }
+    };
+    auto gather = [&](const u64* src, int n, float* dst) {
+        for (int j = tid; j < n; j += kCompute) dst[j] = rd.get(src + j);
+        if (compute_any(rd.failed)) dead = true;
+    };
+
+    const size_t head_stride = (size_t)a.n_ctx * kHd;
+    for (int l = 0; l < L && !dead; ++l) {
+        const PersistLayer& Lw = a.layers[l];
+        u64* pk = a.pk + (size_t)l * lay.per_layer;
+        const u64* pk_prev = a.pk + (size_t)(l - 1) * lay.per_layer;
+        const size_t cache0 = ((size_t)slot * L + l) * 2 * nkv;
+
+        // ---- RMSNorm + Q/K/V + bias + RoPE + KV store -----------------
+        if (l == 0) {
+            for (int j = tid; j < H; j += kCompute) xr[j] = __half2float(a.E[(size_t)t * H + j]);
+        } else {
+            gather(pk_prev + lay.x2, H, xr);
+            if (dead) break;
+        }
+        SyncCompute::sync();
+        norm_rows_to_smem<1, SyncCompute>(xr, 1, H, Lw.attn_norm, a.eps, xs, H, red);
+        consume(2 * split(np, c, G), 2 * split(np, c + 1, G), rpc_h, [&](const __half* st, int r0, int n) {
+            for (int q = warp; q < n / 2; q += 8) {
+                const __half* rows[2] = {st + (size_t)(2 * q) * H, st + (size_t)(2 * q + 1) * H};
+                float acc[2][1];
+                warp_rows_dot<1, 2, LdShared>(rows, H, xs, H, acc);
+                if (lane == 0) {
+                    const int pr = r0 + 2 * q;           // packed row of the pair
+                    const int s = pr / kHd, i = (pr % kHd) >> 1;
+                    const float v0 = acc[0][0] + Lw.bqkv[pr], v1 = acc[1][0] + Lw.bqkv[pr + 1];
+                    if (s < nh + nkv) {
+                        float ra, rb;
+                        rope_pair(v0, v1, a.rope[(size_t)p * (kHd / 2) + i], ra, rb);
+                        if (s >= nh) {
+                            float* kr = a.kv + (cache0 + (s - nh)) * head_stride + (size_t)p * kHd;
+                            kr[i] = ra;
+                            kr[i + kHd / 2] = rb;
+                        }
+                        pk_put(pk + lay.qkv + s * kHd + i, ra, ep);
+                        pk_put(pk + lay.qkv + s * kHd + i + kHd / 2, rb, ep);
+                    } else {
+                        float* vr = a.kv + (cache0 + nkv + (s - nh - nkv)) * head_stride + (size_t)p * kHd;
+                        vr[i] = v0;
+                        vr[i + kHd / 2] = v1;
+                        pk_put(pk + lay.qkv + s * kHd + i, v0, ep);
+                        pk_put(pk + lay.qkv + s * kHd + i + kHd / 2, v1, ep);
+                    }
+                }
+            }
+        });
+        if (dead) break;
+
+        // ---- attention: units (kv head g, chunk of 64 keys) ----------
+        for (int u = c; u < nkv * n_chunks && !dead; u += G) {
+            const int g = u / n_chunks, ch = u % n_chunks;
+            const int j0 = ch * kAttCh, nj = min(kAttCh, p + 1 - j0);
+            SyncCompute::sync();  // the previous unit is done with `at`
+            for (int e = tid; e < group * kHd; e += kCompute)
+                at.q[e / kHd][e % kHd] = rd.get(pk + lay.qkv + (size_t)g * group * kHd + e);
+            const float* kb = a.kv + (cache0 + g) * head_stride + (size_t)j0 * kHd;
+            const float* vb = a.kv + (cache0 + nkv + g) * head_stride + (size_t)j0 * kHd;
+            for (int e = tid; e < nj * (kHd / 4); e += kCompute) {
+                const int j = e / (kHd / 4), d4 = (e % (kHd / 4)) * 4;
+                float4 kk, vv;
+                if (j0 + j < p) {
+                    kk = __ldcg(reinterpret_cast<const float4*>(kb + (size_t)j * kHd + d4));
+                    vv = __ldcg(reinterpret_cast<const float4*>(vb + (size_t)j * kHd + d4));
+                } else {  // this step's key and value: from the packets
+                    const u64* kp = pk + lay.qkv + (size_t)(nh + g) * kHd + d4;
+                    const u64* vp = pk + lay.qkv + (size_t)(nh + nkv + g) * kHd + d4;
+                    kk = make_float4(rd.get(kp), rd.get(kp + 1), rd.get(kp + 2), rd.get(kp + 3));
+                    vv = make_float4(rd.get(vp), rd.get(vp + 1), rd.get(vp + 2), rd.get(vp + 3));
+                }
+                at.k[j][d4] = kk.x;
+                at.k[j][d4 + 1] = kk.y;
+                at.k[j][d4 + 2] = kk.z;
+                at.k[j][d4 + 3] = kk.w;
+                *reinterpret_cast<float4*>(&at.v[j][d4]) = vv;
+            }
+            if (compute_any(rd.failed)) {
+                dead = true;
+                break;
+            }
+            attn_chunk<SyncCompute>(at, group, nj, [&](int h, int d, float acc, float m, float lsum) {
+                u64* pr = pk + lay.att + ((size_t)(g * group + h) * a.max_chunks + ch) * kPartStride;
+                pk_put(pr + 2 + d, acc, ep);
+                if (d == 0) {
+                    pk_put(pr, m, ep);
+                    pk_put(pr + 1, lsum, ep);
+                }
+            });
+        }
+        if (dead) break;
+        SyncCompute::sync();
+
+        // ---- merge the chunks (every CTA), o_proj + residual -----------
+        for (int e = tid; e < nh * kHd; e += kCompute) {
+            const int h = e / kHd, d = e % kHd;
+            const u64* ph = pk + lay.att + (size_t)h * a.max_chunks * kPartStride;
+            xs[e] = attn_merge(n_chunks, d, [&](int cc, int i) { return rd.get(ph + (size_t)cc * kPartStride + i); });
+        }
+        if (compute_any(rd.failed)) break;
+        consume(2 * split(H / 2, c, G), 2 * split(H / 2, c + 1, G), rpc_h, [&](const __half* st, int r0, int n) {
+            for (int q = warp; q < n / 2; q += 8) {
+                const __half* rows[2] = {st + (size_t)(2 * q) * H, st + (size_t)(2 * q + 1) * H};
+                float acc[2][1];
+                warp_rows_dot<1, 2, LdShared>(rows, H, xs, H, acc);
+                if (lane == 0) {
+                    const int r = r0 + 2 * q;
+                    // xr still holds this layer's input x (gathered for Q/K/V).
+                    pk_put(pk + lay.x1 + r, xr[r] + acc[0][0], ep);
+                    pk_put(pk + lay.x1 + r + 1, xr[r + 1] + acc[1][0], ep);
+                }
+            }
+        });
+        if (dead) break;
+
+        // ---- RMSNorm + gate/up + SiLU(gate) * up ----------------------
+        gather(pk + lay.x1, H, xr);
+        if (dead) break;
+        SyncCompute::sync();
+        norm_rows_to_smem<1, SyncCompute>(xr, 1, H, Lw.ffn_norm, a.eps, xs, H, red);
+        consume(2 * split(I, c, G), 2 * split(I, c + 1, G), rpc_h, [&](const __half* st, int r0, int n) {
+            for (int q = warp; q < n / 2; q += 8) {
+                const __half* rows[2] = {st + (size_t)(2 * q) * H, st + (size_t)(2 * q + 1) * H};
+                float acc[2][1];
+                warp_rows_dot<1, 2, LdShared>(rows, H, xs, H, acc);
+                if (lane == 0) pk_put(pk + lay.m + (r0 >> 1) + q, silu_f(acc[0][0]) * acc[1][0], ep);
+            }
+        });
+        if (dead) break;
+
+        // ---- down + residual ------------------------------------------
+        SyncCompute::sync();
+        gather(pk + lay.m, I, xs);
+        if (dead) break;
+        SyncCompute::sync();
+        consume(split(H, c, G), split(H, c + 1, G), rpc_i, [&](const __half* st, int r0, int n) {
+            for (int q = warp; q < n; q += 8) {
+                const __half* rows[1] = {st + (size_t)q * I};
+                float acc[1][1];
+                warp_rows_dot<1, 1, LdShared>(rows, I, xs, I, acc);
+                // xr holds x after the attention add (gathered for gate/up).
+                if (lane == 0) pk_put(pk + lay.x2 + r0 + q, xr[r0 + q] + acc[0][0], ep);
+            }
+        });
+        if (dead) break;
+    }
+
+    // ---- final RMSNorm + tied LM head + argmax --------------------------
+    __shared__ float wv_s[8];
+    __shared__ int wi_s[8];
+    float best_v = -INFINITY;
+    int best_i = 0x7fffffff;
+    if (!dead) {
+        SyncCompute::sync();
+        gather(a.pk + (size_t)(L - 1) * lay.per_layer + lay.x2, H, xr);
+    }
+    if (!dead) {
+        SyncCompute::sync();
+        norm_rows_to_smem<1, SyncCompute>(xr, 1, H, a.final_norm, a.eps, xs, H, red);
+        if (c == 0)
+            for (int j = tid; j < H; j += kCompute) a.hidden[j] = xs[j];
+        consume(split(V, c, G), split(V, c + 1, G), rpc_h, [&](const __half* st, int r0, int n) {
+            for (int q = warp; 2 * q < n; q += 8) {
+                const bool two = 2 * q + 1 < n;
+                const __half* rows[2] = {st + (size_t)(2 * q) * H, st + (size_t)(two ? 2 * q + 1 : 2 * q) * H};
+                float acc[2][1];
+                warp_rows_dot<1, 2, LdShared>(rows, H, xs, H, acc);
+                if (lane == 0) {
+                    const int r = r0 + 2 * q;
+                    if (a.logits) {
+                        a.logits[r] = acc[0][0];
+                        if (two) a.logits[r + 1] = acc[1][0];
+                    }
+                    argmax_merge(best_v, best_i, acc[0][0], r);
+                    if (two) argmax_merge(best_v, best_i, acc[1][0], r + 1);
+                }
+            }
+        });
+    }
+    if (!dead) {
+        if (lane == 0) {
+            wv_s[warp] = best_v;
+            wi_s[warp] = best_i;
+        }
+        SyncCompute::sync();
+        u64* am = a.pk + (size_t)L * lay.per_layer;
+        if (tid == 0) {
+            float v = wv_s[0];
+            int i = wi_s[0];
+            for (int w = 1; w < 8; ++w) argmax_merge(v, i, wv_s[w], wi_s[w]);
+            pk_put(am + 2 * c, v, ep);
+            pk_put(am + 2 * c + 1, __int_as_float(i), ep);
+        }
+        if (c == 0) {
+            // Stage 2: merge the per-CTA pairs; the id becomes the next token.
+            float v = -INFINITY;
+            int i = 0x7fffffff;
+            for (int k = tid; k < G; k += kCompute) argmax_merge(v, i, rd.get(am + 2 * k), __float_as_int(rd.get(am + 2 * k + 1)));
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+                argmax_merge(v, i, ov, oi);
+            }
+            SyncCompute::sync();
+            if (lane == 0) {
+                wv_s[warp] = v;
+                wi_s[warp] = i;
+            }
+            const bool failed = compute_any(rd.failed);
+            if (tid == 0 && !failed) {
+                float fv = wv_s[0];
+                int fi = wi_s[0];
+                for (int w = 1; w < 8; ++w) argmax_merge(fv, fi, wv_s[w], wi_s[w]);
+                if (fi < 0 || fi >= V) {
+                    raise_guard(a.err, kGuardShape);
+                    fi = 0;
+                }
+                a.ids_hist[(size_t)(*a.step % kIdsHist) * a.hist_stride] = fi;
+                a.tok[0] = fi;
+                a.pos[0] = p + 1;
+                *a.step = *a.step + 1;
+                *a.epoch = ep;
+            }
+            if (failed) dead = true;
+        }
+    }
+    if (dead) {
+        *abort = 1;
+        if (tid == 0) raise_guard(a.err, kGuardTimeout);
+    }
+}
+
+cudaError_t persistent_setup(Ctx& c) {
+    const qwen2_config& g = c.cfg;
+    const int H = g.hidden, I = g.intermediate;
+    c.pers.ok = false;
+    const size_t act = std::max(sizeof(AttnSmem), (size_t)std::max(H, I) * 4);
+    const size_t smem = (size_t)kPersistStages * kPersistStage + 256 + act + (size_t)H * 4;
+    int dev_max = 0;
+    cudaDeviceGetAttribute(&dev_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, c.device);
+    const int rows_h = (kPersistStage / (2 * H)) & ~1;
+    const int rows_i = kPersistStage / (2 * I);
+    if (smem + 1024 > (size_t)dev_max || rows_h < 2 || rows_i < 1) return cudaSuccess;  // unsupported shape
+    cudaError_t e = cudaFuncSetAttribute(k_decode_persistent, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_decode_persistent, kThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaSuccess;
+    int coop = 0;
+    cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, c.device);
+    if (!coop) return cudaSuccess;
+    c.pers.grid = c.n_sm;
+    c.pers.smem = smem;
+    c.pers.rows_h = rows_h;
+    c.pers.rows_i = rows_i;
+    c.pers.act_floats = (int)(act / 4);
+    c.pers.max_chunks = (g.n_ctx + kAttCh - 1) / kAttCh;
+    const PkLayout lay(c.nqkv, H, I, g.n_head, c.pers.max_chunks);
+    const size_t n_pk = (size_t)g.n_layer * lay.per_layer + 2 * (size_t)c.pers.grid;
+    std::vector<PersistLayer> hl(g.n_layer);
+    for (int l = 0; l < g.n_layer; ++l) {
+        const DevLayer& D = c.layers[l];
+        hl[l] = PersistLayer{D.wqkv.w, D.wo.w, D.wgu.w, D.wd.w, D.bqkv, D.attn_norm, D.ffn_norm};
+    }
+    void* p = nullptr;
+    if ((e = cudaMalloc(&p, hl.size() * sizeof(PersistLayer))) != cudaSuccess) return e;
+    c.allocs.push_back(p);
+    c.pers.layers = static_cast<PersistLayer*>(p);
+    if ((e = cudaMemcpy(p, hl.data(), hl.size() * sizeof(PersistLayer), cudaMemcpyHostToDevice)) != cudaSuccess)
+        return e;
+    if ((e = cudaMalloc(&p, n_pk * 8)) != cudaSuccess) return e;
+    c.allocs.push_back(p);
+    c.pers.pk = static_cast<unsigned long long*>(p);
+    if ((e = cudaMemset(p, 0, n_pk * 8)) != cudaSuccess) return e;
+    if ((e = cudaMalloc(&p, 4)) != cudaSuccess) return e;
+    c.allocs.push_back(p);
+    c.pers.epoch = static_cast<unsigned*>(p);
+    if ((e = cudaMemset(p, 0, 4)) != cudaSuccess) return e;
+    c.pers.ok = true;
+    return cudaSuccess;
+}
+
+cudaError_t enqueue_decode_persistent(Ctx& c, bool want_logits, cudaStream_t st) {
+    PersistentArgs a;
+    a.layers = c.pers.layers;
+    a.E = c.embed.w;
+    a.final_norm = c.final_norm;
+    a.kv = c.kv;
+    a.rope = c.rope;
+    a.tok = c.ds.tok;
+    a.pos = c.ds.pos;
+    a.slot = c.ds.slot;
+    a.step = c.ds.step;
+    a.ids_hist = c.ds.ids_hist;
+    a.hist_stride = c.cfg.max_seqs;
+    a.epoch = c.pers.epoch;
+    a.pk = c.pers.pk;
+    a.logits = want_logits ? c.ws.logits : nullptr;
+    a.hidden = c.ws.hidden;
+    a.err = c.err;
+    a.H = c.cfg.hidden;
+    a.I = c.cfg.intermediate;
+    a.V = c.cfg.vocab;
+    a.L = c.cfg.n_layer;
+    a.nh = c.cfg.n_head;
+    a.nkv = c.cfg.n_kv_head;
+    a.n_ctx = c.cfg.n_ctx;
+    a.nqkv = c.nqkv;
+    a.eps = c.cfg.rms_eps;
+    a.stages = kPersistStages;
+    a.rows_h = c.pers.rows_h;
+    a.rows_i = c.pers.rows_i;
+    a.act_floats = c.pers.act_floats;
+    a.max_chunks = c.pers.max_chunks;
+    a.max_seqs = c.cfg.max_seqs;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(c.pers.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = c.pers.smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_decode_persistent, a);
+}
+
+}  // namespace qwen2

@@ -14,11 +14,20 @@
 
 namespace qwen2 {
 
+// Where a weight row is read from: global memory (streamed, read-only path)
+// or shared memory (a stage the persistent kernel's producer filled).
+struct LdGlobal {
+    __device__ __forceinline__ static uint4 ld(const __half* p) { return ld_stream_v4(p); }
+};
+struct LdShared {
+    __device__ __forceinline__ static uint4 ld(const __half* p) { return *reinterpret_cast<const uint4*>(p); }
+};
+
 // Dot products of R weight rows with NB activation vectors held in shared
 // memory (xs + nb*ldx, 16-byte aligned, K floats each).  Loads of all R rows
 // are issued together, U chunks per lane per row at a time.  acc[r][nb] is
 // valid in lane 0.
-template <int NB, int R, int U = 8>
+template <int NB, int R, class Ld = LdGlobal, int U = 8>
 __device__ __forceinline__ void warp_rows_dot(const __half* const (&rows)[R], int K,
                                               const float* xs, int ldx, float (&acc)[R][NB]) {
     const int lane = threadIdx.x & 31;
@@ -34,7 +43,7 @@ __device__ __forceinline__ void warp_rows_dot(const __half* const (&rows)[R], in
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int c = lane + 32 * (i0 + u);
-                wv[r][u] = c < kc ? ld_stream_v4(rows[r] + (size_t)c * 8) : make_uint4(0, 0, 0, 0);
+                wv[r][u] = c < kc ? Ld::ld(rows[r] + (size_t)c * 8) : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -56,30 +65,30 @@ __device__ __forceinline__ void warp_rows_dot(const __half* const (&rows)[R], in
 
 // RMSNorm of NB rows into shared memory: xs[b][j] = (x[b][j] * s_b) * w[j]
 // with s_b = rms_scale(sum_j x[b][j]^2).  Rows b >= B are zero-filled.  The
-// sum of squares is accumulated per thread in index order (stride
-// blockDim.x) and reduced by block_sum; every normalising kernel runs with
-// 256 threads so the statistic rounds alike everywhere.
-template <int NB>
+// sum of squares is accumulated per thread in index order (stride 256 over
+// a 256-thread group) and reduced by block_sum, so the statistic rounds
+// alike in every kernel.  `x` may point to global or shared memory.
+template <int NB, class S = SyncBlock>
 __device__ __forceinline__ void norm_rows_to_smem(const float* __restrict__ x, int B, int H,
                                                   const float* __restrict__ w, float eps,
                                                   float* xs, int ldx, float* red) {
+    const int tid = threadIdx.x;
 #pragma unroll 1
     for (int b = 0; b < NB; ++b) {
         if (b >= B) {
-            for (int j = threadIdx.x; j < H; j += blockDim.x) xs[b * ldx + j] = 0.f;
+            for (int j = tid; j < H; j += 256) xs[b * ldx + j] = 0.f;
             continue;
         }
         const float* xr = x + (size_t)b * H;
         float ss = 0.f;
-        for (int j = threadIdx.x; j < H; j += blockDim.x) {
+        for (int j = tid; j < H; j += 256) {
             const float v = xr[j];
             ss = fmaf(v, v, ss);
         }
-        const float s = rms_scale(block_sum(ss, red), H, eps);
-        for (int j = threadIdx.x; j < H; j += blockDim.x)
-            xs[b * ldx + j] = __fmul_rn(__fmul_rn(xr[j], s), w[j]);
+        const float s = rms_scale(block_sum<S>(ss, red), H, eps);
+        for (int j = tid; j < H; j += 256) xs[b * ldx + j] = __fmul_rn(__fmul_rn(xr[j], s), w[j]);
     }
-    __syncthreads();
+    S::sync();
 }
 
 // NeoX rotation of the pair (a, b) = (x_i, x_{i+hd/2}) by (cos, sin):

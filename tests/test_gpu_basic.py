@@ -85,26 +85,34 @@ def test_free_running_decode_steps_matches_oracle(q2):
     np.testing.assert_array_equal(host[:, 0], out)
 
 
+@pytest.mark.parametrize("shape_name", ["ragged", "toy"])
 @pytest.mark.parametrize("flags", ["fuse", "graph"])
-def test_variants_are_bit_identical(q2, flags):
-    shape = synth.SHAPES["ragged"]
+def test_variants_are_bit_identical(q2, flags, shape_name):
+    shape = synth.SHAPES[shape_name]
     w = synth.make_weights(shape, 1)
     prompt = synth.make_tokens(shape.vocab, 40, 9)
-    variants = ([0, q2.FLAG_NO_FUSE_QKV | q2.FLAG_NO_FUSE_FFN, q2.FLAG_NO_FUSE_QKV, q2.FLAG_NO_FUSE_FFN]
-                if flags == "fuse" else [0, q2.FLAG_NO_GRAPH])
+    # Batch-1 decode runs the persistent kernel by default; the unfused flags
+    # and FLAG_NO_MEGAKERNEL select the per-step kernels.
+    variants = ([0, q2.FLAG_NO_MEGAKERNEL, q2.FLAG_NO_FUSE_QKV | q2.FLAG_NO_FUSE_FFN, q2.FLAG_NO_FUSE_QKV,
+                 q2.FLAG_NO_FUSE_FFN]
+                if flags == "fuse" else [0, q2.FLAG_NO_GRAPH, q2.FLAG_NO_GRAPH | q2.FLAG_NO_MEGAKERNEL])
     outs = []
     for f in variants:
-        with q2.Qwen2Model(shape, w, n_ctx=96, max_seqs=1, max_tokens=64, flags=f) as m:
+        with q2.Qwen2Model(shape, w, n_ctx=128, max_seqs=1, max_tokens=64, flags=f) as m:
             m.prefill([0], [prompt])
             rows = []
             tok = 5
             for s in range(6):
                 lg, ids = m.decode_step([0], [tok], [40 + s])
                 rows.append(lg.cpu().numpy().copy())
+                rows.append(m.final_hidden(1).cpu().numpy()[0].copy())
                 tok = int(ids[0])
-            outs.append(np.stack(rows))
+            ids = m.decode_steps([0], [tok], [46], 70).cpu().numpy()
+            m.synchronize()
+            outs.append((np.concatenate([r.ravel() for r in rows]), ids))
     for o in outs[1:]:
-        assert np.array_equal(o.view(np.uint32), outs[0].view(np.uint32))
+        assert np.array_equal(o[0].view(np.uint32), outs[0][0].view(np.uint32))
+        np.testing.assert_array_equal(o[1], outs[0][1])
 
 
 def test_batch_invariance(q2):
