@@ -247,20 +247,24 @@ def main():
     e2e = {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": 3 * 4,
            "d2h_bytes_per_step": int(host_ids.nbytes)}
 
+    persistent = bool(model.features & q2.FEATURE_PERSISTENT_DECODE) and not (
+        args.flags & (q2.FLAG_NO_MEGAKERNEL | q2.FLAG_NO_FUSE_QKV | q2.FLAG_NO_FUSE_FFN))
     hbm, tflops, src = peaks()
     bytes_tok = decode_bytes_per_token(shape, np.arange(p0, p0 + n_steps))
     per_token_s = (ms / 1e3) / (args.steps * n_steps)
     achieved = bytes_tok / per_token_s / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                "traffic": None, "kernel": "one decode token (the whole step, all kernels of the graph)",
+                "traffic": None, "kernel": "one decode token: " + (
+                    "k_decode_persistent (one launch per token)" if persistent else "all kernels of the step graph"),
                 "peak_source": src, "bytes_per_launch": bytes_tok}
-    launches_per_token = 2 + shape.n_layer * 5
+    launches_per_token = 1 if persistent else 2 + shape.n_layer * 5
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32 activations, f16 weights",
             "data": "synthetic (seeded random weights of the Qwen2.5-0.5B shape, uniform-random tokens)",
             "config": config, "clocks": clocks.summary(), "e2e": e2e, "roofline": roofline,
-            "gpu_launches": launches_per_token * n_steps * args.steps}
+            "gpu_launches": launches_per_token * n_steps * args.steps,
+            "decode_kernel": "persistent" if persistent else "per-step"}
     if rank == 0 and not args.skip_cpu_baseline:
         rate, done, dt = oracle_decode_rate(shape, weights, prompt, 64, budget_s=15.0)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",

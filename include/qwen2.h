@@ -72,6 +72,11 @@ extern "C" {
 #define QWEN2_FLAG_NO_GRAPH      0x4u  /* launch decode kernels one by one, without a CUDA graph */
 #define QWEN2_FLAG_NO_MEGAKERNEL 0x8u  /* decode with one kernel per step of the layer instead of the
                                           persistent single-launch decode kernel */
+#define QWEN2_FLAG_PROFILE       0x10u /* the persistent decode kernel records per-phase timestamps
+                                          (qwen2_profile_marks); costs a few stores per phase */
+
+/* ---- feature bits (qwen2_features) --------------------------------------- */
+#define QWEN2_FEATURE_PERSISTENT_DECODE 0x1u  /* batch-1 decode runs the persistent single-launch kernel */
 
 typedef struct qwen2_config {
     int32_t n_layer;        /* num_hidden_layers (24 on Qwen2.5-0.5B) */
@@ -197,6 +202,19 @@ int qwen2_synchronize(qwen2_ctx *ctx, void *stream);
  * biases, norm weights and, for Q8_0, scales), with 256-byte alignment
  * padding between tensors. */
 int64_t qwen2_weight_bytes(const qwen2_ctx *ctx);
+
+/* Feature bits of this context (QWEN2_FEATURE_*): which kernels its calls
+ * will run on this device and shape.  0 for NULL. */
+uint32_t qwen2_features(const qwen2_ctx *ctx);
+
+/* Timestamps of the last persistent decode launch of a context created with
+ * QWEN2_FLAG_PROFILE: out receives up to max_marks int64 values laid out
+ * [cta][mark] (the GPU global timer in ns; mark 0 is the launch start, then
+ * one mark per finished phase: per layer Q/K/V, attention, chunk merge,
+ * o_proj, gate/up, down; then the LM head and the final argmax).  *n_cta
+ * and *n_marks receive the two sizes.  QWEN2_E_ARG if profiling is off.
+ * Synchronises the device. */
+int qwen2_profile_marks(qwen2_ctx *ctx, int64_t *out, int64_t max_marks, int32_t *n_cta, int32_t *n_marks);
 
 /* Bytes one sequence's KV cache takes: n_layer * 2 * n_kv_head * n_ctx *
  * head_dim * 4 (24 KB per position on Qwen2.5-0.5B, minfer page section 6). */

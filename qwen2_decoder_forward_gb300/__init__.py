@@ -37,13 +37,15 @@ FLAG_NO_FUSE_QKV = 0x1
 FLAG_NO_FUSE_FFN = 0x2
 FLAG_NO_GRAPH = 0x4
 FLAG_NO_MEGAKERNEL = 0x8
+FLAG_PROFILE = 0x10
+FEATURE_PERSISTENT_DECODE = 0x1
 
 # Every symbol include/qwen2.h declares.
 EXPORTS = (
     "qwen2_create", "qwen2_destroy", "qwen2_last_error", "qwen2_kv_cache",
     "qwen2_prefill", "qwen2_decode_step", "qwen2_decode_steps",
     "qwen2_final_hidden", "qwen2_synchronize", "qwen2_weight_bytes",
-    "qwen2_kv_bytes_per_seq", "qwen2_quantize_q8_0",
+    "qwen2_kv_bytes_per_seq", "qwen2_quantize_q8_0", "qwen2_features", "qwen2_profile_marks",
 )
 
 
@@ -115,6 +117,10 @@ def lib() -> ctypes.CDLL:
     L.qwen2_kv_bytes_per_seq.restype = i64
     L.qwen2_quantize_q8_0.argtypes = [_P, i64, i64, _P, _P]
     L.qwen2_quantize_q8_0.restype = ctypes.c_int
+    L.qwen2_features.argtypes = [_P]
+    L.qwen2_features.restype = ctypes.c_uint32
+    L.qwen2_profile_marks.argtypes = [_P, _P, i64, pi32, pi32]
+    L.qwen2_profile_marks.restype = ctypes.c_int
     _lib = L
     return L
 
@@ -222,6 +228,21 @@ class Qwen2Model:
     @property
     def weight_bytes(self) -> int:
         return int(lib().qwen2_weight_bytes(self._h))
+
+    @property
+    def features(self) -> int:
+        """QWEN2_FEATURE_* bits: which kernels this context runs."""
+        return int(lib().qwen2_features(self._h))
+
+    def profile_marks(self) -> np.ndarray:
+        """Per-phase timestamps (ns) of the last persistent decode launch,
+        [n_cta, n_marks] (context created with FLAG_PROFILE)."""
+        n_cta, n_marks = ctypes.c_int32(), ctypes.c_int32()
+        cap = 4096 * 256
+        buf = np.zeros(cap, dtype=np.int64)
+        self._check(lib().qwen2_profile_marks(self._h, buf.ctypes.data, cap, ctypes.byref(n_cta),
+                                              ctypes.byref(n_marks)))
+        return buf[:n_cta.value * n_marks.value].reshape(n_cta.value, n_marks.value)
 
     # -- the entry points ----------------------------------------------------
     def prefill(self, seq_ids, tokens, positions=None, n_out: int = 1, want_logits: bool = True,

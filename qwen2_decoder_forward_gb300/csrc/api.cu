@@ -282,6 +282,7 @@ int qwen2_create(const qwen2_config* cfg, const qwen2_weights* weights, qwen2_ct
     if (cudaStreamCreateWithFlags(&c.cap_stream, cudaStreamNonBlocking) != cudaSuccess)
         return bail(QWEN2_E_CUDA, "cannot create the capture stream");
     if (cudaDeviceSynchronize() != cudaSuccess) return bail(QWEN2_E_CUDA, "set-up failed on the device");
+    if (!c.pers.ok) c.last_error = "note: persistent decode kernel unavailable: " + c.pers.why_not;
     *out = h;
     return QWEN2_OK;
 }
@@ -494,6 +495,24 @@ int qwen2_synchronize(qwen2_ctx* h, void* stream) {
 }
 
 int64_t qwen2_weight_bytes(const qwen2_ctx* h) { return h ? (int64_t)h->c.wbytes : 0; }
+
+uint32_t qwen2_features(const qwen2_ctx* h) {
+    if (!h) return 0;
+    return h->c.pers.ok ? QWEN2_FEATURE_PERSISTENT_DECODE : 0u;
+}
+
+int qwen2_profile_marks(qwen2_ctx* h, int64_t* out, int64_t max_marks, int32_t* n_cta, int32_t* n_marks) {
+    if (!h) return QWEN2_E_ARG;
+    Ctx& c = h->c;
+    if (!c.pers.prof || !out || !n_cta || !n_marks)
+        return fail(&c, QWEN2_E_ARG, "profiling is off (create with QWEN2_FLAG_PROFILE) or null argument");
+    *n_cta = c.pers.grid;
+    *n_marks = c.pers.prof_marks;
+    const int64_t n = std::min<int64_t>(max_marks, (int64_t)c.pers.grid * c.pers.prof_marks);
+    Q2_CHECK(&c, cudaDeviceSynchronize());
+    Q2_CHECK(&c, cudaMemcpy(out, c.pers.prof, n * 8, cudaMemcpyDeviceToHost));
+    return QWEN2_OK;
+}
 
 int64_t qwen2_kv_bytes_per_seq(const qwen2_config* g) {
     if (!g) return 0;

@@ -92,9 +92,13 @@ struct PersistState {
     int rows_h = 0, rows_i = 0;       // weight rows per ring stage (K = H, K = I)
     int act_floats = 0;               // activation / attention scratch floats
     int max_chunks = 0;               // attention chunks of 64 keys at n_ctx
+    int merge_group = 0;              // chunks merged per shared-memory pass
     PersistLayer* layers = nullptr;   // [n_layer] on the device
     unsigned long long* pk = nullptr; // activation packets (value + epoch)
     unsigned* epoch = nullptr;        // launches so far (never reset)
+    long long* prof = nullptr;        // per-phase timestamps (QWEN2_FLAG_PROFILE)
+    int prof_marks = 0;
+    std::string why_not;              // why the kernel is unavailable, if it is
 };
 
 struct Ctx {

@@ -130,6 +130,31 @@ struct PkReader {
     }
 };
 
+// Read n packets with all of a thread's loads in flight at once (element j
+// at addr(j) goes to store(j, value)); only packets not yet of this epoch
+// are polled again.  Threads of the 256-thread compute group take elements
+// tid, tid + 256, ...
+template <int KMAX, class Addr, class Store>
+__device__ __forceinline__ void pk_gather(PkReader& rd, int n, Addr addr, Store store) {
+    const int tid = threadIdx.x;
+    for (int j0 = 0; j0 < n; j0 += KMAX * 256) {
+        u64 w[KMAX];
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k) {
+            const int j = j0 + tid + 256 * k;
+            if (j < n) w[k] = pk_raw(addr(j));
+        }
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k) {
+            const int j = j0 + tid + 256 * k;
+            if (j < n) {
+                const float v = (unsigned)(w[k] >> 32) == rd.ep ? __uint_as_float((unsigned)w[k]) : rd.get(addr(j));
+                store(j, v);
+            }
+        }
+    }
+}
+
 __device__ __forceinline__ int split(int n, int c, int G) { return (int)(((long long)n * c) / G); }
 
 }  // namespace
@@ -147,7 +172,7 @@ struct PkLayout {
     }
 };
 
-__global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArgs a) {
+__global__ void __maxnreg__(224) k_decode_persistent(PersistentArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* ring = smem;
     u64* full = reinterpret_cast<u64*>(smem + a.stages * kPersistStage);
@@ -228,6 +253,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
     PkReader rd{ep};
     int it = 0;
     bool dead = false;
+    int mark_i = 0;
+    auto mark = [&]() {
+        if (a.prof && tid == 0) a.prof[(size_t)c * a.prof_marks + mark_i] = (long long)now_ns();
+        ++mark_i;
+    };
+    mark();
     // Consume this CTA's chunks of one matrix slice in order: fn(stage, row0, n).
     auto consume = [&](int r0, int r1, int rpc, auto&& fn) {
         for (int r = r0; !dead && r < r1; r += rpc) {
@@ -246,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
         }
     };
     auto gather = [&](const u64* src, int n, float* dst) {
-        for (int j = tid; j < n; j += kCompute) dst[j] = rd.get(src + j);
+        pk_gather<10>(rd, n, [&](int j) { return src + j; }, [&](int j, float v) { dst[j] = v; });
         if (compute_any(rd.failed)) dead = true;
     };
 
@@ -296,33 +327,47 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
             }
         });
         if (dead) break;
+        mark();
 
         // ---- attention: units (kv head g, chunk of 64 keys) ----------
         for (int u = c; u < nkv * n_chunks && !dead; u += G) {
             const int g = u / n_chunks, ch = u % n_chunks;
             const int j0 = ch * kAttCh, nj = min(kAttCh, p + 1 - j0);
             SyncCompute::sync();  // the previous unit is done with `at`
-            for (int e = tid; e < group * kHd; e += kCompute)
-                at.q[e / kHd][e % kHd] = rd.get(pk + lay.qkv + (size_t)g * group * kHd + e);
+            const u64* qp = pk + lay.qkv + (size_t)g * group * kHd;
+            pk_gather<2>(rd, group * kHd, [&](int e) { return qp + e; },
+                         [&](int e, float v) { at.q[e / kHd][e % kHd] = v; });
             const float* kb = a.kv + (cache0 + g) * head_stride + (size_t)j0 * kHd;
             const float* vb = a.kv + (cache0 + nkv + g) * head_stride + (size_t)j0 * kHd;
-            for (int e = tid; e < nj * (kHd / 4); e += kCompute) {
-                const int j = e / (kHd / 4), d4 = (e % (kHd / 4)) * 4;
-                float4 kk, vv;
-                if (j0 + j < p) {
-                    kk = __ldcg(reinterpret_cast<const float4*>(kb + (size_t)j * kHd + d4));
-                    vv = __ldcg(reinterpret_cast<const float4*>(vb + (size_t)j * kHd + d4));
-                } else {  // this step's key and value: from the packets
-                    const u64* kp = pk + lay.qkv + (size_t)(nh + g) * kHd + d4;
-                    const u64* vp = pk + lay.qkv + (size_t)(nh + nkv + g) * kHd + d4;
-                    kk = make_float4(rd.get(kp), rd.get(kp + 1), rd.get(kp + 2), rd.get(kp + 3));
-                    vv = make_float4(rd.get(vp), rd.get(vp + 1), rd.get(vp + 2), rd.get(vp + 3));
+            const int nold = min(nj, p - j0);  // keys of earlier steps, read from the cache
+            float4 kk[4], vv[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int e = tid + 256 * k, j = e / (kHd / 4), d4 = (e % (kHd / 4)) * 4;
+                if (j < nold) {
+                    kk[k] = __ldcg(reinterpret_cast<const float4*>(kb + (size_t)j * kHd + d4));
+                    vv[k] = __ldcg(reinterpret_cast<const float4*>(vb + (size_t)j * kHd + d4));
                 }
-                at.k[j][d4] = kk.x;
-                at.k[j][d4 + 1] = kk.y;
-                at.k[j][d4 + 2] = kk.z;
-                at.k[j][d4 + 3] = kk.w;
-                *reinterpret_cast<float4*>(&at.v[j][d4]) = vv;
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int e = tid + 256 * k, j = e / (kHd / 4), d4 = (e % (kHd / 4)) * 4;
+                if (j < nold) {
+                    at.k[j][d4] = kk[k].x;
+                    at.k[j][d4 + 1] = kk[k].y;
+                    at.k[j][d4 + 2] = kk[k].z;
+                    at.k[j][d4 + 3] = kk[k].w;
+                    *reinterpret_cast<float4*>(&at.v[j][d4]) = vv[k];
+                }
+            }
+            if (nold < nj) {  // this step's key and value (position p): from the packets
+                const u64* kp = pk + lay.qkv + (size_t)(nh + g) * kHd;
+                const u64* vp = pk + lay.qkv + (size_t)(nh + nkv + g) * kHd;
+                pk_gather<1>(rd, 2 * kHd, [&](int e) { return e < kHd ? kp + e : vp + (e - kHd); },
+                             [&](int e, float v) {
+                                 if (e < kHd) at.k[nold][e] = v;
+                                 else at.v[nold][e - kHd] = v;
+                             });
             }
             if (compute_any(rd.failed)) {
                 dead = true;
@@ -339,14 +384,70 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
         }
         if (dead) break;
         SyncCompute::sync();
+        mark();
 
         // ---- merge the chunks (every CTA), o_proj + residual -----------
-        for (int e = tid; e < nh * kHd; e += kCompute) {
-            const int h = e / kHd, d = e % kHd;
-            const u64* ph = pk + lay.att + (size_t)h * a.max_chunks * kPartStride;
-            xs[e] = attn_merge(n_chunks, d, [&](int cc, int i) { return rd.get(ph + (size_t)cc * kPartStride + i); });
+        // Same arithmetic as attn_merge: M = max m_c, then in chunk order
+        // w = e^(m_c - M), L = fma(w, l_c, L), O = fma(w, acc_c, O); o = O / L.
+        // The chunk maxima are gathered first, then (l, acc) a group of
+        // chunks at a time through shared memory.
+        {
+            float* mst = act + H;                         // [nh][n_chunks]
+            float* gst = mst + nh * a.max_chunks;         // [nh][group][65]
+            const int gc_max = a.merge_group;
+            const u64* att = pk + lay.att;
+            pk_gather<4>(rd, nh * n_chunks,
+                         [&](int j) { return att + ((size_t)(j / n_chunks) * a.max_chunks + j % n_chunks) * kPartStride; },
+                         [&](int j, float v) { mst[j] = v; });
+            if (compute_any(rd.failed)) break;
+            float Mv[4], Lv[4], Ov[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int e = tid + 256 * k;
+                Mv[k] = -INFINITY;
+                Lv[k] = 0.f;
+                Ov[k] = 0.f;
+                if (e < nh * kHd)
+                    for (int cc = 0; cc < n_chunks; ++cc) Mv[k] = fmaxf(Mv[k], mst[(e / kHd) * n_chunks + cc]);
+            }
+            for (int c0 = 0; c0 < n_chunks && !dead; c0 += gc_max) {
+                const int gc = min(gc_max, n_chunks - c0);
+                const int per_h = gc * (kHd + 1);
+                pk_gather<16>(rd, nh * per_h,
+                              [&](int j) {
+                                  const int h = j / per_h, r = j % per_h;
+                                  return att + ((size_t)h * a.max_chunks + c0 + r / (kHd + 1)) * kPartStride + 1 +
+                                         r % (kHd + 1);
+                              },
+                              [&](int j, float v) { gst[j] = v; });
+                if (compute_any(rd.failed)) {
+                    dead = true;
+                    break;
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int e = tid + 256 * k;
+                    if (e < nh * kHd) {
+                        const int h = e / kHd, d = e % kHd;
+                        for (int cc = 0; cc < gc; ++cc) {
+                            const float w = expf(mst[h * n_chunks + c0 + cc] - Mv[k]);
+                            const float* gp = gst + (size_t)(h * gc + cc) * (kHd + 1);
+                            Lv[k] = fmaf(w, gp[0], Lv[k]);
+                            Ov[k] = fmaf(w, gp[1 + d], Ov[k]);
+                        }
+                    }
+                }
+                SyncCompute::sync();
+            }
+            if (dead) break;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int e = tid + 256 * k;
+                if (e < nh * kHd) xs[e] = Ov[k] / Lv[k];
+            }
+            SyncCompute::sync();
         }
-        if (compute_any(rd.failed)) break;
+        mark();
         consume(2 * split(H / 2, c, G), 2 * split(H / 2, c + 1, G), rpc_h, [&](const __half* st, int r0, int n) {
             for (int q = warp; q < n / 2; q += 8) {
                 const __half* rows[2] = {st + (size_t)(2 * q) * H, st + (size_t)(2 * q + 1) * H};
@@ -361,6 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
             }
         });
         if (dead) break;
+        mark();
 
         // ---- RMSNorm + gate/up + SiLU(gate) * up ----------------------
         gather(pk + lay.x1, H, xr);
@@ -376,6 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
             }
         });
         if (dead) break;
+        mark();
 
         // ---- down + residual ------------------------------------------
         SyncCompute::sync();
@@ -392,6 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
             }
         });
         if (dead) break;
+        mark();
     }
 
     // ---- final RMSNorm + tied LM head + argmax --------------------------
@@ -427,6 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
         });
     }
     if (!dead) {
+        mark();
         if (lane == 0) {
             wv_s[warp] = best_v;
             wi_s[warp] = best_i;
@@ -444,7 +549,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
             // Stage 2: merge the per-CTA pairs; the id becomes the next token.
             float v = -INFINITY;
             int i = 0x7fffffff;
-            for (int k = tid; k < G; k += kCompute) argmax_merge(v, i, rd.get(am + 2 * k), __float_as_int(rd.get(am + 2 * k + 1)));
+            for (int k = tid; k < G; k += kCompute) {
+                const float kv_ = rd.get(am + 2 * k);
+                argmax_merge(v, i, kv_, __float_as_int(rd.get(am + 2 * k + 1)));
+            }
             for (int o = 16; o > 0; o >>= 1) {
                 const float ov = __shfl_xor_sync(0xffffffffu, v, o);
                 const int oi = __shfl_xor_sync(0xffffffffu, i, o);
@@ -472,6 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
             }
             if (failed) dead = true;
         }
+        mark();
     }
     if (dead) {
         *abort = 1;
@@ -489,22 +598,39 @@ cudaError_t persistent_setup(Ctx& c) {
     cudaDeviceGetAttribute(&dev_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, c.device);
     const int rows_h = (kPersistStage / (2 * H)) & ~1;
     const int rows_i = kPersistStage / (2 * I);
-    if (smem + 1024 > (size_t)dev_max || rows_h < 2 || rows_i < 1) return cudaSuccess;  // unsupported shape
+    if (smem + 1024 > (size_t)dev_max || rows_h < 2 || rows_i < 1) {
+        c.pers.why_not = "shared memory or stage size does not fit this shape";
+        return cudaSuccess;
+    }
     cudaError_t e = cudaFuncSetAttribute(k_decode_persistent, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_decode_persistent, kThreads, smem);
     if (e != cudaSuccess) return e;
-    if (per_sm < 1) return cudaSuccess;
+    if (per_sm < 1) {
+        c.pers.why_not = "occupancy query gives 0 blocks per SM";
+        return cudaSuccess;
+    }
     int coop = 0;
     cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, c.device);
-    if (!coop) return cudaSuccess;
+    if (!coop) {
+        c.pers.why_not = "device has no cooperative launch";
+        return cudaSuccess;
+    }
     c.pers.grid = c.n_sm;
     c.pers.smem = smem;
     c.pers.rows_h = rows_h;
     c.pers.rows_i = rows_i;
     c.pers.act_floats = (int)(act / 4);
     c.pers.max_chunks = (g.n_ctx + kAttCh - 1) / kAttCh;
+    // Chunk-merge staging: o [H], chunk maxima [nh][max_chunks], then
+    // (l, acc) of `merge_group` chunks per head.
+    const int left = c.pers.act_floats - H - g.n_head * c.pers.max_chunks;
+    c.pers.merge_group = left / (g.n_head * (kHd + 1));
+    if (c.pers.merge_group < 1 || g.n_head * kHd > 1024) {
+        c.pers.why_not = "attention merge staging does not fit (n_ctx or heads too large)";
+        return cudaSuccess;
+    }
     const PkLayout lay(c.nqkv, H, I, g.n_head, c.pers.max_chunks);
     const size_t n_pk = (size_t)g.n_layer * lay.per_layer + 2 * (size_t)c.pers.grid;
     std::vector<PersistLayer> hl(g.n_layer);
@@ -526,6 +652,14 @@ cudaError_t persistent_setup(Ctx& c) {
     c.allocs.push_back(p);
     c.pers.epoch = static_cast<unsigned*>(p);
     if ((e = cudaMemset(p, 0, 4)) != cudaSuccess) return e;
+    if (g.flags & QWEN2_FLAG_PROFILE) {
+        c.pers.prof_marks = persistent_marks(g.n_layer);
+        const size_t nb = (size_t)c.pers.grid * c.pers.prof_marks * 8;
+        if ((e = cudaMalloc(&p, nb)) != cudaSuccess) return e;
+        c.allocs.push_back(p);
+        c.pers.prof = static_cast<long long*>(p);
+        if ((e = cudaMemset(p, 0, nb)) != cudaSuccess) return e;
+    }
     c.pers.ok = true;
     return cudaSuccess;
 }
@@ -563,6 +697,9 @@ cudaError_t enqueue_decode_persistent(Ctx& c, bool want_logits, cudaStream_t st)
     a.act_floats = c.pers.act_floats;
     a.max_chunks = c.pers.max_chunks;
     a.max_seqs = c.cfg.max_seqs;
+    a.merge_group = c.pers.merge_group;
+    a.prof = c.pers.prof;
+    a.prof_marks = c.pers.prof_marks;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(c.pers.grid);
     cfg.blockDim = dim3(kThreads);

@@ -27,8 +27,12 @@ struct PersistentArgs {
     int* err;
     int H, I, V, L, nh, nkv, n_ctx, nqkv;
     float eps;
-    int stages, rows_h, rows_i, act_floats, max_chunks, max_seqs;
+    int stages, rows_h, rows_i, act_floats, max_chunks, max_seqs, merge_group;
+    long long* prof;   // nullable: [grid][prof_marks] timestamps
+    int prof_marks;
 };
+
+inline int persistent_marks(int n_layer) { return 1 + 6 * n_layer + 2; }
 
 // Size the kernel for this context and allocate its packet buffers; leaves
 // c.pers.ok false (and returns cudaSuccess) when the shape or device does
