@@ -209,11 +209,15 @@ uint32_t qwen2_features(const qwen2_ctx *ctx);
 
 /* Timestamps of the last persistent decode launch of a context created with
  * QWEN2_FLAG_PROFILE: out receives up to max_marks int64 values laid out
- * [cta][mark] (the GPU global timer in ns; mark 0 is the launch start, then
- * one mark per finished phase: per layer Q/K/V, attention, chunk merge,
- * o_proj, gate/up, down; then the LM head and the final argmax).  *n_cta
- * and *n_marks receive the two sizes.  QWEN2_E_ARG if profiling is off.
- * Synchronises the device. */
+ * [cta][mark] (the GPU global timer in ns, 0 where a CTA did not pass a
+ * mark).  Mark 0 is the launch start; layer l owns marks 1 + 16 l + k for
+ * k = 0 input x gathered, 1 normed, 2 Q/K/V done, 3 queries ready
+ * (attention CTAs only), 4 attention done, 5 attention partials counted,
+ * 6 chunk merge done, 7 o_proj done, 8 x counted, 9 x gathered, 10 gate/up
+ * done, 11 SwiGLU output counted, 12 gathered, 13 down done; marks
+ * 1 + 16 L, 2 + 16 L and 3 + 16 L are the final x gathered, the LM head
+ * done and the argmax done.  *n_cta and *n_marks receive the two sizes.
+ * QWEN2_E_ARG if profiling is off.  Synchronises the device. */
 int qwen2_profile_marks(qwen2_ctx *ctx, int64_t *out, int64_t max_marks, int32_t *n_cta, int32_t *n_marks);
 
 /* Bytes one sequence's KV cache takes: n_layer * 2 * n_kv_head * n_ctx *

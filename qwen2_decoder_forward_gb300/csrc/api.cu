@@ -486,6 +486,7 @@ int qwen2_synchronize(qwen2_ctx* h, void* stream) {
     Q2_CHECK(&c, cudaMemcpy(&word, c.err, 4, cudaMemcpyDeviceToHost));
     if (word) {
         Q2_CHECK(&c, cudaMemset(c.err, 0, 4));
+        Q2_CHECK(&c, persistent_reset(c));
         static const char* names[] = {"none", "position outside [0, n_ctx)", "token outside [0, vocab)",
                                       "unexpected shape", "bounded wait timed out"};
         const char* nm = word > 0 && word < 5 ? names[word] : "unknown";

@@ -38,10 +38,16 @@ __device__ __forceinline__ void attn_chunk(AttnSmem& sm, int group, int nj, Emit
         const int h = e / kAttCh, j = e % kAttCh;
         float s = -INFINITY;
         if (j < nj) {
-            float acc = 0.f;
-#pragma unroll 16
-            for (int d = 0; d < kHd; ++d) acc = fmaf(sm.q[h][d], sm.k[j][d], acc);
-            s = acc * 0.125f;
+            // Four partial sums over d = 4i + {0,1,2,3}, added in a fixed order.
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+            for (int d = 0; d < kHd; d += 4) {
+                a0 = fmaf(sm.q[h][d], sm.k[j][d], a0);
+                a1 = fmaf(sm.q[h][d + 1], sm.k[j][d + 1], a1);
+                a2 = fmaf(sm.q[h][d + 2], sm.k[j][d + 2], a2);
+                a3 = fmaf(sm.q[h][d + 3], sm.k[j][d + 3], a3);
+            }
+            s = ((a0 + a1) + (a2 + a3)) * 0.125f;
         }
         sm.p[h][j] = s;
     }
@@ -63,9 +69,19 @@ __device__ __forceinline__ void attn_chunk(AttnSmem& sm, int group, int nj, Emit
     S::sync();
     for (int e = tid; e < group * kHd; e += 256) {
         const int h = e / kHd, d = e % kHd;
-        float acc = 0.f;
-        for (int j = 0; j < nj; ++j) acc = fmaf(sm.p[h][j], sm.v[j][d], acc);
-        emit(h, d, acc, sm.m[h], sm.l[h]);
+        // Four partial sums over keys j = 4i + {0,1,2,3} below nj & ~3, the
+        // last nj % 4 keys into the first, then added in a fixed order (rows
+        // of v past nj are never read).
+        const int nj4 = nj & ~3;
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        for (int j = 0; j < nj4; j += 4) {
+            a0 = fmaf(sm.p[h][j], sm.v[j][d], a0);
+            a1 = fmaf(sm.p[h][j + 1], sm.v[j + 1][d], a1);
+            a2 = fmaf(sm.p[h][j + 2], sm.v[j + 2][d], a2);
+            a3 = fmaf(sm.p[h][j + 3], sm.v[j + 3][d], a3);
+        }
+        for (int j = nj4; j < nj; ++j) a0 = fmaf(sm.p[h][j], sm.v[j][d], a0);
+        emit(h, d, (a0 + a1) + (a2 + a3), sm.m[h], sm.l[h]);
     }
 }
 

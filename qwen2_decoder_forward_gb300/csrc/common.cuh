@@ -50,6 +50,18 @@ __device__ __forceinline__ float dot8_f16(uint4 w, const float* x, float acc) {
     return acc;
 }
 
+// The same sum as dot8_f16 with the eight activations already in registers
+// (xa = x[0..3], xb = x[4..7]), for kernels that share one load of x
+// between several weight rows.
+__device__ __forceinline__ float dot8_f16_r(uint4 w, float4 xa, float4 xb, float acc) {
+    float2 f;
+    f = h2_to_f2(w.x); acc = fmaf(f.x, xa.x, acc); acc = fmaf(f.y, xa.y, acc);
+    f = h2_to_f2(w.y); acc = fmaf(f.x, xa.z, acc); acc = fmaf(f.y, xa.w, acc);
+    f = h2_to_f2(w.z); acc = fmaf(f.x, xb.x, acc); acc = fmaf(f.y, xb.y, acc);
+    f = h2_to_f2(w.w); acc = fmaf(f.x, xb.z, acc); acc = fmaf(f.y, xb.w, acc);
+    return acc;
+}
+
 // Sum over the 32 lanes by a fixed xor butterfly; lane 0's value is the one
 // every kernel uses.
 __device__ __forceinline__ float warp_sum(float v) {

@@ -95,7 +95,9 @@ struct PersistState {
     int merge_group = 0;              // chunks merged per shared-memory pass
     PersistLayer* layers = nullptr;   // [n_layer] on the device
     unsigned long long* pk = nullptr; // activation packets (value + epoch)
-    unsigned* epoch = nullptr;        // launches so far (never reset)
+    unsigned* epoch = nullptr;        // completed launches (reset only after a device guard)
+    unsigned long long* cnt = nullptr; // per-phase arrival counters
+    size_t pk_bytes = 0, cnt_bytes = 0;
     long long* prof = nullptr;        // per-phase timestamps (QWEN2_FLAG_PROFILE)
     int prof_marks = 0;
     std::string why_not;              // why the kernel is unavailable, if it is

@@ -108,6 +108,28 @@ __device__ __forceinline__ u64 pk_raw(const u64* p) {
     return w;
 }
 
+// Per-phase arrival counters: every CTA adds 1 when it has written its
+// packets of a phase; a consumer CTA has one thread wait until the counter
+// reaches epoch * CTAs and then reads the packets once (each packet still
+// carries its epoch, so an early counter only costs a re-poll).  Polling
+// one line with one thread per CTA is far cheaper than every thread
+// polling the packets themselves.
+constexpr int kCntStride = 16;  // one 128-byte line per counter
+__device__ __forceinline__ void cnt_arrive(u64* cnt) {
+    asm volatile("red.relaxed.gpu.global.add.u64 [%0], 1;" ::"l"(cnt) : "memory");
+}
+__device__ __forceinline__ bool cnt_wait(const u64* cnt, u64 target) {
+    u64 v = pk_raw(cnt);
+    if (v >= target) return true;
+    const u64 t0 = now_ns();
+    while (v < target) {
+        if (now_ns() - t0 > kWaitNs) return false;
+        __nanosleep(20);
+        v = pk_raw(cnt);
+    }
+    return true;
+}
+
 // Reader of packets of one epoch; after a failed wait it returns 0 at once
 // and the thread's `failed` flag stays set.
 struct PkReader {
@@ -131,14 +153,16 @@ struct PkReader {
 };
 
 // Read n packets with all of a thread's loads in flight at once (element j
-// at addr(j) goes to store(j, value)); only packets not yet of this epoch
-// are polled again.  Threads of the 256-thread compute group take elements
-// tid, tid + 256, ...
+// at addr(j) goes to store(j, value)).  Packets not yet of this epoch are
+// all polled again together, so a thread waits about one L2 round trip
+// after the last of its packets lands.  Threads of the 256-thread compute
+// group take elements tid, tid + 256, ...
 template <int KMAX, class Addr, class Store>
 __device__ __forceinline__ void pk_gather(PkReader& rd, int n, Addr addr, Store store) {
     const int tid = threadIdx.x;
     for (int j0 = 0; j0 < n; j0 += KMAX * 256) {
         u64 w[KMAX];
+        unsigned pending = 0;
 #pragma unroll
         for (int k = 0; k < KMAX; ++k) {
             const int j = j0 + tid + 256 * k;
@@ -148,9 +172,33 @@ __device__ __forceinline__ void pk_gather(PkReader& rd, int n, Addr addr, Store 
         for (int k = 0; k < KMAX; ++k) {
             const int j = j0 + tid + 256 * k;
             if (j < n) {
-                const float v = (unsigned)(w[k] >> 32) == rd.ep ? __uint_as_float((unsigned)w[k]) : rd.get(addr(j));
-                store(j, v);
+                if ((unsigned)(w[k] >> 32) == rd.ep) store(j, __uint_as_float((unsigned)w[k]));
+                else pending |= 1u << k;
             }
+        }
+        if (pending && !rd.failed) {
+            const u64 t0 = now_ns();
+            while (pending) {
+                __nanosleep(100);
+#pragma unroll
+                for (int k = 0; k < KMAX; ++k)
+                    if (pending & (1u << k)) w[k] = pk_raw(addr(j0 + tid + 256 * k));
+#pragma unroll
+                for (int k = 0; k < KMAX; ++k)
+                    if ((pending & (1u << k)) && (unsigned)(w[k] >> 32) == rd.ep) {
+                        store(j0 + tid + 256 * k, __uint_as_float((unsigned)w[k]));
+                        pending &= ~(1u << k);
+                    }
+                if (pending && now_ns() - t0 > kWaitNs) {
+                    rd.failed = true;
+                    break;
+                }
+            }
+        }
+        if (rd.failed) {
+#pragma unroll
+            for (int k = 0; k < KMAX; ++k)
+                if (pending & (1u << k)) store(j0 + tid + 256 * k, 0.f);
         }
     }
 }
@@ -159,20 +207,34 @@ __device__ __forceinline__ int split(int n, int c, int G) { return (int)(((long 
 
 }  // namespace
 
-// Packet buffer layout per layer (offsets in packets).
+// Packet buffer layout per layer (offsets in packets).  Every buffer is
+// written kPkRep times; CTA c reads copy c % kPkRep, so the reads of the
+// 152 CTAs spread over kPkRep times more L2 lines.
+constexpr int kPkRep = 4;
 struct PkLayout {
-    int qkv, x1, m, x2, att, per_layer;
+    int qkv, x1, m, x2, att, per_layer;          // offsets of copy 0
+    int n_qkv, n_x, n_m, n_att;                  // packets per copy
     __host__ __device__ PkLayout(int nqkv, int H, int I, int nh, int max_chunks) {
+        n_qkv = nqkv;
+        n_x = H;
+        n_m = I;
+        n_att = nh * max_chunks * kPartStride;
         qkv = 0;
-        x1 = nqkv;
-        m = x1 + H;
-        x2 = m + I;
-        att = x2 + H;
-        per_layer = att + nh * max_chunks * kPartStride;
+        x1 = qkv + kPkRep * n_qkv;
+        m = x1 + kPkRep * n_x;
+        x2 = m + kPkRep * n_m;
+        att = x2 + kPkRep * n_x;
+        per_layer = att + kPkRep * n_att;
     }
 };
 
-__global__ void __maxnreg__(224) k_decode_persistent(PersistentArgs a) {
+// Write one value to all copies of a buffer (`stride` packets apart).
+__device__ __forceinline__ void pk_put_all(u64* p, int stride, float v, unsigned ep) {
+#pragma unroll
+    for (int r = 0; r < kPkRep; ++r) pk_put(p + (size_t)r * stride, v, ep);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* ring = smem;
     u64* full = reinterpret_cast<u64*>(smem + a.stages * kPersistStage);
@@ -248,40 +310,96 @@ __global__ void __maxnreg__(224) k_decode_persistent(PersistentArgs a) {
     }
 
     // ------------------------------------------------------------------
-    // Compute warps.
+    // Compute warps.  Every load that does not depend on the incoming
+    // activations (norm weights, biases, RoPE factors, cached keys/values)
+    // is issued before the wait for them.
     // ------------------------------------------------------------------
     PkReader rd{ep};
     int it = 0;
-    bool dead = false;
-    int mark_i = 0;
-    auto mark = [&]() {
-        if (a.prof && tid == 0) a.prof[(size_t)c * a.prof_marks + mark_i] = (long long)now_ns();
-        ++mark_i;
+    bool dead = false, bad = false;
+    // Profiling marks (QWEN2_FLAG_PROFILE): mark(id) stores the global timer
+    // at slot id; per layer l the slots are 1 + 16 l + k (see kMark*).
+    auto mark = [&](int id) {
+        if (a.prof && tid == 0) a.prof[(size_t)c * a.prof_marks + id] = (long long)now_ns();
     };
-    mark();
+    mark(0);
     // Consume this CTA's chunks of one matrix slice in order: fn(stage, row0, n).
+    // A wait that gives up marks the thread bad; the phase end turns that
+    // into a group-wide decision.
     auto consume = [&](int r0, int r1, int rpc, auto&& fn) {
-        for (int r = r0; !dead && r < r1; r += rpc) {
+        for (int r = r0; r < r1; r += rpc) {
             const int n = min(rpc, r1 - r);
             const int s = it % a.stages;
             const unsigned k = it / a.stages;
-            const bool ok = mbar_wait(&full[s], k & 1, abort);
-            if (compute_any(!ok)) {
-                dead = true;
-                break;
-            }
-            fn(reinterpret_cast<const __half*>(ring + (size_t)s * kPersistStage), r, n);
+            if (!bad && !mbar_wait(&full[s], k & 1, abort)) bad = true;
+            if (!bad) fn(reinterpret_cast<const __half*>(ring + (size_t)s * kPersistStage), r, n);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
             ++it;
         }
     };
+    // Consume a whole slice at once when it fits in the ring: wait for all
+    // its stages, let fn spread its rows over the warps (row_ptr(r) is the
+    // shared-memory copy of row r), then release the stages.
+    auto consume_all = [&](int r0, int r1, int rpc, int K, auto&& fn) {
+        const int nch = (r1 - r0 + rpc - 1) / rpc;
+        for (int j = 0; j < nch; ++j) {
+            const int s = (it + j) % a.stages;
+            const unsigned k = (it + j) / a.stages;
+            if (!bad && !mbar_wait(&full[s], k & 1, abort)) bad = true;
+        }
+        const int it0 = it;
+        if (!bad)
+            fn([&](int r) {
+                const int j = (r - r0) / rpc;
+                return reinterpret_cast<const __half*>(ring + (size_t)((it0 + j) % a.stages) * kPersistStage) +
+                       (size_t)((r - r0) % rpc) * K;
+            });
+        __syncwarp();
+        if (lane == 0)
+            for (int j = 0; j < nch; ++j) mbar_arrive(&empty[(it0 + j) % a.stages]);
+        it += nch;
+    };
+    auto phase_end = [&]() {
+        dead = compute_any(bad || rd.failed);
+        return dead;
+    };
+    // Arrive at / wait for counter `k` of this launch (thread 0 of the group).
+    auto arrive = [&](int k) {
+        if (tid == 0) cnt_arrive(a.cnt + (size_t)k * kCntStride);
+    };
+    auto wait_cnt = [&](int k) {
+        if (tid == 0 && !cnt_wait(a.cnt + (size_t)k * kCntStride, (u64)ep * (u64)G)) bad = true;
+        SyncCompute::sync();
+    };
     auto gather = [&](const u64* src, int n, float* dst) {
-        pk_gather<10>(rd, n, [&](int j) { return src + j; }, [&](int j, float v) { dst[j] = v; });
-        if (compute_any(rd.failed)) dead = true;
+        pk_gather<8>(rd, n, [&](int j) { return src + j; }, [&](int j, float v) { dst[j] = v; });
+    };
+    // Norm weights of the next normalisation, in registers (j = tid + 256 k).
+    float nw[4];
+    auto load_norm = [&](const float* w) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) nw[k] = tid + 256 * k < H ? w[tid + 256 * k] : 0.f;
+    };
+    // RMSNorm of xr into xs with the prefetched weights; the same arithmetic
+    // as norm_rows_to_smem (per-thread sum in index order, block_sum).
+    auto norm = [&]() {
+        float ss = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (tid + 256 * k < H) ss = fmaf(xr[tid + 256 * k], xr[tid + 256 * k], ss);
+        const float sc = rms_scale(block_sum<SyncCompute>(ss, red), H, a.eps);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (tid + 256 * k < H) xs[tid + 256 * k] = __fmul_rn(__fmul_rn(xr[tid + 256 * k], sc), nw[k]);
+        SyncCompute::sync();
     };
 
+    __shared__ float pre_bias[64];
+    __shared__ float2 pre_rope[32];
     const size_t head_stride = (size_t)a.n_ctx * kHd;
+    const int qkv_r0 = 2 * split(np, c, G), qkv_r1 = 2 * split(np, c + 1, G);
+    const int rc = c % kPkRep;  // the packet copy this CTA reads
     for (int l = 0; l < L && !dead; ++l) {
         const PersistLayer& Lw = a.layers[l];
         u64* pk = a.pk + (size_t)l * lay.per_layer;
@@ -289,57 +407,67 @@ __global__ void __maxnreg__(224) k_decode_persistent(PersistentArgs a) {
         const size_t cache0 = ((size_t)slot * L + l) * 2 * nkv;
 
         // ---- RMSNorm + Q/K/V + bias + RoPE + KV store -----------------
+        load_norm(Lw.attn_norm);
+        for (int r = qkv_r0 + tid; r < qkv_r1 && r - qkv_r0 < 64; r += kCompute) {
+            pre_bias[r - qkv_r0] = Lw.bqkv[r];
+            if (((r - qkv_r0) & 1) == 0) pre_rope[(r - qkv_r0) >> 1] = a.rope[(size_t)p * (kHd / 2) + ((r % kHd) >> 1)];
+        }
         if (l == 0) {
             for (int j = tid; j < H; j += kCompute) xr[j] = __half2float(a.E[(size_t)t * H + j]);
         } else {
-            gather(pk_prev + lay.x2, H, xr);
-            if (dead) break;
+            wait_cnt((l - 1) * 5 + 4);
+            gather(pk_prev + lay.x2 + (size_t)rc * lay.n_x, H, xr);
         }
-        SyncCompute::sync();
-        norm_rows_to_smem<1, SyncCompute>(xr, 1, H, Lw.attn_norm, a.eps, xs, H, red);
-        consume(2 * split(np, c, G), 2 * split(np, c + 1, G), rpc_h, [&](const __half* st, int r0, int n) {
-            for (int q = warp; q < n / 2; q += 8) {
-                const __half* rows[2] = {st + (size_t)(2 * q) * H, st + (size_t)(2 * q + 1) * H};
+        if (phase_end()) break;
+        const int mb = 1 + 16 * l;
+        mark(mb + 0);
+        norm();
+        mark(mb + 1);
+        consume_all(qkv_r0, qkv_r1, rpc_h, H, [&](auto row_ptr) {
+            for (int q = warp; q < (qkv_r1 - qkv_r0) / 2; q += 8) {
+                const int pr = qkv_r0 + 2 * q;  // packed row of the pair
+                const __half* rows[2] = {row_ptr(pr), row_ptr(pr + 1)};
                 float acc[2][1];
-                warp_rows_dot<1, 2, LdShared>(rows, H, xs, H, acc);
+                warp_rows_dot<1, 2, LdShared, 4>(rows, H, xs, H, acc);
                 if (lane == 0) {
-                    const int pr = r0 + 2 * q;           // packed row of the pair
                     const int s = pr / kHd, i = (pr % kHd) >> 1;
-                    const float v0 = acc[0][0] + Lw.bqkv[pr], v1 = acc[1][0] + Lw.bqkv[pr + 1];
+                    const int lr = pr - qkv_r0;
+                    const float b0 = lr < 64 ? pre_bias[lr] : Lw.bqkv[pr];
+                    const float b1 = lr < 64 ? pre_bias[lr + 1] : Lw.bqkv[pr + 1];
+                    const float v0 = acc[0][0] + b0, v1 = acc[1][0] + b1;
                     if (s < nh + nkv) {
+                        const float2 cs = lr < 64 ? pre_rope[lr >> 1] : a.rope[(size_t)p * (kHd / 2) + i];
                         float ra, rb;
-                        rope_pair(v0, v1, a.rope[(size_t)p * (kHd / 2) + i], ra, rb);
+                        rope_pair(v0, v1, cs, ra, rb);
+                        pk_put_all(pk + lay.qkv + s * kHd + i, lay.n_qkv, ra, ep);
+                        pk_put_all(pk + lay.qkv + s * kHd + i + kHd / 2, lay.n_qkv, rb, ep);
                         if (s >= nh) {
                             float* kr = a.kv + (cache0 + (s - nh)) * head_stride + (size_t)p * kHd;
                             kr[i] = ra;
                             kr[i + kHd / 2] = rb;
                         }
-                        pk_put(pk + lay.qkv + s * kHd + i, ra, ep);
-                        pk_put(pk + lay.qkv + s * kHd + i + kHd / 2, rb, ep);
                     } else {
+                        pk_put_all(pk + lay.qkv + s * kHd + i, lay.n_qkv, v0, ep);
+                        pk_put_all(pk + lay.qkv + s * kHd + i + kHd / 2, lay.n_qkv, v1, ep);
                         float* vr = a.kv + (cache0 + nkv + (s - nh - nkv)) * head_stride + (size_t)p * kHd;
                         vr[i] = v0;
                         vr[i + kHd / 2] = v1;
-                        pk_put(pk + lay.qkv + s * kHd + i, v0, ep);
-                        pk_put(pk + lay.qkv + s * kHd + i + kHd / 2, v1, ep);
                     }
                 }
             }
         });
-        if (dead) break;
-        mark();
+        if (phase_end()) break;
+        arrive(l * 5 + 0);
+        mark(mb + 2);
 
         // ---- attention: units (kv head g, chunk of 64 keys) ----------
-        for (int u = c; u < nkv * n_chunks && !dead; u += G) {
+        bool qkv_seen = false;
+        for (int u = c; u < nkv * n_chunks; u += G) {
             const int g = u / n_chunks, ch = u % n_chunks;
             const int j0 = ch * kAttCh, nj = min(kAttCh, p + 1 - j0);
-            SyncCompute::sync();  // the previous unit is done with `at`
-            const u64* qp = pk + lay.qkv + (size_t)g * group * kHd;
-            pk_gather<2>(rd, group * kHd, [&](int e) { return qp + e; },
-                         [&](int e, float v) { at.q[e / kHd][e % kHd] = v; });
+            const int nold = min(nj, p - j0);  // keys of earlier steps, read from the cache
             const float* kb = a.kv + (cache0 + g) * head_stride + (size_t)j0 * kHd;
             const float* vb = a.kv + (cache0 + nkv + g) * head_stride + (size_t)j0 * kHd;
-            const int nold = min(nj, p - j0);  // keys of earlier steps, read from the cache
             float4 kk[4], vv[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -349,6 +477,15 @@ __global__ void __maxnreg__(224) k_decode_persistent(PersistentArgs a) {
                     vv[k] = __ldcg(reinterpret_cast<const float4*>(vb + (size_t)j * kHd + d4));
                 }
             }
+            SyncCompute::sync();  // the previous unit is done with `at`
+            if (!qkv_seen) {
+                wait_cnt(l * 5 + 0);
+                qkv_seen = true;
+                mark(mb + 3);
+            }
+            const u64* qp = pk + lay.qkv + (size_t)rc * lay.n_qkv + (size_t)g * group * kHd;
+            pk_gather<2>(rd, group * kHd, [&](int e) { return qp + e; },
+                         [&](int e, float v) { at.q[e / kHd][e % kHd] = v; });
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int e = tid + 256 * k, j = e / (kHd / 4), d4 = (e % (kHd / 4)) * 4;
@@ -361,141 +498,195 @@ __global__ void __maxnreg__(224) k_decode_persistent(PersistentArgs a) {
                 }
             }
             if (nold < nj) {  // this step's key and value (position p): from the packets
-                const u64* kp = pk + lay.qkv + (size_t)(nh + g) * kHd;
-                const u64* vp = pk + lay.qkv + (size_t)(nh + nkv + g) * kHd;
+                const u64* kp = pk + lay.qkv + (size_t)rc * lay.n_qkv + (size_t)(nh + g) * kHd;
+                const u64* vp = pk + lay.qkv + (size_t)rc * lay.n_qkv + (size_t)(nh + nkv + g) * kHd;
                 pk_gather<1>(rd, 2 * kHd, [&](int e) { return e < kHd ? kp + e : vp + (e - kHd); },
                              [&](int e, float v) {
                                  if (e < kHd) at.k[nold][e] = v;
                                  else at.v[nold][e - kHd] = v;
                              });
             }
-            if (compute_any(rd.failed)) {
-                dead = true;
-                break;
-            }
+            SyncCompute::sync();
             attn_chunk<SyncCompute>(at, group, nj, [&](int h, int d, float acc, float m, float lsum) {
                 u64* pr = pk + lay.att + ((size_t)(g * group + h) * a.max_chunks + ch) * kPartStride;
-                pk_put(pr + 2 + d, acc, ep);
+                pk_put_all(pr + 2 + d, lay.n_att, acc, ep);
                 if (d == 0) {
-                    pk_put(pr, m, ep);
-                    pk_put(pr + 1, lsum, ep);
+                    pk_put_all(pr, lay.n_att, m, ep);
+                    pk_put_all(pr + 1, lay.n_att, lsum, ep);
                 }
             });
         }
-        if (dead) break;
-        SyncCompute::sync();
-        mark();
+        if (phase_end()) break;
+        arrive(l * 5 + 1);
+        mark(mb + 4);
 
         // ---- merge the chunks (every CTA), o_proj + residual -----------
         // Same arithmetic as attn_merge: M = max m_c, then in chunk order
         // w = e^(m_c - M), L = fma(w, l_c, L), O = fma(w, acc_c, O); o = O / L.
-        // The chunk maxima are gathered first, then (l, acc) a group of
-        // chunks at a time through shared memory.
         {
-            float* mst = act + H;                         // [nh][n_chunks]
-            float* gst = mst + nh * a.max_chunks;         // [nh][group][65]
-            const int gc_max = a.merge_group;
-            const u64* att = pk + lay.att;
-            pk_gather<4>(rd, nh * n_chunks,
-                         [&](int j) { return att + ((size_t)(j / n_chunks) * a.max_chunks + j % n_chunks) * kPartStride; },
-                         [&](int j, float v) { mst[j] = v; });
-            if (compute_any(rd.failed)) break;
+            const u64* att = pk + lay.att + (size_t)rc * lay.n_att;
+            float* stg = act + H;
+            const int whole = nh * n_chunks * kPartStride;
             float Mv[4], Lv[4], Ov[4];
+            wait_cnt(l * 5 + 1);
+            mark(mb + 5);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const int e = tid + 256 * k;
                 Mv[k] = -INFINITY;
                 Lv[k] = 0.f;
                 Ov[k] = 0.f;
-                if (e < nh * kHd)
-                    for (int cc = 0; cc < n_chunks; ++cc) Mv[k] = fmaxf(Mv[k], mst[(e / kHd) * n_chunks + cc]);
             }
-            for (int c0 = 0; c0 < n_chunks && !dead; c0 += gc_max) {
-                const int gc = min(gc_max, n_chunks - c0);
-                const int per_h = gc * (kHd + 1);
-                pk_gather<16>(rd, nh * per_h,
-                              [&](int j) {
-                                  const int h = j / per_h, r = j % per_h;
-                                  return att + ((size_t)h * a.max_chunks + c0 + r / (kHd + 1)) * kPartStride + 1 +
-                                         r % (kHd + 1);
-                              },
-                              [&](int j, float v) { gst[j] = v; });
-                if (compute_any(rd.failed)) {
-                    dead = true;
-                    break;
-                }
+            if (whole <= a.act_floats - H) {
+                // All partials in one gather: stg[h][c][66].
+                pk_gather<8>(rd, whole,
+                             [&](int j) {
+                                 const int h = j / (n_chunks * kPartStride), r = j % (n_chunks * kPartStride);
+                                 return att + (size_t)h * a.max_chunks * kPartStride + r;
+                             },
+                             [&](int j, float v) { stg[j] = v; });
+                SyncCompute::sync();
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int e = tid + 256 * k;
                     if (e < nh * kHd) {
                         const int h = e / kHd, d = e % kHd;
-                        for (int cc = 0; cc < gc; ++cc) {
-                            const float w = expf(mst[h * n_chunks + c0 + cc] - Mv[k]);
-                            const float* gp = gst + (size_t)(h * gc + cc) * (kHd + 1);
-                            Lv[k] = fmaf(w, gp[0], Lv[k]);
-                            Ov[k] = fmaf(w, gp[1 + d], Ov[k]);
+                        const float* ph = stg + (size_t)h * n_chunks * kPartStride;
+                        for (int cc = 0; cc < n_chunks; ++cc) Mv[k] = fmaxf(Mv[k], ph[cc * kPartStride]);
+                        for (int cc = 0; cc < n_chunks; ++cc) {
+                            const float w = expf(ph[cc * kPartStride] - Mv[k]);
+                            Lv[k] = fmaf(w, ph[cc * kPartStride + 1], Lv[k]);
+                            Ov[k] = fmaf(w, ph[cc * kPartStride + 2 + d], Ov[k]);
                         }
                     }
                 }
+            } else {
+                // Long context: chunk maxima first, then (l, acc) a group of
+                // chunks at a time.
+                float* mst = stg;                        // [nh][n_chunks]
+                float* gst = mst + nh * a.max_chunks;    // [nh][group][65]
+                const int gc_max = a.merge_group;
+                pk_gather<4>(rd, nh * n_chunks,
+                             [&](int j) {
+                                 return att + ((size_t)(j / n_chunks) * a.max_chunks + j % n_chunks) * kPartStride;
+                             },
+                             [&](int j, float v) { mst[j] = v; });
                 SyncCompute::sync();
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int e = tid + 256 * k;
+                    if (e < nh * kHd)
+                        for (int cc = 0; cc < n_chunks; ++cc) Mv[k] = fmaxf(Mv[k], mst[(e / kHd) * n_chunks + cc]);
+                }
+                for (int c0 = 0; c0 < n_chunks; c0 += gc_max) {
+                    const int gc = min(gc_max, n_chunks - c0);
+                    const int per_h = gc * (kHd + 1);
+                    pk_gather<8>(rd, nh * per_h,
+                                 [&](int j) {
+                                     const int h = j / per_h, r = j % per_h;
+                                     return att + ((size_t)h * a.max_chunks + c0 + r / (kHd + 1)) * kPartStride + 1 +
+                                            r % (kHd + 1);
+                                 },
+                                 [&](int j, float v) { gst[j] = v; });
+                    SyncCompute::sync();
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int e = tid + 256 * k;
+                        if (e < nh * kHd) {
+                            const int h = e / kHd, d = e % kHd;
+                            for (int cc = 0; cc < gc; ++cc) {
+                                const float w = expf(mst[h * n_chunks + c0 + cc] - Mv[k]);
+                                const float* gp = gst + (size_t)(h * gc + cc) * (kHd + 1);
+                                Lv[k] = fmaf(w, gp[0], Lv[k]);
+                                Ov[k] = fmaf(w, gp[1 + d], Ov[k]);
+                            }
+                        }
+                    }
+                    SyncCompute::sync();
+                }
             }
-            if (dead) break;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int e = tid + 256 * k;
                 if (e < nh * kHd) xs[e] = Ov[k] / Lv[k];
             }
-            SyncCompute::sync();
+            if (phase_end()) break;
         }
-        mark();
-        consume(2 * split(H / 2, c, G), 2 * split(H / 2, c + 1, G), rpc_h, [&](const __half* st, int r0, int n) {
-            for (int q = warp; q < n / 2; q += 8) {
-                const __half* rows[2] = {st + (size_t)(2 * q) * H, st + (size_t)(2 * q + 1) * H};
+        mark(mb + 6);
+        const int o_r0 = 2 * split(H / 2, c, G), o_r1 = 2 * split(H / 2, c + 1, G);
+        consume_all(o_r0, o_r1, rpc_h, H, [&](auto row_ptr) {
+            for (int q = warp; q < (o_r1 - o_r0) / 2; q += 8) {
+                const int r = o_r0 + 2 * q;
+                const __half* rows[2] = {row_ptr(r), row_ptr(r + 1)};
                 float acc[2][1];
-                warp_rows_dot<1, 2, LdShared>(rows, H, xs, H, acc);
+                warp_rows_dot<1, 2, LdShared, 4>(rows, H, xs, H, acc);
                 if (lane == 0) {
-                    const int r = r0 + 2 * q;
                     // xr still holds this layer's input x (gathered for Q/K/V).
-                    pk_put(pk + lay.x1 + r, xr[r] + acc[0][0], ep);
-                    pk_put(pk + lay.x1 + r + 1, xr[r + 1] + acc[1][0], ep);
+                    pk_put_all(pk + lay.x1 + r, lay.n_x, xr[r] + acc[0][0], ep);
+                    pk_put_all(pk + lay.x1 + r + 1, lay.n_x, xr[r + 1] + acc[1][0], ep);
                 }
             }
         });
-        if (dead) break;
-        mark();
+        load_norm(Lw.ffn_norm);
+        if (phase_end()) break;
+        arrive(l * 5 + 2);
+        mark(mb + 7);
 
         // ---- RMSNorm + gate/up + SiLU(gate) * up ----------------------
-        gather(pk + lay.x1, H, xr);
-        if (dead) break;
-        SyncCompute::sync();
-        norm_rows_to_smem<1, SyncCompute>(xr, 1, H, Lw.ffn_norm, a.eps, xs, H, red);
-        consume(2 * split(I, c, G), 2 * split(I, c + 1, G), rpc_h, [&](const __half* st, int r0, int n) {
-            for (int q = warp; q < n / 2; q += 8) {
-                const __half* rows[2] = {st + (size_t)(2 * q) * H, st + (size_t)(2 * q + 1) * H};
+        wait_cnt(l * 5 + 2);
+        mark(mb + 8);
+        gather(pk + lay.x1 + (size_t)rc * lay.n_x, H, xr);
+        if (phase_end()) break;
+        mark(mb + 9);
+        norm();
+        const int gu_r0 = 2 * split(I, c, G), gu_r1 = 2 * split(I, c + 1, G);
+        auto gu_rows = [&](auto row_ptr, int q0, int q1) {
+            for (int q = q0 + warp; q < q1; q += 8) {
+                const int r = gu_r0 + 2 * q;
+                const __half* rows[2] = {row_ptr(r), row_ptr(r + 1)};
                 float acc[2][1];
-                warp_rows_dot<1, 2, LdShared>(rows, H, xs, H, acc);
-                if (lane == 0) pk_put(pk + lay.m + (r0 >> 1) + q, silu_f(acc[0][0]) * acc[1][0], ep);
+                warp_rows_dot<1, 2, LdShared, 4>(rows, H, xs, H, acc);
+                if (lane == 0) pk_put_all(pk + lay.m + (r >> 1), lay.n_m, silu_f(acc[0][0]) * acc[1][0], ep);
             }
-        });
-        if (dead) break;
-        mark();
+        };
+        if ((gu_r1 - gu_r0 + rpc_h - 1) / rpc_h <= a.stages) {
+            consume_all(gu_r0, gu_r1, rpc_h, H, [&](auto row_ptr) { gu_rows(row_ptr, 0, (gu_r1 - gu_r0) / 2); });
+        } else {
+            consume(gu_r0, gu_r1, rpc_h, [&](const __half* st, int r0, int n) {
+                gu_rows([&](int r) { return st + (size_t)(r - r0) * H; }, (r0 - gu_r0) / 2, (r0 - gu_r0 + n) / 2);
+            });
+        }
+        if (phase_end()) break;
+        arrive(l * 5 + 3);
+        mark(mb + 10);
 
         // ---- down + residual ------------------------------------------
-        SyncCompute::sync();
-        gather(pk + lay.m, I, xs);
-        if (dead) break;
-        SyncCompute::sync();
-        consume(split(H, c, G), split(H, c + 1, G), rpc_i, [&](const __half* st, int r0, int n) {
-            for (int q = warp; q < n; q += 8) {
-                const __half* rows[1] = {st + (size_t)q * I};
+        wait_cnt(l * 5 + 3);
+        mark(mb + 11);
+        const u64* mp = pk + lay.m + (size_t)rc * lay.n_m;
+        pk_gather<20>(rd, I, [&](int j) { return mp + j; }, [&](int j, float v) { xs[j] = v; });
+        if (phase_end()) break;
+        mark(mb + 12);
+        const int d_r0 = split(H, c, G), d_r1 = split(H, c + 1, G);
+        auto down_rows = [&](auto row_ptr, int q0, int q1) {
+            for (int q = q0 + warp; q < q1; q += 8) {
+                const int r = d_r0 + q;
+                const __half* rows[1] = {row_ptr(r)};
                 float acc[1][1];
-                warp_rows_dot<1, 1, LdShared>(rows, I, xs, I, acc);
+                warp_rows_dot<1, 1, LdShared, 4>(rows, I, xs, I, acc);
                 // xr holds x after the attention add (gathered for gate/up).
-                if (lane == 0) pk_put(pk + lay.x2 + r0 + q, xr[r0 + q] + acc[0][0], ep);
+                if (lane == 0) pk_put_all(pk + lay.x2 + r, lay.n_x, xr[r] + acc[0][0], ep);
             }
-        });
-        if (dead) break;
-        mark();
+        };
+        if ((d_r1 - d_r0 + rpc_i - 1) / rpc_i <= a.stages) {
+            consume_all(d_r0, d_r1, rpc_i, I, [&](auto row_ptr) { down_rows(row_ptr, 0, d_r1 - d_r0); });
+        } else {
+            consume(d_r0, d_r1, rpc_i, [&](const __half* st, int r0, int n) {
+                down_rows([&](int r) { return st + (size_t)(r - r0) * I; }, r0 - d_r0, r0 - d_r0 + n);
+            });
+        }
+        if (phase_end()) break;
+        arrive(l * 5 + 4);
+        mark(mb + 13);
     }
 
     // ---- final RMSNorm + tied LM head + argmax --------------------------
@@ -504,12 +695,14 @@ __global__ void __maxnreg__(224) k_decode_persistent(PersistentArgs a) {
     float best_v = -INFINITY;
     int best_i = 0x7fffffff;
     if (!dead) {
-        SyncCompute::sync();
-        gather(a.pk + (size_t)(L - 1) * lay.per_layer + lay.x2, H, xr);
+        load_norm(a.final_norm);
+        wait_cnt((L - 1) * 5 + 4);
+        gather(a.pk + (size_t)(L - 1) * lay.per_layer + lay.x2 + (size_t)rc * lay.n_x, H, xr);
+        phase_end();
+        mark(1 + 16 * L);
     }
     if (!dead) {
-        SyncCompute::sync();
-        norm_rows_to_smem<1, SyncCompute>(xr, 1, H, a.final_norm, a.eps, xs, H, red);
+        norm();
         if (c == 0)
             for (int j = tid; j < H; j += kCompute) a.hidden[j] = xs[j];
         consume(split(V, c, G), split(V, c + 1, G), rpc_h, [&](const __half* st, int r0, int n) {
@@ -517,7 +710,7 @@ __global__ void __maxnreg__(224) k_decode_persistent(PersistentArgs a) {
                 const bool two = 2 * q + 1 < n;
                 const __half* rows[2] = {st + (size_t)(2 * q) * H, st + (size_t)(two ? 2 * q + 1 : 2 * q) * H};
                 float acc[2][1];
-                warp_rows_dot<1, 2, LdShared>(rows, H, xs, H, acc);
+                warp_rows_dot<1, 2, LdShared, 4>(rows, H, xs, H, acc);
                 if (lane == 0) {
                     const int r = r0 + 2 * q;
                     if (a.logits) {
@@ -529,9 +722,10 @@ __global__ void __maxnreg__(224) k_decode_persistent(PersistentArgs a) {
                 }
             }
         });
+        phase_end();
     }
     if (!dead) {
-        mark();
+        mark(2 + 16 * L);
         if (lane == 0) {
             wv_s[warp] = best_v;
             wi_s[warp] = best_i;
@@ -545,8 +739,10 @@ __global__ void __maxnreg__(224) k_decode_persistent(PersistentArgs a) {
             pk_put(am + 2 * c, v, ep);
             pk_put(am + 2 * c + 1, __int_as_float(i), ep);
         }
+        arrive(L * 5);
         if (c == 0) {
             // Stage 2: merge the per-CTA pairs; the id becomes the next token.
+            wait_cnt(L * 5);
             float v = -INFINITY;
             int i = 0x7fffffff;
             for (int k = tid; k < G; k += kCompute) {
@@ -580,7 +776,7 @@ __global__ void __maxnreg__(224) k_decode_persistent(PersistentArgs a) {
             }
             if (failed) dead = true;
         }
-        mark();
+        mark(3 + 16 * L);
     }
     if (dead) {
         *abort = 1;
@@ -598,7 +794,9 @@ cudaError_t persistent_setup(Ctx& c) {
     cudaDeviceGetAttribute(&dev_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, c.device);
     const int rows_h = (kPersistStage / (2 * H)) & ~1;
     const int rows_i = kPersistStage / (2 * I);
-    if (smem + 1024 > (size_t)dev_max || rows_h < 2 || rows_i < 1) {
+    const int max_qkv_rows = 2 * ((c.nqkv / 2 + c.n_sm - 1) / c.n_sm), max_o_rows = 2 * ((H / 2 + c.n_sm - 1) / c.n_sm);
+    if (smem + 1024 > (size_t)dev_max || rows_h < 2 || rows_i < 1 ||
+        max_qkv_rows > rows_h * kPersistStages || max_o_rows > rows_h * kPersistStages) {
         c.pers.why_not = "shared memory or stage size does not fit this shape";
         return cudaSuccess;
     }
@@ -648,6 +846,12 @@ cudaError_t persistent_setup(Ctx& c) {
     c.allocs.push_back(p);
     c.pers.pk = static_cast<unsigned long long*>(p);
     if ((e = cudaMemset(p, 0, n_pk * 8)) != cudaSuccess) return e;
+    c.pers.pk_bytes = n_pk * 8;
+    c.pers.cnt_bytes = (size_t)(g.n_layer * 5 + 1) * kCntStride * 8;
+    if ((e = cudaMalloc(&p, c.pers.cnt_bytes)) != cudaSuccess) return e;
+    c.allocs.push_back(p);
+    c.pers.cnt = static_cast<unsigned long long*>(p);
+    if ((e = cudaMemset(p, 0, c.pers.cnt_bytes)) != cudaSuccess) return e;
     if ((e = cudaMalloc(&p, 4)) != cudaSuccess) return e;
     c.allocs.push_back(p);
     c.pers.epoch = static_cast<unsigned*>(p);
@@ -662,6 +866,14 @@ cudaError_t persistent_setup(Ctx& c) {
     }
     c.pers.ok = true;
     return cudaSuccess;
+}
+
+cudaError_t persistent_reset(Ctx& c) {
+    if (!c.pers.ok) return cudaSuccess;
+    cudaError_t e = cudaMemset(c.pers.pk, 0, c.pers.pk_bytes);
+    if (e == cudaSuccess) e = cudaMemset(c.pers.cnt, 0, c.pers.cnt_bytes);
+    if (e == cudaSuccess) e = cudaMemset(c.pers.epoch, 0, 4);
+    return e;
 }
 
 cudaError_t enqueue_decode_persistent(Ctx& c, bool want_logits, cudaStream_t st) {
@@ -699,7 +911,12 @@ cudaError_t enqueue_decode_persistent(Ctx& c, bool want_logits, cudaStream_t st)
     a.max_seqs = c.cfg.max_seqs;
     a.merge_group = c.pers.merge_group;
     a.prof = c.pers.prof;
+    a.cnt = c.pers.cnt;
     a.prof_marks = c.pers.prof_marks;
+    if (c.pers.prof) {
+        cudaError_t e = cudaMemsetAsync(c.pers.prof, 0, (size_t)c.pers.grid * c.pers.prof_marks * 8, st);
+        if (e != cudaSuccess) return e;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(c.pers.grid);
     cfg.blockDim = dim3(kThreads);

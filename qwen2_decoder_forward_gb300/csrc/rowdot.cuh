@@ -50,10 +50,12 @@ __device__ __forceinline__ void warp_rows_dot(const __half* const (&rows)[R], in
             const int c = lane + 32 * (i0 + u);
             if (c < kc) {
 #pragma unroll
-                for (int r = 0; r < R; ++r)
+                for (int nb = 0; nb < NB; ++nb) {
+                    const float4 xa = *reinterpret_cast<const float4*>(xs + nb * ldx + c * 8);
+                    const float4 xb = *reinterpret_cast<const float4*>(xs + nb * ldx + c * 8 + 4);
 #pragma unroll
-                    for (int nb = 0; nb < NB; ++nb)
-                        acc[r][nb] = dot8_f16(wv[r][u], xs + nb * ldx + c * 8, acc[r][nb]);
+                    for (int r = 0; r < R; ++r) acc[r][nb] = dot8_f16_r(wv[r][u], xa, xb, acc[r][nb]);
+                }
             }
         }
     }

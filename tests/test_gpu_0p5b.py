@@ -41,6 +41,7 @@ def test_decode_batch1_prompt128_256_steps(q2, weights, orc):
     ref = orc.greedy_decode(cache, int(pre["ids"][0]), len(prompt), wl.decode_steps)
     with q2.Qwen2Model(SHAPE, weights, n_ctx=wl.n_ctx, max_seqs=1, max_tokens=len(prompt)) as m:
         assert m.weight_bytes >= 987_922_432
+        assert m.features & q2.FEATURE_PERSISTENT_DECODE, q2.lib().qwen2_last_error(m._h).decode()
         logits, ids = m.prefill([0], [prompt])
         check_logits_ids(logits.cpu().numpy(), ids.cpu().numpy(), pre["logits"], "prefill")
         check_hidden(m.final_hidden(1).cpu().numpy(), pre["final_norm_output"], "prefill")

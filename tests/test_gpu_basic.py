@@ -99,6 +99,8 @@ def test_variants_are_bit_identical(q2, flags, shape_name):
     outs = []
     for f in variants:
         with q2.Qwen2Model(shape, w, n_ctx=128, max_seqs=1, max_tokens=64, flags=f) as m:
+            if f == 0:
+                assert m.features & q2.FEATURE_PERSISTENT_DECODE, q2.lib().qwen2_last_error(m._h).decode()
             m.prefill([0], [prompt])
             rows = []
             tok = 5
