@@ -35,32 +35,22 @@ __device__ __forceinline__ float2 h2_to_f2(uint32_t v) {
     return __half22float2(h);
 }
 
-// acc += sum_{e<8} w[e] * x[e], with w eight f16 values packed in a uint4 and
-// x eight f32 values in shared or global memory (16-byte aligned).  The
-// products are added in element order; every kernel that dots a weight row
-// uses this one routine so that fused and unfused paths round alike.
-__device__ __forceinline__ float dot8_f16(uint4 w, const float* x, float acc) {
-    const float4 xa = *reinterpret_cast<const float4*>(x);
-    const float4 xb = *reinterpret_cast<const float4*>(x + 4);
+// Four-way split of a lane's partial dot product: products of elements
+// (0,1), (2,3), (4,5), (6,7) of every 8-element chunk go to a[0..3], each
+// in chunk order; dot4_total adds them as (a0 + a1) + (a2 + a3).  Four
+// independent chains keep the FMA pipes busy with few warps.  Every f16
+// GEMV kernel uses these, so all paths round alike.
+struct Acc4 {
+    float a[4];
+};
+__device__ __forceinline__ void dot8_f16_4(uint4 w, float4 xa, float4 xb, Acc4& acc) {
     float2 f;
-    f = h2_to_f2(w.x); acc = fmaf(f.x, xa.x, acc); acc = fmaf(f.y, xa.y, acc);
-    f = h2_to_f2(w.y); acc = fmaf(f.x, xa.z, acc); acc = fmaf(f.y, xa.w, acc);
-    f = h2_to_f2(w.z); acc = fmaf(f.x, xb.x, acc); acc = fmaf(f.y, xb.y, acc);
-    f = h2_to_f2(w.w); acc = fmaf(f.x, xb.z, acc); acc = fmaf(f.y, xb.w, acc);
-    return acc;
+    f = h2_to_f2(w.x); acc.a[0] = fmaf(f.x, xa.x, acc.a[0]); acc.a[0] = fmaf(f.y, xa.y, acc.a[0]);
+    f = h2_to_f2(w.y); acc.a[1] = fmaf(f.x, xa.z, acc.a[1]); acc.a[1] = fmaf(f.y, xa.w, acc.a[1]);
+    f = h2_to_f2(w.z); acc.a[2] = fmaf(f.x, xb.x, acc.a[2]); acc.a[2] = fmaf(f.y, xb.y, acc.a[2]);
+    f = h2_to_f2(w.w); acc.a[3] = fmaf(f.x, xb.z, acc.a[3]); acc.a[3] = fmaf(f.y, xb.w, acc.a[3]);
 }
-
-// The same sum as dot8_f16 with the eight activations already in registers
-// (xa = x[0..3], xb = x[4..7]), for kernels that share one load of x
-// between several weight rows.
-__device__ __forceinline__ float dot8_f16_r(uint4 w, float4 xa, float4 xb, float acc) {
-    float2 f;
-    f = h2_to_f2(w.x); acc = fmaf(f.x, xa.x, acc); acc = fmaf(f.y, xa.y, acc);
-    f = h2_to_f2(w.y); acc = fmaf(f.x, xa.z, acc); acc = fmaf(f.y, xa.w, acc);
-    f = h2_to_f2(w.z); acc = fmaf(f.x, xb.x, acc); acc = fmaf(f.y, xb.y, acc);
-    f = h2_to_f2(w.w); acc = fmaf(f.x, xb.z, acc); acc = fmaf(f.y, xb.w, acc);
-    return acc;
-}
+__device__ __forceinline__ float dot4_total(const Acc4& acc) { return (acc.a[0] + acc.a[1]) + (acc.a[2] + acc.a[3]); }
 
 // Sum over the 32 lanes by a fixed xor butterfly; lane 0's value is the one
 // every kernel uses.

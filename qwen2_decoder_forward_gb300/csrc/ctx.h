@@ -87,6 +87,7 @@ struct PersistLayer {
 // State of the persistent batch-1 decode kernel.
 struct PersistState {
     bool ok = false;                  // the kernel fits this shape and device
+    const void* kernel = nullptr;     // the instantiation for this shape
     int grid = 0;                     // one CTA per SM
     size_t smem = 0;                  // dynamic shared memory per CTA
     int rows_h = 0, rows_i = 0;       // weight rows per ring stage (K = H, K = I)

@@ -2,16 +2,19 @@
 //
 // One CTA per SM, all resident (cooperative launch).  Each CTA owns a fixed
 // slice of every weight matrix: the Q/K/V, o_proj and gate/up row pairs and
-// the down_proj and LM-head rows, split evenly over the CTAs.  A producer
-// warp streams the CTA's slices, in the order they are used, through a ring
-// of shared-memory stages with bulk (TMA) copies and mbarriers; the weights
-// do not depend on the activations, so the stream runs ahead of the compute
-// and never waits for a data dependency.  Eight compute warps run the steps
-// of the layer (minfer "Qwen2 / Qwen2.5 Architecture Support", section 1)
-// and exchange activation vectors through global "packets": 64-bit words
-// holding a float and the launch's epoch, written and read with single-copy
-// atomic 64-bit accesses, so a reader that sees the current epoch has the
-// value -- one L2 round trip per dependency, no grid barrier.
+// the down_proj and LM-head rows, split evenly over the CTAs.  The CTA's
+// slices stream, in the order they are used, through a ring of six 28 KB
+// shared-memory stages filled by bulk (TMA) copies with mbarriers, issued by
+// one lane of a feeding warpgroup, so the weight stream runs ahead of the
+// compute and never waits for activations.  The feeding warpgroup hands its
+// registers to the two compute warpgroups (setmaxnreg), which then need not
+// spill.  The compute warps run
+// the steps of the layer (minfer "Qwen2 / Qwen2.5 Architecture Support",
+// section 1) and exchange activation vectors through global "packets":
+// 64-bit words holding a float and the launch's epoch, written and read
+// with single-copy atomic 64-bit accesses, so a reader that sees the
+// current epoch has the value.  A per-phase arrival counter, polled by one
+// thread per CTA, tells a consumer when to read them.
 //
 // Per layer the dependencies are x -> Q/K/V (norm needs all of x), q/k/v ->
 // attention, attention partials -> o_proj (the chunk merge is recomputed by
@@ -19,8 +22,9 @@
 // is the per-step kernels' own (rowdot.cuh, attn.cuh), so the logits are
 // bit-identical to the multi-kernel path.
 //
-// Every wait is bounded: a wait that gives up raises kGuardTimeout, and the
-// CTA stops issuing copies, waits for the ones in flight and returns.
+// Every wait is bounded (2 s of the global timer): a wait that gives up
+// raises kGuardTimeout, and the CTA stops, waits for its copies in flight
+// and returns.
 #include "attn.cuh"
 #include "ctx.h"
 #include "persistent.h"
@@ -30,8 +34,12 @@ namespace qwen2 {
 
 namespace {
 
-constexpr int kCompute = 256;
-constexpr int kThreads = 288;             // 8 compute warps + 1 producer warp
+constexpr int kCompute = 256;            // warpgroups 0-1: the compute warps
+constexpr int kThreads = 384;            // + warpgroup 2, whose first lane feeds the weight ring
+// Register split (setmaxnreg): launched at 168 per thread (384 x 168 =
+// 64512); the feeding warpgroup drops to 40 and the compute warpgroups rise
+// to 232: 4 x 32 x 40 + 8 x 32 x 232 = 64512, the launch's own total.
+constexpr int kRegFeed = 40, kRegCompute = 232;
 constexpr unsigned long long kWaitNs = 2000000000ull;  // a wait gives up after 2 s
 
 typedef unsigned long long u64;
@@ -59,6 +67,17 @@ __device__ __forceinline__ bool mbar_try_wait(u64* b, unsigned parity) {
         : "memory");
     return ok != 0;
 }
+__device__ __forceinline__ bool mbar_test(u64* b, unsigned parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ void mbar_arrive(u64* b) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
 }
@@ -73,16 +92,7 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
 }
-// Bounded mbarrier wait; gives up after kWaitNs or when `abort` is set.
-__device__ __forceinline__ bool mbar_wait(u64* b, unsigned parity, volatile int* abort) {
-    if (mbar_try_wait(b, parity)) return true;
-    const u64 t0 = now_ns();
-    while (now_ns() - t0 < kWaitNs) {
-        if (mbar_try_wait(b, parity)) return true;
-        if (abort && *abort) return false;
-    }
-    return false;
-}
+
 
 // Named-barrier OR over the 256 compute threads.
 __device__ __forceinline__ bool compute_any(bool v) {
@@ -118,17 +128,6 @@ constexpr int kCntStride = 16;  // one 128-byte line per counter
 __device__ __forceinline__ void cnt_arrive(u64* cnt) {
     asm volatile("red.relaxed.gpu.global.add.u64 [%0], 1;" ::"l"(cnt) : "memory");
 }
-__device__ __forceinline__ bool cnt_wait(const u64* cnt, u64 target) {
-    u64 v = pk_raw(cnt);
-    if (v >= target) return true;
-    const u64 t0 = now_ns();
-    while (v < target) {
-        if (now_ns() - t0 > kWaitNs) return false;
-        __nanosleep(20);
-        v = pk_raw(cnt);
-    }
-    return true;
-}
 
 // Reader of packets of one epoch; after a failed wait it returns 0 at once
 // and the thread's `failed` flag stays set.
@@ -157,8 +156,8 @@ struct PkReader {
 // all polled again together, so a thread waits about one L2 round trip
 // after the last of its packets lands.  Threads of the 256-thread compute
 // group take elements tid, tid + 256, ...
-template <int KMAX, class Addr, class Store>
-__device__ __forceinline__ void pk_gather(PkReader& rd, int n, Addr addr, Store store) {
+template <int KMAX, class Addr, class Store, class Idle>
+__device__ __forceinline__ void pk_gather(PkReader& rd, int n, Addr addr, Store store, Idle idle) {
     const int tid = threadIdx.x;
     for (int j0 = 0; j0 < n; j0 += KMAX * 256) {
         u64 w[KMAX];
@@ -179,6 +178,7 @@ __device__ __forceinline__ void pk_gather(PkReader& rd, int n, Addr addr, Store 
         if (pending && !rd.failed) {
             const u64 t0 = now_ns();
             while (pending) {
+                idle();
                 __nanosleep(100);
 #pragma unroll
                 for (int k = 0; k < KMAX; ++k)
@@ -205,6 +205,7 @@ __device__ __forceinline__ void pk_gather(PkReader& rd, int n, Addr addr, Store 
 
 __device__ __forceinline__ int split(int n, int c, int G) { return (int)(((long long)n * c) / G); }
 
+
 }  // namespace
 
 // Packet buffer layout per layer (offsets in packets).  Every buffer is
@@ -228,20 +229,163 @@ struct PkLayout {
     }
 };
 
+// The weight stream of one CTA: its slices of every matrix, in the order the
+// compute uses them, cut into chunks of rows_h (K = H) or rows_i (K = I)
+// rows, one chunk per ring stage.  Thread 0 calls refill() whenever it is
+// about to wait; refill never blocks: it issues bulk copies into every stage
+// the compute has released, in order.
+struct Feeder {
+    const PersistentArgs* a;
+    unsigned char* ring;
+    u64* full;
+    u64* empty;
+    int c, G;
+    int l = 0, ph = 0, r = 0, r1 = 0;  // next chunk: layer (L: LM head), phase, row range
+    int issued = 0;
+    bool done = false;
+
+    __device__ __forceinline__ void range() {
+        const int H = a->H, I = a->I;
+        if (l == a->L) {
+            r = split(a->V, c, G);
+            r1 = split(a->V, c + 1, G);
+        } else if (ph == 0) {
+            r = 2 * split(a->nqkv / 2, c, G);
+            r1 = 2 * split(a->nqkv / 2, c + 1, G);
+        } else if (ph == 1) {
+            r = 2 * split(H / 2, c, G);
+            r1 = 2 * split(H / 2, c + 1, G);
+        } else if (ph == 2) {
+            r = 2 * split(I, c, G);
+            r1 = 2 * split(I, c + 1, G);
+        } else {
+            r = split(H, c, G);
+            r1 = split(H, c + 1, G);
+        }
+    }
+    __device__ __forceinline__ void init(const PersistentArgs* a_, unsigned char* ring_, u64* full_, u64* empty_,
+                                         int c_, int G_) {
+        a = a_;
+        ring = ring_;
+        full = full_;
+        empty = empty_;
+        c = c_;
+        G = G_;
+        range();
+    }
+    __device__ __forceinline__ void refill() {
+        while (!done) {
+            while (r >= r1) {  // next phase with rows
+                if (l == a->L) {
+                    done = true;
+                    return;
+                }
+                if (++ph == 4) {
+                    ph = 0;
+                    ++l;
+                }
+                range();
+            }
+            const int s = issued % a->stages;
+            const unsigned k = issued / a->stages;
+            if (k > 0 && !mbar_test(&empty[s], (k - 1) & 1)) return;
+            const bool down = l < a->L && ph == 3;
+            const int K = down ? a->I : a->H;
+            const int n = min(down ? a->rows_i : a->rows_h, r1 - r);
+            const __half* W = l == a->L ? a->E
+                              : ph == 0 ? a->layers[l].wqkv
+                              : ph == 1 ? a->layers[l].wo
+                              : ph == 2 ? a->layers[l].wgu
+                                        : a->layers[l].wd;
+            const unsigned bytes = (unsigned)n * K * 2;
+            mbar_expect_tx(&full[s], bytes);
+            bulk_g2s(ring + (size_t)s * kPersistStage, W + (size_t)r * K, bytes, &full[s]);
+            r += n;
+            ++issued;
+        }
+    }
+    // Feed the whole sequence, waiting (bounded) for each stage to be
+    // released; false if a wait gave up.
+    __device__ __forceinline__ bool run() {
+        while (!done) {
+            refill();
+            if (done) break;
+            const int s = issued % a->stages;
+            const unsigned k = issued / a->stages;
+            const u64 t0 = now_ns();
+            while (!mbar_test(&empty[s], (k - 1) & 1)) {
+                if (now_ns() - t0 > kWaitNs) return false;
+                __nanosleep(20);
+            }
+        }
+        return true;
+    }
+    // Before leaving early: wait (bounded) for the copies still in flight.
+    __device__ __forceinline__ void drain() {
+        for (int j = max(0, issued - a->stages); j < issued; ++j) {
+            const u64 t0 = now_ns();
+            while (!mbar_try_wait(&full[j % a->stages], (j / a->stages) & 1) && now_ns() - t0 < kWaitNs) {
+            }
+        }
+    }
+};
+
 // Write one value to all copies of a buffer (`stride` packets apart).
 __device__ __forceinline__ void pk_put_all(u64* p, int stride, float v, unsigned ep) {
 #pragma unroll
     for (int r = 0; r < kPkRep; ++r) pk_put(p + (size_t)r * stride, v, ep);
 }
 
+// Dot products of this warp's row pairs: rows (2w, 2w + 1) of each of the
+// consecutive ring stages from s0 that hold rows of a slice of nrows rows
+// (sixteen per stage).  Pair i's two sums go to res[2i], res[2i + 1] (lane
+// 0).  Compiled as a function of its own with K known: inside the large
+// kernel body the same loop ran several times slower.
+template <int K>
+__device__ __noinline__ void warp_stage_pairs(const unsigned char* ring, int s0, int stages, int nrows,
+                                              const float* xs, float* res) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int s = s0;
+    for (int i = 0; 16 * i + 2 * warp < nrows; ++i) {
+        const __half* st = reinterpret_cast<const __half*>(ring + (size_t)s * kPersistStage);
+        const bool two = 16 * i + 2 * warp + 1 < nrows;
+        const __half* rows[2] = {st + (size_t)(2 * warp) * K, st + (size_t)(two ? 2 * warp + 1 : 2 * warp) * K};
+        float acc[2][1];
+        warp_rows_dot<1, 2, LdShared, 4>(rows, K, xs, K, acc);
+        if (lane == 0) {
+            res[2 * i] = acc[0][0];
+            res[2 * i + 1] = acc[1][0];
+        }
+        s = s + 1 == stages ? 0 : s + 1;
+    }
+    __syncwarp();
+}
+
+// Dot products of this warp's rows q = w, w + 8, ... of a slice of nrows
+// rows of K stored rpc to a stage from s0; row k's sum goes to res[k].
+template <int K>
+__device__ __noinline__ void warp_stage_rows(const unsigned char* ring, int s0, int stages, int rpc, int nrows,
+                                             const float* xs, float* res) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int q = warp, k = 0; q < nrows; q += 8, ++k) {
+        const int j = q / rpc;
+        const int s = (s0 + j) % stages;
+        const __half* rows[1] = {reinterpret_cast<const __half*>(ring + (size_t)s * kPersistStage) +
+                                 (size_t)(q - j * rpc) * K};
+        float acc[1][1];
+        warp_rows_dot<1, 1, LdShared, 4>(rows, K, xs, K, acc);
+        if (lane == 0) res[k] = acc[0][0];
+    }
+    __syncwarp();
+}
+
+template <int HC, int IC>
 __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* ring = smem;
     u64* full = reinterpret_cast<u64*>(smem + a.stages * kPersistStage);
     u64* empty = full + a.stages;
     float* red = reinterpret_cast<float*>(empty + a.stages);
-    int* misc = reinterpret_cast<int*>(red + 8);  // [0] abort
-    volatile int* abort = misc;
     float* act = reinterpret_cast<float*>(smem + a.stages * kPersistStage + 256);
     float* xr = act + a.act_floats;  // raw x [H]
     AttnSmem& at = *reinterpret_cast<AttnSmem*>(act);
@@ -249,7 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x, G = gridDim.x;
-    const int H = a.H, I = a.I, V = a.V, L = a.L, nh = a.nh, nkv = a.nkv;
+    constexpr int H = HC, I = IC;
+    const int V = a.V, L = a.L, nh = a.nh, nkv = a.nkv;
     const int group = nh / nkv;
     const int np = a.nqkv / 2;
     const int rpc_h = a.rows_h, rpc_i = a.rows_i;
@@ -259,7 +404,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kCompute / 32);
         }
-        misc[0] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -273,41 +417,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
     const int n_chunks = (p + 1 + kAttCh - 1) / kAttCh;
     const PkLayout lay(a.nqkv, H, I, nh, a.max_chunks);
 
-    // ------------------------------------------------------------------
-    // Producer: one lane streams this CTA's weight slices into the ring.
-    // ------------------------------------------------------------------
-    if (warp == kCompute / 32) {
-        if (lane != 0) return;
-        int it = 0;
-        bool ok = true;
-        auto issue = [&](const __half* W, int K, int r0, int r1, int rpc) {
-            for (int r = r0; ok && r < r1; r += rpc) {
-                const int n = min(rpc, r1 - r);
-                const int s = it % a.stages;
-                const unsigned k = it / a.stages;
-                if (k > 0 && !mbar_wait(&empty[s], (k - 1) & 1, abort)) {
-                    ok = false;
-                    break;
-                }
-                const unsigned bytes = (unsigned)n * K * 2;
-                mbar_expect_tx(&full[s], bytes);
-                bulk_g2s(ring + (size_t)s * kPersistStage, W + (size_t)r * K, bytes, &full[s]);
-                ++it;
-            }
-        };
-        for (int l = 0; l < L && ok; ++l) {
-            const PersistLayer& Lw = a.layers[l];
-            issue(Lw.wqkv, H, 2 * split(np, c, G), 2 * split(np, c + 1, G), rpc_h);
-            issue(Lw.wo, H, 2 * split(H / 2, c, G), 2 * split(H / 2, c + 1, G), rpc_h);
-            issue(Lw.wgu, H, 2 * split(I, c, G), 2 * split(I, c + 1, G), rpc_h);
-            issue(Lw.wd, I, split(H, c, G), split(H, c + 1, G), rpc_i);
-        }
-        if (ok) issue(a.E, H, split(V, c, G), split(V, c + 1, G), rpc_h);
-        // Wait for every copy still in flight before leaving.
-        for (int j = max(0, it - a.stages); j < it; ++j) mbar_wait(&full[j % a.stages], (j / a.stages) & 1, nullptr);
-        if (!ok && c == 0) raise_guard(a.err, kGuardTimeout);
+    if (warp >= kCompute / 32) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegFeed));
+        if (tid != kCompute) return;
+        Feeder feed;
+        feed.init(&a, ring, full, empty, c, G);
+        if (!feed.run()) raise_guard(a.err, kGuardTimeout);
+        feed.drain();
         return;
     }
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegCompute));
 
     // ------------------------------------------------------------------
     // Compute warps.  Every load that does not depend on the incoming
@@ -326,40 +445,49 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
     // Consume this CTA's chunks of one matrix slice in order: fn(stage, row0, n).
     // A wait that gives up marks the thread bad; the phase end turns that
     // into a group-wide decision.
+    // Wait (bounded) for ring stage s to hold its chunk (parity par).
+    auto wait_full = [&](int s, unsigned par) -> bool {
+        if (mbar_try_wait(&full[s], par)) return true;
+        const u64 t0 = now_ns();
+        while (now_ns() - t0 < kWaitNs)
+            if (mbar_try_wait(&full[s], par)) return true;
+        return false;
+    };
+    auto idle = [&]() {};
     auto consume = [&](int r0, int r1, int rpc, auto&& fn) {
         for (int r = r0; r < r1; r += rpc) {
             const int n = min(rpc, r1 - r);
             const int s = it % a.stages;
             const unsigned k = it / a.stages;
-            if (!bad && !mbar_wait(&full[s], k & 1, abort)) bad = true;
+            if (!bad && !wait_full(s, k & 1)) bad = true;
             if (!bad) fn(reinterpret_cast<const __half*>(ring + (size_t)s * kPersistStage), r, n);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
             ++it;
+            idle();
         }
     };
     // Consume a whole slice at once when it fits in the ring: wait for all
-    // its stages, let fn spread its rows over the warps (row_ptr(r) is the
-    // shared-memory copy of row r), then release the stages.
-    auto consume_all = [&](int r0, int r1, int rpc, int K, auto&& fn) {
+    // its stages, run fn(stage of the slice's first chunk) -- the slice's
+    // chunks sit in consecutive stages, modulo the ring -- then release them.
+    auto consume_all = [&](int r0, int r1, int rpc, auto&& fn, int ready_mark = -1) {
         const int nch = (r1 - r0 + rpc - 1) / rpc;
         for (int j = 0; j < nch; ++j) {
             const int s = (it + j) % a.stages;
             const unsigned k = (it + j) / a.stages;
-            if (!bad && !mbar_wait(&full[s], k & 1, abort)) bad = true;
+            if (!bad && !wait_full(s, k & 1)) bad = true;
         }
+        if (ready_mark >= 0) mark(ready_mark);
         const int it0 = it;
-        if (!bad)
-            fn([&](int r) {
-                const int j = (r - r0) / rpc;
-                return reinterpret_cast<const __half*>(ring + (size_t)((it0 + j) % a.stages) * kPersistStage) +
-                       (size_t)((r - r0) % rpc) * K;
-            });
+        if (!bad) fn(it0 % a.stages);
         __syncwarp();
         if (lane == 0)
             for (int j = 0; j < nch; ++j) mbar_arrive(&empty[(it0 + j) % a.stages]);
         it += nch;
+        idle();
     };
+    __shared__ float res_s[8][16];  // per-warp dot results of the current phase
+    float* res = res_s[warp];
     auto phase_end = [&]() {
         dead = compute_any(bad || rd.failed);
         return dead;
@@ -369,11 +497,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
         if (tid == 0) cnt_arrive(a.cnt + (size_t)k * kCntStride);
     };
     auto wait_cnt = [&](int k) {
-        if (tid == 0 && !cnt_wait(a.cnt + (size_t)k * kCntStride, (u64)ep * (u64)G)) bad = true;
+        if (tid == 0) {
+            const u64* cp = a.cnt + (size_t)k * kCntStride;
+            const u64 target = (u64)ep * (u64)G;
+            if (pk_raw(cp) < target) {
+                const u64 t0 = now_ns();
+                while (pk_raw(cp) < target) {
+                    if (now_ns() - t0 > kWaitNs) {
+                        bad = true;
+                        break;
+                    }
+                    __nanosleep(20);
+                }
+            }
+        }
         SyncCompute::sync();
     };
     auto gather = [&](const u64* src, int n, float* dst) {
-        pk_gather<8>(rd, n, [&](int j) { return src + j; }, [&](int j, float v) { dst[j] = v; });
+        pk_gather<8>(rd, n, [&](int j) { return src + j; }, [&](int j, float v) { dst[j] = v; }, idle);
     };
     // Norm weights of the next normalisation, in registers (j = tid + 256 k).
     float nw[4];
@@ -395,8 +536,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
         SyncCompute::sync();
     };
 
-    __shared__ float pre_bias[64];
-    __shared__ float2 pre_rope[32];
     const size_t head_stride = (size_t)a.n_ctx * kHd;
     const int qkv_r0 = 2 * split(np, c, G), qkv_r1 = 2 * split(np, c + 1, G);
     const int rc = c % kPkRep;  // the packet copy this CTA reads
@@ -408,9 +547,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
 
         // ---- RMSNorm + Q/K/V + bias + RoPE + KV store -----------------
         load_norm(Lw.attn_norm);
-        for (int r = qkv_r0 + tid; r < qkv_r1 && r - qkv_r0 < 64; r += kCompute) {
-            pre_bias[r - qkv_r0] = Lw.bqkv[r];
-            if (((r - qkv_r0) & 1) == 0) pre_rope[(r - qkv_r0) >> 1] = a.rope[(size_t)p * (kHd / 2) + ((r % kHd) >> 1)];
+        // Bias and RoPE factors of this warp's first pair, loaded now so the
+        // epilogue does not wait for them.
+        float pb0 = 0.f, pb1 = 0.f;
+        float2 pcs = make_float2(1.f, 0.f);
+        if (lane == 0 && qkv_r0 + 2 * warp < qkv_r1) {
+            const int pr = qkv_r0 + 2 * warp;
+            pb0 = Lw.bqkv[pr];
+            pb1 = Lw.bqkv[pr + 1];
+            pcs = a.rope[(size_t)p * (kHd / 2) + ((pr % kHd) >> 1)];
         }
         if (l == 0) {
             for (int j = tid; j < H; j += kCompute) xr[j] = __half2float(a.E[(size_t)t * H + j]);
@@ -423,20 +568,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
         mark(mb + 0);
         norm();
         mark(mb + 1);
-        consume_all(qkv_r0, qkv_r1, rpc_h, H, [&](auto row_ptr) {
-            for (int q = warp; q < (qkv_r1 - qkv_r0) / 2; q += 8) {
+        // Sixteen rows per stage, one row pair per warp: warp w takes rows
+        // 2w, 2w + 1 of each stage of its slice.
+        consume_all(qkv_r0, qkv_r1, rpc_h, [&](int s0) {
+            warp_stage_pairs<H>(ring, s0, a.stages, qkv_r1 - qkv_r0, xs, res);
+            for (int q = warp, i = 0; 2 * q < qkv_r1 - qkv_r0; q += 8, ++i) {
                 const int pr = qkv_r0 + 2 * q;  // packed row of the pair
-                const __half* rows[2] = {row_ptr(pr), row_ptr(pr + 1)};
-                float acc[2][1];
-                warp_rows_dot<1, 2, LdShared, 4>(rows, H, xs, H, acc);
+                const float acc[2][1] = {{res[2 * i]}, {res[2 * i + 1]}};
                 if (lane == 0) {
                     const int s = pr / kHd, i = (pr % kHd) >> 1;
-                    const int lr = pr - qkv_r0;
-                    const float b0 = lr < 64 ? pre_bias[lr] : Lw.bqkv[pr];
-                    const float b1 = lr < 64 ? pre_bias[lr + 1] : Lw.bqkv[pr + 1];
+                    const bool first = q == warp;
+                    const float b0 = first ? pb0 : Lw.bqkv[pr];
+                    const float b1 = first ? pb1 : Lw.bqkv[pr + 1];
                     const float v0 = acc[0][0] + b0, v1 = acc[1][0] + b1;
                     if (s < nh + nkv) {
-                        const float2 cs = lr < 64 ? pre_rope[lr >> 1] : a.rope[(size_t)p * (kHd / 2) + i];
+                        const float2 cs = first ? pcs : a.rope[(size_t)p * (kHd / 2) + i];
                         float ra, rb;
                         rope_pair(v0, v1, cs, ra, rb);
                         pk_put_all(pk + lay.qkv + s * kHd + i, lay.n_qkv, ra, ep);
@@ -485,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
             }
             const u64* qp = pk + lay.qkv + (size_t)rc * lay.n_qkv + (size_t)g * group * kHd;
             pk_gather<2>(rd, group * kHd, [&](int e) { return qp + e; },
-                         [&](int e, float v) { at.q[e / kHd][e % kHd] = v; });
+                         [&](int e, float v) { at.q[e / kHd][e % kHd] = v; }, idle);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int e = tid + 256 * k, j = e / (kHd / 4), d4 = (e % (kHd / 4)) * 4;
@@ -504,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
                              [&](int e, float v) {
                                  if (e < kHd) at.k[nold][e] = v;
                                  else at.v[nold][e - kHd] = v;
-                             });
+                             }, idle);
             }
             SyncCompute::sync();
             attn_chunk<SyncCompute>(at, group, nj, [&](int h, int d, float acc, float m, float lsum) {
@@ -543,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
                                  const int h = j / (n_chunks * kPartStride), r = j % (n_chunks * kPartStride);
                                  return att + (size_t)h * a.max_chunks * kPartStride + r;
                              },
-                             [&](int j, float v) { stg[j] = v; });
+                             [&](int j, float v) { stg[j] = v; }, idle);
                 SyncCompute::sync();
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
@@ -569,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
                              [&](int j) {
                                  return att + ((size_t)(j / n_chunks) * a.max_chunks + j % n_chunks) * kPartStride;
                              },
-                             [&](int j, float v) { mst[j] = v; });
+                             [&](int j, float v) { mst[j] = v; }, idle);
                 SyncCompute::sync();
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
@@ -586,7 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
                                      return att + ((size_t)h * a.max_chunks + c0 + r / (kHd + 1)) * kPartStride + 1 +
                                             r % (kHd + 1);
                                  },
-                                 [&](int j, float v) { gst[j] = v; });
+                                 [&](int j, float v) { gst[j] = v; }, idle);
                     SyncCompute::sync();
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
@@ -613,12 +759,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
         }
         mark(mb + 6);
         const int o_r0 = 2 * split(H / 2, c, G), o_r1 = 2 * split(H / 2, c + 1, G);
-        consume_all(o_r0, o_r1, rpc_h, H, [&](auto row_ptr) {
-            for (int q = warp; q < (o_r1 - o_r0) / 2; q += 8) {
+        consume_all(o_r0, o_r1, rpc_h, [&](int s0) {
+            warp_stage_pairs<H>(ring, s0, a.stages, o_r1 - o_r0, xs, res);
+            for (int q = warp, i = 0; 2 * q < o_r1 - o_r0; q += 8, ++i) {
                 const int r = o_r0 + 2 * q;
-                const __half* rows[2] = {row_ptr(r), row_ptr(r + 1)};
-                float acc[2][1];
-                warp_rows_dot<1, 2, LdShared, 4>(rows, H, xs, H, acc);
+                const float acc[2][1] = {{res[2 * i]}, {res[2 * i + 1]}};
                 if (lane == 0) {
                     // xr still holds this layer's input x (gathered for Q/K/V).
                     pk_put_all(pk + lay.x1 + r, lay.n_x, xr[r] + acc[0][0], ep);
@@ -639,20 +784,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
         mark(mb + 9);
         norm();
         const int gu_r0 = 2 * split(I, c, G), gu_r1 = 2 * split(I, c + 1, G);
-        auto gu_rows = [&](auto row_ptr, int q0, int q1) {
-            for (int q = q0 + warp; q < q1; q += 8) {
-                const int r = gu_r0 + 2 * q;
-                const __half* rows[2] = {row_ptr(r), row_ptr(r + 1)};
-                float acc[2][1];
-                warp_rows_dot<1, 2, LdShared, 4>(rows, H, xs, H, acc);
-                if (lane == 0) pk_put_all(pk + lay.m + (r >> 1), lay.n_m, silu_f(acc[0][0]) * acc[1][0], ep);
-            }
+        // Pair (gate j, up j) in rows 2j, 2j + 1 of the stage; one per warp.
+        // Pair (gate j, up j) in rows 2j, 2j + 1; one pair per warp per stage.
+        auto gu_out = [&](int r0, int n) {
+            for (int q = warp, i = 0; 2 * q < n; q += 8, ++i)
+                if (lane == 0) pk_put_all(pk + lay.m + ((r0 + 2 * q) >> 1), lay.n_m, silu_f(res[2 * i]) * res[2 * i + 1], ep);
         };
         if ((gu_r1 - gu_r0 + rpc_h - 1) / rpc_h <= a.stages) {
-            consume_all(gu_r0, gu_r1, rpc_h, H, [&](auto row_ptr) { gu_rows(row_ptr, 0, (gu_r1 - gu_r0) / 2); });
+            consume_all(gu_r0, gu_r1, rpc_h, [&](int s0) {
+                warp_stage_pairs<H>(ring, s0, a.stages, gu_r1 - gu_r0, xs, res);
+                gu_out(gu_r0, gu_r1 - gu_r0);
+            }, mb + 14);
         } else {
             consume(gu_r0, gu_r1, rpc_h, [&](const __half* st, int r0, int n) {
-                gu_rows([&](int r) { return st + (size_t)(r - r0) * H; }, (r0 - gu_r0) / 2, (r0 - gu_r0 + n) / 2);
+                warp_stage_pairs<H>(reinterpret_cast<const unsigned char*>(st), 0, 1, n, xs, res);
+                gu_out(r0, n);
             });
         }
         if (phase_end()) break;
@@ -663,25 +809,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
         wait_cnt(l * 5 + 3);
         mark(mb + 11);
         const u64* mp = pk + lay.m + (size_t)rc * lay.n_m;
-        pk_gather<20>(rd, I, [&](int j) { return mp + j; }, [&](int j, float v) { xs[j] = v; });
+        pk_gather<20>(rd, I, [&](int j) { return mp + j; }, [&](int j, float v) { xs[j] = v; }, idle);
         if (phase_end()) break;
         mark(mb + 12);
         const int d_r0 = split(H, c, G), d_r1 = split(H, c + 1, G);
-        auto down_rows = [&](auto row_ptr, int q0, int q1) {
-            for (int q = q0 + warp; q < q1; q += 8) {
-                const int r = d_r0 + q;
-                const __half* rows[1] = {row_ptr(r)};
-                float acc[1][1];
-                warp_rows_dot<1, 1, LdShared, 4>(rows, I, xs, I, acc);
-                // xr holds x after the attention add (gathered for gate/up).
-                if (lane == 0) pk_put_all(pk + lay.x2 + r, lay.n_x, xr[r] + acc[0][0], ep);
-            }
+        // xr holds x after the attention add (gathered for gate/up).
+        auto down_out = [&](int r0, int n) {
+            for (int q = warp, k = 0; q < n; q += 8, ++k)
+                if (lane == 0) pk_put_all(pk + lay.x2 + r0 + q, lay.n_x, xr[r0 + q] + res[k], ep);
         };
         if ((d_r1 - d_r0 + rpc_i - 1) / rpc_i <= a.stages) {
-            consume_all(d_r0, d_r1, rpc_i, I, [&](auto row_ptr) { down_rows(row_ptr, 0, d_r1 - d_r0); });
+            consume_all(d_r0, d_r1, rpc_i, [&](int s0) {
+                warp_stage_rows<I>(ring, s0, a.stages, rpc_i, d_r1 - d_r0, xs, res);
+                down_out(d_r0, d_r1 - d_r0);
+            }, mb + 15);
         } else {
             consume(d_r0, d_r1, rpc_i, [&](const __half* st, int r0, int n) {
-                down_rows([&](int r) { return st + (size_t)(r - r0) * I; }, r0 - d_r0, r0 - d_r0 + n);
+                warp_stage_rows<I>(reinterpret_cast<const unsigned char*>(st), 0, 1, rpc_i, n, xs, res);
+                down_out(r0, n);
             });
         }
         if (phase_end()) break;
@@ -706,11 +851,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
         if (c == 0)
             for (int j = tid; j < H; j += kCompute) a.hidden[j] = xs[j];
         consume(split(V, c, G), split(V, c + 1, G), rpc_h, [&](const __half* st, int r0, int n) {
-            for (int q = warp; 2 * q < n; q += 8) {
+            warp_stage_pairs<H>(reinterpret_cast<const unsigned char*>(st), 0, 1, n, xs, res);
+            for (int q = warp, i = 0; 2 * q < n; q += 8, ++i) {
                 const bool two = 2 * q + 1 < n;
-                const __half* rows[2] = {st + (size_t)(2 * q) * H, st + (size_t)(two ? 2 * q + 1 : 2 * q) * H};
-                float acc[2][1];
-                warp_rows_dot<1, 2, LdShared, 4>(rows, H, xs, H, acc);
+                const float acc[2][1] = {{res[2 * i]}, {res[2 * i + 1]}};
                 if (lane == 0) {
                     const int r = r0 + 2 * q;
                     if (a.logits) {
@@ -778,11 +922,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
         }
         mark(3 + 16 * L);
     }
-    if (dead) {
-        *abort = 1;
-        if (tid == 0) raise_guard(a.err, kGuardTimeout);
-    }
+    if (dead && tid == 0) raise_guard(a.err, kGuardTimeout);
 }
+
+namespace {
+// The shapes the persistent kernel is instantiated for (hidden, intermediate).
+typedef void (*PersistKernel)(PersistentArgs);
+PersistKernel pick_kernel(int H, int I) {
+    if (H == 896 && I == 4864) return k_decode_persistent<896, 4864>;  // Qwen2.5-0.5B
+    if (H == 256 && I == 1024) return k_decode_persistent<256, 1024>;
+    if (H == 384 && I == 640) return k_decode_persistent<384, 640>;
+    return nullptr;
+}
+}  // namespace
 
 cudaError_t persistent_setup(Ctx& c) {
     const qwen2_config& g = c.cfg;
@@ -792,7 +944,8 @@ cudaError_t persistent_setup(Ctx& c) {
     const size_t smem = (size_t)kPersistStages * kPersistStage + 256 + act + (size_t)H * 4;
     int dev_max = 0;
     cudaDeviceGetAttribute(&dev_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, c.device);
-    const int rows_h = (kPersistStage / (2 * H)) & ~1;
+    // Sixteen rows of K = H per stage (one row pair per compute warp).
+    const int rows_h = 2 * H * 16 <= kPersistStage ? 16 : 0;
     const int rows_i = kPersistStage / (2 * I);
     const int max_qkv_rows = 2 * ((c.nqkv / 2 + c.n_sm - 1) / c.n_sm), max_o_rows = 2 * ((H / 2 + c.n_sm - 1) / c.n_sm);
     if (smem + 1024 > (size_t)dev_max || rows_h < 2 || rows_i < 1 ||
@@ -800,10 +953,16 @@ cudaError_t persistent_setup(Ctx& c) {
         c.pers.why_not = "shared memory or stage size does not fit this shape";
         return cudaSuccess;
     }
-    cudaError_t e = cudaFuncSetAttribute(k_decode_persistent, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const PersistKernel kern = pick_kernel(H, I);
+    if (!kern) {
+        c.pers.why_not = "no persistent kernel instantiated for hidden " + std::to_string(H) + ", intermediate " +
+                         std::to_string(I);
+        return cudaSuccess;
+    }
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_decode_persistent, kThreads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) {
         c.pers.why_not = "occupancy query gives 0 blocks per SM";
@@ -816,6 +975,7 @@ cudaError_t persistent_setup(Ctx& c) {
         return cudaSuccess;
     }
     c.pers.grid = c.n_sm;
+    c.pers.kernel = reinterpret_cast<const void*>(kern);
     c.pers.smem = smem;
     c.pers.rows_h = rows_h;
     c.pers.rows_i = rows_i;
@@ -927,7 +1087,7 @@ cudaError_t enqueue_decode_persistent(Ctx& c, bool want_logits, cudaStream_t st)
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_decode_persistent, a);
+    return cudaLaunchKernelEx(&cfg, reinterpret_cast<PersistKernel>(c.pers.kernel), a);
 }
 
 }  // namespace qwen2

@@ -1,13 +1,15 @@
 // The canonical weight-row dot product every f16 GEMV kernel of libqwen2 uses.
 //
 // A row of K f16 weights is read as K/8 chunks of 16 bytes; lane l of the
-// warp takes chunks l, l+32, l+64, ... in that order, adds each chunk's eight
-// products into its own f32 partial (dot8_f16, element order), and the 32
-// partials are summed by the xor butterfly of warp_sum (lane 0's value).
-// Because the lane assignment depends on the row alone, a row's result does
-// not depend on which rows share the warp, on the number of activation
-// vectors, or on which kernel computes it: fused and unfused paths, batch 1
-// and batch B, all round alike.
+// warp takes chunks l, l+32, l+64, ... in that order and adds each chunk's
+// eight products into four partial sums by element pair (dot8_f16_4); the
+// lane's total (a0 + a1) + (a2 + a3) is then summed over the 32 lanes by
+// the xor butterfly of warp_sum (lane 0's value).  Because the lane
+// assignment depends on the row alone, a row's result does not depend on
+// which rows share the warp, on the number of activation vectors, on where
+// the weights are read from, or on which kernel computes it: fused and
+// unfused paths, per-step and persistent kernels, batch 1 and batch B, all
+// round alike.
 #pragma once
 
 #include "common.cuh"
@@ -24,7 +26,8 @@ struct LdShared {
 };
 
 // Dot products of R weight rows with NB activation vectors held in shared
-// memory (xs + nb*ldx, 16-byte aligned, K floats each).  Loads of all R rows
+// memory (xs + nb*ldx, 16-byte aligned, K floats each; xs must point into
+// shared memory).  Loads of all R rows
 // are issued together, U chunks per lane per row at a time.  acc[r][nb] is
 // valid in lane 0.
 template <int NB, int R, class Ld = LdGlobal, int U = 8>
@@ -32,10 +35,13 @@ __device__ __forceinline__ void warp_rows_dot(const __half* const (&rows)[R], in
                                               const float* xs, int ldx, float (&acc)[R][NB]) {
     const int lane = threadIdx.x & 31;
     const int kc = K >> 3;
+    Acc4 part[R][NB];
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) acc[r][nb] = 0.f;
+        for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) part[r][nb].a[e] = 0.f;
     for (int i0 = 0; i0 * 32 < kc; i0 += U) {
         uint4 wv[R][U];
 #pragma unroll
@@ -54,7 +60,7 @@ __device__ __forceinline__ void warp_rows_dot(const __half* const (&rows)[R], in
                     const float4 xa = *reinterpret_cast<const float4*>(xs + nb * ldx + c * 8);
                     const float4 xb = *reinterpret_cast<const float4*>(xs + nb * ldx + c * 8 + 4);
 #pragma unroll
-                    for (int r = 0; r < R; ++r) acc[r][nb] = dot8_f16_r(wv[r][u], xa, xb, acc[r][nb]);
+                    for (int r = 0; r < R; ++r) dot8_f16_4(wv[r][u], xa, xb, part[r][nb]);
                 }
             }
         }
@@ -62,7 +68,7 @@ __device__ __forceinline__ void warp_rows_dot(const __half* const (&rows)[R], in
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) acc[r][nb] = warp_sum(acc[r][nb]);
+        for (int nb = 0; nb < NB; ++nb) acc[r][nb] = warp_sum(dot4_total(part[r][nb]));
 }
 
 // RMSNorm of NB rows into shared memory: xs[b][j] = (x[b][j] * s_b) * w[j]
