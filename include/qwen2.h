@@ -224,6 +224,32 @@ int qwen2_profile_marks(qwen2_ctx *ctx, int64_t *out, int64_t max_marks, int32_t
  * head_dim * 4 (24 KB per position on Qwen2.5-0.5B, minfer page section 6). */
 int64_t qwen2_kv_bytes_per_seq(const qwen2_config *cfg);
 
+/* Tied LM head and greedy argmax on already-normalised rows, with no device
+ * allocation and no context.  Not an operation of its own in the Qwen2
+ * description: it is the decode step's last stage (logits = E . h with the
+ * embedding matrix E as the output projection, then the greedy id) offered
+ * for callers that own every byte of device memory through their own
+ * allocator and cannot let a library call cudaMalloc or hold a context.
+ *   embed:  device, f16 bits [vocab][hidden_size], row-major (E itself).
+ *   hidden: device, f32 [n_rows][hidden_size], the final RMSNorm output.
+ *   logits: device, f32 [n_rows][vocab], or NULL to skip writing logits.
+ *   ids:    device, int32 [n_rows]: the lowest index of each row's maximum.
+ * Asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
+ * Limits: 1 <= n_rows <= 8; hidden_size a multiple of 8, at most 1024;
+ * vocab >= 1.  Outside them: QWEN2_E_ARG, nothing launched.
+ * Scratch: a fixed static device array of the library (about 32 KB per
+ * device).  The first call on a device looks up its address with that
+ * device current; make that first call before any other use that must not
+ * see a runtime call other than a kernel launch and a memset.  Each call
+ * zeroes the scratch's arrival counter on `stream` before its kernel.  Two
+ * calls in flight at once on one device (other streams or threads) share
+ * the scratch and race: order them.  The logits are bitwise those of
+ * qwen2_decode_step for the same rows.  Errors: QWEN2_E_ARG, QWEN2_E_CUDA;
+ * qwen2_last_error(NULL) describes the failure. */
+int qwen2_lm_head_argmax_noalloc(const uint16_t *embed, const float *hidden, int32_t n_rows,
+                                 int32_t hidden_size, int32_t vocab, float *logits, int32_t *ids,
+                                 void *stream);
+
 /* Host-only Q8_0 quantisation of an f16 matrix [rows][k] (k a multiple of
  * 32), as the library's packer does it: blocks of 32 along k;
  * d = max|x| / 127 in f32; q = clamp(round-half-away(x / d), -127, 127)

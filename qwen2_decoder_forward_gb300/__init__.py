@@ -46,6 +46,7 @@ EXPORTS = (
     "qwen2_prefill", "qwen2_decode_step", "qwen2_decode_steps",
     "qwen2_final_hidden", "qwen2_synchronize", "qwen2_weight_bytes",
     "qwen2_kv_bytes_per_seq", "qwen2_quantize_q8_0", "qwen2_features", "qwen2_profile_marks",
+    "qwen2_lm_head_argmax_noalloc",
 )
 
 
@@ -121,6 +122,8 @@ def lib() -> ctypes.CDLL:
     L.qwen2_features.restype = ctypes.c_uint32
     L.qwen2_profile_marks.argtypes = [_P, _P, i64, pi32, pi32]
     L.qwen2_profile_marks.restype = ctypes.c_int
+    L.qwen2_lm_head_argmax_noalloc.argtypes = [_P, _P, i32, i32, i32, _P, _P, _P]
+    L.qwen2_lm_head_argmax_noalloc.restype = ctypes.c_int
     _lib = L
     return L
 
@@ -150,6 +153,31 @@ def quantize_q8_0(w: np.ndarray):
     if rc:
         raise Qwen2Error(rc, "qwen2_quantize_q8_0 rejected its arguments")
     return q, d.view(np.float16)
+
+
+def lm_head_argmax_noalloc(embed, hidden, logits=None, ids=None, want_logits: bool = True, stream=None):
+    """Tied LM head + greedy argmax on normalised rows through
+    qwen2_lm_head_argmax_noalloc (no context, no device allocation by the
+    library).  embed: CUDA f16 [V, H]; hidden: CUDA f32 [rows, H].  Output
+    tensors are allocated here by torch unless passed in.  Returns
+    (logits f32 [rows, V] or None, ids int32 [rows])."""
+    import torch
+    if embed.dtype != torch.float16 or hidden.dtype != torch.float32 or not (embed.is_cuda and hidden.is_cuda):
+        raise ValueError("embed must be CUDA f16 and hidden CUDA f32")
+    rows, h = hidden.shape
+    v = embed.shape[0]
+    if embed.shape[1] != h:
+        raise ValueError("embed and hidden disagree on the hidden size")
+    if want_logits and logits is None:
+        logits = torch.empty((rows, v), dtype=torch.float32, device=hidden.device)
+    if ids is None:
+        ids = torch.empty((rows,), dtype=torch.int32, device=hidden.device)
+    rc = lib().qwen2_lm_head_argmax_noalloc(_data_ptr(embed), _data_ptr(hidden), rows, h, v,
+                                            _data_ptr(logits if want_logits else None), _data_ptr(ids),
+                                            _stream_ptr(stream))
+    if rc:
+        raise Qwen2Error(rc, lib().qwen2_last_error(None).decode())
+    return (logits if want_logits else None), ids
 
 
 def kv_bytes_per_seq(shape, n_ctx: int) -> int:

@@ -33,6 +33,13 @@ int cuda_fail(Ctx* c, cudaError_t e, const char* what) {
     return fail(c, QWEN2_E_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
 }
 
+}  // namespace
+
+// Message of a failed call that has no context (qwen2_last_error(NULL)).
+void qwen2::set_thread_error(const std::string& msg) { g_create_error = msg; }
+
+namespace {
+
 #define Q2_CHECK(c, call)                                  \
     do {                                                   \
         cudaError_t e_ = (call);                           \

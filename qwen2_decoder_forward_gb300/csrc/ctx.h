@@ -146,4 +146,8 @@ int pack_weights(Ctx& c, const qwen2_weights* w, std::string& err);
 void quantize_q8_0_host(const uint16_t* w, int64_t rows, int64_t k, int8_t* q, uint16_t* d);
 int build_rope_table(Ctx& c, std::string& err);
 
+// Records the message of a failed call made without a context; read back
+// with qwen2_last_error(NULL).
+void set_thread_error(const std::string& msg);
+
 }  // namespace qwen2

@@ -96,3 +96,13 @@ def test_q8_0_packer_rejects_ragged_k(L):
     q = np.empty((2, 48), dtype=np.int8)
     d = np.empty((2, 2), dtype=np.uint16)
     assert L.qwen2_quantize_q8_0(w.ctypes.data, 2, 48, q.ctypes.data, d.ctypes.data) == q2.QWEN2_E_ARG
+
+
+def test_no_alloc_head_rejects_bad_sizes_before_any_cuda_call(L):
+    # Non-null dummy pointers: argument checks come before any CUDA call.
+    fake = ctypes.c_void_p(16)
+    assert L.qwen2_lm_head_argmax_noalloc(fake, fake, 9, 896, 151936, None, fake, None) == 1
+    assert b"n_rows" in L.qwen2_last_error(None)
+    assert L.qwen2_lm_head_argmax_noalloc(fake, fake, 1, 1032, 151936, None, fake, None) == 1
+    assert b"hidden_size" in L.qwen2_last_error(None)
+    assert L.qwen2_lm_head_argmax_noalloc(fake, fake, 1, 896, 151936, None, None, None) == 1
