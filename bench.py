@@ -111,6 +111,25 @@ def decode_bytes_per_token(shape, positions) -> float:
     return float(np.mean(w + small + kv_pos * (p + 2)))
 
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum, mean
+# of 3 launches at positions ~150) from one ncu capture of the persistent
+# decode kernel, valid only while the kernel's sources hash to `src`.
+TRAFFIC = {"k_decode_persistent": {"src": "d4268477ed2a556d", "bytes": 1001816235.0}}
+KERNEL_SOURCES = ("persistent.cu", "persistent.h", "rowdot.cuh", "common.cuh", "attn.cuh", "ctx.h")
+
+
+def kernel_traffic(name: str):
+    import hashlib
+    rec = TRAFFIC.get(name)
+    if rec is None:
+        return None
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "qwen2_decoder_forward_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return rec["bytes"] if h.hexdigest()[:16] == rec["src"] else None
+
+
 def cpu_threads() -> int:
     try:
         from threadpoolctl import threadpool_info
@@ -254,7 +273,8 @@ def main():
     per_token_s = (ms / 1e3) / (args.steps * n_steps)
     achieved = bytes_tok / per_token_s / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                "traffic": None, "kernel": "one decode token: " + (
+                "traffic": kernel_traffic("k_decode_persistent") if persistent else None,
+                "kernel": "one decode token: " + (
                     "k_decode_persistent (one launch per token)" if persistent else "all kernels of the step graph"),
                 "peak_source": src, "bytes_per_launch": bytes_tok}
     launches_per_token = 1 if persistent else 2 + shape.n_layer * 5

@@ -379,6 +379,31 @@ __device__ __noinline__ void warp_stage_rows(const unsigned char* ring, int s0, 
     __syncwarp();
 }
 
+// One attention chunk (keys, values and queries already in `at`) for the
+// `group` query heads of a kv head; writes each head's partial (m, l,
+// acc[64]) to every packet copy: head h's partial at out + h * head_stride.
+__device__ __noinline__ void attn_unit_compute(AttnSmem* at, int group, int nj, u64* out, int head_stride,
+                                               int copy_stride, unsigned ep) {
+    attn_chunk<SyncCompute>(*at, group, nj, [&](int h, int d, float acc, float m, float lsum) {
+        u64* pr = out + (size_t)h * head_stride;
+        pk_put_all(pr + 2 + d, copy_stride, acc, ep);
+        if (d == 0) {
+            pk_put_all(pr, copy_stride, m, ep);
+            pk_put_all(pr + 1, copy_stride, lsum, ep);
+        }
+    });
+}
+
+// Merge of all chunk partials staged in shared memory as stg[h][c][66]
+// into o (nh * 64 values): the attn_merge arithmetic, in chunk order.
+__device__ __noinline__ void merge_staged(const float* stg, int nh, int n_chunks, float* o) {
+    for (int e = threadIdx.x; e < nh * kHd; e += kCompute) {
+        const int h = e / kHd, d = e % kHd;
+        const float* ph = stg + (size_t)h * n_chunks * kPartStride;
+        o[e] = attn_merge(n_chunks, d, [&](int cc, int i) { return ph[cc * kPartStride + i]; });
+    }
+}
+
 template <int HC, int IC>
 __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -653,14 +678,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
                              }, idle);
             }
             SyncCompute::sync();
-            attn_chunk<SyncCompute>(at, group, nj, [&](int h, int d, float acc, float m, float lsum) {
-                u64* pr = pk + lay.att + ((size_t)(g * group + h) * a.max_chunks + ch) * kPartStride;
-                pk_put_all(pr + 2 + d, lay.n_att, acc, ep);
-                if (d == 0) {
-                    pk_put_all(pr, lay.n_att, m, ep);
-                    pk_put_all(pr + 1, lay.n_att, lsum, ep);
-                }
-            });
+            attn_unit_compute(&at, group, nj, pk + lay.att + ((size_t)(g * group) * a.max_chunks + ch) * kPartStride,
+                              a.max_chunks * kPartStride, lay.n_att, ep);
         }
         if (phase_end()) break;
         arrive(l * 5 + 1);
@@ -691,20 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
                              },
                              [&](int j, float v) { stg[j] = v; }, idle);
                 SyncCompute::sync();
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int e = tid + 256 * k;
-                    if (e < nh * kHd) {
-                        const int h = e / kHd, d = e % kHd;
-                        const float* ph = stg + (size_t)h * n_chunks * kPartStride;
-                        for (int cc = 0; cc < n_chunks; ++cc) Mv[k] = fmaxf(Mv[k], ph[cc * kPartStride]);
-                        for (int cc = 0; cc < n_chunks; ++cc) {
-                            const float w = expf(ph[cc * kPartStride] - Mv[k]);
-                            Lv[k] = fmaf(w, ph[cc * kPartStride + 1], Lv[k]);
-                            Ov[k] = fmaf(w, ph[cc * kPartStride + 2 + d], Ov[k]);
-                        }
-                    }
-                }
+                merge_staged(stg, nh, n_chunks, xs);
             } else {
                 // Long context: chunk maxima first, then (l, acc) a group of
                 // chunks at a time.
@@ -749,11 +755,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
                     }
                     SyncCompute::sync();
                 }
-            }
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int e = tid + 256 * k;
-                if (e < nh * kHd) xs[e] = Ov[k] / Lv[k];
+                for (int k = 0; k < 4; ++k) {
+                    const int e = tid + 256 * k;
+                    if (e < nh * kHd) xs[e] = Ov[k] / Lv[k];
+                }
             }
             if (phase_end()) break;
         }
@@ -764,10 +770,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
             for (int q = warp, i = 0; 2 * q < o_r1 - o_r0; q += 8, ++i) {
                 const int r = o_r0 + 2 * q;
                 const float acc[2][1] = {{res[2 * i]}, {res[2 * i + 1]}};
-                if (lane == 0) {
-                    // xr still holds this layer's input x (gathered for Q/K/V).
-                    pk_put_all(pk + lay.x1 + r, lay.n_x, xr[r] + acc[0][0], ep);
-                    pk_put_all(pk + lay.x1 + r + 1, lay.n_x, xr[r + 1] + acc[1][0], ep);
+                // xr still holds this layer's input x (gathered for Q/K/V);
+                // lanes 0-7 write copy (lane % 4) of row r + lane / 4.
+                if (lane < 2 * kPkRep) {
+                    const int e = lane / kPkRep, k = lane % kPkRep;
+                    pk_put(pk + lay.x1 + (size_t)k * lay.n_x + r + e, xr[r + e] + res[2 * i + e], ep);
                 }
             }
         });
@@ -786,9 +793,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
         const int gu_r0 = 2 * split(I, c, G), gu_r1 = 2 * split(I, c + 1, G);
         // Pair (gate j, up j) in rows 2j, 2j + 1 of the stage; one per warp.
         // Pair (gate j, up j) in rows 2j, 2j + 1; one pair per warp per stage.
+        // Lane 4i + k writes copy k of pair i's output.
         auto gu_out = [&](int r0, int n) {
-            for (int q = warp, i = 0; 2 * q < n; q += 8, ++i)
-                if (lane == 0) pk_put_all(pk + lay.m + ((r0 + 2 * q) >> 1), lay.n_m, silu_f(res[2 * i]) * res[2 * i + 1], ep);
+            const int i = lane / kPkRep, k = lane % kPkRep, q = warp + 8 * i;
+            if (i < 32 / kPkRep && 2 * q < n)
+                pk_put(pk + lay.m + (size_t)k * lay.n_m + ((r0 + 2 * q) >> 1), silu_f(res[2 * i]) * res[2 * i + 1], ep);
         };
         if ((gu_r1 - gu_r0 + rpc_h - 1) / rpc_h <= a.stages) {
             consume_all(gu_r0, gu_r1, rpc_h, [&](int s0) {
@@ -815,8 +824,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
         const int d_r0 = split(H, c, G), d_r1 = split(H, c + 1, G);
         // xr holds x after the attention add (gathered for gate/up).
         auto down_out = [&](int r0, int n) {
-            for (int q = warp, k = 0; q < n; q += 8, ++k)
-                if (lane == 0) pk_put_all(pk + lay.x2 + r0 + q, lay.n_x, xr[r0 + q] + res[k], ep);
+            const int i = lane / kPkRep, k = lane % kPkRep, q = warp + 8 * i;
+            if (i < 32 / kPkRep && q < n) pk_put(pk + lay.x2 + (size_t)k * lay.n_x + r0 + q, xr[r0 + q] + res[i], ep);
         };
         if ((d_r1 - d_r0 + rpc_i - 1) / rpc_i <= a.stages) {
             consume_all(d_r0, d_r1, rpc_i, [&](int s0) {
@@ -854,15 +863,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
             warp_stage_pairs<H>(reinterpret_cast<const unsigned char*>(st), 0, 1, n, xs, res);
             for (int q = warp, i = 0; 2 * q < n; q += 8, ++i) {
                 const bool two = 2 * q + 1 < n;
-                const float acc[2][1] = {{res[2 * i]}, {res[2 * i + 1]}};
                 if (lane == 0) {
                     const int r = r0 + 2 * q;
+                    const float l0 = res[2 * i], l1 = res[2 * i + 1];
                     if (a.logits) {
-                        a.logits[r] = acc[0][0];
-                        if (two) a.logits[r + 1] = acc[1][0];
+                        a.logits[r] = l0;
+                        if (two) a.logits[r + 1] = l1;
                     }
-                    argmax_merge(best_v, best_i, acc[0][0], r);
-                    if (two) argmax_merge(best_v, best_i, acc[1][0], r + 1);
+                    argmax_merge(best_v, best_i, l0, r);
+                    if (two) argmax_merge(best_v, best_i, l1, r + 1);
                 }
             }
         });
