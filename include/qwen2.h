@@ -77,6 +77,7 @@ extern "C" {
 
 /* ---- feature bits (qwen2_features) --------------------------------------- */
 #define QWEN2_FEATURE_PERSISTENT_DECODE 0x1u  /* batch-1 decode runs the persistent single-launch kernel */
+#define QWEN2_FEATURE_TENSOR_PREFILL    0x2u  /* prefill GEMMs run on the tcgen05 tensor cores */
 
 typedef struct qwen2_config {
     int32_t n_layer;        /* num_hidden_layers (24 on Qwen2.5-0.5B) */

@@ -39,6 +39,7 @@ FLAG_NO_GRAPH = 0x4
 FLAG_NO_MEGAKERNEL = 0x8
 FLAG_PROFILE = 0x10
 FEATURE_PERSISTENT_DECODE = 0x1
+FEATURE_TENSOR_PREFILL = 0x2
 
 # Every symbol include/qwen2.h declares.
 EXPORTS = (

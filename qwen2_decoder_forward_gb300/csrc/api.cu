@@ -102,7 +102,7 @@ int validate_config(const qwen2_config* g, std::string& msg) {
         msg = "weight_format " + std::to_string(g->weight_format) + " is not supported by this build";
         return QWEN2_E_UNSUPPORTED;
     }
-    if (g->prefill_mode != QWEN2_PREFILL_F32) {
+    if (g->prefill_mode != QWEN2_PREFILL_F32 && g->prefill_mode != QWEN2_PREFILL_TENSOR) {
         msg = "prefill_mode " + std::to_string(g->prefill_mode) + " is not supported by this build";
         return QWEN2_E_UNSUPPORTED;
     }
@@ -165,6 +165,13 @@ int setup_workspace(Ctx& c) {
     A(&w.x2, (size_t)R * H);
     A(&w.q2, (size_t)R * nq);
     A(&w.ids, R);
+    if (g.prefill_mode == QWEN2_PREFILL_TENSOR) {
+        A(&w.xn_h, (size_t)R * H);
+        A(&w.xn_l, (size_t)R * H);
+        A(&w.o_h, (size_t)R * nq);
+        A(&w.o_l, (size_t)R * nq);
+        A(&w.mlp_h, (size_t)R * I);
+    }
     A(&c.ds.tok, S);
     A(&c.ds.pos, S);
     A(&c.ds.slot, S);
@@ -286,6 +293,10 @@ int qwen2_create(const qwen2_config* cfg, const qwen2_weights* weights, qwen2_ct
     if (decode_set_smem_limits(max_smem) != cudaSuccess || prefill_set_smem_limits() != cudaSuccess)
         return bail(QWEN2_E_CUDA, "cannot set kernel shared-memory limits");
     if (persistent_setup(c) != cudaSuccess) return bail(QWEN2_E_CUDA, "persistent decode kernel set-up failed");
+    if (cfg->prefill_mode == QWEN2_PREFILL_TENSOR) {
+        r = tc_setup(c, msg);
+        if (r != QWEN2_OK) return bail(r, "tensor-core prefill set-up failed: " + msg);
+    }
     if (cudaStreamCreateWithFlags(&c.cap_stream, cudaStreamNonBlocking) != cudaSuccess)
         return bail(QWEN2_E_CUDA, "cannot create the capture stream");
     if (cudaDeviceSynchronize() != cudaSuccess) return bail(QWEN2_E_CUDA, "set-up failed on the device");
@@ -506,7 +517,7 @@ int64_t qwen2_weight_bytes(const qwen2_ctx* h) { return h ? (int64_t)h->c.wbytes
 
 uint32_t qwen2_features(const qwen2_ctx* h) {
     if (!h) return 0;
-    return h->c.pers.ok ? QWEN2_FEATURE_PERSISTENT_DECODE : 0u;
+    return (h->c.pers.ok ? QWEN2_FEATURE_PERSISTENT_DECODE : 0u) | (h->c.tc.ok ? QWEN2_FEATURE_TENSOR_PREFILL : 0u);
 }
 
 int qwen2_profile_marks(qwen2_ctx* h, int64_t* out, int64_t max_marks, int32_t* n_cta, int32_t* n_marks) {

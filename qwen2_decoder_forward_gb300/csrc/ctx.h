@@ -1,6 +1,7 @@
 // Internal state of a libqwen2 context and the launchers the C ABI drives.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -59,7 +60,11 @@ struct Workspace {
     int* blk = nullptr;        // prefill: attention query-block plan (4 arrays)
     float* x2 = nullptr;       // [rows][H] kept rows of the residual (tail cut)
     float* q2 = nullptr;       // [rows][nh*hd] kept rows of q (tail cut)
-    __half* xn_h = nullptr;    // [rows][max(H, I)] f16 operand rows (tensor prefill)
+    __half* xn_h = nullptr;    // [rows][H] f16 normed rows (tensor prefill operand), and
+    __half* xn_l = nullptr;    //   their f16 remainders x - f32(xn_h)
+    __half* o_h = nullptr;     // [rows][nh*hd] f16 attention output (tensor prefill operand), and
+    __half* o_l = nullptr;     //   its f16 remainders
+    __half* mlp_h = nullptr;   // [rows][I] f16 SiLU(gate) * up (tensor prefill operand)
     int* ids = nullptr;        // [rows] prefill ids staging
     float* out_logits = nullptr; // [rows_out][V] staging when the caller's logits are host memory
     size_t out_logits_rows = 0;
@@ -104,6 +109,17 @@ struct PersistState {
     std::string why_not;              // why the kernel is unavailable, if it is
 };
 
+// TMA tensor maps of the tensor-core prefill GEMMs (encoded once; every
+// pointer they hold is fixed for the context's lifetime).
+struct TcLayerMaps {
+    CUtensorMap wqkv, wo, wgu, wd;
+};
+struct TcState {
+    bool ok = false;
+    CUtensorMap a_xn, a_xn_lo, a_o, a_o_lo, a_mlp;   // activation operands [max_rows][K]
+    std::vector<TcLayerMaps> layers;
+};
+
 struct Ctx {
     qwen2_config cfg{};
     int device = 0;
@@ -121,6 +137,7 @@ struct Ctx {
     Workspace ws;
     DecodeState ds;
     PersistState pers;
+    TcState tc;
     int max_rows = 0;             // rows the prefill workspace holds
     int last_rows_out = 0;        // rows of the last call's final_norm_output
     cudaStream_t cap_stream = nullptr;
@@ -140,6 +157,10 @@ cudaError_t enqueue_decode_step(Ctx& c, int B, bool want_logits, cudaStream_t st
 cudaError_t enqueue_lm_head(Ctx& c, const float* xin, int B, float* logits, int* ids, bool decode,
                             cudaStream_t st);
 cudaError_t decode_set_smem_limits(int max_bytes);
+// o_proj + residual, RMSNorm + gate/up + SwiGLU and down + residual of
+// `layer` on `rows` rows of x (f32 [rows][H]) with attention output o (f32
+// [rows][nh*hd]), through the decode GEMV kernels (groups of 8 rows).
+cudaError_t enqueue_rows_o_ffn(Ctx& c, int layer, float* x, const float* o, int rows, cudaStream_t st);
 
 // ---- pack.cu -------------------------------------------------------------------
 int pack_weights(Ctx& c, const qwen2_weights* w, std::string& err);

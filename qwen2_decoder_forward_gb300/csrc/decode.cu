@@ -530,7 +530,35 @@ cudaError_t decode_nb(Ctx& c, int B, bool want_logits, cudaStream_t st) {
     return lm_head_nb<NB>(c, c.ws.x, B, want_logits ? c.ws.logits : nullptr, nullptr, c.ws.hidden, true, st);
 }
 
+template <int NB>
+cudaError_t rows_o_ffn_nb(Ctx& c, int l, float* x, const float* o, int B, cudaStream_t st) {
+    const DevLayer& L = c.layers[l];
+    const int H = c.cfg.hidden, I = c.cfg.intermediate, nq = c.cfg.n_head * kHd;
+    const int cap = c.n_sm * 8;
+    StepArgs a = make_step_args(c, B, nullptr, nullptr, nullptr, x);
+    k_gemv_residual<NB><<<blocks_for(H / 2, cap), kThreads, NB * nq * 4, st>>>(L.wo.w, H, nq, o, B, x);
+    k_gateup_fused<NB><<<blocks_for(I, cap), kThreads, (NB * H + kWarps) * 4, st>>>(a, L.wgu.w, L.ffn_norm);
+    k_gemv_residual<NB><<<blocks_for(H / 2, cap), kThreads, NB * I * 4, st>>>(L.wd.w, H, I, c.ws.mlp, B, x);
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t enqueue_rows_o_ffn(Ctx& c, int layer, float* x, const float* o, int rows, cudaStream_t st) {
+    const int H = c.cfg.hidden, nq = c.cfg.n_head * kHd;
+    for (int b0 = 0; b0 < rows; b0 += 8) {
+        const int nb = rows - b0 < 8 ? rows - b0 : 8;
+        float* xg = x + (size_t)b0 * H;
+        const float* og = o + (size_t)b0 * nq;
+        cudaError_t e;
+        if (nb <= 1) e = rows_o_ffn_nb<1>(c, layer, xg, og, nb, st);
+        else if (nb <= 2) e = rows_o_ffn_nb<2>(c, layer, xg, og, nb, st);
+        else if (nb <= 4) e = rows_o_ffn_nb<4>(c, layer, xg, og, nb, st);
+        else e = rows_o_ffn_nb<8>(c, layer, xg, og, nb, st);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
 
 cudaError_t enqueue_lm_head(Ctx& c, const float* xin, int B, float* logits, int* ids, bool decode,
                             cudaStream_t st) {

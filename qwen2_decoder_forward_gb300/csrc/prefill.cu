@@ -13,6 +13,7 @@ namespace {
 
 constexpr int kT = 256;
 constexpr int kHd = 64;
+constexpr int kGemvRows = 32;   // at most this many rows: o_proj and FFN as GEMVs
 
 __global__ void __launch_bounds__(kT) k_embed_rows(const int* __restrict__ tok, int V, int H,
                                                    const __half* __restrict__ E, float* __restrict__ x,
@@ -26,7 +27,31 @@ __global__ void __launch_bounds__(kT) k_embed_rows(const int* __restrict__ tok, 
     for (int j = threadIdx.x; j < H; j += blockDim.x) x[(size_t)r * H + j] = __half2float(E[(size_t)t * H + j]);
 }
 
-// out[r] = RMSNorm(x[r]) * w.
+// v as an f16 pair: hi = f16(v), lo = f16(v - hi) (v - hi is exact in f32).
+__device__ __forceinline__ void put_split(__half* hi, __half* lo, size_t i, float v) {
+    const __half h = __float2half_rn(v);
+    hi[i] = h;
+    lo[i] = __float2half_rn(v - __half2float(h));
+}
+
+// out[r] = RMSNorm(x[r]) * w in f32, or, for the tensor-core operands, as
+// f16 hi / lo pairs.
+__global__ void __launch_bounds__(kT) k_norm_rows_split(const float* __restrict__ x, int H,
+                                                        const float* __restrict__ w, float eps,
+                                                        __half* __restrict__ hi, __half* __restrict__ lo) {
+    __shared__ float red[kT / 32];
+    const int r = blockIdx.x;
+    const float* xr = x + (size_t)r * H;
+    float ss = 0.f;
+    for (int j = threadIdx.x; j < H; j += blockDim.x) {
+        const float v = xr[j];
+        ss = fmaf(v, v, ss);
+    }
+    const float s = rms_scale(block_sum(ss, red), H, eps);
+    for (int j = threadIdx.x; j < H; j += blockDim.x)
+        put_split(hi, lo, (size_t)r * H + j, __fmul_rn(__fmul_rn(xr[j], s), w[j]));
+}
+
 __global__ void __launch_bounds__(kT) k_norm_rows(const float* __restrict__ x, int H, const float* __restrict__ w,
                                                   float eps, float* __restrict__ out) {
     __shared__ float red[kT / 32];
@@ -255,9 +280,14 @@ __global__ void __launch_bounds__(kT) k_attn_prefill(PrefillAttnArgs a, int laye
         const int v = warp + 8 * t;
         if (v >= nv) continue;
         const int ri = v / group, h = v % group;
-        float* orow = a.o + (size_t)(r0 + ri) * a.nh * kHd + (size_t)(g * group + h) * kHd;
-        orow[lane] = o0[t] / l_[t];
-        orow[lane + 32] = o1[t] / l_[t];
+        const size_t off = (size_t)(r0 + ri) * a.nh * kHd + (size_t)(g * group + h) * kHd;
+        if (a.o_h) {
+            put_split(a.o_h, a.o_l, off + lane, o0[t] / l_[t]);
+            put_split(a.o_h, a.o_l, off + lane + 32, o1[t] / l_[t]);
+        } else {
+            a.o[off + lane] = o0[t] / l_[t];
+            a.o[off + lane + 32] = o1[t] / l_[t];
+        }
     }
 }
 
@@ -306,6 +336,7 @@ cudaError_t enqueue_prefill(Ctx& c, int rows, int n_keep, const PrefillPlan& pla
                             int* ids_dev, cudaStream_t st) {
     const qwen2_config& g = c.cfg;
     const int H = g.hidden, I = g.intermediate, nq = g.n_head * kHd;
+    const bool tensor = g.prefill_mode == QWEN2_PREFILL_TENSOR;
     Workspace& w = c.ws;
     k_embed_rows<<<rows, kT, 0, st>>>(w.rows_tok, g.vocab, H, c.embed.w, w.x, c.err);
     float* x = w.x;
@@ -318,13 +349,22 @@ cudaError_t enqueue_prefill(Ctx& c, int rows, int n_keep, const PrefillPlan& pla
         const bool last = l == g.n_layer - 1;
         PrefillEpi e = base_epi(c, l, pos, slot, x, q);
         // RMSNorm, stacked QKV product + bias + RoPE + KV store (all rows).
-        k_norm_rows<<<cur, kT, 0, st>>>(x, H, L.attn_norm, g.rms_eps, w.xn);
         e.kind = kEpiQKV;
         e.bias = L.bqkv;
-        k_gemm_f32<<<gemm_grid(cur, c.nqkv), kT, 0, st>>>(w.xn, L.wqkv.w, cur, c.nqkv, H, e);
+        if (tensor) {
+            k_norm_rows_split<<<cur, kT, 0, st>>>(x, H, L.attn_norm, g.rms_eps, w.xn_h, w.xn_l);
+            cudaError_t err = tc_gemm_qkv(c, l, cur, e, st);
+            if (err != cudaSuccess) return err;
+        } else {
+            k_norm_rows<<<cur, kT, 0, st>>>(x, H, L.attn_norm, g.rms_eps, w.xn);
+            k_gemm_f32<<<gemm_grid(cur, c.nqkv), kT, 0, st>>>(w.xn, L.wqkv.w, cur, c.nqkv, H, e);
+        }
         const int* blk_row0 = plan.blk_row0;
         const int* blk_nrows = plan.blk_nrows;
         int n_blk = plan.n_blk;
+        // The rest of the layer runs on tensor cores unless the tail cut
+        // left only the kept rows (a handful: the CUDA-core kernels take them).
+        bool tc = tensor;
         if (last && n_keep < cur) {
             // Tail cut: only the kept rows go on to attention, o_proj, FFN, head.
             k_gather_rows<<<n_keep, kT, 0, st>>>(x, H, w.keep_rows, w.x2);
@@ -340,18 +380,39 @@ cudaError_t enqueue_prefill(Ctx& c, int rows, int n_keep, const PrefillPlan& pla
             blk_nrows = plan.kblk_nrows;
             n_blk = plan.n_kblk;
             e = base_epi(c, l, pos, slot, x, q);
+            tc = false;
         }
-        PrefillAttnArgs aa{q, w.o, c.kv, pos, slot, blk_row0, blk_nrows, g.n_head, g.n_kv_head, g.n_ctx, g.n_layer};
-        k_attn_prefill<<<dim3(g.n_kv_head, n_blk), kT, kAttnSmem, st>>>(aa, l);
-        // o_proj + residual.
-        e.kind = kEpiResidual;
-        k_gemm_f32<<<gemm_grid(cur, H), kT, 0, st>>>(w.o, L.wo.w, cur, H, nq, e);
-        // RMSNorm, gate/up + SiLU * up, down + residual.
-        k_norm_rows<<<cur, kT, 0, st>>>(x, H, L.ffn_norm, g.rms_eps, w.xn);
-        e.kind = kEpiSwiGLU;
-        k_gemm_f32<<<gemm_grid(cur, 2 * I), kT, 0, st>>>(w.xn, L.wgu.w, cur, 2 * I, H, e);
-        e.kind = kEpiResidual;
-        k_gemm_f32<<<gemm_grid(cur, H), kT, 0, st>>>(w.mlp, L.wd.w, cur, H, I, e);
+        PrefillAttnArgs aa{q, w.o, tc ? w.o_h : nullptr, w.o_l, c.kv, pos, slot, blk_row0, blk_nrows,
+                           g.n_head, g.n_kv_head, g.n_ctx, g.n_layer};
+        if (tc) {
+            cudaError_t err = enqueue_attn_prefill_mma(aa, l, n_blk, st);
+            if (err != cudaSuccess) return err;
+        } else {
+            k_attn_prefill<<<dim3(g.n_kv_head, n_blk), kT, kAttnSmem, st>>>(aa, l);
+        }
+        if (!tc && cur <= kGemvRows) {
+            // A few rows (the tail cut's, or a short prompt): the decode GEMV
+            // kernels stream each weight once for up to 8 rows.
+            cudaError_t err = enqueue_rows_o_ffn(c, l, x, w.o, cur, st);
+            if (err != cudaSuccess) return err;
+        } else if (tc) {
+            // o_proj + residual; RMSNorm, gate/up + SiLU * up, down + residual.
+            cudaError_t err = tc_gemm_o(c, l, cur, x, st);
+            if (err == cudaSuccess) {
+                k_norm_rows_split<<<cur, kT, 0, st>>>(x, H, L.ffn_norm, g.rms_eps, w.xn_h, w.xn_l);
+                err = tc_gemm_gu(c, l, cur, st);
+            }
+            if (err == cudaSuccess) err = tc_gemm_down(c, l, cur, x, st);
+            if (err != cudaSuccess) return err;
+        } else {
+            e.kind = kEpiResidual;
+            k_gemm_f32<<<gemm_grid(cur, H), kT, 0, st>>>(w.o, L.wo.w, cur, H, nq, e);
+            k_norm_rows<<<cur, kT, 0, st>>>(x, H, L.ffn_norm, g.rms_eps, w.xn);
+            e.kind = kEpiSwiGLU;
+            k_gemm_f32<<<gemm_grid(cur, 2 * I), kT, 0, st>>>(w.xn, L.wgu.w, cur, 2 * I, H, e);
+            e.kind = kEpiResidual;
+            k_gemm_f32<<<gemm_grid(cur, H), kT, 0, st>>>(w.mlp, L.wd.w, cur, H, I, e);
+        }
         cudaError_t err = cudaGetLastError();
         if (err != cudaSuccess) return err;
     }

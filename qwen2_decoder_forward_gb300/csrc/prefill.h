@@ -31,7 +31,9 @@ struct PrefillEpi {
 
 struct PrefillAttnArgs {
     const float* q;         // [rows][nh*64] rotated queries
-    float* o;               // [rows][nh*64] head outputs
+    float* o;               // [rows][nh*64] head outputs (f32), or
+    __half* o_h;            //   f16 hi / lo pairs when o_h is not null
+    __half* o_l;            //   (tensor-core operands: o = o_h + o_l)
     const float* kv;
     const int* pos;
     const int* slot;
@@ -51,6 +53,20 @@ struct PrefillPlan {
 };
 
 constexpr int kPrefillQB = 16;   // query rows per attention block
+
+// ---- tensor-core path (prefill_tc.cu) --------------------------------------
+// Encodes the TMA tensor maps and raises the GEMM shared-memory limits;
+// needs ws.xn_h / o_h / mlp_h and the packed weights.
+int tc_setup(Ctx& c, std::string& why);
+// The four GEMMs of `layer` over the first M workspace rows.
+cudaError_t tc_gemm_qkv(const Ctx& c, int layer, int M, const PrefillEpi& e, cudaStream_t st);
+cudaError_t tc_gemm_o(const Ctx& c, int layer, int M, float* x, cudaStream_t st);
+cudaError_t tc_gemm_gu(const Ctx& c, int layer, int M, cudaStream_t st);
+cudaError_t tc_gemm_down(const Ctx& c, int layer, int M, float* x, cudaStream_t st);
+
+// Causal GQA attention of the tensor-core path (prefill_attn.cu): writes
+// a.o_h / a.o_l; grid (nkv, n_blk) over the 16-row query blocks.
+cudaError_t enqueue_attn_prefill_mma(const PrefillAttnArgs& a, int layer, int n_blk, cudaStream_t st);
 
 cudaError_t enqueue_prefill(Ctx& c, int rows, int n_keep, const PrefillPlan& plan, float* logits_dev,
                             int* ids_dev, cudaStream_t st);

@@ -92,3 +92,23 @@ def test_prefill_8x512_tail_cut(q2, weights, orc):
     for j, i in enumerate((0, 5)):
         check_logits_ids(lg[i:i + 1], ig[i:i + 1], refs[j]["logits"], f"prefill seq {i}")
         check_hidden(hid[i:i + 1], refs[j]["final_norm_output"], f"prefill seq {i}")
+
+
+def test_prefill_8x512_tensor_cores(q2, weights, orc):
+    """Config 4 as the benchmark runs it: tcgen05 GEMMs on f16 operands."""
+    wl = synth.WORKLOADS["0.5b-prefill-8x512"]
+    prompts = wl.prompts(SHAPE.vocab)
+    caches = {i: orc.new_cache() for i in (0, 3, 7)}
+    refs = {i: orc.prefill(caches[i], prompts[i]) for i in caches}
+    with q2.Qwen2Model(SHAPE, weights, n_ctx=wl.n_ctx, max_seqs=8, max_tokens=8 * 512,
+                       prefill_mode=q2.PREFILL_TENSOR) as m:
+        assert m.features & q2.FEATURE_TENSOR_PREFILL
+        logits, ids = m.prefill(list(range(8)), prompts, n_out=1)
+        lg, ig = logits.cpu().numpy(), ids.cpu().numpy()
+        hid = m.final_hidden(8).cpu().numpy()
+        kv3 = m.kv_cache()[3].cpu().numpy()
+        m.synchronize()
+    for i, r in refs.items():
+        check_logits_ids(lg[i:i + 1], ig[i:i + 1], r["logits"], f"tensor prefill seq {i}")
+        check_hidden(hid[i:i + 1], r["final_norm_output"], f"tensor prefill seq {i}")
+    check_kv(kv3, caches[3], np.r_[0:8, 250:258, 504:512], "tensor prefill KV seq 3")

@@ -175,3 +175,40 @@ def test_kv_cache_save_and_restore(q2):
         rest = m.decode_steps([0], [int(first[-1])], [22], 10).cpu().numpy()[:, 0]
         m.synchronize()
     np.testing.assert_array_equal(np.concatenate([first, rest]), full)
+
+
+@pytest.mark.parametrize("shape_name", ["toy", "ragged", "toy-mha"])
+def test_tensor_core_prefill(q2, shape_name):
+    """QWEN2_PREFILL_TENSOR (tcgen05 GEMMs on f16 operands): two sequences of
+    37 and 150 rows (two 128-row tiles, the second ragged) with the tail cut,
+    then one 60-row prompt with every row kept (no cut: all layers on tensor
+    cores), against the oracle; KV cache rows too."""
+    shape = synth.SHAPES[shape_name]
+    w = synth.make_weights(shape, 0)
+    n_ctx = 192
+    prompts = [synth.make_tokens(shape.vocab, 37, 17), synth.make_tokens(shape.vocab, 150, 18)]
+    orc = oracle.build_oracle(shape, w, n_ctx)
+    ref = []
+    for p in prompts:
+        cache = orc.new_cache()
+        ref.append((orc.forward(cache, p, np.arange(len(p)), n_out=2), None, cache))
+    full = synth.make_tokens(shape.vocab, 60, 19)
+    fcache = orc.new_cache()
+    fref = orc.forward(fcache, full, np.arange(len(full)), n_out=len(full))
+    with q2.Qwen2Model(shape, w, n_ctx=n_ctx, max_seqs=2, max_tokens=192,
+                       prefill_mode=q2.PREFILL_TENSOR) as m:
+        assert m.features & q2.FEATURE_TENSOR_PREFILL
+        logits, ids = m.prefill([0, 1], prompts, n_out=2)
+        hid = m.final_hidden(4).cpu().numpy()
+        lg, ig = logits.cpu().numpy(), ids.cpu().numpy()
+        kv = m.kv_cache().cpu().numpy()
+        for s in range(2):
+            pre = ref[s][0]
+            check_logits_ids(lg[2 * s:2 * s + 2], ig[2 * s:2 * s + 2], pre["logits"], f"tensor prefill seq {s}")
+            check_hidden(hid[2 * s:2 * s + 2], pre["final_norm_output"], f"tensor prefill seq {s}")
+            check_kv(kv[s], ref[s][2], np.arange(len(prompts[s])), f"tensor prefill KV seq {s}")
+        logits, ids = m.prefill([0], [full], n_out=len(full))
+        hid = m.final_hidden(len(full)).cpu().numpy()
+        check_logits_ids(logits.cpu().numpy(), ids.cpu().numpy(), fref["logits"], "tensor prefill, no cut")
+        check_hidden(hid, fref["final_norm_output"], "tensor prefill, no cut")
+        m.synchronize()
