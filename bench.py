@@ -130,6 +130,41 @@ def kernel_traffic(name: str):
     return rec["bytes"] if h.hexdigest()[:16] == rec["src"] else None
 
 
+def prefill_flops(shape, lens, n_keep: int) -> float:
+    """Algorithmic FLOPs of one prefill with the tail cut: every row through
+    the first L-1 layers and the last layer's Q/K/V product; causal GQA
+    attention of every row in the first L-1 layers and of the kept rows in
+    the last; o_proj and the FFN of the kept rows in the last layer; the LM
+    head on the kept rows (2 flops per multiply-add)."""
+    H, I, V, L = shape.hidden, shape.intermediate, shape.vocab, shape.n_layer
+    nq, nkv = shape.n_head * shape.head_dim, shape.n_kv_head * shape.head_dim
+    qkv = 2 * (nq + 2 * nkv) * H
+    rest = 2 * (H * nq + 2 * I * H + H * I)
+    lens = [int(n) for n in lens]
+    rows = sum(lens)
+    per_key = 4 * shape.n_head * shape.head_dim          # q.k and p.v, all heads
+    att_all = sum(n * (n + 1) // 2 for n in lens) * per_key
+    kept_keys = sum(sum(n - k for k in range(n_keep)) for n in lens)
+    att_kept = kept_keys * per_key
+    return float((L - 1) * rows * (qkv + rest) + rows * qkv + len(lens) * n_keep * rest
+                 + (L - 1) * att_all + att_kept + 2 * len(lens) * n_keep * V * H)
+
+
+def oracle_prefill_rate(shape, weights, prompt, budget_s: float = 20.0):
+    """The oracle's prefill tokens/s on the host cores (one prompt)."""
+    import oracle
+    orc = oracle.build_oracle(shape, weights, 4096)
+    t0 = time.perf_counter()
+    done = 0
+    while done == 0 or time.perf_counter() - t0 < budget_s / 4:
+        orc.prefill(orc.new_cache(), prompt)
+        done += len(prompt)
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return done / dt, done, dt
+
+
 def cpu_threads() -> int:
     try:
         from threadpoolctl import threadpool_info
@@ -159,6 +194,125 @@ def oracle_decode_rate(shape, weights, prompt, n_tokens: int, budget_s: float = 
     return done / dt, done, dt
 
 
+def bench_prefill(args, wl, shape, weights, rank, world, local):
+    """Prefill workloads: a step is one qwen2_prefill of all the workload's
+    sequences through the tail cut (one kept row per sequence, greedy ids
+    out).  Tokens are host arrays (the C ABI copies them, 4 bytes a token)."""
+    prompts = wl.prompts(shape.vocab)
+    lens = [len(p) for p in prompts]
+    n_tok = sum(lens)
+    config = {"workload": f"{wl.name}: {shape.name} shape, {wl.n_seq} sequences x {wl.prompt_len} tokens, "
+                          f"causal prefill with the tail cut (last row of each sequence to the LM head), "
+                          f"{'tensor-core f16 operands' if wl.prefill == 'tensor' else 'f32 CUDA cores'}, "
+                          f"f32 accumulation and KV, n_ctx {wl.n_ctx}",
+              "global_batch": wl.n_seq * world, "seq_len": wl.prompt_len, "parallelism": f"replicas x{world}",
+              "l2": "weights (988 MB) exceed L2 (129 MB): no flush between steps"}
+    flops = prefill_flops(shape, lens, 1)
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        rate, done, dt = oracle_prefill_rate(shape, weights, prompts[0])
+        line = {"impl": "reference", "metric": METRIC, "value": rate, "unit": "tokens/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": n_tok / rate * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic (seeded random weights)", "config": config,
+                "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+                                 "sample": f"{done // len(prompts[0])} prefill(s) of one {len(prompts[0])}-token "
+                                           f"sequence"},
+                "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    import qwen2_decoder_forward_gb300 as q2
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    mode = q2.PREFILL_TENSOR if wl.prefill == "tensor" else q2.PREFILL_F32
+    model = q2.Qwen2Model(shape, weights, n_ctx=wl.n_ctx, max_seqs=wl.n_seq, max_tokens=n_tok,
+                          prefill_mode=mode, flags=args.flags)
+    seqs = list(range(wl.n_seq))
+    ids = torch.empty((wl.n_seq,), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(out):
+        model.prefill(seqs, prompts, n_out=1, want_logits=False, ids_out=out)
+
+    for _ in range(max(3, args.warmup)):
+        step(ids)
+    model.synchronize()
+
+    def barrier():
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    with ClockSampler(local) as clocks:
+        start.record(stream)
+        for _ in range(args.steps):
+            step(ids)
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms = start.elapsed_time(end)
+    if dist:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    model.synchronize()
+    value = args.steps * n_tok * world / (ms / 1e3)
+    # End to end: host token arrays in, ids read back into host memory.
+    host_ids = np.empty((wl.n_seq,), dtype=np.int32)
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step(host_ids)
+    e2e_s = time.perf_counter() - t0
+    if dist:
+        t = torch.tensor([e2e_s], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    hbm, tflops, src = peaks()
+    achieved = flops / (ms / 1e3 / args.steps) / 1e12
+    tensor = bool(model.features & q2.FEATURE_TENSOR_PREFILL)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": tflops, "unit": "TFLOP/s",
+                "frac": achieved / tflops, "traffic": None,
+                "kernel": "one whole prefill (all kernels; tcgen05 GEMMs dominate)" if tensor else
+                          "one whole prefill (f32 CUDA-core kernels)",
+                "peak_source": src + " bf16 dense burst (f16 has the same tensor rate)",
+                "flops_per_launch": flops}
+    # Launches per step: embed; per layer norm, QKV, attention, O, norm, GU,
+    # down (the last layer: norm, QKV, 4 gathers, attention, 3 GEMVs); LM head.
+    launches = 1 + (shape.n_layer - 1) * 7 + 2 + 4 + 1 + 3 + 1
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16 tensor-core operands (activations as f16 hi/lo pairs), f32 "
+                                      "accumulation, f32 residual/softmax/KV" if tensor else "f32",
+            "data": "synthetic (seeded random weights of the Qwen2.5-0.5B shape, uniform-random tokens)",
+            "config": config, "clocks": clocks.summary(),
+            "e2e": {"value": args.steps * n_tok * world / e2e_s, "unit": "tokens/s",
+                    # token, position and slot per row, kept-row indices, and
+                    # the (first row, row count) plan of the 16-row blocks
+                    "h2d_bytes_per_step": int(12 * n_tok + 4 * wl.n_seq
+                                              + 8 * (sum((n + 15) // 16 for n in lens) + wl.n_seq)),
+                    "d2h_bytes_per_step": int(host_ids.nbytes)},
+            "roofline": roofline, "gpu_launches": launches * args.steps}
+    if rank == 0 and not args.skip_cpu_baseline:
+        rate, done, dt = oracle_prefill_rate(shape, weights, prompts[0], budget_s=15.0)
+        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+                                "sample": f"{done // len(prompts[0])} prefill(s) of one {len(prompts[0])}-token "
+                                          f"sequence"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    model.close()
+    if dist:
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -185,6 +339,8 @@ def main():
               "l2": "weights (988 MB) exceed L2 (129 MB): no flush between steps"}
     weights = synth.make_weights(shape, wl.weight_seed)
     prompt = wl.prompts(shape.vocab)[0]
+    if wl.decode_steps == 0:
+        return bench_prefill(args, wl, shape, weights, rank, world, local)
 
     if args.impl == "reference":
         if rank != 0:
