@@ -98,8 +98,16 @@ int validate_config(const qwen2_config* g, std::string& msg) {
         msg = "n_head must be a multiple of n_kv_head with at most 8 query heads per kv head";
         return QWEN2_E_UNSUPPORTED;
     }
-    if (g->weight_format != QWEN2_WEIGHTS_F16) {
+    if (g->weight_format != QWEN2_WEIGHTS_F16 && g->weight_format != QWEN2_WEIGHTS_Q8_0) {
         msg = "weight_format " + std::to_string(g->weight_format) + " is not supported by this build";
+        return QWEN2_E_UNSUPPORTED;
+    }
+    if (g->weight_format == QWEN2_WEIGHTS_Q8_0 && g->prefill_mode != QWEN2_PREFILL_F32) {
+        msg = "Q8_0 weights prefill on the f32 path only (QWEN2_PREFILL_F32)";
+        return QWEN2_E_UNSUPPORTED;
+    }
+    if (g->weight_format == QWEN2_WEIGHTS_Q8_0 && g->hidden > 1024) {
+        msg = "Q8_0 weights need hidden <= 1024 (the batched product stages one activation chunk)";
         return QWEN2_E_UNSUPPORTED;
     }
     if (g->prefill_mode != QWEN2_PREFILL_F32 && g->prefill_mode != QWEN2_PREFILL_TENSOR) {
@@ -165,6 +173,11 @@ int setup_workspace(Ctx& c) {
     A(&w.x2, (size_t)R * H);
     A(&w.q2, (size_t)R * nq);
     A(&w.ids, R);
+    if (g.weight_format == QWEN2_WEIGHTS_Q8_0) {
+        const size_t blocks = ((size_t)g.vocab + 127) / 128;
+        A(&w.lm_val, blocks * 32);
+        A(&w.lm_idx, blocks * 32);
+    }
     if (g.prefill_mode == QWEN2_PREFILL_TENSOR) {
         A(&w.xn_h, (size_t)R * H);
         A(&w.xn_l, (size_t)R * H);
@@ -213,6 +226,10 @@ bool use_persistent(const Ctx& c, int B) {
     const uint32_t off = QWEN2_FLAG_NO_MEGAKERNEL | QWEN2_FLAG_NO_FUSE_QKV | QWEN2_FLAG_NO_FUSE_FFN;
     return B == 1 && c.pers.ok && !(c.cfg.flags & off);
 }
+
+// Sequences one decode step can carry: 8 with f16 weights (the row-dot
+// GEMV kernels), 32 with Q8_0 weights (the batched tensor-core product).
+int max_decode_batch(const Ctx& c) { return c.cfg.weight_format == QWEN2_WEIGHTS_Q8_0 ? 32 : 8; }
 
 cudaError_t enqueue_step(Ctx& c, int B, bool want_logits, cudaStream_t st) {
     if (use_persistent(c, B)) return enqueue_decode_persistent(c, want_logits, st);
@@ -431,7 +448,9 @@ int qwen2_decode_step(qwen2_ctx* h, int32_t n_seq, const int32_t* seq_ids, const
     c.last_error.clear();
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (n_seq < 1 || n_seq > c.cfg.max_seqs) return fail(&c, QWEN2_E_ARG, "n_seq outside [1, max_seqs]");
-    if (n_seq > 8) return fail(&c, QWEN2_E_UNSUPPORTED, "more than 8 sequences per decode step");
+    if (n_seq > max_decode_batch(c))
+        return fail(&c, QWEN2_E_UNSUPPORTED, "more than " + std::to_string(max_decode_batch(c)) +
+                                                 " sequences per decode step with these weights");
     if (!seq_ids || !tokens || !positions) return fail(&c, QWEN2_E_ARG, "null input pointer");
     int r = check_seq_ids(c, n_seq, seq_ids);
     if (r) return r;
@@ -459,7 +478,9 @@ int qwen2_decode_steps(qwen2_ctx* h, int32_t n_seq, const int32_t* seq_ids, cons
     c.last_error.clear();
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (n_seq < 1 || n_seq > c.cfg.max_seqs) return fail(&c, QWEN2_E_ARG, "n_seq outside [1, max_seqs]");
-    if (n_seq > 8) return fail(&c, QWEN2_E_UNSUPPORTED, "more than 8 sequences per decode step");
+    if (n_seq > max_decode_batch(c))
+        return fail(&c, QWEN2_E_UNSUPPORTED, "more than " + std::to_string(max_decode_batch(c)) +
+                                                 " sequences per decode step with these weights");
     if (!seq_ids || !first_tokens || !start_positions || !ids) return fail(&c, QWEN2_E_ARG, "null pointer");
     if (n_steps < 1) return fail(&c, QWEN2_E_ARG, "n_steps must be >= 1");
     int r = check_seq_ids(c, n_seq, seq_ids);

@@ -49,6 +49,8 @@ struct Workspace {
     float* am_val = nullptr;   // LM-head per-block argmax values [blocks][8]
     int* am_idx = nullptr;     // LM-head per-block argmax indices [blocks][8]
     int* am_count = nullptr;   // LM-head arrival counter
+    float* lm_val = nullptr;   // Q8_0 LM-head per-CTA argmax values [ceil(V/128)][32]
+    int* lm_idx = nullptr;     // Q8_0 LM-head per-CTA argmax indices
     float* hidden = nullptr;   // [rows_out][H] final_norm_output
     float* logits = nullptr;   // [max_seqs][V] decode logits staging
     int* rows_tok = nullptr;   // prefill: per-row token

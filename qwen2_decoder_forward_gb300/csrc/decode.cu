@@ -5,6 +5,7 @@
 // with a two-stage block argmax.  Also the unfused variants the
 // QWEN2_FLAG_NO_FUSE_* flags select.
 #include "attn.cuh"
+#include "bgemm.cuh"
 #include "ctx.h"
 #include "rowdot.cuh"
 
@@ -12,6 +13,7 @@ namespace qwen2 {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kLmNtw = 2;   // Q8_0 LM head: n-tiles per warp (128 vocab rows per CTA)
 
 struct StepArgs {
     const int* tok;
@@ -46,6 +48,20 @@ __global__ void __launch_bounds__(kThreads) k_embed_f16(StepArgs a, const __half
     }
     const __half* row = E + (size_t)t * a.H;
     for (int j = threadIdx.x; j < a.H; j += blockDim.x) a.x[(size_t)b * a.H + j] = __half2float(row[j]);
+}
+
+// Q8_0 embedding row: x[b][j] = f32(d[t][j / 32]) * q[t][j].
+__global__ void __launch_bounds__(kThreads) k_embed_q8(StepArgs a, const int8_t* __restrict__ Eq,
+                                                       const __half* __restrict__ Ed) {
+    const int b = blockIdx.x;
+    int t = a.tok[b];
+    if (t < 0 || t >= a.V) {
+        if (threadIdx.x == 0) raise_guard(a.err, kGuardToken);
+        t = 0;
+    }
+    for (int j = threadIdx.x; j < a.H; j += blockDim.x)
+        a.x[(size_t)b * a.H + j] =
+            __half2float(Ed[(size_t)t * (a.H / 32) + j / 32]) * (float)Eq[(size_t)t * a.H + j];
 }
 
 // ---------------------------------------------------------------------------
@@ -415,6 +431,135 @@ __global__ void __launch_bounds__(kThreads) k_lm_head(LmArgs a) {
 }
 
 // ---------------------------------------------------------------------------
+// Epilogues of the batched Q8_0 product (bgemm.cuh) for decode rows.
+// ---------------------------------------------------------------------------
+struct EpiQkvQ8 {
+    StepArgs a;
+    int layer;
+    const float* bias;
+    __device__ __forceinline__ void pair(int b, int n, float v0, float v1) {
+        qkv_pair_epilogue(a, layer, n >> 1, b, v0, v1, bias);
+    }
+    __device__ __forceinline__ void finish(bool) {}
+};
+
+struct EpiResidualQ8 {
+    float* x;
+    int H;
+    __device__ __forceinline__ void pair(int b, int n, float v0, float v1) {
+        float2* d = reinterpret_cast<float2*>(x + (size_t)b * H + n);
+        float2 t = *d;
+        t.x += v0;
+        t.y += v1;
+        *d = t;
+    }
+    __device__ __forceinline__ void finish(bool) {}
+};
+
+// Packed rows (2j, 2j+1) = (gate j, up j): mlp[b][j] = SiLU(gate) * up.
+struct EpiSwigluQ8 {
+    float* mlp;
+    int I;
+    __device__ __forceinline__ void pair(int b, int n, float g, float u) {
+        mlp[(size_t)b * I + (n >> 1)] = silu_f(g) * u;
+    }
+    __device__ __forceinline__ void finish(bool) {}
+};
+
+// Tied LM head + greedy argmax for up to 32 rows: logits (optional), then
+// per CTA the best (value, lowest index) of each row, then the last CTA to
+// finish merges them (and, for decode, feeds the ids back as next tokens).
+struct EpiLmQ8 {
+    float* logits;
+    int V, B;
+    float* am_val;  // [gridDim][32]
+    int* am_idx;
+    int* count;
+    int* ids;
+    int decode;
+    int* tok;
+    int* pos;
+    int* step;
+    int* ids_hist;
+    int hist_stride;
+    int* err;
+    float bv[4];
+    int bi[4];
+    __device__ __forceinline__ void pair(int b, int n, float v0, float v1) {
+        if (logits) {
+            logits[(size_t)b * V + n] = v0;
+            if (n + 1 < V) logits[(size_t)b * V + n + 1] = v1;
+        }
+        const int k = b >> 3;  // this thread's rows are m*16 + gi and m*16 + gi + 8
+        argmax_merge(bv[k], bi[k], v0, n);
+        if (n + 1 < V) argmax_merge(bv[k], bi[k], v1, n + 1);
+    }
+    __device__ void finish(bool) {
+        __shared__ float sv[bg::kWarps][32];
+        __shared__ int si[bg::kWarps][32];
+        __shared__ int last_s;
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, ti = lane & 3;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+#pragma unroll
+            for (int o = 1; o <= 2; o <<= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv[k], o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi[k], o);
+                argmax_merge(bv[k], bi[k], ov, oi);
+            }
+            if (ti == 0) {
+                sv[warp][(k >> 1) * 16 + gi + (k & 1) * 8] = bv[k];
+                si[warp][(k >> 1) * 16 + gi + (k & 1) * 8] = bi[k];
+            }
+        }
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            const int b = threadIdx.x;
+            float v = sv[0][b];
+            int i = si[0][b];
+            for (int w = 1; w < bg::kWarps; ++w) argmax_merge(v, i, sv[w][b], si[w][b]);
+            am_val[blockIdx.x * 32 + b] = v;
+            am_idx[blockIdx.x * 32 + b] = i;
+        }
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) last_s = (atomicAdd(count, 1) == (int)gridDim.x - 1);
+        __syncthreads();
+        if (!last_s) return;
+        __threadfence();
+        for (int b = warp; b < B; b += bg::kWarps) {
+            float v = -INFINITY;
+            int i = 0x7fffffff;
+            for (int k = lane; k < (int)gridDim.x; k += 32)
+                argmax_merge(v, i, __ldcg(am_val + k * 32 + b), __ldcg(am_idx + k * 32 + b));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+                argmax_merge(v, i, ov, oi);
+            }
+            if (lane == 0) {
+                if (i < 0 || i >= V) {
+                    raise_guard(err, kGuardShape);
+                    i = 0;
+                }
+                if (ids) ids[b] = i;
+                if (decode) {
+                    ids_hist[(size_t)(*step % kIdsHist) * hist_stride + b] = i;
+                    tok[b] = i;
+                    pos[b] = pos[b] + 1;
+                }
+            }
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            *count = 0;
+            if (decode) *step = *step + 1;
+        }
+    }
+};
+
+// ---------------------------------------------------------------------------
 // Launchers.
 // ---------------------------------------------------------------------------
 namespace {
@@ -530,6 +675,82 @@ cudaError_t decode_nb(Ctx& c, int B, bool want_logits, cudaStream_t st) {
     return lm_head_nb<NB>(c, c.ws.x, B, want_logits ? c.ws.logits : nullptr, nullptr, c.ws.hidden, true, st);
 }
 
+// ---- Q8_0 weights: the batched tensor-core product for any B <= 32 ---------
+template <int MT, int NTW, int KS, class Epi>
+cudaError_t bgemm(const Ctx& c, const float* X, int B, int K, const DevMat& W, int N, const Epi& e,
+                  cudaStream_t st) {
+    constexpr int rows_cta = (bg::kWarps / KS) * NTW * 8;
+    const int grid = (N + rows_cta - 1) / rows_cta;
+    bg::k_bgemm_q8<MT, NTW, KS, Epi><<<grid, bg::kThreads, bg::smem_bytes(MT), st>>>(X, B, K, W.q, W.d, N, e);
+    return cudaGetLastError();
+}
+
+template <int MT>
+cudaError_t layer_q8(Ctx& c, const StepArgs& a, int l, cudaStream_t st) {
+    const DevLayer& L = c.layers[l];
+    const int H = c.cfg.hidden, I = c.cfg.intermediate, nq = c.cfg.n_head * kHd;
+    k_rmsnorm_rows<<<a.B, kThreads, 0, st>>>(a.x, H, L.attn_norm, a.eps, c.ws.xn);
+    cudaError_t e = bgemm<MT, 1, 4>(c, c.ws.xn, a.B, H, L.wqkv, c.nqkv, EpiQkvQ8{a, l, L.bqkv}, st);
+    if (e != cudaSuccess) return e;
+    k_attn_decode<<<dim3(c.cfg.n_kv_head, c.ws.att_max_chunks, a.B), kThreads, 0, st>>>(
+        a, l, c.ws.att_part, c.ws.att_count, c.ws.att_max_chunks);
+    e = bgemm<MT, 1, 4>(c, c.ws.o, a.B, nq, L.wo, H, EpiResidualQ8{a.x, H}, st);
+    if (e != cudaSuccess) return e;
+    k_rmsnorm_rows<<<a.B, kThreads, 0, st>>>(a.x, H, L.ffn_norm, a.eps, c.ws.xn);
+    e = bgemm<MT, 1, 1>(c, c.ws.xn, a.B, H, L.wgu, 2 * I, EpiSwigluQ8{c.ws.mlp, I}, st);
+    if (e != cudaSuccess) return e;
+    return bgemm<MT, 1, 4>(c, c.ws.mlp, a.B, I, L.wd, H, EpiResidualQ8{a.x, H}, st);
+}
+
+template <int MT>
+cudaError_t lm_head_q8(Ctx& c, const float* xin, int B, float* logits, int* ids, float* hidden, bool decode,
+                       cudaStream_t st) {
+    k_rmsnorm_rows<<<B, kThreads, 0, st>>>(xin, c.cfg.hidden, c.final_norm, c.cfg.rms_eps, hidden);
+    EpiLmQ8 e{};
+    e.logits = logits;
+    e.V = c.cfg.vocab;
+    e.B = B;
+    e.am_val = c.ws.lm_val;
+    e.am_idx = c.ws.lm_idx;
+    e.count = c.ws.am_count;
+    e.ids = ids;
+    e.decode = decode ? 1 : 0;
+    e.tok = c.ds.tok;
+    e.pos = c.ds.pos;
+    e.step = c.ds.step;
+    e.ids_hist = c.ds.ids_hist;
+    e.hist_stride = c.cfg.max_seqs;
+    e.err = c.err;
+    for (int k = 0; k < 4; ++k) {
+        e.bv[k] = -INFINITY;
+        e.bi[k] = 0x7fffffff;
+    }
+    return bgemm<MT, kLmNtw, 1>(c, hidden, B, c.cfg.hidden, c.embed, c.cfg.vocab, e, st);
+}
+
+template <int MT>
+cudaError_t decode_q8(Ctx& c, int B, bool want_logits, cudaStream_t st) {
+    StepArgs a = make_step_args(c, B, c.ds.tok, c.ds.pos, c.ds.slot, c.ws.x);
+    k_embed_q8<<<B, kThreads, 0, st>>>(a, c.embed.q, c.embed.d);
+    for (int l = 0; l < c.cfg.n_layer; ++l) {
+        cudaError_t e = layer_q8<MT>(c, a, l, st);
+        if (e != cudaSuccess) return e;
+    }
+    return lm_head_q8<MT>(c, c.ws.x, B, want_logits ? c.ws.logits : nullptr, nullptr, c.ws.hidden, true, st);
+}
+
+template <int MT>
+cudaError_t rows_o_ffn_q8(Ctx& c, int l, float* x, const float* o, int B, cudaStream_t st) {
+    const DevLayer& L = c.layers[l];
+    const int H = c.cfg.hidden, I = c.cfg.intermediate, nq = c.cfg.n_head * kHd;
+    cudaError_t e = bgemm<MT, 1, 4>(c, o, B, nq, L.wo, H, EpiResidualQ8{x, H}, st);
+    if (e != cudaSuccess) return e;
+    k_rmsnorm_rows<<<B, kThreads, 0, st>>>(x, H, L.ffn_norm, c.cfg.rms_eps, c.ws.xn);
+    e = bgemm<MT, 1, 1>(c, c.ws.xn, B, H, L.wgu, 2 * I, EpiSwigluQ8{c.ws.mlp, I}, st);
+    if (e != cudaSuccess) return e;
+    return bgemm<MT, 1, 4>(c, c.ws.mlp, B, I, L.wd, H, EpiResidualQ8{x, H}, st);
+}
+
 template <int NB>
 cudaError_t rows_o_ffn_nb(Ctx& c, int l, float* x, const float* o, int B, cudaStream_t st) {
     const DevLayer& L = c.layers[l];
@@ -546,6 +767,15 @@ cudaError_t rows_o_ffn_nb(Ctx& c, int l, float* x, const float* o, int B, cudaSt
 
 cudaError_t enqueue_rows_o_ffn(Ctx& c, int layer, float* x, const float* o, int rows, cudaStream_t st) {
     const int H = c.cfg.hidden, nq = c.cfg.n_head * kHd;
+    if (c.cfg.weight_format == QWEN2_WEIGHTS_Q8_0) {
+        for (int b0 = 0; b0 < rows; b0 += 32) {
+            const int nb = rows - b0 < 32 ? rows - b0 : 32;
+            cudaError_t e = nb <= 16 ? rows_o_ffn_q8<1>(c, layer, x + (size_t)b0 * H, o + (size_t)b0 * nq, nb, st)
+                                     : rows_o_ffn_q8<2>(c, layer, x + (size_t)b0 * H, o + (size_t)b0 * nq, nb, st);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }
     for (int b0 = 0; b0 < rows; b0 += 8) {
         const int nb = rows - b0 < 8 ? rows - b0 : 8;
         float* xg = x + (size_t)b0 * H;
@@ -562,9 +792,23 @@ cudaError_t enqueue_rows_o_ffn(Ctx& c, int layer, float* x, const float* o, int 
 
 cudaError_t enqueue_lm_head(Ctx& c, const float* xin, int B, float* logits, int* ids, bool decode,
                             cudaStream_t st) {
-    if (decode && B > 8) return cudaErrorInvalidValue;
     const int H = c.cfg.hidden;
     const size_t V = (size_t)c.cfg.vocab;
+    if (c.cfg.weight_format == QWEN2_WEIGHTS_Q8_0) {
+        if (decode && B > 32) return cudaErrorInvalidValue;
+        for (int b0 = 0; b0 < B; b0 += 32) {
+            const int nb = B - b0 < 32 ? B - b0 : 32;
+            const float* xg = xin + (size_t)b0 * H;
+            float* lg = logits ? logits + (size_t)b0 * V : nullptr;
+            int* ig = ids ? ids + b0 : nullptr;
+            float* hg = c.ws.hidden + (size_t)b0 * H;
+            cudaError_t e = nb <= 16 ? lm_head_q8<1>(c, xg, nb, lg, ig, hg, decode, st)
+                                     : lm_head_q8<2>(c, xg, nb, lg, ig, hg, decode, st);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }
+    if (decode && B > 8) return cudaErrorInvalidValue;
     for (int b0 = 0; b0 < B; b0 += 8) {
         const int nb = B - b0 < 8 ? B - b0 : 8;
         const float* xg = xin + (size_t)b0 * H;
@@ -582,6 +826,11 @@ cudaError_t enqueue_lm_head(Ctx& c, const float* xin, int B, float* logits, int*
 }
 
 cudaError_t enqueue_decode_step(Ctx& c, int B, bool want_logits, cudaStream_t st) {
+    if (c.cfg.weight_format == QWEN2_WEIGHTS_Q8_0) {
+        if (B <= 16) return decode_q8<1>(c, B, want_logits, st);
+        if (B <= 32) return decode_q8<2>(c, B, want_logits, st);
+        return cudaErrorInvalidValue;
+    }
     if (B <= 1) return decode_nb<1>(c, B, want_logits, st);
     if (B <= 2) return decode_nb<2>(c, B, want_logits, st);
     if (B <= 4) return decode_nb<4>(c, B, want_logits, st);
@@ -613,6 +862,18 @@ cudaError_t decode_set_smem_limits(int max_bytes) {
     Q2_SMEM_NB(1) Q2_SMEM_NB(2) Q2_SMEM_NB(4) Q2_SMEM_NB(8)
 #undef Q2_SMEM_NB
 #undef Q2_SMEM
+#define Q2_BG(MT, NTW, KS, EPI)                                                                             \
+    if (e == cudaSuccess)                                                                                   \
+        e = cudaFuncSetAttribute(bg::k_bgemm_q8<MT, NTW, KS, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                 (int)bg::smem_bytes(MT));
+#define Q2_BG_MT(MT)                  \
+    Q2_BG(MT, 1, 4, EpiQkvQ8)         \
+    Q2_BG(MT, 1, 4, EpiResidualQ8)    \
+    Q2_BG(MT, 1, 1, EpiSwigluQ8)      \
+    Q2_BG(MT, kLmNtw, 1, EpiLmQ8)
+    Q2_BG_MT(1) Q2_BG_MT(2)
+#undef Q2_BG_MT
+#undef Q2_BG
     return e;
 }
 

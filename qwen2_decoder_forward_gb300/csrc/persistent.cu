@@ -949,6 +949,10 @@ cudaError_t persistent_setup(Ctx& c) {
     const qwen2_config& g = c.cfg;
     const int H = g.hidden, I = g.intermediate;
     c.pers.ok = false;
+    if (g.weight_format != QWEN2_WEIGHTS_F16) {
+        c.pers.why_not = "the persistent kernel streams f16 weights only";
+        return cudaSuccess;
+    }
     const size_t act = std::max(sizeof(AttnSmem), (size_t)std::max(H, I) * 4);
     const size_t smem = (size_t)kPersistStages * kPersistStage + 256 + act + (size_t)H * 4;
     int dev_max = 0;

@@ -15,16 +15,25 @@ constexpr int kT = 256;
 constexpr int kHd = 64;
 constexpr int kGemvRows = 32;   // at most this many rows: o_proj and FFN as GEMVs
 
-__global__ void __launch_bounds__(kT) k_embed_rows(const int* __restrict__ tok, int V, int H,
-                                                   const __half* __restrict__ E, float* __restrict__ x,
-                                                   int* err) {
+// A weight matrix in f16 (w) or Q8_0 (q, d); see DevMat.
+struct WMat {
+    const __half* w;
+    const int8_t* q;
+    const __half* d;
+};
+WMat wmat(const DevMat& m) { return WMat{m.w, m.q, m.d}; }
+
+__global__ void __launch_bounds__(kT) k_embed_rows(const int* __restrict__ tok, int V, int H, WMat E,
+                                                   float* __restrict__ x, int* err) {
     const int r = blockIdx.x;
     int t = tok[r];
     if (t < 0 || t >= V) {
         if (threadIdx.x == 0) raise_guard(err, kGuardToken);
         t = 0;
     }
-    for (int j = threadIdx.x; j < H; j += blockDim.x) x[(size_t)r * H + j] = __half2float(E[(size_t)t * H + j]);
+    for (int j = threadIdx.x; j < H; j += blockDim.x)
+        x[(size_t)r * H + j] = E.w ? __half2float(E.w[(size_t)t * H + j])
+                                   : __half2float(E.d[(size_t)t * (H / 32) + j / 32]) * (float)E.q[(size_t)t * H + j];
 }
 
 // v as an f16 pair: hi = f16(v), lo = f16(v - hi) (v - hi is exact in f32).
@@ -116,8 +125,8 @@ __device__ __forceinline__ void epilogue_store(const PrefillEpi& e, int m, int n
     }
 }
 
-__global__ void __launch_bounds__(kT) k_gemm_f32(const float* __restrict__ A, const __half* __restrict__ W, int M,
-                                                 int N, int K, PrefillEpi e) {
+__global__ void __launch_bounds__(kT) k_gemm_f32(const float* __restrict__ A, WMat W, int M, int N, int K,
+                                                 PrefillEpi e) {
     __shared__ float As[GBK][GBM + 1];
     __shared__ float Ws[GBK][GBN + 1];
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
@@ -141,15 +150,30 @@ __global__ void __launch_bounds__(kT) k_gemm_f32(const float* __restrict__ A, co
             As[k4 + 3][r] = v.w;
         }
         {
-            // W tile: 128 rows x 16 k halves = 256 x 8 halves.
+            // W tile: 128 rows x 16 k = 256 x 8 values (Q8_0: the exact
+            // product of the block scale and the int8 value, in f32).
             const int r = tid >> 1, k8 = (tid & 1) * 8;
-            uint4 w = make_uint4(0, 0, 0, 0);
-            if (n0 + r < N) w = ld_stream_v4(W + (size_t)(n0 + r) * K + k0 + k8);
-            float2 f;
-            f = h2_to_f2(w.x); Ws[k8 + 0][r] = f.x; Ws[k8 + 1][r] = f.y;
-            f = h2_to_f2(w.y); Ws[k8 + 2][r] = f.x; Ws[k8 + 3][r] = f.y;
-            f = h2_to_f2(w.z); Ws[k8 + 4][r] = f.x; Ws[k8 + 5][r] = f.y;
-            f = h2_to_f2(w.w); Ws[k8 + 6][r] = f.x; Ws[k8 + 7][r] = f.y;
+            if (W.w) {
+                uint4 w = make_uint4(0, 0, 0, 0);
+                if (n0 + r < N) w = ld_stream_v4(W.w + (size_t)(n0 + r) * K + k0 + k8);
+                float2 f;
+                f = h2_to_f2(w.x); Ws[k8 + 0][r] = f.x; Ws[k8 + 1][r] = f.y;
+                f = h2_to_f2(w.y); Ws[k8 + 2][r] = f.x; Ws[k8 + 3][r] = f.y;
+                f = h2_to_f2(w.z); Ws[k8 + 4][r] = f.x; Ws[k8 + 5][r] = f.y;
+                f = h2_to_f2(w.w); Ws[k8 + 6][r] = f.x; Ws[k8 + 7][r] = f.y;
+            } else {
+                uint2 q8 = make_uint2(0, 0);
+                float dsc = 0.f;
+                if (n0 + r < N) {
+                    q8 = *reinterpret_cast<const uint2*>(W.q + (size_t)(n0 + r) * K + k0 + k8);
+                    dsc = __half2float(W.d[(size_t)(n0 + r) * (K / 32) + (k0 + k8) / 32]);
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t word = i < 4 ? q8.x : q8.y;
+                    Ws[k8 + i][r] = dsc * (float)(int8_t)((word >> (8 * (i & 3))) & 0xffu);
+                }
+            }
         }
         __syncthreads();
 #pragma unroll
@@ -226,10 +250,15 @@ __global__ void __launch_bounds__(kT) k_attn_prefill(PrefillAttnArgs a, int laye
     for (int j0 = 0; j0 <= pmax; j0 += 64) {
         const int nj = min(64, pmax + 1 - j0);
         __syncthreads();
-        for (int e = tid; e < nj * (kHd / 4); e += kT) {
+        // Rows j >= nj are zeroed: their probabilities are 0, and 0 times
+        // whatever an earlier kernel left in shared memory need not be 0.
+        for (int e = tid; e < 64 * (kHd / 4); e += kT) {
             const int j = e / (kHd / 4), d4 = (e % (kHd / 4)) * 4;
-            const float4 kk = __ldcg(reinterpret_cast<const float4*>(kbase + (size_t)(j0 + j) * kHd + d4));
-            const float4 vv = __ldcg(reinterpret_cast<const float4*>(vbase + (size_t)(j0 + j) * kHd + d4));
+            float4 kk = make_float4(0.f, 0.f, 0.f, 0.f), vv = kk;
+            if (j < nj) {
+                kk = __ldcg(reinterpret_cast<const float4*>(kbase + (size_t)(j0 + j) * kHd + d4));
+                vv = __ldcg(reinterpret_cast<const float4*>(vbase + (size_t)(j0 + j) * kHd + d4));
+            }
             float* kr = k_s + j * (kHd + 1) + d4;
             kr[0] = kk.x;
             kr[1] = kk.y;
@@ -338,7 +367,7 @@ cudaError_t enqueue_prefill(Ctx& c, int rows, int n_keep, const PrefillPlan& pla
     const int H = g.hidden, I = g.intermediate, nq = g.n_head * kHd;
     const bool tensor = g.prefill_mode == QWEN2_PREFILL_TENSOR;
     Workspace& w = c.ws;
-    k_embed_rows<<<rows, kT, 0, st>>>(w.rows_tok, g.vocab, H, c.embed.w, w.x, c.err);
+    k_embed_rows<<<rows, kT, 0, st>>>(w.rows_tok, g.vocab, H, wmat(c.embed), w.x, c.err);
     float* x = w.x;
     float* q = w.q;
     const int* pos = w.rows_pos;
@@ -357,7 +386,7 @@ cudaError_t enqueue_prefill(Ctx& c, int rows, int n_keep, const PrefillPlan& pla
             if (err != cudaSuccess) return err;
         } else {
             k_norm_rows<<<cur, kT, 0, st>>>(x, H, L.attn_norm, g.rms_eps, w.xn);
-            k_gemm_f32<<<gemm_grid(cur, c.nqkv), kT, 0, st>>>(w.xn, L.wqkv.w, cur, c.nqkv, H, e);
+            k_gemm_f32<<<gemm_grid(cur, c.nqkv), kT, 0, st>>>(w.xn, wmat(L.wqkv), cur, c.nqkv, H, e);
         }
         const int* blk_row0 = plan.blk_row0;
         const int* blk_nrows = plan.blk_nrows;
@@ -406,12 +435,12 @@ cudaError_t enqueue_prefill(Ctx& c, int rows, int n_keep, const PrefillPlan& pla
             if (err != cudaSuccess) return err;
         } else {
             e.kind = kEpiResidual;
-            k_gemm_f32<<<gemm_grid(cur, H), kT, 0, st>>>(w.o, L.wo.w, cur, H, nq, e);
+            k_gemm_f32<<<gemm_grid(cur, H), kT, 0, st>>>(w.o, wmat(L.wo), cur, H, nq, e);
             k_norm_rows<<<cur, kT, 0, st>>>(x, H, L.ffn_norm, g.rms_eps, w.xn);
             e.kind = kEpiSwiGLU;
-            k_gemm_f32<<<gemm_grid(cur, 2 * I), kT, 0, st>>>(w.xn, L.wgu.w, cur, 2 * I, H, e);
+            k_gemm_f32<<<gemm_grid(cur, 2 * I), kT, 0, st>>>(w.xn, wmat(L.wgu), cur, 2 * I, H, e);
             e.kind = kEpiResidual;
-            k_gemm_f32<<<gemm_grid(cur, H), kT, 0, st>>>(w.mlp, L.wd.w, cur, H, I, e);
+            k_gemm_f32<<<gemm_grid(cur, H), kT, 0, st>>>(w.mlp, wmat(L.wd), cur, H, I, e);
         }
         cudaError_t err = cudaGetLastError();
         if (err != cudaSuccess) return err;
