@@ -98,17 +98,19 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def decode_bytes_per_token(shape, positions) -> float:
-    """Algorithmic HBM bytes of one batch-1 decode token at position p:
-    f16 weights once + f32 biases and norms + the embedding row + the KV
-    read of positions 0..p and the KV write of position p."""
+def decode_bytes_per_step(shape, positions, q8: bool = False) -> float:
+    """Algorithmic HBM bytes of one decode step of B sequences at positions
+    p_b: the weights once (f16: 2 bytes an element; Q8_0: 1 byte plus a
+    2-byte scale per 32) + f32 biases and norms + B embedding rows + per
+    sequence the KV read of positions 0..p_b and the KV write of p_b."""
     H, I, V, L = shape.hidden, shape.intermediate, shape.vocab, shape.n_layer
     nq, nkv = shape.n_head * shape.head_dim, shape.n_kv_head * shape.head_dim
-    w = 2 * (V * H + L * ((nq + 2 * nkv) * H + H * nq + 2 * I * H + H * I))
-    small = 4 * (L * (nq + 2 * nkv + 2 * H) + H) + 2 * H
-    kv_pos = L * 2 * nkv * 4
+    per_elem = 1 + 2 / 32 if q8 else 2
+    elems = V * H + L * ((nq + 2 * nkv) * H + H * nq + 2 * I * H + H * I)
+    small = 4 * (L * (nq + 2 * nkv + 2 * H) + H)
     p = np.asarray(positions, dtype=np.float64)
-    return float(np.mean(w + small + kv_pos * (p + 2)))
+    kv_pos = L * 2 * nkv * 4
+    return float(elems * per_elem + small + len(p) * H * per_elem + kv_pos * np.sum(p + 2))
 
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum, mean
@@ -176,11 +178,11 @@ def cpu_threads() -> int:
     return len(os.sched_getaffinity(0))
 
 
-def oracle_decode_rate(shape, weights, prompt, n_tokens: int, budget_s: float = 15.0):
+def oracle_decode_rate(shape, weights, prompt, n_tokens: int, budget_s: float = 15.0, weight_format: str = "f16"):
     """The oracle's greedy decode tokens/s on the host cores: prefill the
     prompt (untimed), then time decode steps until n_tokens or the budget."""
     import oracle
-    orc = oracle.build_oracle(shape, weights, 4096)
+    orc = oracle.build_oracle(shape, weights, 4096, weight_format=weight_format)
     cache = orc.new_cache()
     pre = orc.prefill(cache, prompt)
     tok = int(pre["ids"][0])
@@ -313,48 +315,38 @@ def bench_prefill(args, wl, shape, weights, rank, world, local):
         dist.destroy_process_group()
 
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
-    ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="0.5b-decode-b1")
-    ap.add_argument("--tokens-per-step", type=int, default=0,
-                    help="override the decode tokens of one timed step (profiling runs only)")
-    ap.add_argument("--skip-cpu-baseline", action="store_true", help="profiling runs: no oracle timing")
-    ap.add_argument("--flags", type=int, default=0, help="QWEN2_FLAG_* bits for the context")
-    args = ap.parse_args()
-    wl = synth.WORKLOADS[args.workload]
-    shape = synth.SHAPES[wl.shape]
-
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    config = {"workload": f"{wl.name}: {shape.name} shape, batch {wl.n_seq}, prompt {wl.prompt_len}, "
-                          f"{wl.decode_steps} greedy decode steps per timed step, f16 weights, f32 KV, "
-                          f"n_ctx {wl.n_ctx}",
-              "global_batch": wl.n_seq * world, "seq_len": wl.prompt_len + wl.decode_steps,
+def bench_decode(args, wl, shape, weights, rank, world, local):
+    """Decode workloads: the prompts are prefilled once (untimed); a step is
+    one qwen2_decode_steps call of decode_steps greedy tokens for every
+    sequence (one CUDA-graph replay, or one persistent launch, per token;
+    ids fed back on the device)."""
+    prompts = wl.prompts(shape.vocab)
+    lens = [len(p) for p in prompts]
+    q8 = wl.weight_format == "q8_0"
+    B = wl.n_seq
+    ragged = len(set(lens)) > 1
+    config = {"workload": f"{wl.name}: {shape.name} shape, batch {B}, "
+                          + (f"ragged prompts U{{{wl.ragged_lo}..{wl.ragged_hi}}} (mean {np.mean(lens):.0f})"
+                             if ragged else f"prompt {lens[0]}")
+                          + f", {wl.decode_steps} greedy decode steps per timed step, "
+                          + ("Q8_0" if q8 else "f16") + f" weights, f32 KV, n_ctx {wl.n_ctx}",
+              "global_batch": B * world, "seq_len": int(max(lens)) + wl.decode_steps,
               "parallelism": f"replicas x{world}",
-              "l2": "weights (988 MB) exceed L2 (129 MB): no flush between steps"}
-    weights = synth.make_weights(shape, wl.weight_seed)
-    prompt = wl.prompts(shape.vocab)[0]
-    if wl.decode_steps == 0:
-        return bench_prefill(args, wl, shape, weights, rank, world, local)
-
+              "l2": "weights (" + ("525" if q8 else "988") + " MB) and KV exceed L2 (129 MB): no flush between steps"}
     if args.impl == "reference":
         if rank != 0:
             return
-        n = max(1, args.steps)
-        rate, done, dt = oracle_decode_rate(shape, weights, prompt, 4 * n, budget_s=20.0)
-        cores = cpu_threads()
+        s = int(np.argmin(lens))
+        rate, done, dt = oracle_decode_rate(shape, weights, prompts[s], 4 * max(1, args.steps), budget_s=20.0,
+                                            weight_format=wl.weight_format)
         line = {"impl": "reference", "metric": METRIC, "value": rate, "unit": "tokens/s",
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": 1e3 / rate, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded random weights)",
                 "config": config,
-                "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                                 "sample": f"{done} greedy decode tokens after a {len(prompt)}-token prefill"},
+                "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+                                 "sample": f"{done} greedy decode tokens of one sequence after a "
+                                           f"{lens[s]}-token prefill"},
                 "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
         return
@@ -368,18 +360,19 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
     n_steps = args.tokens_per_step or wl.decode_steps
-    model = q2.Qwen2Model(shape, weights, n_ctx=wl.n_ctx, max_seqs=1, max_tokens=len(prompt), flags=args.flags)
-    _, ids = model.prefill([0], [prompt])
-    first = int(ids[0])
-    p0 = len(prompt)
-    out = torch.empty((n_steps, 1), dtype=torch.int32, device="cuda")
+    model = q2.Qwen2Model(shape, weights, n_ctx=wl.n_ctx, max_seqs=B, max_tokens=sum(lens),
+                          weight_format=q2.WEIGHTS_Q8_0 if q8 else q2.WEIGHTS_F16, flags=args.flags)
+    seqs = list(range(B))
+    _, ids = model.prefill(seqs, prompts)
+    first = [int(t) for t in ids.cpu().numpy()]
+    out = torch.empty((n_steps, B), dtype=torch.int32, device="cuda")
     stream = torch.cuda.current_stream()
 
-    def step():
-        model.decode_steps([0], [first], [p0], n_steps, ids_out=out)
+    def step(dst):
+        model.decode_steps(seqs, first, lens, n_steps, ids_out=dst)
 
     for _ in range(max(3, args.warmup)):
-        step()
+        step(out)
     model.synchronize()
 
     def barrier():
@@ -392,7 +385,7 @@ def main():
     with ClockSampler(local) as clocks:
         start.record(stream)
         for _ in range(args.steps):
-            step()
+            step(out)
         end.record(stream)
         torch.cuda.synchronize()
     barrier()
@@ -402,54 +395,87 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
     model.synchronize()
-    tokens = args.steps * n_steps * world
+    tokens = args.steps * n_steps * B * world
     value = tokens / (ms / 1e3)
-    ms_per_step = ms / args.steps
 
-    # End to end through the public API with host buffers: host token and
-    # position inputs, ids read back into host memory each step.
-    host_ids = np.empty((n_steps, 1), dtype=np.int32)
+    # End to end through the public API with host buffers: host token,
+    # position and sequence-id inputs, ids read back into host memory.
+    host_ids = np.empty((n_steps, B), dtype=np.int32)
     barrier()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        model.decode_steps([0], [first], [p0], n_steps, ids_out=host_ids)
-    t1 = time.perf_counter()
-    e2e_s = t1 - t0
+        step(host_ids)
+    e2e_s = time.perf_counter() - t0
     if dist:
         t = torch.tensor([e2e_s], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_s = float(t.item())
-    e2e = {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": 3 * 4,
+    e2e = {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": 3 * 4 * B,
            "d2h_bytes_per_step": int(host_ids.nbytes)}
 
-    persistent = bool(model.features & q2.FEATURE_PERSISTENT_DECODE) and not (
+    persistent = B == 1 and bool(model.features & q2.FEATURE_PERSISTENT_DECODE) and not (
         args.flags & (q2.FLAG_NO_MEGAKERNEL | q2.FLAG_NO_FUSE_QKV | q2.FLAG_NO_FUSE_FFN))
     hbm, tflops, src = peaks()
-    bytes_tok = decode_bytes_per_token(shape, np.arange(p0, p0 + n_steps))
-    per_token_s = (ms / 1e3) / (args.steps * n_steps)
-    achieved = bytes_tok / per_token_s / 1e9
+    step_bytes = float(np.mean([decode_bytes_per_step(shape, [n + i for n in lens], q8) for i in range(n_steps)]))
+    per_dec_s = (ms / 1e3) / (args.steps * n_steps)
+    achieved = step_bytes / per_dec_s / 1e9
+    if persistent:
+        kname = "one decode token: k_decode_persistent (one launch per token)"
+        launches = 1
+    elif q8:
+        kname = f"one decode step of {B} sequences: all kernels of the step graph (Q8_0 warp-MMA products, " \
+                "split-K attention)"
+        launches = 1 + shape.n_layer * 7 + 2
+    else:
+        kname = f"one decode step of {B} sequences: all kernels of the step graph"
+        launches = 2 + shape.n_layer * 5
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                 "traffic": kernel_traffic("k_decode_persistent") if persistent else None,
-                "kernel": "one decode token: " + (
-                    "k_decode_persistent (one launch per token)" if persistent else "all kernels of the step graph"),
-                "peak_source": src, "bytes_per_launch": bytes_tok}
-    launches_per_token = 1 if persistent else 2 + shape.n_layer * 5
+                "kernel": kname, "peak_source": src, "bytes_per_launch": step_bytes}
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32 activations, f16 weights",
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32 activations, " + ("Q8_0 weights (exact f32 dequantisation; f16 hi/lo MMA operands)"
+                                            if q8 else "f16 weights"),
             "data": "synthetic (seeded random weights of the Qwen2.5-0.5B shape, uniform-random tokens)",
             "config": config, "clocks": clocks.summary(), "e2e": e2e, "roofline": roofline,
-            "gpu_launches": launches_per_token * n_steps * args.steps,
+            "gpu_launches": launches * n_steps * args.steps,
             "decode_kernel": "persistent" if persistent else "per-step"}
     if rank == 0 and not args.skip_cpu_baseline:
-        rate, done, dt = oracle_decode_rate(shape, weights, prompt, 64, budget_s=15.0)
+        s = int(np.argmin(lens))
+        rate, done, dt = oracle_decode_rate(shape, weights, prompts[s], 64, budget_s=15.0,
+                                            weight_format=wl.weight_format)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
-                                "sample": f"{done} greedy decode tokens after a {len(prompt)}-token prefill"}
+                                "sample": f"{done} greedy decode tokens of one sequence after a "
+                                          f"{lens[s]}-token prefill"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     model.close()
     if dist:
         dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="0.5b-decode-b1", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--tokens-per-step", type=int, default=0,
+                    help="override the decode tokens of one timed step (profiling runs only)")
+    ap.add_argument("--skip-cpu-baseline", action="store_true", help="profiling runs: no oracle timing")
+    ap.add_argument("--flags", type=int, default=0, help="QWEN2_FLAG_* bits for the context")
+    args = ap.parse_args()
+    wl = synth.WORKLOADS[args.workload]
+    shape = synth.SHAPES[wl.shape]
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    weights = synth.make_weights(shape, wl.weight_seed)
+    if wl.decode_steps == 0:
+        return bench_prefill(args, wl, shape, weights, rank, world, local)
+    return bench_decode(args, wl, shape, weights, rank, world, local)
 
 
 if __name__ == "__main__":

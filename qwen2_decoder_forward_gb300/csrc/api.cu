@@ -174,9 +174,15 @@ int setup_workspace(Ctx& c) {
     A(&w.q2, (size_t)R * nq);
     A(&w.ids, R);
     if (g.weight_format == QWEN2_WEIGHTS_Q8_0) {
-        const size_t blocks = ((size_t)g.vocab + 127) / 128;
+        const size_t blocks = ((size_t)g.vocab + 255) / 256;
+        const size_t rq = (size_t)c.max_rows_q8;
         A(&w.lm_val, blocks * 32);
         A(&w.lm_idx, blocks * 32);
+        A(&w.q8_ah, rq * std::max(H, nq));
+        A(&w.q8_al, rq * std::max(H, nq));
+        A(&w.q8_mh, rq * I);
+        A(&w.q8_ml, rq * I);
+        A(&w.q8_part, (size_t)((I + 1023) / 1024) * rq * H);
     }
     if (g.prefill_mode == QWEN2_PREFILL_TENSOR) {
         A(&w.xn_h, (size_t)R * H);

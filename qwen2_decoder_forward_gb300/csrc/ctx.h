@@ -49,8 +49,13 @@ struct Workspace {
     float* am_val = nullptr;   // LM-head per-block argmax values [blocks][8]
     int* am_idx = nullptr;     // LM-head per-block argmax indices [blocks][8]
     int* am_count = nullptr;   // LM-head arrival counter
-    float* lm_val = nullptr;   // Q8_0 LM-head per-CTA argmax values [ceil(V/128)][32]
+    float* lm_val = nullptr;   // Q8_0 LM-head per-CTA argmax values [ceil(V/256)][32]
     int* lm_idx = nullptr;     // Q8_0 LM-head per-CTA argmax indices
+    __half* q8_ah = nullptr;   // Q8_0 product operand, f16 hi [32][H] (normed rows, attention output)
+    __half* q8_al = nullptr;   //   and lo
+    __half* q8_mh = nullptr;   // SiLU(gate) * up as f16 hi [32][I]
+    __half* q8_ml = nullptr;   //   and lo
+    float* q8_part = nullptr;  // down-product partials [ceil(I/1024)][32][H]
     float* hidden = nullptr;   // [rows_out][H] final_norm_output
     float* logits = nullptr;   // [max_seqs][V] decode logits staging
     int* rows_tok = nullptr;   // prefill: per-row token
@@ -141,6 +146,7 @@ struct Ctx {
     PersistState pers;
     TcState tc;
     int max_rows = 0;             // rows the prefill workspace holds
+    int max_rows_q8 = 32;         // rows one Q8_0 batched product carries
     int last_rows_out = 0;        // rows of the last call's final_norm_output
     cudaStream_t cap_stream = nullptr;
     std::map<int, cudaGraphExec_t> graphs;   // key: B | (want_logits << 16)

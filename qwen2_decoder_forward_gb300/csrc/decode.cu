@@ -13,7 +13,7 @@ namespace qwen2 {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kLmNtw = 2;   // Q8_0 LM head: n-tiles per warp (128 vocab rows per CTA)
+constexpr int kLmNtw = 4;   // Q8_0 LM head: n-tiles per warp (256 vocab rows per CTA)
 
 struct StepArgs {
     const int* tok;
@@ -23,6 +23,8 @@ struct StepArgs {
     float* x;
     float* q;
     float* o;
+    __half* o_hi;  // nullable: the attention output also as f16 hi / lo (Q8_0 product operand)
+    __half* o_lo;
     float* mlp;
     float* kv;
     const float2* rope;
@@ -254,8 +256,11 @@ __global__ void __launch_bounds__(kThreads) k_attn_decode(StepArgs a, int layer,
     for (int e = tid; e < group * kHd; e += kThreads) {
         const int h = e / kHd, d = e % kHd;
         const float* ph = part + (((size_t)b * a.nh + g * group + h) * max_chunks) * kPartStride;
-        a.o[(size_t)b * a.nh * kHd + (size_t)(g * group + h) * kHd + d] =
+        const size_t oi = (size_t)b * a.nh * kHd + (size_t)(g * group + h) * kHd + d;
+        const float ov =
             attn_merge(n_chunks, d, [&](int cc, int i) { return __ldcg(ph + (size_t)cc * kPartStride + i); });
+        a.o[oi] = ov;
+        if (a.o_hi) bg::split_h(ov, a.o_hi[oi], a.o_lo[oi]);
     }
     if (tid == 0) count[b * a.nkv + g] = 0;
 }
@@ -431,39 +436,98 @@ __global__ void __launch_bounds__(kThreads) k_lm_head(LmArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// Epilogues of the batched Q8_0 product (bgemm.cuh) for decode rows.
+// The Q8_0 decode path: RMSNorm (with the split-k partials of the previous
+// down product added first) writing the product operand as f16 hi / lo, and
+// the epilogues of the batched product (bgemm.cuh).
 // ---------------------------------------------------------------------------
+// x[b] += sum_s part[s][b] (fixed order, when nparts > 0; x written back),
+// then n = RMSNorm(x[b]) * w: to out (f32, nullable) and as hi / lo.
+__global__ void __launch_bounds__(kThreads) k_norm_split(float* __restrict__ x, const float* __restrict__ part,
+                                                         int nparts, size_t part_stride, int H,
+                                                         const float* __restrict__ w, float eps,
+                                                         float* __restrict__ out, __half* __restrict__ hi,
+                                                         __half* __restrict__ lo) {
+    __shared__ float red[kWarps];
+    const int b = blockIdx.x;
+    float* xr = x + (size_t)b * H;
+    float ss = 0.f;
+    for (int j = threadIdx.x; j < H; j += blockDim.x) {
+        float v = xr[j];
+        if (nparts > 0) {
+            for (int s = 0; s < nparts; ++s) v += part[(size_t)s * part_stride + (size_t)b * H + j];
+            xr[j] = v;
+        }
+        ss = fmaf(v, v, ss);
+    }
+    const float sc = rms_scale(block_sum(ss, red), H, eps);
+    for (int j = threadIdx.x; j < H; j += blockDim.x) {
+        const float v = __fmul_rn(__fmul_rn(xr[j], sc), w[j]);
+        if (out) out[(size_t)b * H + j] = v;
+        bg::split_h(v, hi[(size_t)b * H + j], lo[(size_t)b * H + j]);
+    }
+}
+
+// Rows of f32 as hi / lo (the attention output of prefill's kept rows).
+__global__ void __launch_bounds__(kThreads) k_split_rows(const float* __restrict__ src, int n, __half* __restrict__ hi,
+                                                         __half* __restrict__ lo) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) bg::split_h(src[i], hi[i], lo[i]);
+}
+
+// x[b] += sum_s part[s][b] in s order.
+__global__ void __launch_bounds__(kThreads) k_add_parts(float* __restrict__ x, const float* __restrict__ part,
+                                                        int nparts, size_t part_stride, int n) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        float v = x[i];
+        for (int s = 0; s < nparts; ++s) v += part[(size_t)s * part_stride + i];
+        x[i] = v;
+    }
+}
+
 struct EpiQkvQ8 {
     StepArgs a;
     int layer;
     const float* bias;
-    __device__ __forceinline__ void pair(int b, int n, float v0, float v1) {
+    __device__ __forceinline__ void pair(int b, int n, float v0, float v1, int) {
         qkv_pair_epilogue(a, layer, n >> 1, b, v0, v1, bias);
     }
-    __device__ __forceinline__ void finish(bool) {}
+    __device__ __forceinline__ void finish() {}
 };
 
 struct EpiResidualQ8 {
     float* x;
     int H;
-    __device__ __forceinline__ void pair(int b, int n, float v0, float v1) {
+    __device__ __forceinline__ void pair(int b, int n, float v0, float v1, int) {
         float2* d = reinterpret_cast<float2*>(x + (size_t)b * H + n);
         float2 t = *d;
         t.x += v0;
         t.y += v1;
         *d = t;
     }
-    __device__ __forceinline__ void finish(bool) {}
+    __device__ __forceinline__ void finish() {}
 };
 
-// Packed rows (2j, 2j+1) = (gate j, up j): mlp[b][j] = SiLU(gate) * up.
-struct EpiSwigluQ8 {
-    float* mlp;
-    int I;
-    __device__ __forceinline__ void pair(int b, int n, float g, float u) {
-        mlp[(size_t)b * I + (n >> 1)] = silu_f(g) * u;
+// Partial sums of k chunk `chunk`: part[chunk][b][n].
+struct EpiPartQ8 {
+    float* part;
+    size_t stride;
+    int N;
+    __device__ __forceinline__ void pair(int b, int n, float v0, float v1, int chunk) {
+        *reinterpret_cast<float2*>(part + chunk * stride + (size_t)b * N + n) = make_float2(v0, v1);
     }
-    __device__ __forceinline__ void finish(bool) {}
+    __device__ __forceinline__ void finish() {}
+};
+
+// Packed rows (2j, 2j+1) = (gate j, up j): m[b][j] = SiLU(gate) * up, as
+// hi / lo (the operand of the down product).
+struct EpiSwigluQ8 {
+    __half* hi;
+    __half* lo;
+    int I;
+    __device__ __forceinline__ void pair(int b, int n, float g, float u, int) {
+        const size_t i = (size_t)b * I + (n >> 1);
+        bg::split_h(silu_f(g) * u, hi[i], lo[i]);
+    }
+    __device__ __forceinline__ void finish() {}
 };
 
 // Tied LM head + greedy argmax for up to 32 rows: logits (optional), then
@@ -485,7 +549,7 @@ struct EpiLmQ8 {
     int* err;
     float bv[4];
     int bi[4];
-    __device__ __forceinline__ void pair(int b, int n, float v0, float v1) {
+    __device__ __forceinline__ void pair(int b, int n, float v0, float v1, int) {
         if (logits) {
             logits[(size_t)b * V + n] = v0;
             if (n + 1 < V) logits[(size_t)b * V + n + 1] = v1;
@@ -494,7 +558,7 @@ struct EpiLmQ8 {
         argmax_merge(bv[k], bi[k], v0, n);
         if (n + 1 < V) argmax_merge(bv[k], bi[k], v1, n + 1);
     }
-    __device__ void finish(bool) {
+    __device__ void finish() {
         __shared__ float sv[bg::kWarps][32];
         __shared__ int si[bg::kWarps][32];
         __shared__ int last_s;
@@ -573,6 +637,8 @@ StepArgs make_step_args(Ctx& c, int B, const int* tok, const int* pos, const int
     a.x = x;
     a.q = c.ws.q;
     a.o = c.ws.o;
+    a.o_hi = nullptr;
+    a.o_lo = nullptr;
     a.mlp = c.ws.mlp;
     a.kv = c.kv;
     a.rope = c.rope;
@@ -676,43 +742,72 @@ cudaError_t decode_nb(Ctx& c, int B, bool want_logits, cudaStream_t st) {
 }
 
 // ---- Q8_0 weights: the batched tensor-core product for any B <= 32 ---------
+// Shapes: QKV and o_proj 8 weight rows per CTA (8 warps split k); gate/up
+// 64 rows per CTA; down 8 rows per CTA and k split into chunks of 1024
+// whose partials the next RMSNorm adds; LM head 256 rows per CTA.
 template <int MT, int NTW, int KS, class Epi>
-cudaError_t bgemm(const Ctx& c, const float* X, int B, int K, const DevMat& W, int N, const Epi& e,
-                  cudaStream_t st) {
+cudaError_t bgemm(const Ctx& c, const __half* ah, const __half* al, int B, int K, int kc_len, const DevMat& W, int N,
+                  const Epi& e, cudaStream_t st) {
     constexpr int rows_cta = (bg::kWarps / KS) * NTW * 8;
-    const int grid = (N + rows_cta - 1) / rows_cta;
-    bg::k_bgemm_q8<MT, NTW, KS, Epi><<<grid, bg::kThreads, bg::smem_bytes(MT), st>>>(X, B, K, W.q, W.d, N, e);
+    const dim3 grid((N + rows_cta - 1) / rows_cta, (K + kc_len - 1) / kc_len);
+    bg::k_bgemm_q8<MT, NTW, KS, Epi><<<grid, bg::kThreads, bg::smem_bytes(MT), st>>>(ah, al, B, K, kc_len, W.q, W.d,
+                                                                                     N, e, c.err);
     return cudaGetLastError();
+}
+
+int down_chunks(const Ctx& c) { return (c.cfg.intermediate + bg::kKc - 1) / bg::kKc; }
+
+// The steps of one layer after the attention: o_proj + residual, RMSNorm,
+// gate/up + SwiGLU, down as split-k partials (added by the caller's next
+// RMSNorm or by k_add_parts).
+template <int MT>
+cudaError_t o_ffn_q8(Ctx& c, int l, float* x, int B, cudaStream_t st) {
+    const DevLayer& L = c.layers[l];
+    const int H = c.cfg.hidden, I = c.cfg.intermediate, nq = c.cfg.n_head * kHd;
+    Workspace& w = c.ws;
+    cudaError_t e = bgemm<MT, 1, 8>(c, w.q8_ah, w.q8_al, B, nq, nq, L.wo, H, EpiResidualQ8{x, H}, st);
+    if (e != cudaSuccess) return e;
+    k_norm_split<<<B, kThreads, 0, st>>>(x, nullptr, 0, 0, H, L.ffn_norm, c.cfg.rms_eps, nullptr, w.q8_ah, w.q8_al);
+    e = bgemm<MT, 4, 4>(c, w.q8_ah, w.q8_al, B, H, H, L.wgu, 2 * I, EpiSwigluQ8{w.q8_mh, w.q8_ml, I}, st);
+    if (e != cudaSuccess) return e;
+    return bgemm<MT, 1, 8>(c, w.q8_mh, w.q8_ml, B, I, bg::kKc, L.wd, H,
+                           EpiPartQ8{w.q8_part, (size_t)c.max_rows_q8 * H, H}, st);
 }
 
 template <int MT>
 cudaError_t layer_q8(Ctx& c, const StepArgs& a, int l, cudaStream_t st) {
     const DevLayer& L = c.layers[l];
-    const int H = c.cfg.hidden, I = c.cfg.intermediate, nq = c.cfg.n_head * kHd;
-    k_rmsnorm_rows<<<a.B, kThreads, 0, st>>>(a.x, H, L.attn_norm, a.eps, c.ws.xn);
-    cudaError_t e = bgemm<MT, 1, 4>(c, c.ws.xn, a.B, H, L.wqkv, c.nqkv, EpiQkvQ8{a, l, L.bqkv}, st);
+    const int H = c.cfg.hidden;
+    Workspace& w = c.ws;
+    // The previous layer's down partials go into x before its RMSNorm.
+    k_norm_split<<<a.B, kThreads, 0, st>>>(a.x, w.q8_part, l > 0 ? down_chunks(c) : 0, (size_t)c.max_rows_q8 * H, H,
+                                           L.attn_norm, a.eps, nullptr, w.q8_ah, w.q8_al);
+    cudaError_t e = bgemm<MT, 1, 8>(c, w.q8_ah, w.q8_al, a.B, H, H, L.wqkv, c.nqkv, EpiQkvQ8{a, l, L.bqkv}, st);
     if (e != cudaSuccess) return e;
+    StepArgs ao = a;
+    ao.o_hi = w.q8_ah;
+    ao.o_lo = w.q8_al;
     k_attn_decode<<<dim3(c.cfg.n_kv_head, c.ws.att_max_chunks, a.B), kThreads, 0, st>>>(
-        a, l, c.ws.att_part, c.ws.att_count, c.ws.att_max_chunks);
-    e = bgemm<MT, 1, 4>(c, c.ws.o, a.B, nq, L.wo, H, EpiResidualQ8{a.x, H}, st);
-    if (e != cudaSuccess) return e;
-    k_rmsnorm_rows<<<a.B, kThreads, 0, st>>>(a.x, H, L.ffn_norm, a.eps, c.ws.xn);
-    e = bgemm<MT, 1, 1>(c, c.ws.xn, a.B, H, L.wgu, 2 * I, EpiSwigluQ8{c.ws.mlp, I}, st);
-    if (e != cudaSuccess) return e;
-    return bgemm<MT, 1, 4>(c, c.ws.mlp, a.B, I, L.wd, H, EpiResidualQ8{a.x, H}, st);
+        ao, l, c.ws.att_part, c.ws.att_count, c.ws.att_max_chunks);
+    return o_ffn_q8<MT>(c, l, a.x, a.B, st);
 }
 
+// Final RMSNorm (adding `nparts` pending down partials to x first) and the
+// tied LM head + argmax on B <= 32 rows.
 template <int MT>
-cudaError_t lm_head_q8(Ctx& c, const float* xin, int B, float* logits, int* ids, float* hidden, bool decode,
+cudaError_t lm_head_q8(Ctx& c, float* x, int nparts, int B, float* logits, int* ids, float* hidden, bool decode,
                        cudaStream_t st) {
-    k_rmsnorm_rows<<<B, kThreads, 0, st>>>(xin, c.cfg.hidden, c.final_norm, c.cfg.rms_eps, hidden);
+    const int H = c.cfg.hidden;
+    Workspace& w = c.ws;
+    k_norm_split<<<B, kThreads, 0, st>>>(x, w.q8_part, nparts, (size_t)c.max_rows_q8 * H, H, c.final_norm,
+                                         c.cfg.rms_eps, hidden, w.q8_ah, w.q8_al);
     EpiLmQ8 e{};
     e.logits = logits;
     e.V = c.cfg.vocab;
     e.B = B;
-    e.am_val = c.ws.lm_val;
-    e.am_idx = c.ws.lm_idx;
-    e.count = c.ws.am_count;
+    e.am_val = w.lm_val;
+    e.am_idx = w.lm_idx;
+    e.count = w.am_count;
     e.ids = ids;
     e.decode = decode ? 1 : 0;
     e.tok = c.ds.tok;
@@ -725,7 +820,7 @@ cudaError_t lm_head_q8(Ctx& c, const float* xin, int B, float* logits, int* ids,
         e.bv[k] = -INFINITY;
         e.bi[k] = 0x7fffffff;
     }
-    return bgemm<MT, kLmNtw, 1>(c, hidden, B, c.cfg.hidden, c.embed, c.cfg.vocab, e, st);
+    return bgemm<MT, kLmNtw, 1>(c, w.q8_ah, w.q8_al, B, H, H, c.embed, c.cfg.vocab, e, st);
 }
 
 template <int MT>
@@ -736,19 +831,19 @@ cudaError_t decode_q8(Ctx& c, int B, bool want_logits, cudaStream_t st) {
         cudaError_t e = layer_q8<MT>(c, a, l, st);
         if (e != cudaSuccess) return e;
     }
-    return lm_head_q8<MT>(c, c.ws.x, B, want_logits ? c.ws.logits : nullptr, nullptr, c.ws.hidden, true, st);
+    return lm_head_q8<MT>(c, c.ws.x, down_chunks(c), B, want_logits ? c.ws.logits : nullptr, nullptr, c.ws.hidden,
+                          true, st);
 }
 
 template <int MT>
 cudaError_t rows_o_ffn_q8(Ctx& c, int l, float* x, const float* o, int B, cudaStream_t st) {
-    const DevLayer& L = c.layers[l];
-    const int H = c.cfg.hidden, I = c.cfg.intermediate, nq = c.cfg.n_head * kHd;
-    cudaError_t e = bgemm<MT, 1, 4>(c, o, B, nq, L.wo, H, EpiResidualQ8{x, H}, st);
+    const int H = c.cfg.hidden, nq = c.cfg.n_head * kHd;
+    k_split_rows<<<(B * nq + kThreads - 1) / kThreads, kThreads, 0, st>>>(o, B * nq, c.ws.q8_ah, c.ws.q8_al);
+    cudaError_t e = o_ffn_q8<MT>(c, l, x, B, st);
     if (e != cudaSuccess) return e;
-    k_rmsnorm_rows<<<B, kThreads, 0, st>>>(x, H, L.ffn_norm, c.cfg.rms_eps, c.ws.xn);
-    e = bgemm<MT, 1, 1>(c, c.ws.xn, B, H, L.wgu, 2 * I, EpiSwigluQ8{c.ws.mlp, I}, st);
-    if (e != cudaSuccess) return e;
-    return bgemm<MT, 1, 4>(c, c.ws.mlp, B, I, L.wd, H, EpiResidualQ8{x, H}, st);
+    k_add_parts<<<(B * H + kThreads - 1) / kThreads, kThreads, 0, st>>>(x, c.ws.q8_part, down_chunks(c),
+                                                                       (size_t)c.max_rows_q8 * H, B * H);
+    return cudaGetLastError();
 }
 
 template <int NB>
@@ -802,8 +897,9 @@ cudaError_t enqueue_lm_head(Ctx& c, const float* xin, int B, float* logits, int*
             float* lg = logits ? logits + (size_t)b0 * V : nullptr;
             int* ig = ids ? ids + b0 : nullptr;
             float* hg = c.ws.hidden + (size_t)b0 * H;
-            cudaError_t e = nb <= 16 ? lm_head_q8<1>(c, xg, nb, lg, ig, hg, decode, st)
-                                     : lm_head_q8<2>(c, xg, nb, lg, ig, hg, decode, st);
+            float* xw = const_cast<float*>(xg);
+            cudaError_t e = nb <= 16 ? lm_head_q8<1>(c, xw, 0, nb, lg, ig, hg, decode, st)
+                                     : lm_head_q8<2>(c, xw, 0, nb, lg, ig, hg, decode, st);
             if (e != cudaSuccess) return e;
         }
         return cudaSuccess;
@@ -867,9 +963,10 @@ cudaError_t decode_set_smem_limits(int max_bytes) {
         e = cudaFuncSetAttribute(bg::k_bgemm_q8<MT, NTW, KS, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                                  (int)bg::smem_bytes(MT));
 #define Q2_BG_MT(MT)                  \
-    Q2_BG(MT, 1, 4, EpiQkvQ8)         \
-    Q2_BG(MT, 1, 4, EpiResidualQ8)    \
-    Q2_BG(MT, 1, 1, EpiSwigluQ8)      \
+    Q2_BG(MT, 1, 8, EpiQkvQ8)         \
+    Q2_BG(MT, 1, 8, EpiResidualQ8)    \
+    Q2_BG(MT, 4, 4, EpiSwigluQ8)      \
+    Q2_BG(MT, 1, 8, EpiPartQ8)        \
     Q2_BG(MT, kLmNtw, 1, EpiLmQ8)
     Q2_BG_MT(1) Q2_BG_MT(2)
 #undef Q2_BG_MT
