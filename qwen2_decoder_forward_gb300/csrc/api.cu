@@ -182,7 +182,8 @@ int setup_workspace(Ctx& c) {
         A(&w.q8_al, rq * std::max(H, nq));
         A(&w.q8_mh, rq * I);
         A(&w.q8_ml, rq * I);
-        A(&w.q8_part, (size_t)((I + 1023) / 1024) * rq * H);
+        A(&w.q8_part, (size_t)((I + kQ8DownKc - 1) / kQ8DownKc) * rq * H);
+        A(&w.q8_cnt, (size_t)(H + 63) / 64);
     }
     if (g.prefill_mode == QWEN2_PREFILL_TENSOR) {
         A(&w.xn_h, (size_t)R * H);

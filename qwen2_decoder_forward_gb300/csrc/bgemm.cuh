@@ -21,9 +21,13 @@
 // index).  A CTA of 8 warps owns kGroups x NTW x 8 consecutive weight rows;
 // warp w takes n-tile group w % kGroups and every KS-th 32-block of the
 // chunk (the KS warps of a group add their partials in a fixed order at the
-// end).  The chunk's activation rows are brought into shared memory with
-// one bulk copy per row (hi and lo) on an mbarrier; weights stream from
-// global memory one block ahead of the MMAs.
+// end).  Each warp issues the loads of its first kDepth weight blocks before
+// anything else and keeps kDepth blocks in flight, so the weight stream's
+// latency is paid about once per CTA rather than once per block.  The
+// chunk's activation rows reach shared memory through a prologue: either one
+// bulk copy per row (hi and lo, issued by the 32 lanes of warp 0 on one
+// mbarrier), or an RMSNorm of f32 rows computed in the CTA (one warp per
+// row), which saves the separate normalisation kernel.
 #pragma once
 
 #include "common.cuh"
@@ -35,11 +39,15 @@ namespace bg {
 constexpr int kThreads = 256;
 constexpr int kWarps = 8;
 constexpr int kKc = 1024;   // largest k chunk
-constexpr int kPad = 32;    // row padding in halves (64 bytes: conflict-free 16-byte fragment loads)
+constexpr int kDepth = 4;   // weight blocks in flight per warp
 constexpr unsigned long long kWaitNs = 2000000000ull;
 
-__host__ __device__ constexpr size_t smem_bytes(int mt) {
-    return (size_t)2 * (mt * 16) * (kKc + kPad) * 2 + 16;
+// Shared-memory row stride (halves) of a k chunk of kc columns: kc rounded
+// up to 64, plus 32, so consecutive rows sit 64 bytes apart modulo 128 and
+// the 16-byte fragment loads of 8 rows x 4 lanes are conflict-free.
+__host__ __device__ constexpr int row_ld(int kc) { return (kc + 63) / 64 * 64 + 32; }
+__host__ __device__ constexpr size_t smem_bytes(int mt, int kc) {
+    return (size_t)2 * (mt * 16) * row_ld(kc) * 2 + 16;
 }
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -73,10 +81,23 @@ __device__ __forceinline__ void split_h(float v, __half& hi, __half& lo) {
     lo = __float2half_rn(v - __half2float(hi));
 }
 
+// One 32-block of NTW n-tiles as this lane's fragment: 8 int8 values of
+// row n0 + 8t + gi, and the raw f16 scales of rows n0 + 8t + 2ti and
+// n0 + 8t + 2ti + 1 (converted at use, so the loads stay in flight).
 struct WeightBlock {
     uint2 q;
-    float d0, d1;
+    uint32_t d0, d1;
 };
+
+__device__ __forceinline__ uint32_t ld_stream_u16(const void* p) {
+    unsigned short v;
+    asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float h_bits_to_f(uint32_t bits) {
+    return __half2float(__ushort_as_half((unsigned short)bits));
+}
 
 template <int NTW>
 __device__ __forceinline__ void load_block(const int8_t* __restrict__ Q, const __half* __restrict__ D, int N, int K,
@@ -85,26 +106,134 @@ __device__ __forceinline__ void load_block(const int8_t* __restrict__ Q, const _
     for (int t = 0; t < NTW; ++t) {
         const int row = n0 + t * 8 + gi, rs = n0 + t * 8 + 2 * ti;
         w[t].q = row < N ? ld_stream_u2(Q + (size_t)row * K + kg + 8 * ti) : make_uint2(0u, 0u);
-        w[t].d0 = rs < N ? __half2float(D[(size_t)rs * (K / 32) + kg / 32]) : 0.f;
-        w[t].d1 = rs + 1 < N ? __half2float(D[(size_t)(rs + 1) * (K / 32) + kg / 32]) : 0.f;
+        w[t].d0 = rs < N ? ld_stream_u16(D + (size_t)rs * (K / 32) + kg / 32) : 0u;
+        w[t].d1 = rs + 1 < N ? ld_stream_u16(D + (size_t)(rs + 1) * (K / 32) + kg / 32) : 0u;
     }
 }
 
+// ---- prologues: the chunk's activation rows into shared memory -------------
+// stage(ah, al, ld, rows, K, kc0, kc, bar, err): rows 0..rows-1 of columns
+// [kc0, kc0 + kc) as f16 hi / lo, row stride ld halves.  Returns false if a
+// bounded wait gave up.  Every thread of the CTA calls it.
+
+// Rows already split into hi / lo in global memory: one bulk copy per row
+// and half, issued by the lanes of warp 0.
+struct ProCopy {
+    const __half* hi;
+    const __half* lo;
+    __device__ __forceinline__ bool stage(__half* ah, __half* al, int ld, int rows, int K, int kc0, int kc,
+                                          uint64_t* bar) const {
+        using namespace sm100;
+        const int tid = threadIdx.x;
+        const unsigned row_bytes = (unsigned)kc * 2;
+        if (tid == 0) mbar_expect_tx(bar, 2u * row_bytes * (unsigned)rows);
+        __syncwarp();
+        if (tid < rows) {
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                    smem_addr(ah + tid * ld)),
+                "l"(hi + (size_t)tid * K + kc0), "r"(row_bytes), "r"(smem_addr(bar))
+                : "memory");
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                    smem_addr(al + tid * ld)),
+                "l"(lo + (size_t)tid * K + kc0), "r"(row_bytes), "r"(smem_addr(bar))
+                : "memory");
+        }
+        return mbar_wait(bar, 0, global_ns() + kWaitNs);
+    }
+};
+
+// RMSNorm of f32 rows x (nnterp encyclopedia "qwen2": x / sqrt(mean x^2 +
+// eps) * w), computed here and split into hi / lo; the chunk must be the
+// whole row (kc0 = 0, kc = K <= kKc, K a multiple of 4).  Warp w takes rows
+// w, w + 8, w + 16, w + 24 two at a time, with all of a pair's loads issued
+// together (one round trip per pair).  If `out` is set, the normalised f32
+// rows are also written there (by the CTA with blockIdx (0, 0)).
+struct ProNorm {
+    const float* x;
+    const float* w;
+    float eps;
+    float* out;
+
+    __device__ __forceinline__ void emit(__half* ah, __half* al, int ld, int r, int K, int j, float4 v, float sc,
+                                         bool write_out) const {
+        const float4 g = *reinterpret_cast<const float4*>(w + j);
+        const float n0 = __fmul_rn(__fmul_rn(v.x, sc), g.x), n1 = __fmul_rn(__fmul_rn(v.y, sc), g.y);
+        const float n2 = __fmul_rn(__fmul_rn(v.z, sc), g.z), n3 = __fmul_rn(__fmul_rn(v.w, sc), g.w);
+        if (write_out) *reinterpret_cast<float4*>(out + (size_t)r * K + j) = make_float4(n0, n1, n2, n3);
+        __half h[4], l[4];
+        split_h(n0, h[0], l[0]);
+        split_h(n1, h[1], l[1]);
+        split_h(n2, h[2], l[2]);
+        split_h(n3, h[3], l[3]);
+        *reinterpret_cast<uint2*>(ah + r * ld + j) = *reinterpret_cast<const uint2*>(h);
+        *reinterpret_cast<uint2*>(al + r * ld + j) = *reinterpret_cast<const uint2*>(l);
+    }
+
+    __device__ __forceinline__ bool stage(__half* ah, __half* al, int ld, int rows, int K, int, int,
+                                          uint64_t*) const {
+        constexpr int kSteps = kKc / 128;
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        const bool write_out = out && blockIdx.x == 0 && blockIdx.y == 0;
+        for (int r0 = warp; r0 < rows; r0 += 2 * kWarps) {
+            const int r1 = r0 + kWarps;
+            const bool has1 = r1 < rows;
+            float4 v0[kSteps], v1[kSteps];
+            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < kSteps; ++i) {
+                const int j = 4 * lane + 128 * i;
+                v0[i] = j < K ? *reinterpret_cast<const float4*>(x + (size_t)r0 * K + j) : z;
+                v1[i] = (j < K && has1) ? *reinterpret_cast<const float4*>(x + (size_t)r1 * K + j) : z;
+            }
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+            for (int i = 0; i < kSteps; ++i) {
+                s0 = fmaf(v0[i].x, v0[i].x, s0); s0 = fmaf(v0[i].y, v0[i].y, s0);
+                s0 = fmaf(v0[i].z, v0[i].z, s0); s0 = fmaf(v0[i].w, v0[i].w, s0);
+                s1 = fmaf(v1[i].x, v1[i].x, s1); s1 = fmaf(v1[i].y, v1[i].y, s1);
+                s1 = fmaf(v1[i].z, v1[i].z, s1); s1 = fmaf(v1[i].w, v1[i].w, s1);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+                s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+            }
+            const float sc0 = 1.0f / sqrtf(s0 / (float)K + eps);
+            const float sc1 = 1.0f / sqrtf(s1 / (float)K + eps);
+#pragma unroll
+            for (int i = 0; i < kSteps; ++i) {
+                const int j = 4 * lane + 128 * i;
+                if (j < K) {
+                    emit(ah, al, ld, r0, K, j, v0[i], sc0, write_out);
+                    if (has1) emit(ah, al, ld, r1, K, j, v1[i], sc1, write_out);
+                }
+            }
+        }
+        __syncthreads();
+        return true;
+    }
+};
+
 // Epi::pair(b, n, v0, v1, chunk): outputs (b, n) and (b, n + 1), n even,
-// partial over k chunk `chunk`.  Epi::finish(err): once per CTA, all threads.
-template <int MT, int NTW, int KS, class Epi>
-__global__ void __launch_bounds__(kThreads) k_bgemm_q8(const __half* __restrict__ Ah, const __half* __restrict__ Al,
-                                                       int B, int K, int kc_len, const int8_t* __restrict__ Q,
-                                                       const __half* __restrict__ D, int N, Epi epi, int* err) {
+// partial over k chunk `chunk`.  Epi::finish(): once per CTA, all threads,
+// after every pair of the CTA.
+// Grid (ceil(N / rows_cta), ceil(K / kc_len)), kThreads threads, dynamic
+// shared memory smem_bytes(MT, kc_len); kc_len a multiple of 32, <= kKc.
+template <int MT, int NTW, int KS, class Epi, class Pro>
+__global__ void __launch_bounds__(kThreads) k_bgemm_q8(Pro pro, int B, int K, int kc_len,
+                                                       const int8_t* __restrict__ Q, const __half* __restrict__ D,
+                                                       int N, Epi epi, int* err) {
     using namespace sm100;
     extern __shared__ __align__(16) unsigned char smem[];
     constexpr int kRows = MT * 16;
-    constexpr int kLd = kKc + kPad;
     constexpr int kGroups = kWarps / KS;
     static_assert(kWarps % KS == 0, "KS divides the warps");
+    const int ld = row_ld(kc_len);
     __half* ah = reinterpret_cast<__half*>(smem);
-    __half* al = ah + kRows * kLd;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(al + kRows * kLd);
+    __half* al = ah + kRows * ld;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(al + kRows * ld);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gi = lane >> 2, ti = lane & 3;
     const int grp = warp % kGroups, ks = warp / kGroups;
@@ -112,69 +241,66 @@ __global__ void __launch_bounds__(kThreads) k_bgemm_q8(const __half* __restrict_
     const int kc0 = blockIdx.y * kc_len;
     const int kc = min(kc_len, K - kc0);
     const int Bc = min(B, kRows);
+    const int nb = kc / 32;
 
-    // Stage rows 0..Bc-1 of the chunk (hi and lo); rows past B are never
-    // read for a kept output (each MMA row is its own output row).
+    // The first kDepth weight blocks of this warp go out before anything
+    // waits.
+    WeightBlock wq[kDepth][NTW];
+#pragma unroll
+    for (int i = 0; i < kDepth; ++i)
+        if (ks + i * KS < nb) load_block<NTW>(Q, D, N, K, n0, gi, ti, kc0 + (ks + i * KS) * 32, wq[i]);
+
     if (tid == 0) {
         mbar_init(bar, 1);
         mbar_init_fence();
     }
     __syncthreads();
-    if (tid == 0) {
-        const unsigned row_bytes = (unsigned)kc * 2;
-        mbar_expect_tx(bar, 2u * row_bytes * (unsigned)Bc);
-        for (int r = 0; r < Bc; ++r) {
-            asm volatile(
-                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                    smem_addr(ah + r * kLd)),
-                "l"(Ah + (size_t)r * K + kc0), "r"(row_bytes), "r"(smem_addr(bar))
-                : "memory");
-            asm volatile(
-                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                    smem_addr(al + r * kLd)),
-                "l"(Al + (size_t)r * K + kc0), "r"(row_bytes), "r"(smem_addr(bar))
-                : "memory");
-        }
-    }
+    // Rows past B are never read for a kept output (each MMA row is its own
+    // output row).
+    const bool staged = pro.stage(ah, al, ld, Bc, K, kc0, kc, bar);
+    if (!staged && lane == 0) raise_guard(err, kGuardTimeout);
+
     float acc[MT][NTW][4];
 #pragma unroll
     for (int m = 0; m < MT; ++m)
 #pragma unroll
         for (int t = 0; t < NTW; ++t) acc[m][t][0] = acc[m][t][1] = acc[m][t][2] = acc[m][t][3] = 0.f;
-    const int nb = kc / 32;
-    WeightBlock wc[NTW];
-    if (ks < nb) load_block<NTW>(Q, D, N, K, n0, gi, ti, kc0 + ks * 32, wc);
-    const bool staged = mbar_wait(bar, 0, global_ns() + kWaitNs);
-    if (!staged && lane == 0) raise_guard(err, kGuardTimeout);
     if (staged) {
-        for (int kb = ks; kb < nb; kb += KS) {
-            WeightBlock wn[NTW];
-            if (kb + KS < nb) load_block<NTW>(Q, D, N, K, n0, gi, ti, kc0 + (kb + KS) * 32, wn);
+        for (int kb0 = ks; kb0 < nb; kb0 += kDepth * KS) {
 #pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                const __half* hr = ah + (m * 16 + gi) * kLd + kb * 32 + 8 * ti;
-                const __half* lr = al + (m * 16 + gi) * kLd + kb * 32 + 8 * ti;
-                const uint4 h0 = *reinterpret_cast<const uint4*>(hr);
-                const uint4 h1 = *reinterpret_cast<const uint4*>(hr + 8 * kLd);
-                const uint4 l0 = *reinterpret_cast<const uint4*>(lr);
-                const uint4 l1 = *reinterpret_cast<const uint4*>(lr + 8 * kLd);
+            for (int i = 0; i < kDepth; ++i) {
+                const int kb = kb0 + i * KS;
+                if (kb < nb) {
 #pragma unroll
-                for (int t = 0; t < NTW; ++t) {
-                    const uint32_t b00 = i8x2_to_h2(wc[t].q.x, 0x4140u), b01 = i8x2_to_h2(wc[t].q.x, 0x4342u);
-                    const uint32_t b10 = i8x2_to_h2(wc[t].q.y, 0x4140u), b11 = i8x2_to_h2(wc[t].q.y, 0x4342u);
-                    float p[4] = {0.f, 0.f, 0.f, 0.f};
-                    mma16816(p, h0.x, h1.x, h0.y, h1.y, b00, b01);
-                    mma16816(p, l0.x, l1.x, l0.y, l1.y, b00, b01);
-                    mma16816(p, h0.z, h1.z, h0.w, h1.w, b10, b11);
-                    mma16816(p, l0.z, l1.z, l0.w, l1.w, b10, b11);
-                    acc[m][t][0] = fmaf(wc[t].d0, p[0], acc[m][t][0]);
-                    acc[m][t][1] = fmaf(wc[t].d1, p[1], acc[m][t][1]);
-                    acc[m][t][2] = fmaf(wc[t].d0, p[2], acc[m][t][2]);
-                    acc[m][t][3] = fmaf(wc[t].d1, p[3], acc[m][t][3]);
+                    for (int m = 0; m < MT; ++m) {
+                        const __half* hr = ah + (m * 16 + gi) * ld + kb * 32 + 8 * ti;
+                        const __half* lr = al + (m * 16 + gi) * ld + kb * 32 + 8 * ti;
+                        const uint4 h0 = *reinterpret_cast<const uint4*>(hr);
+                        const uint4 h1 = *reinterpret_cast<const uint4*>(hr + 8 * ld);
+                        const uint4 l0 = *reinterpret_cast<const uint4*>(lr);
+                        const uint4 l1 = *reinterpret_cast<const uint4*>(lr + 8 * ld);
+#pragma unroll
+                        for (int t = 0; t < NTW; ++t) {
+                            const WeightBlock& wb = wq[i][t];
+                            const uint32_t b00 = i8x2_to_h2(wb.q.x, 0x4140u), b01 = i8x2_to_h2(wb.q.x, 0x4342u);
+                            const uint32_t b10 = i8x2_to_h2(wb.q.y, 0x4140u), b11 = i8x2_to_h2(wb.q.y, 0x4342u);
+                            float p[4] = {0.f, 0.f, 0.f, 0.f};
+                            mma16816(p, h0.x, h1.x, h0.y, h1.y, b00, b01);
+                            mma16816(p, l0.x, l1.x, l0.y, l1.y, b00, b01);
+                            mma16816(p, h0.z, h1.z, h0.w, h1.w, b10, b11);
+                            mma16816(p, l0.z, l1.z, l0.w, l1.w, b10, b11);
+                            const float d0 = h_bits_to_f(wb.d0), d1 = h_bits_to_f(wb.d1);
+                            acc[m][t][0] = fmaf(d0, p[0], acc[m][t][0]);
+                            acc[m][t][1] = fmaf(d1, p[1], acc[m][t][1]);
+                            acc[m][t][2] = fmaf(d0, p[2], acc[m][t][2]);
+                            acc[m][t][3] = fmaf(d1, p[3], acc[m][t][3]);
+                        }
+                    }
+                    // Refill this slot with the block kDepth steps ahead.
+                    if (kb + kDepth * KS < nb)
+                        load_block<NTW>(Q, D, N, K, n0, gi, ti, kc0 + (kb + kDepth * KS) * 32, wq[i]);
                 }
             }
-#pragma unroll
-            for (int t = 0; t < NTW; ++t) wc[t] = wn[t];
         }
     }
     if (KS > 1) {

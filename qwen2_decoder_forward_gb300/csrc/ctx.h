@@ -37,6 +37,9 @@ struct DevLayer {
     const float* ffn_norm = nullptr;
 };
 
+// Columns of k per CTA of the Q8_0 down product (split-k chunk).
+constexpr int kQ8DownKc = 448;
+
 struct Workspace {
     float* x = nullptr;        // [rows][H] residual stream
     float* xn = nullptr;       // [rows][max(H, I)] normed rows (unfused / prefill)
@@ -55,7 +58,8 @@ struct Workspace {
     __half* q8_al = nullptr;   //   and lo
     __half* q8_mh = nullptr;   // SiLU(gate) * up as f16 hi [32][I]
     __half* q8_ml = nullptr;   //   and lo
-    float* q8_part = nullptr;  // down-product partials [ceil(I/1024)][32][H]
+    float* q8_part = nullptr;  // down-product partials [ceil(I/kQ8DownKc)][32][H]
+    int* q8_cnt = nullptr;     // down-product arrival counters, one per 64 output rows
     float* hidden = nullptr;   // [rows_out][H] final_norm_output
     float* logits = nullptr;   // [max_seqs][V] decode logits staging
     int* rows_tok = nullptr;   // prefill: per-row token

@@ -7,6 +7,7 @@
 #include "attn.cuh"
 #include "bgemm.cuh"
 #include "ctx.h"
+#include "flash_decode.cuh"
 #include "rowdot.cuh"
 
 namespace qwen2 {
@@ -473,16 +474,6 @@ __global__ void __launch_bounds__(kThreads) k_split_rows(const float* __restrict
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) bg::split_h(src[i], hi[i], lo[i]);
 }
 
-// x[b] += sum_s part[s][b] in s order.
-__global__ void __launch_bounds__(kThreads) k_add_parts(float* __restrict__ x, const float* __restrict__ part,
-                                                        int nparts, size_t part_stride, int n) {
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
-        float v = x[i];
-        for (int s = 0; s < nparts; ++s) v += part[(size_t)s * part_stride + i];
-        x[i] = v;
-    }
-}
-
 struct EpiQkvQ8 {
     StepArgs a;
     int layer;
@@ -506,15 +497,39 @@ struct EpiResidualQ8 {
     __device__ __forceinline__ void finish() {}
 };
 
-// Partial sums of k chunk `chunk`: part[chunk][b][n].
-struct EpiPartQ8 {
+// Down product split over k: the partial sums of k chunk `chunk` go to
+// part[chunk][b][n]; the last CTA of a row group to finish (all gridDim.y
+// chunks written) adds them to the residual x in chunk order.
+struct EpiDownQ8 {
     float* part;
-    size_t stride;
-    int N;
+    size_t stride;  // floats between chunks
+    int N;          // output rows (hidden)
+    int B;
+    int rows_cta;
+    float* x;
+    int* count;     // [gridDim.x] arrival counters, zero between launches
     __device__ __forceinline__ void pair(int b, int n, float v0, float v1, int chunk) {
         *reinterpret_cast<float2*>(part + chunk * stride + (size_t)b * N + n) = make_float2(v0, v1);
     }
-    __device__ __forceinline__ void finish() {}
+    __device__ void finish() {
+        __shared__ int last_s;
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) last_s = atomicAdd(&count[blockIdx.x], 1) == (int)gridDim.y - 1;
+        __syncthreads();
+        if (!last_s) return;
+        __threadfence();
+        const int n0 = blockIdx.x * rows_cta;
+        const int nr = min(rows_cta, N - n0);
+        for (int e = threadIdx.x; e < B * nr; e += blockDim.x) {
+            const int b = e / nr;
+            const size_t i = (size_t)b * N + n0 + (e - b * nr);
+            float v = x[i];
+            for (int s = 0; s < (int)gridDim.y; ++s) v += __ldcg(part + s * stride + i);
+            x[i] = v;
+        }
+        if (threadIdx.x == 0) count[blockIdx.x] = 0;
+    }
 };
 
 // Packed rows (2j, 2j+1) = (gate j, up j): m[b][j] = SiLU(gate) * up, as
@@ -743,35 +758,73 @@ cudaError_t decode_nb(Ctx& c, int B, bool want_logits, cudaStream_t st) {
 
 // ---- Q8_0 weights: the batched tensor-core product for any B <= 32 ---------
 // Shapes: QKV and o_proj 8 weight rows per CTA (8 warps split k); gate/up
-// 64 rows per CTA; down 8 rows per CTA and k split into chunks of 1024
-// whose partials the next RMSNorm adds; LM head 256 rows per CTA.
-template <int MT, int NTW, int KS, class Epi>
-cudaError_t bgemm(const Ctx& c, const __half* ah, const __half* al, int B, int K, int kc_len, const DevMat& W, int N,
-                  const Epi& e, cudaStream_t st) {
+// 64 rows per CTA; down 64 rows per CTA with k cut into chunks of
+// kQ8DownKc columns (one wave of about 150 CTAs at the 0.5B shape), reduced
+// into the residual by the last CTA of each row group; LM head 256 rows per
+// CTA.  QKV and gate/up normalise their input rows themselves.
+template <int MT, int NTW, int KS, class Epi, class Pro>
+cudaError_t bgemm(const Ctx& c, const Pro& pro, int B, int K, int kc_len, const DevMat& W, int N, const Epi& e,
+                  cudaStream_t st) {
     constexpr int rows_cta = (bg::kWarps / KS) * NTW * 8;
     const dim3 grid((N + rows_cta - 1) / rows_cta, (K + kc_len - 1) / kc_len);
-    bg::k_bgemm_q8<MT, NTW, KS, Epi><<<grid, bg::kThreads, bg::smem_bytes(MT), st>>>(ah, al, B, K, kc_len, W.q, W.d,
-                                                                                     N, e, c.err);
+    bg::k_bgemm_q8<MT, NTW, KS, Epi, Pro><<<grid, bg::kThreads, bg::smem_bytes(MT, kc_len), st>>>(
+        pro, B, K, kc_len, W.q, W.d, N, e, c.err);
     return cudaGetLastError();
 }
 
-int down_chunks(const Ctx& c) { return (c.cfg.intermediate + bg::kKc - 1) / bg::kKc; }
+constexpr int kDownNtw = 2, kDownKs = 2;
+constexpr int kDownRows = (bg::kWarps / kDownKs) * kDownNtw * 8;
 
-// The steps of one layer after the attention: o_proj + residual, RMSNorm,
-// gate/up + SwiGLU, down as split-k partials (added by the caller's next
-// RMSNorm or by k_add_parts).
+// The steps of one layer after the attention: o_proj + residual, RMSNorm +
+// gate/up + SwiGLU, down + residual (split over k, reduced in-kernel).
 template <int MT>
 cudaError_t o_ffn_q8(Ctx& c, int l, float* x, int B, cudaStream_t st) {
     const DevLayer& L = c.layers[l];
     const int H = c.cfg.hidden, I = c.cfg.intermediate, nq = c.cfg.n_head * kHd;
     Workspace& w = c.ws;
-    cudaError_t e = bgemm<MT, 1, 8>(c, w.q8_ah, w.q8_al, B, nq, nq, L.wo, H, EpiResidualQ8{x, H}, st);
+    cudaError_t e = bgemm<MT, 1, 8>(c, bg::ProCopy{w.q8_ah, w.q8_al}, B, nq, nq, L.wo, H, EpiResidualQ8{x, H}, st);
     if (e != cudaSuccess) return e;
-    k_norm_split<<<B, kThreads, 0, st>>>(x, nullptr, 0, 0, H, L.ffn_norm, c.cfg.rms_eps, nullptr, w.q8_ah, w.q8_al);
-    e = bgemm<MT, 4, 4>(c, w.q8_ah, w.q8_al, B, H, H, L.wgu, 2 * I, EpiSwigluQ8{w.q8_mh, w.q8_ml, I}, st);
+    e = bgemm<MT, 4, 4>(c, bg::ProNorm{x, L.ffn_norm, c.cfg.rms_eps, nullptr}, B, H, H, L.wgu, 2 * I,
+                        EpiSwigluQ8{w.q8_mh, w.q8_ml, I}, st);
     if (e != cudaSuccess) return e;
-    return bgemm<MT, 1, 8>(c, w.q8_mh, w.q8_ml, B, I, bg::kKc, L.wd, H,
-                           EpiPartQ8{w.q8_part, (size_t)c.max_rows_q8 * H, H}, st);
+    EpiDownQ8 ed{w.q8_part, (size_t)c.max_rows_q8 * H, H, B, kDownRows, x, w.q8_cnt};
+    return bgemm<MT, kDownNtw, kDownKs>(c, bg::ProCopy{w.q8_mh, w.q8_ml}, B, I, kQ8DownKc, L.wd, H, ed, st);
+}
+
+// Batched decode attention of the Q8_0 path: the persistent flash-decoding
+// kernel (any mix of positions, up to 32 rows, n_ctx <= 4096, group <= 8),
+// else the split-K kernel.
+cudaError_t attn_batched(const Ctx& c, const StepArgs& a, int l, cudaStream_t st) {
+    const int group = a.nh / a.nkv;
+    if (a.B > fd::kMaxRows || c.ws.att_max_chunks > fd::kMaxChunks || group > 8) {
+        k_attn_decode<<<dim3(c.cfg.n_kv_head, c.ws.att_max_chunks, a.B), kThreads, 0, st>>>(
+            a, l, c.ws.att_part, c.ws.att_count, c.ws.att_max_chunks);
+        return cudaGetLastError();
+    }
+    fd::Args f;
+    f.q = a.q;
+    f.kv = a.kv;
+    f.pos = a.pos;
+    f.slot = a.slot;
+    f.part = c.ws.att_part;
+    f.count = c.ws.att_count;
+    f.o = a.o;
+    f.o_hi = a.o_hi;
+    f.o_lo = a.o_lo;
+    f.err = a.err;
+    f.B = a.B;
+    f.nh = a.nh;
+    f.nkv = a.nkv;
+    f.n_ctx = a.n_ctx;
+    f.L = a.L;
+    f.layer = l;
+    f.max_chunks = c.ws.att_max_chunks;
+    const int grid = 2 * c.n_sm;
+    if (group == 7)
+        k_attn_flash<7><<<grid, fd::kThreads, sizeof(fd::Smem), st>>>(f);
+    else
+        k_attn_flash<8><<<grid, fd::kThreads, sizeof(fd::Smem), st>>>(f);
+    return cudaGetLastError();
 }
 
 template <int MT>
@@ -779,28 +832,25 @@ cudaError_t layer_q8(Ctx& c, const StepArgs& a, int l, cudaStream_t st) {
     const DevLayer& L = c.layers[l];
     const int H = c.cfg.hidden;
     Workspace& w = c.ws;
-    // The previous layer's down partials go into x before its RMSNorm.
-    k_norm_split<<<a.B, kThreads, 0, st>>>(a.x, w.q8_part, l > 0 ? down_chunks(c) : 0, (size_t)c.max_rows_q8 * H, H,
-                                           L.attn_norm, a.eps, nullptr, w.q8_ah, w.q8_al);
-    cudaError_t e = bgemm<MT, 1, 8>(c, w.q8_ah, w.q8_al, a.B, H, H, L.wqkv, c.nqkv, EpiQkvQ8{a, l, L.bqkv}, st);
+    cudaError_t e = bgemm<MT, 1, 8>(c, bg::ProNorm{a.x, L.attn_norm, a.eps, nullptr}, a.B, H, H, L.wqkv, c.nqkv,
+                                    EpiQkvQ8{a, l, L.bqkv}, st);
     if (e != cudaSuccess) return e;
     StepArgs ao = a;
     ao.o_hi = w.q8_ah;
     ao.o_lo = w.q8_al;
-    k_attn_decode<<<dim3(c.cfg.n_kv_head, c.ws.att_max_chunks, a.B), kThreads, 0, st>>>(
-        ao, l, c.ws.att_part, c.ws.att_count, c.ws.att_max_chunks);
+    e = attn_batched(c, ao, l, st);
+    if (e != cudaSuccess) return e;
     return o_ffn_q8<MT>(c, l, a.x, a.B, st);
 }
 
-// Final RMSNorm (adding `nparts` pending down partials to x first) and the
-// tied LM head + argmax on B <= 32 rows.
+// Final RMSNorm and the tied LM head + argmax on B <= 32 rows.
 template <int MT>
-cudaError_t lm_head_q8(Ctx& c, float* x, int nparts, int B, float* logits, int* ids, float* hidden, bool decode,
+cudaError_t lm_head_q8(Ctx& c, float* x, int B, float* logits, int* ids, float* hidden, bool decode,
                        cudaStream_t st) {
     const int H = c.cfg.hidden;
     Workspace& w = c.ws;
-    k_norm_split<<<B, kThreads, 0, st>>>(x, w.q8_part, nparts, (size_t)c.max_rows_q8 * H, H, c.final_norm,
-                                         c.cfg.rms_eps, hidden, w.q8_ah, w.q8_al);
+    k_norm_split<<<B, kThreads, 0, st>>>(x, nullptr, 0, 0, H, c.final_norm, c.cfg.rms_eps, hidden, w.q8_ah,
+                                         w.q8_al);
     EpiLmQ8 e{};
     e.logits = logits;
     e.V = c.cfg.vocab;
@@ -820,7 +870,7 @@ cudaError_t lm_head_q8(Ctx& c, float* x, int nparts, int B, float* logits, int* 
         e.bv[k] = -INFINITY;
         e.bi[k] = 0x7fffffff;
     }
-    return bgemm<MT, kLmNtw, 1>(c, w.q8_ah, w.q8_al, B, H, H, c.embed, c.cfg.vocab, e, st);
+    return bgemm<MT, kLmNtw, 1>(c, bg::ProCopy{w.q8_ah, w.q8_al}, B, H, H, c.embed, c.cfg.vocab, e, st);
 }
 
 template <int MT>
@@ -831,19 +881,14 @@ cudaError_t decode_q8(Ctx& c, int B, bool want_logits, cudaStream_t st) {
         cudaError_t e = layer_q8<MT>(c, a, l, st);
         if (e != cudaSuccess) return e;
     }
-    return lm_head_q8<MT>(c, c.ws.x, down_chunks(c), B, want_logits ? c.ws.logits : nullptr, nullptr, c.ws.hidden,
-                          true, st);
+    return lm_head_q8<MT>(c, c.ws.x, B, want_logits ? c.ws.logits : nullptr, nullptr, c.ws.hidden, true, st);
 }
 
 template <int MT>
 cudaError_t rows_o_ffn_q8(Ctx& c, int l, float* x, const float* o, int B, cudaStream_t st) {
-    const int H = c.cfg.hidden, nq = c.cfg.n_head * kHd;
+    const int nq = c.cfg.n_head * kHd;
     k_split_rows<<<(B * nq + kThreads - 1) / kThreads, kThreads, 0, st>>>(o, B * nq, c.ws.q8_ah, c.ws.q8_al);
-    cudaError_t e = o_ffn_q8<MT>(c, l, x, B, st);
-    if (e != cudaSuccess) return e;
-    k_add_parts<<<(B * H + kThreads - 1) / kThreads, kThreads, 0, st>>>(x, c.ws.q8_part, down_chunks(c),
-                                                                       (size_t)c.max_rows_q8 * H, B * H);
-    return cudaGetLastError();
+    return o_ffn_q8<MT>(c, l, x, B, st);
 }
 
 template <int NB>
@@ -898,8 +943,8 @@ cudaError_t enqueue_lm_head(Ctx& c, const float* xin, int B, float* logits, int*
             int* ig = ids ? ids + b0 : nullptr;
             float* hg = c.ws.hidden + (size_t)b0 * H;
             float* xw = const_cast<float*>(xg);
-            cudaError_t e = nb <= 16 ? lm_head_q8<1>(c, xw, 0, nb, lg, ig, hg, decode, st)
-                                     : lm_head_q8<2>(c, xw, 0, nb, lg, ig, hg, decode, st);
+            cudaError_t e = nb <= 16 ? lm_head_q8<1>(c, xw, nb, lg, ig, hg, decode, st)
+                                     : lm_head_q8<2>(c, xw, nb, lg, ig, hg, decode, st);
             if (e != cudaSuccess) return e;
         }
         return cudaSuccess;
@@ -958,16 +1003,20 @@ cudaError_t decode_set_smem_limits(int max_bytes) {
     Q2_SMEM_NB(1) Q2_SMEM_NB(2) Q2_SMEM_NB(4) Q2_SMEM_NB(8)
 #undef Q2_SMEM_NB
 #undef Q2_SMEM
-#define Q2_BG(MT, NTW, KS, EPI)                                                                             \
-    if (e == cudaSuccess)                                                                                   \
-        e = cudaFuncSetAttribute(bg::k_bgemm_q8<MT, NTW, KS, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                                 (int)bg::smem_bytes(MT));
-#define Q2_BG_MT(MT)                  \
-    Q2_BG(MT, 1, 8, EpiQkvQ8)         \
-    Q2_BG(MT, 1, 8, EpiResidualQ8)    \
-    Q2_BG(MT, 4, 4, EpiSwigluQ8)      \
-    Q2_BG(MT, 1, 8, EpiPartQ8)        \
-    Q2_BG(MT, kLmNtw, 1, EpiLmQ8)
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_attn_flash<7>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(fd::Smem));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_attn_flash<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(fd::Smem));
+#define Q2_BG(MT, NTW, KS, EPI, PRO)                                                                          \
+    if (e == cudaSuccess)                                                                                     \
+        e = cudaFuncSetAttribute(bg::k_bgemm_q8<MT, NTW, KS, EPI, PRO>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                 (int)bg::smem_bytes(MT, bg::kKc));
+#define Q2_BG_MT(MT)                                          \
+    Q2_BG(MT, 1, 8, EpiQkvQ8, bg::ProNorm)                    \
+    Q2_BG(MT, 1, 8, EpiResidualQ8, bg::ProCopy)               \
+    Q2_BG(MT, 4, 4, EpiSwigluQ8, bg::ProNorm)                 \
+    Q2_BG(MT, kDownNtw, kDownKs, EpiDownQ8, bg::ProCopy)      \
+    Q2_BG(MT, kLmNtw, 1, EpiLmQ8, bg::ProCopy)
     Q2_BG_MT(1) Q2_BG_MT(2)
 #undef Q2_BG_MT
 #undef Q2_BG
