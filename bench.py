@@ -424,8 +424,8 @@ def bench_decode(args, wl, shape, weights, rank, world, local):
         launches = 1
     elif q8:
         kname = f"one decode step of {B} sequences: all kernels of the step graph (Q8_0 warp-MMA products, " \
-                "split-K attention)"
-        launches = 1 + shape.n_layer * 7 + 2
+                "TF32 flash-decoding attention + merge)"
+        launches = 1 + shape.n_layer * 6 + 2
     else:
         kname = f"one decode step of {B} sequences: all kernels of the step graph"
         launches = 2 + shape.n_layer * 5

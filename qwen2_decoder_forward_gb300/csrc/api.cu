@@ -12,6 +12,7 @@
 #include "ctx.h"
 #include "persistent.h"
 #include "prefill.h"
+#include "tmap.h"
 
 using namespace qwen2;
 
@@ -312,6 +313,11 @@ int qwen2_create(const qwen2_config* cfg, const qwen2_weights* weights, qwen2_ct
     if (r != QWEN2_OK) return bail(r, "KV cache allocation of " + std::to_string(c.kv_floats * 4) + " bytes failed");
     r = setup_workspace(c);
     if (r != QWEN2_OK) return bail(r, "workspace allocation failed");
+    // The cache as a [rows][64] f32 matrix for the batched decode attention's
+    // tensor copies (64-position tiles); if it cannot be encoded, that
+    // attention falls back to its split-k kernel.
+    if (cfg->head_dim == 64)
+        c.kvmap_ok = encode_rows64_f32(&c.kvmap, c.kv, (uint64_t)(c.kv_floats / 64), 64);
     int max_smem = 0;
     cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, c.device);
     if (decode_set_smem_limits(max_smem) != cudaSuccess || prefill_set_smem_limits() != cudaSuccess)

@@ -140,15 +140,17 @@ struct ProCopy {
                 "l"(lo + (size_t)tid * K + kc0), "r"(row_bytes), "r"(smem_addr(bar))
                 : "memory");
         }
-        return mbar_wait(bar, 0, global_ns() + kWaitNs);
+        return mbar_wait(bar, 0, kWaitNs);
     }
 };
 
 // RMSNorm of f32 rows x (nnterp encyclopedia "qwen2": x / sqrt(mean x^2 +
 // eps) * w), computed here and split into hi / lo; the chunk must be the
-// whole row (kc0 = 0, kc = K <= kKc, K a multiple of 4).  Warp w takes rows
-// w, w + 8, w + 16, w + 24 two at a time, with all of a pair's loads issued
-// together (one round trip per pair).  If `out` is set, the normalised f32
+// whole row (kc0 = 0, kc = K <= kKc, K a multiple of 4).  With W warps,
+// warp w takes rows w and w + W (then w + 2W, w + 3W), a pair at a time
+// with all of the pair's loads issued together: one round trip per pair
+// (a single one for 32 rows and 16 warps); the norm weights are loaded
+// once per warp.  If `out` is set, the normalised f32
 // rows are also written there (by the CTA with blockIdx (0, 0)).
 struct ProNorm {
     const float* x;
@@ -156,9 +158,8 @@ struct ProNorm {
     float eps;
     float* out;
 
-    __device__ __forceinline__ void emit(__half* ah, __half* al, int ld, int r, int K, int j, float4 v, float sc,
-                                         bool write_out) const {
-        const float4 g = *reinterpret_cast<const float4*>(w + j);
+    __device__ __forceinline__ static void emit(__half* ah, __half* al, float* out, int ld, int r, int K, int j,
+                                                float4 v, float4 g, float sc, bool write_out) {
         const float n0 = __fmul_rn(__fmul_rn(v.x, sc), g.x), n1 = __fmul_rn(__fmul_rn(v.y, sc), g.y);
         const float n2 = __fmul_rn(__fmul_rn(v.z, sc), g.z), n3 = __fmul_rn(__fmul_rn(v.w, sc), g.w);
         if (write_out) *reinterpret_cast<float4*>(out + (size_t)r * K + j) = make_float4(n0, n1, n2, n3);
@@ -174,13 +175,19 @@ struct ProNorm {
     __device__ __forceinline__ bool stage(__half* ah, __half* al, int ld, int rows, int K, int, int,
                                           uint64_t*) const {
         constexpr int kSteps = kKc / 128;
-        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
         const bool write_out = out && blockIdx.x == 0 && blockIdx.y == 0;
-        for (int r0 = warp; r0 < rows; r0 += 2 * kWarps) {
-            const int r1 = r0 + kWarps;
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 g[kSteps];
+#pragma unroll
+        for (int i = 0; i < kSteps; ++i) {
+            const int j = 4 * lane + 128 * i;
+            g[i] = j < K ? *reinterpret_cast<const float4*>(w + j) : z;
+        }
+        for (int r0 = warp; r0 < rows; r0 += 2 * nw) {
+            const int r1 = r0 + nw;
             const bool has1 = r1 < rows;
             float4 v0[kSteps], v1[kSteps];
-            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int i = 0; i < kSteps; ++i) {
                 const int j = 4 * lane + 128 * i;
@@ -206,8 +213,8 @@ struct ProNorm {
             for (int i = 0; i < kSteps; ++i) {
                 const int j = 4 * lane + 128 * i;
                 if (j < K) {
-                    emit(ah, al, ld, r0, K, j, v0[i], sc0, write_out);
-                    if (has1) emit(ah, al, ld, r1, K, j, v1[i], sc1, write_out);
+                    emit(ah, al, out, ld, r0, K, j, v0[i], g[i], sc0, write_out);
+                    if (has1) emit(ah, al, out, ld, r1, K, j, v1[i], g[i], sc1, write_out);
                 }
             }
         }
@@ -219,17 +226,22 @@ struct ProNorm {
 // Epi::pair(b, n, v0, v1, chunk): outputs (b, n) and (b, n + 1), n even,
 // partial over k chunk `chunk`.  Epi::finish(): once per CTA, all threads,
 // after every pair of the CTA.
-// Grid (ceil(N / rows_cta), ceil(K / kc_len)), kThreads threads, dynamic
-// shared memory smem_bytes(MT, kc_len); kc_len a multiple of 32, <= kKc.
-template <int MT, int NTW, int KS, class Epi, class Pro>
-__global__ void __launch_bounds__(kThreads) k_bgemm_q8(Pro pro, int B, int K, int kc_len,
-                                                       const int8_t* __restrict__ Q, const __half* __restrict__ D,
-                                                       int N, Epi epi, int* err) {
+// W warps per CTA (32 W threads).  Grid (ceil(N / rows_cta), ceil(K /
+// kc_len)), rows_cta = (W / KS) NTW 8; dynamic shared memory
+// smem_bytes(MT, kc_len); kc_len a multiple of 32, <= kKc.
+// With KS > 1 the KS warps of a group exchange their partial tiles through
+// shared memory and warp ks finishes the tiles j = m NTW + t with j % KS ==
+// ks (sum over the KS partials in ks order, then the epilogue), so the
+// epilogue work is spread over all warps.
+template <int MT, int NTW, int KS, class Epi, class Pro, int W = kWarps, int DEPTH = kDepth>
+__global__ void __launch_bounds__(W * 32) k_bgemm_q8(Pro pro, int B, int K, int kc_len,
+                                                     const int8_t* __restrict__ Q, const __half* __restrict__ D,
+                                                     int N, Epi epi, int* err) {
     using namespace sm100;
     extern __shared__ __align__(16) unsigned char smem[];
     constexpr int kRows = MT * 16;
-    constexpr int kGroups = kWarps / KS;
-    static_assert(kWarps % KS == 0, "KS divides the warps");
+    constexpr int kGroups = W / KS;
+    static_assert(W % KS == 0, "KS divides the warps");
     const int ld = row_ld(kc_len);
     __half* ah = reinterpret_cast<__half*>(smem);
     __half* al = ah + kRows * ld;
@@ -243,11 +255,11 @@ __global__ void __launch_bounds__(kThreads) k_bgemm_q8(Pro pro, int B, int K, in
     const int Bc = min(B, kRows);
     const int nb = kc / 32;
 
-    // The first kDepth weight blocks of this warp go out before anything
+    // The first DEPTH weight blocks of this warp go out before anything
     // waits.
-    WeightBlock wq[kDepth][NTW];
+    WeightBlock wq[DEPTH][NTW];
 #pragma unroll
-    for (int i = 0; i < kDepth; ++i)
+    for (int i = 0; i < DEPTH; ++i)
         if (ks + i * KS < nb) load_block<NTW>(Q, D, N, K, n0, gi, ti, kc0 + (ks + i * KS) * 32, wq[i]);
 
     if (tid == 0) {
@@ -266,11 +278,27 @@ __global__ void __launch_bounds__(kThreads) k_bgemm_q8(Pro pro, int B, int K, in
 #pragma unroll
         for (int t = 0; t < NTW; ++t) acc[m][t][0] = acc[m][t][1] = acc[m][t][2] = acc[m][t][3] = 0.f;
     if (staged) {
-        for (int kb0 = ks; kb0 < nb; kb0 += kDepth * KS) {
+        for (int kb0 = ks; kb0 < nb; kb0 += DEPTH * KS) {
 #pragma unroll
-            for (int i = 0; i < kDepth; ++i) {
+            for (int i = 0; i < DEPTH; ++i) {
                 const int kb = kb0 + i * KS;
                 if (kb < nb) {
+                    // The weights of this block as f16 pairs, once for all m.
+                    uint32_t bw[NTW][4];
+                    float dsc[NTW][2];
+#pragma unroll
+                    for (int t = 0; t < NTW; ++t) {
+                        const WeightBlock& wb = wq[i][t];
+                        bw[t][0] = i8x2_to_h2(wb.q.x, 0x4140u);
+                        bw[t][1] = i8x2_to_h2(wb.q.x, 0x4342u);
+                        bw[t][2] = i8x2_to_h2(wb.q.y, 0x4140u);
+                        bw[t][3] = i8x2_to_h2(wb.q.y, 0x4342u);
+                        dsc[t][0] = h_bits_to_f(wb.d0);
+                        dsc[t][1] = h_bits_to_f(wb.d1);
+                    }
+                    // Refill this slot with the block DEPTH steps ahead.
+                    if (kb + DEPTH * KS < nb)
+                        load_block<NTW>(Q, D, N, K, n0, gi, ti, kc0 + (kb + DEPTH * KS) * 32, wq[i]);
 #pragma unroll
                     for (int m = 0; m < MT; ++m) {
                         const __half* hr = ah + (m * 16 + gi) * ld + kb * 32 + 8 * ti;
@@ -281,67 +309,65 @@ __global__ void __launch_bounds__(kThreads) k_bgemm_q8(Pro pro, int B, int K, in
                         const uint4 l1 = *reinterpret_cast<const uint4*>(lr + 8 * ld);
 #pragma unroll
                         for (int t = 0; t < NTW; ++t) {
-                            const WeightBlock& wb = wq[i][t];
-                            const uint32_t b00 = i8x2_to_h2(wb.q.x, 0x4140u), b01 = i8x2_to_h2(wb.q.x, 0x4342u);
-                            const uint32_t b10 = i8x2_to_h2(wb.q.y, 0x4140u), b11 = i8x2_to_h2(wb.q.y, 0x4342u);
                             float p[4] = {0.f, 0.f, 0.f, 0.f};
-                            mma16816(p, h0.x, h1.x, h0.y, h1.y, b00, b01);
-                            mma16816(p, l0.x, l1.x, l0.y, l1.y, b00, b01);
-                            mma16816(p, h0.z, h1.z, h0.w, h1.w, b10, b11);
-                            mma16816(p, l0.z, l1.z, l0.w, l1.w, b10, b11);
-                            const float d0 = h_bits_to_f(wb.d0), d1 = h_bits_to_f(wb.d1);
-                            acc[m][t][0] = fmaf(d0, p[0], acc[m][t][0]);
-                            acc[m][t][1] = fmaf(d1, p[1], acc[m][t][1]);
-                            acc[m][t][2] = fmaf(d0, p[2], acc[m][t][2]);
-                            acc[m][t][3] = fmaf(d1, p[3], acc[m][t][3]);
+                            mma16816(p, h0.x, h1.x, h0.y, h1.y, bw[t][0], bw[t][1]);
+                            mma16816(p, l0.x, l1.x, l0.y, l1.y, bw[t][0], bw[t][1]);
+                            mma16816(p, h0.z, h1.z, h0.w, h1.w, bw[t][2], bw[t][3]);
+                            mma16816(p, l0.z, l1.z, l0.w, l1.w, bw[t][2], bw[t][3]);
+                            acc[m][t][0] = fmaf(dsc[t][0], p[0], acc[m][t][0]);
+                            acc[m][t][1] = fmaf(dsc[t][1], p[1], acc[m][t][1]);
+                            acc[m][t][2] = fmaf(dsc[t][0], p[2], acc[m][t][2]);
+                            acc[m][t][3] = fmaf(dsc[t][1], p[3], acc[m][t][3]);
                         }
                     }
-                    // Refill this slot with the block kDepth steps ahead.
-                    if (kb + kDepth * KS < nb)
-                        load_block<NTW>(Q, D, N, K, n0, gi, ti, kc0 + (kb + kDepth * KS) * 32, wq[i]);
                 }
             }
         }
     }
-    if (KS > 1) {
-        // Warps ks > 0 hand their partials to warp ks = 0 of the group,
-        // which adds them in ks order.
-        float* red = reinterpret_cast<float*>(smem);
-        constexpr int kVals = MT * NTW * 4;
-        __syncthreads();
-        if (ks > 0) {
-            float* dst = red + (((ks - 1) * kGroups + grp) * 32 + lane) * kVals;
-#pragma unroll
-            for (int m = 0; m < MT; ++m)
-#pragma unroll
-                for (int t = 0; t < NTW; ++t)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) dst[(m * NTW + t) * 4 + i] = acc[m][t][i];
+    auto emit_tile = [&](int m, int t, const float (&v)[4]) {
+        const int n = n0 + t * 8 + 2 * ti;
+        const int b0 = m * 16 + gi, b1 = b0 + 8;
+        if (n < N) {
+            if (b0 < B) epi.pair(b0, n, v[0], v[1], blockIdx.y);
+            if (b1 < B) epi.pair(b1, n, v[2], v[3], blockIdx.y);
         }
+    };
+    if (KS == 1) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int t = 0; t < NTW; ++t) emit_tile(m, t, acc[m][t]);
+    } else {
+        // Every warp parks its partial tiles; warp ks then sums tiles
+        // j % KS == ks over the group's KS warps in ks order.  Layout
+        // [ks][grp][tile][lane] of float4: each store and load of a warp is
+        // 512 contiguous bytes (no bank conflicts).
+        float4* red = reinterpret_cast<float4*>(smem);
+        constexpr int kTiles = MT * NTW;
         __syncthreads();
-        if (ks == 0) {
-            for (int s = 1; s < KS; ++s) {
-                const float* src = red + (((s - 1) * kGroups + grp) * 32 + lane) * kVals;
 #pragma unroll
-                for (int m = 0; m < MT; ++m)
+        for (int m = 0; m < MT; ++m)
 #pragma unroll
-                    for (int t = 0; t < NTW; ++t)
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) acc[m][t][i] += src[(m * NTW + t) * 4 + i];
-            }
-        }
-    }
-    if (ks == 0) {
+            for (int t = 0; t < NTW; ++t)
+                red[((ks * kGroups + grp) * kTiles + m * NTW + t) * 32 + lane] =
+                    make_float4(acc[m][t][0], acc[m][t][1], acc[m][t][2], acc[m][t][3]);
+        __syncthreads();
 #pragma unroll
         for (int m = 0; m < MT; ++m)
 #pragma unroll
             for (int t = 0; t < NTW; ++t) {
-                const int n = n0 + t * 8 + 2 * ti;
-                const int b0 = m * 16 + gi, b1 = b0 + 8;
-                if (n < N) {
-                    if (b0 < B) epi.pair(b0, n, acc[m][t][0], acc[m][t][1], blockIdx.y);
-                    if (b1 < B) epi.pair(b1, n, acc[m][t][2], acc[m][t][3], blockIdx.y);
+                const int j = m * NTW + t;
+                if (j % KS != ks) continue;
+                float4 a = red[(grp * kTiles + j) * 32 + lane];
+                for (int s = 1; s < KS; ++s) {
+                    const float4 b = red[((s * kGroups + grp) * kTiles + j) * 32 + lane];
+                    a.x += b.x;
+                    a.y += b.y;
+                    a.z += b.z;
+                    a.w += b.w;
                 }
+                const float v[4] = {a.x, a.y, a.z, a.w};
+                emit_tile(m, t, v);
             }
     }
     epi.finish();

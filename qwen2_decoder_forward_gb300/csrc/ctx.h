@@ -143,6 +143,8 @@ struct Ctx {
     const float* final_norm = nullptr;
     float* kv = nullptr;          // [max_seqs][L][2][nkv][n_ctx][hd]
     size_t kv_floats = 0;
+    CUtensorMap kvmap;            // kv as a [rows][64] f32 matrix, 32 x 64 boxes, 128-byte swizzle
+    bool kvmap_ok = false;        // the map encoded (batched decode attention uses it)
     float2* rope = nullptr;       // [n_ctx][hd/2] (cos, sin), from double on the host
     int* err = nullptr;           // device guard word
     Workspace ws;

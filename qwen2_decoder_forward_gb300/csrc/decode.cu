@@ -501,6 +501,7 @@ struct EpiResidualQ8 {
 // part[chunk][b][n]; the last CTA of a row group to finish (all gridDim.y
 // chunks written) adds them to the residual x in chunk order.
 struct EpiDownQ8 {
+    static constexpr int kMaxParts = 16;
     float* part;
     size_t stride;  // floats between chunks
     int N;          // output rows (hidden)
@@ -521,12 +522,37 @@ struct EpiDownQ8 {
         __threadfence();
         const int n0 = blockIdx.x * rows_cta;
         const int nr = min(rows_cta, N - n0);
-        for (int e = threadIdx.x; e < B * nr; e += blockDim.x) {
-            const int b = e / nr;
-            const size_t i = (size_t)b * N + n0 + (e - b * nr);
-            float v = x[i];
-            for (int s = 0; s < (int)gridDim.y; ++s) v += __ldcg(part + s * stride + i);
-            x[i] = v;
+        const int np = (int)gridDim.y;
+        if (np <= kMaxParts && nr % 4 == 0 && N % 4 == 0 && stride % 4 == 0) {
+            // Four outputs per thread step, every partial's load in flight
+            // at once; the sum is still x + part 0 + part 1 + ... in order.
+            const int nq = nr / 4;
+            for (int e = threadIdx.x; e < B * nq; e += blockDim.x) {
+                const int b = e / nq;
+                const size_t i = (size_t)b * N + n0 + 4 * (e - b * nq);
+                float4 pv[kMaxParts];
+#pragma unroll
+                for (int s = 0; s < kMaxParts; ++s)
+                    if (s < np) pv[s] = __ldcg(reinterpret_cast<const float4*>(part + s * stride + i));
+                float4 v = *reinterpret_cast<const float4*>(x + i);
+#pragma unroll
+                for (int s = 0; s < kMaxParts; ++s)
+                    if (s < np) {
+                        v.x += pv[s].x;
+                        v.y += pv[s].y;
+                        v.z += pv[s].z;
+                        v.w += pv[s].w;
+                    }
+                *reinterpret_cast<float4*>(x + i) = v;
+            }
+        } else {
+            for (int e = threadIdx.x; e < B * nr; e += blockDim.x) {
+                const int b = e / nr;
+                const size_t i = (size_t)b * N + n0 + (e - b * nr);
+                float v = x[i];
+                for (int s = 0; s < np; ++s) v += __ldcg(part + s * stride + i);
+                x[i] = v;
+            }
         }
         if (threadIdx.x == 0) count[blockIdx.x] = 0;
     }
@@ -796,14 +822,14 @@ cudaError_t o_ffn_q8(Ctx& c, int l, float* x, int B, cudaStream_t st) {
 // else the split-K kernel.
 cudaError_t attn_batched(const Ctx& c, const StepArgs& a, int l, cudaStream_t st) {
     const int group = a.nh / a.nkv;
-    if (a.B > fd::kMaxRows || c.ws.att_max_chunks > fd::kMaxChunks || group > 8) {
+    if (!c.kvmap_ok || a.B > fd::kMaxRows || c.ws.att_max_chunks > fd::kMaxChunks || group > fd::kGroupMax ||
+        c.cfg.head_dim != fd::kDh) {
         k_attn_decode<<<dim3(c.cfg.n_kv_head, c.ws.att_max_chunks, a.B), kThreads, 0, st>>>(
             a, l, c.ws.att_part, c.ws.att_count, c.ws.att_max_chunks);
         return cudaGetLastError();
     }
     fd::Args f;
     f.q = a.q;
-    f.kv = a.kv;
     f.pos = a.pos;
     f.slot = a.slot;
     f.part = c.ws.att_part;
@@ -820,10 +846,8 @@ cudaError_t attn_batched(const Ctx& c, const StepArgs& a, int l, cudaStream_t st
     f.layer = l;
     f.max_chunks = c.ws.att_max_chunks;
     const int grid = 2 * c.n_sm;
-    if (group == 7)
-        k_attn_flash<7><<<grid, fd::kThreads, sizeof(fd::Smem), st>>>(f);
-    else
-        k_attn_flash<8><<<grid, fd::kThreads, sizeof(fd::Smem), st>>>(f);
+    k_attn_flash<<<grid, fd::kThreads, fd::kSmemBytes, st>>>(c.kvmap, f);
+    k_attn_merge<<<a.B * a.nkv, kMergeThreads, 0, st>>>(f, grid);
     return cudaGetLastError();
 }
 
@@ -1004,9 +1028,7 @@ cudaError_t decode_set_smem_limits(int max_bytes) {
 #undef Q2_SMEM_NB
 #undef Q2_SMEM
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_attn_flash<7>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(fd::Smem));
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_attn_flash<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(fd::Smem));
+        e = cudaFuncSetAttribute(k_attn_flash, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fd::kSmemBytes);
 #define Q2_BG(MT, NTW, KS, EPI, PRO)                                                                          \
     if (e == cudaSuccess)                                                                                     \
         e = cudaFuncSetAttribute(bg::k_bgemm_q8<MT, NTW, KS, EPI, PRO>, cudaFuncAttributeMaxDynamicSharedMemorySize, \

@@ -1,5 +1,6 @@
 // Batched GQA decode attention over an f32 KV cache, for many sequences at
-// ragged positions in one launch (flash-decoding with a persistent grid).
+// ragged positions in one launch (flash-decoding with a persistent grid and
+// warp-level TF32 tensor-core products).
 //
 // What it computes (nnterp encyclopedia "qwen2", grouped-query attention;
 // minfer "Qwen2 / Qwen2.5 Architecture Support", section 1): for every row b
@@ -17,15 +18,20 @@
 // segments in chunk order and writes o (f32, and the f16 hi / lo pair the
 // following Q8_0 product reads).
 //
-// Inside a CTA: warp 4 (one elected lane) streams each unit's K and V rows
-// (2 x 16 KB, contiguous in the cache) into a ring of shared-memory stages
-// with cp.async.bulk, completion counted on an mbarrier per stage; warps 0-3
-// consume.  Warp w takes keys 16w .. 16w+15 of the chunk, four at a time:
-// lane (k4 = lane / 8, c8 = lane % 8) holds dims 4 c8 .. 4 c8 + 3 and
-// 32 + 4 c8 .. 32 + 4 c8 + 3 of key 4t + k4 (two conflict-free 16-byte
-// shared loads) and the same dims of every query head in registers; its 8
-// partial dot products are reduce-scattered over the 8 lanes of the key
-// (xor 4, 2, 1), leaving lane c8 with the score of head c8.
+// Inside a CTA: warp 4 (one elected lane) loads each unit's K and V tiles
+// (64 positions x 64 floats each) with four TMA tensor copies into a ring
+// of shared-memory stages (128-byte swizzle, so the fragment loads below
+// are conflict-free), completion counted on an mbarrier per stage; warps
+// 0-3 consume, warp w taking keys 16w .. 16w + 15 of the chunk:
+//   scores  S^T[key][head] = K[key][:] . Q[head][:]   (m16n8k8, M = 16 keys,
+//           N = 8 head slots, K = 8 dims per step, 8 steps);
+//   values  O^T[dim][head] += V^T[dim][key] . P^T[key][head] (M = 16 dims,
+//           4 tiles, K = 8 keys per step, 2 steps).
+// Precision: q, k and the probabilities enter the MMAs rounded to TF32
+// (10-bit mantissa, round to nearest); v enters as a TF32 hi / lo pair (two
+// MMAs), the same split the tensor-core prefill uses for v; the softmax
+// statistics, the sums l (of the rounded probabilities) and the accumulators
+// are f32.
 #pragma once
 
 #include "common.cuh"
@@ -41,15 +47,17 @@ constexpr int kConsumers = 4;           // consumer warps
 constexpr int kThreads = (kConsumers + 1) * 32;
 constexpr int kMaxRows = 32;            // rows (sequences) per launch
 constexpr int kMaxChunks = 64;          // n_ctx <= 4096
-constexpr int kPart = kDh + 2;    // partial: m, l, acc[64]
+constexpr int kGroupMax = 8;            // query heads per kv head
+constexpr int kPart = kDh + 2;          // partial: m, l, acc[64]
+constexpr int kHalf = kCh * 32;         // floats of one swizzled half tile (64 rows x 128 bytes)
+constexpr unsigned kUnitBytes = 4u * kHalf * 4u;  // K and V, two halves each
 constexpr unsigned long long kWaitNs = 2000000000ull;
 
 struct Args {
     const float* q;         // [B][nh][64] rotated queries
-    const float* kv;        // cache [slots][L][2][nkv][n_ctx][64]
     const int* pos;         // [B] position of each row (attends to 0..pos)
     const int* slot;        // [B] cache slot of each row
-    float* part;            // partials [slots... indexed by row b][nh][max_chunks][66]
+    float* part;            // partials [B][nh][max_chunks][66]
     int* count;             // [B][nkv] arrival counters, zero between launches
     float* o;               // [B][nh][64]
     __half* o_hi;           // nullable [B][nh][64]
@@ -59,23 +67,24 @@ struct Args {
 };
 
 struct Smem {
-    float ring[kStages][2][kCh][kDh];   // K rows then V rows of one unit
-    float wacc[kConsumers][8][kDh];     // per-warp segment accumulators
-    float wm[kConsumers][8];
-    float wl[kConsumers][8];
+    // [stage][K, V][dims 0-31, 32-63][row][32 floats], each half tile
+    // 128-byte swizzled (1024-byte aligned).
+    float ring[kStages][2][2][kHalf];
+    float qs[kStages][kGroupMax * kDh];    // the unit's query heads, when it starts a segment
+    float wacc[kConsumers][kGroupMax][kDh];  // per-warp segment accumulators
+    float wm[kConsumers][kGroupMax];
+    float wl[kConsumers][kGroupMax];
     uint64_t full[kStages];
     uint64_t empty[kStages];
     int base[kMaxRows + 1];             // first unit of each row
     int nch[kMaxRows];                  // chunks of each row (0 if its position is invalid)
     int posv[kMaxRows];                 // position of each row
-    int segs[kMaxChunks];               // merge: first chunk of each segment
-    int nseg;
-    int last;
+    int slotv[kMaxRows];                // cache slot of each row
     int abort;                          // a bounded wait gave up: skip the remaining work
 };
+// Dynamic shared memory to request: the ring needs 1024-byte alignment.
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
 
-static_assert(sizeof(float) * 2 * 8 * kMaxChunks <= sizeof(float) * kConsumers * 8 * kDh,
-              "the merge's per-segment maxima and sums fit in the warp accumulators");
 
 __device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -102,9 +111,28 @@ __device__ __forceinline__ Unit decode_unit(const Smem& sm, int B, int u) {
     return t;
 }
 
-__device__ __forceinline__ const float* kv_rows(const Args& a, int b, int which, int g, int p0) {
-    const size_t slot = (size_t)a.slot[b];
-    return a.kv + ((((slot * a.L + a.layer) * 2 + which) * a.nkv + g) * (size_t)a.n_ctx + p0) * kDh;
+// Row of the cache viewed as a [rows][64] f32 matrix: position p0 of
+// (slot, layer, K or V, kv head g).
+__device__ __forceinline__ int kv_row(const Args& a, int slot, int which, int g, int p0) {
+    return (((slot * a.L + a.layer) * 2 + which) * a.nkv + g) * a.n_ctx + p0;
+}
+
+// Is chunk c of (b, g) the first chunk of a segment (of the CTA that holds it)?
+__device__ __forceinline__ bool seg_start(const int* base, const int* nch, int b, int g, int c, unsigned U,
+                                          unsigned G) {
+    if (c == 0) return true;
+    const unsigned u = (unsigned)(base[b] + g * nch[b] + c);
+    return unit_start((unsigned)unit_cta(u, U, G), U, G) == (int)u;
+}
+
+// Float index of element (row, f) (f < 32) in a 128-byte-swizzled half tile:
+// the 16-byte chunk f / 4 of row r sits at chunk (f / 4) ^ (r % 8).
+__device__ __forceinline__ int swz(int row, int f) { return row * 32 + ((((f >> 2) ^ (row & 7)) << 2) | (f & 3)); }
+
+__device__ __forceinline__ uint32_t tf32_rn(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
 }
 
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
@@ -115,82 +143,69 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
         : "memory");
 }
 
-// Is chunk c of (b, g) the first chunk of a segment (of the CTA that holds it)?
-__device__ __forceinline__ bool seg_start(const Smem& sm, int b, int g, int c, unsigned U, unsigned G) {
-    if (c == 0) return true;
-    const unsigned u = (unsigned)(sm.base[b] + g * sm.nch[b] + c);
-    return unit_start((unsigned)unit_cta(u, U, G), U, G) == (int)u;
+// Row table of a launch (warp 0 of the block): per row its position, slot
+// and chunk count (0 if the position is invalid) and its first unit.
+__device__ __forceinline__ void row_table(const Args& a, int* base, int* nch, int* posv, int* slotv) {
+    const int lane = threadIdx.x & 31;
+    int n = 0, p = 0, sl = 0;
+    if (lane < a.B) {
+        p = a.pos[lane];
+        sl = a.slot[lane];
+        if (p < 0 || p >= a.n_ctx) {
+            if (blockIdx.x == 0) raise_guard(a.err, kGuardPosition);
+            p = 0;
+        } else if ((p + kCh) / kCh > min(a.max_chunks, kMaxChunks)) {
+            if (blockIdx.x == 0) raise_guard(a.err, kGuardShape);
+            p = 0;
+        } else {
+            n = (p + kCh) / kCh;
+        }
+    }
+    int v = n * a.nkv;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += t;
+    }
+    nch[lane] = n;
+    if (posv) posv[lane] = p;
+    if (slotv) slotv[lane] = sl;
+    base[lane + 1] = v;
+    if (lane == 0) base[0] = 0;
 }
 
-// Sum of v[h] over the 8 lanes of a key (lanes differing in bits 0-2),
-// scattered so that lane c8 returns head c8's total: halves are exchanged
-// over xor 4, then quarters over xor 2, then singles over xor 1.
-__device__ __forceinline__ float reduce_scatter8(const float (&v)[8], int c8) {
-    const bool b2 = (c8 & 4) != 0, b1 = (c8 & 2) != 0, b0 = (c8 & 1) != 0;
-    float w4[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float send = b2 ? v[i] : v[i + 4];
-        const float keep = b2 ? v[i + 4] : v[i];
-        w4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-    }
-    float w2[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const float send = b1 ? w4[i] : w4[i + 2];
-        const float keep = b1 ? w4[i + 2] : w4[i];
-        w2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-    }
-    const float send = b0 ? w2[0] : w2[1];
-    const float keep = b0 ? w2[1] : w2[0];
-    return keep + __shfl_xor_sync(0xffffffffu, send, 1);
+// d += a . b for one 16 x 8 x 8 TF32 tile (f32 accumulation).
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 }  // namespace fd
+}  // namespace qwen2
 
-// NG: query-head slots per lane group (7 when the group is exactly 7,
-// otherwise 8 with the heads past the group masked).  Grid: any number of
-// CTAs (two per SM fit); block fd::kThreads; dynamic shared memory
-// sizeof(fd::Smem).
-template <int NG>
-__global__ void __launch_bounds__(fd::kThreads, 2) k_attn_flash(fd::Args a) {
+namespace qwen2 {
+
+// Grid: any number of CTAs (two per SM fit); block fd::kThreads; dynamic
+// shared memory fd::kSmemBytes.  kvmap: the KV cache as a [rows][64] f32
+// matrix (rows = slots * L * 2 * nkv * n_ctx), boxes of 32 floats x 64 rows,
+// 128-byte swizzle.
+__global__ void __launch_bounds__(fd::kThreads, 2)
+    k_attn_flash(const __grid_constant__ CUtensorMap kvmap, fd::Args a) {
     using namespace fd;
-    extern __shared__ __align__(128) unsigned char fd_smem_raw[];
-    Smem& sm = *reinterpret_cast<Smem*>(fd_smem_raw);
+    extern __shared__ unsigned char fd_smem_raw[];
+    Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(fd_smem_raw) + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int group = a.nh / a.nkv;
-    if (group > NG || a.B > kMaxRows) {
+    if (group > kGroupMax || a.B > kMaxRows) {
         if (tid == 0 && blockIdx.x == 0) raise_guard(a.err, kGuardShape);
         return;
     }
     if (warp == 0) {
-        // Row table: chunks per row and the first unit of each row.
-        int n = 0, p = 0;
-        if (lane < a.B) {
-            p = a.pos[lane];
-            if (p < 0 || p >= a.n_ctx) {
-                if (blockIdx.x == 0) raise_guard(a.err, kGuardPosition);
-                p = 0;
-            } else if ((p + kCh) / kCh > min(a.max_chunks, kMaxChunks)) {
-                if (blockIdx.x == 0) raise_guard(a.err, kGuardShape);
-                p = 0;
-            } else {
-                n = (p + kCh) / kCh;
-            }
-        }
-        int v = n * a.nkv;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int t = __shfl_up_sync(0xffffffffu, v, o);
-            if (lane >= o) v += t;
-        }
-        sm.nch[lane] = n;
-        sm.posv[lane] = p;
-        sm.base[lane + 1] = v;
-        if (lane == 0) {
-            sm.base[0] = 0;
-            sm.abort = 0;
-        }
+        row_table(a, sm.base, sm.nch, sm.posv, sm.slotv);
+        if (lane == 0) sm.abort = 0;
     }
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -199,145 +214,163 @@ __global__ void __launch_bounds__(fd::kThreads, 2) k_attn_flash(fd::Args a) {
         }
         sm100::mbar_init_fence();
     }
-    if (warp < kConsumers) {
-        // Key rows past a unit's length keep whatever an earlier unit left:
-        // start from zeros so they are always finite (their weight is 0).
-        float4* r = reinterpret_cast<float4*>(&sm.ring[0][0][0][0]);
-        constexpr int n4 = kStages * 2 * kCh * kDh / 4;
-        for (int i = tid; i < n4; i += kConsumers * 32) r[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    }
     __syncthreads();
     const unsigned U = (unsigned)sm.base[a.B], G = gridDim.x;
     const int u0 = unit_start(blockIdx.x, U, G), u1 = unit_start(blockIdx.x + 1, U, G);
 
     if (warp == kConsumers) {
-        // Producer: one lane issues the K and V bulk copies of each unit.
+        // Producer: one lane issues the four tensor copies of each unit.
         if (lane == 0) {
+            sm100::tma_prefetch_desc(&kvmap);
             int k = 0;
             for (int u = u0; u < u1; ++u, ++k) {
                 const int s = k % kStages;
                 if (k >= kStages &&
-                    !sm100::mbar_wait(&sm.empty[s], ((k / kStages) & 1) ^ 1, sm100::global_ns() + kWaitNs)) {
+                    !sm100::mbar_wait(&sm.empty[s], ((k / kStages) & 1) ^ 1, kWaitNs)) {
                     raise_guard(a.err, kGuardTimeout);
                     break;
                 }
                 const Unit t = decode_unit(sm, a.B, u);
-                const unsigned bytes = (unsigned)t.nj * kDh * 4;
-                sm100::mbar_expect_tx(&sm.full[s], 2 * bytes);
-                bulk_g2s(&sm.ring[s][0][0][0], kv_rows(a, t.b, 0, t.g, t.c * kCh), bytes, &sm.full[s]);
-                bulk_g2s(&sm.ring[s][1][0][0], kv_rows(a, t.b, 1, t.g, t.c * kCh), bytes, &sm.full[s]);
+                const int yk = kv_row(a, sm.slotv[t.b], 0, t.g, t.c * kCh);
+                const int yv = kv_row(a, sm.slotv[t.b], 1, t.g, t.c * kCh);
+                // A unit that starts a segment also brings its query heads.
+                const bool first = u == u0 || t.c == 0;
+                const unsigned qbytes = first ? (unsigned)(group * kDh * 4) : 0u;
+                sm100::mbar_expect_tx(&sm.full[s], kUnitBytes + qbytes);
+                if (first)
+                    bulk_g2s(sm.qs[s], a.q + ((size_t)t.b * a.nh + (size_t)t.g * group) * kDh, qbytes, &sm.full[s]);
+                sm100::tma_load_2d(sm.ring[s][0][0], &kvmap, 0, yk, &sm.full[s]);
+                sm100::tma_load_2d(sm.ring[s][0][1], &kvmap, 32, yk, &sm.full[s]);
+                sm100::tma_load_2d(sm.ring[s][1][0], &kvmap, 0, yv, &sm.full[s]);
+                sm100::tma_load_2d(sm.ring[s][1][1], &kvmap, 32, yv, &sm.full[s]);
             }
             // Every copy lands before the CTA exits, even after an abort.
             for (int kk = k > kStages ? k - kStages : 0; kk < k; ++kk)
-                sm100::mbar_wait(&sm.full[kk % kStages], (kk / kStages) & 1, sm100::global_ns() + kWaitNs);
+                sm100::mbar_wait(&sm.full[kk % kStages], (kk / kStages) & 1, kWaitNs);
         }
         return;
     }
 
-
     // ---- consumers: warps 0-3 ---------------------------------------------
-    const int k4 = lane >> 3, c8 = lane & 7;
-    float qr[NG][8], acc[NG][8];
-    float m_run = -INFINITY, l_run = 0.f;
+    const int g8 = lane >> 2, t4 = lane & 3;   // fragment row group, thread in group
+    const int key0 = 16 * warp;                // this warp's keys within a chunk
+    const int h0 = 2 * t4, h1 = 2 * t4 + 1;    // the two head slots of this thread's scores / outputs
+    uint32_t qb[8][2];                         // B fragments of Q^T (TF32), per 8-dim step
+    float oacc[4][4];                          // O^T[16 mt + g8 (+8)][h0, h1]
+    float m_run0 = -INFINITY, m_run1 = -INFINITY, l_run0 = 0.f, l_run1 = 0.f;
     int c_first = 0;
     int k = 0;
     for (int u = u0; u < u1; ++u, ++k) {
         const Unit t = decode_unit(sm, a.B, u);
-        if (u == u0 || t.c == 0) {
-            // A new segment: this (b, g)'s query heads, fresh running state.
-            c_first = t.c;
-            const float* qb = a.q + ((size_t)t.b * a.nh + (size_t)t.g * group) * kDh;
-#pragma unroll
-            for (int h = 0; h < NG; ++h) {
-                float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
-                if (h < group) {
-                    x0 = *reinterpret_cast<const float4*>(qb + h * kDh + 4 * c8);
-                    x1 = *reinterpret_cast<const float4*>(qb + h * kDh + 32 + 4 * c8);
-                }
-                qr[h][0] = x0.x; qr[h][1] = x0.y; qr[h][2] = x0.z; qr[h][3] = x0.w;
-                qr[h][4] = x1.x; qr[h][5] = x1.y; qr[h][6] = x1.z; qr[h][7] = x1.w;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) acc[h][i] = 0.f;
-            }
-            m_run = -INFINITY;
-            l_run = 0.f;
-        }
         const int s = k % kStages;
         bool ok = *reinterpret_cast<volatile int*>(&sm.abort) == 0;
-        if (ok && !sm100::mbar_wait(&sm.full[s], (k / kStages) & 1, sm100::global_ns() + kWaitNs)) {
+        if (ok && !sm100::mbar_wait(&sm.full[s], (k / kStages) & 1, kWaitNs)) {
             raise_guard(a.err, kGuardTimeout);
             sm.abort = 1;
             ok = false;
         }
+        if (u == u0 || t.c == 0) {
+            // A new segment: this (b, g)'s query heads (brought with the
+            // unit), fresh running state.
+            c_first = t.c;
+            const float* qh = sm.qs[s] + g8 * kDh;
+#pragma unroll
+            for (int s8 = 0; s8 < 8; ++s8) {
+                const bool hv = ok && g8 < group;
+                qb[s8][0] = tf32_rn(hv ? qh[8 * s8 + t4] : 0.f);
+                qb[s8][1] = tf32_rn(hv ? qh[8 * s8 + t4 + 4] : 0.f);
+            }
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt) oacc[mt][0] = oacc[mt][1] = oacc[mt][2] = oacc[mt][3] = 0.f;
+            m_run0 = m_run1 = -INFINITY;
+            l_run0 = l_run1 = 0.f;
+        }
         if (ok) {
-            const float* Ks = &sm.ring[s][0][0][0];
-            const float* Vs = &sm.ring[s][1][0][0];
-            // Scores of keys 16 warp + 4 i + k4 for head c8.
-            float sc[4];
+            const float* Kt = sm.ring[s][0][0];
+            const float* Vt = sm.ring[s][1][0];
+            // Scores S^T[key0 + g8 (+8)][h0, h1] over the 64 dims, as two
+            // independent chains (dims 0-31, 32-63) added at the end.
+            float sc[4] = {0.f, 0.f, 0.f, 0.f}, sc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int j = 16 * warp + 4 * i + k4;
-                const float4 ka = *reinterpret_cast<const float4*>(Ks + j * kDh + 4 * c8);
-                const float4 kb = *reinterpret_cast<const float4*>(Ks + j * kDh + 32 + 4 * c8);
-                float v[8];
-#pragma unroll
-                for (int h = 0; h < 8; ++h) {
-                    if (h < NG) {
-                        float d = qr[h][0] * ka.x;
-                        d = fmaf(qr[h][1], ka.y, d);
-                        d = fmaf(qr[h][2], ka.z, d);
-                        d = fmaf(qr[h][3], ka.w, d);
-                        d = fmaf(qr[h][4], kb.x, d);
-                        d = fmaf(qr[h][5], kb.y, d);
-                        d = fmaf(qr[h][6], kb.z, d);
-                        d = fmaf(qr[h][7], kb.w, d);
-                        v[h] = d;
-                    } else {
-                        v[h] = 0.f;
-                    }
-                }
-                const float r = reduce_scatter8(v, c8);
-                // hd = 64: the scale 1/8 is exact.
-                sc[i] = (j < t.nj && c8 < group) ? r * 0.125f : -INFINITY;
+            for (int s8 = 0; s8 < 8; ++s8) {
+                const float* Kh = Kt + (s8 >> 2) * kHalf;
+                const int f = 8 * (s8 & 3) + t4;
+                uint32_t af[4];
+                af[0] = tf32_rn(Kh[swz(key0 + g8, f)]);
+                af[1] = tf32_rn(Kh[swz(key0 + g8 + 8, f)]);
+                af[2] = tf32_rn(Kh[swz(key0 + g8, f + 4)]);
+                af[3] = tf32_rn(Kh[swz(key0 + g8 + 8, f + 4)]);
+                if (s8 < 4) mma_tf32(sc, af, qb[s8][0], qb[s8][1]);
+                else mma_tf32(sc2, af, qb[s8][0], qb[s8][1]);
             }
-            // Online softmax over this warp's 16 keys (per head c8).
-            float mt = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
-            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
-            const float m_new = fmaxf(m_run, mt);
-            const float m_use = m_new == -INFINITY ? 0.f : m_new;
-            const float alpha = expf(m_run - m_use);
-            float p[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) p[i] = expf(sc[i] - m_use);
-            l_run = fmaf(l_run, alpha, (p[0] + p[1]) + (p[2] + p[3]));
-            m_run = m_new;
-            if (__any_sync(0xffffffffu, c8 < group && alpha != 1.f)) {
+            for (int i = 0; i < 4; ++i) sc[i] += sc2[i];
+            // hd = 64: the scale 1/8 is exact.  Keys past the chunk's length
+            // and head slots past the group get -inf.
+            const bool klo = key0 + g8 < t.nj, khi = key0 + g8 + 8 < t.nj;
+            const bool v0 = h0 < group, v1 = h1 < group;
+            sc[0] = (klo && v0) ? sc[0] * 0.125f : -INFINITY;
+            sc[1] = (klo && v1) ? sc[1] * 0.125f : -INFINITY;
+            sc[2] = (khi && v0) ? sc[2] * 0.125f : -INFINITY;
+            sc[3] = (khi && v1) ? sc[3] * 0.125f : -INFINITY;
+            // Online softmax over this warp's 16 keys, per head slot.
+            float mt0 = fmaxf(sc[0], sc[2]), mt1 = fmaxf(sc[1], sc[3]);
 #pragma unroll
-                for (int h = 0; h < NG; ++h) {
-                    const float ah = __shfl_sync(0xffffffffu, alpha, h);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[h][e] *= ah;
-                }
+            for (int o = 4; o < 32; o <<= 1) {
+                mt0 = fmaxf(mt0, __shfl_xor_sync(0xffffffffu, mt0, o));
+                mt1 = fmaxf(mt1, __shfl_xor_sync(0xffffffffu, mt1, o));
             }
-            // acc[h] += p[h][j] * V[j] over this lane's keys.
+            const float mn0 = fmaxf(m_run0, mt0), mn1 = fmaxf(m_run1, mt1);
+            const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
+            const float al0 = expf(m_run0 - mu0), al1 = expf(m_run1 - mu1);
+            m_run0 = mn0;
+            m_run1 = mn1;
+            // Probabilities rounded to TF32 here, so l sums what the MMA uses.
+            uint32_t pb[4];
+            pb[0] = tf32_rn(expf(sc[0] - mu0));
+            pb[1] = tf32_rn(expf(sc[1] - mu1));
+            pb[2] = tf32_rn(expf(sc[2] - mu0));
+            pb[3] = tf32_rn(expf(sc[3] - mu1));
+            l_run0 = fmaf(l_run0, al0, __uint_as_float(pb[0]) + __uint_as_float(pb[2]));
+            l_run1 = fmaf(l_run1, al1, __uint_as_float(pb[1]) + __uint_as_float(pb[3]));
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int j = 16 * warp + 4 * i + k4;
-                const float4 va = *reinterpret_cast<const float4*>(Vs + j * kDh + 4 * c8);
-                const float4 vb = *reinterpret_cast<const float4*>(Vs + j * kDh + 32 + 4 * c8);
+            for (int mt = 0; mt < 4; ++mt) {
+                oacc[mt][0] *= al0;
+                oacc[mt][1] *= al1;
+                oacc[mt][2] *= al0;
+                oacc[mt][3] *= al1;
+            }
+            // O^T += V^T . P^T.  Within each 8-key step the k index runs
+            // over keys in the order 0, 2, 4, 6 (k = 0..3) and 1, 3, 5, 7
+            // (k = 4..7), so thread (g8, t4) needs P[key 2 t4 (+1)][head g8]:
+            // scores of key j sit in thread (j % 8, head / 2) as component
+            // (head % 2) + 2 (j / 8).
 #pragma unroll
-                for (int h = 0; h < NG; ++h) {
-                    const float ph = __shfl_sync(0xffffffffu, p[i], (k4 << 3) | h);
-                    acc[h][0] = fmaf(ph, va.x, acc[h][0]);
-                    acc[h][1] = fmaf(ph, va.y, acc[h][1]);
-                    acc[h][2] = fmaf(ph, va.z, acc[h][2]);
-                    acc[h][3] = fmaf(ph, va.w, acc[h][3]);
-                    acc[h][4] = fmaf(ph, vb.x, acc[h][4]);
-                    acc[h][5] = fmaf(ph, vb.y, acc[h][5]);
-                    acc[h][6] = fmaf(ph, vb.z, acc[h][6]);
-                    acc[h][7] = fmaf(ph, vb.w, acc[h][7]);
+            for (int kk = 0; kk < 2; ++kk) {
+                const int src0 = (2 * t4) * 4 + (g8 >> 1), src1 = (2 * t4 + 1) * 4 + (g8 >> 1);
+                const uint32_t e0 = __shfl_sync(0xffffffffu, pb[2 * kk], src0);
+                const uint32_t o0 = __shfl_sync(0xffffffffu, pb[2 * kk + 1], src0);
+                const uint32_t e1 = __shfl_sync(0xffffffffu, pb[2 * kk], src1);
+                const uint32_t o1 = __shfl_sync(0xffffffffu, pb[2 * kk + 1], src1);
+                const uint32_t b0 = (g8 & 1) ? o0 : e0, b1 = (g8 & 1) ? o1 : e1;
+                const int r0 = key0 + 8 * kk + 2 * t4;  // keys of k = t4 and k = t4 + 4
+#pragma unroll
+                for (int mt = 0; mt < 4; ++mt) {
+                    const float* Vh = Vt + (mt >> 1) * kHalf;
+                    const int f = 16 * (mt & 1) + g8;
+                    const float va = Vh[swz(r0, f)], vb = Vh[swz(r0, f + 8)];
+                    const float vc = Vh[swz(r0 + 1, f)], vd = Vh[swz(r0 + 1, f + 8)];
+                    uint32_t ah[4], alo[4];
+                    ah[0] = tf32_rn(va);
+                    ah[1] = tf32_rn(vb);
+                    ah[2] = tf32_rn(vc);
+                    ah[3] = tf32_rn(vd);
+                    alo[0] = __float_as_uint(va - __uint_as_float(ah[0]));
+                    alo[1] = __float_as_uint(vb - __uint_as_float(ah[1]));
+                    alo[2] = __float_as_uint(vc - __uint_as_float(ah[2]));
+                    alo[3] = __float_as_uint(vd - __uint_as_float(ah[3]));
+                    mma_tf32(oacc[mt], ah, b0, b1);
+                    mma_tf32(oacc[mt], alo, b0, b1);
                 }
             }
         }
@@ -346,26 +379,25 @@ __global__ void __launch_bounds__(fd::kThreads, 2) k_attn_flash(fd::Args a) {
 
         if (t.c != sm.nch[t.b] - 1 && u + 1 != u1) continue;
         // ---- end of a segment: combine the 4 warps, write one partial ------
-        float lt = l_run;
-        lt += __shfl_xor_sync(0xffffffffu, lt, 8);
-        lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+        float lt0 = l_run0, lt1 = l_run1;
 #pragma unroll
-        for (int h = 0; h < NG; ++h)
+        for (int o = 4; o < 32; o <<= 1) {
+            lt0 += __shfl_xor_sync(0xffffffffu, lt0, o);
+            lt1 += __shfl_xor_sync(0xffffffffu, lt1, o);
+        }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], 8);
-                acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], 16);
-            }
-        if (k4 == 0) {
-#pragma unroll
-            for (int h = 0; h < NG; ++h) {
-                *reinterpret_cast<float4*>(&sm.wacc[warp][h][4 * c8]) =
-                    make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
-                *reinterpret_cast<float4*>(&sm.wacc[warp][h][32 + 4 * c8]) =
-                    make_float4(acc[h][4], acc[h][5], acc[h][6], acc[h][7]);
-            }
-            sm.wm[warp][c8] = m_run;
-            sm.wl[warp][c8] = lt;
+        for (int mt = 0; mt < 4; ++mt) {
+            const int d = 16 * mt + g8;
+            sm.wacc[warp][h0][d] = oacc[mt][0];
+            sm.wacc[warp][h1][d] = oacc[mt][1];
+            sm.wacc[warp][h0][d + 8] = oacc[mt][2];
+            sm.wacc[warp][h1][d + 8] = oacc[mt][3];
+        }
+        if (g8 == 0) {
+            sm.wm[warp][h0] = m_run0;
+            sm.wm[warp][h1] = m_run1;
+            sm.wl[warp][h0] = lt0;
+            sm.wl[warp][h1] = lt1;
         }
         consumers_sync();
         const size_t head0 = (size_t)t.b * a.nh + (size_t)t.g * group;
@@ -388,84 +420,79 @@ __global__ void __launch_bounds__(fd::kThreads, 2) k_attn_flash(fd::Args a) {
                 pr[1] = Lsum;
             }
         }
-        __threadfence();
         consumers_sync();
-        if (warp == 0) {
-            // Count this (b, g)'s segments; the CTA that brings the count to
-            // that number merges them.
-            const int nch = sm.nch[t.b];
-            const bool s0 = lane < nch && seg_start(sm, t.b, t.g, lane, U, G);
-            const bool s1 = lane + 32 < nch && seg_start(sm, t.b, t.g, lane + 32, U, G);
-            const unsigned m0 = __ballot_sync(0xffffffffu, s0), m1 = __ballot_sync(0xffffffffu, s1);
-            const int nseg = __popc(m0) + __popc(m1);
-            int prev = 0;
-            if (lane == 0) prev = atomicAdd(&a.count[t.b * a.nkv + t.g], 1);
-            prev = __shfl_sync(0xffffffffu, prev, 0);
-            const bool last = prev == nseg - 1;
-            if (last) {
-                const unsigned lt_mask = (1u << lane) - 1u;
-                if (s0) sm.segs[__popc(m0 & lt_mask)] = lane;
-                if (s1) sm.segs[__popc(m0) + __popc(m1 & lt_mask)] = lane + 32;
-            }
-            if (lane == 0) {
-                sm.nseg = nseg;
-                sm.last = last ? 1 : 0;
-            }
-        }
-        consumers_sync();
-        if (sm.last) {
-            // Merge the segments in chunk order (all loads of a step issued
-            // together): per head M = max m_s, then the weights e^(m_s - M)
-            // and L = sum e^(m_s - M) l_s, then o = sum e^(m_s - M) acc_s / L.
-            __threadfence();
-            const int nseg = sm.nseg;
-            float* ms = &sm.wacc[0][0][0];   // [8][kMaxChunks] segment maxima, then weights
-            float* ls = ms + 8 * kMaxChunks; // [8][kMaxChunks] segment sums
-            for (int e = tid; e < group * nseg; e += kConsumers * 32) {
-                const int h = e % group, i = e / group;
-                const float* pc = a.part + ((head0 + h) * a.max_chunks + sm.segs[i]) * kPart;
-                ms[h * kMaxChunks + i] = __ldcg(pc);
-                ls[h * kMaxChunks + i] = __ldcg(pc + 1);
-            }
-            consumers_sync();
-            if (tid < group) {
-                const int h = tid;
-                float M = -INFINITY;
-                for (int i = 0; i < nseg; ++i) M = fmaxf(M, ms[h * kMaxChunks + i]);
-                float Lsum = 0.f;
-                for (int i = 0; i < nseg; ++i) {
-                    const float wt = expf(ms[h * kMaxChunks + i] - M);
-                    ms[h * kMaxChunks + i] = wt;
-                    Lsum = fmaf(wt, ls[h * kMaxChunks + i], Lsum);
-                }
-                sm.wl[0][h] = Lsum;
-            }
-            consumers_sync();
-            for (int e = tid; e < group * kDh; e += kConsumers * 32) {
-                const int h = e >> 6, d = e & 63;
-                const float* ph = a.part + (head0 + h) * a.max_chunks * kPart + 2 + d;
-                float O = 0.f;
-                for (int i0 = 0; i0 < nseg; i0 += 8) {
-                    float v[8];
+    }
+}
+
+// Merge of the segments k_attn_flash wrote for one (row b, kv head g) per
+// block (grid B * nkv, kMergeThreads threads; thread e takes output (head
+// e / 64, dim e % 64)), in chunk order: M = max m_s, L = sum e^(m_s - M)
+// l_s, o = sum e^(m_s - M) acc_s / L (f32, and the f16 hi / lo pair when
+// o_hi is set).  Each thread issues the loads of eight segments at once.
+// flash_grid: the grid size the attention ran with (it fixes the segments).
+constexpr int kMergeThreads = fd::kGroupMax * fd::kDh;
+__global__ void __launch_bounds__(kMergeThreads) k_attn_merge(fd::Args a, int flash_grid) {
+    using namespace fd;
+    __shared__ int base[kMaxRows + 1], nch[kMaxRows], segs[kMaxChunks];
+    __shared__ int nseg_s;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int group = a.nh / a.nkv;
+    const int b = blockIdx.x / a.nkv, g = blockIdx.x % a.nkv;
+    if (group > kGroupMax || a.B > kMaxRows || b >= a.B) return;
+    if (warp == 0) {
+        row_table(a, base, nch, nullptr, nullptr);
+        __syncwarp();
+        const unsigned U = (unsigned)base[a.B], G = (unsigned)flash_grid;
+        const int n = nch[b];
+        const bool s0 = lane < n && seg_start(base, nch, b, g, lane, U, G);
+        const bool s1 = lane + 32 < n && seg_start(base, nch, b, g, lane + 32, U, G);
+        const unsigned m0 = __ballot_sync(0xffffffffu, s0), m1 = __ballot_sync(0xffffffffu, s1);
+        const unsigned lt_mask = (1u << lane) - 1u;
+        if (s0) segs[__popc(m0 & lt_mask)] = lane;
+        if (s1) segs[__popc(m0) + __popc(m1 & lt_mask)] = lane + 32;
+        if (lane == 0) nseg_s = __popc(m0) + __popc(m1);
+    }
+    __syncthreads();
+    const int nseg = nseg_s;
+    const int h = tid >> 6, d = tid & 63;
+    if (nseg == 0 || h >= group) return;  // invalid position: reported by the attention
+    const size_t head = (size_t)b * a.nh + (size_t)g * group + h;
+    const float* ph = a.part + head * a.max_chunks * kPart;
+    float M = -INFINITY, Lsum = 0.f, O = 0.f;
+    for (int i0 = 0; i0 < nseg; i0 += 8) {
+        float mv[8], lv[8], av[8];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        v[j] = i0 + j < nseg ? __ldcg(ph + sm.segs[i0 + j] * kPart) : 0.f;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        if (i0 + j < nseg) O = fmaf(ms[h * kMaxChunks + i0 + j], v[j], O);
-                }
-                const float ov = O / sm.wl[0][h];
-                const size_t oi = (head0 + h) * kDh + d;
-                a.o[oi] = ov;
-                if (a.o_hi) {
-                    const __half hi = __float2half_rn(ov);
-                    a.o_hi[oi] = hi;
-                    a.o_lo[oi] = __float2half_rn(ov - __half2float(hi));
-                }
-            }
-            if (tid == 0) a.count[t.b * a.nkv + t.g] = 0;
+        for (int j = 0; j < 8; ++j) {
+            const bool in = i0 + j < nseg;
+            const float* pc = ph + (in ? segs[i0 + j] : 0) * kPart;
+            mv[j] = in ? __ldcg(pc) : -INFINITY;
+            lv[j] = in ? __ldcg(pc + 1) : 0.f;
+            av[j] = in ? __ldcg(pc + 2 + d) : 0.f;
         }
-        consumers_sync();
+        // Running rescale over groups of eight segments; with nseg <= 8 (the
+        // usual case) this is the plain formula.
+        float m8 = mv[0];
+#pragma unroll
+        for (int j = 1; j < 8; ++j) m8 = fmaxf(m8, mv[j]);
+        const float Mn = fmaxf(M, m8);
+        const float c = M == -INFINITY ? 0.f : expf(M - Mn);
+        Lsum *= c;
+        O *= c;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float wt = mv[j] == -INFINITY ? 0.f : expf(mv[j] - Mn);
+            Lsum = fmaf(wt, lv[j], Lsum);
+            O = fmaf(wt, av[j], O);
+        }
+        M = Mn;
+    }
+    const float ov = O / Lsum;
+    const size_t oi = head * kDh + d;
+    a.o[oi] = ov;
+    if (a.o_hi) {
+        const __half hi = __float2half_rn(ov);
+        a.o_hi[oi] = hi;
+        a.o_lo[oi] = __float2half_rn(ov - __half2float(hi));
     }
 }
 

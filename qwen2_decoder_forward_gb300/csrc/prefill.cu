@@ -61,6 +61,53 @@ __global__ void __launch_bounds__(kT) k_norm_rows_split(const float* __restrict_
         put_split(hi, lo, (size_t)r * H + j, __fmul_rn(__fmul_rn(xr[j], s), w[j]));
 }
 
+// The same normalisation with one warp per row and every load of the row
+// issued at once (H a multiple of 4, H <= 32 * 4 * kNormSteps): rows * 32
+// threads in all, kT / 32 rows per CTA.
+constexpr int kNormSteps = 8;
+__global__ void __launch_bounds__(kT) k_norm_rows_split_w(const float* __restrict__ x, int rows, int H,
+                                                          const float* __restrict__ w, float eps,
+                                                          __half* __restrict__ hi, __half* __restrict__ lo) {
+    const int r = blockIdx.x * (kT / 32) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (r >= rows) return;
+    const float* xr = x + (size_t)r * H;
+    float4 v[kNormSteps];
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < kNormSteps; ++i) {
+        const int j = 4 * lane + 128 * i;
+        v[i] = j < H ? *reinterpret_cast<const float4*>(xr + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < kNormSteps; ++i) {
+        ss = fmaf(v[i].x, v[i].x, ss);
+        ss = fmaf(v[i].y, v[i].y, ss);
+        ss = fmaf(v[i].z, v[i].z, ss);
+        ss = fmaf(v[i].w, v[i].w, ss);
+    }
+    const float s = rms_scale(warp_sum(ss), H, eps);
+#pragma unroll
+    for (int i = 0; i < kNormSteps; ++i) {
+        const int j = 4 * lane + 128 * i;
+        if (j >= H) break;
+        const float4 g = *reinterpret_cast<const float4*>(w + j);
+        const size_t o = (size_t)r * H + j;
+        put_split(hi, lo, o, __fmul_rn(__fmul_rn(v[i].x, s), g.x));
+        put_split(hi, lo, o + 1, __fmul_rn(__fmul_rn(v[i].y, s), g.y));
+        put_split(hi, lo, o + 2, __fmul_rn(__fmul_rn(v[i].z, s), g.z));
+        put_split(hi, lo, o + 3, __fmul_rn(__fmul_rn(v[i].w, s), g.w));
+    }
+}
+
+// Normalise rows of x into the f16 hi / lo operand pair.
+void launch_norm_split(const float* x, int rows, int H, const float* w, float eps, __half* hi, __half* lo,
+                       cudaStream_t st) {
+    if (H % 4 == 0 && H <= 32 * 4 * kNormSteps)
+        k_norm_rows_split_w<<<(rows + kT / 32 - 1) / (kT / 32), kT, 0, st>>>(x, rows, H, w, eps, hi, lo);
+    else
+        k_norm_rows_split<<<rows, kT, 0, st>>>(x, H, w, eps, hi, lo);
+}
+
 __global__ void __launch_bounds__(kT) k_norm_rows(const float* __restrict__ x, int H, const float* __restrict__ w,
                                                   float eps, float* __restrict__ out) {
     __shared__ float red[kT / 32];
@@ -381,7 +428,7 @@ cudaError_t enqueue_prefill(Ctx& c, int rows, int n_keep, const PrefillPlan& pla
         e.kind = kEpiQKV;
         e.bias = L.bqkv;
         if (tensor) {
-            k_norm_rows_split<<<cur, kT, 0, st>>>(x, H, L.attn_norm, g.rms_eps, w.xn_h, w.xn_l);
+            launch_norm_split(x, cur, H, L.attn_norm, g.rms_eps, w.xn_h, w.xn_l, st);
             cudaError_t err = tc_gemm_qkv(c, l, cur, e, st);
             if (err != cudaSuccess) return err;
         } else {
@@ -428,7 +475,7 @@ cudaError_t enqueue_prefill(Ctx& c, int rows, int n_keep, const PrefillPlan& pla
             // o_proj + residual; RMSNorm, gate/up + SiLU * up, down + residual.
             cudaError_t err = tc_gemm_o(c, l, cur, x, st);
             if (err == cudaSuccess) {
-                k_norm_rows_split<<<cur, kT, 0, st>>>(x, H, L.ffn_norm, g.rms_eps, w.xn_h, w.xn_l);
+                launch_norm_split(x, cur, H, L.ffn_norm, g.rms_eps, w.xn_h, w.xn_l, st);
                 err = tc_gemm_gu(c, l, cur, st);
             }
             if (err == cudaSuccess) err = tc_gemm_down(c, l, cur, x, st);

@@ -89,18 +89,33 @@ __global__ void __launch_bounds__(kT) k_attn_prefill_mma(PrefillAttnArgs a, int 
     const float* kbase = a.kv + (cache0 + g) * head_stride;
     const float* vbase = a.kv + (cache0 + a.nkv + g) * head_stride;
 
-    for (int j0 = 0; j0 <= pmax; j0 += kKT) {
+    // Each thread stages four (key, 4-dim) pieces of K and V per tile; the
+    // next tile's loads are issued before the current tile's products, so
+    // they arrive while the MMAs run.
+    constexpr int kPieces = kKT * (kD / 4) / kT;
+    float4 kr[kPieces], vr[kPieces];
+    auto load_tile = [&](int j0) {
         const int nj = min(kKT, pmax + 1 - j0);
-        __syncthreads();
-        // Stage keys j0 .. j0 + nj - 1 (zeros past them): k and v rounded to
-        // f16, v's remainder as a second f16.
-        for (int e = tid; e < kKT * (kD / 4); e += kT) {
-            const int j = e / (kD / 4), d = 4 * (e % (kD / 4));
-            float4 kk = make_float4(0.f, 0.f, 0.f, 0.f), vv = kk;
+#pragma unroll
+        for (int i = 0; i < kPieces; ++i) {
+            const int e = tid + kT * i, j = e / (kD / 4), d = 4 * (e % (kD / 4));
+            kr[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            vr[i] = kr[i];
             if (j < nj) {
-                kk = __ldcg(reinterpret_cast<const float4*>(kbase + (size_t)(j0 + j) * kD + d));
-                vv = __ldcg(reinterpret_cast<const float4*>(vbase + (size_t)(j0 + j) * kD + d));
+                kr[i] = __ldcg(reinterpret_cast<const float4*>(kbase + (size_t)(j0 + j) * kD + d));
+                vr[i] = __ldcg(reinterpret_cast<const float4*>(vbase + (size_t)(j0 + j) * kD + d));
             }
+        }
+    };
+    load_tile(0);
+    for (int j0 = 0; j0 <= pmax; j0 += kKT) {
+        __syncthreads();
+        // Stage keys j0 .. j0 + 63 (zeros past the last): k and v rounded to
+        // f16, v's remainder as a second f16.
+#pragma unroll
+        for (int i = 0; i < kPieces; ++i) {
+            const int e = tid + kT * i, j = e / (kD / 4), d = 4 * (e % (kD / 4));
+            const float4 kk = kr[i], vv = vr[i];
             const __half2 k01 = __floats2half2_rn(kk.x, kk.y), k23 = __floats2half2_rn(kk.z, kk.w);
             const __half2 v01 = __floats2half2_rn(vv.x, vv.y), v23 = __floats2half2_rn(vv.z, vv.w);
             const float2 f01 = __half22float2(v01), f23 = __half22float2(v23);
@@ -112,6 +127,7 @@ __global__ void __launch_bounds__(kT) k_attn_prefill_mma(PrefillAttnArgs a, int 
             *reinterpret_cast<__half2*>(&sm.vl[j][d + 2]) = __floats2half2_rn(vv.z - f23.x, vv.w - f23.y);
         }
         __syncthreads();
+        if (j0 + kKT <= pmax) load_tile(j0 + kKT);
         if (!compute) continue;
         if (j0 == 0) {
 #pragma unroll

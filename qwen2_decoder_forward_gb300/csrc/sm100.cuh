@@ -40,10 +40,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, unsigned parity) {
     return ok != 0;
 }
 // Waits for the phase of parity `parity` to complete; gives up (returns
-// false) once the global timer passes `deadline`.
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, unsigned parity, unsigned long long deadline) {
+// false) after `timeout_ns` of the global timer.  The timer is read only
+// once the first try finds the phase still open.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, unsigned parity, unsigned long long timeout_ns) {
+    if (mbar_try_wait(b, parity)) return true;
+    const unsigned long long t0 = global_ns();
     while (!mbar_try_wait(b, parity))
-        if (global_ns() > deadline) return false;
+        if (global_ns() - t0 > timeout_ns) return false;
     return true;
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t* b) {

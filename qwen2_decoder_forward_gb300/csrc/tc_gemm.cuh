@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
                 const int m0 = (t % n_m) * kBM, n0 = (t / n_m) * BN;
                 for (int kb = 0; kb < nk; ++kb) {
-                    if (!mbar_wait(&empty[s], ph ^ 1u, global_ns() + kWaitNs)) {
+                    if (!mbar_wait(&empty[s], ph ^ 1u, kWaitNs)) {
                         ok = false;
                         break;
                     }
@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Wait for this thread's last loads to land (immediate when the
             // MMAs consumed them) so no copy is in flight at exit.
             for (long long j = issued - 1; j >= 0 && j >= issued - C::kStages; --j)
-                if (!mbar_wait(&full[j % C::kStages], (unsigned)((j / C::kStages) & 1), global_ns() + kWaitNs))
+                if (!mbar_wait(&full[j % C::kStages], (unsigned)((j / C::kStages) & 1), kWaitNs))
                     ok = false;
         }
     } else if (warp == 1) {
@@ -122,14 +122,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             int s = 0, acc = 0;
             unsigned ph = 0, aph = 0;
             for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-                if (!mbar_wait(&tempty[acc], aph ^ 1u, global_ns() + kWaitNs)) {
+                if (!mbar_wait(&tempty[acc], aph ^ 1u, kWaitNs)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(acc * BN);
                 for (int kb = 0; kb < nk; ++kb) {
-                    if (!mbar_wait(&full[s], ph, global_ns() + kWaitNs)) {
+                    if (!mbar_wait(&full[s], ph, kWaitNs)) {
                         ok = false;
                         break;
                     }
@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // One lane waits; the warp follows its verdict, so the
             // warp-collective TMEM loads below never diverge.
             int got = 1;
-            if (lane == 0) got = mbar_wait(&tfull[acc], aph, global_ns() + kWaitNs) ? 1 : 0;
+            if (lane == 0) got = mbar_wait(&tfull[acc], aph, kWaitNs) ? 1 : 0;
             got = __shfl_sync(0xffffffffu, got, 0);
             if (!got) {
                 ok = false;

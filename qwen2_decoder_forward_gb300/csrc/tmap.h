@@ -42,4 +42,22 @@ inline bool encode_kmajor_f16(CUtensorMap* m, const void* base, uint64_t rows, u
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Map of a row-major f32 matrix [rows][64] read in boxes of 32 floats (128
+// bytes) x box_rows rows with the 128-byte swizzle; reads past `rows` return
+// zeros.  Requirements checked here: base 16-byte aligned, rows < 2^31,
+// box_rows in [1, 256].
+inline bool encode_rows64_f32(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc || !base || (reinterpret_cast<uintptr_t>(base) & 15) || rows == 0 || rows >= (1ull << 31) ||
+        box_rows == 0 || box_rows > 256)
+        return false;
+    const cuuint64_t dims[2] = {64, rows};
+    const cuuint64_t strides[1] = {64 * 4};
+    const cuuint32_t box[2] = {32, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace qwen2
