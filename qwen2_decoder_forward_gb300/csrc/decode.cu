@@ -845,6 +845,22 @@ cudaError_t attn_batched(const Ctx& c, const StepArgs& a, int l, cudaStream_t st
     f.L = a.L;
     f.layer = l;
     f.max_chunks = c.ws.att_max_chunks;
+    // The rest of this layer's weights (o_proj, gate/up, down, biases,
+    // norms) and the next layer's Q/K/V, contiguous in the packed blob.
+    f.pf = nullptr;
+    f.pf_bytes = 0;
+    if (c.cfg.weight_format == QWEN2_WEIGHTS_Q8_0) {
+        const DevLayer& L = c.layers[l];
+        const unsigned char* b0 = reinterpret_cast<const unsigned char*>(L.wo.q);
+        const unsigned char* b1 = l + 1 < c.cfg.n_layer
+                                      ? reinterpret_cast<const unsigned char*>(c.layers[l + 1].wqkv.d) +
+                                            (size_t)c.layers[l + 1].wqkv.rows * (c.layers[l + 1].wqkv.k / 32) * 2
+                                      : reinterpret_cast<const unsigned char*>(L.ffn_norm + c.cfg.hidden);
+        if (b1 > b0 && (reinterpret_cast<uintptr_t>(b0) & 15) == 0) {
+            f.pf = b0;
+            f.pf_bytes = (size_t)(b1 - b0) & ~(size_t)15;
+        }
+    }
     const int grid = 2 * c.n_sm;
     k_attn_flash<<<grid, fd::kThreads, fd::kSmemBytes, st>>>(c.kvmap, f);
     k_attn_merge<<<a.B * a.nkv, kMergeThreads, 0, st>>>(f, grid);

@@ -64,6 +64,8 @@ struct Args {
     __half* o_lo;
     int* err;
     int B, nh, nkv, n_ctx, L, layer, max_chunks;
+    const unsigned char* pf;  // nullable: bytes to prefetch into L2 for the kernels that follow
+    size_t pf_bytes;          // (a multiple of 16, 16-byte aligned)
 };
 
 struct Smem {
@@ -222,6 +224,17 @@ __global__ void __launch_bounds__(fd::kThreads, 2)
         // Producer: one lane issues the four tensor copies of each unit.
         if (lane == 0) {
             sm100::tma_prefetch_desc(&kvmap);
+            // This CTA's share of the weights the next products stream: the
+            // attention leaves DRAM bandwidth over, so they can wait in L2.
+            if (a.pf) {
+                const size_t share = (a.pf_bytes / gridDim.x + 15) & ~(size_t)15;
+                const size_t b0 = share * blockIdx.x;
+                const size_t b1 = min(a.pf_bytes, b0 + share);
+                for (size_t o = b0; o < b1; o += 16384)
+                    sm100::prefetch_l2(a.pf + o, (unsigned)min((size_t)16384, b1 - o));
+            }
+            // K and V are read once: first out of L2.
+            const uint64_t pol = sm100::policy_evict_first();
             int k = 0;
             for (int u = u0; u < u1; ++u, ++k) {
                 const int s = k % kStages;
@@ -239,10 +252,10 @@ __global__ void __launch_bounds__(fd::kThreads, 2)
                 sm100::mbar_expect_tx(&sm.full[s], kUnitBytes + qbytes);
                 if (first)
                     bulk_g2s(sm.qs[s], a.q + ((size_t)t.b * a.nh + (size_t)t.g * group) * kDh, qbytes, &sm.full[s]);
-                sm100::tma_load_2d(sm.ring[s][0][0], &kvmap, 0, yk, &sm.full[s]);
-                sm100::tma_load_2d(sm.ring[s][0][1], &kvmap, 32, yk, &sm.full[s]);
-                sm100::tma_load_2d(sm.ring[s][1][0], &kvmap, 0, yv, &sm.full[s]);
-                sm100::tma_load_2d(sm.ring[s][1][1], &kvmap, 32, yv, &sm.full[s]);
+                sm100::tma_load_2d_hint(sm.ring[s][0][0], &kvmap, 0, yk, &sm.full[s], pol);
+                sm100::tma_load_2d_hint(sm.ring[s][0][1], &kvmap, 32, yk, &sm.full[s], pol);
+                sm100::tma_load_2d_hint(sm.ring[s][1][0], &kvmap, 0, yv, &sm.full[s], pol);
+                sm100::tma_load_2d_hint(sm.ring[s][1][1], &kvmap, 32, yv, &sm.full[s], pol);
             }
             // Every copy lands before the CTA exits, even after an abort.
             for (int kk = k > kStages ? k - kStages : 0; kk < k; ++kk)

@@ -405,7 +405,8 @@ dim3 gemm_grid(int M, int N) { return dim3((N + GBN - 1) / GBN, (M + GBM - 1) / 
 }  // namespace
 
 cudaError_t prefill_set_smem_limits() {
-    return cudaFuncSetAttribute(k_attn_prefill, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
+    cudaError_t e = cudaFuncSetAttribute(k_attn_prefill, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
+    return e == cudaSuccess ? prefill_attn_mma_set_smem() : e;
 }
 
 cudaError_t enqueue_prefill(Ctx& c, int rows, int n_keep, const PrefillPlan& plan, float* logits_dev,

@@ -67,6 +67,7 @@ cudaError_t tc_gemm_down(const Ctx& c, int layer, int M, float* x, cudaStream_t 
 // Causal GQA attention of the tensor-core path (prefill_attn.cu): writes
 // a.o_h / a.o_l; grid (nkv, n_blk) over the 16-row query blocks.
 cudaError_t enqueue_attn_prefill_mma(const PrefillAttnArgs& a, int layer, int n_blk, cudaStream_t st);
+cudaError_t prefill_attn_mma_set_smem();
 
 cudaError_t enqueue_prefill(Ctx& c, int rows, int n_keep, const PrefillPlan& plan, float* logits_dev,
                             int* ids_dev, cudaStream_t st);

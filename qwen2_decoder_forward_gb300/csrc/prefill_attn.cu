@@ -25,6 +25,7 @@ constexpr int kLd = kD + 8;     // padded shared row (halves): conflict-free ldm
 constexpr float kScaleLog2 = 0.125f * 1.4426950408889634f;  // 1/sqrt(64) * log2(e)
 
 struct AttnTcSmem {
+    float stage[2][2][kKT][kD];   // f32 K and V tiles in flight (double-buffered, cp.async)
     __half k[kKT][kLd];
     __half vh[kKT][kLd];
     __half vl[kKT][kLd];
@@ -54,8 +55,16 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-__global__ void __launch_bounds__(kT) k_attn_prefill_mma(PrefillAttnArgs a, int layer) {
-    __shared__ __align__(16) AttnTcSmem sm;
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+    // 16 bytes from global to shared memory; zeros when !valid.
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+
+__global__ void __launch_bounds__(kT, 2) k_attn_prefill_mma(PrefillAttnArgs a, int layer) {
+    extern __shared__ __align__(16) unsigned char pa_smem[];
+    AttnTcSmem& sm = *reinterpret_cast<AttnTcSmem*>(pa_smem);
     const int g = blockIdx.x, blk = blockIdx.y;
     const int r0 = a.blk_row0[blk], nr = a.blk_nrows[blk];
     const int group = a.nh / a.nkv;
@@ -89,33 +98,38 @@ __global__ void __launch_bounds__(kT) k_attn_prefill_mma(PrefillAttnArgs a, int 
     const float* kbase = a.kv + (cache0 + g) * head_stride;
     const float* vbase = a.kv + (cache0 + a.nkv + g) * head_stride;
 
-    // Each thread stages four (key, 4-dim) pieces of K and V per tile; the
-    // next tile's loads are issued before the current tile's products, so
-    // they arrive while the MMAs run.
+    // Each tile's f32 K and V rows travel with cp.async into one of two
+    // staging buffers, one tile ahead of the products; each thread then
+    // converts its four (key, 4-dim) pieces of the current tile.
     constexpr int kPieces = kKT * (kD / 4) / kT;
-    float4 kr[kPieces], vr[kPieces];
-    auto load_tile = [&](int j0) {
+    auto issue_tile = [&](int j0, int buf) {
         const int nj = min(kKT, pmax + 1 - j0);
 #pragma unroll
         for (int i = 0; i < kPieces; ++i) {
             const int e = tid + kT * i, j = e / (kD / 4), d = 4 * (e % (kD / 4));
-            kr[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            vr[i] = kr[i];
-            if (j < nj) {
-                kr[i] = __ldcg(reinterpret_cast<const float4*>(kbase + (size_t)(j0 + j) * kD + d));
-                vr[i] = __ldcg(reinterpret_cast<const float4*>(vbase + (size_t)(j0 + j) * kD + d));
-            }
+            const bool in = j < nj;
+            const size_t off = (size_t)(in ? j0 + j : 0) * kD + d;
+            cp_async16(&sm.stage[buf][0][j][d], kbase + off, in);
+            cp_async16(&sm.stage[buf][1][j][d], vbase + off, in);
         }
+        asm volatile("cp.async.commit_group;" ::: "memory");
     };
-    load_tile(0);
-    for (int j0 = 0; j0 <= pmax; j0 += kKT) {
+    issue_tile(0, 0);
+    for (int j0 = 0, buf = 0; j0 <= pmax; j0 += kKT, buf ^= 1) {
+        if (j0 + kKT <= pmax) {
+            issue_tile(j0 + kKT, buf ^ 1);
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+        }
         __syncthreads();
         // Stage keys j0 .. j0 + 63 (zeros past the last): k and v rounded to
         // f16, v's remainder as a second f16.
 #pragma unroll
         for (int i = 0; i < kPieces; ++i) {
             const int e = tid + kT * i, j = e / (kD / 4), d = 4 * (e % (kD / 4));
-            const float4 kk = kr[i], vv = vr[i];
+            const float4 kk = *reinterpret_cast<const float4*>(&sm.stage[buf][0][j][d]);
+            const float4 vv = *reinterpret_cast<const float4*>(&sm.stage[buf][1][j][d]);
             const __half2 k01 = __floats2half2_rn(kk.x, kk.y), k23 = __floats2half2_rn(kk.z, kk.w);
             const __half2 v01 = __floats2half2_rn(vv.x, vv.y), v23 = __floats2half2_rn(vv.z, vv.w);
             const float2 f01 = __half22float2(v01), f23 = __half22float2(v23);
@@ -127,7 +141,6 @@ __global__ void __launch_bounds__(kT) k_attn_prefill_mma(PrefillAttnArgs a, int 
             *reinterpret_cast<__half2*>(&sm.vl[j][d + 2]) = __floats2half2_rn(vv.z - f23.x, vv.w - f23.y);
         }
         __syncthreads();
-        if (j0 + kKT <= pmax) load_tile(j0 + kKT);
         if (!compute) continue;
         if (j0 == 0) {
 #pragma unroll
@@ -234,8 +247,13 @@ __global__ void __launch_bounds__(kT) k_attn_prefill_mma(PrefillAttnArgs a, int 
 }  // namespace
 
 cudaError_t enqueue_attn_prefill_mma(const PrefillAttnArgs& a, int layer, int n_blk, cudaStream_t st) {
-    k_attn_prefill_mma<<<dim3(a.nkv, n_blk), kT, 0, st>>>(a, layer);
+    k_attn_prefill_mma<<<dim3(a.nkv, n_blk), kT, sizeof(AttnTcSmem), st>>>(a, layer);
     return cudaGetLastError();
+}
+
+cudaError_t prefill_attn_mma_set_smem() {
+    return cudaFuncSetAttribute(k_attn_prefill_mma, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)sizeof(AttnTcSmem));
 }
 
 }  // namespace qwen2

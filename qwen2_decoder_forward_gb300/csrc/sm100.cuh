@@ -72,6 +72,27 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, int
         : "memory");
 }
 
+// L2 eviction-priority policies for the cache-hinted copies below.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+// 2-D tiled load as tma_load_2d, with an L2 eviction-priority hint.
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m, int x, int y, uint64_t* bar,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+// Asynchronous prefetch of `bytes` (a multiple of 16, 16-byte aligned) of
+// global memory into L2; no completion to wait for.
+__device__ __forceinline__ void prefetch_l2(const void* p, unsigned bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // ---- tcgen05 -------------------------------------------------------------------
 // TMEM allocation of `cols` columns (a power of two >= 32) by one whole warp;
 // the TMEM address is written to shared memory at `slot`.
