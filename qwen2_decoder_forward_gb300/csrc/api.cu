@@ -408,6 +408,27 @@ int qwen2_prefill(qwen2_ctx* h, int32_t n_seq, const int32_t* seq_ids, const int
         off += n;
     }
     const int n_keep = (int)keep.size();
+    {
+        // Longest query blocks (most keys) first, so the causal attention's
+        // heavy blocks do not form the tail of the grid.
+        std::vector<int> ord(b0.size());
+        for (size_t i = 0; i < ord.size(); ++i) ord[i] = (int)i;
+        auto last_pos = [&](int i) {
+            int m = 0;
+            for (int r = 0; r < bn[i]; ++r) m = std::max(m, (int)positions[b0[i] + r]);
+            return m;
+        };
+        std::vector<int> key(ord.size());
+        for (size_t i = 0; i < ord.size(); ++i) key[i] = last_pos((int)i);
+        std::stable_sort(ord.begin(), ord.end(), [&](int x, int y) { return key[x] > key[y]; });
+        std::vector<int> s0(ord.size()), sn(ord.size());
+        for (size_t i = 0; i < ord.size(); ++i) {
+            s0[i] = b0[ord[i]];
+            sn[i] = bn[ord[i]];
+        }
+        b0.swap(s0);
+        bn.swap(sn);
+    }
     plan.insert(plan.end(), b0.begin(), b0.end());
     plan.insert(plan.end(), bn.begin(), bn.end());
     plan.insert(plan.end(), kb0.begin(), kb0.end());

@@ -71,19 +71,27 @@ __global__ void __launch_bounds__(kT, 2) k_attn_prefill_mma(PrefillAttnArgs a, i
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gi = lane >> 2, ti = lane & 3;  // MMA fragment row group, thread in group
     const int slot = a.slot[r0];
-    int pmax = 0;
-    for (int r = 0; r < nr; ++r) pmax = max(pmax, a.pos[r0 + r]);
+    // Largest position of the block's rows (one load per lane, then a warp
+    // max: no chain of dependent loads).
+    int pmax = lane < nr ? a.pos[r0 + lane] : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) pmax = max(pmax, __shfl_xor_sync(0xffffffffu, pmax, o));
     const bool compute = warp < group;
     const int hq = g * group + warp;
 
-    // This warp's 16 query rows as f16 (rows past nr are zero).
+    // This warp's 16 query rows as f16 (rows past nr are zero); lane l
+    // takes dims 2l, 2l + 1 of every row, all 16 loads issued together.
+    static_assert(kD == 64, "one float2 per lane per row");
     if (compute) {
-        for (int e = lane; e < 16 * (kD / 2); e += 32) {
-            const int r = e / (kD / 2), d = 2 * (e % (kD / 2));
-            float2 v = make_float2(0.f, 0.f);
-            if (r < nr) v = *reinterpret_cast<const float2*>(a.q + (size_t)(r0 + r) * a.nh * kD + (size_t)hq * kD + d);
-            *reinterpret_cast<__half2*>(&sm.q[warp][r][d]) = __floats2half2_rn(v.x, v.y);
-        }
+        float2 qv[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+            qv[r] = r < nr ? *reinterpret_cast<const float2*>(a.q + (size_t)(r0 + r) * a.nh * kD + (size_t)hq * kD +
+                                                               2 * lane)
+                           : make_float2(0.f, 0.f);
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+            *reinterpret_cast<__half2*>(&sm.q[warp][r][2 * lane]) = __floats2half2_rn(qv[r].x, qv[r].y);
     }
     const int pa = gi < nr ? a.pos[r0 + gi] : -1;          // positions of this thread's rows
     const int pb = gi + 8 < nr ? a.pos[r0 + gi + 8] : -1;
