@@ -223,6 +223,8 @@ struct ProNorm {
     }
 };
 
+// Epi::start(n_cta0, rows_cta, B): all threads, before the main loop (the
+// CTA's output rows are n_cta0 .. n_cta0 + rows_cta - 1).
 // Epi::pair(b, n, v0, v1, chunk): outputs (b, n) and (b, n + 1), n even,
 // partial over k chunk `chunk`.  Epi::finish(): once per CTA, all threads,
 // after every pair of the CTA.
@@ -262,6 +264,10 @@ __global__ void __launch_bounds__(W * 32) k_bgemm_q8(Pro pro, int B, int K, int 
     for (int i = 0; i < DEPTH; ++i)
         if (ks + i * KS < nb) load_block<NTW>(Q, D, N, K, n0, gi, ti, kc0 + (ks + i * KS) * 32, wq[i]);
 
+    // Loads the epilogue needs from global memory go out now, to land in
+    // shared memory long before the epilogue (the barrier below publishes
+    // them).
+    epi.start(blockIdx.x * (kGroups * NTW * 8), kGroups * NTW * 8, B);
     if (tid == 0) {
         mbar_init(bar, 1);
         mbar_init_fence();

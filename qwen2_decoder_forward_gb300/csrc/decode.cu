@@ -474,25 +474,96 @@ __global__ void __launch_bounds__(kThreads) k_split_rows(const float* __restrict
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) bg::split_h(src[i], hi[i], lo[i]);
 }
 
+// Q/K/V pairs of the batched product.  start() brings the rows' positions
+// and cache slots, the CTA's biases and the RoPE factors of its pairs into
+// shared memory while the product runs, so the epilogue itself issues no
+// dependent global loads.
+constexpr int kQkvRowsMax = 16;   // output rows per CTA this epilogue supports
+__shared__ int qkv_pos_s[32], qkv_slot_s[32];
+__shared__ float qkv_bias_s[kQkvRowsMax];
+__shared__ float2 qkv_rope_s[32][kQkvRowsMax / 2];
 struct EpiQkvQ8 {
     StepArgs a;
     int layer;
     const float* bias;
-    __device__ __forceinline__ void pair(int b, int n, float v0, float v1, int) {
-        qkv_pair_epilogue(a, layer, n >> 1, b, v0, v1, bias);
+    int n_cta0;
+    __device__ __forceinline__ void start(int n0, int rows, int B) {
+        n_cta0 = n0;
+        const int tid = threadIdx.x;
+        if (rows > kQkvRowsMax || B > 32) {
+            if (tid == 0) raise_guard(a.err, kGuardShape);
+            return;
+        }
+        const int N = (a.nh + 2 * a.nkv) * kHd;
+        if (tid < 32) {
+            qkv_pos_s[tid] = tid < B ? a.pos[tid] : 0;
+            qkv_slot_s[tid] = tid < B ? a.slot[tid] : 0;
+        }
+        if (tid < rows && n0 + tid < N) qkv_bias_s[tid] = bias[n0 + tid];
+        const int np = rows / 2;
+        for (int e = tid; e < 32 * np; e += blockDim.x) {
+            const int b = e / np, k = e % np;
+            const int p = b < B ? a.pos[b] : 0;
+            const int i = ((n0 + 2 * k) % kHd) >> 1;
+            qkv_rope_s[b][k] = (p >= 0 && p < a.n_ctx) ? a.rope[(size_t)p * (kHd / 2) + i] : make_float2(1.f, 0.f);
+        }
+    }
+    // Packed rows (n, n + 1) = elements i and i + hd/2 of head slot s: bias,
+    // NeoX rotation for q and k, then q to the query buffer, k and v to the
+    // cache slot of the row's position (the arithmetic of qkv_pair_epilogue).
+    __device__ __forceinline__ void pair(int b, int n, float d0, float d1, int) {
+        const int s = n / kHd, i = (n % kHd) >> 1, k = (n - n_cta0) >> 1;
+        const int p = qkv_pos_s[b];
+        if (p < 0 || p >= a.n_ctx) {
+            raise_guard(a.err, kGuardPosition);
+            return;
+        }
+        const float v0 = d0 + qkv_bias_s[n - n_cta0];
+        const float v1 = d1 + qkv_bias_s[n - n_cta0 + 1];
+        if (s < a.nh + a.nkv) {
+            float ra, rb;
+            rope_pair(v0, v1, qkv_rope_s[b][k], ra, rb);
+            if (s < a.nh) {
+                float* qr = a.q + (size_t)b * a.nh * kHd + s * kHd;
+                qr[i] = ra;
+                qr[i + kHd / 2] = rb;
+            } else {
+                float* kr = kv_ptr(a, qkv_slot_s[b], layer, 0, s - a.nh, p);
+                kr[i] = ra;
+                kr[i + kHd / 2] = rb;
+            }
+        } else {
+            float* vr = kv_ptr(a, qkv_slot_s[b], layer, 1, s - a.nh - a.nkv, p);
+            vr[i] = v0;
+            vr[i + kHd / 2] = v1;
+        }
     }
     __device__ __forceinline__ void finish() {}
 };
 
+// Residual add of the batched product: start() loads the CTA's slice of x
+// (rows b < B, columns n_cta0 .. n_cta0 + rows - 1) into shared memory.
+constexpr int kResRowsMax = 16;
+__shared__ float res_x_s[32][kResRowsMax];
 struct EpiResidualQ8 {
     float* x;
     int H;
+    int n_cta0 = 0;
+    int* err = nullptr;
+    __device__ __forceinline__ void start(int n0, int rows, int B) {
+        n_cta0 = n0;
+        if (rows > kResRowsMax || B > 32) {
+            if (threadIdx.x == 0) raise_guard(err, kGuardShape);
+            return;
+        }
+        for (int e = threadIdx.x; e < B * rows; e += blockDim.x) {
+            const int b = e / rows, c = e % rows;
+            if (n0 + c < H) res_x_s[b][c] = x[(size_t)b * H + n0 + c];
+        }
+    }
     __device__ __forceinline__ void pair(int b, int n, float v0, float v1, int) {
-        float2* d = reinterpret_cast<float2*>(x + (size_t)b * H + n);
-        float2 t = *d;
-        t.x += v0;
-        t.y += v1;
-        *d = t;
+        const int c = n - n_cta0;
+        *reinterpret_cast<float2*>(x + (size_t)b * H + n) = make_float2(res_x_s[b][c] + v0, res_x_s[b][c + 1] + v1);
     }
     __device__ __forceinline__ void finish() {}
 };
@@ -502,6 +573,7 @@ struct EpiResidualQ8 {
 // chunks written) adds them to the residual x in chunk order.
 struct EpiDownQ8 {
     static constexpr int kMaxParts = 16;
+    __device__ __forceinline__ void start(int, int, int) {}
     float* part;
     size_t stride;  // floats between chunks
     int N;          // output rows (hidden)
@@ -564,6 +636,7 @@ struct EpiSwigluQ8 {
     __half* hi;
     __half* lo;
     int I;
+    __device__ __forceinline__ void start(int, int, int) {}
     __device__ __forceinline__ void pair(int b, int n, float g, float u, int) {
         const size_t i = (size_t)b * I + (n >> 1);
         bg::split_h(silu_f(g) * u, hi[i], lo[i]);
@@ -590,6 +663,7 @@ struct EpiLmQ8 {
     int* err;
     float bv[4];
     int bi[4];
+    __device__ __forceinline__ void start(int, int, int) {}
     __device__ __forceinline__ void pair(int b, int n, float v0, float v1, int) {
         if (logits) {
             logits[(size_t)b * V + n] = v0;
@@ -808,7 +882,7 @@ cudaError_t o_ffn_q8(Ctx& c, int l, float* x, int B, cudaStream_t st) {
     const DevLayer& L = c.layers[l];
     const int H = c.cfg.hidden, I = c.cfg.intermediate, nq = c.cfg.n_head * kHd;
     Workspace& w = c.ws;
-    cudaError_t e = bgemm<MT, 1, 8>(c, bg::ProCopy{w.q8_ah, w.q8_al}, B, nq, nq, L.wo, H, EpiResidualQ8{x, H}, st);
+    cudaError_t e = bgemm<MT, 1, 8>(c, bg::ProCopy{w.q8_ah, w.q8_al}, B, nq, nq, L.wo, H, EpiResidualQ8{x, H, 0, c.err}, st);
     if (e != cudaSuccess) return e;
     e = bgemm<MT, 4, 4>(c, bg::ProNorm{x, L.ffn_norm, c.cfg.rms_eps, nullptr}, B, H, H, L.wgu, 2 * I,
                         EpiSwigluQ8{w.q8_mh, w.q8_ml, I}, st);
@@ -873,7 +947,7 @@ cudaError_t layer_q8(Ctx& c, const StepArgs& a, int l, cudaStream_t st) {
     const int H = c.cfg.hidden;
     Workspace& w = c.ws;
     cudaError_t e = bgemm<MT, 1, 8>(c, bg::ProNorm{a.x, L.attn_norm, a.eps, nullptr}, a.B, H, H, L.wqkv, c.nqkv,
-                                    EpiQkvQ8{a, l, L.bqkv}, st);
+                                    EpiQkvQ8{a, l, L.bqkv, 0}, st);
     if (e != cudaSuccess) return e;
     StepArgs ao = a;
     ao.o_hi = w.q8_ah;

@@ -272,8 +272,10 @@ __global__ void __launch_bounds__(kT) k_attn_prefill(PrefillAttnArgs a, int laye
     const int nv = nr * group;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int slot = a.slot[r0];
-    int pmax = 0;
-    for (int r = 0; r < nr; ++r) pmax = max(pmax, a.pos[r0 + r]);
+    // Largest position of the block's rows: one load per lane, a warp max.
+    int pmax = lane < nr ? a.pos[r0 + lane] : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) pmax = max(pmax, __shfl_xor_sync(0xffffffffu, pmax, o));
     for (int e = tid; e < nv * kHd; e += kT) {
         const int v = e / kHd, d = e % kHd;
         const int ri = v / group, h = v % group;
