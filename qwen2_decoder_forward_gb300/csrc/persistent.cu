@@ -214,18 +214,26 @@ __device__ __forceinline__ int split(int n, int c, int G) { return (int)(((long 
 constexpr int kPkRep = 4;
 struct PkLayout {
     int qkv, x1, m, x2, att, per_layer;          // offsets of copy 0
-    int n_qkv, n_x, n_m, n_att;                  // packets per copy
+    int n_qkv, n_x, n_m, n_att, n_o;             // packets per copy
     __host__ __device__ PkLayout(int nqkv, int H, int I, int nh, int max_chunks) {
         n_qkv = nqkv;
         n_x = H;
         n_m = I;
         n_att = nh * max_chunks * kPartStride;
+        n_o = nh * kHd;
         qkv = 0;
         x1 = qkv + kPkRep * n_qkv;
         m = x1 + kPkRep * n_x;
         x2 = m + kPkRep * n_m;
         att = x2 + kPkRep * n_x;
         per_layer = att + kPkRep * n_att;
+    }
+    // The merged attention output of layer l (long context), kept after
+    // all layers' buffers and the argmax pairs of `grid` CTAs: placing it
+    // inside each layer's block shifted the hot buffers and cost about 5 %
+    // at short context (measured).
+    __host__ __device__ size_t o_base(int L, int grid, int l) const {
+        return (size_t)L * per_layer + 2 * (size_t)grid + (size_t)l * kPkRep * n_o;
     }
 };
 
@@ -401,6 +409,22 @@ __device__ __noinline__ void merge_staged(const float* stg, int nh, int n_chunks
         const int h = e / kHd, d = e % kHd;
         const float* ph = stg + (size_t)h * n_chunks * kPartStride;
         o[e] = attn_merge(n_chunks, d, [&](int cc, int i) { return ph[cc * kPartStride + i]; });
+    }
+}
+
+// Long-context merge of one head: gather its n_chunks partials into stg,
+// merge them with the attn_merge arithmetic (chunk order) and publish the
+// 64 outputs to every packet copy of dst.  A function of its own so that
+// the main loop's code generation does not change with it.
+__device__ __noinline__ void merge_head(PkReader& rd, const u64* att_h, int n_chunks, float* stg, u64* dst,
+                                        int copy_stride, unsigned ep) {
+    pk_gather<8>(rd, n_chunks * kPartStride, [&](int j) { return att_h + j; }, [&](int j, float v) { stg[j] = v; },
+                 [] {});
+    SyncCompute::sync();
+    const int tid = threadIdx.x;
+    if (tid < kHd) {
+        const float ov = attn_merge(n_chunks, tid, [&](int cc, int i) { return stg[cc * kPartStride + i]; });
+        pk_put_all(dst + tid, copy_stride, ov, ep);
     }
 }
 
@@ -585,7 +609,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
         if (l == 0) {
             for (int j = tid; j < H; j += kCompute) xr[j] = __half2float(a.E[(size_t)t * H + j]);
         } else {
-            wait_cnt((l - 1) * 5 + 4);
             gather(pk_prev + lay.x2 + (size_t)rc * lay.n_x, H, xr);
         }
         if (phase_end()) break;
@@ -692,15 +715,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
             const u64* att = pk + lay.att + (size_t)rc * lay.n_att;
             float* stg = act + H;
             const int whole = nh * n_chunks * kPartStride;
-            float Mv[4], Lv[4], Ov[4];
             wait_cnt(l * 5 + 1);
             mark(mb + 5);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                Mv[k] = -INFINITY;
-                Lv[k] = 0.f;
-                Ov[k] = 0.f;
-            }
             if (whole <= a.act_floats - H) {
                 // All partials in one gather: stg[h][c][66].
                 pk_gather<8>(rd, whole,
@@ -712,54 +728,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
                 SyncCompute::sync();
                 merge_staged(stg, nh, n_chunks, xs);
             } else {
-                // Long context: chunk maxima first, then (l, acc) a group of
-                // chunks at a time.
-                float* mst = stg;                        // [nh][n_chunks]
-                float* gst = mst + nh * a.max_chunks;    // [nh][group][65]
-                const int gc_max = a.merge_group;
-                pk_gather<4>(rd, nh * n_chunks,
-                             [&](int j) {
-                                 return att + ((size_t)(j / n_chunks) * a.max_chunks + j % n_chunks) * kPartStride;
-                             },
-                             [&](int j, float v) { mst[j] = v; }, idle);
-                SyncCompute::sync();
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int e = tid + 256 * k;
-                    if (e < nh * kHd)
-                        for (int cc = 0; cc < n_chunks; ++cc) Mv[k] = fmaxf(Mv[k], mst[(e / kHd) * n_chunks + cc]);
-                }
-                for (int c0 = 0; c0 < n_chunks; c0 += gc_max) {
-                    const int gc = min(gc_max, n_chunks - c0);
-                    const int per_h = gc * (kHd + 1);
-                    pk_gather<8>(rd, nh * per_h,
-                                 [&](int j) {
-                                     const int h = j / per_h, r = j % per_h;
-                                     return att + ((size_t)h * a.max_chunks + c0 + r / (kHd + 1)) * kPartStride + 1 +
-                                            r % (kHd + 1);
-                                 },
-                                 [&](int j, float v) { gst[j] = v; }, idle);
-                    SyncCompute::sync();
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int e = tid + 256 * k;
-                        if (e < nh * kHd) {
-                            const int h = e / kHd, d = e % kHd;
-                            for (int cc = 0; cc < gc; ++cc) {
-                                const float w = expf(mst[h * n_chunks + c0 + cc] - Mv[k]);
-                                const float* gp = gst + (size_t)(h * gc + cc) * (kHd + 1);
-                                Lv[k] = fmaf(w, gp[0], Lv[k]);
-                                Ov[k] = fmaf(w, gp[1 + d], Ov[k]);
-                            }
-                        }
-                    }
-                    SyncCompute::sync();
-                }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int e = tid + 256 * k;
-                    if (e < nh * kHd) xs[e] = Ov[k] / Lv[k];
-                }
+                // Long context: CTA h (h < nh) merges head h's chunks (the
+                // attn_merge arithmetic) and publishes o_h; every CTA then
+                // gathers all of o.  The merge work and its L2 reads are no
+                // longer repeated on every CTA.
+                if (c < nh)
+                    merge_head(rd, att + (size_t)c * a.max_chunks * kPartStride, n_chunks, stg,
+                               a.pk + lay.o_base(L, G, l) + (size_t)c * kHd, lay.n_o, ep);
+                gather(a.pk + lay.o_base(L, G, l) + (size_t)rc * lay.n_o, nh * kHd, xs);
             }
             if (phase_end()) break;
         }
@@ -769,7 +745,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
             warp_stage_pairs<H>(ring, s0, a.stages, o_r1 - o_r0, xs, res);
             for (int q = warp, i = 0; 2 * q < o_r1 - o_r0; q += 8, ++i) {
                 const int r = o_r0 + 2 * q;
-                const float acc[2][1] = {{res[2 * i]}, {res[2 * i + 1]}};
                 // xr still holds this layer's input x (gathered for Q/K/V);
                 // lanes 0-7 write copy (lane % 4) of row r + lane / 4.
                 if (lane < 2 * kPkRep) {
@@ -784,7 +759,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
         mark(mb + 7);
 
         // ---- RMSNorm + gate/up + SiLU(gate) * up ----------------------
-        wait_cnt(l * 5 + 2);
+        // The packets carry the epoch: gather them directly (a thread
+        // re-polls the ones not yet written) instead of first waiting for
+        // the phase's arrival counter, which would add an L2 round trip.
         mark(mb + 8);
         gather(pk + lay.x1 + (size_t)rc * lay.n_x, H, xr);
         if (phase_end()) break;
@@ -815,6 +792,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
         mark(mb + 10);
 
         // ---- down + residual ------------------------------------------
+        // SiLU(gate) * up is a large gather (I packets): poll the counter
+        // first rather than have every thread re-poll packets.
         wait_cnt(l * 5 + 3);
         mark(mb + 11);
         const u64* mp = pk + lay.m + (size_t)rc * lay.n_m;
@@ -994,16 +973,16 @@ cudaError_t persistent_setup(Ctx& c) {
     c.pers.rows_i = rows_i;
     c.pers.act_floats = (int)(act / 4);
     c.pers.max_chunks = (g.n_ctx + kAttCh - 1) / kAttCh;
-    // Chunk-merge staging: o [H], chunk maxima [nh][max_chunks], then
-    // (l, acc) of `merge_group` chunks per head.
-    const int left = c.pers.act_floats - H - g.n_head * c.pers.max_chunks;
-    c.pers.merge_group = left / (g.n_head * (kHd + 1));
-    if (c.pers.merge_group < 1 || g.n_head * kHd > 1024) {
+    // Chunk-merge staging after o [H]: all heads' partials at short
+    // context, one head's partials (the per-head merge) at long context.
+    c.pers.merge_group = 0;
+    if (c.pers.max_chunks * kPartStride > c.pers.act_floats - H || g.n_head * kHd > 1024 ||
+        g.n_head > c.pers.grid) {
         c.pers.why_not = "attention merge staging does not fit (n_ctx or heads too large)";
         return cudaSuccess;
     }
     const PkLayout lay(c.nqkv, H, I, g.n_head, c.pers.max_chunks);
-    const size_t n_pk = (size_t)g.n_layer * lay.per_layer + 2 * (size_t)c.pers.grid;
+    const size_t n_pk = lay.o_base(g.n_layer, c.pers.grid, g.n_layer);
     std::vector<PersistLayer> hl(g.n_layer);
     for (int l = 0; l < g.n_layer; ++l) {
         const DevLayer& D = c.layers[l];

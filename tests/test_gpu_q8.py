@@ -26,15 +26,21 @@ def _prompts(shape, lens, seed):
     return [synth.make_tokens(shape.vocab, n, seed + i) for i, n in enumerate(lens)]
 
 
-@pytest.mark.parametrize("shape_name,lens", [("toy", [20, 45, 33]), ("ragged", [20, 45, 33]),
-                                             ("toy", list(range(5, 25)))])
-def test_q8_prefill_and_teacher_forced_batched_decode(q2, shape_name, lens):
+@pytest.mark.parametrize("shape_name,lens,n_ctx", [
+    ("toy", [20, 45, 33], 128), ("ragged", [20, 45, 33], 128), ("toy", list(range(5, 25)), 128),
+    # one query head per kv head (group 1) through the batched attention
+    ("toy-mha", [20, 45, 33], 128),
+    # long rows: many 64-key chunks, segments split across CTAs
+    ("toy", [2500, 40, 1200, 700], 4096),
+    # n_ctx above 4096: the batched decode falls back to the split-k attention
+    ("toy", [70, 130], 4160)])
+def test_q8_prefill_and_teacher_forced_batched_decode(q2, shape_name, lens, n_ctx):
     """3 sequences (one 16-row M-tile) or 20 (two M-tiles): prefill on the f32
     path with Q8_0 weights, then teacher-forced decode steps of all rows at
     once, each row against the oracle on the same Q8_0 blocks."""
     shape = synth.SHAPES[shape_name]
     w = synth.make_weights(shape, 0)
-    n_ctx, n_steps = 128, 4
+    n_steps = 4
     prompts = _prompts(shape, lens, 300)
     orc = oracle.build_oracle(shape, w, n_ctx, weight_format="q8_0")
     refs = []
