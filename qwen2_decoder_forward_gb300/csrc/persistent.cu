@@ -402,17 +402,7 @@ __device__ __noinline__ void attn_unit_compute(AttnSmem* at, int group, int nj, 
     });
 }
 
-// Merge of all chunk partials staged in shared memory as stg[h][c][66]
-// into o (nh * 64 values): the attn_merge arithmetic, in chunk order.
-__device__ __noinline__ void merge_staged(const float* stg, int nh, int n_chunks, float* o) {
-    for (int e = threadIdx.x; e < nh * kHd; e += kCompute) {
-        const int h = e / kHd, d = e % kHd;
-        const float* ph = stg + (size_t)h * n_chunks * kPartStride;
-        o[e] = attn_merge(n_chunks, d, [&](int cc, int i) { return ph[cc * kPartStride + i]; });
-    }
-}
-
-// Long-context merge of one head: gather its n_chunks partials into stg,
+// Merge of one head: gather its n_chunks partials into stg,
 // merge them with the attn_merge arithmetic (chunk order) and publish the
 // 64 outputs to every packet copy of dst.  A function of its own so that
 // the main loop's code generation does not change with it.
@@ -708,35 +698,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
         arrive(l * 5 + 1);
         mark(mb + 4);
 
-        // ---- merge the chunks (every CTA), o_proj + residual -----------
-        // Same arithmetic as attn_merge: M = max m_c, then in chunk order
-        // w = e^(m_c - M), L = fma(w, l_c, L), O = fma(w, acc_c, O); o = O / L.
+        // ---- attention output, o_proj + residual -------------------------
+        // CTA h (h < nh) merges head h's chunk partials (the attn_merge
+        // arithmetic, in chunk order) and publishes o_h; every CTA gathers
+        // all of o.  Two short L2 round trips on the critical path instead
+        // of every CTA gathering and merging every partial.
         {
             const u64* att = pk + lay.att + (size_t)rc * lay.n_att;
-            float* stg = act + H;
-            const int whole = nh * n_chunks * kPartStride;
+            u64* ob = a.pk + lay.o_base(L, G, l);
             wait_cnt(l * 5 + 1);
             mark(mb + 5);
-            if (whole <= a.act_floats - H) {
-                // All partials in one gather: stg[h][c][66].
-                pk_gather<8>(rd, whole,
-                             [&](int j) {
-                                 const int h = j / (n_chunks * kPartStride), r = j % (n_chunks * kPartStride);
-                                 return att + (size_t)h * a.max_chunks * kPartStride + r;
-                             },
-                             [&](int j, float v) { stg[j] = v; }, idle);
-                SyncCompute::sync();
-                merge_staged(stg, nh, n_chunks, xs);
-            } else {
-                // Long context: CTA h (h < nh) merges head h's chunks (the
-                // attn_merge arithmetic) and publishes o_h; every CTA then
-                // gathers all of o.  The merge work and its L2 reads are no
-                // longer repeated on every CTA.
-                if (c < nh)
-                    merge_head(rd, att + (size_t)c * a.max_chunks * kPartStride, n_chunks, stg,
-                               a.pk + lay.o_base(L, G, l) + (size_t)c * kHd, lay.n_o, ep);
-                gather(a.pk + lay.o_base(L, G, l) + (size_t)rc * lay.n_o, nh * kHd, xs);
-            }
+            if (c < nh)
+                merge_head(rd, att + (size_t)c * a.max_chunks * kPartStride, n_chunks, act + H, ob + (size_t)c * kHd,
+                           lay.n_o, ep);
+            gather(ob + (size_t)rc * lay.n_o, nh * kHd, xs);
             if (phase_end()) break;
         }
         mark(mb + 6);
