@@ -116,7 +116,7 @@ def decode_bytes_per_step(shape, positions, q8: bool = False) -> float:
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum, mean
 # of 3 launches at positions ~150) from one ncu capture of the persistent
 # decode kernel, valid only while the kernel's sources hash to `src`.
-TRAFFIC = {"k_decode_persistent": {"src": "d4268477ed2a556d", "bytes": 1001816235.0}}
+TRAFFIC = {"k_decode_persistent": {"src": "7e75ea6ed5e43637", "bytes": 1003552170.7}}
 KERNEL_SOURCES = ("persistent.cu", "persistent.h", "rowdot.cuh", "common.cuh", "attn.cuh", "ctx.h")
 
 
