@@ -114,16 +114,17 @@ def decode_bytes_per_step(shape, positions, q8: bool = False) -> float:
 
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum, mean
-# of 3 launches at positions ~150) from one ncu capture of the persistent
-# decode kernel, valid only while the kernel's sources hash to `src`.
-TRAFFIC = {"k_decode_persistent": {"src": "7e75ea6ed5e43637", "bytes": 1003552170.7}}
+# of 3 launches at positions ~150 of the 0.5b-decode-b1 workload) from one
+# ncu capture of the persistent decode kernel, valid only for that workload
+# and only while the kernel's sources hash to `src`.
+TRAFFIC = {"k_decode_persistent": {"workload": "0.5b-decode-b1", "src": "7e75ea6ed5e43637", "bytes": 1003552170.7}}
 KERNEL_SOURCES = ("persistent.cu", "persistent.h", "rowdot.cuh", "common.cuh", "attn.cuh", "ctx.h")
 
 
-def kernel_traffic(name: str):
+def kernel_traffic(name: str, workload: str):
     import hashlib
     rec = TRAFFIC.get(name)
-    if rec is None:
+    if rec is None or rec.get("workload") != workload:
         return None
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
@@ -430,7 +431,7 @@ def bench_decode(args, wl, shape, weights, rank, world, local):
         kname = f"one decode step of {B} sequences: all kernels of the step graph"
         launches = 2 + shape.n_layer * 5
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                "traffic": kernel_traffic("k_decode_persistent") if persistent else None,
+                "traffic": kernel_traffic("k_decode_persistent", wl.name) if persistent else None,
                 "kernel": kname, "peak_source": src, "bytes_per_launch": step_bytes}
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
