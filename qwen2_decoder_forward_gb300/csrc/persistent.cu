@@ -389,15 +389,16 @@ __device__ __noinline__ void warp_stage_rows(const unsigned char* ring, int s0, 
 
 // One attention chunk (keys, values and queries already in `at`) for the
 // `group` query heads of a kv head; writes each head's partial (m, l,
-// acc[64]) to every packet copy: head h's partial at out + h * head_stride.
+// acc[64]) to packet copy 0 (only the head's merging CTA reads it): head
+// h's partial at out + h * head_stride.
 __device__ __noinline__ void attn_unit_compute(AttnSmem* at, int group, int nj, u64* out, int head_stride,
-                                               int copy_stride, unsigned ep) {
+                                               unsigned ep) {
     attn_chunk<SyncCompute>(*at, group, nj, [&](int h, int d, float acc, float m, float lsum) {
         u64* pr = out + (size_t)h * head_stride;
-        pk_put_all(pr + 2 + d, copy_stride, acc, ep);
+        pk_put(pr + 2 + d, acc, ep);
         if (d == 0) {
-            pk_put_all(pr, copy_stride, m, ep);
-            pk_put_all(pr + 1, copy_stride, lsum, ep);
+            pk_put(pr, m, ep);
+            pk_put(pr + 1, lsum, ep);
         }
     });
 }
@@ -692,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
             }
             SyncCompute::sync();
             attn_unit_compute(&at, group, nj, pk + lay.att + ((size_t)(g * group) * a.max_chunks + ch) * kPartStride,
-                              a.max_chunks * kPartStride, lay.n_att, ep);
+                              a.max_chunks * kPartStride, ep);
         }
         if (phase_end()) break;
         arrive(l * 5 + 1);
@@ -704,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
         // all of o.  Two short L2 round trips on the critical path instead
         // of every CTA gathering and merging every partial.
         {
-            const u64* att = pk + lay.att + (size_t)rc * lay.n_att;
+            const u64* att = pk + lay.att;  // partials: copy 0 only
             u64* ob = a.pk + lay.o_base(L, G, l);
             wait_cnt(l * 5 + 1);
             mark(mb + 5);
