@@ -624,16 +624,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
                         const float2 cs = first ? pcs : a.rope[(size_t)p * (kHd / 2) + i];
                         float ra, rb;
                         rope_pair(v0, v1, cs, ra, rb);
-                        pk_put_all(pk + lay.qkv + s * kHd + i, lay.n_qkv, ra, ep);
-                        pk_put_all(pk + lay.qkv + s * kHd + i + kHd / 2, lay.n_qkv, rb, ep);
+                        pk_put(pk + lay.qkv + s * kHd + i, ra, ep);
+                        pk_put(pk + lay.qkv + s * kHd + i + kHd / 2, rb, ep);
                         if (s >= nh) {
                             float* kr = a.kv + (cache0 + (s - nh)) * head_stride + (size_t)p * kHd;
                             kr[i] = ra;
                             kr[i + kHd / 2] = rb;
                         }
                     } else {
-                        pk_put_all(pk + lay.qkv + s * kHd + i, lay.n_qkv, v0, ep);
-                        pk_put_all(pk + lay.qkv + s * kHd + i + kHd / 2, lay.n_qkv, v1, ep);
+                        pk_put(pk + lay.qkv + s * kHd + i, v0, ep);
+                        pk_put(pk + lay.qkv + s * kHd + i + kHd / 2, v1, ep);
                         float* vr = a.kv + (cache0 + nkv + (s - nh - nkv)) * head_stride + (size_t)p * kHd;
                         vr[i] = v0;
                         vr[i + kHd / 2] = v1;
@@ -668,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
                 qkv_seen = true;
                 mark(mb + 3);
             }
-            const u64* qp = pk + lay.qkv + (size_t)rc * lay.n_qkv + (size_t)g * group * kHd;
+            const u64* qp = pk + lay.qkv + (size_t)g * group * kHd;
             pk_gather<2>(rd, group * kHd, [&](int e) { return qp + e; },
                          [&](int e, float v) { at.q[e / kHd][e % kHd] = v; }, idle);
 #pragma unroll
@@ -683,8 +683,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
                 }
             }
             if (nold < nj) {  // this step's key and value (position p): from the packets
-                const u64* kp = pk + lay.qkv + (size_t)rc * lay.n_qkv + (size_t)(nh + g) * kHd;
-                const u64* vp = pk + lay.qkv + (size_t)rc * lay.n_qkv + (size_t)(nh + nkv + g) * kHd;
+                const u64* kp = pk + lay.qkv + (size_t)(nh + g) * kHd;
+                const u64* vp = pk + lay.qkv + (size_t)(nh + nkv + g) * kHd;
                 pk_gather<1>(rd, 2 * kHd, [&](int e) { return e < kHd ? kp + e : vp + (e - kHd); },
                              [&](int e, float v) {
                                  if (e < kHd) at.k[nold][e] = v;
