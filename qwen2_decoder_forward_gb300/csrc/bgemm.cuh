@@ -379,5 +379,117 @@ __global__ void __launch_bounds__(W * 32) k_bgemm_q8(Pro pro, int B, int K, int 
     epi.finish();
 }
 
+// The same product for tall N (the LM head) with KS = 1: a persistent grid
+// whose CTA stages the activation rows once and then walks row tiles
+// blockIdx.x, blockIdx.x + gridDim.x, ...  Each warp's weight stream runs
+// straight on from one tile into the next (the DEPTH-deep register ring
+// refills with the next tile's first blocks while the current tile's last
+// blocks are multiplied).  Grid: up to the SM count (one CTA per SM); the
+// k chunk is the whole row (kc_len = K).  With LO = false only the f16 hi
+// part of the activations enters the MMAs (half the tensor work; the
+// activation then carries 11 bits, as in an f16 GEMM).
+template <int MT, int NTW, class Epi, class Pro, bool LO = true, int DEPTH = kDepth>
+__global__ void __launch_bounds__(kThreads) k_bgemm_q8_tiles(Pro pro, int B, int K, const int8_t* __restrict__ Q,
+                                                             const __half* __restrict__ D, int N, Epi epi, int* err) {
+    using namespace sm100;
+    extern __shared__ __align__(16) unsigned char smem[];
+    constexpr int kRows = MT * 16;
+    constexpr int kRowsCta = kWarps * NTW * 8;
+    const int ld = row_ld(K);
+    __half* ah = reinterpret_cast<__half*>(smem);
+    __half* al = ah + kRows * ld;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(al + kRows * ld);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int gi = lane >> 2, ti = lane & 3;
+    const int Bc = min(B, kRows);
+    const int nb = K / 32;
+    const int n_tiles = (N + kRowsCta - 1) / kRowsCta;
+    const int my_tiles = blockIdx.x < n_tiles ? (n_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int total = my_tiles * nb;  // this warp's (tile, block) steps
+    auto step_n0 = [&](int s) { return (int)(blockIdx.x + (s / nb) * gridDim.x) * kRowsCta + warp * NTW * 8; };
+
+    WeightBlock wq[DEPTH][NTW];
+#pragma unroll
+    for (int i = 0; i < DEPTH; ++i)
+        if (i < total) load_block<NTW>(Q, D, N, K, step_n0(i), gi, ti, (i % nb) * 32, wq[i]);
+    epi.start(0, 0, B);
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    const bool staged = pro.stage(ah, al, ld, Bc, K, 0, K, bar);
+    if (!staged && lane == 0) raise_guard(err, kGuardTimeout);
+
+    float acc[MT][NTW][4];
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int t = 0; t < NTW; ++t) acc[m][t][0] = acc[m][t][1] = acc[m][t][2] = acc[m][t][3] = 0.f;
+    if (staged) {
+        for (int s0 = 0; s0 < total; s0 += DEPTH) {
+#pragma unroll
+            for (int i = 0; i < DEPTH; ++i) {
+                const int s = s0 + i;
+                if (s < total) {
+                    const int kb = s % nb;
+                    uint32_t bw[NTW][4];
+                    float dsc[NTW][2];
+#pragma unroll
+                    for (int t = 0; t < NTW; ++t) {
+                        const WeightBlock& wb = wq[i][t];
+                        bw[t][0] = i8x2_to_h2(wb.q.x, 0x4140u);
+                        bw[t][1] = i8x2_to_h2(wb.q.x, 0x4342u);
+                        bw[t][2] = i8x2_to_h2(wb.q.y, 0x4140u);
+                        bw[t][3] = i8x2_to_h2(wb.q.y, 0x4342u);
+                        dsc[t][0] = h_bits_to_f(wb.d0);
+                        dsc[t][1] = h_bits_to_f(wb.d1);
+                    }
+                    if (s + DEPTH < total)
+                        load_block<NTW>(Q, D, N, K, step_n0(s + DEPTH), gi, ti, ((s + DEPTH) % nb) * 32, wq[i]);
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        const __half* hr = ah + (m * 16 + gi) * ld + kb * 32 + 8 * ti;
+                        const __half* lr = al + (m * 16 + gi) * ld + kb * 32 + 8 * ti;
+                        const uint4 h0 = *reinterpret_cast<const uint4*>(hr);
+                        const uint4 h1 = *reinterpret_cast<const uint4*>(hr + 8 * ld);
+                        const uint4 l0 = LO ? *reinterpret_cast<const uint4*>(lr) : make_uint4(0u, 0u, 0u, 0u);
+                        const uint4 l1 = LO ? *reinterpret_cast<const uint4*>(lr + 8 * ld) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                        for (int t = 0; t < NTW; ++t) {
+                            float p[4] = {0.f, 0.f, 0.f, 0.f};
+                            mma16816(p, h0.x, h1.x, h0.y, h1.y, bw[t][0], bw[t][1]);
+                            if (LO) mma16816(p, l0.x, l1.x, l0.y, l1.y, bw[t][0], bw[t][1]);
+                            mma16816(p, h0.z, h1.z, h0.w, h1.w, bw[t][2], bw[t][3]);
+                            if (LO) mma16816(p, l0.z, l1.z, l0.w, l1.w, bw[t][2], bw[t][3]);
+                            acc[m][t][0] = fmaf(dsc[t][0], p[0], acc[m][t][0]);
+                            acc[m][t][1] = fmaf(dsc[t][1], p[1], acc[m][t][1]);
+                            acc[m][t][2] = fmaf(dsc[t][0], p[2], acc[m][t][2]);
+                            acc[m][t][3] = fmaf(dsc[t][1], p[3], acc[m][t][3]);
+                        }
+                    }
+                    if (kb == nb - 1) {
+                        // The tile's last block: its outputs, then a fresh tile.
+                        const int n0 = step_n0(s);
+#pragma unroll
+                        for (int m = 0; m < MT; ++m)
+#pragma unroll
+                            for (int t = 0; t < NTW; ++t) {
+                                const int n = n0 + t * 8 + 2 * ti;
+                                const int b0 = m * 16 + gi, b1 = b0 + 8;
+                                if (n < N) {
+                                    if (b0 < B) epi.pair(b0, n, acc[m][t][0], acc[m][t][1], 0);
+                                    if (b1 < B) epi.pair(b1, n, acc[m][t][2], acc[m][t][3], 0);
+                                }
+                                acc[m][t][0] = acc[m][t][1] = acc[m][t][2] = acc[m][t][3] = 0.f;
+                            }
+                    }
+                }
+            }
+        }
+    }
+    epi.finish();
+}
+
 }  // namespace bg
 }  // namespace qwen2

@@ -709,8 +709,19 @@ struct EpiLmQ8 {
         for (int b = warp; b < B; b += bg::kWarps) {
             float v = -INFINITY;
             int i = 0x7fffffff;
-            for (int k = lane; k < (int)gridDim.x; k += 32)
-                argmax_merge(v, i, __ldcg(am_val + k * 32 + b), __ldcg(am_idx + k * 32 + b));
+            for (int k0 = lane; k0 < (int)gridDim.x; k0 += 32 * 8) {
+                // Eight CTAs' pairs per lane in flight, merged in CTA order.
+                float vv[8];
+                int ii[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int k = k0 + 32 * j;
+                    vv[j] = k < (int)gridDim.x ? __ldcg(am_val + k * 32 + b) : -INFINITY;
+                    ii[j] = k < (int)gridDim.x ? __ldcg(am_idx + k * 32 + b) : 0x7fffffff;
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) argmax_merge(v, i, vv[j], ii[j]);
+            }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
                 const float ov = __shfl_xor_sync(0xffffffffu, v, o);
@@ -984,7 +995,16 @@ cudaError_t lm_head_q8(Ctx& c, float* x, int B, float* logits, int* ids, float* 
         e.bv[k] = -INFINITY;
         e.bi[k] = 0x7fffffff;
     }
-    return bgemm<MT, kLmNtw, 1>(c, bg::ProCopy{w.q8_ah, w.q8_al}, B, H, H, c.embed, c.cfg.vocab, e, st);
+    // One CTA per SM walking the vocabulary's 256-row tiles: the activation
+    // rows are staged once per SM, not once per tile.  The normalised rows
+    // enter as f16 only (no lo part): the logits are the last product, and
+    // an 11-bit activation rounding moves them by about 1e-3 at most at this
+    // scale, far inside the 2e-2 bound, for half the tensor work.
+    const int tiles = (c.cfg.vocab + bg::kWarps * kLmNtw * 8 - 1) / (bg::kWarps * kLmNtw * 8);
+    const int grid = tiles < c.n_sm ? tiles : c.n_sm;
+    bg::k_bgemm_q8_tiles<MT, kLmNtw, EpiLmQ8, bg::ProCopy, false><<<grid, bg::kThreads, bg::smem_bytes(MT, H), st>>>(
+        bg::ProCopy{w.q8_ah, w.q8_al}, B, H, c.embed.q, c.embed.d, c.cfg.vocab, e, c.err);
+    return cudaGetLastError();
 }
 
 template <int MT>
@@ -1123,6 +1143,12 @@ cudaError_t decode_set_smem_limits(int max_bytes) {
     if (e == cudaSuccess)                                                                                     \
         e = cudaFuncSetAttribute(bg::k_bgemm_q8<MT, NTW, KS, EPI, PRO>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                                  (int)bg::smem_bytes(MT, bg::kKc));
+#define Q2_BGT(MT)                                                                                          \
+    if (e == cudaSuccess)                                                                                   \
+        e = cudaFuncSetAttribute(bg::k_bgemm_q8_tiles<MT, kLmNtw, EpiLmQ8, bg::ProCopy, false>,                     \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bg::smem_bytes(MT, bg::kKc));
+    Q2_BGT(1) Q2_BGT(2)
+#undef Q2_BGT
 #define Q2_BG_MT(MT)                                          \
     Q2_BG(MT, 1, 8, EpiQkvQ8, bg::ProNorm)                    \
     Q2_BG(MT, 1, 8, EpiResidualQ8, bg::ProCopy)               \
