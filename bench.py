@@ -98,6 +98,42 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+class Replicas:
+    """Coordination of N independent replicas, one process per GPU (the
+    forward has no exchange step, so the only collectives are the timing
+    barrier and the max over ranks).  backend "nccl" with a CUDA device on
+    the GPU box; "gloo" with device None runs the same logic on the CPU."""
+
+    def __init__(self, world: int, backend: str = "nccl", device=None):
+        self.world, self.device, self.dist = world, device, None
+        if world > 1:
+            import torch.distributed as dist
+            kw = {"device_id": device} if backend == "nccl" else {}
+            dist.init_process_group(backend, **kw)
+            self.dist = dist
+
+    def barrier(self):
+        import torch
+        if self.dist:
+            self.dist.barrier()
+        if self.device is not None:
+            torch.cuda.synchronize()
+
+    def max(self, x: float) -> float:
+        """The largest of every rank's x (the slowest replica's time)."""
+        if not self.dist:
+            return float(x)
+        import torch
+        t = torch.tensor([float(x)], dtype=torch.float64, device=self.device)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.dist:
+            self.dist.destroy_process_group()
+            self.dist = None
+
+
 def decode_bytes_per_step(shape, positions, q8: bool = False) -> float:
     """Algorithmic HBM bytes of one decode step of B sequences at positions
     p_b: the weights once (f16: 2 bytes an element; Q8_0: 1 byte plus a
@@ -229,10 +265,7 @@ def bench_prefill(args, wl, shape, weights, rank, world, local):
     import torch
     import qwen2_decoder_forward_gb300 as q2
     torch.cuda.set_device(local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    reps = Replicas(world, "nccl", torch.device("cuda", local))
     mode = q2.PREFILL_TENSOR if wl.prefill == "tensor" else q2.PREFILL_F32
     model = q2.Qwen2Model(shape, weights, n_ctx=wl.n_ctx, max_seqs=wl.n_seq, max_tokens=n_tok,
                           prefill_mode=mode, flags=args.flags)
@@ -247,38 +280,25 @@ def bench_prefill(args, wl, shape, weights, rank, world, local):
         step(ids)
     model.synchronize()
 
-    def barrier():
-        if dist:
-            dist.barrier()
-        torch.cuda.synchronize()
-
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
+    reps.barrier()
     with ClockSampler(local) as clocks:
         start.record(stream)
         for _ in range(args.steps):
             step(ids)
         end.record(stream)
         torch.cuda.synchronize()
-    barrier()
-    ms = start.elapsed_time(end)
-    if dist:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    reps.barrier()
+    ms = reps.max(start.elapsed_time(end))
     model.synchronize()
     value = args.steps * n_tok * world / (ms / 1e3)
     # End to end: host token arrays in, ids read back into host memory.
     host_ids = np.empty((wl.n_seq,), dtype=np.int32)
-    barrier()
+    reps.barrier()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         step(host_ids)
-    e2e_s = time.perf_counter() - t0
-    if dist:
-        t = torch.tensor([e2e_s], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = reps.max(time.perf_counter() - t0)
     hbm, tflops, src = peaks()
     achieved = flops / (ms / 1e3 / args.steps) / 1e12
     tensor = bool(model.features & q2.FEATURE_TENSOR_PREFILL)
@@ -312,8 +332,7 @@ def bench_prefill(args, wl, shape, weights, rank, world, local):
     if rank == 0:
         print(json.dumps(line), flush=True)
     model.close()
-    if dist:
-        dist.destroy_process_group()
+    reps.close()
 
 
 def bench_decode(args, wl, shape, weights, rank, world, local):
@@ -355,10 +374,7 @@ def bench_decode(args, wl, shape, weights, rank, world, local):
     import torch
     import qwen2_decoder_forward_gb300 as q2
     torch.cuda.set_device(local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    reps = Replicas(world, "nccl", torch.device("cuda", local))
 
     n_steps = args.tokens_per_step or wl.decode_steps
     model = q2.Qwen2Model(shape, weights, n_ctx=wl.n_ctx, max_seqs=B, max_tokens=sum(lens),
@@ -376,25 +392,16 @@ def bench_decode(args, wl, shape, weights, rank, world, local):
         step(out)
     model.synchronize()
 
-    def barrier():
-        if dist:
-            dist.barrier()
-        torch.cuda.synchronize()
-
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
+    reps.barrier()
     with ClockSampler(local) as clocks:
         start.record(stream)
         for _ in range(args.steps):
             step(out)
         end.record(stream)
         torch.cuda.synchronize()
-    barrier()
-    ms = start.elapsed_time(end)
-    if dist:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    reps.barrier()
+    ms = reps.max(start.elapsed_time(end))
     model.synchronize()
     tokens = args.steps * n_steps * B * world
     value = tokens / (ms / 1e3)
@@ -402,15 +409,11 @@ def bench_decode(args, wl, shape, weights, rank, world, local):
     # End to end through the public API with host buffers: host token,
     # position and sequence-id inputs, ids read back into host memory.
     host_ids = np.empty((n_steps, B), dtype=np.int32)
-    barrier()
+    reps.barrier()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         step(host_ids)
-    e2e_s = time.perf_counter() - t0
-    if dist:
-        t = torch.tensor([e2e_s], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = reps.max(time.perf_counter() - t0)
     e2e = {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": 3 * 4 * B,
            "d2h_bytes_per_step": int(host_ids.nbytes)}
 
@@ -452,8 +455,7 @@ def bench_decode(args, wl, shape, weights, rank, world, local):
     if rank == 0:
         print(json.dumps(line), flush=True)
     model.close()
-    if dist:
-        dist.destroy_process_group()
+    reps.close()
 
 
 def main():
@@ -473,6 +475,8 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference" and rank != 0:
+        return  # the oracle arm runs on rank 0 alone; other ranks exit 0 without work
     weights = synth.make_weights(shape, wl.weight_seed)
     if wl.decode_steps == 0:
         return bench_prefill(args, wl, shape, weights, rank, world, local)
