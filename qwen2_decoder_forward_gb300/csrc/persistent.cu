@@ -344,42 +344,110 @@ __device__ __forceinline__ void pk_put_all(u64* p, int stride, float v, unsigned
     for (int r = 0; r < kPkRep; ++r) pk_put(p + (size_t)r * stride, v, ep);
 }
 
+// The kernel's dynamic shared memory, named at file scope so that the
+// out-of-line helpers below derive their pointers from a shared-memory
+// object (a generic pointer passed in leaves the compiler generic loads).
+// Layout: the weight ring (kPersistStages stages), then the mbarriers and
+// the reduction scratch (256 bytes), then the activation area (kActOff).
+extern __shared__ __align__(128) unsigned char persist_smem[];
+constexpr int kActOff = kPersistStages * kPersistStage + 256;
+
+__device__ __forceinline__ float* act_smem() { return reinterpret_cast<float*>(persist_smem + kActOff); }
+__device__ __forceinline__ const __half* stage_smem(int s) {
+    return reinterpret_cast<const __half*>(persist_smem + (size_t)s * kPersistStage);
+}
+__device__ __forceinline__ u64* full_bars() { return reinterpret_cast<u64*>(persist_smem + kPersistStages * kPersistStage); }
+
+// One lane's share of an activation vector of K floats as the canonical
+// row dot reads it (rowdot.cuh): chunks c = lane + 32 u of eight floats,
+// held in registers so that a warp reading many rows loads x once.
+template <int K>
+struct XLane {
+    static constexpr int kC = K / 8, kP = (kC + 31) / 32;
+    float4 a[kP], b[kP];
+    __device__ __forceinline__ void load(const float* xs) {
+        const int lane = threadIdx.x & 31;
+#pragma unroll
+        for (int u = 0; u < kP; ++u) {
+            const int c = lane + 32 * u;
+            if (c < kC) {
+                a[u] = *reinterpret_cast<const float4*>(xs + c * 8);
+                b[u] = *reinterpret_cast<const float4*>(xs + c * 8 + 4);
+            } else {
+                a[u] = b[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+    }
+};
+
+// The canonical row dot of R rows (in shared memory) with x in registers:
+// lane l adds chunks l, l + 32, ... in that order into four partial sums
+// per row, then the xor butterfly -- warp_rows_dot's operations in its
+// order, so the same bits.
+template <int K, int R>
+__device__ __forceinline__ void rows_dot_x(const __half* const (&rows)[R], const XLane<K>& x, float (&acc)[R]) {
+    constexpr int kC = XLane<K>::kC, kP = XLane<K>::kP;
+    const int lane = threadIdx.x & 31;
+    Acc4 part[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) part[r].a[e] = 0.f;
+    uint4 wv[R][kP];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int u = 0; u < kP; ++u) {
+            const int c = lane + 32 * u;
+            wv[r][u] = c < kC ? *reinterpret_cast<const uint4*>(rows[r] + (size_t)c * 8) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+    for (int u = 0; u < kP; ++u)
+        if (lane + 32 * u < kC)
+#pragma unroll
+            for (int r = 0; r < R; ++r) dot8_f16_4(wv[r][u], x.a[u], x.b[u], part[r]);
+#pragma unroll
+    for (int r = 0; r < R; ++r) acc[r] = warp_sum(dot4_total(part[r]));
+}
+
 // Dot products of this warp's row pairs: rows (2w, 2w + 1) of each of the
 // consecutive ring stages from s0 that hold rows of a slice of nrows rows
-// (sixteen per stage).  Pair i's two sums go to res[2i], res[2i + 1] (lane
-// 0).  Compiled as a function of its own with K known: inside the large
-// kernel body the same loop ran several times slower.
+// (sixteen per stage), against the activation vector at the start of the
+// activation area.  Pair i's two sums go to res[2i], res[2i + 1] (lane 0).
+// Compiled as a function of its own with K known: inside the large kernel
+// body the same loop ran several times slower.
 template <int K>
-__device__ __noinline__ void warp_stage_pairs(const unsigned char* ring, int s0, int stages, int nrows,
-                                              const float* xs, float* res) {
+__device__ __noinline__ void warp_stage_pairs(int s0, int nrows, float* res) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    XLane<K> x;
+    x.load(act_smem());
     int s = s0;
     for (int i = 0; 16 * i + 2 * warp < nrows; ++i) {
-        const __half* st = reinterpret_cast<const __half*>(ring + (size_t)s * kPersistStage);
+        const __half* st = stage_smem(s);
         const bool two = 16 * i + 2 * warp + 1 < nrows;
         const __half* rows[2] = {st + (size_t)(2 * warp) * K, st + (size_t)(two ? 2 * warp + 1 : 2 * warp) * K};
-        float acc[2][1];
-        warp_rows_dot<1, 2, LdShared, 4>(rows, K, xs, K, acc);
+        float acc[2];
+        rows_dot_x<K, 2>(rows, x, acc);
         if (lane == 0) {
-            res[2 * i] = acc[0][0];
-            res[2 * i + 1] = acc[1][0];
+            res[2 * i] = acc[0];
+            res[2 * i + 1] = acc[1];
         }
-        s = s + 1 == stages ? 0 : s + 1;
+        s = s + 1 == kPersistStages ? 0 : s + 1;
     }
     __syncwarp();
 }
 
 // Dot products of this warp's rows q = w, w + 8, ... of a slice of nrows
-// rows of K stored rpc to a stage from s0; row k's sum goes to res[k].
+// rows of K stored rpc to a stage from s0, against the activation vector;
+// row k's sum goes to res[k].
 template <int K>
-__device__ __noinline__ void warp_stage_rows(const unsigned char* ring, int s0, int stages, int rpc, int nrows,
-                                             const float* xs, float* res) {
+__device__ __noinline__ void warp_stage_rows(int s0, int rpc, int nrows, float* res) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float* xs = act_smem();
     for (int q = warp, k = 0; q < nrows; q += 8, ++k) {
         const int j = q / rpc;
-        const int s = (s0 + j) % stages;
-        const __half* rows[1] = {reinterpret_cast<const __half*>(ring + (size_t)s * kPersistStage) +
-                                 (size_t)(q - j * rpc) * K};
+        const int s = (s0 + j) % kPersistStages;
+        const __half* rows[1] = {stage_smem(s) + (size_t)(q - j * rpc) * K};
         float acc[1][1];
         warp_rows_dot<1, 1, LdShared, 4>(rows, K, xs, K, acc);
         if (lane == 0) res[k] = acc[0][0];
@@ -387,13 +455,68 @@ __device__ __noinline__ void warp_stage_rows(const unsigned char* ring, int s0, 
     __syncwarp();
 }
 
-// One attention chunk (keys, values and queries already in `at`) for the
-// `group` query heads of a kv head; writes each head's partial (m, l,
-// acc[64]) to packet copy 0 (only the head's merging CTA reads it): head
-// h's partial at out + h * head_stride.
-__device__ __noinline__ void attn_unit_compute(AttnSmem* at, int group, int nj, u64* out, int head_stride,
-                                               unsigned ep) {
-    attn_chunk<SyncCompute>(*at, group, nj, [&](int h, int d, float acc, float m, float lsum) {
+// Wait (bounded) for an mbarrier phase.
+__device__ __forceinline__ bool wait_bar(u64* b, unsigned par) {
+    if (mbar_try_wait(b, par)) return true;
+    const u64 t0 = now_ns();
+    while (now_ns() - t0 < kWaitNs)
+        if (mbar_try_wait(b, par)) return true;
+    return false;
+}
+
+// The tied LM head over this CTA's vocabulary rows [r0, r1): chunks of 16
+// rows stream through the ring from ring position it0; the final-normed
+// hidden state (activation area) is held in registers for the whole slice.
+// Warp w takes rows 2w, 2w + 1 of each chunk; lane 0 stores the logits (if
+// asked) and keeps the warp's running argmax (lowest index on ties).
+// Returns false if a wait gave up (the stages are still released).
+template <int K>
+__device__ __noinline__ bool lm_head_rows(int it0, int r0, int r1, float* logits, float* best_v, int* best_i) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    u64* full = full_bars();
+    u64* empty = full + kPersistStages;
+    XLane<K> x;
+    x.load(act_smem());
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    bool ok = true;
+    int it = it0;
+    for (int r = r0; r < r1; r += 16, ++it) {
+        const int n = min(16, r1 - r);
+        const int s = it % kPersistStages;
+        if (ok && !wait_bar(&full[s], (unsigned)(it / kPersistStages) & 1u)) ok = false;
+        if (ok && 2 * warp < n) {
+            const __half* st = stage_smem(s);
+            const bool two = 2 * warp + 1 < n;
+            const __half* rows[2] = {st + (size_t)(2 * warp) * K, st + (size_t)(two ? 2 * warp + 1 : 2 * warp) * K};
+            float acc[2];
+            rows_dot_x<K, 2>(rows, x, acc);
+            if (lane == 0) {
+                const int row = r + 2 * warp;
+                if (logits) {
+                    logits[row] = acc[0];
+                    if (two) logits[row + 1] = acc[1];
+                }
+                argmax_merge(bv, bi, acc[0], row);
+                if (two) argmax_merge(bv, bi, acc[1], row + 1);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    *best_v = bv;
+    *best_i = bi;
+    return ok;
+}
+
+// One attention chunk (keys, values and queries already in the attention
+// area) for `group` query heads of one kv head (all of its heads, or a
+// subset); writes each head's partial (m, l, acc[64]) to packet copy 0
+// (only the head's merging CTA reads it): head h's partial at
+// out + h * head_stride.
+__device__ __noinline__ void attn_unit_compute(int group, int nj, u64* out, int head_stride, unsigned ep) {
+    AttnSmem& at = *reinterpret_cast<AttnSmem*>(act_smem());
+    attn_chunk<SyncCompute>(at, group, nj, [&](int h, int d, float acc, float m, float lsum) {
         u64* pr = out + (size_t)h * head_stride;
         pk_put(pr + 2 + d, acc, ep);
         if (d == 0) {
@@ -403,12 +526,14 @@ __device__ __noinline__ void attn_unit_compute(AttnSmem* at, int group, int nj, 
     });
 }
 
-// Merge of one head: gather its n_chunks partials into stg,
+// Merge of one head: gather its n_chunks partials into the activation
+// area at float offset stg_off,
 // merge them with the attn_merge arithmetic (chunk order) and publish the
 // 64 outputs to every packet copy of dst.  A function of its own so that
 // the main loop's code generation does not change with it.
-__device__ __noinline__ void merge_head(PkReader& rd, const u64* att_h, int n_chunks, float* stg, u64* dst,
+__device__ __noinline__ void merge_head(PkReader& rd, const u64* att_h, int n_chunks, int stg_off, u64* dst,
                                         int copy_stride, unsigned ep) {
+    float* stg = act_smem() + stg_off;
     pk_gather<8>(rd, n_chunks * kPartStride, [&](int j) { return att_h + j; }, [&](int j, float v) { stg[j] = v; },
                  [] {});
     SyncCompute::sync();
@@ -421,12 +546,11 @@ __device__ __noinline__ void merge_head(PkReader& rd, const u64* att_h, int n_ch
 
 template <int HC, int IC>
 __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArgs a) {
-    extern __shared__ __align__(128) unsigned char smem[];
-    unsigned char* ring = smem;
-    u64* full = reinterpret_cast<u64*>(smem + a.stages * kPersistStage);
-    u64* empty = full + a.stages;
-    float* red = reinterpret_cast<float*>(empty + a.stages);
-    float* act = reinterpret_cast<float*>(smem + a.stages * kPersistStage + 256);
+    unsigned char* ring = persist_smem;
+    u64* full = full_bars();
+    u64* empty = full + kPersistStages;
+    float* red = reinterpret_cast<float*>(empty + kPersistStages);
+    float* act = act_smem();
     float* xr = act + a.act_floats;  // raw x [H]
     AttnSmem& at = *reinterpret_cast<AttnSmem*>(act);
     float* xs = act;
@@ -500,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
             const int s = it % a.stages;
             const unsigned k = it / a.stages;
             if (!bad && !wait_full(s, k & 1)) bad = true;
-            if (!bad) fn(reinterpret_cast<const __half*>(ring + (size_t)s * kPersistStage), r, n);
+            if (!bad) fn(s, r, n);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
             ++it;
@@ -610,7 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
         // Sixteen rows per stage, one row pair per warp: warp w takes rows
         // 2w, 2w + 1 of each stage of its slice.
         consume_all(qkv_r0, qkv_r1, rpc_h, [&](int s0) {
-            warp_stage_pairs<H>(ring, s0, a.stages, qkv_r1 - qkv_r0, xs, res);
+            warp_stage_pairs<H>(s0, qkv_r1 - qkv_r0, res);
             for (int q = warp, i = 0; 2 * q < qkv_r1 - qkv_r0; q += 8, ++i) {
                 const int pr = qkv_r0 + 2 * q;  // packed row of the pair
                 const float acc[2][1] = {{res[2 * i]}, {res[2 * i + 1]}};
@@ -645,10 +769,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
         arrive(l * 5 + 0);
         mark(mb + 2);
 
-        // ---- attention: units (kv head g, chunk of 64 keys) ----------
+        // ---- attention: units (kv head g, chunk of 64 keys, query heads) -
+        // When there are fewer (kv head, chunk) pairs than CTAs, each pair's
+        // query heads are split into hsplit subsets on different CTAs: a
+        // head's scores, softmax and sums do not depend on the other heads
+        // of its group, so the partials are the same bits, computed by up
+        // to `group` times more SMs.
         bool qkv_seen = false;
-        for (int u = c; u < nkv * n_chunks; u += G) {
-            const int g = u / n_chunks, ch = u % n_chunks;
+        const int hsplit = max(1, min(group, G / (nkv * n_chunks)));
+        for (int u = c; u < nkv * n_chunks * hsplit; u += G) {
+            const int sub = u % hsplit, gu_ = u / hsplit;
+            const int g = gu_ / n_chunks, ch = gu_ % n_chunks;
+            const int h0 = sub * group / hsplit, hn = (sub + 1) * group / hsplit - h0;
             const int j0 = ch * kAttCh, nj = min(kAttCh, p + 1 - j0);
             const int nold = min(nj, p - j0);  // keys of earlier steps, read from the cache
             const float* kb = a.kv + (cache0 + g) * head_stride + (size_t)j0 * kHd;
@@ -668,8 +800,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
                 qkv_seen = true;
                 mark(mb + 3);
             }
-            const u64* qp = pk + lay.qkv + (size_t)g * group * kHd;
-            pk_gather<2>(rd, group * kHd, [&](int e) { return qp + e; },
+            const u64* qp = pk + lay.qkv + (size_t)(g * group + h0) * kHd;
+            pk_gather<2>(rd, hn * kHd, [&](int e) { return qp + e; },
                          [&](int e, float v) { at.q[e / kHd][e % kHd] = v; }, idle);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -692,7 +824,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
                              }, idle);
             }
             SyncCompute::sync();
-            attn_unit_compute(&at, group, nj, pk + lay.att + ((size_t)(g * group) * a.max_chunks + ch) * kPartStride,
+            attn_unit_compute(hn, nj,
+                              pk + lay.att + ((size_t)(g * group + h0) * a.max_chunks + ch) * kPartStride,
                               a.max_chunks * kPartStride, ep);
         }
         if (phase_end()) break;
@@ -710,7 +843,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
             wait_cnt(l * 5 + 1);
             mark(mb + 5);
             if (c < nh)
-                merge_head(rd, att + (size_t)c * a.max_chunks * kPartStride, n_chunks, act + H, ob + (size_t)c * kHd,
+                merge_head(rd, att + (size_t)c * a.max_chunks * kPartStride, n_chunks, H, ob + (size_t)c * kHd,
                            lay.n_o, ep);
             gather(ob + (size_t)rc * lay.n_o, nh * kHd, xs);
             if (phase_end()) break;
@@ -718,7 +851,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
         mark(mb + 6);
         const int o_r0 = 2 * split(H / 2, c, G), o_r1 = 2 * split(H / 2, c + 1, G);
         consume_all(o_r0, o_r1, rpc_h, [&](int s0) {
-            warp_stage_pairs<H>(ring, s0, a.stages, o_r1 - o_r0, xs, res);
+            warp_stage_pairs<H>(s0, o_r1 - o_r0, res);
             for (int q = warp, i = 0; 2 * q < o_r1 - o_r0; q += 8, ++i) {
                 const int r = o_r0 + 2 * q;
                 // xr still holds this layer's input x (gathered for Q/K/V);
@@ -754,12 +887,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
         };
         if ((gu_r1 - gu_r0 + rpc_h - 1) / rpc_h <= a.stages) {
             consume_all(gu_r0, gu_r1, rpc_h, [&](int s0) {
-                warp_stage_pairs<H>(ring, s0, a.stages, gu_r1 - gu_r0, xs, res);
+                warp_stage_pairs<H>(s0, gu_r1 - gu_r0, res);
                 gu_out(gu_r0, gu_r1 - gu_r0);
             }, mb + 14);
         } else {
-            consume(gu_r0, gu_r1, rpc_h, [&](const __half* st, int r0, int n) {
-                warp_stage_pairs<H>(reinterpret_cast<const unsigned char*>(st), 0, 1, n, xs, res);
+            consume(gu_r0, gu_r1, rpc_h, [&](int s, int r0, int n) {
+                warp_stage_pairs<H>(s, n, res);
                 gu_out(r0, n);
             });
         }
@@ -784,12 +917,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
         };
         if ((d_r1 - d_r0 + rpc_i - 1) / rpc_i <= a.stages) {
             consume_all(d_r0, d_r1, rpc_i, [&](int s0) {
-                warp_stage_rows<I>(ring, s0, a.stages, rpc_i, d_r1 - d_r0, xs, res);
+                warp_stage_rows<I>(s0, rpc_i, d_r1 - d_r0, res);
                 down_out(d_r0, d_r1 - d_r0);
             }, mb + 15);
         } else {
-            consume(d_r0, d_r1, rpc_i, [&](const __half* st, int r0, int n) {
-                warp_stage_rows<I>(reinterpret_cast<const unsigned char*>(st), 0, 1, rpc_i, n, xs, res);
+            consume(d_r0, d_r1, rpc_i, [&](int s, int r0, int n) {
+                warp_stage_rows<I>(s, rpc_i, n, res);
                 down_out(r0, n);
             });
         }
@@ -814,22 +947,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
         norm();
         if (c == 0)
             for (int j = tid; j < H; j += kCompute) a.hidden[j] = xs[j];
-        consume(split(V, c, G), split(V, c + 1, G), rpc_h, [&](const __half* st, int r0, int n) {
-            warp_stage_pairs<H>(reinterpret_cast<const unsigned char*>(st), 0, 1, n, xs, res);
-            for (int q = warp, i = 0; 2 * q < n; q += 8, ++i) {
-                const bool two = 2 * q + 1 < n;
-                if (lane == 0) {
-                    const int r = r0 + 2 * q;
-                    const float l0 = res[2 * i], l1 = res[2 * i + 1];
-                    if (a.logits) {
-                        a.logits[r] = l0;
-                        if (two) a.logits[r + 1] = l1;
-                    }
-                    argmax_merge(best_v, best_i, l0, r);
-                    if (two) argmax_merge(best_v, best_i, l1, r + 1);
-                }
-            }
-        });
+        const int v0 = split(V, c, G), v1 = split(V, c + 1, G);
+        float bv;
+        int bi;
+        if (!lm_head_rows<H>(it, v0, v1, a.logits, &bv, &bi)) bad = true;
+        best_v = bv;
+        best_i = bi;
+        it += (v1 - v0 + 15) / 16;
         phase_end();
     }
     if (!dead) {
