@@ -410,51 +410,6 @@ __device__ __forceinline__ void rows_dot_x(const __half* const (&rows)[R], const
     for (int r = 0; r < R; ++r) acc[r] = warp_sum(dot4_total(part[r]));
 }
 
-// Dot products of this warp's row pairs: rows (2w, 2w + 1) of each of the
-// consecutive ring stages from s0 that hold rows of a slice of nrows rows
-// (sixteen per stage), against the activation vector at the start of the
-// activation area.  Pair i's two sums go to res[2i], res[2i + 1] (lane 0).
-// Compiled as a function of its own with K known: inside the large kernel
-// body the same loop ran several times slower.
-template <int K>
-__device__ __noinline__ void warp_stage_pairs(int s0, int nrows, float* res) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    XLane<K> x;
-    x.load(act_smem());
-    int s = s0;
-    for (int i = 0; 16 * i + 2 * warp < nrows; ++i) {
-        const __half* st = stage_smem(s);
-        const bool two = 16 * i + 2 * warp + 1 < nrows;
-        const __half* rows[2] = {st + (size_t)(2 * warp) * K, st + (size_t)(two ? 2 * warp + 1 : 2 * warp) * K};
-        float acc[2];
-        rows_dot_x<K, 2>(rows, x, acc);
-        if (lane == 0) {
-            res[2 * i] = acc[0];
-            res[2 * i + 1] = acc[1];
-        }
-        s = s + 1 == kPersistStages ? 0 : s + 1;
-    }
-    __syncwarp();
-}
-
-// Dot products of this warp's rows q = w, w + 8, ... of a slice of nrows
-// rows of K stored rpc to a stage from s0, against the activation vector;
-// row k's sum goes to res[k].
-template <int K>
-__device__ __noinline__ void warp_stage_rows(int s0, int rpc, int nrows, float* res) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const float* xs = act_smem();
-    for (int q = warp, k = 0; q < nrows; q += 8, ++k) {
-        const int j = q / rpc;
-        const int s = (s0 + j) % kPersistStages;
-        const __half* rows[1] = {stage_smem(s) + (size_t)(q - j * rpc) * K};
-        float acc[1][1];
-        warp_rows_dot<1, 1, LdShared, 4>(rows, K, xs, K, acc);
-        if (lane == 0) res[k] = acc[0][0];
-    }
-    __syncwarp();
-}
-
 // Wait (bounded) for an mbarrier phase.
 __device__ __forceinline__ bool wait_bar(u64* b, unsigned par) {
     if (mbar_try_wait(b, par)) return true;
@@ -462,6 +417,82 @@ __device__ __forceinline__ bool wait_bar(u64* b, unsigned par) {
     while (now_ns() - t0 < kWaitNs)
         if (mbar_try_wait(b, par)) return true;
     return false;
+}
+
+// Dot products of this warp's row pairs of a slice of nrows rows whose
+// chunks (sixteen rows each) sit in the ring from position it0 on: rows
+// (2w, 2w + 1) of each chunk, against the activation vector at the start of
+// the activation area.  Pair i's two sums go to res[2i], res[2i + 1] (lane
+// 0).  Each warp waits for a chunk's stage only when it reads it and
+// releases it (one of the stage's eight arrivals) as soon as its dot is
+// done, so the ring refills while the slice is still being computed.
+// Returns false if a wait gave up (the stages are still released).
+// Compiled as a function of its own with K known: inside the large kernel
+// body the same loop ran several times slower.
+template <int K>
+__device__ __noinline__ bool warp_stage_pairs(int it0, int nrows, float* res) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    u64* full = full_bars();
+    u64* empty = full + kPersistStages;
+    XLane<K> x;
+    x.load(act_smem());
+    bool ok = true;
+    const int nch = (nrows + 15) / 16;
+    for (int i = 0; i < nch; ++i) {
+        const int it = it0 + i, s = it % kPersistStages;
+        if (16 * i + 2 * warp < nrows) {
+            if (ok && !wait_bar(&full[s], (unsigned)(it / kPersistStages) & 1u)) ok = false;
+            if (ok) {
+                const __half* st = stage_smem(s);
+                const bool two = 16 * i + 2 * warp + 1 < nrows;
+                const __half* rows[2] = {st + (size_t)(2 * warp) * K,
+                                         st + (size_t)(two ? 2 * warp + 1 : 2 * warp) * K};
+                float acc[2];
+                rows_dot_x<K, 2>(rows, x, acc);
+                if (lane == 0) {
+                    res[2 * i] = acc[0];
+                    res[2 * i + 1] = acc[1];
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    __syncwarp();
+    return ok;
+}
+
+// Dot products of this warp's rows q = w, w + 8, ... of a slice of nrows
+// rows of K stored rpc to a chunk, the chunks in the ring from position it0
+// on, against the activation vector; row k's sum goes to res[k].  Waits and
+// releases per stage as warp_stage_pairs does.
+template <int K>
+__device__ __noinline__ bool warp_stage_rows(int it0, int rpc, int nrows, float* res) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    u64* full = full_bars();
+    u64* empty = full + kPersistStages;
+    const float* xs = act_smem();
+    bool ok = true;
+    const int nch = (nrows + rpc - 1) / rpc;
+    int k = 0;
+    for (int j = 0; j < nch; ++j) {
+        const int it = it0 + j, s = it % kPersistStages;
+        for (int q = j * rpc; q < min(nrows, (j + 1) * rpc); ++q) {
+            if ((q & 7) != warp) continue;
+            if (ok && !wait_bar(&full[s], (unsigned)(it / kPersistStages) & 1u)) ok = false;
+            if (ok) {
+                const __half* rows[1] = {stage_smem(s) + (size_t)(q - j * rpc) * K};
+                float acc[1][1];
+                warp_rows_dot<1, 1, LdShared, 4>(rows, K, xs, K, acc);
+                if (lane == 0) res[k] = acc[0][0];
+            }
+            ++k;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    __syncwarp();
+    return ok;
 }
 
 // The tied LM head over this CTA's vocabulary rows [r0, r1): chunks of 16
@@ -561,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
     const int V = a.V, L = a.L, nh = a.nh, nkv = a.nkv;
     const int group = nh / nkv;
     const int np = a.nqkv / 2;
-    const int rpc_h = a.rows_h, rpc_i = a.rows_i;
+    const int rpc_i = a.rows_i;
 
     if (tid == 0) {
         for (int s = 0; s < a.stages; ++s) {
@@ -606,52 +637,36 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
         if (a.prof && tid == 0) a.prof[(size_t)c * a.prof_marks + id] = (long long)now_ns();
     };
     mark(0);
-    // Consume this CTA's chunks of one matrix slice in order: fn(stage, row0, n).
-    // A wait that gives up marks the thread bad; the phase end turns that
-    // into a group-wide decision.
-    // Wait (bounded) for ring stage s to hold its chunk (parity par).
-    auto wait_full = [&](int s, unsigned par) -> bool {
-        if (mbar_try_wait(&full[s], par)) return true;
-        const u64 t0 = now_ns();
-        while (now_ns() - t0 < kWaitNs)
-            if (mbar_try_wait(&full[s], par)) return true;
-        return false;
-    };
     auto idle = [&]() {};
-    auto consume = [&](int r0, int r1, int rpc, auto&& fn) {
-        for (int r = r0; r < r1; r += rpc) {
-            const int n = min(rpc, r1 - r);
-            const int s = it % a.stages;
-            const unsigned k = it / a.stages;
-            if (!bad && !wait_full(s, k & 1)) bad = true;
-            if (!bad) fn(s, r, n);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-            ++it;
-            idle();
-        }
-    };
-    // Consume a whole slice at once when it fits in the ring: wait for all
-    // its stages, run fn(stage of the slice's first chunk) -- the slice's
-    // chunks sit in consecutive stages, modulo the ring -- then release them.
-    auto consume_all = [&](int r0, int r1, int rpc, auto&& fn, int ready_mark = -1) {
-        const int nch = (r1 - r0 + rpc - 1) / rpc;
-        for (int j = 0; j < nch; ++j) {
-            const int s = (it + j) % a.stages;
-            const unsigned k = (it + j) / a.stages;
-            if (!bad && !wait_full(s, k & 1)) bad = true;
-        }
-        if (ready_mark >= 0) mark(ready_mark);
-        const int it0 = it;
-        if (!bad) fn(it0 % a.stages);
-        __syncwarp();
-        if (lane == 0)
-            for (int j = 0; j < nch; ++j) mbar_arrive(&empty[(it0 + j) % a.stages]);
-        it += nch;
-        idle();
-    };
     __shared__ float res_s[8][16];  // per-warp dot results of the current phase
     float* res = res_s[warp];
+    // Stream this CTA's slice [r0, r1) of a K = H matrix (sixteen rows to a
+    // ring stage) through warp_stage_pairs, then epi(first row, rows) on the
+    // results in res.  A slice of more stages than res holds pairs for a
+    // warp goes one stage per call.  A wait that gives up marks the thread
+    // bad (the epilogue is skipped); the phase end turns that into a
+    // group-wide decision.
+    auto stream_pairs = [&](int r0, int r1, auto&& epi) {
+        const int nch = (r1 - r0 + 15) / 16;
+        const int per = nch <= 8 ? nch : 1;
+        for (int j = 0; j < nch; j += per) {
+            const int rr = r0 + 16 * j, nn = min(16 * per, r1 - rr);
+            if (warp_stage_pairs<H>(it + j, nn, res)) epi(rr, nn);
+            else bad = true;
+        }
+        it += nch;
+    };
+    // The same for the K = I slice of down_proj, rpc rows to a stage.
+    auto stream_rows = [&](int r0, int r1, int rpc, auto&& epi) {
+        const int nch = (r1 - r0 + rpc - 1) / rpc;
+        const int per = (r1 - r0) <= 8 * 16 ? nch : 1;
+        for (int j = 0; j < nch; j += per) {
+            const int rr = r0 + rpc * j, nn = min(rpc * per, r1 - rr);
+            if (warp_stage_rows<I>(it + j, rpc, nn, res)) epi(rr, nn);
+            else bad = true;
+        }
+        it += nch;
+    };
     auto phase_end = [&]() {
         dead = compute_any(bad || rd.failed);
         return dead;
@@ -733,14 +748,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
         mark(mb + 1);
         // Sixteen rows per stage, one row pair per warp: warp w takes rows
         // 2w, 2w + 1 of each stage of its slice.
-        consume_all(qkv_r0, qkv_r1, rpc_h, [&](int s0) {
-            warp_stage_pairs<H>(s0, qkv_r1 - qkv_r0, res);
-            for (int q = warp, i = 0; 2 * q < qkv_r1 - qkv_r0; q += 8, ++i) {
-                const int pr = qkv_r0 + 2 * q;  // packed row of the pair
+        stream_pairs(qkv_r0, qkv_r1, [&](int r0_, int n_) {
+            for (int q = warp, i = 0; 2 * q < n_; q += 8, ++i) {
+                const int pr = r0_ + 2 * q;  // packed row of the pair
                 const float acc[2][1] = {{res[2 * i]}, {res[2 * i + 1]}};
                 if (lane == 0) {
                     const int s = pr / kHd, i = (pr % kHd) >> 1;
-                    const bool first = q == warp;
+                    const bool first = pr == qkv_r0 + 2 * warp;
                     const float b0 = first ? pb0 : Lw.bqkv[pr];
                     const float b1 = first ? pb1 : Lw.bqkv[pr + 1];
                     const float v0 = acc[0][0] + b0, v1 = acc[1][0] + b1;
@@ -850,10 +864,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
         }
         mark(mb + 6);
         const int o_r0 = 2 * split(H / 2, c, G), o_r1 = 2 * split(H / 2, c + 1, G);
-        consume_all(o_r0, o_r1, rpc_h, [&](int s0) {
-            warp_stage_pairs<H>(s0, o_r1 - o_r0, res);
-            for (int q = warp, i = 0; 2 * q < o_r1 - o_r0; q += 8, ++i) {
-                const int r = o_r0 + 2 * q;
+        stream_pairs(o_r0, o_r1, [&](int r0_, int n_) {
+            for (int q = warp, i = 0; 2 * q < n_; q += 8, ++i) {
+                const int r = r0_ + 2 * q;
                 // xr still holds this layer's input x (gathered for Q/K/V);
                 // lanes 0-7 write copy (lane % 4) of row r + lane / 4.
                 if (lane < 2 * kPkRep) {
@@ -885,17 +898,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
             if (i < 32 / kPkRep && 2 * q < n)
                 pk_put(pk + lay.m + (size_t)k * lay.n_m + ((r0 + 2 * q) >> 1), silu_f(res[2 * i]) * res[2 * i + 1], ep);
         };
-        if ((gu_r1 - gu_r0 + rpc_h - 1) / rpc_h <= a.stages) {
-            consume_all(gu_r0, gu_r1, rpc_h, [&](int s0) {
-                warp_stage_pairs<H>(s0, gu_r1 - gu_r0, res);
-                gu_out(gu_r0, gu_r1 - gu_r0);
-            }, mb + 14);
-        } else {
-            consume(gu_r0, gu_r1, rpc_h, [&](int s, int r0, int n) {
-                warp_stage_pairs<H>(s, n, res);
-                gu_out(r0, n);
-            });
-        }
+        stream_pairs(gu_r0, gu_r1, gu_out);
         if (phase_end()) break;
         arrive(l * 5 + 3);
         mark(mb + 10);
@@ -915,17 +918,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
             const int i = lane / kPkRep, k = lane % kPkRep, q = warp + 8 * i;
             if (i < 32 / kPkRep && q < n) pk_put(pk + lay.x2 + (size_t)k * lay.n_x + r0 + q, xr[r0 + q] + res[i], ep);
         };
-        if ((d_r1 - d_r0 + rpc_i - 1) / rpc_i <= a.stages) {
-            consume_all(d_r0, d_r1, rpc_i, [&](int s0) {
-                warp_stage_rows<I>(s0, rpc_i, d_r1 - d_r0, res);
-                down_out(d_r0, d_r1 - d_r0);
-            }, mb + 15);
-        } else {
-            consume(d_r0, d_r1, rpc_i, [&](int s, int r0, int n) {
-                warp_stage_rows<I>(s, rpc_i, n, res);
-                down_out(r0, n);
-            });
-        }
+        stream_rows(d_r0, d_r1, rpc_i, down_out);
         if (phase_end()) break;
         arrive(l * 5 + 4);
         mark(mb + 13);

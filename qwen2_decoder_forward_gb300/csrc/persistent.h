@@ -37,9 +37,8 @@ struct PersistentArgs {
 // k = 0 x gathered, 1 normed, 2 Q/K/V done, 3 q ready (attention CTAs),
 // 4 attention done, 5 partials counted, 6 merge done, 7 o_proj done,
 // 8 x1 counted, 9 x1 gathered, 10 gate/up done, 11 m counted,
-// 12 m gathered, 13 down done, 14 gate/up weights in shared memory, 15 down
-// weights in shared memory; then 1 + 16 L final x gathered, 2 + 16 L
-// LM head done, 3 + 16 L argmax done.
+// 12 m gathered, 13 down done (14 and 15 unused); then 1 + 16 L final x
+// gathered, 2 + 16 L LM head done, 3 + 16 L argmax done.
 inline int persistent_marks(int n_layer) { return 4 + 16 * n_layer; }
 
 // Size the kernel for this context and allocate its packet buffers; leaves
