@@ -438,7 +438,36 @@ __device__ __noinline__ bool warp_stage_pairs(int it0, int nrows, float* res) {
     x.load(act_smem());
     bool ok = true;
     const int nch = (nrows + 15) / 16;
-    for (int i = 0; i < nch; ++i) {
+    int i = 0;
+    // Two stages at a time where this warp has a full pair in both: the
+    // four rows' loads and reductions overlap (each row's own operations and
+    // their order are unchanged).
+    for (; i + 1 < nch && 16 * (i + 1) + 2 * warp + 1 < nrows; i += 2) {
+        const int itA = it0 + i, sA = itA % kPersistStages;
+        const int itB = itA + 1, sB = itB % kPersistStages;
+        if (ok && !wait_bar(&full[sA], (unsigned)(itA / kPersistStages) & 1u)) ok = false;
+        if (ok && !wait_bar(&full[sB], (unsigned)(itB / kPersistStages) & 1u)) ok = false;
+        if (ok) {
+            const __half* stA = stage_smem(sA);
+            const __half* stB = stage_smem(sB);
+            const __half* rows[4] = {stA + (size_t)(2 * warp) * K, stA + (size_t)(2 * warp + 1) * K,
+                                     stB + (size_t)(2 * warp) * K, stB + (size_t)(2 * warp + 1) * K};
+            float acc[4];
+            rows_dot_x<K, 4>(rows, x, acc);
+            if (lane == 0) {
+                res[2 * i] = acc[0];
+                res[2 * i + 1] = acc[1];
+                res[2 * i + 2] = acc[2];
+                res[2 * i + 3] = acc[3];
+            }
+        }
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(&empty[sA]);
+            mbar_arrive(&empty[sB]);
+        }
+    }
+    for (; i < nch; ++i) {
         const int it = it0 + i, s = it % kPersistStages;
         if (16 * i + 2 * warp < nrows) {
             if (ok && !wait_bar(&full[s], (unsigned)(it / kPersistStages) & 1u)) ok = false;
@@ -462,16 +491,55 @@ __device__ __noinline__ bool warp_stage_pairs(int it0, int nrows, float* res) {
     return ok;
 }
 
+// An activation vector of K floats stored as two half arrays: floats
+// 0..3 of each 8-float chunk c at xa[4c..4c+3], floats 4..7 at
+// xh[4c..4c+3] (xh = xa + K/2), so a warp reading chunk c = lane + 32 u
+// reads 16 consecutive bytes per lane from each half: no bank conflicts,
+// where the plain layout (32-byte lane stride) conflicts two ways.
+__device__ __forceinline__ int split_half_index(int j, int half) {
+    return ((j & 7) < 4 ? 0 : half) + (j >> 3) * 4 + (j & 3);
+}
+
+// The canonical row dot (lane l adds chunks l, l + 32, ... in order into
+// four partial sums, then the xor butterfly) of one shared-memory row with
+// x in the split-half layout, U chunks of loads in flight per lane: the
+// operations and order of warp_rows_dot, so the same bits.
+template <int K, int U>
+__device__ __forceinline__ float row_dot_split(const __half* row, const float* xa, const float* xh) {
+    constexpr int kC = K / 8;
+    const int lane = threadIdx.x & 31;
+    Acc4 part;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) part.a[e] = 0.f;
+    for (int i0 = 0; i0 * 32 < kC; i0 += U) {
+        uint4 wv[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int c = lane + 32 * (i0 + u);
+            wv[u] = c < kC ? *reinterpret_cast<const uint4*>(row + (size_t)c * 8) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int c = lane + 32 * (i0 + u);
+            if (c < kC)
+                dot8_f16_4(wv[u], *reinterpret_cast<const float4*>(xa + 4 * c),
+                           *reinterpret_cast<const float4*>(xh + 4 * c), part);
+        }
+    }
+    return warp_sum(dot4_total(part));
+}
+
 // Dot products of this warp's rows q = w, w + 8, ... of a slice of nrows
 // rows of K stored rpc to a chunk, the chunks in the ring from position it0
-// on, against the activation vector; row k's sum goes to res[k].  Waits and
-// releases per stage as warp_stage_pairs does.
+// on, against the activation vector in the split-half layout; row k's sum
+// goes to res[k].  Waits and releases per stage as warp_stage_pairs does.
 template <int K>
 __device__ __noinline__ bool warp_stage_rows(int it0, int rpc, int nrows, float* res) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     u64* full = full_bars();
     u64* empty = full + kPersistStages;
-    const float* xs = act_smem();
+    const float* xa = act_smem();
+    const float* xh = xa + K / 2;
     bool ok = true;
     const int nch = (nrows + rpc - 1) / rpc;
     int k = 0;
@@ -481,10 +549,8 @@ __device__ __noinline__ bool warp_stage_rows(int it0, int rpc, int nrows, float*
             if ((q & 7) != warp) continue;
             if (ok && !wait_bar(&full[s], (unsigned)(it / kPersistStages) & 1u)) ok = false;
             if (ok) {
-                const __half* rows[1] = {stage_smem(s) + (size_t)(q - j * rpc) * K};
-                float acc[1][1];
-                warp_rows_dot<1, 1, LdShared, 4>(rows, K, xs, K, acc);
-                if (lane == 0) res[k] = acc[0][0];
+                const float v = row_dot_split<K, 8>(stage_smem(s) + (size_t)(q - j * rpc) * K, xa, xh);
+                if (lane == 0) res[k] = v;
             }
             ++k;
         }
@@ -716,7 +782,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
     };
 
     const size_t head_stride = (size_t)a.n_ctx * kHd;
+    // This CTA's row ranges, the same for every layer.
     const int qkv_r0 = 2 * split(np, c, G), qkv_r1 = 2 * split(np, c + 1, G);
+    const int o_r0 = 2 * split(H / 2, c, G), o_r1 = 2 * split(H / 2, c + 1, G);
+    const int gu_r0 = 2 * split(I, c, G), gu_r1 = 2 * split(I, c + 1, G);
+    const int d_r0 = split(H, c, G), d_r1 = split(H, c + 1, G);
     const int rc = c % kPkRep;  // the packet copy this CTA reads
     for (int l = 0; l < L && !dead; ++l) {
         const PersistLayer& Lw = a.layers[l];
@@ -863,7 +933,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
             if (phase_end()) break;
         }
         mark(mb + 6);
-        const int o_r0 = 2 * split(H / 2, c, G), o_r1 = 2 * split(H / 2, c + 1, G);
         stream_pairs(o_r0, o_r1, [&](int r0_, int n_) {
             for (int q = warp, i = 0; 2 * q < n_; q += 8, ++i) {
                 const int r = r0_ + 2 * q;
@@ -889,14 +958,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
         if (phase_end()) break;
         mark(mb + 9);
         norm();
-        const int gu_r0 = 2 * split(I, c, G), gu_r1 = 2 * split(I, c + 1, G);
-        // Pair (gate j, up j) in rows 2j, 2j + 1 of the stage; one per warp.
         // Pair (gate j, up j) in rows 2j, 2j + 1; one pair per warp per stage.
-        // Lane 4i + k writes copy k of pair i's output.
+        // Lane 4i + k writes copy k of pair i's output, element j of m stored
+        // at its split-half position, the layout down_proj reads.
         auto gu_out = [&](int r0, int n) {
             const int i = lane / kPkRep, k = lane % kPkRep, q = warp + 8 * i;
             if (i < 32 / kPkRep && 2 * q < n)
-                pk_put(pk + lay.m + (size_t)k * lay.n_m + ((r0 + 2 * q) >> 1), silu_f(res[2 * i]) * res[2 * i + 1], ep);
+                pk_put(pk + lay.m + (size_t)k * lay.n_m + split_half_index((r0 + 2 * q) >> 1, I / 2),
+                       silu_f(res[2 * i]) * res[2 * i + 1], ep);
         };
         stream_pairs(gu_r0, gu_r1, gu_out);
         if (phase_end()) break;
@@ -912,7 +981,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
         pk_gather<20>(rd, I, [&](int j) { return mp + j; }, [&](int j, float v) { xs[j] = v; }, idle);
         if (phase_end()) break;
         mark(mb + 12);
-        const int d_r0 = split(H, c, G), d_r1 = split(H, c + 1, G);
         // xr holds x after the attention add (gathered for gate/up).
         auto down_out = [&](int r0, int n) {
             const int i = lane / kPkRep, k = lane % kPkRep, q = warp + 8 * i;
