@@ -153,7 +153,7 @@ def decode_bytes_per_step(shape, positions, q8: bool = False) -> float:
 # of 3 launches at positions ~150 of the 0.5b-decode-b1 workload) from one
 # ncu capture of the persistent decode kernel, valid only for that workload
 # and only while the kernel's sources hash to `src`.
-TRAFFIC = {"k_decode_persistent": {"workload": "0.5b-decode-b1", "src": "5a27b4a94cc8b59f", "bytes": 1000950613.3}}
+TRAFFIC = {"k_decode_persistent": {"workload": "0.5b-decode-b1", "src": "e065afd5e7c596cd", "bytes": 1001531477.3}}
 KERNEL_SOURCES = ("persistent.cu", "persistent.h", "rowdot.cuh", "common.cuh", "attn.cuh", "ctx.h")
 
 
