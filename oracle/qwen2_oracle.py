@@ -378,3 +378,26 @@ class Qwen2Oracle:
             out["logits"] = np.stack(logits)
             out["final_norm_output"] = np.stack(hidden)
         return out
+
+    def greedy_generate(self, cache: KVCache, first_token: int, start_pos: int,
+                        max_steps: int, stop_ids) -> dict:
+        """Greedy generation that ends at a stop token: generation stops at
+        the end-of-sequence id or the chat end-of-turn id (minfer page,
+        section 5 "Tokenizer and chat", stop tokens eos and im_end; nnterp
+        encyclopedia qwen2, "The chat template writes a system turn":
+        <|endoftext|> 151643 and <|im_end|> 151645).  Steps as in
+        greedy_decode; the first generated id that is in ``stop_ids`` is the
+        last one kept.  Returns ``ids`` [max_steps] with -1 after that id
+        and ``n_generated`` (the ids kept, the stop id included)."""
+        stops = {int(t) for t in stop_ids}
+        tok = int(first_token)
+        ids = np.full(max_steps, -1, dtype=np.int32)
+        n = 0
+        for s in range(max_steps):
+            r = self.forward(cache, [tok], [start_pos + s])
+            tok = int(r["ids"][0])
+            ids[s] = tok
+            n = s + 1
+            if tok in stops:
+                break
+        return {"ids": ids, "n_generated": n}

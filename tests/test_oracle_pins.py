@@ -399,3 +399,39 @@ def test_q8_0_oracle_forward_is_close_to_f16():
     la = a.forward(a.new_cache(), toks, np.arange(5))["logits"]
     lb = b.forward(b.new_cache(), toks, np.arange(5))["logits"]
     assert 0 < np.max(np.abs(la - lb)) < 0.05 * np.max(np.abs(la))
+
+
+def test_generation_stops_at_the_first_stop_id():
+    """Stop tokens end generation (minfer page section 5, eos and im_end):
+    the stop-aware generation is the plain greedy decode cut right after the
+    first generated id that is a stop id, the stop id kept, -1 after it."""
+    o, _ = tiny_oracle(n_ctx=32)
+    prompt = synth.make_tokens(TINY.vocab, 5, 21)
+    pre = o.forward(o.new_cache(), prompt, np.arange(5))
+    first = int(pre["ids"][-1])
+
+    def primed():
+        c = o.new_cache()
+        o.forward(c, prompt, np.arange(5))
+        return c
+
+    n = 20
+    ref = o.greedy_decode(primed(), first, 5, n, keep_logits=False)["ids"]
+    # A stop id first generated at step k: ids up to and including k.
+    for k in (0, 3, n - 1):
+        stop = int(ref[k])
+        k_first = int(np.flatnonzero(ref == stop)[0])
+        r = o.greedy_generate(primed(), first, 5, n, [stop])
+        assert r["n_generated"] == k_first + 1
+        np.testing.assert_array_equal(r["ids"][:k_first + 1], ref[:k_first + 1])
+        assert np.all(r["ids"][k_first + 1:] == -1)
+    # Stop ids that are never generated (or none): the plain greedy decode.
+    never = [t for t in range(TINY.vocab) if t not in set(ref.tolist())][:2]
+    for stops in ([], never):
+        r = o.greedy_generate(primed(), first, 5, n, stops)
+        assert r["n_generated"] == n
+        np.testing.assert_array_equal(r["ids"], ref)
+    # The earliest of several stop ids wins.
+    r = o.greedy_generate(primed(), first, 5, n, [int(ref[9]), int(ref[2])])
+    k_first = min(int(np.flatnonzero(ref == ref[9])[0]), int(np.flatnonzero(ref == ref[2])[0]))
+    assert r["n_generated"] == k_first + 1
