@@ -188,6 +188,28 @@ int qwen2_decode_steps(qwen2_ctx *ctx, int32_t n_seq, const int32_t *seq_ids,
                        const int32_t *first_tokens, const int32_t *start_positions,
                        int32_t n_steps, int32_t *ids, void *stream);
 
+/* Greedy decode that ends at stop tokens: generation stops at the
+ * end-of-sequence id or the chat end-of-turn id (minfer page, section 5
+ * "Tokenizer and chat", stop tokens eos and im_end; the nnterp
+ * encyclopedia's qwen2 page names them: <|endoftext|> 151643 on base
+ * models, <|im_end|> 151645 on instruct models).  Steps as
+ * qwen2_decode_steps, and the same errors and position checks, plus:
+ *   stop_ids     host int32 [n_stop], 0 <= n_stop <= 8, each in [0, vocab)
+ *                (QWEN2_E_ARG otherwise); with n_stop = 0 no id is masked
+ *   ids          int32 [n_steps][n_seq], host or device: the id each step
+ *                produced, -1 after the sequence's first generated stop id
+ *   n_generated  int32 [n_seq], host or device, not NULL: the ids kept per
+ *                sequence, the stop id included (n_steps when none came)
+ * The step graph has a fixed shape, so every step is still computed for
+ * every sequence: KV entries past a sequence's stop hold the continuation,
+ * which attention never reads before a later call writes those positions
+ * again.  The stop ids of first_tokens (inputs, not generated) do not
+ * count. */
+int qwen2_decode_steps_stop(qwen2_ctx *ctx, int32_t n_seq, const int32_t *seq_ids,
+                            const int32_t *first_tokens, const int32_t *start_positions,
+                            int32_t n_steps, const int32_t *stop_ids, int32_t n_stop,
+                            int32_t *ids, int32_t *n_generated, void *stream);
+
 /* Copy the final-norm output rows (the input of the LM head,
  * "final_norm_output" in the nnterp names) of the last prefill or decode
  * step into dst: f32 [rows][H], rows <= n_seq*n_out of that call.  Device or

@@ -44,7 +44,7 @@ FEATURE_TENSOR_PREFILL = 0x2
 # Every symbol include/qwen2.h declares.
 EXPORTS = (
     "qwen2_create", "qwen2_destroy", "qwen2_last_error", "qwen2_kv_cache",
-    "qwen2_prefill", "qwen2_decode_step", "qwen2_decode_steps",
+    "qwen2_prefill", "qwen2_decode_step", "qwen2_decode_steps", "qwen2_decode_steps_stop",
     "qwen2_final_hidden", "qwen2_synchronize", "qwen2_weight_bytes",
     "qwen2_kv_bytes_per_seq", "qwen2_quantize_q8_0", "qwen2_features", "qwen2_profile_marks",
     "qwen2_lm_head_argmax_noalloc",
@@ -109,6 +109,8 @@ def lib() -> ctypes.CDLL:
     L.qwen2_decode_step.restype = ctypes.c_int
     L.qwen2_decode_steps.argtypes = [_P, i32, pi32, pi32, pi32, i32, _P, _P]
     L.qwen2_decode_steps.restype = ctypes.c_int
+    L.qwen2_decode_steps_stop.argtypes = [_P, i32, pi32, pi32, pi32, i32, pi32, i32, _P, _P, _P]
+    L.qwen2_decode_steps_stop.restype = ctypes.c_int
     L.qwen2_final_hidden.argtypes = [_P, _P, i32, _P]
     L.qwen2_final_hidden.restype = ctypes.c_int
     L.qwen2_synchronize.argtypes = [_P, _P]
@@ -325,6 +327,26 @@ class Qwen2Model:
             self._h, n, _ptr_i32(seq_ids), _ptr_i32(first_tokens), _ptr_i32(start_positions), n_steps,
             _data_ptr(ids_out), _stream_ptr(stream)))
         return ids_out
+
+    def generate(self, seq_ids, first_tokens, start_positions, max_steps: int, stop_ids, ids_out=None,
+                 n_generated_out=None, stream=None):
+        """Greedy decode of up to ``max_steps`` tokens per sequence that ends
+        at the first generated id in ``stop_ids`` (at most 8): returns
+        (ids [max_steps, n_seq] with -1 after each sequence's stop id,
+        n_generated [n_seq] counting the stop id), CUDA tensors unless the
+        outputs are given."""
+        import torch
+        seq_ids, first_tokens, start_positions = _i32(seq_ids), _i32(first_tokens), _i32(start_positions)
+        stops = _i32(stop_ids)
+        n = len(seq_ids)
+        if ids_out is None:
+            ids_out = torch.empty((max_steps, n), dtype=torch.int32, device="cuda")
+        if n_generated_out is None:
+            n_generated_out = torch.empty((n,), dtype=torch.int32, device="cuda")
+        self._check(lib().qwen2_decode_steps_stop(
+            self._h, n, _ptr_i32(seq_ids), _ptr_i32(first_tokens), _ptr_i32(start_positions), max_steps,
+            _ptr_i32(stops), len(stops), _data_ptr(ids_out), _data_ptr(n_generated_out), _stream_ptr(stream)))
+        return ids_out, n_generated_out
 
     def final_hidden(self, rows: int, stream=None):
         """final_norm_output rows of the last call, [rows, H] CUDA tensor."""

@@ -198,6 +198,9 @@ int setup_workspace(Ctx& c) {
     A(&c.ds.slot, S);
     A(&c.ds.step, 1);
     A(&c.ds.ids_hist, (size_t)kIdsHist * S);
+    A(&c.ds.stop_ids, kMaxStopIds);
+    A(&c.ds.stop_done, S);
+    A(&c.ds.n_gen, S);
     A(&c.err, 1);
     return r;
 }
@@ -505,8 +508,11 @@ int qwen2_decode_step(qwen2_ctx* h, int32_t n_seq, const int32_t* seq_ids, const
     return QWEN2_OK;
 }
 
-int qwen2_decode_steps(qwen2_ctx* h, int32_t n_seq, const int32_t* seq_ids, const int32_t* first_tokens,
-                       const int32_t* start_positions, int32_t n_steps, int32_t* ids, void* stream) {
+// decode_steps with optional stop ids; with n_generated NULL (plain
+// decode_steps) no stop handling runs at all.
+static int decode_steps_impl(qwen2_ctx* h, int32_t n_seq, const int32_t* seq_ids, const int32_t* first_tokens,
+                      const int32_t* start_positions, int32_t n_steps, const int32_t* stop_ids, int32_t n_stop,
+                      int32_t* ids, int32_t* n_generated, void* stream) {
     if (!h) return QWEN2_E_ARG;
     Ctx& c = h->c;
     c.last_error.clear();
@@ -517,6 +523,13 @@ int qwen2_decode_steps(qwen2_ctx* h, int32_t n_seq, const int32_t* seq_ids, cons
                                                  " sequences per decode step with these weights");
     if (!seq_ids || !first_tokens || !start_positions || !ids) return fail(&c, QWEN2_E_ARG, "null pointer");
     if (n_steps < 1) return fail(&c, QWEN2_E_ARG, "n_steps must be >= 1");
+    if (n_stop < 0 || n_stop > kMaxStopIds)
+        return fail(&c, QWEN2_E_ARG, "n_stop outside [0, " + std::to_string(kMaxStopIds) + "]");
+    const bool stops = n_generated != nullptr;
+    if (n_stop > 0 && (!stop_ids || !stops)) return fail(&c, QWEN2_E_ARG, "null stop_ids or n_generated");
+    for (int k = 0; k < n_stop; ++k)
+        if (stop_ids[k] < 0 || stop_ids[k] >= c.cfg.vocab)
+            return fail(&c, QWEN2_E_ARG, "stop id " + std::to_string(stop_ids[k]) + " outside [0, vocab)");
     int r = check_seq_ids(c, n_seq, seq_ids);
     if (r) return r;
     if ((r = check_tokens(c, n_seq, first_tokens))) return r;
@@ -525,18 +538,35 @@ int qwen2_decode_steps(qwen2_ctx* h, int32_t n_seq, const int32_t* seq_ids, cons
     Q2_CHECK(&c, cudaMemcpyAsync(d.tok, first_tokens, n_seq * 4, cudaMemcpyHostToDevice, st));
     Q2_CHECK(&c, cudaMemcpyAsync(d.pos, start_positions, n_seq * 4, cudaMemcpyHostToDevice, st));
     Q2_CHECK(&c, cudaMemcpyAsync(d.slot, seq_ids, n_seq * 4, cudaMemcpyHostToDevice, st));
+    if (n_stop > 0) Q2_CHECK(&c, cudaMemcpyAsync(d.stop_ids, stop_ids, n_stop * 4, cudaMemcpyHostToDevice, st));
     Q2_CHECK(&c, cudaMemsetAsync(d.step, 0, 4, st));
-    const bool host_out = !is_device_ptr(ids);
+    const bool host_out = !is_device_ptr(ids) || (stops && !is_device_ptr(n_generated));
     for (int s0 = 0; s0 < n_steps; s0 += kIdsHist) {
         const int n = std::min(kIdsHist, n_steps - s0);
         for (int s = 0; s < n; ++s)
             if ((r = run_decode_step(c, n_seq, false, st))) return r;
+        if (stops) Q2_CHECK(&c, enqueue_stop_mask(c, n_seq, n, n_stop, s0 == 0, st));
         Q2_CHECK(&c, cudaMemcpy2DAsync(ids + (size_t)s0 * n_seq, n_seq * 4, d.ids_hist, c.cfg.max_seqs * 4,
                                        n_seq * 4, n, cudaMemcpyDefault, st));
     }
+    if (stops) Q2_CHECK(&c, cudaMemcpyAsync(n_generated, d.n_gen, n_seq * 4, cudaMemcpyDefault, st));
     c.last_rows_out = n_seq;
     if (host_out) Q2_CHECK(&c, cudaStreamSynchronize(st));
     return QWEN2_OK;
+}
+
+int qwen2_decode_steps(qwen2_ctx* h, int32_t n_seq, const int32_t* seq_ids, const int32_t* first_tokens,
+                       const int32_t* start_positions, int32_t n_steps, int32_t* ids, void* stream) {
+    return decode_steps_impl(h, n_seq, seq_ids, first_tokens, start_positions, n_steps, nullptr, 0, ids, nullptr,
+                             stream);
+}
+
+int qwen2_decode_steps_stop(qwen2_ctx* h, int32_t n_seq, const int32_t* seq_ids, const int32_t* first_tokens,
+                            const int32_t* start_positions, int32_t n_steps, const int32_t* stop_ids,
+                            int32_t n_stop, int32_t* ids, int32_t* n_generated, void* stream) {
+    if (h && !n_generated) return fail(&h->c, QWEN2_E_ARG, "n_generated is NULL");
+    return decode_steps_impl(h, n_seq, seq_ids, first_tokens, start_positions, n_steps, stop_ids, n_stop, ids,
+                             n_generated, stream);
 }
 
 int qwen2_final_hidden(qwen2_ctx* h, float* dst, int32_t rows, void* stream) {

@@ -92,7 +92,11 @@ struct DecodeState {
     int* slot = nullptr;     // [max_seqs] KV slot (sequence id)
     int* step = nullptr;     // [1] index of the step within a decode_steps run
     int* ids_hist = nullptr; // [kIdsHist][max_seqs] ids per step
+    int* stop_ids = nullptr;  // [kMaxStopIds] stop ids of a decode_steps_stop run
+    int* stop_done = nullptr; // [max_seqs] 1 once the sequence generated a stop id
+    int* n_gen = nullptr;     // [max_seqs] ids kept so far, the stop id included
 };
+constexpr int kMaxStopIds = 8;
 
 // Per-layer weight pointers the persistent decode kernel reads.
 struct PersistLayer {
@@ -164,6 +168,11 @@ struct Ctx {
 // Enqueue one decode step for the first B slots of DecodeState on `st`
 // (B <= 8).  Logits go to ws.logits when want_logits.
 cudaError_t enqueue_decode_step(Ctx& c, int B, bool want_logits, cudaStream_t st);
+// Stop tokens over the first n_steps rows of the id history (one chunk of a
+// decode_steps_stop run): ids after a sequence's first stop id become -1,
+// and stop_done / n_gen carry over from the previous chunk unless first
+// (n_stop may be 0: nothing is masked and n_gen counts every step).
+cudaError_t enqueue_stop_mask(Ctx& c, int n_seq, int n_steps, int n_stop, bool first, cudaStream_t st);
 
 // LM head + argmax over `B` rows of `xin` (f32 [B][H]); writes the hidden
 // rows (ws.hidden), optional logits [B][V] and ids [B].  `decode` selects the

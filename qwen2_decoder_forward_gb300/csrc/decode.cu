@@ -1161,4 +1161,48 @@ cudaError_t decode_set_smem_limits(int max_bytes) {
     return e;
 }
 
+namespace {
+
+// Stop tokens (minfer page section 5, "Tokenizer and chat": generation ends
+// at eos or im_end) over one chunk of the id history, one thread per
+// sequence, steps in order: once a sequence has generated one of the stop
+// ids, its later ids become -1; n_gen counts the ids kept, the stop id
+// included.  done / n_gen carry over from the previous chunk of the same
+// run unless `first`.
+__global__ void k_stop_mask(int* ids_hist, int stride, int n_steps, int n_seq, const int* stop_ids, int n_stop,
+                            int* done, int* n_gen, int first) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= n_seq) return;
+    int stop[kMaxStopIds];
+    for (int k = 0; k < kMaxStopIds; ++k) stop[k] = k < n_stop ? stop_ids[k] : -1;
+    int d = first ? 0 : done[b];
+    int g = first ? 0 : n_gen[b];
+    for (int s = 0; s < n_steps; ++s) {
+        int* p = ids_hist + (size_t)s * stride + b;
+        if (d) {
+            *p = -1;
+            continue;
+        }
+        const int id = *p;
+        ++g;
+        for (int k = 0; k < kMaxStopIds; ++k)
+            if (k < n_stop && id == stop[k]) d = 1;
+    }
+    done[b] = d;
+    n_gen[b] = g;
+}
+
+}  // namespace
+
+cudaError_t enqueue_stop_mask(Ctx& c, int n_seq, int n_steps, int n_stop, bool first, cudaStream_t st) {
+    if (n_seq < 1 || n_seq > c.cfg.max_seqs || n_steps < 1 || n_steps > kIdsHist || n_stop < 0 ||
+        n_stop > kMaxStopIds)
+        return cudaErrorInvalidValue;
+    const int threads = 128;
+    k_stop_mask<<<(n_seq + threads - 1) / threads, threads, 0, st>>>(c.ds.ids_hist, c.cfg.max_seqs, n_steps, n_seq,
+                                                                        c.ds.stop_ids, n_stop, c.ds.stop_done,
+                                                                        c.ds.n_gen, first ? 1 : 0);
+    return cudaGetLastError();
+}
+
 }  // namespace qwen2

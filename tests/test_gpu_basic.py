@@ -85,6 +85,68 @@ def test_free_running_decode_steps_matches_oracle(q2):
     np.testing.assert_array_equal(host[:, 0], out)
 
 
+@pytest.mark.parametrize("shape_name,batch", [("toy", 1), ("ragged", 3)])
+def test_generation_stops_at_stop_ids(q2, shape_name, batch):
+    """Stop tokens (minfer page section 5): after each sequence's first
+    generated stop id the ids are -1 and n_generated counts the stop id.
+    Batch 1 runs the persistent kernel, batch 3 the step graph.  The result
+    must be the GPU's own plain greedy sequence cut at the stop (exact), and
+    the oracle's stop-aware generation wherever the two greedy sequences
+    agree up to the stop."""
+    shape = synth.SHAPES[shape_name]
+    w = synth.make_weights(shape, 0)
+    n, n_ctx = 24, 64
+    prompts = [synth.make_tokens(shape.vocab, 6 + 5 * b, 600 + b) for b in range(batch)]
+    orc, ref = run_oracle(shape, w, prompts, n, n_ctx)
+    seqs = list(range(batch))
+    with q2.Qwen2Model(shape, w, n_ctx=n_ctx, max_seqs=batch, max_tokens=sum(len(p) for p in prompts)) as m:
+        _, ids0 = m.prefill(seqs, prompts)
+        first = [int(t) for t in ids0.cpu().numpy()]
+        starts = [len(p) for p in prompts]
+        plain = m.decode_steps(seqs, first, starts, n).cpu().numpy()
+        # Stop ids that occur: one early in the first sequence, one later in
+        # the last, and one that never occurs in the batch's plain output.
+        never = next(t for t in range(shape.vocab) if t not in set(plain.reshape(-1).tolist()))
+        stops = [int(plain[4, 0]), int(plain[13, batch - 1]), never]
+        ids, n_gen = m.generate(seqs, first, starts, n, stops)
+        ids, n_gen = ids.cpu().numpy(), n_gen.cpu().numpy()
+        # Host outputs give the same.
+        h_ids = np.zeros((n, batch), dtype=np.int32)
+        h_n = np.zeros((batch,), dtype=np.int32)
+        m.generate(seqs, first, starts, n, stops, ids_out=h_ids, n_generated_out=h_n)
+        # No stop ids: nothing masked, every step counted.
+        ids_all, n_all = m.generate(seqs, first, starts, n, [])
+        with pytest.raises(q2.Qwen2Error) as e:
+            m.generate(seqs, first, starts, n, [shape.vocab])
+        assert e.value.code == q2.QWEN2_E_ARG
+        with pytest.raises(q2.Qwen2Error) as e:
+            m.generate(seqs, first, starts, n, list(range(9)))
+        assert e.value.code == q2.QWEN2_E_ARG
+        m.synchronize()
+    np.testing.assert_array_equal(h_ids, ids)
+    np.testing.assert_array_equal(h_n, n_gen)
+    np.testing.assert_array_equal(ids_all.cpu().numpy(), plain)
+    assert np.all(n_all.cpu().numpy() == n)
+    for b in range(batch):
+        hit = [s for s in range(n) if int(plain[s, b]) in stops]
+        k = hit[0] if hit else n - 1
+        assert int(n_gen[b]) == k + 1
+        np.testing.assert_array_equal(ids[:k + 1, b], plain[:k + 1, b])
+        assert np.all(ids[k + 1:, b] == -1)
+        # Against the oracle: the GPU's plain sequence matches the oracle's
+        # up to a near-tie (checked); up to there the stop must agree too.
+        pre, dec, _ = ref[b]
+        if first[b] != int(pre["ids"][-1]):
+            continue
+        agree = check_free_running(plain[:, b], dec["ids"], dec["logits"], f"seq {b}")
+        if agree > k:
+            cache = orc.new_cache()
+            orc.forward(cache, prompts[b], np.arange(len(prompts[b])))
+            r = orc.greedy_generate(cache, first[b], len(prompts[b]), n, stops)
+            assert r["n_generated"] == int(n_gen[b])
+            np.testing.assert_array_equal(r["ids"], ids[:, b])
+
+
 @pytest.mark.parametrize("shape_name", ["ragged", "toy"])
 @pytest.mark.parametrize("flags", ["fuse", "graph"])
 def test_variants_are_bit_identical(q2, flags, shape_name):
