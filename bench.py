@@ -149,24 +149,32 @@ def decode_bytes_per_step(shape, positions, q8: bool = False) -> float:
     return float(elems * per_elem + small + len(p) * H * per_elem + kv_pos * np.sum(p + 2))
 
 
-# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum, mean
-# of 3 launches at positions ~150 of the 0.5b-decode-b1 workload) from one
-# ncu capture of the persistent decode kernel, valid only for that workload
-# and only while the kernel's sources hash to `src`.
-TRAFFIC = {"k_decode_persistent": {"workload": "0.5b-decode-b1", "src": "e065afd5e7c596cd", "bytes": 1001531477.3}}
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum of
+# the 21st launch, a position near 150 of the 0.5b-decode-b1 workload) from
+# the `--set full` ncu capture of the persistent decode kernel, valid only
+# for that workload and only while the kernel's sources -- their code, with
+# // comments and blank lines left out -- hash to `src`.
+TRAFFIC = {"k_decode_persistent": {"workload": "0.5b-decode-b1", "src": "842422b03eb52ad4", "bytes": 1003233280.0}}
 KERNEL_SOURCES = ("persistent.cu", "persistent.h", "rowdot.cuh", "common.cuh", "attn.cuh", "ctx.h")
 
 
-def kernel_traffic(name: str, workload: str):
+def kernel_source_hash() -> str:
     import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "qwen2_decoder_forward_gb300", "csrc", f)) as fh:
+            for line in fh:
+                code = line.split("//", 1)[0].rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
+    return h.hexdigest()[:16]
+
+
+def kernel_traffic(name: str, workload: str):
     rec = TRAFFIC.get(name)
     if rec is None or rec.get("workload") != workload:
         return None
-    h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "qwen2_decoder_forward_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
-    return rec["bytes"] if h.hexdigest()[:16] == rec["src"] else None
+    return rec["bytes"] if kernel_source_hash() == rec["src"] else None
 
 
 def prefill_flops(shape, lens, n_keep: int) -> float:

@@ -6,20 +6,22 @@
 // slices stream, in the order they are used, through a ring of six 28 KB
 // shared-memory stages filled by bulk (TMA) copies with mbarriers, issued by
 // one lane of a feeding warpgroup, so the weight stream runs ahead of the
-// compute and never waits for activations.  The feeding warpgroup hands its
-// registers to the two compute warpgroups (setmaxnreg), which then need not
-// spill.  The compute warps run
-// the steps of the layer (minfer "Qwen2 / Qwen2.5 Architecture Support",
+// compute and never waits for activations; each compute warp waits for a
+// stage when it reads it and releases it when its dot products are done.
+// The feeding warpgroup hands its registers to the two compute warpgroups
+// (setmaxnreg), which then need not spill.  The compute warps run the
+// steps of the layer (minfer "Qwen2 / Qwen2.5 Architecture Support",
 // section 1) and exchange activation vectors through global "packets":
 // 64-bit words holding a float and the launch's epoch, written and read
 // with single-copy atomic 64-bit accesses, so a reader that sees the
 // current epoch has the value.  A per-phase arrival counter, polled by one
-// thread per CTA, tells a consumer when to read them.
+// thread per CTA, tells a consumer when to read the larger exchanges.
 //
 // Per layer the dependencies are x -> Q/K/V (norm needs all of x), q/k/v ->
-// attention, attention partials -> o_proj (the chunk merge is recomputed by
-// every CTA), x -> gate/up (norm), SiLU(gate)*up -> down.  The arithmetic
-// is the per-step kernels' own (rowdot.cuh, attn.cuh), so the logits are
+// attention units (kv head, key chunk, query heads), the units' partials
+// -> the merge of head h by CTA h -> o, broadcast to every CTA -> o_proj,
+// x -> gate/up (norm), SiLU(gate)*up -> down.  The arithmetic is the
+// per-step kernels' own (rowdot.cuh, attn.cuh), so the logits are
 // bit-identical to the multi-kernel path.
 //
 // Every wait is bounded (2 s of the global timer): a wait that gives up
