@@ -14,8 +14,9 @@ diagram):
       - GQA attention (Q K^T scale -> softmax -> V) - WO matmul - + residual
       - RMSNorm - gate/up matmuls - SiLU(gate) * up - down matmul - + residual
 
-then the final RMSNorm and the tied LM head (nnterp encyclopedia qwen2,
-"The readout is the plain projection"; Module 7 section 7.3, W_lm = E).
+then the final RMSNorm and the LM head (nnterp encyclopedia qwen2,
+"The readout is the plain projection"; Module 7 section 7.3: tied, W_lm =
+E, unless the weights carry a separate ``lm_head``).
 A matrix product is a library primitive (numpy ``@``); there is no blocking,
 fusion or reordering beyond the definition.
 
@@ -184,6 +185,11 @@ class OracleWeights:
             return np.asarray(a, dtype=np.float64)
 
         self.embed = mat(weights["embed"])
+        # The readout matrix: the embedding itself when the LM head is tied
+        # (0.5B to 3B), a separate matrix from 7B up (nnterp encyclopedia
+        # qwen2, "The readout is the plain projection").
+        lm = weights.get("lm_head")
+        self.lm_head = self.embed if lm is None else mat(lm)
         self.final_norm = np.asarray(weights["final_norm"], dtype=np.float64)
         self.layers = []
         for lw in weights["layers"]:
@@ -345,7 +351,7 @@ class Qwen2Oracle:
                 probes["layer_output"].append(x.copy())
         x = x[x.shape[0] - n_keep:]
         f = rms_norm(x, self.w.final_norm, c.rms_eps)
-        logits = f @ self.w.embed.T
+        logits = f @ self.w.lm_head.T
         if rec:
             probes["final_norm_output"] = f
             probes["logits"] = logits

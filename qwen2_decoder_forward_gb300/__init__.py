@@ -206,6 +206,11 @@ class Qwen2Model:
 
     def __init__(self, shape, weights: dict, n_ctx: int, max_seqs: int = 1, max_tokens: int = 128,
                  weight_format: int = WEIGHTS_F16, prefill_mode: int = PREFILL_F32, flags: int = 0):
+        # The library's LM head is the embedding (tied, as on 0.5B to 3B); a
+        # separate head matrix would otherwise be dropped without a word.
+        if weights.get("lm_head") is not None or not getattr(shape, "tie_embeddings", True):
+            raise Qwen2Error(QWEN2_E_UNSUPPORTED, "an untied LM head (a separate lm_head matrix) is not "
+                                                  "supported by this build")
         L = lib()
         self.shape = shape
         self.n_ctx, self.max_seqs, self.max_tokens = n_ctx, max_seqs, max_tokens

@@ -49,6 +49,7 @@ class ModelShape:
     vocab: int
     rms_eps: float = 1e-6
     rope_theta: float = 1e6
+    tie_embeddings: bool = True   # False: a separate LM head matrix
 
 
 SHAPES = {
@@ -70,6 +71,18 @@ SHAPES = {
     "toy-mha": ModelShape("toy-mha", n_layer=2, hidden=256, n_head=4,
                           n_kv_head=4, head_dim=64, intermediate=1024,
                           vocab=4096),
+    # head_dim 128, the head width of every size above 0.5B (nnterp
+    # encyclopedia qwen2, "Grouped-query attention"): 4 q heads over 2 kv
+    # heads, tied LM head (as 1.5B and 3B).
+    "toy-hd128": ModelShape("toy-hd128", n_layer=2, hidden=512, n_head=4,
+                            n_kv_head=2, head_dim=128, intermediate=1024,
+                            vocab=4096),
+    # head_dim 128 with 8 q heads over 4 kv heads and an untied LM head, the
+    # layout of 7B (28 over 4, separate embedding and unembedding: nnterp
+    # "Grouped-query attention" and "The readout is the plain projection").
+    "toy-untied": ModelShape("toy-untied", n_layer=2, hidden=1024, n_head=8,
+                             n_kv_head=4, head_dim=128, intermediate=1024,
+                             vocab=4096, tie_embeddings=False),
 }
 
 
@@ -93,7 +106,9 @@ def make_weights(shape: ModelShape, seed: int = 0) -> dict:
 
     Returns ``{"embed": f16 [V, H], "final_norm": f32 [H], "layers": [dict]}``
     where each layer dict has the keys of :data:`LAYER_KEYS`.  The LM head is
-    tied to ``embed`` (no separate array).
+    tied to ``embed`` (no separate array) unless ``shape.tie_embeddings`` is
+    False; then ``"lm_head"``, f16 [V, H], is drawn after every other array,
+    so the tied arrays of a shape are the same draws either way.
     """
     return _make_weights_cached(shape, seed)
 
@@ -122,6 +137,8 @@ def _make_weights_cached(shape: ModelShape, seed: int) -> dict:
         }
         w["layers"].append(layer)
     w["final_norm"] = _draw(rng, (H,), "norm")
+    if not shape.tie_embeddings:
+        w["lm_head"] = _draw(rng, (V, H), "matrix")
     for arr in _iter_arrays(w):
         arr.setflags(write=False)
     return w
@@ -130,6 +147,8 @@ def _make_weights_cached(shape: ModelShape, seed: int) -> dict:
 def _iter_arrays(w):
     yield w["embed"]
     yield w["final_norm"]
+    if "lm_head" in w:
+        yield w["lm_head"]
     for layer in w["layers"]:
         for k in LAYER_KEYS:
             yield layer[k]

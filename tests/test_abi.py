@@ -106,3 +106,13 @@ def test_no_alloc_head_rejects_bad_sizes_before_any_cuda_call(L):
     assert L.qwen2_lm_head_argmax_noalloc(fake, fake, 1, 1032, 151936, None, fake, None) == 1
     assert b"hidden_size" in L.qwen2_last_error(None)
     assert L.qwen2_lm_head_argmax_noalloc(fake, fake, 1, 896, 151936, None, None, None) == 1
+
+
+def test_untied_lm_head_is_rejected_before_any_device_work():
+    """The C ABI's LM head is the tied embedding; the binding refuses a
+    separate head matrix instead of dropping it."""
+    shape = synth.SHAPES["toy-untied"]
+    w = synth.make_weights(shape, 0)
+    with pytest.raises(q2.Qwen2Error) as e:
+        q2.Qwen2Model(shape, w, n_ctx=32)
+    assert e.value.code == q2.QWEN2_E_UNSUPPORTED

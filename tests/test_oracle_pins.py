@@ -167,9 +167,10 @@ def test_rope_scores_depend_on_relative_position_only():
 # Attention.
 # ---------------------------------------------------------------------------
 
-def test_gqa_attention_matches_sdpa_with_repeated_kv_heads():
+@pytest.mark.parametrize("hd", [8, 128])
+def test_gqa_attention_matches_sdpa_with_repeated_kv_heads(hd):
     rng = np.random.default_rng(6)
-    T, nh, nkv, hd = 9, 6, 2, 8
+    T, nh, nkv = 9, 6, 2
     q = rng.standard_normal((T, nh, hd))
     K = rng.standard_normal((T, nkv, hd))
     V = rng.standard_normal((T, nkv, hd))
@@ -277,11 +278,14 @@ def _torch_library_forward(shape, w, tokens):
         m = F.rms_norm(x, (H,), weight=t(lw["ffn_norm"]), eps=shape.rms_eps)
         x = x + F.linear(F.silu(F.linear(m, t(lw["wg"]))) * F.linear(m, t(lw["wu"])), t(lw["wd"]))
     f = F.rms_norm(x, (H,), weight=t(w["final_norm"]), eps=shape.rms_eps)
-    return F.linear(f, t(w["embed"])).numpy()
+    return F.linear(f, t(w["lm_head"] if "lm_head" in w else w["embed"])).numpy()
 
 
 @pytest.mark.parametrize("shape", [TINY, dataclasses.replace(TINY, name="tiny-mha", n_kv_head=4),
-                                   dataclasses.replace(TINY, name="tiny-g4", n_head=4, n_kv_head=1)])
+                                   dataclasses.replace(TINY, name="tiny-g4", n_head=4, n_kv_head=1),
+                                   dataclasses.replace(TINY, name="tiny-hd128", hidden=256, n_head=2,
+                                                       n_kv_head=1, head_dim=128),
+                                   dataclasses.replace(TINY, name="tiny-untied", tie_embeddings=False)])
 def test_forward_matches_torch_library_brute_force(shape):
     o, w = tiny_oracle(shape)
     toks = synth.make_tokens(shape.vocab, 12, 11)
@@ -303,6 +307,33 @@ def test_residual_identity_and_readout():
         np.testing.assert_allclose(lhs, probes["layer_output"][i], rtol=1e-15, atol=1e-15)
     np.testing.assert_allclose(r["logits"], probes["final_norm_output"] @ w["embed"].astype(np.float64).T,
                                rtol=1e-14, atol=1e-15)
+
+
+def test_untied_lm_head_is_a_separate_readout():
+    """From 7B up the embedding and the unembedding are separate matrices
+    (nnterp "The readout is the plain projection"): the layers read the
+    embedding only, the logits come from the LM head, and an LM head equal
+    to the embedding is the tied model bit for bit."""
+    untied = dataclasses.replace(TINY, name="tiny-untied", tie_embeddings=False)
+    o_u, w_u = tiny_oracle(untied)
+    assert w_u["lm_head"].shape == w_u["embed"].shape
+    assert not np.array_equal(w_u["lm_head"], w_u["embed"])
+    tied_w = {k: v for k, v in w_u.items() if k != "lm_head"}
+    o_t = oracle.build_oracle(TINY, tied_w, 32)
+    same_w = dict(tied_w, lm_head=np.array(w_u["embed"]))
+    o_s = oracle.build_oracle(untied, same_w, 32)
+    toks = synth.make_tokens(TINY.vocab, 9, 14)
+    r_u = o_u.forward(o_u.new_cache(), toks, np.arange(9))
+    r_t = o_t.forward(o_t.new_cache(), toks, np.arange(9))
+    r_s = o_s.forward(o_s.new_cache(), toks, np.arange(9))
+    np.testing.assert_array_equal(r_s["logits"], r_t["logits"])
+    np.testing.assert_array_equal(r_u["final_norm_output"], r_t["final_norm_output"])
+    np.testing.assert_allclose(r_u["logits"], r_u["final_norm_output"] @ w_u["lm_head"].astype(np.float64).T,
+                               rtol=1e-14, atol=1e-15)
+    assert not np.allclose(r_u["logits"], r_t["logits"])
+    # The tied arrays are the same draws whether or not a head is drawn.
+    for k in ("embed", "final_norm"):
+        np.testing.assert_array_equal(w_u[k], synth.make_weights(TINY, 3)[k])
 
 
 def test_kv_cache_decode_equals_full_recompute():
