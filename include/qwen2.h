@@ -216,6 +216,15 @@ int qwen2_decode_steps_stop(qwen2_ctx *ctx, int32_t n_seq, const int32_t *seq_id
  * host dst. */
 int qwen2_final_hidden(qwen2_ctx *ctx, float *dst, int32_t rows, void *stream);
 
+/* Test hook for failure detection without a GPU fault: enqueue on `stream`
+ * a one-thread kernel that writes `code` into the context's device guard
+ * word the way a kernel does when one of its bounded waits gives up
+ * (first code wins).  The next qwen2_synchronize then reports
+ * QWEN2_E_DEVICE_GUARD with that code, clears the word and resets the
+ * persistent decode kernel's exchange state.  code in [1, 4]
+ * (position, token, shape, timeout); QWEN2_E_ARG otherwise. */
+int qwen2_test_raise_guard(qwen2_ctx *ctx, int32_t code, void *stream);
+
 /* Synchronise `stream` and report any device-side guard that tripped since
  * the last check (QWEN2_E_DEVICE_GUARD, with the guard's code in the
  * message); clears the guard word. */

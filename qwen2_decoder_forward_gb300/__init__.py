@@ -47,7 +47,7 @@ EXPORTS = (
     "qwen2_prefill", "qwen2_decode_step", "qwen2_decode_steps", "qwen2_decode_steps_stop",
     "qwen2_final_hidden", "qwen2_synchronize", "qwen2_weight_bytes",
     "qwen2_kv_bytes_per_seq", "qwen2_quantize_q8_0", "qwen2_features", "qwen2_profile_marks",
-    "qwen2_lm_head_argmax_noalloc",
+    "qwen2_lm_head_argmax_noalloc", "qwen2_test_raise_guard",
 )
 
 
@@ -111,6 +111,8 @@ def lib() -> ctypes.CDLL:
     L.qwen2_decode_steps.restype = ctypes.c_int
     L.qwen2_decode_steps_stop.argtypes = [_P, i32, pi32, pi32, pi32, i32, pi32, i32, _P, _P, _P]
     L.qwen2_decode_steps_stop.restype = ctypes.c_int
+    L.qwen2_test_raise_guard.argtypes = [_P, i32, _P]
+    L.qwen2_test_raise_guard.restype = ctypes.c_int
     L.qwen2_final_hidden.argtypes = [_P, _P, i32, _P]
     L.qwen2_final_hidden.restype = ctypes.c_int
     L.qwen2_synchronize.argtypes = [_P, _P]
@@ -368,6 +370,11 @@ class Qwen2Model:
         dims = (ctypes.c_int64 * 6)()
         self._check(lib().qwen2_kv_cache(self._h, ctypes.byref(base), dims))
         return torch.as_tensor(_CudaArray(base.value, list(dims), "<f4"), device="cuda")
+
+    def test_raise_guard(self, code: int, stream=None):
+        """Test hook: write ``code`` into the device guard word (as a kernel's
+        bounded wait does when it gives up); the next synchronize reports it."""
+        self._check(lib().qwen2_test_raise_guard(self._h, code, _stream_ptr(stream)))
 
     def synchronize(self, stream=None):
         self._check(lib().qwen2_synchronize(self._h, _stream_ptr(stream)))

@@ -16,6 +16,12 @@
 
 using namespace qwen2;
 
+namespace qwen2 {
+// decode.cu: write `code` into the device guard word from a one-thread
+// kernel (the qwen2_test_raise_guard hook).
+cudaError_t enqueue_raise_guard(Ctx& c, int code, cudaStream_t st);
+}  // namespace qwen2
+
 struct qwen2_ctx {
     Ctx c;
 };
@@ -577,6 +583,15 @@ int qwen2_final_hidden(qwen2_ctx* h, float* dst, int32_t rows, void* stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     Q2_CHECK(&c, cudaMemcpyAsync(dst, c.ws.hidden, (size_t)rows * c.cfg.hidden * 4, cudaMemcpyDefault, st));
     if (!is_device_ptr(dst)) Q2_CHECK(&c, cudaStreamSynchronize(st));
+    return QWEN2_OK;
+}
+
+int qwen2_test_raise_guard(qwen2_ctx* h, int32_t code, void* stream) {
+    if (!h) return QWEN2_E_ARG;
+    Ctx& c = h->c;
+    // The guard codes the kernels write: 1 position, 2 token, 3 shape, 4 timeout.
+    if (code < 1 || code > 4) return fail(&c, QWEN2_E_ARG, "guard code outside [1, 4]");
+    Q2_CHECK(&c, enqueue_raise_guard(c, code, static_cast<cudaStream_t>(stream)));
     return QWEN2_OK;
 }
 

@@ -1192,7 +1192,15 @@ __global__ void k_stop_mask(int* ids_hist, int stride, int n_steps, int n_seq, c
     n_gen[b] = g;
 }
 
+// The guard write of a kernel whose bounded wait gave up, on its own.
+__global__ void k_raise_guard(int* err, int code) { raise_guard(err, code); }
+
 }  // namespace
+
+cudaError_t enqueue_raise_guard(Ctx& c, int code, cudaStream_t st) {
+    k_raise_guard<<<1, 1, 0, st>>>(c.err, code);
+    return cudaGetLastError();
+}
 
 cudaError_t enqueue_stop_mask(Ctx& c, int n_seq, int n_steps, int n_stop, bool first, cudaStream_t st) {
     if (n_seq < 1 || n_seq > c.cfg.max_seqs || n_steps < 1 || n_steps > kIdsHist || n_stop < 0 ||

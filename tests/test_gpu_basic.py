@@ -274,3 +274,44 @@ def test_tensor_core_prefill(q2, shape_name):
         check_logits_ids(logits.cpu().numpy(), ids.cpu().numpy(), fref["logits"], "tensor prefill, no cut")
         check_hidden(hid, fref["final_norm_output"], "tensor prefill, no cut")
         m.synchronize()
+
+
+def test_device_guard_is_reported_once_and_decoding_continues(q2):
+    """Failure detection without a GPU fault: the test hook writes the
+    device guard word the way a kernel's bounded wait does when it gives up.
+    synchronize reports QWEN2_E_DEVICE_GUARD once, clears the word and resets
+    the persistent kernel's exchange state, and the next decode gives the
+    same ids as before."""
+    shape = synth.SHAPES["toy"]
+    w = synth.make_weights(shape, 0)
+    prompt = synth.make_tokens(shape.vocab, 16, 1001)
+    with q2.Qwen2Model(shape, w, n_ctx=64, max_seqs=1, max_tokens=16) as m:
+        _, ids = m.prefill([0], [prompt])
+        first = int(ids[0])
+        ref = m.decode_steps([0], [first], [16], 8).cpu().numpy()
+        m.test_raise_guard(4)
+        with pytest.raises(q2.Qwen2Error) as e:
+            m.synchronize()
+        assert e.value.code == q2.QWEN2_E_DEVICE_GUARD
+        assert "bounded wait timed out" in str(e.value)
+        m.synchronize()
+        again = m.decode_steps([0], [first], [16], 8).cpu().numpy()
+        m.synchronize()
+        with pytest.raises(q2.Qwen2Error) as e:
+            m.test_raise_guard(0)
+        assert e.value.code == q2.QWEN2_E_ARG
+    np.testing.assert_array_equal(again, ref)
+
+
+def test_oversized_kv_cache_is_an_allocation_error(q2):
+    """A KV cache larger than the device (65,536 sequences x 32,768
+    positions of the toy model: 4 TB) is QWEN2_E_OOM from create, and the
+    device stays usable."""
+    shape = synth.SHAPES["toy"]
+    w = synth.make_weights(shape, 0)
+    with pytest.raises(q2.Qwen2Error) as e:
+        q2.Qwen2Model(shape, w, n_ctx=32768, max_seqs=65536, max_tokens=16)
+    assert e.value.code == q2.QWEN2_E_OOM
+    with q2.Qwen2Model(shape, w, n_ctx=64, max_seqs=1, max_tokens=16) as m:
+        m.prefill([0], [synth.make_tokens(shape.vocab, 8, 3)])
+        m.synchronize()
