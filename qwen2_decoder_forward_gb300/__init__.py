@@ -28,6 +28,13 @@ QWEN2_E_OOM = 4
 QWEN2_E_CUDA = 5
 QWEN2_E_DEVICE_GUARD = 6
 
+# Stop ids of the Qwen2 / Qwen2.5 tokenizers for generate(): base
+# checkpoints end generation on <|endoftext|>, instruct checkpoints on
+# <|im_end|> (nnterp encyclopedia qwen2, "The chat template writes a system
+# turn"; minfer "Qwen2 / Qwen2.5 Architecture Support", section 5).
+ENDOFTEXT_ID = 151643
+IM_END_ID = 151645
+
 WEIGHTS_F16 = 0
 WEIGHTS_Q8_0 = 1
 PREFILL_F32 = 0

@@ -116,3 +116,11 @@ def test_untied_lm_head_is_rejected_before_any_device_work():
     with pytest.raises(q2.Qwen2Error) as e:
         q2.Qwen2Model(shape, w, n_ctx=32)
     assert e.value.code == q2.QWEN2_E_UNSUPPORTED
+
+
+def test_stop_id_constants_match_the_pages():
+    from conftest import read_golden
+    g = read_golden("qwen2_0p5b_pages.txt")
+    assert q2.ENDOFTEXT_ID == int(g["endoftext_id"])
+    assert q2.IM_END_ID == int(g["im_end_id"])
+    assert max(q2.ENDOFTEXT_ID, q2.IM_END_ID) < synth.SHAPES["qwen2.5-0.5b"].vocab
