@@ -162,11 +162,12 @@ def kernel_source_hash() -> str:
     import hashlib
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "qwen2_decoder_forward_gb300", "csrc", f)) as fh:
-            for line in fh:
-                code = line.split("//", 1)[0].rstrip()
-                if code:
-                    h.update(code.encode() + b"\n")
+        with open(os.path.join(ROOT, "qwen2_decoder_forward_gb300", "csrc", f), "rb") as fh:
+            text = fh.read().decode("utf-8", errors="replace")  # the same on any locale
+        for line in text.splitlines():
+            code = line.split("//", 1)[0].rstrip()
+            if code:
+                h.update(code.encode("utf-8") + b"\n")
     return h.hexdigest()[:16]
 
 

@@ -16,7 +16,7 @@ def pytest_configure(config):
 def read_golden(name: str) -> dict:
     """Parse a ``key = value  # citation`` fixture under tests/golden."""
     out = {}
-    with open(os.path.join(ROOT, "tests", "golden", name)) as f:
+    with open(os.path.join(ROOT, "tests", "golden", name), encoding="utf-8") as f:
         for line in f:
             line = line.split("#", 1)[0].strip()
             if not line:

@@ -24,7 +24,7 @@ def L():
 
 
 def header_symbols():
-    src = open(os.path.join(ROOT, "include", "qwen2.h")).read()
+    src = open(os.path.join(ROOT, "include", "qwen2.h"), encoding="utf-8").read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return set(re.findall(r"\b(qwen2_[a-z0-9_]+)\s*\(", src))
 
