@@ -6,18 +6,21 @@ package and its CUDA library) never imports it and has no CPU fallback.
 
 Parity status per function (what pins each one is in ``tests/``):
 rms_norm, rope_neox, silu, softmax_rows, gqa_attention, Qwen2Oracle.forward,
-quantize_q8_0 / dequantize_q8_0 are all pinned; end-to-end logits of a real
+quantize_q8_0 / dequantize_q8_0 and quantize_q4_0 / dequantize_q4_0 are all
+pinned; end-to-end logits of a real
 Qwen2 checkpoint are parity unpinned (no checkpoint exists here).
 """
 from .qwen2_oracle import (KVCache, OracleConfig, OracleWeights, PositionError,
                            Qwen2Oracle, gqa_attention, greedy_ids, rms_norm,
                            rope_inv_freq, rope_neox, silu, softmax_rows)
+from .q4_0 import dequantize_q4_0, pack_nibbles, quantize_q4_0, unpack_nibbles
 from .q8_0 import QK, dequantize_q8_0, quantize_q8_0
 
 __all__ = [
     "KVCache", "OracleConfig", "OracleWeights", "PositionError", "Qwen2Oracle",
     "gqa_attention", "greedy_ids", "rms_norm", "rope_inv_freq", "rope_neox",
     "silu", "softmax_rows", "QK", "dequantize_q8_0", "quantize_q8_0",
+    "dequantize_q4_0", "quantize_q4_0", "pack_nibbles", "unpack_nibbles",
     "build_oracle",
 ]
 

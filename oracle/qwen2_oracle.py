@@ -39,6 +39,7 @@ import dataclasses
 
 import numpy as np
 
+from . import q4_0 as _q4
 from . import q8_0 as _q8
 
 
@@ -164,9 +165,10 @@ class _Layer:
 class OracleWeights:
     """float64 copies of one model's weights.
 
-    ``weight_format`` "f16" widens the f16 matrices exactly; "q8_0" first
-    quantises every linear matrix and the tied embedding with
-    :func:`oracle.q8_0.quantize_q8_0` and widens the dequantised values (the
+    ``weight_format`` "f16" widens the f16 matrices exactly; "q8_0" (or
+    "q4_0") first quantises every linear matrix and the tied embedding with
+    :func:`oracle.q8_0.quantize_q8_0` (:func:`oracle.q4_0.quantize_q4_0`)
+    and widens the dequantised values (the
     embedding gather and the LM head then both read the quantised matrix,
     since it is one tied matrix, Module 7 section 7.3).  Q/K/V are stacked
     into one ``[(nh + 2 nkv) hd, H]`` matrix and gate/up into one
@@ -174,7 +176,7 @@ class OracleWeights:
     """
 
     def __init__(self, weights: dict, weight_format: str = "f16"):
-        if weight_format not in ("f16", "q8_0"):
+        if weight_format not in ("f16", "q8_0", "q4_0"):
             raise ValueError(weight_format)
         self.weight_format = weight_format
 
@@ -182,6 +184,9 @@ class OracleWeights:
             if weight_format == "q8_0":
                 q, d = _q8.quantize_q8_0(a)
                 return _q8.dequantize_q8_0(q, d)
+            if weight_format == "q4_0":
+                q, d = _q4.quantize_q4_0(a)
+                return _q4.dequantize_q4_0(q, d)
             return np.asarray(a, dtype=np.float64)
 
         self.embed = mat(weights["embed"])

@@ -466,3 +466,60 @@ def test_generation_stops_at_the_first_stop_id():
     r = o.greedy_generate(primed(), first, 5, n, [int(ref[9]), int(ref[2])])
     k_first = min(int(np.flatnonzero(ref == ref[9])[0]), int(np.flatnonzero(ref == ref[2])[0]))
     assert r["n_generated"] == k_first + 1
+
+
+# ---------------------------------------------------------------------------
+# Q4_0 (the reading in oracle/q4_0.py: blocks of 32 along K, d = amax / 7,
+# codes c + 8 in nibbles, element 2j low / 2j + 1 high).
+# ---------------------------------------------------------------------------
+
+def test_q4_0_special_blocks_rounding_and_nibble_order():
+    w = np.zeros((4, 64), dtype=np.float16)
+    w[1, :32] = 0.5                       # constant block -> c = 7 everywhere
+    w[2, 3] = -2.0                        # one-hot negative -> c = -7 at 3
+    w[3, :4] = [7.0, 2.5, -2.5, 0.5]      # d = 1 exactly: halves round away from zero
+    packed, d = oracle.quantize_q4_0(w)
+    assert packed.dtype == np.uint8 and packed.shape == (4, 32)
+    assert d.dtype == np.float16 and d.shape == (4, 2)
+    codes = oracle.unpack_nibbles(packed)
+    assert np.all(codes[0] == 8) and np.all(d[0] == 0)
+    assert np.all(codes[1, :32] == 15) and np.all(codes[1, 32:] == 8)
+    assert d[1, 0] == np.float16(np.float32(0.5) / np.float32(7))
+    assert codes[2, 3] == 1 and np.count_nonzero(codes[2] - 8) == 1
+    assert d[3, 0] == 1.0
+    np.testing.assert_array_equal(codes[3, :4], [15, 11, 5, 9])   # 7, 3, -3, 1 (+8)
+    assert packed[3, 0] == 0xBF and packed[3, 1] == 0x95          # low nibble = even element
+    assert np.all(codes >= 1) and np.all(codes <= 15)
+
+
+def test_q4_0_round_trip_bound_exact_dequant_and_size():
+    rng = np.random.default_rng(31)
+    w = (rng.standard_normal((8, 256)) * 0.02).astype(np.float16)
+    packed, d = oracle.quantize_q4_0(w)
+    assert packed.nbytes + d.nbytes == (w.size // 32) * 18           # 4.5 bits an element
+    deq = oracle.dequantize_q4_0(packed, d)
+    x = w.astype(np.float64).reshape(8, 8, 32)
+    dd = (np.max(np.abs(w.astype(np.float32).reshape(8, 8, 32)), axis=2) / np.float32(7)).astype(np.float64)
+    dh = d.astype(np.float64)
+    bound = dd / 2 + 7 * np.abs(dd - dh) + 1e-12
+    assert np.all(np.abs(x - deq.reshape(8, 8, 32)) <= bound[:, :, None])
+    c = oracle.unpack_nibbles(packed).astype(np.float32) - 8
+    f32 = (d.astype(np.float32).repeat(32, axis=1) * c)              # the float32 product
+    np.testing.assert_array_equal(f32.astype(np.float64), deq)
+    codes = rng.integers(0, 16, size=(3, 64)).astype(np.uint8)
+    np.testing.assert_array_equal(oracle.unpack_nibbles(oracle.pack_nibbles(codes)), codes)
+
+
+def test_q4_0_oracle_forward_tracks_f16():
+    shape = dataclasses.replace(TINY, hidden=64, head_dim=16, intermediate=96)
+    w = synth.make_weights(shape, 17)
+    a = oracle.build_oracle(shape, w, 16)
+    b4 = oracle.build_oracle(shape, w, 16, weight_format="q4_0")
+    b8 = oracle.build_oracle(shape, w, 16, weight_format="q8_0")
+    toks = synth.make_tokens(shape.vocab, 8, 18)
+    la = a.forward(a.new_cache(), toks, np.arange(8))["logits"]
+    l4 = b4.forward(b4.new_cache(), toks, np.arange(8))["logits"]
+    l8 = b8.forward(b8.new_cache(), toks, np.arange(8))["logits"]
+    e4, e8 = np.max(np.abs(l4 - la)), np.max(np.abs(l8 - la))
+    assert 0 < e8 < e4                       # 4-bit codes are coarser than 8-bit ones
+    assert np.corrcoef(l4.ravel(), la.ravel())[0, 1] > 0.95
