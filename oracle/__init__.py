@@ -14,12 +14,12 @@ from .qwen2_oracle import (KVCache, OracleConfig, OracleWeights, PositionError,
                            Qwen2Oracle, gqa_attention, greedy_ids, rms_norm,
                            rope_inv_freq, rope_neox, silu, softmax_rows)
 from .q4_0 import dequantize_q4_0, pack_nibbles, quantize_q4_0, unpack_nibbles
-from .q8_0 import QK, dequantize_q8_0, quantize_q8_0
+from .q8_0 import QK, dequantize_q8_0, q8_0_matmul, quantize_q8_0
 
 __all__ = [
     "KVCache", "OracleConfig", "OracleWeights", "PositionError", "Qwen2Oracle",
     "gqa_attention", "greedy_ids", "rms_norm", "rope_inv_freq", "rope_neox",
-    "silu", "softmax_rows", "QK", "dequantize_q8_0", "quantize_q8_0",
+    "silu", "softmax_rows", "QK", "dequantize_q8_0", "quantize_q8_0", "q8_0_matmul",
     "dequantize_q4_0", "quantize_q4_0", "pack_nibbles", "unpack_nibbles",
     "build_oracle",
 ]

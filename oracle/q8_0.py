@@ -53,3 +53,27 @@ def dequantize_q8_0(q: np.ndarray, d: np.ndarray) -> np.ndarray:
     rows, k = q.shape
     scale = d.astype(np.float64)[:, :, None]
     return (scale * q.reshape(rows, k // QK, QK).astype(np.float64)).reshape(rows, k)
+
+
+def q8_0_matmul(x: np.ndarray, wq: np.ndarray, wd: np.ndarray) -> np.ndarray:
+    """A product with both operands in Q8_0: ``x @ W^T`` for f32 activation
+    rows ``x`` [rows, K] and a Q8_0 weight matrix (``wq`` int8 [out, K],
+    ``wd`` float16 [out, K // 32]).
+
+    The minfer page "Qwen2 / Qwen2.5 Architecture Support", section 6, says
+    the CPU path runs on Q8_0 activations and the CUDA prefill on an int8
+    MMQ product, without further detail.  Reading: each activation row is
+    rounded to float32 and quantised to Q8_0 exactly as a weight row is
+    (module docstring).  Each 32-block's int8 products are summed exactly,
+    that integer is scaled by the two blocks' f16 scales, and the blocks are
+    added in order (float64 here)."""
+    xq, xd = quantize_q8_0(np.asarray(x, dtype=np.float32))
+    rows, k = xq.shape
+    nb = k // QK
+    xs = xq.reshape(rows, nb, QK).astype(np.int64)
+    ws = wq.reshape(wq.shape[0], nb, QK).astype(np.int64)
+    out = np.zeros((rows, wq.shape[0]), dtype=np.float64)
+    for b in range(nb):
+        isum = xs[:, b, :] @ ws[:, b, :].T                      # exact integers
+        out += isum.astype(np.float64) * np.outer(xd[:, b].astype(np.float64), wd[:, b].astype(np.float64))
+    return out

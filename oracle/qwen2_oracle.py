@@ -159,7 +159,8 @@ def greedy_ids(logits: np.ndarray) -> np.ndarray:
 # ---------------------------------------------------------------------------
 
 class _Layer:
-    __slots__ = ("attn_norm", "wqkv", "bqkv", "wo", "ffn_norm", "wgu", "wd")
+    __slots__ = ("attn_norm", "wqkv", "bqkv", "wo", "ffn_norm", "wgu", "wd",
+                 "wqkv_codes", "wo_codes", "wgu_codes", "wd_codes")
 
 
 class OracleWeights:
@@ -172,7 +173,9 @@ class OracleWeights:
     embedding gather and the LM head then both read the quantised matrix,
     since it is one tied matrix, Module 7 section 7.3).  Q/K/V are stacked
     into one ``[(nh + 2 nkv) hd, H]`` matrix and gate/up into one
-    ``[2I, H]`` matrix; the unfused forward reads row slices of them.
+    ``[2I, H]`` matrix; the unfused forward reads row slices of them.  With
+    "q8_0" each matrix also keeps its codes (``*_codes``: int8 values and
+    f16 scales) for the Q8_0-activation products.
     """
 
     def __init__(self, weights: dict, weight_format: str = "f16"):
@@ -181,31 +184,39 @@ class OracleWeights:
         self.weight_format = weight_format
 
         def mat(a):
+            """(float64 matrix, its Q8_0 codes or None)."""
             if weight_format == "q8_0":
                 q, d = _q8.quantize_q8_0(a)
-                return _q8.dequantize_q8_0(q, d)
+                return _q8.dequantize_q8_0(q, d), (q, d)
             if weight_format == "q4_0":
                 q, d = _q4.quantize_q4_0(a)
-                return _q4.dequantize_q4_0(q, d)
-            return np.asarray(a, dtype=np.float64)
+                return _q4.dequantize_q4_0(q, d), None
+            return np.asarray(a, dtype=np.float64), None
 
-        self.embed = mat(weights["embed"])
+        def stack(parts):
+            m = np.concatenate([p[0] for p in parts], axis=0)
+            if any(p[1] is None for p in parts):
+                return m, None
+            return m, (np.concatenate([p[1][0] for p in parts], axis=0),
+                       np.concatenate([p[1][1] for p in parts], axis=0))
+
+        self.embed, self.embed_codes = mat(weights["embed"])
         # The readout matrix: the embedding itself when the LM head is tied
         # (0.5B to 3B), a separate matrix from 7B up (nnterp encyclopedia
         # qwen2, "The readout is the plain projection").
         lm = weights.get("lm_head")
-        self.lm_head = self.embed if lm is None else mat(lm)
+        self.lm_head, self.lm_head_codes = (self.embed, self.embed_codes) if lm is None else mat(lm)
         self.final_norm = np.asarray(weights["final_norm"], dtype=np.float64)
         self.layers = []
         for lw in weights["layers"]:
             L = _Layer()
             L.attn_norm = np.asarray(lw["attn_norm"], dtype=np.float64)
-            L.wqkv = np.concatenate([mat(lw["wq"]), mat(lw["wk"]), mat(lw["wv"])], axis=0)
+            L.wqkv, L.wqkv_codes = stack([mat(lw["wq"]), mat(lw["wk"]), mat(lw["wv"])])
             L.bqkv = np.concatenate([lw["bq"], lw["bk"], lw["bv"]]).astype(np.float64)
-            L.wo = mat(lw["wo"])
+            L.wo, L.wo_codes = mat(lw["wo"])
             L.ffn_norm = np.asarray(lw["ffn_norm"], dtype=np.float64)
-            L.wgu = np.concatenate([mat(lw["wg"]), mat(lw["wu"])], axis=0)
-            L.wd = mat(lw["wd"])
+            L.wgu, L.wgu_codes = stack([mat(lw["wg"]), mat(lw["wu"])])
+            L.wd, L.wd_codes = mat(lw["wd"])
             self.layers.append(L)
 
 
@@ -233,7 +244,9 @@ class Qwen2Oracle:
     """
 
     def __init__(self, cfg: OracleConfig, weights: OracleWeights,
-                 fuse_qkv: bool = True, fuse_ffn: bool = True):
+                 fuse_qkv: bool = True, fuse_ffn: bool = True, act_q8: bool = False):
+        if act_q8 and (weights.weight_format != "q8_0" or not (fuse_qkv and fuse_ffn)):
+            raise ValueError("Q8_0 activations need Q8_0 weights and the fused products")
         if cfg.hidden != cfg.n_head * cfg.head_dim:
             raise ValueError("head_dim must equal hidden / n_head")
         if cfg.n_head % cfg.n_kv_head:
@@ -242,6 +255,14 @@ class Qwen2Oracle:
         self.w = weights
         self.fuse_qkv = fuse_qkv
         self.fuse_ffn = fuse_ffn
+        self.act_q8 = act_q8
+
+    def _lin(self, x: np.ndarray, W: np.ndarray, codes) -> np.ndarray:
+        """x @ W^T; with ``act_q8`` the product of the Q8_0-quantised rows of x
+        and W's Q8_0 codes (:func:`oracle.q8_0.q8_0_matmul`)."""
+        if self.act_q8:
+            return _q8.q8_0_matmul(x, *codes)
+        return x @ W.T
 
     def new_cache(self) -> KVCache:
         return KVCache(self.cfg)
@@ -252,7 +273,7 @@ class Qwen2Oracle:
         c = self.cfg
         nq, nk = c.n_head * c.head_dim, c.n_kv_head * c.head_dim
         if self.fuse_qkv:
-            y = n @ L.wqkv.T + L.bqkv
+            y = self._lin(n, L.wqkv, L.wqkv_codes) + L.bqkv
             q, k, v = y[:, :nq], y[:, nq:nq + nk], y[:, nq + nk:]
         else:
             q = n @ L.wqkv[:nq].T + L.bqkv[:nq]
@@ -263,14 +284,14 @@ class Qwen2Oracle:
     def _ffn(self, L: _Layer, m: np.ndarray):
         I = self.cfg.intermediate
         if self.fuse_ffn:
-            gu = m @ L.wgu.T
+            gu = self._lin(m, L.wgu, L.wgu_codes)
             g, u = gu[:, :I], gu[:, I:]
         else:
             g = m @ L.wgu[:I].T
             u = m @ L.wgu[I:].T
         act = silu(g)
         neurons = act * u
-        return act, neurons, neurons @ L.wd.T
+        return act, neurons, self._lin(neurons, L.wd, L.wd_codes)
 
     # -- the whole forward ----------------------------------------------------
 
@@ -332,7 +353,7 @@ class Qwen2Oracle:
             cache.V[li, positions] = v
             o = gqa_attention(q, cache.K[li, :P], cache.V[li, :P], positions)
             o = o.reshape(T, c.n_head * c.head_dim)
-            attn_out = o @ L.wo.T
+            attn_out = self._lin(o, L.wo, L.wo_codes)
             if rec:
                 probes["attention_norm_output"].append(n)
                 probes["attention_queries"].append(q)
@@ -356,7 +377,7 @@ class Qwen2Oracle:
                 probes["layer_output"].append(x.copy())
         x = x[x.shape[0] - n_keep:]
         f = rms_norm(x, self.w.final_norm, c.rms_eps)
-        logits = f @ self.w.lm_head.T
+        logits = self._lin(f, self.w.lm_head, self.w.lm_head_codes)
         if rec:
             probes["final_norm_output"] = f
             probes["logits"] = logits

@@ -523,3 +523,57 @@ def test_q4_0_oracle_forward_tracks_f16():
     e4, e8 = np.max(np.abs(l4 - la)), np.max(np.abs(l8 - la))
     assert 0 < e8 < e4                       # 4-bit codes are coarser than 8-bit ones
     assert np.corrcoef(l4.ravel(), la.ravel())[0, 1] > 0.95
+
+
+# ---------------------------------------------------------------------------
+# Products with Q8_0 activations (the reading in oracle.q8_0.q8_0_matmul).
+# ---------------------------------------------------------------------------
+
+def test_q8_0_matmul_is_the_product_of_the_dequantised_operands():
+    rng = np.random.default_rng(41)
+    x = rng.standard_normal((5, 96)).astype(np.float32) * 3
+    w = (rng.standard_normal((7, 96)) * 0.02).astype(np.float16)
+    wq, wd = oracle.quantize_q8_0(w)
+    xq, xd = oracle.quantize_q8_0(x)
+    ref = torch.from_numpy(oracle.dequantize_q8_0(xq, xd)) @ torch.from_numpy(oracle.dequantize_q8_0(wq, wd)).T
+    out = oracle.q8_0_matmul(x, wq, wd)
+    np.testing.assert_allclose(out, ref.numpy(), rtol=1e-12, atol=1e-14)
+
+
+def test_q8_0_matmul_is_lossless_on_q8_0_activations_and_bounded_otherwise():
+    rng = np.random.default_rng(42)
+    w = (rng.standard_normal((6, 64)) * 0.02).astype(np.float16)
+    wq, wd = oracle.quantize_q8_0(w)
+    wdeq = oracle.dequantize_q8_0(wq, wd)
+    # Rows already on the Q8_0 grid (|code| reaching 127 in every block):
+    # quantising them again gives back the same values.
+    codes = rng.integers(-127, 128, size=(3, 2, 32))
+    codes[:, :, 0] = 127
+    scale = rng.uniform(0.01, 1.0, size=(3, 2)).astype(np.float16).astype(np.float32)
+    x = (scale[:, :, None] * codes).reshape(3, 64).astype(np.float32)
+    np.testing.assert_allclose(oracle.q8_0_matmul(x, wq, wd), x.astype(np.float64) @ wdeq.T, rtol=1e-13, atol=1e-15)
+    # Any rows: the error is within the activations' quantisation bound.
+    x = rng.standard_normal((4, 64)).astype(np.float32)
+    xb = x.reshape(4, 2, 32)
+    d = (np.max(np.abs(xb), axis=2) / np.float32(127)).astype(np.float64)
+    dh = d.astype(np.float32).astype(np.float16).astype(np.float64)
+    elem = (d / 2 + 127 * np.abs(d - dh))[:, :, None] * np.ones((1, 1, 32))
+    bound = elem.reshape(4, 64) @ np.abs(wdeq).T + 1e-12
+    err = np.abs(oracle.q8_0_matmul(x, wq, wd) - x.astype(np.float64) @ wdeq.T)
+    assert np.all(err <= bound) and np.max(err) > 0
+
+
+def test_q8_0_activation_forward_tracks_the_q8_0_weight_forward():
+    shape = dataclasses.replace(TINY, hidden=64, head_dim=16, intermediate=96)
+    w = synth.make_weights(shape, 17)
+    cfg = oracle.OracleConfig.from_shape(shape, 16)
+    wq8 = oracle.OracleWeights(w, "q8_0")
+    a = oracle.Qwen2Oracle(cfg, wq8)
+    b = oracle.Qwen2Oracle(cfg, wq8, act_q8=True)
+    toks = synth.make_tokens(shape.vocab, 8, 18)
+    la = a.forward(a.new_cache(), toks, np.arange(8))["logits"]
+    lb = b.forward(b.new_cache(), toks, np.arange(8))["logits"]
+    assert 0 < np.max(np.abs(la - lb)) < 0.05 * np.max(np.abs(la))
+    assert np.corrcoef(la.ravel(), lb.ravel())[0, 1] > 0.99
+    with pytest.raises(ValueError):
+        oracle.Qwen2Oracle(cfg, oracle.OracleWeights(w, "f16"), act_q8=True)
