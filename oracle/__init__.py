@@ -5,10 +5,12 @@ leg of ``bench.py``.  The product path (the ``qwen2_decoder_forward_gb300``
 package and its CUDA library) never imports it and has no CPU fallback.
 
 Parity status per function (what pins each one is in ``tests/``):
-rms_norm, rope_neox, silu, softmax_rows, gqa_attention, Qwen2Oracle.forward,
-quantize_q8_0 / dequantize_q8_0 and quantize_q4_0 / dequantize_q4_0 are all
-pinned; end-to-end logits of a real
-Qwen2 checkpoint are parity unpinned (no checkpoint exists here).
+rms_norm, rope_neox, silu, softmax_rows, gqa_attention, Qwen2Oracle.forward
+(head_dim 64 and 128, tied and untied LM head, f16 / Q8_0 / Q4_0 weights,
+Q8_0 activations), Qwen2Oracle.greedy_generate, quantize_q8_0 /
+dequantize_q8_0, q8_0_matmul, quantize_q4_0 / dequantize_q4_0 and the
+nibble packing are all pinned.  End-to-end logits of a real Qwen2
+checkpoint are parity unpinned (no checkpoint exists here).
 """
 from .qwen2_oracle import (KVCache, OracleConfig, OracleWeights, PositionError,
                            Qwen2Oracle, gqa_attention, greedy_ids, rms_norm,
