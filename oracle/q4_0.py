@@ -25,6 +25,8 @@ from __future__ import annotations
 
 import numpy as np
 
+from .q8_0 import round_half_away_magnitude
+
 QK = 32
 
 
@@ -43,8 +45,7 @@ def quantize_q4_0(w: np.ndarray):
     d = (amax / np.float32(7.0)).astype(np.float32)        # float32 division
     safe = np.where(d == 0, np.float32(1.0), d)[:, :, None]
     v = (x / safe).astype(np.float32)                      # float32 division
-    # Round half away from zero; |v| <= 7.0001, so |v| + 0.5 is exact.
-    c = np.sign(v) * np.floor(np.abs(v) + np.float32(0.5))
+    c = np.sign(v) * round_half_away_magnitude(np.abs(v))
     c = np.clip(c, -7, 7)
     c = np.where((d == 0)[:, :, None], 0, c)
     codes = (c + 8).astype(np.uint8).reshape(rows, k)

@@ -24,6 +24,21 @@ import numpy as np
 QK = 32
 
 
+def round_half_away_magnitude(a: np.ndarray) -> np.ndarray:
+    """Round non-negative float32 magnitudes to the nearest integer, ties
+    upward (so ``sign * result`` rounds half away from zero).
+
+    ``floor(a + 0.5)`` is not this: for ``a = 0.49999997`` (the largest
+    float32 below one half) the sum rounds to 1.0 in float32.  Here the
+    fractional part ``a - floor(a)`` is exact in float32 (both terms share
+    the binade of ``a`` or the floor is zero), so the comparison with one
+    half decides the tie exactly."""
+    a = np.asarray(a, dtype=np.float32)
+    fl = np.floor(a)
+    frac = (a - fl).astype(np.float32)
+    return fl + (frac >= np.float32(0.5)).astype(np.float32)
+
+
 def quantize_q8_0(w: np.ndarray):
     """Quantise a float16 matrix ``[rows, K]`` (K a multiple of 32).
 
@@ -39,9 +54,7 @@ def quantize_q8_0(w: np.ndarray):
     d = (amax / np.float32(127.0)).astype(np.float32)      # float32 division
     safe = np.where(d == 0, np.float32(1.0), d)[:, :, None]
     v = (x / safe).astype(np.float32)                      # float32 division
-    # Round half away from zero: |v| <= 127.0001, so |v| + 0.5 is exact in
-    # float32 and its floor is the rounded magnitude.
-    r = np.sign(v) * np.floor(np.abs(v) + np.float32(0.5))
+    r = np.sign(v) * round_half_away_magnitude(np.abs(v))
     r = np.clip(r, -127, 127)
     r = np.where((d == 0)[:, :, None], 0, r)
     q = r.astype(np.int8).reshape(rows, k)

@@ -91,6 +91,21 @@ def test_q8_0_packer_matches_oracle_bytes(L):
     np.testing.assert_array_equal(d_lib.view(np.uint16), d_orc.view(np.uint16))
 
 
+def test_q8_0_packer_rounds_half_away_like_the_oracle(L):
+    """Half cases decided by the rounding rule alone (a block whose largest
+    magnitude is 127 has d = 1): the packer and the oracle both round half
+    away from zero."""
+    w = np.zeros((2, 64), dtype=np.float16)
+    w[0, :7] = [127.0, 0.5, -0.5, 1.5, -1.5, 2.5, -2.5]
+    w[1, 32:39] = [-127.0, 126.5, -126.5, 3.5, -3.5, 4.5, -4.5]
+    q_lib, d_lib = q2.quantize_q8_0(w)
+    q_orc, d_orc = oracle.quantize_q8_0(w)
+    np.testing.assert_array_equal(q_lib[0, :7], [127, 1, -1, 2, -2, 3, -3])
+    np.testing.assert_array_equal(q_lib[1, 32:39], [-127, 127, -127, 4, -4, 5, -5])
+    np.testing.assert_array_equal(q_lib, q_orc)
+    np.testing.assert_array_equal(d_lib.view(np.uint16), d_orc.view(np.uint16))
+
+
 def test_q8_0_packer_rejects_ragged_k(L):
     w = np.zeros((2, 48), dtype=np.float16)
     q = np.empty((2, 48), dtype=np.int8)

@@ -401,6 +401,55 @@ def test_q8_0_special_blocks():
     assert np.all(np.diff(q[3, :32].astype(int)) >= 0)
 
 
+def test_q8_0_rounds_half_away_from_zero():
+    """Reading of the unnamed Q8_0 rounding (minfer page "Qwen2 / Qwen2.5
+    Architecture Support", sections 3 and 6): round half away from zero.
+    A block whose largest magnitude is 127 has d = 1 exactly, so x / d is x
+    and every half case is decided by the rounding rule alone: half-even
+    would give 0, 2, 2 where half-away gives 1, 2, 3."""
+    w = np.zeros((1, 32), dtype=np.float16)
+    w[0, :7] = [127.0, 0.5, -0.5, 1.5, -1.5, 2.5, -2.5]
+    q, d = oracle.quantize_q8_0(w)
+    assert d[0, 0] == 1.0
+    np.testing.assert_array_equal(q[0, :7], [127, 1, -1, 2, -2, 3, -3])
+    # The largest float32 below one half rounds to 0.  No float16 weight
+    # reaches this quotient; float32 activation rows (the Q8_0 activation
+    # product) can, and floor(|v| + 0.5) in float32 would give 1 here.
+    below = np.nextafter(np.float32(0.5), np.float32(0))
+    x = np.zeros((1, 32), dtype=np.float32)
+    x[0, :3] = [127.0, below, -below]
+    q, d = oracle.quantize_q8_0(x)
+    assert d[0, 0] == 1.0
+    np.testing.assert_array_equal(q[0, :3], [127, 0, 0])
+    # Just above one half, and a large quotient just below a half step.
+    x[0, 1:3] = [np.nextafter(np.float32(0.5), np.float32(1)), np.float32(126.49999)]
+    q, _ = oracle.quantize_q8_0(x)
+    np.testing.assert_array_equal(q[0, 1:3], [1, 126])
+
+
+def test_greedy_ids_take_the_lowest_index_of_a_tie():
+    """Greedy argmax keeps the lowest index among equal maxima, decided on
+    the float32 logits both sides hold (xinfer "Module 7", section 7.3, the
+    on-device argmax; the reading of ties is the lowest index)."""
+    row = np.array([0.25, 3.0, -1.0, 3.0, 3.0], dtype=np.float64)
+    assert oracle.greedy_ids(row[None])[0] == 1
+    assert oracle.greedy_ids(row[None, ::-1].copy())[0] == 0
+    # Two logits that differ in float64 but round to the same float32: a
+    # tie in float32, so the lower index wins although the later one is
+    # larger in float64.
+    a = 1.0
+    b = 1.0 + 2.0 ** -30
+    assert np.float32(a) == np.float32(b) and b > a
+    assert oracle.greedy_ids(np.array([[0.0, a, b]]))[0] == 1
+    # A row of equal values, and a batch of rows with ties at different places.
+    assert oracle.greedy_ids(np.zeros((1, 7)))[0] == 0
+    rows = np.zeros((3, 6))
+    rows[0, [2, 5]] = 1.0
+    rows[1, [4, 1]] = 2.0
+    rows[2, [5]] = 0.5
+    np.testing.assert_array_equal(oracle.greedy_ids(rows), [2, 1, 5])
+
+
 def test_q8_0_round_trip_bound_and_exact_dequant():
     rng = np.random.default_rng(16)
     w = (0.02 * rng.standard_normal((64, 256))).astype(np.float16)
@@ -490,6 +539,13 @@ def test_q4_0_special_blocks_rounding_and_nibble_order():
     np.testing.assert_array_equal(codes[3, :4], [15, 11, 5, 9])   # 7, 3, -3, 1 (+8)
     assert packed[3, 0] == 0xBF and packed[3, 1] == 0x95          # low nibble = even element
     assert np.all(codes >= 1) and np.all(codes <= 15)
+    # Float32 rows: the largest float32 below one half rounds to 0 (code 8).
+    below = np.nextafter(np.float32(0.5), np.float32(0))
+    x = np.zeros((1, 32), dtype=np.float32)
+    x[0, :3] = [7.0, below, -below]
+    packed, d = oracle.quantize_q4_0(x)
+    assert d[0, 0] == 1.0
+    np.testing.assert_array_equal(oracle.unpack_nibbles(packed)[0, :3], [15, 8, 8])
 
 
 def test_q4_0_round_trip_bound_exact_dequant_and_size():
