@@ -265,19 +265,24 @@ int64_t qwen2_kv_bytes_per_seq(const qwen2_config *cfg);
  *   embed:  device, f16 bits [vocab][hidden_size], row-major (E itself).
  *   hidden: device, f32 [n_rows][hidden_size], the final RMSNorm output.
  *   logits: device, f32 [n_rows][vocab], or NULL to skip writing logits.
- *   ids:    device, int32 [n_rows]: the lowest index of each row's maximum.
+ *   ids:    device, int32 [n_rows]: the lowest index of each row's maximum
+ *           (a NaN logit counts above every number, so a row of NaN logits
+ *           gives its first index: every id is inside [0, vocab)).
  * Asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
  * Limits: 1 <= n_rows <= 8; hidden_size a multiple of 8, at most 1024;
- * vocab >= 1.  Outside them: QWEN2_E_ARG, nothing launched.
+ * vocab >= 1; embed 16-byte aligned (rows are read with 16-byte vector
+ * loads; sub-allocated pointers must keep that alignment).  Outside them:
+ * QWEN2_E_ARG, nothing launched.
  * Scratch: a fixed static device array of the library (about 32 KB per
  * device).  The first call on a device looks up its address with that
- * device current; make that first call before any other use that must not
- * see a runtime call other than a kernel launch and a memset.  Each call
- * zeroes the scratch's arrival counter on `stream` before its kernel.  Two
- * calls in flight at once on one device (other streams or threads) share
- * the scratch and race: order them.  The logits are bitwise those of
- * qwen2_decode_step for the same rows.  Errors: QWEN2_E_ARG, QWEN2_E_CUDA;
- * qwen2_last_error(NULL) describes the failure. */
+ * device current, and so does the first call under any other context made
+ * current on that device later; make that first call before any other use
+ * that must not see a runtime call other than a kernel launch and a memset.
+ * Each call zeroes the scratch's arrival counter on `stream` before its
+ * kernel.  Two calls in flight at once on one device (other streams or
+ * threads) share the scratch and race: order them.  The logits are bitwise
+ * those of qwen2_decode_step for the same rows.  Errors: QWEN2_E_ARG,
+ * QWEN2_E_CUDA; qwen2_last_error(NULL) describes the failure. */
 int qwen2_lm_head_argmax_noalloc(const uint16_t *embed, const float *hidden, int32_t n_rows,
                                  int32_t hidden_size, int32_t vocab, float *logits, int32_t *ids,
                                  void *stream);

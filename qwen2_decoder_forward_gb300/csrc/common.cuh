@@ -102,9 +102,13 @@ __device__ __forceinline__ float rms_scale(float sumsq, int n, float eps) {
     return 1.0f / sqrtf(sumsq / (float)n + eps);
 }
 
-// Greedy argmax merge: larger value wins, equal values keep the lower index.
+// Greedy argmax merge.  Keeps the lowest index of the maximum.  NaN orders above every number
+// (the first NaN of a row wins, as numpy's argmax has it), so a row whose
+// logits are all NaN still yields an index inside the vocabulary.
 __device__ __forceinline__ void argmax_merge(float& v, int& i, float ov, int oi) {
-    if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
+    const bool vn = v != v, on = ov != ov;
+    const bool take = on ? (!vn || oi < i) : (!vn && (ov > v || (ov == v && oi < i)));
+    if (take) { v = ov; i = oi; }
 }
 
 // SiLU(z) = z / (1 + e^-z) (hidden_act "silu").

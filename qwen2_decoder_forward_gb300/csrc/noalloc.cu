@@ -14,6 +14,10 @@
 // that are already normalised: logits[r][v] = E[v] . hidden[r], then the
 // lowest index of each row's maximum.  It uses the same row dot product as
 // the decode path's LM head, so its logits match those bit for bit.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+
 #include <mutex>
 #include <string>
 
@@ -39,8 +43,32 @@ struct NaScratch {
 
 static __device__ __align__(256) NaScratch g_na_scratch;
 
+// The scratch's device address per device, with the context it was looked
+// up in: a context created later on the same device (a driver-API context
+// made current by the caller, or the primary context re-created after a
+// reset) holds its own instance of the module, so the address is looked up
+// again whenever the current context is not the recorded one.
+struct NaAddr {
+    CUcontext ctx;
+    NaScratch* addr;
+};
 std::mutex g_na_mutex;
-NaScratch* g_na_addr[kNaMaxDevices] = {};
+NaAddr g_na_addr[kNaMaxDevices] = {};
+
+// The driver's cuCtxGetCurrent, looked up once through the runtime (the
+// library does not link libcuda).
+PFN_cuCtxGetCurrent_v4000 ctx_get_current() {
+    static PFN_cuCtxGetCurrent_v4000 fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        cudaGetLastError();
+        return reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    }();
+    return fn;
+}
 
 template <int NB>
 __global__ void __launch_bounds__(kNaThreads) k_lm_head_noalloc(const __half* __restrict__ E,
@@ -148,29 +176,43 @@ extern "C" int qwen2_lm_head_argmax_noalloc(const uint16_t* embed, const float* 
                          "and vocab >= 1");
         return QWEN2_E_ARG;
     }
+    if (reinterpret_cast<uintptr_t>(embed) & 15) {
+        // Rows are streamed with 16-byte vector loads.
+        set_thread_error("qwen2_lm_head_argmax_noalloc: embed must be 16-byte aligned");
+        return QWEN2_E_ARG;
+    }
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNaMaxDevices) {
         cudaGetLastError();
         set_thread_error("qwen2_lm_head_argmax_noalloc: no usable current CUDA device");
         return QWEN2_E_CUDA;
     }
+    CUcontext ctx = nullptr;
+    PFN_cuCtxGetCurrent_v4000 get_ctx = ctx_get_current();
+    if (!get_ctx || get_ctx(&ctx) != CUDA_SUCCESS) {
+        set_thread_error("qwen2_lm_head_argmax_noalloc: cannot query the current CUDA context");
+        return QWEN2_E_CUDA;
+    }
     NaScratch* sc;
     {
-        // First call on this device: look up the device address of the
-        // static scratch with that device current.
+        // First call on this device (and context): look up the device
+        // address of the static scratch with that device current.
         std::lock_guard<std::mutex> lock(g_na_mutex);
-        if (!g_na_addr[dev]) {
+        if (!ctx || !g_na_addr[dev].addr || g_na_addr[dev].ctx != ctx) {
             void* p = nullptr;
             const cudaError_t e = cudaGetSymbolAddress(&p, g_na_scratch);
-            if (e != cudaSuccess || !p) {
+            // With no context current before, the runtime has now made the
+            // device's primary context current.
+            if (e == cudaSuccess && !ctx && get_ctx(&ctx) != CUDA_SUCCESS) ctx = nullptr;
+            if (e != cudaSuccess || !p || !ctx) {
                 cudaGetLastError();
                 set_thread_error(std::string("qwen2_lm_head_argmax_noalloc: cudaGetSymbolAddress failed: ") +
                                  cudaGetErrorString(e));
                 return QWEN2_E_CUDA;
             }
-            g_na_addr[dev] = static_cast<NaScratch*>(p);
+            g_na_addr[dev] = NaAddr{ctx, static_cast<NaScratch*>(p)};
         }
-        sc = g_na_addr[dev];
+        sc = g_na_addr[dev].addr;
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // The arrival counter must start at zero (a launch that stopped part-way

@@ -121,6 +121,10 @@ def test_no_alloc_head_rejects_bad_sizes_before_any_cuda_call(L):
     assert L.qwen2_lm_head_argmax_noalloc(fake, fake, 1, 1032, 151936, None, fake, None) == 1
     assert b"hidden_size" in L.qwen2_last_error(None)
     assert L.qwen2_lm_head_argmax_noalloc(fake, fake, 1, 896, 151936, None, None, None) == 1
+    # A 2-byte-aligned embedding (a pool sub-allocation) is refused on the
+    # host: the rows are read with 16-byte vector loads.
+    assert L.qwen2_lm_head_argmax_noalloc(ctypes.c_void_p(16 + 2), fake, 1, 896, 151936, None, fake, None) == 1
+    assert b"16-byte" in L.qwen2_last_error(None)
 
 
 def test_untied_lm_head_is_rejected_before_any_device_work():
