@@ -1,12 +1,15 @@
 """Benchmark of the Qwen2 decoder forward on GB300 (one JSON line on stdout).
 
-Default workload: Qwen2.5-0.5B-shaped model (24 layers, hidden 896, 14/2
+Headline workload: Qwen2.5-0.5B-shaped model (24 layers, hidden 896, 14/2
 heads, vocab 151936, tied head), seeded synthetic f16 weights, batch 1: a
 128-token prompt is prefilled once (untimed), then each timed step is one
 greedy generation of 256 tokens at positions 128..383 through
-qwen2_decode_steps (one CUDA-graph replay per token, ids fed back on the
-device).  The weights (988 MB) exceed the 129 MB L2, so no flush is needed
-between steps.
+qwen2_decode_steps (one persistent launch per token, ids fed back on the
+device).  The default run also measures the other workloads the metric
+names and reports them under "workloads": long-context batch-1 decode
+(positions 4000..4095), the 8 x 512 tensor-core prefill, and batched decode
+of 32 ragged sequences on Q8_0 weights.  Every workload's weights (988 MB
+f16, 525 MB Q8_0) exceed the 129 MB L2, so no flush is needed between steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
                     [--workload NAME]
@@ -17,6 +20,7 @@ has no exchange step); value = tokens of all ranks / max rank time.
 from __future__ import annotations
 
 import argparse
+import contextlib
 import json
 import os
 import subprocess
@@ -198,25 +202,55 @@ def prefill_flops(shape, lens, n_keep: int) -> float:
                  + (L - 1) * att_all + att_kept + 2 * len(lens) * n_keep * V * H)
 
 
-def oracle_prefill_rate(shape, weights, prompt, budget_s: float = 20.0):
-    """The oracle's prefill tokens/s on the host cores (one prompt)."""
-    import oracle
-    orc = oracle.build_oracle(shape, weights, 4096)
-    t0 = time.perf_counter()
-    done = 0
-    while done == 0 or time.perf_counter() - t0 < budget_s / 4:
-        orc.prefill(orc.new_cache(), prompt)
-        done += len(prompt)
-        if time.perf_counter() - t0 > budget_s:
-            break
-    dt = time.perf_counter() - t0
-    return done / dt, done, dt
+@contextlib.contextmanager
+def blas_threads(n: int):
+    """Limit the BLAS pool the oracle's numpy calls use to ``n`` threads
+    inside the block (threadpoolctl when present, else numpy's bundled
+    OpenBLAS through its own thread-count entry points)."""
+    try:
+        from threadpoolctl import threadpool_limits
+    except ImportError:
+        threadpool_limits = None
+    if threadpool_limits is not None:
+        with threadpool_limits(limits=n, user_api="blas"):
+            yield
+        return
+    import ctypes
+    lib, getter, setter = None, None, None
+    try:
+        with open("/proc/self/maps") as f:
+            paths = sorted({ln.split()[-1] for ln in f if "openblas" in ln.lower() and ln.split()[-1].startswith("/")})
+        for path in paths:
+            cand = ctypes.CDLL(path)
+            for suffix in ("64_", ""):
+                for pre in ("scipy_openblas_", "openblas_"):
+                    if hasattr(cand, f"{pre}set_num_threads{suffix}"):
+                        lib = cand
+                        setter = getattr(cand, f"{pre}set_num_threads{suffix}")
+                        getter = getattr(cand, f"{pre}get_num_threads{suffix}")
+                        break
+                if lib:
+                    break
+            if lib:
+                break
+    except Exception:
+        lib = None
+    if lib is None:
+        yield
+        return
+    old = int(getter())
+    setter(int(n))
+    try:
+        yield
+    finally:
+        setter(old)
 
 
 def cpu_threads() -> int:
+    """Threads of the BLAS pool the oracle's products run on."""
     try:
         from threadpoolctl import threadpool_info
-        n = [i.get("num_threads") for i in threadpool_info() if i.get("internal_api") == "openblas"]
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
         if n and n[0]:
             return int(n[0])
     except Exception:
@@ -224,57 +258,146 @@ def cpu_threads() -> int:
     return len(os.sched_getaffinity(0))
 
 
-def oracle_decode_rate(shape, weights, prompt, n_tokens: int, budget_s: float = 15.0, weight_format: str = "f16"):
-    """The oracle's greedy decode tokens/s on the host cores: prefill the
-    prompt (untimed), then time decode steps until n_tokens or the budget."""
-    import oracle
-    orc = oracle.build_oracle(shape, weights, 4096, weight_format=weight_format)
-    cache = orc.new_cache()
-    pre = orc.prefill(cache, prompt)
-    tok = int(pre["ids"][0])
-    t0 = time.perf_counter()
-    done = 0
-    while done < n_tokens and (done == 0 or time.perf_counter() - t0 < budget_s):
-        r = orc.forward(cache, [tok], [len(prompt) + done])
-        tok = int(r["ids"][0])
-        done += 1
-    dt = time.perf_counter() - t0
-    return done / dt, done, dt
+class OracleTimer:
+    """Bounded samples of a workload run by the oracle on the host cores.
+
+    Decode samples are single-token forwards at the workload's positions
+    over a key/value cache filled with seeded random values up to that
+    position: the oracle's work per token (every weight once, attention
+    over positions 0..p) is the same as after a real prefill, without the
+    prefill itself (a 4000-token float64 prefill alone takes minutes)."""
+
+    def __init__(self, shape, weights):
+        self.shape, self.weights, self._orc = shape, weights, {}
+
+    def oracle(self, weight_format: str):
+        if weight_format not in self._orc:
+            import oracle
+            self._orc[weight_format] = oracle.build_oracle(self.shape, self.weights, 4096,
+                                                           weight_format=weight_format)
+        return self._orc[weight_format]
+
+    def decode(self, wl, budget_s: float, max_tokens: int):
+        """(tokens/s, tokens, seconds, what) of greedy decode tokens at the
+        workload's positions, round-robin over its sequences."""
+        orc = self.oracle(wl.weight_format)
+        lens = [int(n) for n in wl.prompt_lengths()]
+        rng = np.random.Generator(np.random.PCG64(77))
+        cache = orc.new_cache()
+        filled = 0
+        tok = 17
+        t_total, done = 0.0, 0
+        while done < max_tokens and (done == 0 or t_total < budget_s):
+            s = done % len(lens)
+            pos = lens[s] + (done // len(lens)) % max(1, wl.decode_steps)
+            if pos > filled:
+                cache.K[:, filled:pos] = 0.1 * rng.standard_normal(cache.K[:, filled:pos].shape)
+                cache.V[:, filled:pos] = 0.1 * rng.standard_normal(cache.V[:, filled:pos].shape)
+                filled = pos
+            t0 = time.perf_counter()
+            r = orc.forward(cache, [tok], [pos])
+            t_total += time.perf_counter() - t0
+            tok = int(r["ids"][0])
+            done += 1
+        what = (f"{done} greedy decode tokens at the workload's positions "
+                f"({'sequences round-robin, ' if len(lens) > 1 else ''}first at {lens[0]}; "
+                f"cache filled with seeded random keys/values up to each position), "
+                f"{wl.weight_format} weights")
+        return done / t_total, done, t_total, what
+
+    def prefill(self, wl, budget_s: float, n_rows: int):
+        """(tokens/s, tokens, seconds, what) of prefills of the first
+        ``n_rows`` tokens of the workload's first sequence."""
+        orc = self.oracle(wl.weight_format)
+        prompt = wl.prompts(self.shape.vocab)[0][:n_rows]
+        t_total, done = 0.0, 0
+        while done == 0 or t_total < budget_s / 3:
+            t0 = time.perf_counter()
+            orc.prefill(orc.new_cache(), prompt)
+            t_total += time.perf_counter() - t0
+            done += len(prompt)
+            if t_total > budget_s:
+                break
+        what = f"{done // len(prompt)} causal prefill(s) of one {len(prompt)}-token sequence (tail cut)"
+        return done / t_total, done, t_total, what
+
+    def baseline(self, wl, budget_s: float = 8.0):
+        """The cpu_baseline record: the oracle on every core of the BLAS pool,
+        and on one thread."""
+        cores = cpu_threads()
+        if wl.decode_steps == 0:
+            rate, _, _, what = self.prefill(wl, budget_s, wl.prompt_len)
+            with blas_threads(1):
+                r1, _, _, what1 = self.prefill(wl, budget_s, min(wl.prompt_len, 64))
+        else:
+            rate, _, _, what = self.decode(wl, budget_s, 256)
+            with blas_threads(1):
+                r1, _, _, what1 = self.decode(wl, budget_s, 64)
+        return {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": what,
+                "single_thread": {"value": r1, "unit": "tokens/s", "cores": 1, "sample": what1}}
 
 
-def bench_prefill(args, wl, shape, weights, rank, world, local):
+def workload_config(wl, shape, world: int) -> dict:
+    lens = [int(n) for n in wl.prompt_lengths()]
+    if wl.decode_steps == 0:
+        return {"workload": f"{wl.name}: {shape.name} shape, {wl.n_seq} sequences x {wl.prompt_len} tokens, "
+                            f"causal prefill with the tail cut (last row of each sequence to the LM head), "
+                            f"{'tensor-core f16 operands' if wl.prefill == 'tensor' else 'f32 CUDA cores'}, "
+                            f"f32 accumulation and KV, n_ctx {wl.n_ctx}",
+                "global_batch": wl.n_seq * world, "seq_len": wl.prompt_len, "parallelism": f"replicas x{world}",
+                "l2": "weights (988 MB) exceed L2 (129 MB): no flush between steps"}
+    q8 = wl.weight_format == "q8_0"
+    ragged = len(set(lens)) > 1
+    return {"workload": f"{wl.name}: {shape.name} shape, batch {wl.n_seq}, "
+                        + (f"ragged prompts U{{{wl.ragged_lo}..{wl.ragged_hi}}} (mean {np.mean(lens):.0f})"
+                           if ragged else f"prompt {lens[0]}")
+                        + f", {wl.decode_steps} greedy decode steps per timed step, "
+                        + ("Q8_0" if q8 else "f16") + f" weights, f32 KV, n_ctx {wl.n_ctx}",
+            "global_batch": wl.n_seq * world, "seq_len": int(max(lens)) + wl.decode_steps,
+            "parallelism": f"replicas x{world}",
+            "l2": "weights (" + ("525" if q8 else "988") + " MB) and KV exceed L2 (129 MB): no flush between steps"}
+
+
+def reference_line(args, wl, shape, weights, world: int) -> dict:
+    """The reference arm: the oracle as it stands on the host cores, K timed
+    steps after W warm-up steps, each step a bounded sample of the workload
+    (at most 32 decode tokens, or one prefill of at most 128 tokens)."""
+    timer = OracleTimer(shape, weights)
+    if wl.decode_steps == 0:
+        n_rows = min(wl.prompt_len, 128)
+        sample = lambda: timer.prefill(wl, 0.0, n_rows)  # noqa: E731  (one prefill per step)
+    else:
+        n_tok = min(wl.decode_steps * wl.n_seq, 32)
+        sample = lambda: timer.decode(wl, 1e9, n_tok)  # noqa: E731
+    for _ in range(max(0, args.warmup)):
+        sample()
+    secs, toks, what = 0.0, 0, ""
+    for _ in range(max(1, args.steps)):
+        _, done, dt, what = sample()
+        secs += dt
+        toks += done
+    rate = toks / secs
+    return {"impl": "reference", "metric": METRIC, "value": rate, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            # the measured time of one reference step (one bounded sample)
+            "ms_per_step": secs / max(1, args.steps) * 1e3, "tokens_per_step": toks // max(1, args.steps),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded random weights)", "config": workload_config(wl, shape, world),
+            "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+                             "sample": f"each step: {what}"},
+            "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def run_prefill(args, wl, shape, weights, reps, world):
     """Prefill workloads: a step is one qwen2_prefill of all the workload's
     sequences through the tail cut (one kept row per sequence, greedy ids
     out).  Tokens are host arrays (the C ABI copies them, 4 bytes a token)."""
+    import torch
+    import qwen2_decoder_forward_gb300 as q2
     prompts = wl.prompts(shape.vocab)
     lens = [len(p) for p in prompts]
     n_tok = sum(lens)
-    config = {"workload": f"{wl.name}: {shape.name} shape, {wl.n_seq} sequences x {wl.prompt_len} tokens, "
-                          f"causal prefill with the tail cut (last row of each sequence to the LM head), "
-                          f"{'tensor-core f16 operands' if wl.prefill == 'tensor' else 'f32 CUDA cores'}, "
-                          f"f32 accumulation and KV, n_ctx {wl.n_ctx}",
-              "global_batch": wl.n_seq * world, "seq_len": wl.prompt_len, "parallelism": f"replicas x{world}",
-              "l2": "weights (988 MB) exceed L2 (129 MB): no flush between steps"}
     flops = prefill_flops(shape, lens, 1)
-    if args.impl == "reference":
-        if rank != 0:
-            return
-        rate, done, dt = oracle_prefill_rate(shape, weights, prompts[0])
-        line = {"impl": "reference", "metric": METRIC, "value": rate, "unit": "tokens/s", "n_gpus": args.gpus,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": n_tok / rate * 1e3,
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic (seeded random weights)", "config": config,
-                "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
-                                 "sample": f"{done // len(prompts[0])} prefill(s) of one {len(prompts[0])}-token "
-                                           f"sequence"},
-                "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-        print(json.dumps(line), flush=True)
-        return
-
-    import torch
-    import qwen2_decoder_forward_gb300 as q2
-    torch.cuda.set_device(local)
-    reps = Replicas(world, "nccl", torch.device("cuda", local))
     mode = q2.PREFILL_TENSOR if wl.prefill == "tensor" else q2.PREFILL_F32
     model = q2.Qwen2Model(shape, weights, n_ctx=wl.n_ctx, max_seqs=wl.n_seq, max_tokens=n_tok,
                           prefill_mode=mode, flags=args.flags)
@@ -291,7 +414,7 @@ def bench_prefill(args, wl, shape, weights, rank, world, local):
 
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     reps.barrier()
-    with ClockSampler(local) as clocks:
+    with ClockSampler(torch.cuda.current_device()) as clocks:
         start.record(stream)
         for _ in range(args.steps):
             step(ids)
@@ -322,10 +445,12 @@ def bench_prefill(args, wl, shape, weights, rank, world, local):
     launches = 1 + (shape.n_layer - 1) * 7 + 2 + 4 + 1 + 3 + 1
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f16 tensor-core operands (activations as f16 hi/lo pairs), f32 "
-                                      "accumulation, f32 residual/softmax/KV" if tensor else "f32",
+            "vs_baseline": None,
+            "dtype": "f16 tensor-core operands (activations of Q/K/V, o_proj and gate/up as f16 hi/lo pairs; "
+                     "attention q, k, p in f16 and v as an f16 hi/lo pair), f32 accumulation, f32 "
+                     "residual/softmax/KV" if tensor else "f32",
             "data": "synthetic (seeded random weights of the Qwen2.5-0.5B shape, uniform-random tokens)",
-            "config": config, "clocks": clocks.summary(),
+            "config": workload_config(wl, shape, world), "clocks": clocks.summary(),
             "e2e": {"value": args.steps * n_tok * world / e2e_s, "unit": "tokens/s",
                     # token, position and slot per row, kept-row indices, and
                     # the (first row, row count) plan of the 16-row blocks
@@ -333,60 +458,21 @@ def bench_prefill(args, wl, shape, weights, rank, world, local):
                                               + 8 * (sum((n + 15) // 16 for n in lens) + wl.n_seq)),
                     "d2h_bytes_per_step": int(host_ids.nbytes)},
             "roofline": roofline, "gpu_launches": launches * args.steps}
-    if rank == 0 and not args.skip_cpu_baseline:
-        rate, done, dt = oracle_prefill_rate(shape, weights, prompts[0], budget_s=15.0)
-        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
-                                "sample": f"{done // len(prompts[0])} prefill(s) of one {len(prompts[0])}-token "
-                                          f"sequence"}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
     model.close()
-    reps.close()
+    return line
 
 
-def bench_decode(args, wl, shape, weights, rank, world, local):
+def run_decode(args, wl, shape, weights, reps, world):
     """Decode workloads: the prompts are prefilled once (untimed); a step is
     one qwen2_decode_steps call of decode_steps greedy tokens for every
     sequence (one CUDA-graph replay, or one persistent launch, per token;
     ids fed back on the device)."""
+    import torch
+    import qwen2_decoder_forward_gb300 as q2
     prompts = wl.prompts(shape.vocab)
     lens = [len(p) for p in prompts]
     q8 = wl.weight_format == "q8_0"
     B = wl.n_seq
-    ragged = len(set(lens)) > 1
-    config = {"workload": f"{wl.name}: {shape.name} shape, batch {B}, "
-                          + (f"ragged prompts U{{{wl.ragged_lo}..{wl.ragged_hi}}} (mean {np.mean(lens):.0f})"
-                             if ragged else f"prompt {lens[0]}")
-                          + f", {wl.decode_steps} greedy decode steps per timed step, "
-                          + ("Q8_0" if q8 else "f16") + f" weights, f32 KV, n_ctx {wl.n_ctx}",
-              "global_batch": B * world, "seq_len": int(max(lens)) + wl.decode_steps,
-              "parallelism": f"replicas x{world}",
-              "l2": "weights (" + ("525" if q8 else "988") + " MB) and KV exceed L2 (129 MB): no flush between steps"}
-    if args.impl == "reference":
-        if rank != 0:
-            return
-        s = int(np.argmin(lens))
-        rate, done, dt = oracle_decode_rate(shape, weights, prompts[s], 4 * max(1, args.steps), budget_s=20.0,
-                                            weight_format=wl.weight_format)
-        line = {"impl": "reference", "metric": METRIC, "value": rate, "unit": "tokens/s",
-                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-                # one step of the workload (all its sequences' decode tokens)
-                # at the oracle's rate, as the other arm's step is timed
-                "ms_per_step": wl.decode_steps * B / rate * 1e3, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded random weights)",
-                "config": config,
-                "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
-                                 "sample": f"{done} greedy decode tokens of one sequence after a "
-                                           f"{lens[s]}-token prefill"},
-                "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-        print(json.dumps(line), flush=True)
-        return
-
-    import torch
-    import qwen2_decoder_forward_gb300 as q2
-    torch.cuda.set_device(local)
-    reps = Replicas(world, "nccl", torch.device("cuda", local))
-
     n_steps = args.tokens_per_step or wl.decode_steps
     model = q2.Qwen2Model(shape, weights, n_ctx=wl.n_ctx, max_seqs=B, max_tokens=sum(lens),
                           weight_format=q2.WEIGHTS_Q8_0 if q8 else q2.WEIGHTS_F16, flags=args.flags)
@@ -405,7 +491,7 @@ def bench_decode(args, wl, shape, weights, rank, world, local):
 
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     reps.barrier()
-    with ClockSampler(local) as clocks:
+    with ClockSampler(torch.cuda.current_device()) as clocks:
         start.record(stream)
         for _ in range(args.steps):
             step(out)
@@ -447,26 +533,25 @@ def bench_decode(args, wl, shape, weights, rank, world, local):
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                 "traffic": kernel_traffic("k_decode_persistent", wl.name) if persistent else None,
                 "kernel": kname, "peak_source": src, "bytes_per_launch": step_bytes}
+    dtype = ("f32 activations, Q8_0 weights (exact f32 dequantisation). Products: activations as f16 hi/lo "
+             "MMA operand pairs, the LM head's as f16 only; attention: q, k and p rounded to TF32, v as a "
+             "TF32 hi/lo pair; f32 accumulation, softmax and KV" if q8 else
+             "f32 activations and accumulation, f16 weights, f32 KV")
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None,
-            "dtype": "f32 activations, " + ("Q8_0 weights (exact f32 dequantisation; f16 hi/lo MMA operands)"
-                                            if q8 else "f16 weights"),
+            "vs_baseline": None, "dtype": dtype,
             "data": "synthetic (seeded random weights of the Qwen2.5-0.5B shape, uniform-random tokens)",
-            "config": config, "clocks": clocks.summary(), "e2e": e2e, "roofline": roofline,
-            "gpu_launches": launches * n_steps * args.steps,
+            "config": workload_config(wl, shape, world), "clocks": clocks.summary(), "e2e": e2e,
+            "roofline": roofline, "gpu_launches": launches * n_steps * args.steps,
             "decode_kernel": "persistent" if persistent else "per-step"}
-    if rank == 0 and not args.skip_cpu_baseline:
-        s = int(np.argmin(lens))
-        rate, done, dt = oracle_decode_rate(shape, weights, prompts[s], 64, budget_s=15.0,
-                                            weight_format=wl.weight_format)
-        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
-                                "sample": f"{done} greedy decode tokens of one sequence after a "
-                                          f"{lens[s]}-token prefill"}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
     model.close()
-    reps.close()
+    return line
+
+
+HEADLINE = "0.5b-decode-b1"
+# The other workloads the metric names, measured by the default run and
+# reported under "workloads" of the headline's line.
+OTHERS = ("0.5b-decode-b1-long", "0.5b-prefill-8x512", "0.5b-decode-b32-q8")
 
 
 def main():
@@ -475,23 +560,50 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="0.5b-decode-b1", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default=None, choices=sorted(synth.WORKLOADS),
+                    help="one workload alone (default: the batch-1 decode line, with the other 0.5B "
+                         "workloads under 'workloads')")
     ap.add_argument("--tokens-per-step", type=int, default=0,
                     help="override the decode tokens of one timed step (profiling runs only)")
     ap.add_argument("--skip-cpu-baseline", action="store_true", help="profiling runs: no oracle timing")
     ap.add_argument("--flags", type=int, default=0, help="QWEN2_FLAG_* bits for the context")
     args = ap.parse_args()
-    wl = synth.WORKLOADS[args.workload]
-    shape = synth.SHAPES[wl.shape]
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    if args.impl == "reference" and rank != 0:
-        return  # the oracle arm runs on rank 0 alone; other ranks exit 0 without work
+    name = args.workload or HEADLINE
+    wl = synth.WORKLOADS[name]
+    shape = synth.SHAPES[wl.shape]
+    if args.impl == "reference":
+        if rank != 0:
+            return  # the oracle arm runs on rank 0 alone; other ranks exit 0 without work
+        weights = synth.make_weights(shape, wl.weight_seed)
+        print(json.dumps(reference_line(args, wl, shape, weights, args.gpus)), flush=True)
+        return
+
+    import torch
+    torch.cuda.set_device(local)
+    reps = Replicas(world, "nccl", torch.device("cuda", local))
     weights = synth.make_weights(shape, wl.weight_seed)
-    if wl.decode_steps == 0:
-        return bench_prefill(args, wl, shape, weights, rank, world, local)
-    return bench_decode(args, wl, shape, weights, rank, world, local)
+    run = lambda w: (run_prefill if w.decode_steps == 0 else run_decode)(  # noqa: E731
+        args, w, synth.SHAPES[w.shape], synth.make_weights(synth.SHAPES[w.shape], w.weight_seed), reps, world)
+    line = run(wl)
+    extra = {}
+    if args.workload is None:
+        for other in OTHERS:
+            extra[other] = run(synth.WORKLOADS[other])
+    if rank == 0 and not args.skip_cpu_baseline:
+        timer = OracleTimer(shape, weights)
+        line["cpu_baseline"] = timer.baseline(wl)
+        for other, rec in extra.items():
+            rec["cpu_baseline"] = timer.baseline(synth.WORKLOADS[other])
+    if extra:
+        keep = ("value", "unit", "ms_per_step", "steps", "dtype", "config", "roofline", "e2e", "clocks",
+                "gpu_launches", "cpu_baseline", "decode_kernel")
+        line["workloads"] = {k: {f: v[f] for f in keep if f in v} for k, v in extra.items()}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    reps.close()
 
 
 if __name__ == "__main__":

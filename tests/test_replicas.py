@@ -87,5 +87,7 @@ def test_reference_arm_under_torchrun_world2():
     # The line names the same workload as our arm's line at N = 2.
     assert rec["config"]["parallelism"] == "replicas x2"
     assert rec["config"]["global_batch"] == 2
-    # ms_per_step is one workload step (16 decode tokens) at the oracle's rate.
+    # A reference step is a bounded sample of the workload: here its whole
+    # 16 decode tokens; ms_per_step is the measured time of one such step.
+    assert rec["tokens_per_step"] == 16
     assert rec["ms_per_step"] == pytest.approx(16 / rec["value"] * 1e3)
