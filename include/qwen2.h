@@ -47,7 +47,7 @@ extern "C" {
 #define QWEN2_E_POS              2  /* a position outside [0, n_ctx): a hard error, never truncation
                                        (minfer page section 6: positions[i] < n_ctx is enforced with a
                                        hard Err in the KV-store arm; section 7 item 5) */
-#define QWEN2_E_UNSUPPORTED      3  /* a config this build does not implement (e.g. head_dim != 64) */
+#define QWEN2_E_UNSUPPORTED      3  /* a config this build does not implement (e.g. head_dim 96) */
 #define QWEN2_E_OOM              4  /* device allocation failed */
 #define QWEN2_E_CUDA             5  /* a CUDA runtime call failed */
 #define QWEN2_E_DEVICE_GUARD     6  /* a kernel's own guard tripped (found at qwen2_synchronize) */
@@ -84,7 +84,10 @@ typedef struct qwen2_config {
     int32_t hidden;         /* hidden_size H (896); must be n_head * head_dim and a multiple of 128 */
     int32_t n_head;         /* num_attention_heads (14) */
     int32_t n_kv_head;      /* num_key_value_heads (2); must divide n_head, n_head/n_kv_head <= 8 */
-    int32_t head_dim;       /* H / n_head (64); this build supports 64 */
+    int32_t head_dim;       /* H / n_head: 64 (0.5B) or 128 (every larger size, nnterp
+                             * encyclopedia qwen2, "Grouped-query attention"); 128 runs the
+                             * per-step decode kernels and the f32 prefill (the persistent
+                             * batch-1 kernel and the tensor-core prefill are built for 64) */
     int32_t intermediate;   /* intermediate_size I (4864); a multiple of 128 */
     int32_t vocab;          /* vocab_size V (151936) */
     float   rms_eps;        /* rms_norm_eps (1e-6) */
@@ -116,20 +119,31 @@ typedef struct qwen2_layer_weights {
 } qwen2_layer_weights;
 
 typedef struct qwen2_weights {
-    const uint16_t *embed;             /* [V][H] embed_tokens.weight; also the LM head (tied) */
+    const uint16_t *embed;             /* [V][H] embed_tokens.weight; also the LM head when tied */
+    const uint16_t *lm_head;           /* [V][H] lm_head.weight, or NULL for a tied head (the
+                                        * embedding is the readout: 0.5B to 3B).  From 7B up the
+                                        * embedding and unembedding are separate matrices (nnterp
+                                        * encyclopedia qwen2, "The readout is the plain
+                                        * projection"); the logits are then lm_head . final_norm(x). */
     const float *final_norm;           /* [H] model.norm.weight */
     const qwen2_layer_weights *layers; /* [n_layer] */
 } qwen2_weights;
 
 typedef struct qwen2_ctx qwen2_ctx;
 
-/* Create a context on the current CUDA device: validate `cfg`, pack and
+/* Create a context on the current CUDA device from a config (the minfer
+ * page "Qwen2 / Qwen2.5 Architecture Support", section 2: the HParams
+ * fields -- layers, hidden, heads, KV heads, head_dim, intermediate,
+ * vocabulary, rms_eps, rope_theta -- and the LayerWeights tensors, with the
+ * tied embedding as the output projection) and host weight pointers:
+ * validate `cfg`, pack and
  * upload the weights (the library keeps its own device copies; the host
  * arrays may be freed after the call), allocate the zeroed KV cache of
  * max_seqs sequences, the workspace and the RoPE table.  Synchronous.
  * Errors: QWEN2_E_ARG (null pointers, non-positive sizes), QWEN2_E_UNSUPPORTED
- * (head_dim != 64, H != n_head*head_dim, H or I not a multiple of 128,
- * n_head % n_kv_head != 0, group > 8), QWEN2_E_OOM, QWEN2_E_CUDA.
+ * (head_dim not 64 or 128, head_dim 128 with QWEN2_PREFILL_TENSOR,
+ * H != n_head*head_dim, H or I not a multiple of 128, n_head % n_kv_head
+ * != 0, group > 8), QWEN2_E_OOM, QWEN2_E_CUDA.
  * On success *out receives the context; on failure *out is set to NULL and
  * qwen2_last_error(NULL) describes the failure. */
 int qwen2_create(const qwen2_config *cfg, const qwen2_weights *weights, qwen2_ctx **out);
@@ -143,7 +157,10 @@ void qwen2_destroy(qwen2_ctx *ctx);
  * until the next call on the same context (or thread). */
 const char *qwen2_last_error(const qwen2_ctx *ctx);
 
-/* The KV cache as caller-visible device memory: *base receives a device
+/* The KV cache (minfer page, section 6: an f32 K and V cache per layer,
+ * sized by n_ctx when the context is created -- 24 KB per position on
+ * Qwen2.5-0.5B -- whose slot is the token's position) as caller-visible
+ * device memory: *base receives a device
  * pointer to f32 [max_seqs][n_layer][2][n_kv_head][n_ctx][head_dim]
  * (index 0 of the third axis holds rotated keys, 1 values; slot = position),
  * contiguous row-major; dims[0..5] receive those six sizes.  The memory is
@@ -171,7 +188,12 @@ int qwen2_prefill(qwen2_ctx *ctx, int32_t n_seq, const int32_t *seq_ids,
                   const int32_t *positions, int32_t n_out,
                   float *logits, int32_t *ids, void *stream);
 
-/* One decode step: one row for each of n_seq sequences.
+/* One decode step: one row for each of n_seq sequences, the forward of
+ * minfer page section 1 at one new position per sequence.  Positions are
+ * data (minfer page, section 6): the row's key and value go to slot
+ * `position` of its sequence's cache and it attends to slots 0..position;
+ * a position outside [0, n_ctx) is QWEN2_E_POS with nothing enqueued (a
+ * hard error, never a truncation).
  *   seq_ids, tokens, positions  host int32 [n_seq]
  *   logits  nullable; f32 [n_seq][V]
  *   ids     nullable; int32 [n_seq] greedy ids */

@@ -85,7 +85,7 @@ class _LayerWeights(ctypes.Structure):
 
 
 class _Weights(ctypes.Structure):
-    _fields_ = [("embed", _P), ("final_norm", _P), ("layers", ctypes.POINTER(_LayerWeights))]
+    _fields_ = [("embed", _P), ("lm_head", _P), ("final_norm", _P), ("layers", ctypes.POINTER(_LayerWeights))]
 
 
 _lib = None
@@ -215,11 +215,10 @@ class Qwen2Model:
 
     def __init__(self, shape, weights: dict, n_ctx: int, max_seqs: int = 1, max_tokens: int = 128,
                  weight_format: int = WEIGHTS_F16, prefill_mode: int = PREFILL_F32, flags: int = 0):
-        # The library's LM head is the embedding (tied, as on 0.5B to 3B); a
-        # separate head matrix would otherwise be dropped without a word.
-        if weights.get("lm_head") is not None or not getattr(shape, "tie_embeddings", True):
-            raise Qwen2Error(QWEN2_E_UNSUPPORTED, "an untied LM head (a separate lm_head matrix) is not "
-                                                  "supported by this build")
+        # A separate LM head (untied, 7B and up) is passed as its own
+        # matrix; a shape that declares an untied head must bring one.
+        if weights.get("lm_head") is None and not getattr(shape, "tie_embeddings", True):
+            raise Qwen2Error(QWEN2_E_ARG, "the shape declares an untied LM head but the weights have no lm_head")
         L = lib()
         self.shape = shape
         self.n_ctx, self.max_seqs, self.max_tokens = n_ctx, max_seqs, max_tokens
@@ -240,7 +239,9 @@ class Qwen2Model:
                 setattr(layers[i], k, p(lw[k], np.float16))
             for k in ("bq", "bk", "bv", "attn_norm", "ffn_norm"):
                 setattr(layers[i], k, p(lw[k], np.float32))
-        w = _Weights(p(weights["embed"], np.float16), p(weights["final_norm"], np.float32), layers)
+        head = weights.get("lm_head")
+        w = _Weights(p(weights["embed"], np.float16), p(head, np.float16) if head is not None else None,
+                     p(weights["final_norm"], np.float32), layers)
         h = _P()
         rc = L.qwen2_create(ctypes.byref(self._cfg), ctypes.byref(w), ctypes.byref(h))
         if rc:

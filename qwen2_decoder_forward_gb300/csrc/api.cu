@@ -89,8 +89,12 @@ int validate_config(const qwen2_config* g, std::string& msg) {
         msg = "rms_eps must be >= 0 and rope_theta > 0";
         return QWEN2_E_ARG;
     }
-    if (g->head_dim != 64) {
-        msg = "head_dim " + std::to_string(g->head_dim) + " is not supported (64 only)";
+    if (g->head_dim != 64 && g->head_dim != 128) {
+        msg = "head_dim " + std::to_string(g->head_dim) + " is not supported (64 or 128)";
+        return QWEN2_E_UNSUPPORTED;
+    }
+    if (g->head_dim != 64 && g->prefill_mode == QWEN2_PREFILL_TENSOR) {
+        msg = "the tensor-core prefill is built for head_dim 64; use QWEN2_PREFILL_F32";
         return QWEN2_E_UNSUPPORTED;
     }
     if (g->hidden != g->n_head * g->head_dim) {

@@ -13,27 +13,40 @@
 
 namespace qwen2 {
 
-constexpr int kHd = 64;        // head_dim this build supports
+constexpr int kHd = 64;        // head_dim of the persistent decode kernel (Qwen2.5-0.5B)
 constexpr int kAttCh = 64;     // keys per chunk
 constexpr int kMaxGroup = 8;   // query heads per kv head
 constexpr int kPartStride = kHd + 2;  // one partial: m, l, acc[64]
 
-struct AttnSmem {
-    float q[kMaxGroup][kHd];
-    float k[kAttCh][kHd + 1];   // padded: lanes read different keys
-    float v[kAttCh][kHd];
+// Attention scratch for head_dim HD: q of the group's heads, one chunk of
+// keys and values, the chunk's probabilities and softmax statistics.
+template <int HD>
+struct AttnSmemT {
+    float q[kMaxGroup][HD];
+    float k[kAttCh][HD + 1];   // padded: lanes read different keys
+    float v[kAttCh][HD];
     float p[kMaxGroup][kAttCh];
     float m[kMaxGroup];
     float l[kMaxGroup];
 };
+using AttnSmem = AttnSmemT<kHd>;
+
+// 1 / sqrt(head_dim): 0.125 exactly for 64, the float nearest 1/sqrt(128)
+// for 128.
+template <int HD>
+__host__ __device__ constexpr float attn_scale() {
+    static_assert(HD == 64 || HD == 128, "head_dim 64 or 128");
+    return HD == 64 ? 0.125f : 0.08838834764831843f;
+}
 
 // One chunk of nj <= 64 keys (k, v, q already in `sm`) for `group` query
 // heads, computed by a 256-thread group; emit(h, d, acc, m, l) once per
 // output element.
-template <class S, class Emit>
-__device__ __forceinline__ void attn_chunk(AttnSmem& sm, int group, int nj, Emit emit) {
+template <class S, int HD, class Emit>
+__device__ __forceinline__ void attn_chunk(AttnSmemT<HD>& sm, int group, int nj, Emit emit) {
     const int tid = threadIdx.x;
-    // Scores q_h . k_j / sqrt(hd); hd = 64 makes the scale 0.125 exact.
+    // Scores q_h . k_j / sqrt(hd); hd = 64 makes the scale 0.125 exact,
+    // hd = 128 takes the float nearest 1/sqrt(128).
     for (int e = tid; e < group * kAttCh; e += 256) {
         const int h = e / kAttCh, j = e % kAttCh;
         float s = -INFINITY;
@@ -41,13 +54,13 @@ __device__ __forceinline__ void attn_chunk(AttnSmem& sm, int group, int nj, Emit
             // Four partial sums over d = 4i + {0,1,2,3}, added in a fixed order.
             float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-            for (int d = 0; d < kHd; d += 4) {
+            for (int d = 0; d < HD; d += 4) {
                 a0 = fmaf(sm.q[h][d], sm.k[j][d], a0);
                 a1 = fmaf(sm.q[h][d + 1], sm.k[j][d + 1], a1);
                 a2 = fmaf(sm.q[h][d + 2], sm.k[j][d + 2], a2);
                 a3 = fmaf(sm.q[h][d + 3], sm.k[j][d + 3], a3);
             }
-            s = ((a0 + a1) + (a2 + a3)) * 0.125f;
+            s = ((a0 + a1) + (a2 + a3)) * attn_scale<HD>();
         }
         sm.p[h][j] = s;
     }
@@ -67,8 +80,8 @@ __device__ __forceinline__ void attn_chunk(AttnSmem& sm, int group, int nj, Emit
         }
     }
     S::sync();
-    for (int e = tid; e < group * kHd; e += 256) {
-        const int h = e / kHd, d = e % kHd;
+    for (int e = tid; e < group * HD; e += 256) {
+        const int h = e / HD, d = e % HD;
         // Four partial sums over keys j = 4i + {0,1,2,3} below nj & ~3, the
         // last nj % 4 keys into the first, then added in a fixed order (rows
         // of v past nj are never read).

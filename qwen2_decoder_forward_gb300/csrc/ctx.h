@@ -143,7 +143,8 @@ struct Ctx {
     void* wblob = nullptr;        // all packed weights, one allocation
     size_t wbytes = 0;
     std::vector<DevLayer> layers;
-    DevMat embed;                 // [V][H]; also the LM head
+    DevMat embed;                 // [V][H] token embedding
+    DevMat lm_head;               // [V][H] readout: `embed` itself when tied, else its own matrix
     const float* final_norm = nullptr;
     float* kv = nullptr;          // [max_seqs][L][2][nkv][n_ctx][hd]
     size_t kv_floats = 0;

@@ -31,12 +31,13 @@ struct StepArgs {
     const float2* rope;
     int* err;
     int H, nh, nkv, I, V, n_ctx, L;
+    int hd;  // head_dim: 64 or 128
     float eps;
 };
 
 __device__ __forceinline__ float* kv_ptr(const StepArgs& a, int slot, int layer, int which, int g, int p) {
-    return a.kv + ((((size_t)slot * a.L + layer) * 2 + which) * a.nkv + g) * (size_t)a.n_ctx * kHd +
-           (size_t)p * kHd;
+    return a.kv + ((((size_t)slot * a.L + layer) * 2 + which) * a.nkv + g) * (size_t)a.n_ctx * a.hd +
+           (size_t)p * a.hd;
 }
 
 // ---------------------------------------------------------------------------
@@ -75,8 +76,9 @@ __global__ void __launch_bounds__(kThreads) k_embed_q8(StepArgs a, const int8_t*
 __device__ __forceinline__ void qkv_pair_epilogue(const StepArgs& a, int layer, int pair, int b, float d0,
                                                   float d1, const float* __restrict__ bias) {
     const int r0 = 2 * pair;
-    const int s = r0 / kHd;
-    const int i = (r0 % kHd) >> 1;
+    const int hd = a.hd;
+    const int s = r0 / hd;
+    const int i = (r0 % hd) >> 1;
     const int p = a.pos[b];
     if (p < 0 || p >= a.n_ctx) {
         raise_guard(a.err, kGuardPosition);
@@ -86,20 +88,20 @@ __device__ __forceinline__ void qkv_pair_epilogue(const StepArgs& a, int layer, 
     const float v1 = d1 + bias[r0 + 1];
     if (s < a.nh + a.nkv) {
         float ra, rb;
-        rope_pair(v0, v1, a.rope[(size_t)p * (kHd / 2) + i], ra, rb);
+        rope_pair(v0, v1, a.rope[(size_t)p * (hd / 2) + i], ra, rb);
         if (s < a.nh) {
-            float* qr = a.q + (size_t)b * a.nh * kHd + s * kHd;
+            float* qr = a.q + (size_t)b * a.nh * hd + s * hd;
             qr[i] = ra;
-            qr[i + kHd / 2] = rb;
+            qr[i + hd / 2] = rb;
         } else {
             float* kr = kv_ptr(a, a.slot[b], layer, 0, s - a.nh, p);
             kr[i] = ra;
-            kr[i + kHd / 2] = rb;
+            kr[i + hd / 2] = rb;
         }
     } else {
         float* vr = kv_ptr(a, a.slot[b], layer, 1, s - a.nh - a.nkv, p);
         vr[i] = v0;
-        vr[i + kHd / 2] = v1;
+        vr[i + hd / 2] = v1;
     }
 }
 
@@ -196,15 +198,18 @@ __global__ void __launch_bounds__(kThreads) k_swiglu(const float* __restrict__ r
 }
 
 // ---------------------------------------------------------------------------
-// Split-K GQA decode attention.  Block (g, c, b) takes positions
-// [c*64, min(c*64+64, p+1)) of kv head g for row b and all `group` query
-// heads that read g (each K/V element is read once per group).  It writes
-// the partial (max, sum, acc[64]) per head; the last block of (b, g) to
+// Split-K GQA decode attention (head_dim HD).  Block (g, c, b) takes
+// positions [c*64, min(c*64+64, p+1)) of kv head g for row b and all
+// `group` query heads that read g (each K/V element is read once per
+// group).  It writes the partial (max, sum, acc[HD]) per head; the last block of (b, g) to
 // finish merges the partials in chunk order and writes the head outputs.
 // ---------------------------------------------------------------------------
+template <int HD>
 __global__ void __launch_bounds__(kThreads) k_attn_decode(StepArgs a, int layer, float* __restrict__ part,
                                                           int* __restrict__ count, int max_chunks) {
-    __shared__ __align__(16) AttnSmem sm;
+    extern __shared__ __align__(16) unsigned char attn_dyn[];
+    AttnSmemT<HD>& sm = *reinterpret_cast<AttnSmemT<HD>*>(attn_dyn);
+    constexpr int kStride = HD + 2;  // one partial: m, l, acc[HD]
     __shared__ int last_s;
     const int g = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
     const int group = a.nh / a.nkv;
@@ -221,14 +226,14 @@ __global__ void __launch_bounds__(kThreads) k_attn_decode(StepArgs a, int layer,
     const int slot = a.slot[b];
     const int tid = threadIdx.x;
 
-    for (int e = tid; e < group * kHd; e += kThreads)
-        sm.q[e / kHd][e % kHd] = a.q[(size_t)b * a.nh * kHd + (size_t)g * group * kHd + e];
+    for (int e = tid; e < group * HD; e += kThreads)
+        sm.q[e / HD][e % HD] = a.q[(size_t)b * a.nh * HD + (size_t)g * group * HD + e];
     const float* kb = kv_ptr(a, slot, layer, 0, g, j0);
     const float* vb = kv_ptr(a, slot, layer, 1, g, j0);
-    for (int e = tid; e < nj * (kHd / 4); e += kThreads) {
-        const int j = e / (kHd / 4), d4 = (e % (kHd / 4)) * 4;
-        const float4 kk = __ldcg(reinterpret_cast<const float4*>(kb + (size_t)j * kHd + d4));
-        const float4 vv = __ldcg(reinterpret_cast<const float4*>(vb + (size_t)j * kHd + d4));
+    for (int e = tid; e < nj * (HD / 4); e += kThreads) {
+        const int j = e / (HD / 4), d4 = (e % (HD / 4)) * 4;
+        const float4 kk = __ldcg(reinterpret_cast<const float4*>(kb + (size_t)j * HD + d4));
+        const float4 vv = __ldcg(reinterpret_cast<const float4*>(vb + (size_t)j * HD + d4));
         sm.k[j][d4] = kk.x;
         sm.k[j][d4 + 1] = kk.y;
         sm.k[j][d4 + 2] = kk.z;
@@ -237,7 +242,7 @@ __global__ void __launch_bounds__(kThreads) k_attn_decode(StepArgs a, int layer,
     }
     __syncthreads();
     attn_chunk<SyncBlock>(sm, group, nj, [&](int h, int d, float acc, float m, float l) {
-        float* pr = part + (((size_t)b * a.nh + g * group + h) * max_chunks + c) * kPartStride;
+        float* pr = part + (((size_t)b * a.nh + g * group + h) * max_chunks + c) * kStride;
         pr[2 + d] = acc;
         if (d == 0) {
             pr[0] = m;
@@ -254,12 +259,12 @@ __global__ void __launch_bounds__(kThreads) k_attn_decode(StepArgs a, int layer,
     if (!last_s) return;
     __threadfence();
     // The last block of (b, g) merges the chunks in order.
-    for (int e = tid; e < group * kHd; e += kThreads) {
-        const int h = e / kHd, d = e % kHd;
-        const float* ph = part + (((size_t)b * a.nh + g * group + h) * max_chunks) * kPartStride;
-        const size_t oi = (size_t)b * a.nh * kHd + (size_t)(g * group + h) * kHd + d;
+    for (int e = tid; e < group * HD; e += kThreads) {
+        const int h = e / HD, d = e % HD;
+        const float* ph = part + (((size_t)b * a.nh + g * group + h) * max_chunks) * kStride;
+        const size_t oi = (size_t)b * a.nh * HD + (size_t)(g * group + h) * HD + d;
         const float ov =
-            attn_merge(n_chunks, d, [&](int cc, int i) { return __ldcg(ph + (size_t)cc * kPartStride + i); });
+            attn_merge(n_chunks, d, [&](int cc, int i) { return __ldcg(ph + (size_t)cc * kStride + i); });
         a.o[oi] = ov;
         if (a.o_hi) bg::split_h(ov, a.o_hi[oi], a.o_lo[oi]);
     }
@@ -494,7 +499,7 @@ struct EpiQkvQ8 {
             if (tid == 0) raise_guard(a.err, kGuardShape);
             return;
         }
-        const int N = (a.nh + 2 * a.nkv) * kHd;
+        const int N = (a.nh + 2 * a.nkv) * a.hd;
         if (tid < 32) {
             qkv_pos_s[tid] = tid < B ? a.pos[tid] : 0;
             qkv_slot_s[tid] = tid < B ? a.slot[tid] : 0;
@@ -504,15 +509,15 @@ struct EpiQkvQ8 {
         for (int e = tid; e < 32 * np; e += blockDim.x) {
             const int b = e / np, k = e % np;
             const int p = b < B ? a.pos[b] : 0;
-            const int i = ((n0 + 2 * k) % kHd) >> 1;
-            qkv_rope_s[b][k] = (p >= 0 && p < a.n_ctx) ? a.rope[(size_t)p * (kHd / 2) + i] : make_float2(1.f, 0.f);
+            const int i = ((n0 + 2 * k) % a.hd) >> 1;
+            qkv_rope_s[b][k] = (p >= 0 && p < a.n_ctx) ? a.rope[(size_t)p * (a.hd / 2) + i] : make_float2(1.f, 0.f);
         }
     }
     // Packed rows (n, n + 1) = elements i and i + hd/2 of head slot s: bias,
     // NeoX rotation for q and k, then q to the query buffer, k and v to the
     // cache slot of the row's position (the arithmetic of qkv_pair_epilogue).
     __device__ __forceinline__ void pair(int b, int n, float d0, float d1, int) {
-        const int s = n / kHd, i = (n % kHd) >> 1, k = (n - n_cta0) >> 1;
+        const int s = n / a.hd, i = (n % a.hd) >> 1, k = (n - n_cta0) >> 1;
         const int p = qkv_pos_s[b];
         if (p < 0 || p >= a.n_ctx) {
             raise_guard(a.err, kGuardPosition);
@@ -524,18 +529,18 @@ struct EpiQkvQ8 {
             float ra, rb;
             rope_pair(v0, v1, qkv_rope_s[b][k], ra, rb);
             if (s < a.nh) {
-                float* qr = a.q + (size_t)b * a.nh * kHd + s * kHd;
+                float* qr = a.q + (size_t)b * a.nh * a.hd + s * a.hd;
                 qr[i] = ra;
-                qr[i + kHd / 2] = rb;
+                qr[i + a.hd / 2] = rb;
             } else {
                 float* kr = kv_ptr(a, qkv_slot_s[b], layer, 0, s - a.nh, p);
                 kr[i] = ra;
-                kr[i + kHd / 2] = rb;
+                kr[i + a.hd / 2] = rb;
             }
         } else {
             float* vr = kv_ptr(a, qkv_slot_s[b], layer, 1, s - a.nh - a.nkv, p);
             vr[i] = v0;
-            vr[i + kHd / 2] = v1;
+            vr[i + a.hd / 2] = v1;
         }
     }
     __device__ __forceinline__ void finish() {}
@@ -776,8 +781,20 @@ StepArgs make_step_args(Ctx& c, int B, const int* tok, const int* pos, const int
     a.V = c.cfg.vocab;
     a.n_ctx = c.cfg.n_ctx;
     a.L = c.cfg.n_layer;
+    a.hd = c.cfg.head_dim;
     a.eps = c.cfg.rms_eps;
     return a;
+}
+
+// The split-K decode attention for the context's head_dim.
+void launch_attn_decode(const Ctx& c, const StepArgs& a, int l, cudaStream_t st) {
+    const dim3 grid(c.cfg.n_kv_head, c.ws.att_max_chunks, a.B);
+    if (c.cfg.head_dim == 128)
+        k_attn_decode<128><<<grid, kThreads, sizeof(AttnSmemT<128>), st>>>(a, l, c.ws.att_part, c.ws.att_count,
+                                                                           c.ws.att_max_chunks);
+    else
+        k_attn_decode<64><<<grid, kThreads, sizeof(AttnSmemT<64>), st>>>(a, l, c.ws.att_part, c.ws.att_count,
+                                                                         c.ws.att_max_chunks);
 }
 
 int blocks_for(int warps_needed, int cap) {
@@ -788,7 +805,7 @@ int blocks_for(int warps_needed, int cap) {
 template <int NB>
 cudaError_t layer_step(Ctx& c, const StepArgs& a, int l, cudaStream_t st) {
     const DevLayer& L = c.layers[l];
-    const int H = c.cfg.hidden, I = c.cfg.intermediate, nq = c.cfg.n_head * kHd;
+    const int H = c.cfg.hidden, I = c.cfg.intermediate, nq = c.cfg.n_head * c.cfg.head_dim;
     const int cap = c.n_sm * 8;
     const bool fuse_qkv = !(c.cfg.flags & QWEN2_FLAG_NO_FUSE_QKV);
     const bool fuse_ffn = !(c.cfg.flags & QWEN2_FLAG_NO_FUSE_FFN);
@@ -798,7 +815,7 @@ cudaError_t layer_step(Ctx& c, const StepArgs& a, int l, cudaStream_t st) {
                                                                                       L.attn_norm, np);
     } else {
         k_rmsnorm_rows<<<a.B, kThreads, 0, st>>>(a.x, H, L.attn_norm, a.eps, c.ws.xn);
-        const int nkvd = c.cfg.n_kv_head * kHd;
+        const int nkvd = c.cfg.n_kv_head * c.cfg.head_dim;
         const int r0s[3] = {0, nq, nq + nkvd}, ns[3] = {nq, nkvd, nkvd};
         for (int part = 0; part < 3; ++part)
             k_gemv_rows<NB><<<blocks_for(ns[part] / 2, cap), kThreads, NB * H * 4, st>>>(
@@ -806,8 +823,7 @@ cudaError_t layer_step(Ctx& c, const StepArgs& a, int l, cudaStream_t st) {
         k_qkv_epilogue<<<dim3((c.nqkv / 2 + kThreads - 1) / kThreads, a.B), kThreads, 0, st>>>(a, l, c.ws.raw,
                                                                                              c.nqkv, L.bqkv);
     }
-    k_attn_decode<<<dim3(c.cfg.n_kv_head, c.ws.att_max_chunks, a.B), kThreads, 0, st>>>(
-        a, l, c.ws.att_part, c.ws.att_count, c.ws.att_max_chunks);
+    launch_attn_decode(c, a, l, st);
     k_gemv_residual<NB><<<blocks_for(H / 2, cap), kThreads, NB * nq * 4, st>>>(L.wo.w, H, nq, c.ws.o, a.B, a.x);
     if (fuse_ffn) {
         k_gateup_fused<NB><<<blocks_for(I, cap), kThreads, (NB * H + kWarps) * 4, st>>>(a, L.wgu.w, L.ffn_norm);
@@ -830,7 +846,7 @@ cudaError_t lm_head_nb(Ctx& c, const float* xin, int B, float* logits, int* ids,
     LmArgs la;
     la.xin = xin;
     la.norm_w = c.final_norm;
-    la.E = c.embed.w;
+    la.E = c.lm_head.w;
     la.B = B;
     la.H = c.cfg.hidden;
     la.V = c.cfg.vocab;
@@ -891,7 +907,7 @@ constexpr int kDownRows = (bg::kWarps / kDownKs) * kDownNtw * 8;
 template <int MT>
 cudaError_t o_ffn_q8(Ctx& c, int l, float* x, int B, cudaStream_t st) {
     const DevLayer& L = c.layers[l];
-    const int H = c.cfg.hidden, I = c.cfg.intermediate, nq = c.cfg.n_head * kHd;
+    const int H = c.cfg.hidden, I = c.cfg.intermediate, nq = c.cfg.n_head * c.cfg.head_dim;
     Workspace& w = c.ws;
     cudaError_t e = bgemm<MT, 1, 8>(c, bg::ProCopy{w.q8_ah, w.q8_al}, B, nq, nq, L.wo, H, EpiResidualQ8{x, H, 0, c.err}, st);
     if (e != cudaSuccess) return e;
@@ -909,8 +925,7 @@ cudaError_t attn_batched(const Ctx& c, const StepArgs& a, int l, cudaStream_t st
     const int group = a.nh / a.nkv;
     if (!c.kvmap_ok || a.B > fd::kMaxRows || c.ws.att_max_chunks > fd::kMaxChunks || group > fd::kGroupMax ||
         c.cfg.head_dim != fd::kDh) {
-        k_attn_decode<<<dim3(c.cfg.n_kv_head, c.ws.att_max_chunks, a.B), kThreads, 0, st>>>(
-            a, l, c.ws.att_part, c.ws.att_count, c.ws.att_max_chunks);
+        launch_attn_decode(c, a, l, st);
         return cudaGetLastError();
     }
     fd::Args f;
@@ -1003,7 +1018,7 @@ cudaError_t lm_head_q8(Ctx& c, float* x, int B, float* logits, int* ids, float* 
     const int tiles = (c.cfg.vocab + bg::kWarps * kLmNtw * 8 - 1) / (bg::kWarps * kLmNtw * 8);
     const int grid = tiles < c.n_sm ? tiles : c.n_sm;
     bg::k_bgemm_q8_tiles<MT, kLmNtw, EpiLmQ8, bg::ProCopy, false><<<grid, bg::kThreads, bg::smem_bytes(MT, H), st>>>(
-        bg::ProCopy{w.q8_ah, w.q8_al}, B, H, c.embed.q, c.embed.d, c.cfg.vocab, e, c.err);
+        bg::ProCopy{w.q8_ah, w.q8_al}, B, H, c.lm_head.q, c.lm_head.d, c.cfg.vocab, e, c.err);
     return cudaGetLastError();
 }
 
@@ -1020,7 +1035,7 @@ cudaError_t decode_q8(Ctx& c, int B, bool want_logits, cudaStream_t st) {
 
 template <int MT>
 cudaError_t rows_o_ffn_q8(Ctx& c, int l, float* x, const float* o, int B, cudaStream_t st) {
-    const int nq = c.cfg.n_head * kHd;
+    const int nq = c.cfg.n_head * c.cfg.head_dim;
     k_split_rows<<<(B * nq + kThreads - 1) / kThreads, kThreads, 0, st>>>(o, B * nq, c.ws.q8_ah, c.ws.q8_al);
     return o_ffn_q8<MT>(c, l, x, B, st);
 }
@@ -1028,7 +1043,7 @@ cudaError_t rows_o_ffn_q8(Ctx& c, int l, float* x, const float* o, int B, cudaSt
 template <int NB>
 cudaError_t rows_o_ffn_nb(Ctx& c, int l, float* x, const float* o, int B, cudaStream_t st) {
     const DevLayer& L = c.layers[l];
-    const int H = c.cfg.hidden, I = c.cfg.intermediate, nq = c.cfg.n_head * kHd;
+    const int H = c.cfg.hidden, I = c.cfg.intermediate, nq = c.cfg.n_head * c.cfg.head_dim;
     const int cap = c.n_sm * 8;
     StepArgs a = make_step_args(c, B, nullptr, nullptr, nullptr, x);
     k_gemv_residual<NB><<<blocks_for(H / 2, cap), kThreads, NB * nq * 4, st>>>(L.wo.w, H, nq, o, B, x);
@@ -1040,7 +1055,7 @@ cudaError_t rows_o_ffn_nb(Ctx& c, int l, float* x, const float* o, int B, cudaSt
 }  // namespace
 
 cudaError_t enqueue_rows_o_ffn(Ctx& c, int layer, float* x, const float* o, int rows, cudaStream_t st) {
-    const int H = c.cfg.hidden, nq = c.cfg.n_head * kHd;
+    const int H = c.cfg.hidden, nq = c.cfg.n_head * c.cfg.head_dim;
     if (c.cfg.weight_format == QWEN2_WEIGHTS_Q8_0) {
         for (int b0 = 0; b0 < rows; b0 += 32) {
             const int nb = rows - b0 < 32 ? rows - b0 : 32;
@@ -1139,6 +1154,9 @@ cudaError_t decode_set_smem_limits(int max_bytes) {
 #undef Q2_SMEM
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(k_attn_flash, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fd::kSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_attn_decode<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)sizeof(AttnSmemT<128>));
 #define Q2_BG(MT, NTW, KS, EPI, PRO)                                                                          \
     if (e == cudaSuccess)                                                                                     \
         e = cudaFuncSetAttribute(bg::k_bgemm_q8<MT, NTW, KS, EPI, PRO>, cudaFuncAttributeMaxDynamicSharedMemorySize, \

@@ -116,6 +116,7 @@ int pack_weights(Ctx& c, const qwen2_weights* w, std::string& err) {
         }
     };
     add_mat(V, H);
+    if (w->lm_head) add_mat(V, H);
     add((size_t)H * 4);
     for (int l = 0; l < g.n_layer; ++l) {
         add_mat(c.nqkv, H);
@@ -139,6 +140,7 @@ int pack_weights(Ctx& c, const qwen2_weights* w, std::string& err) {
     Blob b{host.data(), static_cast<char*>(c.wblob)};
 
     c.embed = put_mat(b, V, H, fmt, [&](int r) { return w->embed + (size_t)r * H; });
+    c.lm_head = w->lm_head ? put_mat(b, V, H, fmt, [&](int r) { return w->lm_head + (size_t)r * H; }) : c.embed;
     c.final_norm = put_f32(b, w->final_norm, H);
     c.layers.resize(g.n_layer);
     std::vector<float> bperm(c.nqkv);

@@ -302,7 +302,7 @@ struct Feeder {
             const bool down = l < a->L && ph == 3;
             const int K = down ? a->I : a->H;
             const int n = min(down ? a->rows_i : a->rows_h, r1 - r);
-            const __half* W = l == a->L ? a->E
+            const __half* W = l == a->L ? a->Wlm
                               : ph == 0 ? a->layers[l].wqkv
                               : ph == 1 ? a->layers[l].wo
                               : ph == 2 ? a->layers[l].wgu
@@ -1095,6 +1095,10 @@ cudaError_t persistent_setup(Ctx& c) {
         c.pers.why_not = "the persistent kernel streams f16 weights only";
         return cudaSuccess;
     }
+    if (g.head_dim != kHd) {
+        c.pers.why_not = "the persistent kernel is built for head_dim 64";
+        return cudaSuccess;
+    }
     const size_t act = std::max(sizeof(AttnSmem), (size_t)std::max(H, I) * 4);
     const size_t smem = (size_t)kPersistStages * kPersistStage + 256 + act + (size_t)H * 4;
     int dev_max = 0;
@@ -1195,6 +1199,7 @@ cudaError_t enqueue_decode_persistent(Ctx& c, bool want_logits, cudaStream_t st)
     PersistentArgs a;
     a.layers = c.pers.layers;
     a.E = c.embed.w;
+    a.Wlm = c.lm_head.w;
     a.final_norm = c.final_norm;
     a.kv = c.kv;
     a.rope = c.rope;

@@ -10,7 +10,8 @@ constexpr int kPersistStages = 6;     // ring depth (168 KB)
 
 struct PersistentArgs {
     const PersistLayer* layers;
-    const __half* E;
+    const __half* E;    // token embedding [V][H]
+    const __half* Wlm;  // LM head [V][H] (E itself when tied)
     const float* final_norm;
     float* kv;
     const float2* rope;

@@ -4,6 +4,7 @@
 // causal GQA attention over the KV cache; the tail-row cut (minfer "Qwen2 /
 // Qwen2.5 Architecture Support", section 3, "G3 tail-row optimization"); and
 // the LM head on the kept rows.
+#include "attn.cuh"
 #include "prefill.h"
 #include "rowdot.cuh"
 
@@ -12,7 +13,6 @@ namespace qwen2 {
 namespace {
 
 constexpr int kT = 256;
-constexpr int kHd = 64;
 constexpr int kGemvRows = 32;   // at most this many rows: o_proj and FFN as GEMVs
 
 // A weight matrix in f16 (w) or Q8_0 (q, d); see DevMat.
@@ -141,6 +141,7 @@ __device__ __forceinline__ void epilogue_store(const PrefillEpi& e, int m, int n
         break;
     case kEpiQKV: {
         if (n & 1) break;
+        const int kHd = e.hd;
         const int s = n / kHd, i = (n % kHd) >> 1;
         const int p = e.pos[m];
         if (p < 0 || p >= e.n_ctx) {
@@ -259,13 +260,19 @@ __global__ void __launch_bounds__(kT) k_gemm_f32(const float* __restrict__ A, WM
 constexpr int kQB = kPrefillQB;
 constexpr int kMaxG = 8;
 constexpr int kVecPerWarp = kQB * kMaxG / (kT / 32);
-constexpr int kAttnSmem = (kQB * kMaxG * kHd + 64 * (kHd + 1) + 64 * kHd) * 4;
+template <int HD>
+constexpr int attn_prefill_smem() {
+    return (kQB * kMaxG * HD + 64 * (HD + 1) + 64 * HD) * 4;
+}
 
+// head_dim HD (64 or 128): lane l accumulates output dims l + 32 u.
+template <int HD>
 __global__ void __launch_bounds__(kT) k_attn_prefill(PrefillAttnArgs a, int layer) {
+    constexpr int kHd = HD, kU = HD / 32;
     extern __shared__ __align__(16) float sm[];
-    float* q_s = sm;                       // [kQB*kMaxG][64]
-    float* v_s = q_s + kQB * kMaxG * kHd;  // [64][64]
-    float* k_s = v_s + 64 * kHd;           // [64][65]
+    float* q_s = sm;                       // [kQB*kMaxG][HD]
+    float* v_s = q_s + kQB * kMaxG * kHd;  // [64][HD]
+    float* k_s = v_s + 64 * kHd;           // [64][HD + 1]
     const int g = blockIdx.x, blk = blockIdx.y;
     const int r0 = a.blk_row0[blk], nr = a.blk_nrows[blk];
     const int group = a.nh / a.nkv;
@@ -281,14 +288,14 @@ __global__ void __launch_bounds__(kT) k_attn_prefill(PrefillAttnArgs a, int laye
         const int ri = v / group, h = v % group;
         q_s[e] = a.q[(size_t)(r0 + ri) * a.nh * kHd + (size_t)(g * group + h) * kHd + d];
     }
-    float m_[kVecPerWarp], l_[kVecPerWarp], o0[kVecPerWarp], o1[kVecPerWarp];
+    float m_[kVecPerWarp], l_[kVecPerWarp], o_[kVecPerWarp][kU];
     int p_[kVecPerWarp];
 #pragma unroll
     for (int t = 0; t < kVecPerWarp; ++t) {
         m_[t] = -INFINITY;
         l_[t] = 0.f;
-        o0[t] = 0.f;
-        o1[t] = 0.f;
+#pragma unroll
+        for (int u = 0; u < kU; ++u) o_[t][u] = 0.f;
         const int v = warp + 8 * t;
         p_[t] = v < nv ? a.pos[r0 + v / group] : -1;
     }
@@ -330,26 +337,28 @@ __global__ void __launch_bounds__(kT) k_attn_prefill(PrefillAttnArgs a, int laye
                 s0 = fmaf(qd, k_s[lane * (kHd + 1) + d], s0);
                 s1 = fmaf(qd, k_s[(lane + 32) * (kHd + 1) + d], s1);
             }
-            s0 = ok0 ? s0 * 0.125f : -INFINITY;
-            s1 = ok1 ? s1 * 0.125f : -INFINITY;
+            s0 = ok0 ? s0 * attn_scale<HD>() : -INFINITY;
+            s1 = ok1 ? s1 * attn_scale<HD>() : -INFINITY;
             const float cm = warp_max(fmaxf(s0, s1));
             const float mn = fmaxf(m_[t], cm);
             const float corr = expf(m_[t] - mn);
             const float e0 = expf(s0 - mn), e1 = expf(s1 - mn);
             l_[t] = fmaf(l_[t], corr, warp_sum(e0 + e1));
-            float a0 = o0[t] * corr, a1 = o1[t] * corr;
+            float acc[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) acc[u] = o_[t][u] * corr;
             for (int jj = 0; jj < 32; ++jj) {
                 const float pj = __shfl_sync(0xffffffffu, e0, jj);
-                a0 = fmaf(pj, v_s[jj * kHd + lane], a0);
-                a1 = fmaf(pj, v_s[jj * kHd + lane + 32], a1);
+#pragma unroll
+                for (int u = 0; u < kU; ++u) acc[u] = fmaf(pj, v_s[jj * kHd + lane + 32 * u], acc[u]);
             }
             for (int jj = 0; jj < 32; ++jj) {
                 const float pj = __shfl_sync(0xffffffffu, e1, jj);
-                a0 = fmaf(pj, v_s[(jj + 32) * kHd + lane], a0);
-                a1 = fmaf(pj, v_s[(jj + 32) * kHd + lane + 32], a1);
+#pragma unroll
+                for (int u = 0; u < kU; ++u) acc[u] = fmaf(pj, v_s[(jj + 32) * kHd + lane + 32 * u], acc[u]);
             }
-            o0[t] = a0;
-            o1[t] = a1;
+#pragma unroll
+            for (int u = 0; u < kU; ++u) o_[t][u] = acc[u];
             m_[t] = mn;
         }
     }
@@ -359,12 +368,10 @@ __global__ void __launch_bounds__(kT) k_attn_prefill(PrefillAttnArgs a, int laye
         if (v >= nv) continue;
         const int ri = v / group, h = v % group;
         const size_t off = (size_t)(r0 + ri) * a.nh * kHd + (size_t)(g * group + h) * kHd;
-        if (a.o_h) {
-            put_split(a.o_h, a.o_l, off + lane, o0[t] / l_[t]);
-            put_split(a.o_h, a.o_l, off + lane + 32, o1[t] / l_[t]);
-        } else {
-            a.o[off + lane] = o0[t] / l_[t];
-            a.o[off + lane + 32] = o1[t] / l_[t];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            if (a.o_h) put_split(a.o_h, a.o_l, off + lane + 32 * u, o_[t][u] / l_[t]);
+            else a.o[off + lane + 32 * u] = o_[t][u] / l_[t];
         }
     }
 }
@@ -390,6 +397,7 @@ PrefillEpi base_epi(Ctx& c, int layer, const int* pos, const int* slot, float* x
     e.nkv = c.cfg.n_kv_head;
     e.n_ctx = c.cfg.n_ctx;
     e.L = c.cfg.n_layer;
+    e.hd = c.cfg.head_dim;
     e.layer = layer;
     e.x = x;
     e.q = q;
@@ -407,14 +415,18 @@ dim3 gemm_grid(int M, int N) { return dim3((N + GBN - 1) / GBN, (M + GBM - 1) / 
 }  // namespace
 
 cudaError_t prefill_set_smem_limits() {
-    cudaError_t e = cudaFuncSetAttribute(k_attn_prefill, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
+    cudaError_t e = cudaFuncSetAttribute(k_attn_prefill<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         attn_prefill_smem<64>());
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_attn_prefill<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 attn_prefill_smem<128>());
     return e == cudaSuccess ? prefill_attn_mma_set_smem() : e;
 }
 
 cudaError_t enqueue_prefill(Ctx& c, int rows, int n_keep, const PrefillPlan& plan, float* logits_dev,
                             int* ids_dev, cudaStream_t st) {
     const qwen2_config& g = c.cfg;
-    const int H = g.hidden, I = g.intermediate, nq = g.n_head * kHd;
+    const int H = g.hidden, I = g.intermediate, nq = g.n_head * g.head_dim;
     const bool tensor = g.prefill_mode == QWEN2_PREFILL_TENSOR;
     Workspace& w = c.ws;
     k_embed_rows<<<rows, kT, 0, st>>>(w.rows_tok, g.vocab, H, wmat(c.embed), w.x, c.err);
@@ -467,7 +479,10 @@ cudaError_t enqueue_prefill(Ctx& c, int rows, int n_keep, const PrefillPlan& pla
             cudaError_t err = enqueue_attn_prefill_mma(aa, l, n_blk, st);
             if (err != cudaSuccess) return err;
         } else {
-            k_attn_prefill<<<dim3(g.n_kv_head, n_blk), kT, kAttnSmem, st>>>(aa, l);
+            if (g.head_dim == 128)
+                k_attn_prefill<128><<<dim3(g.n_kv_head, n_blk), kT, attn_prefill_smem<128>(), st>>>(aa, l);
+            else
+                k_attn_prefill<64><<<dim3(g.n_kv_head, n_blk), kT, attn_prefill_smem<64>(), st>>>(aa, l);
         }
         if (!tc && cur <= kGemvRows) {
             // A few rows (the tail cut's, or a short prompt): the decode GEMV

@@ -16,6 +16,7 @@ enum EpiKind : int { kEpiQKV = 0, kEpiResidual = 1, kEpiSwiGLU = 2 };
 struct PrefillEpi {
     int kind;
     int H, I, nh, nkv, n_ctx, L, layer;
+    int hd;  // head_dim (the QKV epilogue's head slots and RoPE pairs)
     float* x;
     float* q;
     __half* q_h;
@@ -30,8 +31,8 @@ struct PrefillEpi {
 };
 
 struct PrefillAttnArgs {
-    const float* q;         // [rows][nh*64] rotated queries
-    float* o;               // [rows][nh*64] head outputs (f32), or
+    const float* q;         // [rows][nh*hd] rotated queries
+    float* o;               // [rows][nh*hd] head outputs (f32), or
     __half* o_h;            //   f16 hi / lo pairs when o_h is not null
     __half* o_l;            //   (tensor-core operands: o = o_h + o_l)
     const float* kv;

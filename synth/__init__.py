@@ -83,6 +83,12 @@ SHAPES = {
     "toy-untied": ModelShape("toy-untied", n_layer=2, hidden=1024, n_head=8,
                              n_kv_head=4, head_dim=128, intermediate=1024,
                              vocab=4096, tie_embeddings=False),
+    # The toy shape (head_dim 64) with an untied LM head: the separate
+    # readout on the batch-1 persistent decode kernel.
+    "toy-untied-hd64": ModelShape("toy-untied-hd64", n_layer=2, hidden=256,
+                                  n_head=4, n_kv_head=2, head_dim=64,
+                                  intermediate=1024, vocab=4096,
+                                  tie_embeddings=False),
 }
 
 

@@ -53,14 +53,15 @@ def _create(L, **over):
     for i in range(len(layers)):
         for f, _ in q2._LayerWeights._fields_:
             setattr(layers[i], f, dummy.ctypes.data)
-    w = q2._Weights(dummy.ctypes.data, dummy.ctypes.data, layers)
+    w = q2._Weights(dummy.ctypes.data, None, dummy.ctypes.data, layers)
     h = ctypes.c_void_p()
     rc = L.qwen2_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h))
     return rc, L.qwen2_last_error(None).decode(), h
 
 
 @pytest.mark.parametrize("over,code", [
-    ({"head_dim": 128, "hidden": 512}, q2.QWEN2_E_UNSUPPORTED),
+    ({"head_dim": 96, "hidden": 384}, q2.QWEN2_E_UNSUPPORTED),
+    ({"head_dim": 128, "hidden": 512, "prefill_mode": 1}, q2.QWEN2_E_UNSUPPORTED),
     ({"hidden": 320}, q2.QWEN2_E_UNSUPPORTED),
     ({"intermediate": 1000}, q2.QWEN2_E_UNSUPPORTED),
     ({"n_kv_head": 3}, q2.QWEN2_E_UNSUPPORTED),
@@ -127,14 +128,20 @@ def test_no_alloc_head_rejects_bad_sizes_before_any_cuda_call(L):
     assert b"16-byte" in L.qwen2_last_error(None)
 
 
-def test_untied_lm_head_is_rejected_before_any_device_work():
-    """The C ABI's LM head is the tied embedding; the binding refuses a
-    separate head matrix instead of dropping it."""
+def test_untied_shape_without_a_head_matrix_is_rejected_before_any_device_work():
+    """A shape that declares an untied LM head must bring the head matrix;
+    the binding refuses it before any library call otherwise."""
     shape = synth.SHAPES["toy-untied"]
-    w = synth.make_weights(shape, 0)
+    w = dict(synth.make_weights(shape, 0))
+    del w["lm_head"]
     with pytest.raises(q2.Qwen2Error) as e:
         q2.Qwen2Model(shape, w, n_ctx=32)
-    assert e.value.code == q2.QWEN2_E_UNSUPPORTED
+    assert e.value.code == q2.QWEN2_E_ARG
+
+
+def test_weights_struct_carries_the_lm_head_between_embed_and_final_norm():
+    names = [f for f, _ in q2._Weights._fields_]
+    assert names == ["embed", "lm_head", "final_norm", "layers"]
 
 
 def test_stop_id_constants_match_the_pages():
