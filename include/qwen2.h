@@ -247,6 +247,19 @@ int qwen2_final_hidden(qwen2_ctx *ctx, float *dst, int32_t rows, void *stream);
  * (position, token, shape, timeout); QWEN2_E_ARG otherwise. */
 int qwen2_test_raise_guard(qwen2_ctx *ctx, int32_t code, void *stream);
 
+/* Test hook for failure detection without a GPU fault: the next
+ * persistent batch-1 decode launch of this context (one launch; the hook is
+ * cleared by it) waits, after layer 0's Q/K/V, on an arrival counter that no
+ * CTA ever arrives at, and every bounded wait of that launch gives up after
+ * wait_us microseconds instead of 2 s.  The wait runs out, the CTAs stop
+ * (each waits, bounded, for its weight copies in flight) and the launch
+ * sets the guard word; the next qwen2_synchronize returns
+ * QWEN2_E_DEVICE_GUARD ("bounded wait timed out") and resets the kernel's
+ * exchange state.  The launch writes no ids; KV rows of layer 0 at its
+ * position may be written.  Errors: QWEN2_E_ARG (wait_us outside [100,
+ * 2000000]), QWEN2_E_UNSUPPORTED (the context has no persistent kernel). */
+int qwen2_test_stall_decode(qwen2_ctx *ctx, int32_t wait_us);
+
 /* Synchronise `stream` and report any device-side guard that tripped since
  * the last check (QWEN2_E_DEVICE_GUARD, with the guard's code in the
  * message); clears the guard word. */

@@ -54,7 +54,7 @@ EXPORTS = (
     "qwen2_prefill", "qwen2_decode_step", "qwen2_decode_steps", "qwen2_decode_steps_stop",
     "qwen2_final_hidden", "qwen2_synchronize", "qwen2_weight_bytes",
     "qwen2_kv_bytes_per_seq", "qwen2_quantize_q8_0", "qwen2_features", "qwen2_profile_marks",
-    "qwen2_lm_head_argmax_noalloc", "qwen2_test_raise_guard",
+    "qwen2_lm_head_argmax_noalloc", "qwen2_test_raise_guard", "qwen2_test_stall_decode",
 )
 
 
@@ -120,6 +120,8 @@ def lib() -> ctypes.CDLL:
     L.qwen2_decode_steps_stop.restype = ctypes.c_int
     L.qwen2_test_raise_guard.argtypes = [_P, i32, _P]
     L.qwen2_test_raise_guard.restype = ctypes.c_int
+    L.qwen2_test_stall_decode.argtypes = [_P, i32]
+    L.qwen2_test_stall_decode.restype = ctypes.c_int
     L.qwen2_final_hidden.argtypes = [_P, _P, i32, _P]
     L.qwen2_final_hidden.restype = ctypes.c_int
     L.qwen2_synchronize.argtypes = [_P, _P]
@@ -383,6 +385,12 @@ class Qwen2Model:
         """Test hook: write ``code`` into the device guard word (as a kernel's
         bounded wait does when it gives up); the next synchronize reports it."""
         self._check(lib().qwen2_test_raise_guard(self._h, code, _stream_ptr(stream)))
+
+    def test_stall_decode(self, wait_us: int = 1000):
+        """Test hook: the next persistent decode launch waits on a counter
+        nothing arrives at, with its bounded waits limited to wait_us; the
+        next synchronize reports the timeout."""
+        self._check(lib().qwen2_test_stall_decode(self._h, int(wait_us)))
 
     def synchronize(self, stream=None):
         self._check(lib().qwen2_synchronize(self._h, _stream_ptr(stream)))

@@ -599,6 +599,19 @@ int qwen2_test_raise_guard(qwen2_ctx* h, int32_t code, void* stream) {
     return QWEN2_OK;
 }
 
+int qwen2_test_stall_decode(qwen2_ctx* h, int32_t wait_us) {
+    if (!h) return QWEN2_E_ARG;
+    Ctx& c = h->c;
+    if (wait_us < 100 || wait_us > 2000000) return fail(&c, QWEN2_E_ARG, "wait_us outside [100, 2000000]");
+    if (!c.pers.ok)
+        return fail(&c, QWEN2_E_UNSUPPORTED, "no persistent decode kernel in this context: " + c.pers.why_not);
+    if (c.cfg.flags & (QWEN2_FLAG_NO_MEGAKERNEL | QWEN2_FLAG_NO_FUSE_QKV | QWEN2_FLAG_NO_FUSE_FFN))
+        return fail(&c, QWEN2_E_UNSUPPORTED, "the context's flags switch the persistent decode kernel off");
+    c.pers.test_stall = 1;
+    c.pers.test_wait_ns = (unsigned long long)wait_us * 1000ull;
+    return QWEN2_OK;
+}
+
 int qwen2_synchronize(qwen2_ctx* h, void* stream) {
     if (!h) return QWEN2_E_ARG;
     Ctx& c = h->c;

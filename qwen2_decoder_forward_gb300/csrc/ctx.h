@@ -121,6 +121,8 @@ struct PersistState {
     size_t pk_bytes = 0, cnt_bytes = 0;
     long long* prof = nullptr;        // per-phase timestamps (QWEN2_FLAG_PROFILE)
     int prof_marks = 0;
+    int test_stall = 0;               // the next launch waits on a counter nothing arrives at
+    unsigned long long test_wait_ns = 0;  // and gives up after this many ns
     std::string why_not;              // why the kernel is unavailable, if it is
 };
 

@@ -42,9 +42,12 @@ constexpr int kThreads = 384;            // + warpgroup 2, whose first lane feed
 // 64512); the feeding warpgroup drops to 40 and the compute warpgroups rise
 // to 232: 4 x 32 x 40 + 8 x 32 x 232 = 64512, the launch's own total.
 constexpr int kRegFeed = 40, kRegCompute = 232;
-constexpr unsigned long long kWaitNs = 2000000000ull;  // a wait gives up after 2 s
-
 typedef unsigned long long u64;
+
+// Every bounded wait of a launch gives up after wait_limit() ns: 2 s
+// (kPersistWaitNs) unless the test hook shortened it for one launch.
+__shared__ u64 wait_limit_s;
+__device__ __forceinline__ u64 wait_limit() { return wait_limit_s; }
 
 __device__ __forceinline__ u64 now_ns() {
     u64 t;
@@ -142,7 +145,7 @@ struct PkReader {
         if ((unsigned)(w >> 32) == ep) return __uint_as_float((unsigned)w);
         const u64 t0 = now_ns();
         while ((unsigned)(w >> 32) != ep) {
-            if (now_ns() - t0 > kWaitNs) {
+            if (now_ns() - t0 > wait_limit()) {
                 failed = true;
                 return 0.f;
             }
@@ -191,7 +194,7 @@ __device__ __forceinline__ void pk_gather(PkReader& rd, int n, Addr addr, Store 
                         store(j0 + tid + 256 * k, __uint_as_float((unsigned)w[k]));
                         pending &= ~(1u << k);
                     }
-                if (pending && now_ns() - t0 > kWaitNs) {
+                if (pending && now_ns() - t0 > wait_limit()) {
                     rd.failed = true;
                     break;
                 }
@@ -324,7 +327,7 @@ struct Feeder {
             const unsigned k = issued / a->stages;
             const u64 t0 = now_ns();
             while (!mbar_test(&empty[s], (k - 1) & 1)) {
-                if (now_ns() - t0 > kWaitNs) return false;
+                if (now_ns() - t0 > wait_limit()) return false;
                 __nanosleep(20);
             }
         }
@@ -334,7 +337,7 @@ struct Feeder {
     __device__ __forceinline__ void drain() {
         for (int j = max(0, issued - a->stages); j < issued; ++j) {
             const u64 t0 = now_ns();
-            while (!mbar_try_wait(&full[j % a->stages], (j / a->stages) & 1) && now_ns() - t0 < kWaitNs) {
+            while (!mbar_try_wait(&full[j % a->stages], (j / a->stages) & 1) && now_ns() - t0 < wait_limit()) {
             }
         }
     }
@@ -416,7 +419,7 @@ __device__ __forceinline__ void rows_dot_x(const __half* const (&rows)[R], const
 __device__ __forceinline__ bool wait_bar(u64* b, unsigned par) {
     if (mbar_try_wait(b, par)) return true;
     const u64 t0 = now_ns();
-    while (now_ns() - t0 < kWaitNs)
+    while (now_ns() - t0 < wait_limit())
         if (mbar_try_wait(b, par)) return true;
     return false;
 }
@@ -663,6 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
     const int rpc_i = a.rows_i;
 
     if (tid == 0) {
+        wait_limit_s = a.wait_ns;
         for (int s = 0; s < a.stages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kCompute / 32);
@@ -750,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
             if (pk_raw(cp) < target) {
                 const u64 t0 = now_ns();
                 while (pk_raw(cp) < target) {
-                    if (now_ns() - t0 > kWaitNs) {
+                    if (now_ns() - t0 > wait_limit()) {
                         bad = true;
                         break;
                     }
@@ -854,6 +858,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
         if (phase_end()) break;
         arrive(l * 5 + 0);
         mark(mb + 2);
+        if (a.test_stall && l == 0) {
+            // Test hook: wait on a counter no CTA arrives at.  The wait runs
+            // out (a shortened limit), the CTAs leave, and the guard word
+            // reports it.
+            wait_cnt(L * 5 + 1);
+            if (phase_end()) break;
+        }
 
         // ---- attention: units (kv head g, chunk of 64 keys, query heads) -
         // When there are fewer (kv head, chunk) pairs than CTAs, each pair's
@@ -1166,7 +1177,9 @@ cudaError_t persistent_setup(Ctx& c) {
     c.pers.pk = static_cast<unsigned long long*>(p);
     if ((e = cudaMemset(p, 0, n_pk * 8)) != cudaSuccess) return e;
     c.pers.pk_bytes = n_pk * 8;
-    c.pers.cnt_bytes = (size_t)(g.n_layer * 5 + 1) * kCntStride * 8;
+    // One counter per phase of every layer, one for the argmax, and one
+    // that nothing arrives at (the failure-detection test hook waits on it).
+    c.pers.cnt_bytes = (size_t)(g.n_layer * 5 + 2) * kCntStride * 8;
     if ((e = cudaMalloc(&p, c.pers.cnt_bytes)) != cudaSuccess) return e;
     c.allocs.push_back(p);
     c.pers.cnt = static_cast<unsigned long long*>(p);
@@ -1233,6 +1246,9 @@ cudaError_t enqueue_decode_persistent(Ctx& c, bool want_logits, cudaStream_t st)
     a.prof = c.pers.prof;
     a.cnt = c.pers.cnt;
     a.prof_marks = c.pers.prof_marks;
+    a.wait_ns = c.pers.test_stall ? c.pers.test_wait_ns : kPersistWaitNs;
+    a.test_stall = c.pers.test_stall;
+    c.pers.test_stall = 0;  // one launch only
     if (c.pers.prof) {
         cudaError_t e = cudaMemsetAsync(c.pers.prof, 0, (size_t)c.pers.grid * c.pers.prof_marks * 8, st);
         if (e != cudaSuccess) return e;

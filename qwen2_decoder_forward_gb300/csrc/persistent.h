@@ -32,7 +32,11 @@ struct PersistentArgs {
     unsigned long long* cnt;  // per-phase arrival counters, one line each
     long long* prof;   // nullable: [grid][prof_marks] timestamps
     int prof_marks;
+    unsigned long long wait_ns;  // every bounded wait gives up after this many ns
+    int test_stall;              // test hook: wait on a counter nothing arrives at
 };
+
+constexpr unsigned long long kPersistWaitNs = 2000000000ull;  // a wait gives up after 2 s
 
 // Profiling slots per CTA: 0 launch start; per layer l, 1 + 16 l + k with
 // k = 0 x gathered, 1 normed, 2 Q/K/V done, 3 q ready (attention CTAs),

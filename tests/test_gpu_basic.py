@@ -303,6 +303,44 @@ def test_device_guard_is_reported_once_and_decoding_continues(q2):
     np.testing.assert_array_equal(again, ref)
 
 
+def test_a_bounded_wait_that_runs_out_is_reported_and_decoding_recovers(q2):
+    """Failure detection without a GPU fault: the test hook makes one
+    persistent decode launch wait on an arrival counter that no CTA arrives
+    at, with a 1 ms limit on its bounded waits.  The wait runs out, every
+    CTA stops (the feeding lane waits for its copies in flight), the launch
+    raises the guard word; synchronize reports QWEN2_E_DEVICE_GUARD once,
+    resets the exchange state, and the same decode then gives the ids of an
+    undisturbed run."""
+    shape = synth.SHAPES["toy"]
+    w = synth.make_weights(shape, 0)
+    prompt = synth.make_tokens(shape.vocab, 16, 1001)
+    with q2.Qwen2Model(shape, w, n_ctx=64, max_seqs=1, max_tokens=16) as m:
+        assert m.features & q2.FEATURE_PERSISTENT_DECODE
+        _, ids = m.prefill([0], [prompt])
+        first = int(ids[0])
+        ref = m.decode_steps([0], [first], [16], 8).cpu().numpy()
+        m.synchronize()
+        for _ in range(2):
+            m.test_stall_decode(1000)
+            m.decode_steps([0], [first], [16], 1)
+            with pytest.raises(q2.Qwen2Error) as e:
+                m.synchronize()
+            assert e.value.code == q2.QWEN2_E_DEVICE_GUARD
+            assert "bounded wait timed out" in str(e.value)
+            m.synchronize()
+            again = m.decode_steps([0], [first], [16], 8).cpu().numpy()
+            m.synchronize()
+            np.testing.assert_array_equal(again, ref)
+        with pytest.raises(q2.Qwen2Error) as e:
+            m.test_stall_decode(10)
+        assert e.value.code == q2.QWEN2_E_ARG
+    for kw in ({"flags": q2.FLAG_NO_MEGAKERNEL}, {"weight_format": q2.WEIGHTS_Q8_0}):
+        with q2.Qwen2Model(shape, w, n_ctx=64, max_seqs=1, max_tokens=16, **kw) as m:
+            with pytest.raises(q2.Qwen2Error) as e:
+                m.test_stall_decode(1000)
+            assert e.value.code == q2.QWEN2_E_UNSUPPORTED
+
+
 def test_oversized_kv_cache_is_an_allocation_error(q2):
     """A KV cache larger than the device (65,536 sequences x 32,768
     positions of the toy model: 4 TB) is QWEN2_E_OOM from create, and the
