@@ -280,7 +280,9 @@ int get_graph(Ctx& c, int B, bool want_logits, cudaGraphExec_t* out) {
 }
 
 int run_decode_step(Ctx& c, int B, bool want_logits, cudaStream_t st) {
-    if (c.cfg.flags & QWEN2_FLAG_NO_GRAPH) {
+    // A launch armed by qwen2_test_stall_decode carries its own arguments:
+    // it runs outside the cached graphs (whose arguments are baked in).
+    if ((c.cfg.flags & QWEN2_FLAG_NO_GRAPH) || (c.pers.test_stall && use_persistent(c, B))) {
         cudaError_t e = enqueue_step(c, B, want_logits, st);
         if (e != cudaSuccess) return cuda_fail(&c, e, "decode step launch");
         return QWEN2_OK;

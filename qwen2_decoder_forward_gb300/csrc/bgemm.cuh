@@ -379,6 +379,169 @@ __global__ void __launch_bounds__(W * 32) k_bgemm_q8(Pro pro, int B, int K, int 
     epi.finish();
 }
 
+// The product with the CTA's whole weight tile staged in shared memory.
+// Before waiting for the previous kernel (pdl_wait), one warp issues a bulk
+// copy of each of the CTA's weight rows (kc bytes of int8 at row stride
+// kc + 32 bytes in shared memory: the 8-row x 32-byte fragment loads then
+// fall on distinct banks) and every thread loads a share of the block
+// scales: the weights never depend on an earlier kernel, so their whole
+// stream is in flight while the previous kernel drains and while the
+// activation rows are staged.  The arithmetic is k_bgemm_q8's: the same
+// fragments, the same block order per warp, the same k-split reduction.
+__host__ __device__ constexpr int wrow_ld(int kc) { return kc + 32; }
+__host__ __device__ constexpr size_t smem_bytes_s(int mt, int kc, int rows_cta) {
+    return (size_t)2 * (mt * 16) * row_ld(kc) * 2 + (size_t)rows_cta * wrow_ld(kc) +
+           (size_t)rows_cta * (kc / 32) * 2 + 64;
+}
+
+template <int MT, int NTW, int KS, class Epi, class Pro, int W = kWarps>
+__global__ void __launch_bounds__(W * 32) k_bgemm_q8s(Pro pro, int B, int K, int kc_len,
+                                                      const int8_t* __restrict__ Q, const __half* __restrict__ D,
+                                                      int N, Epi epi, int* err) {
+    using namespace sm100;
+    extern __shared__ __align__(16) unsigned char smem[];
+    constexpr int kRows = MT * 16;
+    constexpr int kGroups = W / KS;
+    constexpr int kRowsCta = kGroups * NTW * 8;
+    static_assert(W % KS == 0, "KS divides the warps");
+    const int ld = row_ld(kc_len), wld = wrow_ld(kc_len);
+    __half* ah = reinterpret_cast<__half*>(smem);
+    __half* al = ah + kRows * ld;
+    int8_t* wq = reinterpret_cast<int8_t*>(al + kRows * ld);
+    const int nbl = kc_len / 32;  // scale columns per weight row in shared memory
+    uint16_t* wd = reinterpret_cast<uint16_t*>(wq + (size_t)kRowsCta * wld);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(
+        (reinterpret_cast<uintptr_t>(wd + (size_t)kRowsCta * nbl) + 15) & ~uintptr_t(15));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int gi = lane >> 2, ti = lane & 3;
+    const int grp = warp % kGroups, ks = warp / kGroups;
+    const int n_cta0 = blockIdx.x * kRowsCta;
+    const int r0 = grp * NTW * 8;  // this warp's first row within the tile
+    const int n0 = n_cta0 + r0;
+    const int kc0 = blockIdx.y * kc_len;
+    const int kc = min(kc_len, K - kc0);
+    const int Bc = min(B, kRows);
+    const int nb = kc / 32;
+    const int rows = min(kRowsCta, N - n_cta0);
+
+    if (tid == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    // The weight tile: one bulk copy per row (16-byte aligned: K, kc0 and kc
+    // are multiples of 32), completion counted on bar[1].
+    if (warp == 0) {
+        if (lane == 0) mbar_expect_tx(&bar[1], (unsigned)(rows * kc));
+        __syncwarp();
+        for (int r = lane; r < rows; r += 32)
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                    smem_addr(wq + (size_t)r * wld)),
+                "l"(Q + (size_t)(n_cta0 + r) * K + kc0), "r"((unsigned)kc), "r"(smem_addr(&bar[1]))
+                : "memory");
+    }
+    for (int e = tid; e < rows * nb; e += W * 32) {
+        const int r = e / nb, b = e % nb;
+        wd[r * nbl + b] = (uint16_t)ld_stream_u16(D + (size_t)(n_cta0 + r) * (K / 32) + kc0 / 32 + b);
+    }
+    pdl_launch_dependents();
+    pdl_wait();
+    epi.start(n_cta0, kRowsCta, B);
+    __syncthreads();
+    const bool staged = pro.stage(ah, al, ld, Bc, K, kc0, kc, &bar[0]);
+    const bool loaded = mbar_wait(&bar[1], 0, kWaitNs);
+    if ((!staged || !loaded) && lane == 0) raise_guard(err, kGuardTimeout);
+    __syncthreads();  // the scales
+
+    float acc[MT][NTW][4];
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int t = 0; t < NTW; ++t) acc[m][t][0] = acc[m][t][1] = acc[m][t][2] = acc[m][t][3] = 0.f;
+    if (staged && loaded) {
+        for (int kb = ks; kb < nb; kb += KS) {
+            uint32_t bw[NTW][4];
+            float dsc[NTW][2];
+#pragma unroll
+            for (int t = 0; t < NTW; ++t) {
+                const uint2 q = *reinterpret_cast<const uint2*>(wq + (size_t)(r0 + t * 8 + gi) * wld + kb * 32 + 8 * ti);
+                bw[t][0] = i8x2_to_h2(q.x, 0x4140u);
+                bw[t][1] = i8x2_to_h2(q.x, 0x4342u);
+                bw[t][2] = i8x2_to_h2(q.y, 0x4140u);
+                bw[t][3] = i8x2_to_h2(q.y, 0x4342u);
+                dsc[t][0] = h_bits_to_f(wd[(r0 + t * 8 + 2 * ti) * nbl + kb]);
+                dsc[t][1] = h_bits_to_f(wd[(r0 + t * 8 + 2 * ti + 1) * nbl + kb]);
+            }
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                const __half* hr = ah + (m * 16 + gi) * ld + kb * 32 + 8 * ti;
+                const __half* lr = al + (m * 16 + gi) * ld + kb * 32 + 8 * ti;
+                const uint4 h0 = *reinterpret_cast<const uint4*>(hr);
+                const uint4 h1 = *reinterpret_cast<const uint4*>(hr + 8 * ld);
+                const uint4 l0 = *reinterpret_cast<const uint4*>(lr);
+                const uint4 l1 = *reinterpret_cast<const uint4*>(lr + 8 * ld);
+#pragma unroll
+                for (int t = 0; t < NTW; ++t) {
+                    float p[4] = {0.f, 0.f, 0.f, 0.f};
+                    mma16816(p, h0.x, h1.x, h0.y, h1.y, bw[t][0], bw[t][1]);
+                    mma16816(p, l0.x, l1.x, l0.y, l1.y, bw[t][0], bw[t][1]);
+                    mma16816(p, h0.z, h1.z, h0.w, h1.w, bw[t][2], bw[t][3]);
+                    mma16816(p, l0.z, l1.z, l0.w, l1.w, bw[t][2], bw[t][3]);
+                    acc[m][t][0] = fmaf(dsc[t][0], p[0], acc[m][t][0]);
+                    acc[m][t][1] = fmaf(dsc[t][1], p[1], acc[m][t][1]);
+                    acc[m][t][2] = fmaf(dsc[t][0], p[2], acc[m][t][2]);
+                    acc[m][t][3] = fmaf(dsc[t][1], p[3], acc[m][t][3]);
+                }
+            }
+        }
+    }
+    auto emit_tile = [&](int m, int t, const float (&v)[4]) {
+        const int n = n0 + t * 8 + 2 * ti;
+        const int b0 = m * 16 + gi, b1 = b0 + 8;
+        if (n < N) {
+            if (b0 < B) epi.pair(b0, n, v[0], v[1], blockIdx.y);
+            if (b1 < B) epi.pair(b1, n, v[2], v[3], blockIdx.y);
+        }
+    };
+    if (KS == 1) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int t = 0; t < NTW; ++t) emit_tile(m, t, acc[m][t]);
+    } else {
+        float4* red = reinterpret_cast<float4*>(smem);
+        constexpr int kTiles = MT * NTW;
+        __syncthreads();
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int t = 0; t < NTW; ++t)
+                red[((ks * kGroups + grp) * kTiles + m * NTW + t) * 32 + lane] =
+                    make_float4(acc[m][t][0], acc[m][t][1], acc[m][t][2], acc[m][t][3]);
+        __syncthreads();
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int t = 0; t < NTW; ++t) {
+                const int j = m * NTW + t;
+                if (j % KS != ks) continue;
+                float4 a = red[(grp * kTiles + j) * 32 + lane];
+                for (int s = 1; s < KS; ++s) {
+                    const float4 b = red[((s * kGroups + grp) * kTiles + j) * 32 + lane];
+                    a.x += b.x;
+                    a.y += b.y;
+                    a.z += b.z;
+                    a.w += b.w;
+                }
+                const float v[4] = {a.x, a.y, a.z, a.w};
+                emit_tile(m, t, v);
+            }
+    }
+    epi.finish();
+}
+
 // The same product for tall N (the LM head) with KS = 1: a persistent grid
 // whose CTA stages the activation rows once and then walks row tiles
 // blockIdx.x, blockIdx.x + gridDim.x, ...  Each warp's weight stream runs
@@ -412,6 +575,8 @@ __global__ void __launch_bounds__(kThreads) k_bgemm_q8_tiles(Pro pro, int B, int
 #pragma unroll
     for (int i = 0; i < DEPTH; ++i)
         if (i < total) load_block<NTW>(Q, D, N, K, step_n0(i), gi, ti, (i % nb) * 32, wq[i]);
+    pdl_launch_dependents();
+    pdl_wait();  // the activation rows come from the previous kernel
     epi.start(0, 0, B);
     if (tid == 0) {
         mbar_init(bar, 1);

@@ -111,6 +111,17 @@ __device__ __forceinline__ void argmax_merge(float& v, int& i, float ov, int oi)
     if (take) { v = ov; i = oi; }
 }
 
+// Programmatic dependent launch (a kernel launched with the programmatic
+// stream-serialisation attribute may start before the previous kernel of
+// the stream ends): pdl_wait() blocks until the previous kernel has
+// completed and its writes are visible -- every read of data that kernel
+// produces, and every write to data it reads, comes after it.
+// pdl_launch_dependents() lets the next kernel of the stream be scheduled
+// once every CTA of this one has issued it (or exited).  Without the
+// attribute both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // SiLU(z) = z / (1 + e^-z) (hidden_act "silu").
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 

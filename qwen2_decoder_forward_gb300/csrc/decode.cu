@@ -4,6 +4,8 @@
 // the residual add, fused RMSNorm + gate/up + SiLU*up, and the LM head fused
 // with a two-stage block argmax.  Also the unfused variants the
 // QWEN2_FLAG_NO_FUSE_* flags select.
+#include <utility>
+
 #include "attn.cuh"
 #include "bgemm.cuh"
 #include "ctx.h"
@@ -453,6 +455,8 @@ __global__ void __launch_bounds__(kThreads) k_norm_split(float* __restrict__ x, 
                                                          const float* __restrict__ w, float eps,
                                                          float* __restrict__ out, __half* __restrict__ hi,
                                                          __half* __restrict__ lo) {
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ float red[kWarps];
     const int b = blockIdx.x;
     float* xr = x + (size_t)b * H;
@@ -889,14 +893,35 @@ cudaError_t decode_nb(Ctx& c, int B, bool want_logits, cudaStream_t st) {
 // kQ8DownKc columns (one wave of about 150 CTAs at the 0.5B shape), reduced
 // into the residual by the last CTA of each row group; LM head 256 rows per
 // CTA.  QKV and gate/up normalise their input rows themselves.
+// Launch with programmatic stream serialisation: the kernel may start
+// while the previous kernel of the stream drains; it calls pdl_wait()
+// before touching anything that kernel writes or reads.
+template <class... KArgs, class... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+template <int MT, int NTW, int KS>
+constexpr int bgemm_rows_cta() { return (bg::kWarps / KS) * NTW * 8; }
+
 template <int MT, int NTW, int KS, class Epi, class Pro>
 cudaError_t bgemm(const Ctx& c, const Pro& pro, int B, int K, int kc_len, const DevMat& W, int N, const Epi& e,
                   cudaStream_t st) {
-    constexpr int rows_cta = (bg::kWarps / KS) * NTW * 8;
+    constexpr int rows_cta = bgemm_rows_cta<MT, NTW, KS>();
     const dim3 grid((N + rows_cta - 1) / rows_cta, (K + kc_len - 1) / kc_len);
-    bg::k_bgemm_q8<MT, NTW, KS, Epi, Pro><<<grid, bg::kThreads, bg::smem_bytes(MT, kc_len), st>>>(
-        pro, B, K, kc_len, W.q, W.d, N, e, c.err);
-    return cudaGetLastError();
+    return launch_pdl(bg::k_bgemm_q8s<MT, NTW, KS, Epi, Pro>, grid, dim3(bg::kThreads),
+                      bg::smem_bytes_s(MT, kc_len, rows_cta), st, pro, B, K, kc_len, W.q, W.d, N, e, c.err);
 }
 
 constexpr int kDownNtw = 2, kDownKs = 2;
@@ -962,9 +987,9 @@ cudaError_t attn_batched(const Ctx& c, const StepArgs& a, int l, cudaStream_t st
         }
     }
     const int grid = 2 * c.n_sm;
-    k_attn_flash<<<grid, fd::kThreads, fd::kSmemBytes, st>>>(c.kvmap, f);
-    k_attn_merge<<<a.B * a.nkv, kMergeThreads, 0, st>>>(f, grid);
-    return cudaGetLastError();
+    cudaError_t e = launch_pdl(k_attn_flash, dim3(grid), dim3(fd::kThreads), fd::kSmemBytes, st, c.kvmap, f);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(k_attn_merge, dim3(a.B * a.nkv), dim3(kMergeThreads), 0, st, f, grid);
 }
 
 template <int MT>
@@ -989,8 +1014,9 @@ cudaError_t lm_head_q8(Ctx& c, float* x, int B, float* logits, int* ids, float* 
                        cudaStream_t st) {
     const int H = c.cfg.hidden;
     Workspace& w = c.ws;
-    k_norm_split<<<B, kThreads, 0, st>>>(x, nullptr, 0, 0, H, c.final_norm, c.cfg.rms_eps, hidden, w.q8_ah,
-                                         w.q8_al);
+    cudaError_t le = launch_pdl(k_norm_split, dim3(B), dim3(kThreads), 0, st, x, (const float*)nullptr, 0, 0, H,
+                                c.final_norm, c.cfg.rms_eps, hidden, w.q8_ah, w.q8_al);
+    if (le != cudaSuccess) return le;
     EpiLmQ8 e{};
     e.logits = logits;
     e.V = c.cfg.vocab;
@@ -1017,9 +1043,9 @@ cudaError_t lm_head_q8(Ctx& c, float* x, int B, float* logits, int* ids, float* 
     // scale, far inside the 2e-2 bound, for half the tensor work.
     const int tiles = (c.cfg.vocab + bg::kWarps * kLmNtw * 8 - 1) / (bg::kWarps * kLmNtw * 8);
     const int grid = tiles < c.n_sm ? tiles : c.n_sm;
-    bg::k_bgemm_q8_tiles<MT, kLmNtw, EpiLmQ8, bg::ProCopy, false><<<grid, bg::kThreads, bg::smem_bytes(MT, H), st>>>(
-        bg::ProCopy{w.q8_ah, w.q8_al}, B, H, c.lm_head.q, c.lm_head.d, c.cfg.vocab, e, c.err);
-    return cudaGetLastError();
+    return launch_pdl(bg::k_bgemm_q8_tiles<MT, kLmNtw, EpiLmQ8, bg::ProCopy, false>, dim3(grid), dim3(bg::kThreads),
+                      bg::smem_bytes(MT, H), st, bg::ProCopy{w.q8_ah, w.q8_al}, B, H, c.lm_head.q, c.lm_head.d,
+                      c.cfg.vocab, e, c.err);
 }
 
 template <int MT>
@@ -1157,10 +1183,11 @@ cudaError_t decode_set_smem_limits(int max_bytes) {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(k_attn_decode<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)sizeof(AttnSmemT<128>));
-#define Q2_BG(MT, NTW, KS, EPI, PRO)                                                                          \
-    if (e == cudaSuccess)                                                                                     \
-        e = cudaFuncSetAttribute(bg::k_bgemm_q8<MT, NTW, KS, EPI, PRO>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                                 (int)bg::smem_bytes(MT, bg::kKc));
+#define Q2_BG(MT, NTW, KS, EPI, PRO)                                                                     \
+    if (e == cudaSuccess)                                                                                \
+        e = cudaFuncSetAttribute(bg::k_bgemm_q8s<MT, NTW, KS, EPI, PRO>,                                \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,                            \
+                                 (int)bg::smem_bytes_s(MT, bg::kKc, bgemm_rows_cta<MT, NTW, KS>()));
 #define Q2_BGT(MT)                                                                                          \
     if (e == cudaSuccess)                                                                                   \
         e = cudaFuncSetAttribute(bg::k_bgemm_q8_tiles<MT, kLmNtw, EpiLmQ8, bg::ProCopy, false>,                     \

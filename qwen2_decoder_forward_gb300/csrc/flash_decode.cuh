@@ -205,6 +205,8 @@ __global__ void __launch_bounds__(fd::kThreads, 2)
         if (tid == 0 && blockIdx.x == 0) raise_guard(a.err, kGuardShape);
         return;
     }
+    pdl_launch_dependents();
+    pdl_wait();  // q, positions and the new keys come from the previous kernel
     if (warp == 0) {
         row_table(a, sm.base, sm.nch, sm.posv, sm.slotv);
         if (lane == 0) sm.abort = 0;
@@ -452,6 +454,8 @@ __global__ void __launch_bounds__(kMergeThreads) k_attn_merge(fd::Args a, int fl
     const int group = a.nh / a.nkv;
     const int b = blockIdx.x / a.nkv, g = blockIdx.x % a.nkv;
     if (group > kGroupMax || a.B > kMaxRows || b >= a.B) return;
+    pdl_launch_dependents();
+    pdl_wait();  // the attention's partials
     if (warp == 0) {
         row_table(a, base, nch, nullptr, nullptr);
         __syncwarp();
