@@ -58,6 +58,13 @@ extern "C" {
 #define QWEN2_WEIGHTS_Q8_0       1  /* the seven linear weights and the tied embedding / LM head held as
                                        Q8_0 blocks: 32 int8 values along K plus one f16 scale per block;
                                        quantised by the library from the f16 weights given to create */
+#define QWEN2_WEIGHTS_Q4_0       2  /* as Q8_0 with 4-bit codes: blocks of 32 along k, d = max|x| / 7,
+                                       codes clamp(round-half-away(x / d), -7, 7) + 8, two per byte
+                                       (element 2j in the low nibble), one f16 scale per block: 18
+                                       bytes per 32 weights.  Named beside Q8_0 as the tied output
+                                       matmul's format on the minfer page (section 3), never defined
+                                       there: the four-bit counterpart of the Q8_0 reading.  Runs the
+                                       same paths as Q8_0 (batched decode, f32 prefill) */
 
 /* ---- prefill arithmetic -------------------------------------------------- */
 #define QWEN2_PREFILL_F32        0  /* f32 activations, f32 accumulation on CUDA cores */
@@ -329,6 +336,13 @@ int qwen2_lm_head_argmax_noalloc(const uint16_t *embed, const float *hidden, int
  * q: int8 [rows][k]; d: f16 bits [rows][k/32].  Needs no GPU.  The format
  * is named, not defined, on the minfer page (sections 3 and 6). */
 int qwen2_quantize_q8_0(const uint16_t *w, int64_t rows, int64_t k, int8_t *q, uint16_t *d);
+
+/* Host-only Q4_0 quantisation of an f16 matrix [rows][k] (k a multiple of
+ * 32), as the library's packer does it (QWEN2_WEIGHTS_Q4_0): packed:
+ * uint8 [rows][k/2], element 2j in the low nibble of byte j; d: f16 bits
+ * [rows][k/32].  Needs no GPU.  QWEN2_E_ARG for null pointers or a ragged
+ * k. */
+int qwen2_quantize_q4_0(const uint16_t *w, int64_t rows, int64_t k, uint8_t *packed, uint16_t *d);
 
 #ifdef __cplusplus
 }

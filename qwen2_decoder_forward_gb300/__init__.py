@@ -37,6 +37,7 @@ IM_END_ID = 151645
 
 WEIGHTS_F16 = 0
 WEIGHTS_Q8_0 = 1
+WEIGHTS_Q4_0 = 2
 PREFILL_F32 = 0
 PREFILL_TENSOR = 1
 
@@ -53,7 +54,7 @@ EXPORTS = (
     "qwen2_create", "qwen2_destroy", "qwen2_last_error", "qwen2_kv_cache",
     "qwen2_prefill", "qwen2_decode_step", "qwen2_decode_steps", "qwen2_decode_steps_stop",
     "qwen2_final_hidden", "qwen2_synchronize", "qwen2_weight_bytes",
-    "qwen2_kv_bytes_per_seq", "qwen2_quantize_q8_0", "qwen2_features", "qwen2_profile_marks",
+    "qwen2_kv_bytes_per_seq", "qwen2_quantize_q8_0", "qwen2_quantize_q4_0", "qwen2_features", "qwen2_profile_marks",
     "qwen2_lm_head_argmax_noalloc", "qwen2_test_raise_guard", "qwen2_test_stall_decode",
 )
 
@@ -132,6 +133,8 @@ def lib() -> ctypes.CDLL:
     L.qwen2_kv_bytes_per_seq.restype = i64
     L.qwen2_quantize_q8_0.argtypes = [_P, i64, i64, _P, _P]
     L.qwen2_quantize_q8_0.restype = ctypes.c_int
+    L.qwen2_quantize_q4_0.argtypes = [_P, i64, i64, _P, _P]
+    L.qwen2_quantize_q4_0.restype = ctypes.c_int
     L.qwen2_features.argtypes = [_P]
     L.qwen2_features.restype = ctypes.c_uint32
     L.qwen2_profile_marks.argtypes = [_P, _P, i64, pi32, pi32]
@@ -167,6 +170,20 @@ def quantize_q8_0(w: np.ndarray):
     if rc:
         raise Qwen2Error(rc, "qwen2_quantize_q8_0 rejected its arguments")
     return q, d.view(np.float16)
+
+
+def quantize_q4_0(w: np.ndarray):
+    """Q4_0-quantise an f16 matrix [rows, K] with the library's packer
+    (host code; needs no GPU).  Returns (packed uint8 [rows, K/2], element
+    2j in the low nibble of byte j; d f16 [rows, K/32])."""
+    w = np.ascontiguousarray(np.asarray(w, dtype=np.float16))
+    rows, k = w.shape
+    packed = np.empty((rows, k // 2), dtype=np.uint8)
+    d = np.empty((rows, k // 32), dtype=np.uint16)
+    rc = lib().qwen2_quantize_q4_0(w.ctypes.data, rows, k, packed.ctypes.data, d.ctypes.data)
+    if rc:
+        raise Qwen2Error(rc, "qwen2_quantize_q4_0 rejected its arguments")
+    return packed, d.view(np.float16)
 
 
 def lm_head_argmax_noalloc(embed, hidden, logits=None, ids=None, want_logits: bool = True, stream=None):

@@ -109,16 +109,17 @@ int validate_config(const qwen2_config* g, std::string& msg) {
         msg = "n_head must be a multiple of n_kv_head with at most 8 query heads per kv head";
         return QWEN2_E_UNSUPPORTED;
     }
-    if (g->weight_format != QWEN2_WEIGHTS_F16 && g->weight_format != QWEN2_WEIGHTS_Q8_0) {
+    if (g->weight_format != QWEN2_WEIGHTS_F16 && g->weight_format != QWEN2_WEIGHTS_Q8_0 &&
+        g->weight_format != QWEN2_WEIGHTS_Q4_0) {
         msg = "weight_format " + std::to_string(g->weight_format) + " is not supported by this build";
         return QWEN2_E_UNSUPPORTED;
     }
-    if (g->weight_format == QWEN2_WEIGHTS_Q8_0 && g->prefill_mode != QWEN2_PREFILL_F32) {
-        msg = "Q8_0 weights prefill on the f32 path only (QWEN2_PREFILL_F32)";
+    if (block_quantised(*g) && g->prefill_mode != QWEN2_PREFILL_F32) {
+        msg = "Q8_0 and Q4_0 weights prefill on the f32 path only (QWEN2_PREFILL_F32)";
         return QWEN2_E_UNSUPPORTED;
     }
-    if (g->weight_format == QWEN2_WEIGHTS_Q8_0 && g->hidden > 1024) {
-        msg = "Q8_0 weights need hidden <= 1024 (the batched product stages one activation chunk)";
+    if (block_quantised(*g) && g->hidden > 1024) {
+        msg = "Q8_0 and Q4_0 weights need hidden <= 1024 (the batched product stages one activation chunk)";
         return QWEN2_E_UNSUPPORTED;
     }
     if (g->prefill_mode != QWEN2_PREFILL_F32 && g->prefill_mode != QWEN2_PREFILL_TENSOR) {
@@ -184,7 +185,7 @@ int setup_workspace(Ctx& c) {
     A(&w.x2, (size_t)R * H);
     A(&w.q2, (size_t)R * nq);
     A(&w.ids, R);
-    if (g.weight_format == QWEN2_WEIGHTS_Q8_0) {
+    if (block_quantised(g)) {
         const size_t blocks = ((size_t)g.vocab + 255) / 256;
         const size_t rq = (size_t)c.max_rows_q8;
         A(&w.lm_val, blocks * 32);
@@ -250,7 +251,7 @@ bool use_persistent(const Ctx& c, int B) {
 
 // Sequences one decode step can carry: 8 with f16 weights (the row-dot
 // GEMV kernels), 32 with Q8_0 weights (the batched tensor-core product).
-int max_decode_batch(const Ctx& c) { return c.cfg.weight_format == QWEN2_WEIGHTS_Q8_0 ? 32 : 8; }
+int max_decode_batch(const Ctx& c) { return block_quantised(c.cfg) ? 32 : 8; }
 
 cudaError_t enqueue_step(Ctx& c, int B, bool want_logits, cudaStream_t st) {
     if (use_persistent(c, B)) return enqueue_decode_persistent(c, want_logits, st);
@@ -660,6 +661,12 @@ int64_t qwen2_kv_bytes_per_seq(const qwen2_config* g) {
 int qwen2_quantize_q8_0(const uint16_t* w, int64_t rows, int64_t k, int8_t* q, uint16_t* d) {
     if (!w || !q || !d || rows < 0 || k <= 0 || k % 32) return QWEN2_E_ARG;
     quantize_q8_0_host(w, rows, k, q, d);
+    return QWEN2_OK;
+}
+
+int qwen2_quantize_q4_0(const uint16_t* w, int64_t rows, int64_t k, uint8_t* packed, uint16_t* d) {
+    if (!w || !packed || !d || rows < 0 || k <= 0 || k % 32) return QWEN2_E_ARG;
+    quantize_q4_0_host(w, rows, k, packed, d);
     return QWEN2_OK;
 }
 

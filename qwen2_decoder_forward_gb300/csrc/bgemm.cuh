@@ -69,6 +69,20 @@ __device__ __forceinline__ uint32_t i8x2_to_h2(uint32_t w, uint32_t sel) {
     return *reinterpret_cast<const uint32_t*>(&r);
 }
 
+// Eight Q4_0 codes (a 32-bit word, element 2j in the low nibble of byte j)
+// as four exact f16 pairs of (code - 8), in element order: the nibble u
+// becomes the f16 1024 + u (exponent 10, u in the mantissa) and 1032 is
+// subtracted.
+__device__ __forceinline__ void q4x8_to_h2(uint32_t w, uint32_t (&h)[4]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t b = (w >> (8 * j)) & 0xFFu;
+        uint32_t v = (b & 0xFu) | ((b & 0xF0u) << 12) | 0x64006400u;
+        const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&v), __float2half2_rn(1032.f));
+        h[j] = *reinterpret_cast<const uint32_t*>(&r);
+    }
+}
+
 __device__ __forceinline__ uint2 ld_stream_u2(const void* p) {
     uint2 v;
     asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
@@ -99,13 +113,20 @@ __device__ __forceinline__ float h_bits_to_f(uint32_t bits) {
     return __half2float(__ushort_as_half((unsigned short)bits));
 }
 
-template <int NTW>
+// Q4: Q holds [N][K / 2] bytes of codes; the lane's 8 codes are one word.
+template <int NTW, bool Q4 = false>
 __device__ __forceinline__ void load_block(const int8_t* __restrict__ Q, const __half* __restrict__ D, int N, int K,
                                            int n0, int gi, int ti, int kg, WeightBlock (&w)[NTW]) {
 #pragma unroll
     for (int t = 0; t < NTW; ++t) {
         const int row = n0 + t * 8 + gi, rs = n0 + t * 8 + 2 * ti;
-        w[t].q = row < N ? ld_stream_u2(Q + (size_t)row * K + kg + 8 * ti) : make_uint2(0u, 0u);
+        if (Q4)
+            w[t].q = row < N ? make_uint2(__ldg(reinterpret_cast<const unsigned*>(Q + (size_t)row * (K / 2) +
+                                                                                  (kg + 8 * ti) / 2)),
+                                          0u)
+                             : make_uint2(0u, 0u);
+        else
+            w[t].q = row < N ? ld_stream_u2(Q + (size_t)row * K + kg + 8 * ti) : make_uint2(0u, 0u);
         w[t].d0 = rs < N ? ld_stream_u16(D + (size_t)rs * (K / 32) + kg / 32) : 0u;
         w[t].d1 = rs + 1 < N ? ld_stream_u16(D + (size_t)(rs + 1) * (K / 32) + kg / 32) : 0u;
     }
@@ -388,13 +409,15 @@ __global__ void __launch_bounds__(W * 32) k_bgemm_q8(Pro pro, int B, int K, int 
 // stream is in flight while the previous kernel drains and while the
 // activation rows are staged.  The arithmetic is k_bgemm_q8's: the same
 // fragments, the same block order per warp, the same k-split reduction.
-__host__ __device__ constexpr int wrow_ld(int kc) { return kc + 32; }
-__host__ __device__ constexpr size_t smem_bytes_s(int mt, int kc, int rows_cta) {
-    return (size_t)2 * (mt * 16) * row_ld(kc) * 2 + (size_t)rows_cta * wrow_ld(kc) +
+// Q4_0 tiles hold kc / 2 bytes a row at stride kc / 2 + 16 (the 8 rows x
+// 4 lanes of a 32-bit fragment load then fall on 32 distinct banks).
+__host__ __device__ constexpr int wrow_ld(int kc, bool q4 = false) { return q4 ? kc / 2 + 16 : kc + 32; }
+__host__ __device__ constexpr size_t smem_bytes_s(int mt, int kc, int rows_cta, bool q4 = false) {
+    return (size_t)2 * (mt * 16) * row_ld(kc) * 2 + (size_t)rows_cta * wrow_ld(kc, q4) +
            (size_t)rows_cta * (kc / 32) * 2 + 64;
 }
 
-template <int MT, int NTW, int KS, class Epi, class Pro, int W = kWarps>
+template <int MT, int NTW, int KS, class Epi, class Pro, bool Q4 = false, int W = kWarps>
 __global__ void __launch_bounds__(W * 32) k_bgemm_q8s(Pro pro, int B, int K, int kc_len,
                                                       const int8_t* __restrict__ Q, const __half* __restrict__ D,
                                                       int N, Epi epi, int* err) {
@@ -404,7 +427,8 @@ __global__ void __launch_bounds__(W * 32) k_bgemm_q8s(Pro pro, int B, int K, int
     constexpr int kGroups = W / KS;
     constexpr int kRowsCta = kGroups * NTW * 8;
     static_assert(W % KS == 0, "KS divides the warps");
-    const int ld = row_ld(kc_len), wld = wrow_ld(kc_len);
+    const int ld = row_ld(kc_len), wld = wrow_ld(kc_len, Q4);
+    constexpr int kEpb = Q4 ? 2 : 1;  // weights per byte
     __half* ah = reinterpret_cast<__half*>(smem);
     __half* al = ah + kRows * ld;
     int8_t* wq = reinterpret_cast<int8_t*>(al + kRows * ld);
@@ -433,13 +457,14 @@ __global__ void __launch_bounds__(W * 32) k_bgemm_q8s(Pro pro, int B, int K, int
     // The weight tile: one bulk copy per row (16-byte aligned: K, kc0 and kc
     // are multiples of 32), completion counted on bar[1].
     if (warp == 0) {
-        if (lane == 0) mbar_expect_tx(&bar[1], (unsigned)(rows * kc));
+        if (lane == 0) mbar_expect_tx(&bar[1], (unsigned)(rows * (kc / kEpb)));
         __syncwarp();
         for (int r = lane; r < rows; r += 32)
             asm volatile(
                 "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                     smem_addr(wq + (size_t)r * wld)),
-                "l"(Q + (size_t)(n_cta0 + r) * K + kc0), "r"((unsigned)kc), "r"(smem_addr(&bar[1]))
+                "l"(Q + (size_t)(n_cta0 + r) * (K / kEpb) + kc0 / kEpb), "r"((unsigned)(kc / kEpb)),
+                "r"(smem_addr(&bar[1]))
                 : "memory");
     }
     for (int e = tid; e < rows * nb; e += W * 32) {
@@ -466,11 +491,18 @@ __global__ void __launch_bounds__(W * 32) k_bgemm_q8s(Pro pro, int B, int K, int
             float dsc[NTW][2];
 #pragma unroll
             for (int t = 0; t < NTW; ++t) {
-                const uint2 q = *reinterpret_cast<const uint2*>(wq + (size_t)(r0 + t * 8 + gi) * wld + kb * 32 + 8 * ti);
-                bw[t][0] = i8x2_to_h2(q.x, 0x4140u);
-                bw[t][1] = i8x2_to_h2(q.x, 0x4342u);
-                bw[t][2] = i8x2_to_h2(q.y, 0x4140u);
-                bw[t][3] = i8x2_to_h2(q.y, 0x4342u);
+                if (Q4) {
+                    const uint32_t q = *reinterpret_cast<const uint32_t*>(wq + (size_t)(r0 + t * 8 + gi) * wld +
+                                                                          kb * 16 + 4 * ti);
+                    q4x8_to_h2(q, bw[t]);
+                } else {
+                    const uint2 q =
+                        *reinterpret_cast<const uint2*>(wq + (size_t)(r0 + t * 8 + gi) * wld + kb * 32 + 8 * ti);
+                    bw[t][0] = i8x2_to_h2(q.x, 0x4140u);
+                    bw[t][1] = i8x2_to_h2(q.x, 0x4342u);
+                    bw[t][2] = i8x2_to_h2(q.y, 0x4140u);
+                    bw[t][3] = i8x2_to_h2(q.y, 0x4342u);
+                }
                 dsc[t][0] = h_bits_to_f(wd[(r0 + t * 8 + 2 * ti) * nbl + kb]);
                 dsc[t][1] = h_bits_to_f(wd[(r0 + t * 8 + 2 * ti + 1) * nbl + kb]);
             }
@@ -551,7 +583,7 @@ __global__ void __launch_bounds__(W * 32) k_bgemm_q8s(Pro pro, int B, int K, int
 // k chunk is the whole row (kc_len = K).  With LO = false only the f16 hi
 // part of the activations enters the MMAs (half the tensor work; the
 // activation then carries 11 bits, as in an f16 GEMM).
-template <int MT, int NTW, class Epi, class Pro, bool LO = true, int DEPTH = kDepth>
+template <int MT, int NTW, class Epi, class Pro, bool LO = true, bool Q4 = false, int DEPTH = kDepth>
 __global__ void __launch_bounds__(kThreads) k_bgemm_q8_tiles(Pro pro, int B, int K, const int8_t* __restrict__ Q,
                                                              const __half* __restrict__ D, int N, Epi epi, int* err) {
     using namespace sm100;
@@ -574,7 +606,7 @@ __global__ void __launch_bounds__(kThreads) k_bgemm_q8_tiles(Pro pro, int B, int
     WeightBlock wq[DEPTH][NTW];
 #pragma unroll
     for (int i = 0; i < DEPTH; ++i)
-        if (i < total) load_block<NTW>(Q, D, N, K, step_n0(i), gi, ti, (i % nb) * 32, wq[i]);
+        if (i < total) load_block<NTW, Q4>(Q, D, N, K, step_n0(i), gi, ti, (i % nb) * 32, wq[i]);
     pdl_launch_dependents();
     pdl_wait();  // the activation rows come from the previous kernel
     epi.start(0, 0, B);
@@ -603,15 +635,19 @@ __global__ void __launch_bounds__(kThreads) k_bgemm_q8_tiles(Pro pro, int B, int
 #pragma unroll
                     for (int t = 0; t < NTW; ++t) {
                         const WeightBlock& wb = wq[i][t];
-                        bw[t][0] = i8x2_to_h2(wb.q.x, 0x4140u);
-                        bw[t][1] = i8x2_to_h2(wb.q.x, 0x4342u);
-                        bw[t][2] = i8x2_to_h2(wb.q.y, 0x4140u);
-                        bw[t][3] = i8x2_to_h2(wb.q.y, 0x4342u);
+                        if (Q4) {
+                            q4x8_to_h2(wb.q.x, bw[t]);
+                        } else {
+                            bw[t][0] = i8x2_to_h2(wb.q.x, 0x4140u);
+                            bw[t][1] = i8x2_to_h2(wb.q.x, 0x4342u);
+                            bw[t][2] = i8x2_to_h2(wb.q.y, 0x4140u);
+                            bw[t][3] = i8x2_to_h2(wb.q.y, 0x4342u);
+                        }
                         dsc[t][0] = h_bits_to_f(wb.d0);
                         dsc[t][1] = h_bits_to_f(wb.d1);
                     }
                     if (s + DEPTH < total)
-                        load_block<NTW>(Q, D, N, K, step_n0(s + DEPTH), gi, ti, ((s + DEPTH) % nb) * 32, wq[i]);
+                        load_block<NTW, Q4>(Q, D, N, K, step_n0(s + DEPTH), gi, ti, ((s + DEPTH) % nb) * 32, wq[i]);
 #pragma unroll
                     for (int m = 0; m < MT; ++m) {
                         const __half* hr = ah + (m * 16 + gi) * ld + kb * 32 + 8 * ti;

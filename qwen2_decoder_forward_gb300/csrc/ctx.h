@@ -16,12 +16,19 @@ namespace qwen2 {
 
 // One linear weight in device memory.  f16: `w` is [rows][k] halves.
 // Q8_0: `q` is int8 [rows][k] and `d` the f16 scales [rows][k/32].
+// Q4_0 (q4 set): `q` holds [rows][k/2] bytes of 4-bit codes (element 2j in
+// the low nibble of byte j, code = value / scale + 8) and `d` the scales.
 struct DevMat {
     const __half* w = nullptr;
     const int8_t* q = nullptr;
     const __half* d = nullptr;
     int rows = 0, k = 0;
+    bool q4 = false;
 };
+
+// The block-quantised weight formats (Q8_0, Q4_0) run the batched product
+// path; f16 runs the row-dot GEMV kernels and the persistent kernel.
+inline bool block_quantised(const qwen2_config& g) { return g.weight_format != QWEN2_WEIGHTS_F16; }
 
 // Packed layer.  Row orders (chosen so that an output pair an epilogue needs
 // sits on adjacent rows):
@@ -191,6 +198,7 @@ cudaError_t enqueue_rows_o_ffn(Ctx& c, int layer, float* x, const float* o, int 
 // ---- pack.cu -------------------------------------------------------------------
 int pack_weights(Ctx& c, const qwen2_weights* w, std::string& err);
 void quantize_q8_0_host(const uint16_t* w, int64_t rows, int64_t k, int8_t* q, uint16_t* d);
+void quantize_q4_0_host(const uint16_t* w, int64_t rows, int64_t k, uint8_t* packed, uint16_t* d);
 int build_rope_table(Ctx& c, std::string& err);
 
 // Records the message of a failed call made without a context; read back

@@ -56,18 +56,27 @@ __global__ void __launch_bounds__(kThreads) k_embed_f16(StepArgs a, const __half
     for (int j = threadIdx.x; j < a.H; j += blockDim.x) a.x[(size_t)b * a.H + j] = __half2float(row[j]);
 }
 
-// Q8_0 embedding row: x[b][j] = f32(d[t][j / 32]) * q[t][j].
+// Q8_0 embedding row: x[b][j] = f32(d[t][j / 32]) * q[t][j]; Q4_0 (q4):
+// x[b][j] = f32(d[t][j / 32]) * (code - 8), code the nibble j % 2 of byte
+// j / 2 of row t.
 __global__ void __launch_bounds__(kThreads) k_embed_q8(StepArgs a, const int8_t* __restrict__ Eq,
-                                                       const __half* __restrict__ Ed) {
+                                                       const __half* __restrict__ Ed, int q4) {
     const int b = blockIdx.x;
     int t = a.tok[b];
     if (t < 0 || t >= a.V) {
         if (threadIdx.x == 0) raise_guard(a.err, kGuardToken);
         t = 0;
     }
-    for (int j = threadIdx.x; j < a.H; j += blockDim.x)
-        a.x[(size_t)b * a.H + j] =
-            __half2float(Ed[(size_t)t * (a.H / 32) + j / 32]) * (float)Eq[(size_t)t * a.H + j];
+    for (int j = threadIdx.x; j < a.H; j += blockDim.x) {
+        float v;
+        if (q4) {
+            const unsigned byte = (unsigned char)Eq[(size_t)t * (a.H / 2) + j / 2];
+            v = (float)((int)((j & 1) ? byte >> 4 : byte & 0xFu) - 8);
+        } else {
+            v = (float)Eq[(size_t)t * a.H + j];
+        }
+        a.x[(size_t)b * a.H + j] = __half2float(Ed[(size_t)t * (a.H / 32) + j / 32]) * v;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -920,6 +929,10 @@ cudaError_t bgemm(const Ctx& c, const Pro& pro, int B, int K, int kc_len, const 
                   cudaStream_t st) {
     constexpr int rows_cta = bgemm_rows_cta<MT, NTW, KS>();
     const dim3 grid((N + rows_cta - 1) / rows_cta, (K + kc_len - 1) / kc_len);
+    if (W.q4)
+        return launch_pdl(bg::k_bgemm_q8s<MT, NTW, KS, Epi, Pro, true>, grid, dim3(bg::kThreads),
+                          bg::smem_bytes_s(MT, kc_len, rows_cta, true), st, pro, B, K, kc_len, W.q, W.d, N, e,
+                          c.err);
     return launch_pdl(bg::k_bgemm_q8s<MT, NTW, KS, Epi, Pro>, grid, dim3(bg::kThreads),
                       bg::smem_bytes_s(MT, kc_len, rows_cta), st, pro, B, K, kc_len, W.q, W.d, N, e, c.err);
 }
@@ -974,7 +987,7 @@ cudaError_t attn_batched(const Ctx& c, const StepArgs& a, int l, cudaStream_t st
     // norms) and the next layer's Q/K/V, contiguous in the packed blob.
     f.pf = nullptr;
     f.pf_bytes = 0;
-    if (c.cfg.weight_format == QWEN2_WEIGHTS_Q8_0) {
+    if (block_quantised(c.cfg)) {
         const DevLayer& L = c.layers[l];
         const unsigned char* b0 = reinterpret_cast<const unsigned char*>(L.wo.q);
         const unsigned char* b1 = l + 1 < c.cfg.n_layer
@@ -1043,6 +1056,10 @@ cudaError_t lm_head_q8(Ctx& c, float* x, int B, float* logits, int* ids, float* 
     // scale, far inside the 2e-2 bound, for half the tensor work.
     const int tiles = (c.cfg.vocab + bg::kWarps * kLmNtw * 8 - 1) / (bg::kWarps * kLmNtw * 8);
     const int grid = tiles < c.n_sm ? tiles : c.n_sm;
+    if (c.lm_head.q4)
+        return launch_pdl(bg::k_bgemm_q8_tiles<MT, kLmNtw, EpiLmQ8, bg::ProCopy, false, true>, dim3(grid),
+                          dim3(bg::kThreads), bg::smem_bytes(MT, H), st, bg::ProCopy{w.q8_ah, w.q8_al}, B, H,
+                          c.lm_head.q, c.lm_head.d, c.cfg.vocab, e, c.err);
     return launch_pdl(bg::k_bgemm_q8_tiles<MT, kLmNtw, EpiLmQ8, bg::ProCopy, false>, dim3(grid), dim3(bg::kThreads),
                       bg::smem_bytes(MT, H), st, bg::ProCopy{w.q8_ah, w.q8_al}, B, H, c.lm_head.q, c.lm_head.d,
                       c.cfg.vocab, e, c.err);
@@ -1051,7 +1068,7 @@ cudaError_t lm_head_q8(Ctx& c, float* x, int B, float* logits, int* ids, float* 
 template <int MT>
 cudaError_t decode_q8(Ctx& c, int B, bool want_logits, cudaStream_t st) {
     StepArgs a = make_step_args(c, B, c.ds.tok, c.ds.pos, c.ds.slot, c.ws.x);
-    k_embed_q8<<<B, kThreads, 0, st>>>(a, c.embed.q, c.embed.d);
+    k_embed_q8<<<B, kThreads, 0, st>>>(a, c.embed.q, c.embed.d, c.embed.q4 ? 1 : 0);
     for (int l = 0; l < c.cfg.n_layer; ++l) {
         cudaError_t e = layer_q8<MT>(c, a, l, st);
         if (e != cudaSuccess) return e;
@@ -1082,7 +1099,7 @@ cudaError_t rows_o_ffn_nb(Ctx& c, int l, float* x, const float* o, int B, cudaSt
 
 cudaError_t enqueue_rows_o_ffn(Ctx& c, int layer, float* x, const float* o, int rows, cudaStream_t st) {
     const int H = c.cfg.hidden, nq = c.cfg.n_head * c.cfg.head_dim;
-    if (c.cfg.weight_format == QWEN2_WEIGHTS_Q8_0) {
+    if (block_quantised(c.cfg)) {
         for (int b0 = 0; b0 < rows; b0 += 32) {
             const int nb = rows - b0 < 32 ? rows - b0 : 32;
             cudaError_t e = nb <= 16 ? rows_o_ffn_q8<1>(c, layer, x + (size_t)b0 * H, o + (size_t)b0 * nq, nb, st)
@@ -1109,7 +1126,7 @@ cudaError_t enqueue_lm_head(Ctx& c, const float* xin, int B, float* logits, int*
                             cudaStream_t st) {
     const int H = c.cfg.hidden;
     const size_t V = (size_t)c.cfg.vocab;
-    if (c.cfg.weight_format == QWEN2_WEIGHTS_Q8_0) {
+    if (block_quantised(c.cfg)) {
         if (decode && B > 32) return cudaErrorInvalidValue;
         for (int b0 = 0; b0 < B; b0 += 32) {
             const int nb = B - b0 < 32 ? B - b0 : 32;
@@ -1142,7 +1159,7 @@ cudaError_t enqueue_lm_head(Ctx& c, const float* xin, int B, float* logits, int*
 }
 
 cudaError_t enqueue_decode_step(Ctx& c, int B, bool want_logits, cudaStream_t st) {
-    if (c.cfg.weight_format == QWEN2_WEIGHTS_Q8_0) {
+    if (block_quantised(c.cfg)) {
         if (B <= 16) return decode_q8<1>(c, B, want_logits, st);
         if (B <= 32) return decode_q8<2>(c, B, want_logits, st);
         return cudaErrorInvalidValue;
@@ -1187,10 +1204,17 @@ cudaError_t decode_set_smem_limits(int max_bytes) {
     if (e == cudaSuccess)                                                                                \
         e = cudaFuncSetAttribute(bg::k_bgemm_q8s<MT, NTW, KS, EPI, PRO>,                                \
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,                            \
-                                 (int)bg::smem_bytes_s(MT, bg::kKc, bgemm_rows_cta<MT, NTW, KS>()));
+                                 (int)bg::smem_bytes_s(MT, bg::kKc, bgemm_rows_cta<MT, NTW, KS>()));    \
+    if (e == cudaSuccess)                                                                                \
+        e = cudaFuncSetAttribute(bg::k_bgemm_q8s<MT, NTW, KS, EPI, PRO, true>,                          \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,                            \
+                                 (int)bg::smem_bytes_s(MT, bg::kKc, bgemm_rows_cta<MT, NTW, KS>(), true));
 #define Q2_BGT(MT)                                                                                          \
     if (e == cudaSuccess)                                                                                   \
         e = cudaFuncSetAttribute(bg::k_bgemm_q8_tiles<MT, kLmNtw, EpiLmQ8, bg::ProCopy, false>,                     \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bg::smem_bytes(MT, bg::kKc)); \
+    if (e == cudaSuccess)                                                                                   \
+        e = cudaFuncSetAttribute(bg::k_bgemm_q8_tiles<MT, kLmNtw, EpiLmQ8, bg::ProCopy, false, true>,               \
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bg::smem_bytes(MT, bg::kKc));
     Q2_BGT(1) Q2_BGT(2)
 #undef Q2_BGT
@@ -1198,8 +1222,7 @@ cudaError_t decode_set_smem_limits(int max_bytes) {
     Q2_BG(MT, 1, 8, EpiQkvQ8, bg::ProNorm)                    \
     Q2_BG(MT, 1, 8, EpiResidualQ8, bg::ProCopy)               \
     Q2_BG(MT, 4, 4, EpiSwigluQ8, bg::ProNorm)                 \
-    Q2_BG(MT, kDownNtw, kDownKs, EpiDownQ8, bg::ProCopy)      \
-    Q2_BG(MT, kLmNtw, 1, EpiLmQ8, bg::ProCopy)
+    Q2_BG(MT, kDownNtw, kDownKs, EpiDownQ8, bg::ProCopy)
     Q2_BG_MT(1) Q2_BG_MT(2)
 #undef Q2_BG_MT
 #undef Q2_BG

@@ -42,7 +42,17 @@ DevMat put_mat(Blob& b, int rows, int k, int fmt, RowSrc row_src) {
     DevMat m;
     m.rows = rows;
     m.k = k;
-    if (fmt == QWEN2_WEIGHTS_Q8_0) {
+    if (fmt == QWEN2_WEIGHTS_Q4_0) {
+        char* dq;
+        uint8_t* hq = reinterpret_cast<uint8_t*>(b.take((size_t)rows * (k / 2), &dq));
+        char* dd;
+        uint16_t* hd = reinterpret_cast<uint16_t*>(b.take((size_t)rows * (k / 32) * 2, &dd));
+        for (int r = 0; r < rows; ++r)
+            quantize_q4_0_host(row_src(r), 1, k, hq + (size_t)r * (k / 2), hd + (size_t)r * (k / 32));
+        m.q = reinterpret_cast<const int8_t*>(dq);
+        m.d = reinterpret_cast<const __half*>(dd);
+        m.q4 = true;
+    } else if (fmt == QWEN2_WEIGHTS_Q8_0) {
         char* dq;
         int8_t* hq = reinterpret_cast<int8_t*>(b.take((size_t)rows * k, &dq));
         char* dd;
@@ -98,6 +108,33 @@ void quantize_q8_0_host(const uint16_t* w, int64_t rows, int64_t k, int8_t* q, u
     }
 }
 
+// Q4_0 (the four-bit counterpart of the Q8_0 reading): blocks of 32 along
+// k; d = max|x| / 7 in f32; c = clamp(round-half-away(x / d), -7, 7) (c = 0
+// where d = 0), stored as the nibble c + 8, element 2j in the low nibble of
+// byte j; the stored scale is f16(d), round to nearest even.
+void quantize_q4_0_host(const uint16_t* w, int64_t rows, int64_t k, uint8_t* packed, uint16_t* d) {
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t b = 0; b < k / 32; ++b) {
+            const uint16_t* x = w + r * k + b * 32;
+            float amax = 0.f;
+            for (int e = 0; e < 32; ++e) amax = fmaxf(amax, fabsf(h2f(x[e])));
+            const float dd = amax / 7.0f;
+            uint8_t* pp = packed + r * (k / 2) + b * 16;
+            for (int e = 0; e < 32; e += 2) {
+                int c[2] = {0, 0};
+                for (int i = 0; i < 2; ++i) {
+                    if (dd == 0.f) continue;
+                    float v = roundf(h2f(x[e + i]) / dd);  // half away from zero
+                    v = fminf(7.f, fmaxf(-7.f, v));
+                    c[i] = (int)v;
+                }
+                pp[e / 2] = (uint8_t)((c[0] + 8) | ((c[1] + 8) << 4));
+            }
+            d[r * (k / 32) + b] = f2h(dd);
+        }
+    }
+}
+
 int pack_weights(Ctx& c, const qwen2_weights* w, std::string& err) {
     const qwen2_config& g = c.cfg;
     const int H = g.hidden, I = g.intermediate, V = g.vocab, hd = g.head_dim;
@@ -108,7 +145,10 @@ int pack_weights(Ctx& c, const qwen2_weights* w, std::string& err) {
     size_t total = 0;
     auto add = [&](size_t bytes) { total = align_up(total, 256) + bytes; };
     auto add_mat = [&](int rows, int k) {
-        if (fmt == QWEN2_WEIGHTS_Q8_0) {
+        if (fmt == QWEN2_WEIGHTS_Q4_0) {
+            add((size_t)rows * (k / 2));
+            add((size_t)rows * (k / 32) * 2);
+        } else if (fmt == QWEN2_WEIGHTS_Q8_0) {
             add((size_t)rows * k);
             add((size_t)rows * (k / 32) * 2);
         } else {

@@ -15,13 +15,23 @@ namespace {
 constexpr int kT = 256;
 constexpr int kGemvRows = 32;   // at most this many rows: o_proj and FFN as GEMVs
 
-// A weight matrix in f16 (w) or Q8_0 (q, d); see DevMat.
+// A weight matrix in f16 (w), Q8_0 (q, d) or Q4_0 (q4: q holds two codes
+// a byte); see DevMat.
 struct WMat {
     const __half* w;
     const int8_t* q;
     const __half* d;
+    int q4;
 };
-WMat wmat(const DevMat& m) { return WMat{m.w, m.q, m.d}; }
+WMat wmat(const DevMat& m) { return WMat{m.w, m.q, m.d, m.q4 ? 1 : 0}; }
+
+// Element j of row r of a block-quantised matrix with K columns: the code
+// as a signed integer (Q8_0: the int8; Q4_0: the nibble minus 8).
+__device__ __forceinline__ int wq_code(const WMat& m, size_t r, int K, int j) {
+    if (!m.q4) return m.q[r * K + j];
+    const unsigned byte = (unsigned char)m.q[r * (K / 2) + j / 2];
+    return (int)((j & 1) ? byte >> 4 : byte & 0xFu) - 8;
+}
 
 __global__ void __launch_bounds__(kT) k_embed_rows(const int* __restrict__ tok, int V, int H, WMat E,
                                                    float* __restrict__ x, int* err) {
@@ -33,7 +43,7 @@ __global__ void __launch_bounds__(kT) k_embed_rows(const int* __restrict__ tok, 
     }
     for (int j = threadIdx.x; j < H; j += blockDim.x)
         x[(size_t)r * H + j] = E.w ? __half2float(E.w[(size_t)t * H + j])
-                                   : __half2float(E.d[(size_t)t * (H / 32) + j / 32]) * (float)E.q[(size_t)t * H + j];
+                                   : __half2float(E.d[(size_t)t * (H / 32) + j / 32]) * (float)wq_code(E, t, H, j);
 }
 
 // v as an f16 pair: hi = f16(v), lo = f16(v - hi) (v - hi is exact in f32).
@@ -209,6 +219,18 @@ __global__ void __launch_bounds__(kT) k_gemm_f32(const float* __restrict__ A, WM
                 f = h2_to_f2(w.y); Ws[k8 + 2][r] = f.x; Ws[k8 + 3][r] = f.y;
                 f = h2_to_f2(w.z); Ws[k8 + 4][r] = f.x; Ws[k8 + 5][r] = f.y;
                 f = h2_to_f2(w.w); Ws[k8 + 6][r] = f.x; Ws[k8 + 7][r] = f.y;
+            } else if (W.q4) {
+                // Q4_0: 8 codes in one word, element 2j in the low nibble
+                // of byte j; the exact product of the scale and code - 8.
+                uint32_t q4 = 0x88888888u;
+                float dsc = 0.f;
+                if (n0 + r < N) {
+                    q4 = *reinterpret_cast<const uint32_t*>(W.q + (size_t)(n0 + r) * (K / 2) + (k0 + k8) / 2);
+                    dsc = __half2float(W.d[(size_t)(n0 + r) * (K / 32) + (k0 + k8) / 32]);
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    Ws[k8 + i][r] = dsc * (float)((int)((q4 >> (4 * i)) & 0xFu) - 8);
             } else {
                 uint2 q8 = make_uint2(0, 0);
                 float dsc = 0.f;

@@ -107,6 +107,24 @@ def test_q8_0_packer_rounds_half_away_like_the_oracle(L):
     np.testing.assert_array_equal(d_lib.view(np.uint16), d_orc.view(np.uint16))
 
 
+def test_q4_0_packer_matches_oracle_bytes(L):
+    """The library's Q4_0 packer and the oracle's quantiser give the same
+    nibbles and scales (reading of the unnamed format: blocks of 32 along K,
+    d = max|x| / 7, codes round-half-away(x / d) + 8, element 2j in the low
+    nibble of byte j)."""
+    rng = np.random.default_rng(4)
+    w = (0.02 * rng.standard_normal((64, 256))).astype(np.float16)
+    w[3, :32] = 0                                   # an all-zero block
+    w[5, 40] = np.float16(-1.5)                     # one dominant value
+    w[7, 64:96] = np.float16(0.25)                  # a constant block
+    w[9, :6] = [7.0, 0.5, -0.5, 2.5, -2.5, 6.5]     # d = 1: half cases
+    p_lib, d_lib = q2.quantize_q4_0(w)
+    p_orc, d_orc = oracle.quantize_q4_0(w)
+    np.testing.assert_array_equal(p_lib, p_orc)
+    np.testing.assert_array_equal(d_lib.view(np.uint16), d_orc.view(np.uint16))
+    np.testing.assert_array_equal(oracle.unpack_nibbles(p_lib)[9, :6], [15, 9, 7, 11, 5, 15])
+
+
 def test_q8_0_packer_rejects_ragged_k(L):
     w = np.zeros((2, 48), dtype=np.float16)
     q = np.empty((2, 48), dtype=np.int8)
