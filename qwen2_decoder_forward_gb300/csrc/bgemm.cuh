@@ -21,9 +21,9 @@
 // index).  A CTA of 8 warps owns kGroups x NTW x 8 consecutive weight rows;
 // warp w takes n-tile group w % kGroups and every KS-th 32-block of the
 // chunk (the KS warps of a group add their partials in a fixed order at the
-// end).  Each warp issues the loads of its first kDepth weight blocks before
-// anything else and keeps kDepth blocks in flight, so the weight stream's
-// latency is paid about once per CTA rather than once per block.  The
+// end).  The CTA's weight tile is staged in shared memory by bulk copies
+// issued before anything else (k_bgemm_q8s); the LM head's persistent tile
+// walker instead keeps kDepth blocks per warp in flight in registers.  The
 // chunk's activation rows reach shared memory through a prologue: either one
 // bulk copy per row (hi and lo, issued by the 32 lanes of warp 0 on one
 // mbarrier), or an RMSNorm of f32 rows computed in the CTA (one warp per
@@ -251,155 +251,12 @@ struct ProNorm {
 // after every pair of the CTA.
 // W warps per CTA (32 W threads).  Grid (ceil(N / rows_cta), ceil(K /
 // kc_len)), rows_cta = (W / KS) NTW 8; dynamic shared memory
-// smem_bytes(MT, kc_len); kc_len a multiple of 32, <= kKc.
+// smem_bytes_s(MT, kc_len, rows_cta, q4); kc_len a multiple of 32, <= kKc.
 // With KS > 1 the KS warps of a group exchange their partial tiles through
 // shared memory and warp ks finishes the tiles j = m NTW + t with j % KS ==
 // ks (sum over the KS partials in ks order, then the epilogue), so the
 // epilogue work is spread over all warps.
-template <int MT, int NTW, int KS, class Epi, class Pro, int W = kWarps, int DEPTH = kDepth>
-__global__ void __launch_bounds__(W * 32) k_bgemm_q8(Pro pro, int B, int K, int kc_len,
-                                                     const int8_t* __restrict__ Q, const __half* __restrict__ D,
-                                                     int N, Epi epi, int* err) {
-    using namespace sm100;
-    extern __shared__ __align__(16) unsigned char smem[];
-    constexpr int kRows = MT * 16;
-    constexpr int kGroups = W / KS;
-    static_assert(W % KS == 0, "KS divides the warps");
-    const int ld = row_ld(kc_len);
-    __half* ah = reinterpret_cast<__half*>(smem);
-    __half* al = ah + kRows * ld;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(al + kRows * ld);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int gi = lane >> 2, ti = lane & 3;
-    const int grp = warp % kGroups, ks = warp / kGroups;
-    const int n0 = blockIdx.x * (kGroups * NTW * 8) + grp * NTW * 8;
-    const int kc0 = blockIdx.y * kc_len;
-    const int kc = min(kc_len, K - kc0);
-    const int Bc = min(B, kRows);
-    const int nb = kc / 32;
-
-    // The first DEPTH weight blocks of this warp go out before anything
-    // waits.
-    WeightBlock wq[DEPTH][NTW];
-#pragma unroll
-    for (int i = 0; i < DEPTH; ++i)
-        if (ks + i * KS < nb) load_block<NTW>(Q, D, N, K, n0, gi, ti, kc0 + (ks + i * KS) * 32, wq[i]);
-
-    // Loads the epilogue needs from global memory go out now, to land in
-    // shared memory long before the epilogue (the barrier below publishes
-    // them).
-    epi.start(blockIdx.x * (kGroups * NTW * 8), kGroups * NTW * 8, B);
-    if (tid == 0) {
-        mbar_init(bar, 1);
-        mbar_init_fence();
-    }
-    __syncthreads();
-    // Rows past B are never read for a kept output (each MMA row is its own
-    // output row).
-    const bool staged = pro.stage(ah, al, ld, Bc, K, kc0, kc, bar);
-    if (!staged && lane == 0) raise_guard(err, kGuardTimeout);
-
-    float acc[MT][NTW][4];
-#pragma unroll
-    for (int m = 0; m < MT; ++m)
-#pragma unroll
-        for (int t = 0; t < NTW; ++t) acc[m][t][0] = acc[m][t][1] = acc[m][t][2] = acc[m][t][3] = 0.f;
-    if (staged) {
-        for (int kb0 = ks; kb0 < nb; kb0 += DEPTH * KS) {
-#pragma unroll
-            for (int i = 0; i < DEPTH; ++i) {
-                const int kb = kb0 + i * KS;
-                if (kb < nb) {
-                    // The weights of this block as f16 pairs, once for all m.
-                    uint32_t bw[NTW][4];
-                    float dsc[NTW][2];
-#pragma unroll
-                    for (int t = 0; t < NTW; ++t) {
-                        const WeightBlock& wb = wq[i][t];
-                        bw[t][0] = i8x2_to_h2(wb.q.x, 0x4140u);
-                        bw[t][1] = i8x2_to_h2(wb.q.x, 0x4342u);
-                        bw[t][2] = i8x2_to_h2(wb.q.y, 0x4140u);
-                        bw[t][3] = i8x2_to_h2(wb.q.y, 0x4342u);
-                        dsc[t][0] = h_bits_to_f(wb.d0);
-                        dsc[t][1] = h_bits_to_f(wb.d1);
-                    }
-                    // Refill this slot with the block DEPTH steps ahead.
-                    if (kb + DEPTH * KS < nb)
-                        load_block<NTW>(Q, D, N, K, n0, gi, ti, kc0 + (kb + DEPTH * KS) * 32, wq[i]);
-#pragma unroll
-                    for (int m = 0; m < MT; ++m) {
-                        const __half* hr = ah + (m * 16 + gi) * ld + kb * 32 + 8 * ti;
-                        const __half* lr = al + (m * 16 + gi) * ld + kb * 32 + 8 * ti;
-                        const uint4 h0 = *reinterpret_cast<const uint4*>(hr);
-                        const uint4 h1 = *reinterpret_cast<const uint4*>(hr + 8 * ld);
-                        const uint4 l0 = *reinterpret_cast<const uint4*>(lr);
-                        const uint4 l1 = *reinterpret_cast<const uint4*>(lr + 8 * ld);
-#pragma unroll
-                        for (int t = 0; t < NTW; ++t) {
-                            float p[4] = {0.f, 0.f, 0.f, 0.f};
-                            mma16816(p, h0.x, h1.x, h0.y, h1.y, bw[t][0], bw[t][1]);
-                            mma16816(p, l0.x, l1.x, l0.y, l1.y, bw[t][0], bw[t][1]);
-                            mma16816(p, h0.z, h1.z, h0.w, h1.w, bw[t][2], bw[t][3]);
-                            mma16816(p, l0.z, l1.z, l0.w, l1.w, bw[t][2], bw[t][3]);
-                            acc[m][t][0] = fmaf(dsc[t][0], p[0], acc[m][t][0]);
-                            acc[m][t][1] = fmaf(dsc[t][1], p[1], acc[m][t][1]);
-                            acc[m][t][2] = fmaf(dsc[t][0], p[2], acc[m][t][2]);
-                            acc[m][t][3] = fmaf(dsc[t][1], p[3], acc[m][t][3]);
-                        }
-                    }
-                }
-            }
-        }
-    }
-    auto emit_tile = [&](int m, int t, const float (&v)[4]) {
-        const int n = n0 + t * 8 + 2 * ti;
-        const int b0 = m * 16 + gi, b1 = b0 + 8;
-        if (n < N) {
-            if (b0 < B) epi.pair(b0, n, v[0], v[1], blockIdx.y);
-            if (b1 < B) epi.pair(b1, n, v[2], v[3], blockIdx.y);
-        }
-    };
-    if (KS == 1) {
-#pragma unroll
-        for (int m = 0; m < MT; ++m)
-#pragma unroll
-            for (int t = 0; t < NTW; ++t) emit_tile(m, t, acc[m][t]);
-    } else {
-        // Every warp parks its partial tiles; warp ks then sums tiles
-        // j % KS == ks over the group's KS warps in ks order.  Layout
-        // [ks][grp][tile][lane] of float4: each store and load of a warp is
-        // 512 contiguous bytes (no bank conflicts).
-        float4* red = reinterpret_cast<float4*>(smem);
-        constexpr int kTiles = MT * NTW;
-        __syncthreads();
-#pragma unroll
-        for (int m = 0; m < MT; ++m)
-#pragma unroll
-            for (int t = 0; t < NTW; ++t)
-                red[((ks * kGroups + grp) * kTiles + m * NTW + t) * 32 + lane] =
-                    make_float4(acc[m][t][0], acc[m][t][1], acc[m][t][2], acc[m][t][3]);
-        __syncthreads();
-#pragma unroll
-        for (int m = 0; m < MT; ++m)
-#pragma unroll
-            for (int t = 0; t < NTW; ++t) {
-                const int j = m * NTW + t;
-                if (j % KS != ks) continue;
-                float4 a = red[(grp * kTiles + j) * 32 + lane];
-                for (int s = 1; s < KS; ++s) {
-                    const float4 b = red[((s * kGroups + grp) * kTiles + j) * 32 + lane];
-                    a.x += b.x;
-                    a.y += b.y;
-                    a.z += b.z;
-                    a.w += b.w;
-                }
-                const float v[4] = {a.x, a.y, a.z, a.w};
-                emit_tile(m, t, v);
-            }
-    }
-    epi.finish();
-}
-
+//
 // The product with the CTA's whole weight tile staged in shared memory.
 // Before waiting for the previous kernel (pdl_wait), one warp issues a bulk
 // copy of each of the CTA's weight rows (kc bytes of int8 at row stride
@@ -407,8 +264,7 @@ __global__ void __launch_bounds__(W * 32) k_bgemm_q8(Pro pro, int B, int K, int 
 // fall on distinct banks) and every thread loads a share of the block
 // scales: the weights never depend on an earlier kernel, so their whole
 // stream is in flight while the previous kernel drains and while the
-// activation rows are staged.  The arithmetic is k_bgemm_q8's: the same
-// fragments, the same block order per warp, the same k-split reduction.
+// activation rows are staged.
 // Q4_0 tiles hold kc / 2 bytes a row at stride kc / 2 + 16 (the 8 rows x
 // 4 lanes of a 32-bit fragment load then fall on 32 distinct banks).
 __host__ __device__ constexpr int wrow_ld(int kc, bool q4 = false) { return q4 ? kc / 2 + 16 : kc + 32; }
