@@ -70,6 +70,14 @@ extern "C" {
 #define QWEN2_PREFILL_F32        0  /* f32 activations, f32 accumulation on CUDA cores */
 #define QWEN2_PREFILL_TENSOR     1  /* tensor-core (tcgen05) GEMMs on f16 operands with f32 accumulation;
                                        residual, norm statistics, softmax and the KV cache stay f32 */
+#define QWEN2_PREFILL_Q8_ACT     2  /* Q8_0 weights only: every product of the prefill (Q/K/V, o_proj,
+                                       gate/up, down, the LM head of the kept rows) quantises its f32
+                                       activation rows to Q8_0 blocks as the packer quantises weights,
+                                       sums each 32-block's int8 products exactly and scales the sum by
+                                       the two f16 block scales (the minfer page, section 6: the CUDA
+                                       prefill runs an int8 "MMQ" product; the details are this
+                                       library's reading).  At most 64 rows per call reach the LM head.
+                                       Decode steps keep f32 activations */
 
 /* ---- flags ------------------------------------------------------------- */
 #define QWEN2_FLAG_NO_FUSE_QKV   0x1u  /* separate norm, Q, K and V products and epilogue kernels instead of

@@ -40,6 +40,7 @@ WEIGHTS_Q8_0 = 1
 WEIGHTS_Q4_0 = 2
 PREFILL_F32 = 0
 PREFILL_TENSOR = 1
+PREFILL_Q8_ACT = 2
 
 FLAG_NO_FUSE_QKV = 0x1
 FLAG_NO_FUSE_FFN = 0x2

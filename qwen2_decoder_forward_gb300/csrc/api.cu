@@ -114,15 +114,20 @@ int validate_config(const qwen2_config* g, std::string& msg) {
         msg = "weight_format " + std::to_string(g->weight_format) + " is not supported by this build";
         return QWEN2_E_UNSUPPORTED;
     }
-    if (block_quantised(*g) && g->prefill_mode != QWEN2_PREFILL_F32) {
-        msg = "Q8_0 and Q4_0 weights prefill on the f32 path only (QWEN2_PREFILL_F32)";
+    if (g->prefill_mode == QWEN2_PREFILL_Q8_ACT && g->weight_format != QWEN2_WEIGHTS_Q8_0) {
+        msg = "QWEN2_PREFILL_Q8_ACT needs Q8_0 weights";
+        return QWEN2_E_UNSUPPORTED;
+    }
+    if (block_quantised(*g) && g->prefill_mode == QWEN2_PREFILL_TENSOR) {
+        msg = "Q8_0 and Q4_0 weights prefill on the f32 path (QWEN2_PREFILL_F32, or QWEN2_PREFILL_Q8_ACT)";
         return QWEN2_E_UNSUPPORTED;
     }
     if (block_quantised(*g) && g->hidden > 1024) {
         msg = "Q8_0 and Q4_0 weights need hidden <= 1024 (the batched product stages one activation chunk)";
         return QWEN2_E_UNSUPPORTED;
     }
-    if (g->prefill_mode != QWEN2_PREFILL_F32 && g->prefill_mode != QWEN2_PREFILL_TENSOR) {
+    if (g->prefill_mode != QWEN2_PREFILL_F32 && g->prefill_mode != QWEN2_PREFILL_TENSOR &&
+        g->prefill_mode != QWEN2_PREFILL_Q8_ACT) {
         msg = "prefill_mode " + std::to_string(g->prefill_mode) + " is not supported by this build";
         return QWEN2_E_UNSUPPORTED;
     }
@@ -196,6 +201,12 @@ int setup_workspace(Ctx& c) {
         A(&w.q8_ml, rq * I);
         A(&w.q8_part, (size_t)((I + kQ8DownKc - 1) / kQ8DownKc) * rq * H);
         A(&w.q8_cnt, (size_t)(H + 63) / 64);
+    }
+    if (g.prefill_mode == QWEN2_PREFILL_Q8_ACT) {
+        const size_t wmax = std::max({(size_t)H, (size_t)I, (size_t)nq});
+        A(&w.aq, (size_t)R * wmax);
+        A(&w.ad, (size_t)R * wmax / 32);
+        A(&w.q8a_lg, (size_t)kQ8aMaxOut * g.vocab);
     }
     if (g.prefill_mode == QWEN2_PREFILL_TENSOR) {
         A(&w.xn_h, (size_t)R * H);
@@ -400,6 +411,8 @@ int qwen2_prefill(qwen2_ctx* h, int32_t n_seq, const int32_t* seq_ids, const int
         total += n_tokens[s];
     }
     if (total > c.cfg.max_tokens) return fail(&c, QWEN2_E_ARG, "more rows than max_tokens");
+    if (c.cfg.prefill_mode == QWEN2_PREFILL_Q8_ACT && (int64_t)n_seq * n_out > kQ8aMaxOut)
+        return fail(&c, QWEN2_E_ARG, "QWEN2_PREFILL_Q8_ACT sends at most 64 rows to the LM head per call");
     const int rows = (int)total;
     if ((r = check_tokens(c, rows, tokens))) return r;
     if ((r = check_positions(c, rows, positions, 0))) return r;

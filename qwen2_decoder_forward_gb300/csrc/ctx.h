@@ -46,6 +46,8 @@ struct DevLayer {
 
 // Columns of k per CTA of the Q8_0 down product (split-k chunk).
 constexpr int kQ8DownKc = 448;
+// Rows one quantised-activation prefill may send to the LM head.
+constexpr int kQ8aMaxOut = 64;
 
 struct Workspace {
     float* x = nullptr;        // [rows][H] residual stream
@@ -84,6 +86,9 @@ struct Workspace {
     __half* o_l = nullptr;     //   its f16 remainders
     __half* mlp_h = nullptr;   // [rows][I] f16 SiLU(gate) * up (tensor prefill operand)
     int* ids = nullptr;        // [rows] prefill ids staging
+    int8_t* aq = nullptr;      // quantised prefill: activation codes [rows][max(H, I, nh*hd)]
+    __half* ad = nullptr;      //   and their block scales [rows][max(H, I, nh*hd) / 32]
+    float* q8a_lg = nullptr;   //   and the kept rows' logits [kQ8aMaxOut][V]
     float* out_logits = nullptr; // [rows_out][V] staging when the caller's logits are host memory
     size_t out_logits_rows = 0;
     int att_max_chunks = 0;

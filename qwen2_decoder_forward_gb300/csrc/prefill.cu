@@ -4,6 +4,8 @@
 // causal GQA attention over the KV cache; the tail-row cut (minfer "Qwen2 /
 // Qwen2.5 Architecture Support", section 3, "G3 tail-row optimization"); and
 // the LM head on the kept rows.
+#include <algorithm>
+
 #include "attn.cuh"
 #include "prefill.h"
 #include "rowdot.cuh"
@@ -149,6 +151,9 @@ __device__ __forceinline__ void epilogue_store(const PrefillEpi& e, int m, int n
         // Even column 2j holds gate j, column 2j+1 up j.
         if ((n & 1) == 0) e.mlp[(size_t)m * e.I + (n >> 1)] = silu_f(v) * v_next_col;
         break;
+    case kEpiLogits:
+        e.lg[(size_t)m * e.lg_ld + n] = v;
+        break;
     case kEpiQKV: {
         if (n & 1) break;
         const int kHd = e.hd;
@@ -270,6 +275,126 @@ __global__ void __launch_bounds__(kT) k_gemm_f32(const float* __restrict__ A, WM
             const int m = m0 + ty + 16 * i, n = n0 + tx + 16 * j;
             if (m < M && n < N) epilogue_store(e, m, n, acc[i][j], nxt);
         }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Quantised prefill products (QWEN2_PREFILL_Q8_ACT): activation rows in
+// Q8_0 (reading of the minfer page, section 6: the CUDA prefill's int8
+// "MMQ" product), weights in Q8_0.
+// ---------------------------------------------------------------------------
+
+// Each f32 row x[r][0..K) to Q8_0 blocks, as the weight packer quantises:
+// d = max|x| / 127 (f32), q = clamp(round-half-away(x / d), -127, 127) with
+// an f32 division by the unrounded d (q = 0 where d = 0), scale stored as
+// f16(d).  One warp per 32-block, lane = element.
+__global__ void __launch_bounds__(kT) k_quant_rows_q8(const float* __restrict__ x, int rows, int K,
+                                                      int8_t* __restrict__ q, __half* __restrict__ d) {
+    const int lane = threadIdx.x & 31;
+    const int nb = K / 32;
+    for (int blk = blockIdx.x * (kT / 32) + (threadIdx.x >> 5); blk < rows * nb; blk += gridDim.x * (kT / 32)) {
+        const int r = blk / nb, b = blk % nb;
+        const float v = x[(size_t)r * K + b * 32 + lane];
+        const float amax = warp_max(fabsf(v));
+        const float dd = amax / 127.0f;
+        int c = 0;
+        if (dd != 0.f) c = (int)fminf(127.f, fmaxf(-127.f, roundf(v / dd)));  // half away from zero
+        q[(size_t)r * K + b * 32 + lane] = (int8_t)c;
+        if (lane == 0) d[(size_t)r * nb + b] = __float2half_rn(dd);
+    }
+}
+
+// C[M][N] = sum over 32-blocks kb of (sum_32 a[m][k] w[n][k]) * da[m][kb] * dw[n][kb]:
+// each block's int8 products are summed exactly in int32 (dp4a), the
+// integer scaled by the product of the two f16 scales in f32, and the
+// blocks added in order.  128 x 128 tile, one 32-block per step; thread
+// (ty, tx) owns rows ty + 16 i and columns tx + 16 j, as k_gemm_f32.
+__global__ void __launch_bounds__(kT) k_gemm_q8a(const int8_t* __restrict__ A, const __half* __restrict__ Ad,
+                                                 WMat W, int M, int N, int K, PrefillEpi e) {
+    __shared__ int As[8][GBM + 1];   // [word of the block][row]
+    __shared__ int Ws[8][GBN + 1];
+    __shared__ float Asc[GBM], Wsc[GBN];
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    const int m0 = blockIdx.y * GBM, n0 = blockIdx.x * GBN;
+    const int nb = K / 32;
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    for (int kb = 0; kb < nb; ++kb) {
+        // 128 rows x 8 words of each operand: 1024 words, four per thread.
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int idx = tid + t * kT;
+            const int r = idx >> 3, w = idx & 7;
+            int av = 0, wv = 0;
+            if (m0 + r < M) av = *reinterpret_cast<const int*>(A + (size_t)(m0 + r) * K + kb * 32 + 4 * w);
+            if (n0 + r < N) wv = *reinterpret_cast<const int*>(W.q + (size_t)(n0 + r) * K + kb * 32 + 4 * w);
+            As[w][r] = av;
+            Ws[w][r] = wv;
+        }
+        if (tid < GBM) Asc[tid] = m0 + tid < M ? __half2float(Ad[(size_t)(m0 + tid) * nb + kb]) : 0.f;
+        else Wsc[tid - GBM] = n0 + tid - GBM < N ? __half2float(W.d[(size_t)(n0 + tid - GBM) * nb + kb]) : 0.f;
+        __syncthreads();
+        int isum[8][8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) isum[i][j] = 0;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            int a[8], b[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) a[i] = As[w][ty + 16 * i];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) b[j] = Ws[w][tx + 16 * j];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) isum[i][j] = __dp4a(a[i], b[j], isum[i][j]);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                acc[i][j] = fmaf((float)isum[i][j], Asc[ty + 16 * i] * Wsc[tx + 16 * j], acc[i][j]);
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float nxt = __shfl_down_sync(0xffffffffu, acc[i][j], 1);
+            const int m = m0 + ty + 16 * i, n = n0 + tx + 16 * j;
+            if (m < M && n < N) epilogue_store(e, m, n, acc[i][j], nxt);
+        }
+    }
+}
+
+// Greedy id of each logits row (lowest index of the maximum; NaN above
+// every number), one block per row.
+__global__ void __launch_bounds__(kT) k_argmax_rows(const float* __restrict__ lg, int V, int* __restrict__ ids) {
+    __shared__ float sv[kT / 32];
+    __shared__ int si[kT / 32];
+    const int r = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float v = -INFINITY;
+    int i = 0x7fffffff;
+    for (int n = threadIdx.x; n < V; n += kT) argmax_merge(v, i, lg[(size_t)r * V + n], n);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+        argmax_merge(v, i, ov, oi);
+    }
+    if (lane == 0) {
+        sv[warp] = v;
+        si[warp] = i;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < kT / 32; ++w) argmax_merge(v, i, sv[w], si[w]);
+        ids[r] = i;
     }
 }
 
@@ -450,7 +575,15 @@ cudaError_t enqueue_prefill(Ctx& c, int rows, int n_keep, const PrefillPlan& pla
     const qwen2_config& g = c.cfg;
     const int H = g.hidden, I = g.intermediate, nq = g.n_head * g.head_dim;
     const bool tensor = g.prefill_mode == QWEN2_PREFILL_TENSOR;
+    const bool q8a = g.prefill_mode == QWEN2_PREFILL_Q8_ACT;
     Workspace& w = c.ws;
+    // A quantised-activation product: the rows of `act` to Q8_0, then the
+    // exact int8 block sums against the Q8_0 weight matrix.
+    auto q8a_gemm = [&](const float* act, int m, int K, const DevMat& Wm, int N, const PrefillEpi& ep) {
+        const int blocks = std::min((m * (K / 32) + kT / 32 - 1) / (kT / 32), c.n_sm * 8);
+        k_quant_rows_q8<<<blocks, kT, 0, st>>>(act, m, K, w.aq, w.ad);
+        k_gemm_q8a<<<gemm_grid(m, N), kT, 0, st>>>(w.aq, w.ad, wmat(Wm), m, N, K, ep);
+    };
     k_embed_rows<<<rows, kT, 0, st>>>(w.rows_tok, g.vocab, H, wmat(c.embed), w.x, c.err);
     float* x = w.x;
     float* q = w.q;
@@ -468,6 +601,9 @@ cudaError_t enqueue_prefill(Ctx& c, int rows, int n_keep, const PrefillPlan& pla
             launch_norm_split(x, cur, H, L.attn_norm, g.rms_eps, w.xn_h, w.xn_l, st);
             cudaError_t err = tc_gemm_qkv(c, l, cur, e, st);
             if (err != cudaSuccess) return err;
+        } else if (q8a) {
+            k_norm_rows<<<cur, kT, 0, st>>>(x, H, L.attn_norm, g.rms_eps, w.xn);
+            q8a_gemm(w.xn, cur, H, L.wqkv, c.nqkv, e);
         } else {
             k_norm_rows<<<cur, kT, 0, st>>>(x, H, L.attn_norm, g.rms_eps, w.xn);
             k_gemm_f32<<<gemm_grid(cur, c.nqkv), kT, 0, st>>>(w.xn, wmat(L.wqkv), cur, c.nqkv, H, e);
@@ -506,7 +642,15 @@ cudaError_t enqueue_prefill(Ctx& c, int rows, int n_keep, const PrefillPlan& pla
             else
                 k_attn_prefill<64><<<dim3(g.n_kv_head, n_blk), kT, attn_prefill_smem<64>(), st>>>(aa, l);
         }
-        if (!tc && cur <= kGemvRows) {
+        if (q8a) {
+            e.kind = kEpiResidual;
+            q8a_gemm(w.o, cur, nq, L.wo, H, e);
+            k_norm_rows<<<cur, kT, 0, st>>>(x, H, L.ffn_norm, g.rms_eps, w.xn);
+            e.kind = kEpiSwiGLU;
+            q8a_gemm(w.xn, cur, H, L.wgu, 2 * I, e);
+            e.kind = kEpiResidual;
+            q8a_gemm(w.mlp, cur, I, L.wd, H, e);
+        } else if (!tc && cur <= kGemvRows) {
             // A few rows (the tail cut's, or a short prompt): the decode GEMV
             // kernels stream each weight once for up to 8 rows.
             cudaError_t err = enqueue_rows_o_ffn(c, l, x, w.o, cur, st);
@@ -531,6 +675,19 @@ cudaError_t enqueue_prefill(Ctx& c, int rows, int n_keep, const PrefillPlan& pla
         }
         cudaError_t err = cudaGetLastError();
         if (err != cudaSuccess) return err;
+    }
+    if (q8a) {
+        // Final RMSNorm (final_norm_output), then the LM head of the kept
+        // rows as a quantised product into logits, and the greedy ids.
+        k_norm_rows<<<n_keep, kT, 0, st>>>(x, H, c.final_norm, g.rms_eps, w.hidden);
+        PrefillEpi el{};
+        el.kind = kEpiLogits;
+        el.lg = logits_dev ? logits_dev : w.q8a_lg;
+        el.lg_ld = g.vocab;
+        el.err = c.err;
+        q8a_gemm(w.hidden, n_keep, H, c.lm_head, g.vocab, el);
+        if (ids_dev) k_argmax_rows<<<n_keep, kT, 0, st>>>(el.lg, g.vocab, ids_dev);
+        return cudaGetLastError();
     }
     return enqueue_lm_head(c, x, n_keep, logits_dev, ids_dev, false, st);
 }

@@ -5,18 +5,21 @@
 
 namespace qwen2 {
 
-enum EpiKind : int { kEpiQKV = 0, kEpiResidual = 1, kEpiSwiGLU = 2 };
+enum EpiKind : int { kEpiQKV = 0, kEpiResidual = 1, kEpiSwiGLU = 2, kEpiLogits = 3 };
 
 // What a GEMM epilogue does with output element (m, n) of a layer's product.
 //  kEpiQKV:      n indexes the packed Q/K/V rows; pairs (n, n+1) get the
 //                bias, the NeoX rotation (q, k) and go to q / the KV cache
 //  kEpiResidual: x[m][n] += value
 //  kEpiSwiGLU:   pairs (gate j, up j) -> mlp[m][j] = SiLU(gate) * up
+//  kEpiLogits:   lg[m][n] = value (the LM head of the kept rows)
 // Optional f16 copies (q_h, mlp_h) feed the tensor-core path.
 struct PrefillEpi {
     int kind;
     int H, I, nh, nkv, n_ctx, L, layer;
     int hd;  // head_dim (the QKV epilogue's head slots and RoPE pairs)
+    float* lg;  // kEpiLogits: logits [rows][lg_ld]
+    int lg_ld;
     float* x;
     float* q;
     __half* q_h;

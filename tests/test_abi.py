@@ -65,6 +65,8 @@ def _create(L, **over):
     ({"hidden": 320}, q2.QWEN2_E_UNSUPPORTED),
     ({"intermediate": 1000}, q2.QWEN2_E_UNSUPPORTED),
     ({"n_kv_head": 3}, q2.QWEN2_E_UNSUPPORTED),
+    ({"prefill_mode": 2}, q2.QWEN2_E_UNSUPPORTED),           # Q8_0 activations need Q8_0 weights
+    ({"prefill_mode": 2, "weight_format": 2}, q2.QWEN2_E_UNSUPPORTED),
     ({"n_ctx": 0}, q2.QWEN2_E_ARG),
     ({"vocab": 1}, q2.QWEN2_E_ARG),
 ])

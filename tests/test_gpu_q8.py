@@ -101,3 +101,43 @@ def test_q8_free_running_decode_steps_batch_20(q2, fmt):
         m.synchronize()
     for s in range(20):
         check_free_running(out[:, s], refs[s][1]["ids"], refs[s][1]["logits"], f"q8 seq {s}")
+
+
+@pytest.mark.parametrize("shape_name,n_out", [("toy", 1), ("ragged", 3), ("toy-mha", 2)])
+def test_quantised_prefill_matches_the_q8_0_activation_oracle(q2, shape_name, n_out):
+    """QWEN2_PREFILL_Q8_ACT (minfer page, section 6: the CUDA prefill's int8
+    product): every prefill product quantises its activation rows to Q8_0
+    and sums each 32-block's int8 products exactly; compared with
+    Qwen2Oracle(act_q8=True), which does the same in float64, on two
+    sequences (a 128-row tile and a ragged tail), n_out rows kept each, and
+    a third call with every row kept (no tail cut)."""
+    shape = synth.SHAPES[shape_name]
+    w = synth.make_weights(shape, 0)
+    n_ctx = 192
+    orc = oracle.build_oracle(shape, w, n_ctx, weight_format="q8_0", act_q8=True)
+    prompts = [synth.make_tokens(shape.vocab, 37, 41), synth.make_tokens(shape.vocab, 150, 42)]
+    refs = [orc.forward(orc.new_cache(), p, np.arange(len(p)), n_out=n_out) for p in prompts]
+    full = synth.make_tokens(shape.vocab, 40, 43)
+    fref = orc.forward(orc.new_cache(), full, np.arange(len(full)))
+    plain = oracle.build_oracle(shape, w, n_ctx, weight_format="q8_0")
+    pref = plain.forward(plain.new_cache(), prompts[0], np.arange(len(prompts[0])), n_out=n_out)
+    with q2.Qwen2Model(shape, w, n_ctx=n_ctx, max_seqs=2, max_tokens=200, weight_format=q2.WEIGHTS_Q8_0,
+                       prefill_mode=q2.PREFILL_Q8_ACT) as m:
+        logits, ids = m.prefill([0, 1], prompts, n_out=n_out)
+        lg, ig = logits.cpu().numpy(), ids.cpu().numpy()
+        hid = m.final_hidden(2 * n_out).cpu().numpy()
+        for s in range(2):
+            sl = slice(s * n_out, (s + 1) * n_out)
+            check_logits_ids(lg[sl], ig[sl], refs[s]["logits"], f"q8a prefill seq {s}")
+            check_hidden(hid[sl], refs[s]["final_norm_output"], f"q8a prefill seq {s}")
+        # The activation rounding is visible: the Q8_0-activation result is
+        # not the f32-activation one.
+        assert np.abs(lg[:n_out] - pref["logits"]).max() > 1e-4
+        # Every row kept: 40 rows, no tail cut.
+        lgf, igf = m.prefill([0], [full], n_out=40)
+        check_logits_ids(lgf.cpu().numpy(), igf.cpu().numpy(), fref["logits"], "q8a prefill, no cut")
+        # At most 64 rows reach the LM head per call in this mode.
+        with pytest.raises(q2.Qwen2Error) as e:
+            m.prefill([0, 1], [full, full], n_out=33)
+        assert e.value.code == q2.QWEN2_E_ARG
+        m.synchronize()
