@@ -103,6 +103,34 @@ def test_q8_free_running_decode_steps_batch_20(q2, fmt):
         check_free_running(out[:, s], refs[s][1]["ids"], refs[s][1]["logits"], f"q8 seq {s}")
 
 
+# Tolerances of the quantised-activation prefill against the oracle's act_q8
+# forward.  A quantised code is decided by an activation that the GPU holds
+# in f32 and the oracle in f64 (rounded to f32 before quantising): where the
+# two straddle a rounding boundary the codes differ by one, and the forward
+# amplifies such flips.  Measured on the oracle itself (toy shape, a
+# 150-row prompt): perturbing every quantised activation by a relative
+# 1e-6 moves the last row's final_norm_output by 1.1e-2 rel-L2 and the
+# logits by 1.5e-2.  Layer 0's keys and values depend on no earlier
+# quantised product (the embedding, the norm, one Q/K/V product), so they
+# are held to the f32 tolerance; the end-to-end rows to these bounds.
+Q8A_LOGIT_TOL = 5e-2
+Q8A_HIDDEN_REL_L2 = 3e-2
+
+
+def _check_q8a_rows(gpu_lg, gpu_ids, gpu_hid, ref, what):
+    """Logits within Q8A_LOGIT_TOL, final_norm_output within
+    Q8A_HIDDEN_REL_L2, and the greedy id the oracle's unless the oracle's
+    logit of the GPU's id is within twice the row's |dlogit| of its max."""
+    from parity import rel_l2
+    orc_lg = np.asarray(ref["logits"], dtype=np.float64)
+    d = np.abs(np.asarray(gpu_lg, dtype=np.float64) - orc_lg).max(axis=1)
+    assert d.max() <= Q8A_LOGIT_TOL, f"{what}: max |dlogit| {d.max():.3e}"
+    for r in range(len(orc_lg)):
+        g, o = int(gpu_ids[r]), int(np.argmax(orc_lg[r].astype(np.float32)))
+        assert g == o or orc_lg[r][o] - orc_lg[r][g] <= 2 * d[r], f"{what}: row {r} id {g} vs oracle {o}"
+        assert rel_l2(gpu_hid[r], ref["final_norm_output"][r]) <= Q8A_HIDDEN_REL_L2, f"{what}: row {r} hidden"
+
+
 @pytest.mark.parametrize("shape_name,n_out", [("toy", 1), ("ragged", 3), ("toy-mha", 2)])
 def test_quantised_prefill_matches_the_q8_0_activation_oracle(q2, shape_name, n_out):
     """QWEN2_PREFILL_Q8_ACT (minfer page, section 6: the CUDA prefill's int8
@@ -110,13 +138,17 @@ def test_quantised_prefill_matches_the_q8_0_activation_oracle(q2, shape_name, n_
     and sums each 32-block's int8 products exactly; compared with
     Qwen2Oracle(act_q8=True), which does the same in float64, on two
     sequences (a 128-row tile and a ragged tail), n_out rows kept each, and
-    a third call with every row kept (no tail cut)."""
+    a third call with every row kept (no tail cut).  Layer 0's K/V rows of
+    every position are held to rel-L2 1e-3 (the quantiser and the exact
+    block sums of one product); the kept rows to the bounds above."""
+    from parity import rel_l2
     shape = synth.SHAPES[shape_name]
     w = synth.make_weights(shape, 0)
     n_ctx = 192
     orc = oracle.build_oracle(shape, w, n_ctx, weight_format="q8_0", act_q8=True)
     prompts = [synth.make_tokens(shape.vocab, 37, 41), synth.make_tokens(shape.vocab, 150, 42)]
-    refs = [orc.forward(orc.new_cache(), p, np.arange(len(p)), n_out=n_out) for p in prompts]
+    caches = [orc.new_cache() for _ in prompts]
+    refs = [orc.forward(caches[i], p, np.arange(len(p)), n_out=n_out) for i, p in enumerate(prompts)]
     full = synth.make_tokens(shape.vocab, 40, 43)
     fref = orc.forward(orc.new_cache(), full, np.arange(len(full)))
     plain = oracle.build_oracle(shape, w, n_ctx, weight_format="q8_0")
@@ -126,16 +158,22 @@ def test_quantised_prefill_matches_the_q8_0_activation_oracle(q2, shape_name, n_
         logits, ids = m.prefill([0, 1], prompts, n_out=n_out)
         lg, ig = logits.cpu().numpy(), ids.cpu().numpy()
         hid = m.final_hidden(2 * n_out).cpu().numpy()
+        kv = m.kv_cache().cpu().numpy()
         for s in range(2):
             sl = slice(s * n_out, (s + 1) * n_out)
-            check_logits_ids(lg[sl], ig[sl], refs[s]["logits"], f"q8a prefill seq {s}")
-            check_hidden(hid[sl], refs[s]["final_norm_output"], f"q8a prefill seq {s}")
+            _check_q8a_rows(lg[sl], ig[sl], hid[sl], refs[s], f"q8a prefill seq {s}")
+            pos = np.arange(len(prompts[s]))
+            for which, arr in ((0, caches[s].K), (1, caches[s].V)):
+                g = np.transpose(kv[s, 0, which][:, pos], (1, 0, 2))
+                e = rel_l2(g, arr[0, pos])
+                assert e <= 1e-3, f"seq {s} layer-0 {'KV'[which]} rel-L2 {e:.3e}"
         # The activation rounding is visible: the Q8_0-activation result is
         # not the f32-activation one.
         assert np.abs(lg[:n_out] - pref["logits"]).max() > 1e-4
         # Every row kept: 40 rows, no tail cut.
         lgf, igf = m.prefill([0], [full], n_out=40)
-        check_logits_ids(lgf.cpu().numpy(), igf.cpu().numpy(), fref["logits"], "q8a prefill, no cut")
+        hf = m.final_hidden(40).cpu().numpy()
+        _check_q8a_rows(lgf.cpu().numpy(), igf.cpu().numpy(), hf, fref, "q8a prefill, no cut")
         # At most 64 rows reach the LM head per call in this mode.
         with pytest.raises(q2.Qwen2Error) as e:
             m.prefill([0, 1], [full, full], n_out=33)
