@@ -40,7 +40,6 @@ constexpr int kThreads = 256;
 constexpr int kWarps = 8;
 constexpr int kKc = 1024;   // largest k chunk
 constexpr int kDepth = 4;   // weight blocks in flight per warp
-constexpr unsigned long long kWaitNs = 2000000000ull;
 
 // Shared-memory row stride (halves) of a k chunk of kc columns: kc rounded
 // up to 64, plus 32, so consecutive rows sit 64 bytes apart modulo 128 and

@@ -16,6 +16,10 @@ enum GuardCode : int {
     kGuardTimeout = 4,      // a bounded spin-wait gave up
 };
 
+// Every spin-wait of every kernel gives up after this many ns of the global
+// timer (2 s), raises kGuardTimeout and lets its kernel finish.
+constexpr unsigned long long kWaitNs = 2000000000ull;
+
 __device__ __forceinline__ void raise_guard(int* err, int code) {
     if (err) atomicCAS(err, 0, code);
 }

@@ -51,7 +51,6 @@ constexpr int kGroupMax = 8;            // query heads per kv head
 constexpr int kPart = kDh + 2;          // partial: m, l, acc[64]
 constexpr int kHalf = kCh * 32;         // floats of one swizzled half tile (64 rows x 128 bytes)
 constexpr unsigned kUnitBytes = 4u * kHalf * 4u;  // K and V, two halves each
-constexpr unsigned long long kWaitNs = 2000000000ull;
 
 struct Args {
     const float* q;         // [B][nh][64] rotated queries

@@ -1,6 +1,7 @@
 // The persistent single-launch batch-1 decode kernel (persistent.cu).
 #pragma once
 
+#include "common.cuh"
 #include "ctx.h"
 
 namespace qwen2 {
@@ -36,7 +37,7 @@ struct PersistentArgs {
     int test_stall;              // test hook: wait on a counter nothing arrives at
 };
 
-constexpr unsigned long long kPersistWaitNs = 2000000000ull;  // a wait gives up after 2 s
+constexpr unsigned long long kPersistWaitNs = kWaitNs;  // a wait gives up after 2 s unless shortened
 
 // Profiling slots per CTA: 0 launch start; per layer l, 1 + 16 l + k with
 // k = 0 x gathered, 1 normed, 2 Q/K/V done, 3 q ready (attention CTAs),

@@ -104,10 +104,18 @@ __global__ void __launch_bounds__(kT) k_norm_rows_split_w(const float* __restric
         if (j >= H) break;
         const float4 g = *reinterpret_cast<const float4*>(w + j);
         const size_t o = (size_t)r * H + j;
-        put_split(hi, lo, o, __fmul_rn(__fmul_rn(v[i].x, s), g.x));
-        put_split(hi, lo, o + 1, __fmul_rn(__fmul_rn(v[i].y, s), g.y));
-        put_split(hi, lo, o + 2, __fmul_rn(__fmul_rn(v[i].z, s), g.z));
-        put_split(hi, lo, o + 3, __fmul_rn(__fmul_rn(v[i].w, s), g.w));
+        // The four elements' hi and lo halves, each written as one 8-byte
+        // store (a warp writes 256 contiguous bytes of each array).
+        const float n4[4] = {__fmul_rn(__fmul_rn(v[i].x, s), g.x), __fmul_rn(__fmul_rn(v[i].y, s), g.y),
+                             __fmul_rn(__fmul_rn(v[i].z, s), g.z), __fmul_rn(__fmul_rn(v[i].w, s), g.w)};
+        __align__(8) __half h4[4], l4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            h4[e] = __float2half_rn(n4[e]);
+            l4[e] = __float2half_rn(n4[e] - __half2float(h4[e]));
+        }
+        *reinterpret_cast<uint2*>(hi + o) = *reinterpret_cast<const uint2*>(h4);
+        *reinterpret_cast<uint2*>(lo + o) = *reinterpret_cast<const uint2*>(l4);
     }
 }
 

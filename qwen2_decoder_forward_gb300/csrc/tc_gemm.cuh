@@ -26,7 +26,6 @@ namespace tcg {
 constexpr int kBM = 128;          // rows of an output tile (TMEM lanes)
 constexpr int kBK = 64;           // k-block: 64 f16 = one 128-byte swizzle row
 constexpr int kThreads = 192;
-constexpr unsigned long long kWaitNs = 2000000000ull;
 
 // SPLIT: A is given as two f16 matrices, A = A_hi + A_lo (A_hi = f16(a),
 // A_lo = f16(a - A_hi)), and every k-step issues one MMA for each part into
