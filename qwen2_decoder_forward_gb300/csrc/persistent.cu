@@ -893,7 +893,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
             }
             SyncCompute::sync();  // the previous unit is done with `at`
             if (!qkv_seen) {
-                wait_cnt(l * 5 + 0);
+                // q, k and v are read as epoch-tagged packets (a unit re-polls
+                // the ones not yet written): no arrival counter to wait for,
+                // which would add an L2 round trip.
                 qkv_seen = true;
                 mark(mb + 3);
             }
@@ -937,7 +939,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArg
         {
             const u64* att = pk + lay.att;  // partials: copy 0 only
             u64* ob = a.pk + lay.o_base(L, G, l);
-            wait_cnt(l * 5 + 1);
+            // The merging CTA polls the partials' packets by epoch directly.
             mark(mb + 5);
             if (c < nh)
                 merge_head(rd, att + (size_t)c * a.max_chunks * kPartStride, n_chunks, H, ob + (size_t)c * kHd,
