@@ -186,7 +186,7 @@ int setup_workspace(Ctx& c) {
     A(&w.keep_rows, R);
     A(&w.keep_pos, R);
     A(&w.keep_slot, R);
-    A(&w.blk, (size_t)4 * R);
+    A(&w.blk, (size_t)6 * R);
     A(&w.x2, (size_t)R * H);
     A(&w.q2, (size_t)R * nq);
     A(&w.ids, R);
@@ -214,6 +214,9 @@ int setup_workspace(Ctx& c) {
         A(&w.o_h, (size_t)R * nq);
         A(&w.o_l, (size_t)R * nq);
         A(&w.mlp_h, (size_t)R * I);
+        const size_t heads = (size_t)S * g.n_kv_head, n64 = (size_t)att_ctx64(g.n_ctx);
+        A(&w.att_k, heads * n64 * g.head_dim);
+        A(&w.att_vt, heads * 2 * g.head_dim * n64);
     }
     A(&c.ds.tok, S);
     A(&c.ds.pos, S);
@@ -462,6 +465,22 @@ int qwen2_prefill(qwen2_ctx* h, int32_t n_seq, const int32_t* seq_ids, const int
     plan.insert(plan.end(), bn.begin(), bn.end());
     plan.insert(plan.end(), kb0.begin(), kb0.end());
     plan.insert(plan.end(), kbn.begin(), kbn.end());
+    // Per sequence: slot and largest position (the keys its attention reads).
+    int max_tiles = 0;
+    {
+        std::vector<int> ss(n_seq), sp(n_seq);
+        int o = 0;
+        for (int s = 0; s < n_seq; ++s) {
+            int m = 0;
+            for (int i = 0; i < n_tokens[s]; ++i) m = std::max(m, (int)positions[o + i]);
+            o += n_tokens[s];
+            ss[s] = seq_ids[s];
+            sp[s] = m;
+            max_tiles = std::max(max_tiles, m / 64 + 1);
+        }
+        plan.insert(plan.end(), ss.begin(), ss.end());
+        plan.insert(plan.end(), sp.begin(), sp.end());
+    }
     Workspace& w = c.ws;
     Q2_CHECK(&c, cudaMemcpyAsync(w.rows_tok, tokens, rows * 4, cudaMemcpyHostToDevice, st));
     Q2_CHECK(&c, cudaMemcpyAsync(w.rows_pos, positions, rows * 4, cudaMemcpyHostToDevice, st));
@@ -476,6 +495,10 @@ int qwen2_prefill(qwen2_ctx* h, int32_t n_seq, const int32_t* seq_ids, const int
     pp.kblk_row0 = w.blk + 2 * nb;
     pp.kblk_nrows = w.blk + 2 * nb + nkb;
     pp.n_kblk = nkb;
+    pp.seq_slot = w.blk + 2 * nb + 2 * nkb;
+    pp.seq_pmax = pp.seq_slot + n_seq;
+    pp.n_seq = n_seq;
+    pp.max_tiles = max_tiles;
 
     const bool logits_dev = logits && is_device_ptr(logits);
     const bool ids_dev = ids && is_device_ptr(ids);

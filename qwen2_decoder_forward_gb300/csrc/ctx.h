@@ -85,6 +85,8 @@ struct Workspace {
     __half* o_h = nullptr;     // [rows][nh*hd] f16 attention output (tensor prefill operand), and
     __half* o_l = nullptr;     //   its f16 remainders
     __half* mlp_h = nullptr;   // [rows][I] f16 SiLU(gate) * up (tensor prefill operand)
+    __half* att_k = nullptr;   // tensor prefill attention operands of one layer, per slot and kv
+    __half* att_vt = nullptr;  //   head: k as f16 [n_ctx64][hd], v transposed as f16 hi / lo [2][hd][n_ctx64]
     int* ids = nullptr;        // [rows] prefill ids staging
     int8_t* aq = nullptr;      // quantised prefill: activation codes [rows][max(H, I, nh*hd)]
     __half* ad = nullptr;      //   and their block scales [rows][max(H, I, nh*hd) / 32]
@@ -146,6 +148,7 @@ struct TcLayerMaps {
 struct TcState {
     bool ok = false;
     CUtensorMap a_xn, a_xn_lo, a_o, a_o_lo, a_mlp;   // activation operands [max_rows][K]
+    CUtensorMap att_k, att_vt;                        // attention operands (Workspace::att_k / att_vt)
     std::vector<TcLayerMaps> layers;
 };
 

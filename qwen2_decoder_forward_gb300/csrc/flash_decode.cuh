@@ -136,13 +136,7 @@ __device__ __forceinline__ uint32_t tf32_rn(float x) {
     return r;
 }
 
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            sm100::smem_addr(dst)),
-        "l"(src), "r"(bytes), "r"(sm100::smem_addr(bar))
-        : "memory");
-}
+using sm100::bulk_g2s;
 
 // Row table of a launch (warp 0 of the block): per row its position, slot
 // and chunk count (0 if the position is invalid) and its first unit.

@@ -575,7 +575,7 @@ cudaError_t prefill_set_smem_limits() {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(k_attn_prefill<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  attn_prefill_smem<128>());
-    return e == cudaSuccess ? prefill_attn_mma_set_smem() : e;
+    return e == cudaSuccess ? prefill_attn_tc_set_smem() : e;
 }
 
 cudaError_t enqueue_prefill(Ctx& c, int rows, int n_keep, const PrefillPlan& plan, float* logits_dev,
@@ -642,7 +642,7 @@ cudaError_t enqueue_prefill(Ctx& c, int rows, int n_keep, const PrefillPlan& pla
         PrefillAttnArgs aa{q, w.o, tc ? w.o_h : nullptr, w.o_l, c.kv, pos, slot, blk_row0, blk_nrows,
                            g.n_head, g.n_kv_head, g.n_ctx, g.n_layer};
         if (tc) {
-            cudaError_t err = enqueue_attn_prefill_mma(aa, l, n_blk, st);
+            cudaError_t err = enqueue_attn_prefill_tc(c, aa, plan, l, st);
             if (err != cudaSuccess) return err;
         } else {
             if (g.head_dim == 128)

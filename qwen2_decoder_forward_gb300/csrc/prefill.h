@@ -54,7 +54,14 @@ struct PrefillPlan {
     const int* kblk_row0;   // blocks over the kept rows (after the tail cut)
     const int* kblk_nrows;
     int n_kblk;
+    const int* seq_slot;    // per sequence of the call: its slot and its largest position
+    const int* seq_pmax;
+    int n_seq;
+    int max_tiles;          // max over the sequences of seq_pmax / 64 + 1
 };
+
+// Positions of the attention operand buffers rounded up to whole 64-key tiles.
+inline int att_ctx64(int n_ctx) { return (n_ctx + 63) & ~63; }
 
 constexpr int kPrefillQB = 16;   // query rows per attention block
 
@@ -68,10 +75,14 @@ cudaError_t tc_gemm_o(const Ctx& c, int layer, int M, float* x, cudaStream_t st)
 cudaError_t tc_gemm_gu(const Ctx& c, int layer, int M, cudaStream_t st);
 cudaError_t tc_gemm_down(const Ctx& c, int layer, int M, float* x, cudaStream_t st);
 
-// Causal GQA attention of the tensor-core path (prefill_attn.cu): writes
-// a.o_h / a.o_l; grid (nkv, n_blk) over the 16-row query blocks.
-cudaError_t enqueue_attn_prefill_mma(const PrefillAttnArgs& a, int layer, int n_blk, cudaStream_t st);
-cudaError_t prefill_attn_mma_set_smem();
+// Causal GQA attention of the tensor-core path on tcgen05 MMAs into tensor
+// memory (prefill_attn_tc.cu): writes a.o_h / a.o_l; grid (nkv, n_blk) over
+// the 16-row query blocks; head_dim 64, at most 8 query heads per kv head.
+// First converts the keys 0 .. seq_pmax of every sequence of the call into
+// the f16 operand buffers (Workspace::att_k / att_vt), read then by TMA.
+cudaError_t enqueue_attn_prefill_tc(const Ctx& c, const PrefillAttnArgs& a, const PrefillPlan& plan, int layer,
+                                    cudaStream_t st);
+cudaError_t prefill_attn_tc_set_smem();
 
 cudaError_t enqueue_prefill(Ctx& c, int rows, int n_keep, const PrefillPlan& plan, float* logits_dev,
                             int* ids_dev, cudaStream_t st);

@@ -109,7 +109,7 @@ struct EpiSwiGLU {
     }
 };
 
-constexpr int kBnQKV = 128, kBnO = 128, kBnGU = 256, kBnDown = 128;
+constexpr int kBnQKV = 128, kBnO = 224, kBnGU = 256, kBnDown = 224;
 // Which products take their activation operand as an f16 hi + lo pair (see
 // tc_gemm.cuh): the normed rows feeding QKV and gate/up and the attention
 // output feeding o_proj.  With a single f16 rounding of those three operands
@@ -149,6 +149,11 @@ int tc_setup(Ctx& c, std::string& why) {
               encode_kmajor_f16(&t.a_o, c.ws.o_h, R, nq, tcg::kBM) &&
               encode_kmajor_f16(&t.a_o_lo, c.ws.o_l, R, nq, tcg::kBM) &&
               encode_kmajor_f16(&t.a_mlp, c.ws.mlp_h, R, I, tcg::kBM);
+    // Attention operands: k rows [slot][kv head][position] of 64 dims, and
+    // v^T rows [slot][kv head][hi / lo][dim] of n_ctx64 keys; 64 x 64 boxes.
+    const uint64_t heads = (uint64_t)g.max_seqs * g.n_kv_head, n64 = (uint64_t)att_ctx64(g.n_ctx);
+    ok = ok && encode_kmajor_f16(&t.att_k, c.ws.att_k, heads * n64, kHdim, 64) &&
+         encode_kmajor_f16(&t.att_vt, c.ws.att_vt, heads * 2 * kHdim, n64, 64);
     t.layers.resize(g.n_layer);
     for (int l = 0; l < g.n_layer && ok; ++l) {
         const DevLayer& L = c.layers[l];

@@ -57,6 +57,16 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* b, unsigned bytes) {
                  : "memory");
 }
 
+// ---- bulk copies ---------------------------------------------------------------
+// Untiled global -> shared copy of `bytes` (a multiple of 16; both addresses
+// 16-byte aligned) that completes as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
 // ---- TMA -------------------------------------------------------------------------
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");

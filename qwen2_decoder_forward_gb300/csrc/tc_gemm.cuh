@@ -38,9 +38,12 @@ struct GemmCfg {
     static constexpr int kBBytes = BN * kBK * 2;
     static constexpr int kStageBytes = kBOff + kBBytes;
     static constexpr int kStages = (192 * 1024) / kStageBytes;
-    static constexpr uint32_t kTmemCols = 2 * BN;
+    // Two accumulators of BN columns, each at a power-of-two column offset
+    // (kAccCols apart); the allocation is a power of two as well.
+    static constexpr uint32_t kAccCols = BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
+    static constexpr uint32_t kTmemCols = 2 * kAccCols;
     static constexpr size_t kSmem = (size_t)kStages * kStageBytes + 1024 + 256;
-    static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "UMMA N for M = 128");
+    static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "UMMA N for M = 128, whole 32-column epilogue chunks");
     static_assert(kStages >= 2, "at least two stages");
 };
 
@@ -126,7 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d = tmem + (uint32_t)(acc * BN);
+                const uint32_t d = tmem + (uint32_t)acc * C::kAccCols;
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!mbar_wait(&full[s], ph, kWaitNs)) {
                         ok = false;
@@ -171,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const int row = m0 + 32 * q + lane;
-            const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
+            const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)acc * C::kAccCols;
 #pragma unroll 1
             for (int c = 0; c < BN; c += 32) {
                 float v[32];

@@ -276,6 +276,41 @@ def test_tensor_core_prefill(q2, shape_name):
         m.synchronize()
 
 
+@pytest.mark.parametrize("shape_name", ["toy", "ragged"])
+def test_tensor_core_prefill_in_chunks(q2, shape_name):
+    """Chunked prefill on the tensor-core path: the second call's rows attend
+    to keys an earlier call stored (prefixes of 70 and 31 positions, neither
+    a whole 64-key tile; n_ctx 200 is not a multiple of 64 either), against
+    the oracle run in the same chunks; KV cache rows too."""
+    shape = synth.SHAPES[shape_name]
+    w = synth.make_weights(shape, 0)
+    n_ctx = 200
+    a = synth.make_tokens(shape.vocab, 150, 21)
+    b = synth.make_tokens(shape.vocab, 100, 22)
+    cut = (70, 31)
+    orc = oracle.build_oracle(shape, w, n_ctx)
+    caches, refs = [], []
+    for t, c in zip((a, b), cut):
+        cache = orc.new_cache()
+        orc.forward(cache, t[:c], np.arange(c), n_out=1)
+        refs.append(orc.forward(cache, t[c:], np.arange(c, len(t)), n_out=2))
+        caches.append(cache)
+    with q2.Qwen2Model(shape, w, n_ctx=n_ctx, max_seqs=2, max_tokens=192,
+                       prefill_mode=q2.PREFILL_TENSOR) as m:
+        m.prefill([0, 1], [a[:cut[0]], b[:cut[1]]], n_out=1)
+        logits, ids = m.prefill([0, 1], [a[cut[0]:], b[cut[1]:]],
+                                positions=[np.arange(cut[0], len(a)), np.arange(cut[1], len(b))], n_out=2)
+        hid = m.final_hidden(4).cpu().numpy()
+        lg, ig = logits.cpu().numpy(), ids.cpu().numpy()
+        kv = m.kv_cache().cpu().numpy()
+        for s, t in enumerate((a, b)):
+            what = f"chunked tensor prefill seq {s}"
+            check_logits_ids(lg[2 * s:2 * s + 2], ig[2 * s:2 * s + 2], refs[s]["logits"], what)
+            check_hidden(hid[2 * s:2 * s + 2], refs[s]["final_norm_output"], what)
+            check_kv(kv[s], caches[s], np.arange(len(t)), what + " KV")
+        m.synchronize()
+
+
 def test_device_guard_is_reported_once_and_decoding_continues(q2):
     """Failure detection without a GPU fault: the test hook writes the
     device guard word the way a kernel's bounded wait does when it gives up.
