@@ -149,6 +149,8 @@ struct TcState {
     bool ok = false;
     CUtensorMap a_xn, a_xn_lo, a_o, a_o_lo, a_mlp;   // activation operands [max_rows][K]
     CUtensorMap att_k, att_vt;                        // attention operands (Workspace::att_k / att_vt)
+    CUtensorMap lm_e;                                 // LM head rows [V][H] in 128 x 64 boxes
+    bool lm_ok = false;                               // lm_e encoded (the tensor-core LM head serves)
     std::vector<TcLayerMaps> layers;
 };
 

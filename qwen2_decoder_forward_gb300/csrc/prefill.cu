@@ -697,6 +697,7 @@ cudaError_t enqueue_prefill(Ctx& c, int rows, int n_keep, const PrefillPlan& pla
         if (ids_dev) k_argmax_rows<<<n_keep, kT, 0, st>>>(el.lg, g.vocab, ids_dev);
         return cudaGetLastError();
     }
+    if (tensor && lm_head_tc_supported(c)) return enqueue_lm_head_tc(c, x, n_keep, logits_dev, ids_dev, st);
     return enqueue_lm_head(c, x, n_keep, logits_dev, ids_dev, false, st);
 }
 

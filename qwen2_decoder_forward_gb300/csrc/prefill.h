@@ -84,6 +84,12 @@ cudaError_t enqueue_attn_prefill_tc(const Ctx& c, const PrefillAttnArgs& a, cons
                                     cudaStream_t st);
 cudaError_t prefill_attn_tc_set_smem();
 
+// Final norm + LM head + argmax of the kept rows on tcgen05 (lm_head_tc.cu),
+// up to 8 rows per launch; f16 LM head rows, hidden a multiple of 64.
+cudaError_t lm_head_tc_setup(Ctx& c);
+bool lm_head_tc_supported(const Ctx& c);
+cudaError_t enqueue_lm_head_tc(Ctx& c, const float* xin, int B, float* logits, int* ids, cudaStream_t st);
+
 cudaError_t enqueue_prefill(Ctx& c, int rows, int n_keep, const PrefillPlan& plan, float* logits_dev,
                             int* ids_dev, cudaStream_t st);
 cudaError_t prefill_set_smem_limits();

@@ -174,6 +174,11 @@ int tc_setup(Ctx& c, std::string& why) {
         why = "cannot raise the tensor-core GEMM shared-memory limit";
         return QWEN2_E_CUDA;
     }
+    if (lm_head_tc_setup(c) != cudaSuccess) {
+        cudaGetLastError();
+        why = "cannot raise the tensor-core LM head's shared-memory limit";
+        return QWEN2_E_CUDA;
+    }
     t.ok = true;
     return QWEN2_OK;
 }
