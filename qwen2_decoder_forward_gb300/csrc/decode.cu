@@ -902,25 +902,6 @@ cudaError_t decode_nb(Ctx& c, int B, bool want_logits, cudaStream_t st) {
 // kQ8DownKc columns (one wave of about 150 CTAs at the 0.5B shape), reduced
 // into the residual by the last CTA of each row group; LM head 256 rows per
 // CTA.  QKV and gate/up normalise their input rows themselves.
-// Launch with programmatic stream serialisation: the kernel may start
-// while the previous kernel of the stream drains; it calls pdl_wait()
-// before touching anything that kernel writes or reads.
-template <class... KArgs, class... Args>
-cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                       Args&&... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    at[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
-}
-
 template <int MT, int NTW, int KS>
 constexpr int bgemm_rows_cta() { return (bg::kWarps / KS) * NTW * 8; }
 

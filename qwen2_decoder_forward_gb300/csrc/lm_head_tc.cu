@@ -120,6 +120,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_lm_head_tc(const __grid_constan
         tma_prefetch_desc(&tmE);
     }
     if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+    // Launched with programmatic stream serialisation: the set-up above
+    // overlaps the previous kernel; its rows are read only after it.
+    pdl_launch_dependents();
+    pdl_wait();
 
     // ---- prologue: normed rows -> f32 scratch (in the ring) -> B operand ----
     float* xs = reinterpret_cast<float*>(ring);
@@ -362,8 +366,7 @@ cudaError_t enqueue_lm_head_tc(Ctx& c, const float* xin, int B, float* logits, i
         a.am_idx = c.ws.am_idx;
         a.count = c.ws.am_count;
         a.err = c.err;
-        k_lm_head_tc<<<grid, kThreads, lm_tc_smem(stages, H), st>>>(c.tc.lm_e, a);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch_pdl(k_lm_head_tc, dim3(grid), dim3(kThreads), lm_tc_smem(stages, H), st, c.tc.lm_e, a);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -61,6 +61,8 @@ __global__ void __launch_bounds__(kT) k_norm_rows_split(const float* __restrict_
                                                         const float* __restrict__ w, float eps,
                                                         __half* __restrict__ hi, __half* __restrict__ lo) {
     __shared__ float red[kT / 32];
+    pdl_launch_dependents();
+    pdl_wait();
     const int r = blockIdx.x;
     const float* xr = x + (size_t)r * H;
     float ss = 0.f;
@@ -81,7 +83,9 @@ __global__ void __launch_bounds__(kT) k_norm_rows_split_w(const float* __restric
                                                           const float* __restrict__ w, float eps,
                                                           __half* __restrict__ hi, __half* __restrict__ lo) {
     const int r = blockIdx.x * (kT / 32) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    pdl_launch_dependents();
     if (r >= rows) return;
+    pdl_wait();
     const float* xr = x + (size_t)r * H;
     float4 v[kNormSteps];
     float ss = 0.f;
@@ -123,9 +127,10 @@ __global__ void __launch_bounds__(kT) k_norm_rows_split_w(const float* __restric
 void launch_norm_split(const float* x, int rows, int H, const float* w, float eps, __half* hi, __half* lo,
                        cudaStream_t st) {
     if (H % 4 == 0 && H <= 32 * 4 * kNormSteps)
-        k_norm_rows_split_w<<<(rows + kT / 32 - 1) / (kT / 32), kT, 0, st>>>(x, rows, H, w, eps, hi, lo);
+        launch_pdl(k_norm_rows_split_w, dim3((rows + kT / 32 - 1) / (kT / 32)), dim3(kT), 0, st, x, rows, H, w, eps,
+                   hi, lo);
     else
-        k_norm_rows_split<<<rows, kT, 0, st>>>(x, H, w, eps, hi, lo);
+        launch_pdl(k_norm_rows_split, dim3(rows), dim3(kT), 0, st, x, H, w, eps, hi, lo);
 }
 
 __global__ void __launch_bounds__(kT) k_norm_rows(const float* __restrict__ x, int H, const float* __restrict__ w,

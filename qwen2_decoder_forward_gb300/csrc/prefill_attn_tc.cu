@@ -80,6 +80,8 @@ struct OperandArgs {
 __global__ void __launch_bounds__(256) k_att_operands(OperandArgs a) {
     __shared__ float vs[kKT][kD + 1];
     const int t = blockIdx.x, s = blockIdx.y, g = blockIdx.z, tid = threadIdx.x;
+    pdl_launch_dependents();
+    pdl_wait();
     const int pmax = a.seq_pmax[s], j0 = t * kKT;
     if (j0 > pmax) return;
     const int slot = a.seq_slot[s];
@@ -239,6 +241,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         tma_prefetch_desc(&tm_vt);
     }
     if (warp == 4) tmem_alloc(&sm.tmem_slot, kTmemCols);
+    // Launched with programmatic stream serialisation: the set-up above
+    // overlaps the previous kernel; q and the operands are read only after it.
+    pdl_launch_dependents();
+    pdl_wait();
     // Q: 128 rows x 8 chunks, four chunks per thread, f32 -> f16.
     for (int e = tid; e < kRows * 8; e += kThreads) {
         const int r = e >> 3, c = e & 7, i = r / group, h = r % group;
@@ -435,10 +441,10 @@ cudaError_t enqueue_attn_prefill_tc(const Ctx& c, const PrefillAttnArgs& a, cons
                                     cudaStream_t st) {
     const int n64 = att_ctx64(a.n_ctx);
     OperandArgs oa{a.kv, plan.seq_slot, plan.seq_pmax, c.ws.att_k, c.ws.att_vt, a.nkv, a.n_ctx, n64, a.L, layer};
-    k_att_operands<<<dim3(plan.max_tiles, plan.n_seq, a.nkv), 256, 0, st>>>(oa);
-    k_attn_prefill_tc<<<dim3(a.nkv, plan.n_blk), kThreads, kSmemBytes, st>>>(c.tc.att_k, c.tc.att_vt, a, layer, n64,
-                                                                             c.err);
-    return cudaGetLastError();
+    cudaError_t e = launch_pdl(k_att_operands, dim3(plan.max_tiles, plan.n_seq, a.nkv), dim3(256), 0, st, oa);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(k_attn_prefill_tc, dim3(a.nkv, plan.n_blk), dim3(kThreads), kSmemBytes, st, c.tc.att_k,
+                      c.tc.att_vt, a, layer, n64, c.err);
 }
 
 cudaError_t prefill_attn_tc_set_smem() {

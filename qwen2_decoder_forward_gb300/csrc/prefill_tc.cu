@@ -123,9 +123,8 @@ cudaError_t launch(const Ctx& c, const CUtensorMap& a, const CUtensorMap& a2, co
                    int K, const Epi& e, cudaStream_t st) {
     const int tiles = ((M + tcg::kBM - 1) / tcg::kBM) * ((N + BN - 1) / BN);
     const int grid = tiles < c.n_sm ? tiles : c.n_sm;
-    tcg::k_gemm_tc<BN, SPLIT, Epi><<<grid, tcg::kThreads, tcg::GemmCfg<BN, SPLIT>::kSmem, st>>>(a, a2, b, M, N, K,
-                                                                                              e, c.err);
-    return cudaGetLastError();
+    return launch_pdl(tcg::k_gemm_tc<BN, SPLIT, Epi>, dim3(grid), dim3(tcg::kThreads), tcg::GemmCfg<BN, SPLIT>::kSmem,
+                      st, a, a2, b, M, N, K, e, c.err);
 }
 
 template <int BN, bool SPLIT, class Epi>

@@ -87,6 +87,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     bool ok = true;
+    // Launched with programmatic stream serialisation: everything above
+    // overlaps the previous kernel; operands and outputs only after it.
+    pdl_launch_dependents();
+    pdl_wait();
 
     if (warp == 0) {
         if (lane == 0) {
