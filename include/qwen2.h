@@ -275,6 +275,15 @@ int qwen2_test_raise_guard(qwen2_ctx *ctx, int32_t code, void *stream);
  * 2000000]), QWEN2_E_UNSUPPORTED (the context has no persistent kernel). */
 int qwen2_test_stall_decode(qwen2_ctx *ctx, int32_t wait_us);
 
+/* Debug check for writes past the ends of device buffers: every buffer the
+ * context allocates (KV cache, workspace, decode state) sits between two
+ * 256-byte guard regions filled with 0xA5 at create.  Synchronises the
+ * device, reads the guards back and returns QWEN2_E_DEVICE_GUARD (the
+ * message names the buffer's index, size and the first changed byte) if a
+ * kernel wrote into one, else QWEN2_OK.  Costs two small device-to-host
+ * copies per buffer; meant for tests, not for every step. */
+int qwen2_check_canaries(qwen2_ctx *ctx);
+
 /* Synchronise `stream` and report any device-side guard that tripped since
  * the last check (QWEN2_E_DEVICE_GUARD, with the guard's code in the
  * message); clears the guard word. */

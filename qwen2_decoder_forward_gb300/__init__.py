@@ -57,6 +57,7 @@ EXPORTS = (
     "qwen2_final_hidden", "qwen2_synchronize", "qwen2_weight_bytes",
     "qwen2_kv_bytes_per_seq", "qwen2_quantize_q8_0", "qwen2_quantize_q4_0", "qwen2_features", "qwen2_profile_marks",
     "qwen2_lm_head_argmax_noalloc", "qwen2_test_raise_guard", "qwen2_test_stall_decode",
+    "qwen2_check_canaries",
 )
 
 
@@ -124,6 +125,8 @@ def lib() -> ctypes.CDLL:
     L.qwen2_test_raise_guard.restype = ctypes.c_int
     L.qwen2_test_stall_decode.argtypes = [_P, i32]
     L.qwen2_test_stall_decode.restype = ctypes.c_int
+    L.qwen2_check_canaries.argtypes = [_P]
+    L.qwen2_check_canaries.restype = ctypes.c_int
     L.qwen2_final_hidden.argtypes = [_P, _P, i32, _P]
     L.qwen2_final_hidden.restype = ctypes.c_int
     L.qwen2_synchronize.argtypes = [_P, _P]
@@ -412,6 +415,12 @@ class Qwen2Model:
 
     def synchronize(self, stream=None):
         self._check(lib().qwen2_synchronize(self._h, _stream_ptr(stream)))
+
+    def check_canaries(self):
+        """Debug check: raises Qwen2Error (QWEN2_E_DEVICE_GUARD) if a kernel
+        wrote into the guard words around any of the context's device
+        buffers."""
+        self._check(lib().qwen2_check_canaries(self._h))
 
 
 def _data_ptr(t):

@@ -64,18 +64,24 @@ bool is_device_ptr(const void* p) {
 
 template <class T>
 int dev_alloc(Ctx& c, T** p, size_t count, bool zero = true) {
+    // The buffer sits between two guard regions of kCanaryBytes filled with
+    // kCanaryByte; qwen2_check_canaries reads them back.
     void* v = nullptr;
     const size_t bytes = std::max<size_t>(count, 1) * sizeof(T);
-    if (cudaMalloc(&v, bytes) != cudaSuccess) {
+    if (cudaMalloc(&v, bytes + 2 * kCanaryBytes) != cudaSuccess) {
         cudaGetLastError();
         return QWEN2_E_OOM;
     }
-    if (zero && cudaMemset(v, 0, bytes) != cudaSuccess) {
+    unsigned char* user = static_cast<unsigned char*>(v) + kCanaryBytes;
+    if (cudaMemset(v, kCanaryByte, kCanaryBytes) != cudaSuccess ||
+        cudaMemset(user + bytes, kCanaryByte, kCanaryBytes) != cudaSuccess ||
+        (zero && cudaMemset(user, 0, bytes) != cudaSuccess)) {
         cudaFree(v);
         return QWEN2_E_CUDA;
     }
     c.allocs.push_back(v);
-    *p = static_cast<T*>(v);
+    c.canaries.push_back({user, bytes});
+    *p = reinterpret_cast<T*>(user);
     return QWEN2_OK;
 }
 
@@ -648,6 +654,27 @@ int qwen2_test_stall_decode(qwen2_ctx* h, int32_t wait_us) {
         return fail(&c, QWEN2_E_UNSUPPORTED, "the context's flags switch the persistent decode kernel off");
     c.pers.test_stall = 1;
     c.pers.test_wait_ns = (unsigned long long)wait_us * 1000ull;
+    return QWEN2_OK;
+}
+
+int qwen2_check_canaries(qwen2_ctx* h) {
+    if (!h) return QWEN2_E_ARG;
+    Ctx& c = h->c;
+    Q2_CHECK(&c, cudaDeviceSynchronize());
+    std::vector<unsigned char> buf(kCanaryBytes);
+    for (size_t i = 0; i < c.canaries.size(); ++i) {
+        const CanaryRegion& k = c.canaries[i];
+        for (int side = 0; side < 2; ++side) {
+            const unsigned char* at = side ? k.user + k.bytes : k.user - kCanaryBytes;
+            Q2_CHECK(&c, cudaMemcpy(buf.data(), at, kCanaryBytes, cudaMemcpyDeviceToHost));
+            for (size_t j = 0; j < kCanaryBytes; ++j)
+                if (buf[j] != kCanaryByte)
+                    return fail(&c, QWEN2_E_DEVICE_GUARD,
+                                std::string("canary ") + (side ? "after" : "before") + " device buffer #" +
+                                    std::to_string(i) + " (" + std::to_string(k.bytes) + " bytes) overwritten at byte " +
+                                    std::to_string(j));
+        }
+    }
     return QWEN2_OK;
 }
 

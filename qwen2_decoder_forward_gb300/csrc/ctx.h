@@ -145,6 +145,14 @@ struct PersistState {
 struct TcLayerMaps {
     CUtensorMap wqkv, wo, wgu, wd;
 };
+// Every buffer dev_alloc makes has kCanaryBytes of kCanaryByte on each side.
+constexpr size_t kCanaryBytes = 256;
+constexpr unsigned char kCanaryByte = 0xA5;
+struct CanaryRegion {
+    unsigned char* user;  // first byte of the buffer proper
+    size_t bytes;
+};
+
 struct TcState {
     bool ok = false;
     CUtensorMap a_xn, a_xn_lo, a_o, a_o_lo, a_mlp;   // activation operands [max_rows][K]
@@ -181,6 +189,7 @@ struct Ctx {
     cudaStream_t cap_stream = nullptr;
     std::map<int, cudaGraphExec_t> graphs;   // key: B | (want_logits << 16)
     std::vector<void*> allocs;    // device buffers freed at destroy
+    std::vector<CanaryRegion> canaries;  // the same buffers' user regions, between guard words
     std::string last_error;
 };
 

@@ -31,6 +31,7 @@
 #include "ctx.h"
 #include "persistent.h"
 #include "rowdot.cuh"
+#include "sm100.cuh"
 
 namespace qwen2 {
 
@@ -49,55 +50,15 @@ typedef unsigned long long u64;
 __shared__ u64 wait_limit_s;
 __device__ __forceinline__ u64 wait_limit() { return wait_limit_s; }
 
-__device__ __forceinline__ u64 now_ns() {
-    u64 t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ void mbar_init(u64* b, unsigned count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(u64* b, unsigned parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(b)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ bool mbar_test(u64* b, unsigned parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(b)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ void mbar_arrive(u64* b) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(u64* b, unsigned bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, u64* bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-
+// The asynchronous-proxy primitives of sm100.cuh (mbarriers, bulk copies)
+// and its global timer.
+using sm100::bulk_g2s;
+using sm100::mbar_arrive;
+using sm100::mbar_expect_tx;
+using sm100::mbar_init;
+using sm100::mbar_test;
+using sm100::mbar_try_wait;
+__device__ __forceinline__ u64 now_ns() { return sm100::global_ns(); }
 
 // Named-barrier OR over the 256 compute threads.
 __device__ __forceinline__ bool compute_any(bool v) {
@@ -250,8 +211,8 @@ struct PkLayout {
 struct Feeder {
     const PersistentArgs* a;
     unsigned char* ring;
-    u64* full;
-    u64* empty;
+    uint64_t* full;
+    uint64_t* empty;
     int c, G;
     int l = 0, ph = 0, r = 0, r1 = 0;  // next chunk: layer (L: LM head), phase, row range
     int issued = 0;
@@ -276,7 +237,7 @@ struct Feeder {
             r1 = split(H, c + 1, G);
         }
     }
-    __device__ __forceinline__ void init(const PersistentArgs* a_, unsigned char* ring_, u64* full_, u64* empty_,
+    __device__ __forceinline__ void init(const PersistentArgs* a_, unsigned char* ring_, uint64_t* full_, uint64_t* empty_,
                                          int c_, int G_) {
         a = a_;
         ring = ring_;
@@ -361,7 +322,7 @@ __device__ __forceinline__ float* act_smem() { return reinterpret_cast<float*>(p
 __device__ __forceinline__ const __half* stage_smem(int s) {
     return reinterpret_cast<const __half*>(persist_smem + (size_t)s * kPersistStage);
 }
-__device__ __forceinline__ u64* full_bars() { return reinterpret_cast<u64*>(persist_smem + kPersistStages * kPersistStage); }
+__device__ __forceinline__ uint64_t* full_bars() { return reinterpret_cast<uint64_t*>(persist_smem + kPersistStages * kPersistStage); }
 
 // One lane's share of an activation vector of K floats as the canonical
 // row dot reads it (rowdot.cuh): chunks c = lane + 32 u of eight floats,
@@ -416,7 +377,7 @@ __device__ __forceinline__ void rows_dot_x(const __half* const (&rows)[R], const
 }
 
 // Wait (bounded) for an mbarrier phase.
-__device__ __forceinline__ bool wait_bar(u64* b, unsigned par) {
+__device__ __forceinline__ bool wait_bar(uint64_t* b, unsigned par) {
     if (mbar_try_wait(b, par)) return true;
     const u64 t0 = now_ns();
     while (now_ns() - t0 < wait_limit())
@@ -437,8 +398,8 @@ __device__ __forceinline__ bool wait_bar(u64* b, unsigned par) {
 template <int K>
 __device__ __noinline__ bool warp_stage_pairs(int it0, int nrows, float* res) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    u64* full = full_bars();
-    u64* empty = full + kPersistStages;
+    uint64_t* full = full_bars();
+    uint64_t* empty = full + kPersistStages;
     XLane<K> x;
     x.load(act_smem());
     bool ok = true;
@@ -541,8 +502,8 @@ __device__ __forceinline__ float row_dot_split(const __half* row, const float* x
 template <int K>
 __device__ __noinline__ bool warp_stage_rows(int it0, int rpc, int nrows, float* res) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    u64* full = full_bars();
-    u64* empty = full + kPersistStages;
+    uint64_t* full = full_bars();
+    uint64_t* empty = full + kPersistStages;
     const float* xa = act_smem();
     const float* xh = xa + K / 2;
     bool ok = true;
@@ -575,8 +536,8 @@ __device__ __noinline__ bool warp_stage_rows(int it0, int rpc, int nrows, float*
 template <int K>
 __device__ __noinline__ bool lm_head_rows(int it0, int r0, int r1, float* logits, float* best_v, int* best_i) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    u64* full = full_bars();
-    u64* empty = full + kPersistStages;
+    uint64_t* full = full_bars();
+    uint64_t* empty = full + kPersistStages;
     XLane<K> x;
     x.load(act_smem());
     float bv = -INFINITY;
@@ -649,8 +610,8 @@ __device__ __noinline__ void merge_head(PkReader& rd, const u64* att_h, int n_ch
 template <int HC, int IC>
 __global__ void __launch_bounds__(kThreads, 1) k_decode_persistent(PersistentArgs a) {
     unsigned char* ring = persist_smem;
-    u64* full = full_bars();
-    u64* empty = full + kPersistStages;
+    uint64_t* full = full_bars();
+    uint64_t* empty = full + kPersistStages;
     float* red = reinterpret_cast<float*>(empty + kPersistStages);
     float* act = act_smem();
     float* xr = act + a.act_floats;  // raw x [H]

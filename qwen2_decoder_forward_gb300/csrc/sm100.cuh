@@ -39,6 +39,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, unsigned parity) {
         : "memory");
     return ok != 0;
 }
+// One non-blocking probe of the phase of parity `parity`.
+__device__ __forceinline__ bool mbar_test(uint64_t* b, unsigned parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // Waits for the phase of parity `parity` to complete; gives up (returns
 // false) after `timeout_ns` of the global timer.  The timer is read only
 // once the first try finds the phase still open.

@@ -24,3 +24,25 @@ def read_golden(name: str) -> dict:
             k, v = (s.strip() for s in line.split("=", 1))
             out[k] = v
     return out
+
+
+@pytest.fixture(autouse=True)
+def _check_canaries_at_close(request, monkeypatch):
+    """Every model a GPU test closes first has the guard words around its
+    device buffers checked: a kernel that wrote past either end of a buffer
+    fails the test that ran it."""
+    if request.node.get_closest_marker("gpu") is None:
+        yield
+        return
+    import qwen2_decoder_forward_gb300 as q2
+    close = q2.Qwen2Model.close
+
+    def checked_close(self):
+        if getattr(self, "_h", None):
+            try:
+                self.check_canaries()
+            finally:
+                close(self)
+
+    monkeypatch.setattr(q2.Qwen2Model, "close", checked_close)
+    yield

@@ -82,3 +82,37 @@ def test_exact_tie_takes_the_lowest_index(q2, shape_name, batch, kw):
     keep = np.ones(shape.vocab, dtype=bool)
     keep[l] = False
     assert np.array_equal(lg2[:, keep].view(np.uint32), lg[:, keep].view(np.uint32))
+
+
+@pytest.mark.parametrize("shape_name", ["toy", "ragged"])
+def test_exact_tie_in_the_tensor_core_prefill_head(q2, shape_name):
+    """The tensor-core prefill's LM head (tcgen05, E streamed as the MMA's M
+    operand, per-CTA bests merged by the last CTA): copy E[m] of the last
+    kept row's id m into an unused lower row l; the prefill's id must become
+    l, with bit-identical logits for l and m."""
+    shape = synth.SHAPES[shape_name]
+    w = dict(synth.make_weights(shape, 5))
+    prompts = [synth.make_tokens(shape.vocab, 40, 810), synth.make_tokens(shape.vocab, 23, 811)]
+
+    def run(weights):
+        with q2.Qwen2Model(shape, weights, n_ctx=128, max_seqs=2, max_tokens=64,
+                           prefill_mode=q2.PREFILL_TENSOR) as m:
+            assert m.features & q2.FEATURE_TENSOR_PREFILL
+            lg, ids = m.prefill([0, 1], prompts, n_out=3)
+            out = lg.cpu().numpy(), ids.cpu().numpy()
+            m.synchronize()
+        return out
+
+    lg, ids = run(w)
+    m = int(ids[-1])
+    assert m > 0 and lg[-1, m] == lg[-1].max()
+    used = set(int(t) for p in prompts for t in p)
+    l = next(t for t in range(m) if t not in used)
+    w["embed"] = np.array(w["embed"], copy=True)
+    w["embed"][l] = w["embed"][m]
+    lg2, ids2 = run(w)
+    assert lg2[-1, l].view(np.uint32) == lg2[-1, m].view(np.uint32)
+    assert lg2[-1, m].view(np.uint32) == lg[-1, m].view(np.uint32)
+    assert int(ids2[-1]) == l
+    # Every row whose maximum was m now picks l; the others keep their ids.
+    assert list(ids2) == [l if int(i) == m else int(i) for i in ids]

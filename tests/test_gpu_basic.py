@@ -311,6 +311,35 @@ def test_tensor_core_prefill_in_chunks(q2, shape_name):
         m.synchronize()
 
 
+def test_canary_check_finds_a_write_past_a_buffer(q2):
+    """The guard words around the context's device buffers: a clean run
+    passes the check; four bytes written just past the end of the KV cache
+    (into its trailing guard region, which is allocated memory) make the
+    check fail with QWEN2_E_DEVICE_GUARD; restoring them makes it pass."""
+    import torch
+    shape = synth.SHAPES["toy"]
+    w = synth.make_weights(shape, 0)
+    prompt = synth.make_tokens(shape.vocab, 16, 1002)
+    with q2.Qwen2Model(shape, w, n_ctx=64, max_seqs=1, max_tokens=16) as m:
+        _, ids = m.prefill([0], [prompt])
+        m.decode_steps([0], [int(ids[0])], [16], 4)
+        m.check_canaries()
+        kv = m.kv_cache()
+        end = kv.data_ptr() + kv.numel() * 4
+        tail = torch.as_tensor(q2._CudaArray(end, [1], "<i4"), device="cuda")
+        canary = int(np.array([0xA5A5A5A5], dtype=np.uint32).view(np.int32)[0])
+        assert int(tail.item()) == canary
+        tail.fill_(0)
+        torch.cuda.synchronize()
+        with pytest.raises(q2.Qwen2Error) as e:
+            m.check_canaries()
+        assert e.value.code == q2.QWEN2_E_DEVICE_GUARD
+        assert "canary after device buffer" in str(e.value)
+        tail.fill_(canary)
+        torch.cuda.synchronize()
+        m.check_canaries()
+
+
 def test_device_guard_is_reported_once_and_decoding_continues(q2):
     """Failure detection without a GPU fault: the test hook writes the
     device guard word the way a kernel's bounded wait does when it gives up.
