@@ -112,6 +112,30 @@ __device__ __forceinline__ Unit decode_unit(const Smem& sm, int B, int u) {
     return t;
 }
 
+// The unit after t in (b, g, c) order (rows without chunks skipped); only
+// called while a next unit exists.
+__device__ __forceinline__ void next_unit(const Smem& sm, int B, int nkv, Unit& t) {
+    if (++t.c >= sm.nch[t.b]) {
+        t.c = 0;
+        if (++t.g >= nkv) {
+            t.g = 0;
+            do {
+                ++t.b;
+            } while (t.b + 1 < B && sm.nch[t.b] == 0);
+        }
+    }
+    t.nj = min(kCh, sm.posv[t.b] + 1 - t.c * kCh);
+}
+
+// 2^x by the MUFU instruction (relative error about 2^-22; the
+// probabilities are rounded to TF32 afterwards).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+constexpr float kLog2e = 1.4426950408889634f;
+
 // Row of the cache viewed as a [rows][64] f32 matrix: position p0 of
 // (slot, layer, K or V, kv head g).
 __device__ __forceinline__ int kv_row(const Args& a, int slot, int which, int g, int p0) {
@@ -231,6 +255,8 @@ __global__ void __launch_bounds__(fd::kThreads, 2)
             // K and V are read once: first out of L2.
             const uint64_t pol = sm100::policy_evict_first();
             int k = 0;
+            Unit t{};
+            if (u0 < u1) t = decode_unit(sm, a.B, u0);
             for (int u = u0; u < u1; ++u, ++k) {
                 const int s = k % kStages;
                 if (k >= kStages &&
@@ -238,7 +264,7 @@ __global__ void __launch_bounds__(fd::kThreads, 2)
                     raise_guard(a.err, kGuardTimeout);
                     break;
                 }
-                const Unit t = decode_unit(sm, a.B, u);
+                if (u != u0) next_unit(sm, a.B, a.nkv, t);
                 const int yk = kv_row(a, sm.slotv[t.b], 0, t.g, t.c * kCh);
                 const int yv = kv_row(a, sm.slotv[t.b], 1, t.g, t.c * kCh);
                 // A unit that starts a segment also brings its query heads.
@@ -268,8 +294,10 @@ __global__ void __launch_bounds__(fd::kThreads, 2)
     float m_run0 = -INFINITY, m_run1 = -INFINITY, l_run0 = 0.f, l_run1 = 0.f;
     int c_first = 0;
     int k = 0;
+    Unit t{};
+    if (u0 < u1) t = decode_unit(sm, a.B, u0);
     for (int u = u0; u < u1; ++u, ++k) {
-        const Unit t = decode_unit(sm, a.B, u);
+        if (u != u0) next_unit(sm, a.B, a.nkv, t);
         const int s = k % kStages;
         bool ok = *reinterpret_cast<volatile int*>(&sm.abort) == 0;
         if (ok && !sm100::mbar_wait(&sm.full[s], (k / kStages) & 1, kWaitNs)) {
@@ -317,10 +345,13 @@ __global__ void __launch_bounds__(fd::kThreads, 2)
             // and head slots past the group get -inf.
             const bool klo = key0 + g8 < t.nj, khi = key0 + g8 + 8 < t.nj;
             const bool v0 = h0 < group, v1 = h1 < group;
-            sc[0] = (klo && v0) ? sc[0] * 0.125f : -INFINITY;
-            sc[1] = (klo && v1) ? sc[1] * 0.125f : -INFINITY;
-            sc[2] = (khi && v0) ? sc[2] * 0.125f : -INFINITY;
-            sc[3] = (khi && v1) ? sc[3] * 0.125f : -INFINITY;
+            // Scores in base-2 units (log2 e folded into the 1/8): the
+            // running maxima and the exponentials below use 2^x.
+            constexpr float kS2 = 0.125f * kLog2e;
+            sc[0] = (klo && v0) ? sc[0] * kS2 : -INFINITY;
+            sc[1] = (klo && v1) ? sc[1] * kS2 : -INFINITY;
+            sc[2] = (khi && v0) ? sc[2] * kS2 : -INFINITY;
+            sc[3] = (khi && v1) ? sc[3] * kS2 : -INFINITY;
             // Online softmax over this warp's 16 keys, per head slot.
             float mt0 = fmaxf(sc[0], sc[2]), mt1 = fmaxf(sc[1], sc[3]);
 #pragma unroll
@@ -330,15 +361,15 @@ __global__ void __launch_bounds__(fd::kThreads, 2)
             }
             const float mn0 = fmaxf(m_run0, mt0), mn1 = fmaxf(m_run1, mt1);
             const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
-            const float al0 = expf(m_run0 - mu0), al1 = expf(m_run1 - mu1);
+            const float al0 = ex2(m_run0 - mu0), al1 = ex2(m_run1 - mu1);
             m_run0 = mn0;
             m_run1 = mn1;
             // Probabilities rounded to TF32 here, so l sums what the MMA uses.
             uint32_t pb[4];
-            pb[0] = tf32_rn(expf(sc[0] - mu0));
-            pb[1] = tf32_rn(expf(sc[1] - mu1));
-            pb[2] = tf32_rn(expf(sc[2] - mu0));
-            pb[3] = tf32_rn(expf(sc[3] - mu1));
+            pb[0] = tf32_rn(ex2(sc[0] - mu0));
+            pb[1] = tf32_rn(ex2(sc[1] - mu1));
+            pb[2] = tf32_rn(ex2(sc[2] - mu0));
+            pb[3] = tf32_rn(ex2(sc[3] - mu1));
             l_run0 = fmaf(l_run0, al0, __uint_as_float(pb[0]) + __uint_as_float(pb[2]));
             l_run1 = fmaf(l_run1, al1, __uint_as_float(pb[1]) + __uint_as_float(pb[3]));
 #pragma unroll
@@ -417,14 +448,14 @@ __global__ void __launch_bounds__(fd::kThreads, 2)
             float A = 0.f, Lsum = 0.f;
 #pragma unroll
             for (int w = 0; w < kConsumers; ++w) {
-                const float wt = sm.wm[w][h] == -INFINITY ? 0.f : expf(sm.wm[w][h] - M);
+                const float wt = sm.wm[w][h] == -INFINITY ? 0.f : ex2(sm.wm[w][h] - M);
                 A = fmaf(wt, sm.wacc[w][h][d], A);
                 Lsum = fmaf(wt, sm.wl[w][h], Lsum);
             }
             float* pr = a.part + ((head0 + h) * a.max_chunks + c_first) * kPart;
             pr[2 + d] = A;
             if (d == 0) {
-                pr[0] = M;
+                pr[0] = M / kLog2e;  // the partial's maximum in natural-log units, as the merge reads it
                 pr[1] = Lsum;
             }
         }
