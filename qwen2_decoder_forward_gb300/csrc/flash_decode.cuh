@@ -31,7 +31,8 @@
 // (10-bit mantissa, round to nearest); v enters as a TF32 hi / lo pair (two
 // MMAs), the same split the tensor-core prefill uses for v; the softmax
 // statistics, the sums l (of the rounded probabilities) and the accumulators
-// are f32.
+// are f32.  The softmax runs in base 2 (scores scaled by log2(e) / 8,
+// exponentials by ex2); a partial's maximum is stored in natural-log units.
 #pragma once
 
 #include "common.cuh"
