@@ -14,9 +14,9 @@
 // bytes whatever the mix of lengths.  A CTA folds the consecutive chunks of
 // one (b, g) into a single running (max m, sum l, acc[64]) per query head
 // (online softmax) and writes one partial per such segment, at the slot of
-// the segment's first chunk.  The last CTA to finish a (b, g) merges its
-// segments in chunk order and writes o (f32, and the f16 hi / lo pair the
-// following Q8_0 product reads).
+// the segment's first chunk.  k_attn_merge, launched next, merges the
+// segments of each (b, g) in chunk order and writes o (f32, and the f16
+// hi / lo pair the following Q8_0 product reads).
 //
 // Inside a CTA: warp 4 (one elected lane) loads each unit's K and V tiles
 // (64 positions x 64 floats each) with four TMA tensor copies into a ring
