@@ -155,10 +155,11 @@ def decode_bytes_per_step(shape, positions, q8: bool = False) -> float:
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum of
 # the 21st launch, a position near 150 of the 0.5b-decode-b1 workload) from
-# the `--set full` ncu capture of the persistent decode kernel, valid only
+# an ncu capture of those two counters on the persistent decode kernel
+# (profiles/decode_persistent_0p5b_b1_launches.md), valid only
 # for that workload and only while the kernel's sources -- their code, with
 # // comments and blank lines left out -- hash to `src`.
-TRAFFIC = {"k_decode_persistent": {"workload": "0.5b-decode-b1", "src": "842422b03eb52ad4", "bytes": 1003233280.0}}
+TRAFFIC = {"k_decode_persistent": {"workload": "0.5b-decode-b1", "src": "bc3e88d4f74ebdc1", "bytes": 1003649792.0}}
 KERNEL_SOURCES = ("persistent.cu", "persistent.h", "rowdot.cuh", "common.cuh", "attn.cuh", "ctx.h")
 
 
