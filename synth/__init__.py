@@ -71,6 +71,10 @@ SHAPES = {
     "toy-mha": ModelShape("toy-mha", n_layer=2, hidden=256, n_head=4,
                           n_kv_head=4, head_dim=64, intermediate=1024,
                           vocab=4096),
+    # eight query heads per kv head, the widest group the kernels take
+    "toy-g8": ModelShape("toy-g8", n_layer=2, hidden=512, n_head=8,
+                         n_kv_head=1, head_dim=64, intermediate=1024,
+                         vocab=4096),
     # head_dim 128, the head width of every size above 0.5B (nnterp
     # encyclopedia qwen2, "Grouped-query attention"): 4 q heads over 2 kv
     # heads, tied LM head (as 1.5B and 3B).

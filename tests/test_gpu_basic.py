@@ -33,7 +33,7 @@ def run_oracle(shape, w, prompts, n_steps, n_ctx, n_out=1):
     return orc, out
 
 
-@pytest.mark.parametrize("shape_name", ["toy", "ragged", "toy-mha"])
+@pytest.mark.parametrize("shape_name", ["toy", "ragged", "toy-mha", "toy-g8"])
 def test_prefill_and_teacher_forced_decode(q2, shape_name):
     shape = synth.SHAPES[shape_name]
     w = synth.make_weights(shape, 0)
@@ -239,7 +239,7 @@ def test_kv_cache_save_and_restore(q2):
     np.testing.assert_array_equal(np.concatenate([first, rest]), full)
 
 
-@pytest.mark.parametrize("shape_name", ["toy", "ragged", "toy-mha"])
+@pytest.mark.parametrize("shape_name", ["toy", "ragged", "toy-mha", "toy-g8"])
 def test_tensor_core_prefill(q2, shape_name):
     """QWEN2_PREFILL_TENSOR (tcgen05 GEMMs on f16 operands): two sequences of
     37 and 150 rows (two 128-row tiles, the second ragged) with the tail cut,
@@ -276,7 +276,7 @@ def test_tensor_core_prefill(q2, shape_name):
         m.synchronize()
 
 
-@pytest.mark.parametrize("shape_name", ["toy", "ragged"])
+@pytest.mark.parametrize("shape_name", ["toy", "ragged", "toy-g8"])
 def test_tensor_core_prefill_in_chunks(q2, shape_name):
     """Chunked prefill on the tensor-core path: the second call's rows attend
     to keys an earlier call stored (prefixes of 70 and 31 positions, neither

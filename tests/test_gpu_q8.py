@@ -32,6 +32,8 @@ def _prompts(shape, lens, seed):
     ("toy", list(range(5, 25)), 128, "q8_0"),
     # one query head per kv head (group 1) through the batched attention
     ("toy-mha", [20, 45, 33], 128, "q8_0"),
+    # eight query heads per kv head (the widest group) through the same path
+    ("toy-g8", [20, 45, 33], 128, "q8_0"),
     # long rows: many 64-key chunks, segments split across CTAs
     ("toy", [2500, 40, 1200, 700], 4096, "q8_0"),
     # n_ctx above 4096: the batched decode falls back to the split-k attention
