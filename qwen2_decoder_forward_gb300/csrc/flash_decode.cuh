@@ -43,7 +43,7 @@ namespace fd {
 
 constexpr int kDh = 64;                 // head dim
 constexpr int kCh = 64;                 // keys per unit
-constexpr int kStages = 3;
+constexpr int kStages = 2;
 constexpr int kConsumers = 4;           // consumer warps
 constexpr int kThreads = (kConsumers + 1) * 32;
 constexpr int kMaxRows = 32;            // rows (sequences) per launch
