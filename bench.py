@@ -441,11 +441,11 @@ def run_prefill(args, wl, shape, weights, reps, world):
                           "one whole prefill (f32 CUDA-core kernels)",
                 "peak_source": src + " bf16 dense burst (f16 has the same tensor rate)",
                 "flops_per_launch": flops}
-    # Launches per step: embed; per layer norm, QKV, attention (on the tensor
-    # path preceded by its operand conversion), O, norm, GU, down (the last
-    # layer: norm, QKV, 4 gathers, attention, 3 GEMVs); LM head.
-    per_layer = 8 if tensor else 7
-    launches = 1 + (shape.n_layer - 1) * per_layer + 2 + 4 + 1 + 3 + 1
+    # Launches per step: embed; per layer norm, QKV, attention, O, norm, GU,
+    # down (the last layer: norm, QKV, 4 gathers, attention, 3 GEMVs); LM
+    # head.  (The tensor path's attention-operand conversion runs only for
+    # keys an earlier call stored: none here.)
+    launches = 1 + (shape.n_layer - 1) * 7 + 2 + 4 + 1 + 3 + 1
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None,

@@ -471,21 +471,29 @@ int qwen2_prefill(qwen2_ctx* h, int32_t n_seq, const int32_t* seq_ids, const int
     plan.insert(plan.end(), bn.begin(), bn.end());
     plan.insert(plan.end(), kb0.begin(), kb0.end());
     plan.insert(plan.end(), kbn.begin(), kbn.end());
-    // Per sequence: slot and largest position (the keys its attention reads).
-    int max_tiles = 0;
+    // Per sequence: slot, and the end of the positions whose tensor-core
+    // attention operands must be converted from the cache: the positions
+    // before its first row when its rows are consecutive positions (the QKV
+    // epilogue writes its own rows' operands), else all up to the largest.
+    int conv_tiles = 0;
     {
-        std::vector<int> ss(n_seq), sp(n_seq);
+        std::vector<int> ss(n_seq), se(n_seq);
         int o = 0;
         for (int s = 0; s < n_seq; ++s) {
+            const int n = n_tokens[s];
             int m = 0;
-            for (int i = 0; i < n_tokens[s]; ++i) m = std::max(m, (int)positions[o + i]);
-            o += n_tokens[s];
+            bool consecutive = true;
+            for (int i = 0; i < n; ++i) {
+                m = std::max(m, (int)positions[o + i]);
+                if (i > 0 && positions[o + i] != positions[o + i - 1] + 1) consecutive = false;
+            }
             ss[s] = seq_ids[s];
-            sp[s] = m;
-            max_tiles = std::max(max_tiles, m / 64 + 1);
+            se[s] = consecutive ? (int)positions[o] : m + 1;
+            conv_tiles = std::max(conv_tiles, (se[s] + 63) / 64);
+            o += n;
         }
         plan.insert(plan.end(), ss.begin(), ss.end());
-        plan.insert(plan.end(), sp.begin(), sp.end());
+        plan.insert(plan.end(), se.begin(), se.end());
     }
     Workspace& w = c.ws;
     Q2_CHECK(&c, cudaMemcpyAsync(w.rows_tok, tokens, rows * 4, cudaMemcpyHostToDevice, st));
@@ -502,9 +510,9 @@ int qwen2_prefill(qwen2_ctx* h, int32_t n_seq, const int32_t* seq_ids, const int
     pp.kblk_nrows = w.blk + 2 * nb + nkb;
     pp.n_kblk = nkb;
     pp.seq_slot = w.blk + 2 * nb + 2 * nkb;
-    pp.seq_pmax = pp.seq_slot + n_seq;
+    pp.seq_conv = pp.seq_slot + n_seq;
     pp.n_seq = n_seq;
-    pp.max_tiles = max_tiles;
+    pp.conv_tiles = conv_tiles;
 
     const bool logits_dev = logits && is_device_ptr(logits);
     const bool ids_dev = ids && is_device_ptr(ids);

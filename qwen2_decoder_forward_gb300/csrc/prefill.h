@@ -54,10 +54,13 @@ struct PrefillPlan {
     const int* kblk_row0;   // blocks over the kept rows (after the tail cut)
     const int* kblk_nrows;
     int n_kblk;
-    const int* seq_slot;    // per sequence of the call: its slot and its largest position
-    const int* seq_pmax;
+    const int* seq_slot;    // per sequence of the call: its slot, and the end (exclusive)
+    const int* seq_conv;    //   of the positions whose attention operands come from the
+                            //   cache: those before the call's first row when its rows are
+                            //   consecutive positions (the QKV epilogue writes the rest),
+                            //   else every position up to the largest
     int n_seq;
-    int max_tiles;          // max over the sequences of seq_pmax / 64 + 1
+    int conv_tiles;         // max over the sequences of ceil(seq_conv / 64); 0: nothing to convert
 };
 
 // Positions of the attention operand buffers rounded up to whole 64-key tiles.
@@ -78,8 +81,9 @@ cudaError_t tc_gemm_down(const Ctx& c, int layer, int M, float* x, cudaStream_t 
 // Causal GQA attention of the tensor-core path on tcgen05 MMAs into tensor
 // memory (prefill_attn_tc.cu): writes a.o_h / a.o_l; grid (nkv, n_blk) over
 // the 16-row query blocks; head_dim 64, at most 8 query heads per kv head.
-// First converts the keys 0 .. seq_pmax of every sequence of the call into
-// the f16 operand buffers (Workspace::att_k / att_vt), read then by TMA.
+// The f16 operand buffers it reads by TMA (Workspace::att_k / att_vt) hold
+// the call's own keys (the QKV epilogue writes them); it first converts the
+// positions below seq_conv from the f32 cache (keys an earlier call stored).
 cudaError_t enqueue_attn_prefill_tc(const Ctx& c, const PrefillAttnArgs& a, const PrefillPlan& plan, int layer,
                                     cudaStream_t st);
 cudaError_t prefill_attn_tc_set_smem();

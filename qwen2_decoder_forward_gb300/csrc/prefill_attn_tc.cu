@@ -6,11 +6,15 @@
 //
 // Two kernels per layer.
 //
-// k_att_operands converts the keys 0 .. pmax of every sequence of the call,
-// once, from the f32 KV cache into f16 operand buffers laid out for TMA:
+// The attention reads its keys from f16 operand buffers laid out for TMA:
 // k as rows [slot][kv head][position][64 dims] and v transposed as an f16
-// hi / lo pair, rows [slot][kv head][hi, lo][dim][positions].  A whole
-// 64-key tile is written, zeros past pmax.
+// hi / lo pair, rows [slot][kv head][hi, lo][dim][positions].  The QKV
+// product's epilogue writes the call's own rows there as it stores them in
+// the f32 cache; k_att_operands converts, from the cache, the positions an
+// earlier call stored (those below the sequence's seq_conv).  Positions past
+// a sequence's last key inside its last 64-key tile hold stale finite
+// values or the buffers' initial zeros: their scores are masked and their
+// probabilities are exactly 0.
 //
 // k_attn_prefill_tc: block (g, blk) takes up to 16 query positions of one
 // sequence; their group query heads form the rows of one 128-row tile (row
@@ -70,20 +74,22 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
 struct OperandArgs {
     const float* kv;
     const int* seq_slot;
-    const int* seq_pmax;
+    const int* seq_conv;
     __half* att_k;
     __half* att_vt;
     int nkv, n_ctx, n_ctx64, L, layer;
 };
 
-// Grid (tiles, sequences, kv heads), 256 threads: one 64-key tile each.
+// Grid (tiles, sequences, kv heads), 256 threads: the positions below
+// seq_conv of one 64-key tile each.
 __global__ void __launch_bounds__(256) k_att_operands(OperandArgs a) {
     __shared__ float vs[kKT][kD + 1];
     const int t = blockIdx.x, s = blockIdx.y, g = blockIdx.z, tid = threadIdx.x;
     pdl_launch_dependents();
     pdl_wait();
-    const int pmax = a.seq_pmax[s], j0 = t * kKT;
-    if (j0 > pmax) return;
+    const int end = a.seq_conv[s], j0 = t * kKT;
+    if (j0 >= end) return;
+    const int pmax = end - 1;
     const int slot = a.seq_slot[s];
     const size_t head_stride = (size_t)a.n_ctx * kD;
     const size_t cache0 = ((size_t)slot * a.L + a.layer) * 2 * a.nkv;
@@ -104,7 +110,7 @@ __global__ void __launch_bounds__(256) k_att_operands(OperandArgs a) {
         const int e = tid + 256 * i, jv = e >> 4, d4 = 4 * (e & 15);
         vx[i] = j0 + jv <= pmax ? *reinterpret_cast<const float4*>(vb + (size_t)(j0 + jv) * kD + d4) : zero;
     }
-    {
+    if (kin) {
         const float f0[8] = {kx[0].x, kx[0].y, kx[0].z, kx[0].w, kx[1].x, kx[1].y, kx[1].z, kx[1].w};
         const float f1[8] = {kx[2].x, kx[2].y, kx[2].z, kx[2].w, kx[3].x, kx[3].y, kx[3].z, kx[3].w};
         uint4* dst = reinterpret_cast<uint4*>(a.att_k + (head * a.n_ctx64 + j0 + j) * kD + c0);
@@ -133,10 +139,22 @@ __global__ void __launch_bounds__(256) k_att_operands(OperandArgs a) {
             lo[2 * q] = v[2 * q] - b.x;
             lo[2 * q + 1] = v[2 * q + 1] - b.y;
         }
-        __half* row_h = a.att_vt + ((head * 2 + 0) * kD + d) * a.n_ctx64;
-        __half* row_l = a.att_vt + ((head * 2 + 1) * kD + d) * a.n_ctx64;
-        *reinterpret_cast<uint4*>(row_h + j0 + 8 * c) = hi;
-        *reinterpret_cast<uint4*>(row_l + j0 + 8 * c) = pack8(lo);
+        __half* row_h = a.att_vt + ((head * 2 + 0) * kD + d) * a.n_ctx64 + j0 + 8 * c;
+        __half* row_l = a.att_vt + ((head * 2 + 1) * kD + d) * a.n_ctx64 + j0 + 8 * c;
+        const uint4 lw = pack8(lo);
+        if (j0 + 8 * c + 8 <= end) {
+            *reinterpret_cast<uint4*>(row_h) = hi;
+            *reinterpret_cast<uint4*>(row_l) = lw;
+        } else {
+            // The last keys below seq_conv: the ones past it are the QKV
+            // epilogue's (this call's rows) and stay as written.
+            const __half* hh = reinterpret_cast<const __half*>(&hi);
+            const __half* ll = reinterpret_cast<const __half*>(&lw);
+            for (int q = 0; j0 + 8 * c + q < end; ++q) {
+                row_h[q] = hh[q];
+                row_l[q] = ll[q];
+            }
+        }
     }
 }
 
@@ -440,9 +458,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 cudaError_t enqueue_attn_prefill_tc(const Ctx& c, const PrefillAttnArgs& a, const PrefillPlan& plan, int layer,
                                     cudaStream_t st) {
     const int n64 = att_ctx64(a.n_ctx);
-    OperandArgs oa{a.kv, plan.seq_slot, plan.seq_pmax, c.ws.att_k, c.ws.att_vt, a.nkv, a.n_ctx, n64, a.L, layer};
-    cudaError_t e = launch_pdl(k_att_operands, dim3(plan.max_tiles, plan.n_seq, a.nkv), dim3(256), 0, st, oa);
-    if (e != cudaSuccess) return e;
+    if (plan.conv_tiles > 0) {
+        OperandArgs oa{a.kv, plan.seq_slot, plan.seq_conv, c.ws.att_k, c.ws.att_vt, a.nkv, a.n_ctx, n64, a.L,
+                       layer};
+        cudaError_t e = launch_pdl(k_att_operands, dim3(plan.conv_tiles, plan.n_seq, a.nkv), dim3(256), 0, st, oa);
+        if (e != cudaSuccess) return e;
+    }
     return launch_pdl(k_attn_prefill_tc, dim3(a.nkv, plan.n_blk), dim3(kThreads), kSmemBytes, st, c.tc.att_k,
                       c.tc.att_vt, a, layer, n64, c.err);
 }

@@ -30,6 +30,12 @@ struct EpiQKV {
     const int* pos;
     const int* slot;
     int* err;
+    // The attention's f16 operands of the row's key and value (see
+    // prefill_attn_tc.cu): k as att_k [slot][kv head][n_ctx64][64], v
+    // transposed as the hi / lo pair att_vt [slot][kv head][2][64][n_ctx64].
+    __half* att_k;
+    __half* att_vt;
+    int n_ctx64;
     __device__ __forceinline__ void store(int m, int n0, const float (&v)[32]) const {
         const int s = n0 / kHdim, i0 = (n0 % kHdim) >> 1;
         const int p = pos[m];
@@ -70,6 +76,38 @@ struct EpiQKV {
         for (int j = 0; j < 4; ++j) {
             lo[j] = make_float4(a[4 * j], a[4 * j + 1], a[4 * j + 2], a[4 * j + 3]);
             hi[j] = make_float4(b[4 * j], b[4 * j + 1], b[4 * j + 2], b[4 * j + 3]);
+        }
+        if (s < nh) return;
+        // Dims i0 .. i0 + 15 hold a[], dims i0 + 32 .. i0 + 47 hold b[].
+        if (s < nh + nkv) {
+            const size_t head = (size_t)slot[m] * nkv + (s - nh);
+            __half* kr = att_k + (head * n_ctx64 + p) * kHdim;
+            uint32_t ha[8], hb[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const __half2 x = __floats2half2_rn(a[2 * j], a[2 * j + 1]);
+                const __half2 y = __floats2half2_rn(b[2 * j], b[2 * j + 1]);
+                ha[j] = *reinterpret_cast<const uint32_t*>(&x);
+                hb[j] = *reinterpret_cast<const uint32_t*>(&y);
+            }
+            uint4* da = reinterpret_cast<uint4*>(kr + i0);
+            uint4* db = reinterpret_cast<uint4*>(kr + i0 + kHdim / 2);
+            da[0] = make_uint4(ha[0], ha[1], ha[2], ha[3]);
+            da[1] = make_uint4(ha[4], ha[5], ha[6], ha[7]);
+            db[0] = make_uint4(hb[0], hb[1], hb[2], hb[3]);
+            db[1] = make_uint4(hb[4], hb[5], hb[6], hb[7]);
+        } else {
+            const size_t head = (size_t)slot[m] * nkv + (s - nh - nkv);
+            __half* vh = att_vt + (head * 2 * kHdim) * n_ctx64 + p;
+            __half* vl = vh + (size_t)kHdim * n_ctx64;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const __half ah = __float2half_rn(a[j]), bh = __float2half_rn(b[j]);
+                vh[(size_t)(i0 + j) * n_ctx64] = ah;
+                vl[(size_t)(i0 + j) * n_ctx64] = __float2half_rn(a[j] - __half2float(ah));
+                vh[(size_t)(i0 + 32 + j) * n_ctx64] = bh;
+                vl[(size_t)(i0 + 32 + j) * n_ctx64] = __float2half_rn(b[j] - __half2float(bh));
+            }
         }
     }
 };
@@ -183,7 +221,8 @@ int tc_setup(Ctx& c, std::string& why) {
 }
 
 cudaError_t tc_gemm_qkv(const Ctx& c, int layer, int M, const PrefillEpi& p, cudaStream_t st) {
-    EpiQKV e{p.nh, p.nkv, p.n_ctx, p.L, p.layer, p.q, p.kv, p.rope, p.bias, p.pos, p.slot, p.err};
+    EpiQKV e{p.nh, p.nkv, p.n_ctx, p.L, p.layer, p.q, p.kv, p.rope, p.bias, p.pos, p.slot, p.err,
+             c.ws.att_k, c.ws.att_vt, att_ctx64(p.n_ctx)};
     return launch<kBnQKV, kSplitQKV>(c, c.tc.a_xn, c.tc.a_xn_lo, c.tc.layers[layer].wqkv, M, c.nqkv, c.cfg.hidden,
                                      e, st);
 }
