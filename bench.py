@@ -159,8 +159,8 @@ def decode_bytes_per_step(shape, positions, q8: bool = False) -> float:
 # (profiles/decode_persistent_0p5b_b1_launches.md), valid only
 # for that workload and only while the kernel's sources -- their code, with
 # // comments and blank lines left out -- hash to `src`.
-TRAFFIC = {"k_decode_persistent": {"workload": "0.5b-decode-b1", "src": "bc3e88d4f74ebdc1", "bytes": 1003649792.0}}
-KERNEL_SOURCES = ("persistent.cu", "persistent.h", "rowdot.cuh", "common.cuh", "attn.cuh", "ctx.h")
+TRAFFIC = {"k_decode_persistent": {"workload": "0.5b-decode-b1", "src": "45812fb3f0393c9d", "bytes": 1003649792.0}}
+KERNEL_SOURCES = ("persistent.cu", "persistent.h", "rowdot.cuh", "common.cuh", "attn.cuh", "ctx.h", "sm100.cuh")
 
 
 def kernel_source_hash() -> str:
