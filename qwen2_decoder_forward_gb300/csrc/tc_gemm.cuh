@@ -37,7 +37,10 @@ struct GemmCfg {
     static constexpr int kBOff = SPLIT ? 2 * kABytes : kABytes;
     static constexpr int kBBytes = BN * kBK * 2;
     static constexpr int kStageBytes = kBOff + kBBytes;
-    static constexpr int kStages = (192 * 1024) / kStageBytes;
+    // As many stages as 220 KB holds: a CTA's loads in flight are bounded by
+    // the ring, and the long-k products (down: 76 k-blocks a tile) keep the
+    // tensor pipe fed only with the deepest ring that fits.
+    static constexpr int kStages = (220 * 1024) / kStageBytes;
     // Two accumulators of BN columns, each at a power-of-two column offset
     // (kAccCols apart); the allocation is a power of two as well.
     static constexpr uint32_t kAccCols = BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
