@@ -155,6 +155,15 @@ __device__ __forceinline__ bool seg_start(const int* base, const int* nch, int b
 // the 16-byte chunk f / 4 of row r sits at chunk (f / 4) ^ (r % 8).
 __device__ __forceinline__ int swz(int row, int f) { return row * 32 + ((((f >> 2) ^ (row & 7)) << 2) | (f & 3)); }
 
+// Four 8 x 8 matrices of 16-bit elements from shared memory (each lane
+// gives one 16-byte row address); for 32-bit data each matrix is 8 rows x 4
+// words and thread i receives word i % 4 of row i / 4.
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const float* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"((uint32_t)__cvta_generic_to_shared(p)));
+}
+
 __device__ __forceinline__ uint32_t tf32_rn(float x) {
     uint32_t r;
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
@@ -327,16 +336,23 @@ __global__ void __launch_bounds__(fd::kThreads, 2)
             const float* Vt = sm.ring[s][1][0];
             // Scores S^T[key0 + g8 (+8)][h0, h1] over the 64 dims, as two
             // independent chains (dims 0-31, 32-63) added at the end.
+            // The A fragment of each 8-dim step in one ldmatrix.x4: matrix
+            // j (lanes 8j .. 8j + 7 give its row addresses) is keys key0 +
+            // 8 (j & 1) + 0..7 by the 4 dims (16 bytes) 4 (j >> 1) .. + 3 of
+            // the step, so thread (g8, t4) receives K[key0 + g8 (+8)][dim
+            // t4 (+4)] as fragments a0..a3.
             float sc[4] = {0.f, 0.f, 0.f, 0.f}, sc2[4] = {0.f, 0.f, 0.f, 0.f};
+            const int lrow = key0 + (lane & 7) + 8 * ((lane >> 3) & 1);
+            const int lchunk = lane >> 4;  // 0: dims 0-3 of the step, 1: dims 4-7
 #pragma unroll
             for (int s8 = 0; s8 < 8; ++s8) {
                 const float* Kh = Kt + (s8 >> 2) * kHalf;
-                const int f = 8 * (s8 & 3) + t4;
+                const int c = 2 * (s8 & 3) + lchunk;  // 16-byte chunk of the row's 128 bytes
+                uint32_t r[4];
+                ldsm_x4(r, Kh + lrow * 32 + ((c ^ (lrow & 7)) << 2));
                 uint32_t af[4];
-                af[0] = tf32_rn(Kh[swz(key0 + g8, f)]);
-                af[1] = tf32_rn(Kh[swz(key0 + g8 + 8, f)]);
-                af[2] = tf32_rn(Kh[swz(key0 + g8, f + 4)]);
-                af[3] = tf32_rn(Kh[swz(key0 + g8 + 8, f + 4)]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) af[i] = tf32_rn(__uint_as_float(r[i]));
                 if (s8 < 4) mma_tf32(sc, af, qb[s8][0], qb[s8][1]);
                 else mma_tf32(sc2, af, qb[s8][0], qb[s8][1]);
             }
