@@ -233,7 +233,10 @@ __global__ void __launch_bounds__(fd::kThreads, 2)
         return;
     }
     pdl_launch_dependents();
-    pdl_wait();  // q, positions and the new keys come from the previous kernel
+    // Positions and slots are written only by the LM head at the end of the
+    // previous step, which has completed before this step's first kernel
+    // (launched without the PDL attribute) starts: the row table can be
+    // built while the previous kernel drains.
     if (warp == 0) {
         row_table(a, sm.base, sm.nch, sm.posv, sm.slotv);
         if (lane == 0) sm.abort = 0;
@@ -246,6 +249,7 @@ __global__ void __launch_bounds__(fd::kThreads, 2)
         sm100::mbar_init_fence();
     }
     __syncthreads();
+    pdl_wait();  // q and the new keys come from the previous kernel
     const unsigned U = (unsigned)sm.base[a.B], G = gridDim.x;
     const int u0 = unit_start(blockIdx.x, U, G), u1 = unit_start(blockIdx.x + 1, U, G);
 
@@ -496,7 +500,8 @@ __global__ void __launch_bounds__(kMergeThreads) k_attn_merge(fd::Args a, int fl
     const int b = blockIdx.x / a.nkv, g = blockIdx.x % a.nkv;
     if (group > kGroupMax || a.B > kMaxRows || b >= a.B) return;
     pdl_launch_dependents();
-    pdl_wait();  // the attention's partials
+    // The row table and segment list depend on positions only (final for
+    // the step, as in k_attn_flash): built before the wait.
     if (warp == 0) {
         row_table(a, base, nch, nullptr, nullptr);
         __syncwarp();
@@ -511,6 +516,7 @@ __global__ void __launch_bounds__(kMergeThreads) k_attn_merge(fd::Args a, int fl
         if (lane == 0) nseg_s = __popc(m0) + __popc(m1);
     }
     __syncthreads();
+    pdl_wait();  // the attention's partials
     const int nseg = nseg_s;
     const int h = tid >> 6, d = tid & 63;
     if (nseg == 0 || h >= group) return;  // invalid position: reported by the attention
