@@ -327,8 +327,12 @@ __global__ void __launch_bounds__(W * 32) k_bgemm_q8s(Pro pro, int B, int K, int
         wd[r * nbl + b] = (uint16_t)ld_stream_u16(D + (size_t)(n_cta0 + r) * (K / 32) + kc0 / 32 + b);
     }
     pdl_launch_dependents();
+    // An epilogue whose set-up reads only what stays fixed for the step
+    // (positions, slots, biases, tables) does it while the previous kernel
+    // drains.
+    if (Epi::kStartBeforeWait) epi.start(n_cta0, kRowsCta, B);
     pdl_wait();
-    epi.start(n_cta0, kRowsCta, B);
+    if (!Epi::kStartBeforeWait) epi.start(n_cta0, kRowsCta, B);
     __syncthreads();
     const bool staged = pro.stage(ah, al, ld, Bc, K, kc0, kc, &bar[0]);
     const bool loaded = mbar_wait(&bar[1], 0, kWaitNs);

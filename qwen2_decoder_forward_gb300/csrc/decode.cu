@@ -501,6 +501,9 @@ __shared__ int qkv_pos_s[32], qkv_slot_s[32];
 __shared__ float qkv_bias_s[kQkvRowsMax];
 __shared__ float2 qkv_rope_s[32][kQkvRowsMax / 2];
 struct EpiQkvQ8 {
+    // start() reads positions, slots, biases and the RoPE table only: they
+    // stay fixed for the step, so it runs before griddepcontrol.wait.
+    static constexpr bool kStartBeforeWait = true;
     StepArgs a;
     int layer;
     const float* bias;
@@ -564,6 +567,8 @@ struct EpiQkvQ8 {
 constexpr int kResRowsMax = 16;
 __shared__ float res_x_s[32][kResRowsMax];
 struct EpiResidualQ8 {
+    // start() may read what the previous kernels write: after the wait.
+    static constexpr bool kStartBeforeWait = false;
     float* x;
     int H;
     int n_cta0 = 0;
@@ -590,6 +595,8 @@ struct EpiResidualQ8 {
 // part[chunk][b][n]; the last CTA of a row group to finish (all gridDim.y
 // chunks written) adds them to the residual x in chunk order.
 struct EpiDownQ8 {
+    // start() may read what the previous kernels write: after the wait.
+    static constexpr bool kStartBeforeWait = false;
     static constexpr int kMaxParts = 16;
     __device__ __forceinline__ void start(int, int, int) {}
     float* part;
@@ -651,6 +658,8 @@ struct EpiDownQ8 {
 // Packed rows (2j, 2j+1) = (gate j, up j): m[b][j] = SiLU(gate) * up, as
 // hi / lo (the operand of the down product).
 struct EpiSwigluQ8 {
+    // start() may read what the previous kernels write: after the wait.
+    static constexpr bool kStartBeforeWait = false;
     __half* hi;
     __half* lo;
     int I;
@@ -666,6 +675,8 @@ struct EpiSwigluQ8 {
 // per CTA the best (value, lowest index) of each row, then the last CTA to
 // finish merges them (and, for decode, feeds the ids back as next tokens).
 struct EpiLmQ8 {
+    // start() may read what the previous kernels write: after the wait.
+    static constexpr bool kStartBeforeWait = false;
     float* logits;
     int V, B;
     float* am_val;  // [gridDim][32]
