@@ -311,6 +311,37 @@ def test_tensor_core_prefill_in_chunks(q2, shape_name):
         m.synchronize()
 
 
+def test_tensor_core_prefill_at_unordered_positions(q2):
+    """Positions are data: one sequence's rows at the positions 69..0 in
+    reverse, another's at 0..29 and 40..69 (a gap that holds the cache's
+    zeros on both sides).  The tensor-core prefill then converts every key
+    up to each sequence's last position from the f32 cache (its rows are not
+    consecutive), against the oracle given the same positions."""
+    shape = synth.SHAPES["toy"]
+    w = synth.make_weights(shape, 0)
+    n_ctx = 128
+    a = synth.make_tokens(shape.vocab, 70, 31)
+    b = synth.make_tokens(shape.vocab, 60, 32)
+    pa = np.arange(69, -1, -1)
+    pb = np.r_[0:30, 40:70]
+    orc = oracle.build_oracle(shape, w, n_ctx)
+    ca, cb = orc.new_cache(), orc.new_cache()
+    ra = orc.forward(ca, a, pa, n_out=2)
+    rb = orc.forward(cb, b, pb, n_out=2)
+    with q2.Qwen2Model(shape, w, n_ctx=n_ctx, max_seqs=2, max_tokens=192,
+                       prefill_mode=q2.PREFILL_TENSOR) as m:
+        logits, ids = m.prefill([0, 1], [a, b], positions=[pa, pb], n_out=2)
+        hid = m.final_hidden(4).cpu().numpy()
+        lg, ig = logits.cpu().numpy(), ids.cpu().numpy()
+        kv = m.kv_cache().cpu().numpy()
+        m.synchronize()
+    for s, (r, cache, pos) in enumerate(((ra, ca, pa), (rb, cb, pb))):
+        what = f"unordered tensor prefill seq {s}"
+        check_logits_ids(lg[2 * s:2 * s + 2], ig[2 * s:2 * s + 2], r["logits"], what)
+        check_hidden(hid[2 * s:2 * s + 2], r["final_norm_output"], what)
+        check_kv(kv[s], cache, np.sort(pos), what + " KV")
+
+
 def test_canary_check_finds_a_write_past_a_buffer(q2):
     """The guard words around the context's device buffers: a clean run
     passes the check; four bytes written just past the end of the KV cache
