@@ -4,7 +4,8 @@
 // head g serves query heads g*group .. g*group + group - 1; scores
 // q . k / sqrt(64) over keys 0..p).
 //
-// Two kernels per layer.
+// Two kernels per layer; the first (k_att_operands) only when keys stored
+// by an earlier call must be brought in.
 //
 // The attention reads its keys from f16 operand buffers laid out for TMA:
 // k as rows [slot][kv head][position][64 dims] and v transposed as an f16
