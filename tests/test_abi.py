@@ -80,6 +80,8 @@ def test_null_arguments_are_rejected(L):
     h = ctypes.c_void_p()
     assert L.qwen2_create(None, None, ctypes.byref(h)) == q2.QWEN2_E_ARG
     assert L.qwen2_create(None, None, None) == q2.QWEN2_E_ARG
+    # The debug checks of a context refuse a null context on the host.
+    assert L.qwen2_check_canaries(None) == q2.QWEN2_E_ARG
 
 
 def test_q8_0_packer_matches_oracle_bytes(L):
