@@ -23,7 +23,7 @@
 // chunk (the KS warps of a group add their partials in a fixed order at the
 // end).  The CTA's weight tile is staged in shared memory by bulk copies
 // issued before anything else (k_bgemm_q8s); the LM head's persistent tile
-// walker instead keeps kDepth blocks per warp in flight in registers.  The
+// walker instead keeps about eight blocks per warp in flight in registers.  The
 // chunk's activation rows reach shared memory through a prologue: either one
 // bulk copy per row (hi and lo, issued by the 32 lanes of warp 0 on one
 // mbarrier), or an RMSNorm of f32 rows computed in the CTA (one warp per
@@ -39,7 +39,6 @@ namespace bg {
 constexpr int kThreads = 256;
 constexpr int kWarps = 8;
 constexpr int kKc = 1024;   // largest k chunk
-constexpr int kDepth = 4;   // weight blocks in flight per warp
 
 // Shared-memory row stride (halves) of a k chunk of kc columns: kc rounded
 // up to 64, plus 32, so consecutive rows sit 64 bytes apart modulo 128 and
@@ -94,14 +93,6 @@ __device__ __forceinline__ void split_h(float v, __half& hi, __half& lo) {
     lo = __float2half_rn(v - __half2float(hi));
 }
 
-// One 32-block of NTW n-tiles as this lane's fragment: 8 int8 values of
-// row n0 + 8t + gi, and the raw f16 scales of rows n0 + 8t + 2ti and
-// n0 + 8t + 2ti + 1 (converted at use, so the loads stay in flight).
-struct WeightBlock {
-    uint2 q;
-    uint32_t d0, d1;
-};
-
 __device__ __forceinline__ uint32_t ld_stream_u16(const void* p) {
     unsigned short v;
     asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
@@ -110,25 +101,6 @@ __device__ __forceinline__ uint32_t ld_stream_u16(const void* p) {
 
 __device__ __forceinline__ float h_bits_to_f(uint32_t bits) {
     return __half2float(__ushort_as_half((unsigned short)bits));
-}
-
-// Q4: Q holds [N][K / 2] bytes of codes; the lane's 8 codes are one word.
-template <int NTW, bool Q4 = false>
-__device__ __forceinline__ void load_block(const int8_t* __restrict__ Q, const __half* __restrict__ D, int N, int K,
-                                           int n0, int gi, int ti, int kg, WeightBlock (&w)[NTW]) {
-#pragma unroll
-    for (int t = 0; t < NTW; ++t) {
-        const int row = n0 + t * 8 + gi, rs = n0 + t * 8 + 2 * ti;
-        if (Q4)
-            w[t].q = row < N ? make_uint2(__ldg(reinterpret_cast<const unsigned*>(Q + (size_t)row * (K / 2) +
-                                                                                  (kg + 8 * ti) / 2)),
-                                          0u)
-                             : make_uint2(0u, 0u);
-        else
-            w[t].q = row < N ? ld_stream_u2(Q + (size_t)row * K + kg + 8 * ti) : make_uint2(0u, 0u);
-        w[t].d0 = rs < N ? ld_stream_u16(D + (size_t)rs * (K / 32) + kg / 32) : 0u;
-        w[t].d1 = rs + 1 < N ? ld_stream_u16(D + (size_t)(rs + 1) * (K / 32) + kg / 32) : 0u;
-    }
 }
 
 // ---- prologues: the chunk's activation rows into shared memory -------------
@@ -435,17 +407,102 @@ __global__ void __launch_bounds__(W * 32) k_bgemm_q8s(Pro pro, int B, int K, int
 
 // The same product for tall N (the LM head) with KS = 1: a persistent grid
 // whose CTA stages the activation rows once and then walks row tiles
-// blockIdx.x, blockIdx.x + gridDim.x, ...  Each warp's weight stream runs
-// straight on from one tile into the next (the DEPTH-deep register ring
-// refills with the next tile's first blocks while the current tile's last
-// blocks are multiplied).  Grid: up to the SM count (one CTA per SM); the
-// k chunk is the whole row (kc_len = K).  With LO = false only the f16 hi
-// part of the activations enters the MMAs (half the tensor work; the
-// activation then carries 11 bits, as in an f16 GEMM).
-template <int MT, int NTW, class Epi, class Pro, bool LO = true, bool Q4 = false, int DEPTH = kDepth>
+// blockIdx.x, blockIdx.x + gridDim.x, ...  Grid: up to the SM count (one
+// CTA per SM); the k chunk is the whole row (kc_len = K, a multiple of
+// 128).  With LO = false only the f16 hi part of the activations enters
+// the MMAs (half the tensor work; the activation then carries 11 bits, as
+// in an f16 GEMM).
+//
+// Each warp's weight stream is a sequence of groups of kWalkG consecutive
+// 32-blocks of its NTW n-tiles, running straight on from one tile into the
+// next, held in a ring of kWalkRing groups in registers: the ring slot a
+// group was read from is refilled, block by block as its blocks are
+// converted, with the group kWalkRing places ahead, so kWalkRing x kWalkG
+// blocks per warp stay in flight.  The load and compute positions advance
+// as (tile, group) counters, so the loop does no division, and a group's
+// scales (kWalkG f16 values per output row) come in one 8-byte load per
+// row.
+constexpr int kWalkG = 4;     // 32-blocks per group
+constexpr int kWalkRing = 1;  // groups in flight per warp
+
+// One group of one lane: the q words of its row of each n-tile (Q8: 8
+// bytes a block, Q4: 4 bytes) and the raw f16 scales of its two output
+// rows, two per 32-bit word (converted at use, so the loads stay in flight).
+template <int NTW, bool Q4>
+struct WalkGroup {
+    uint32_t q[NTW][kWalkG][Q4 ? 1 : 2];
+    uint32_t d0[NTW][kWalkG / 2], d1[NTW][kWalkG / 2];
+};
+
+// Where the lane's loads of one group start: the first q byte of its row
+// in n-tile 0 (tile t adds 8 t rows) and the first scale of its first
+// output row; the rows past N load zeros.
+struct WalkCursor {
+    const int8_t* q;
+    const __half* d;
+    int row, rs;  // the lane's q row and first output row in n-tile 0
+};
+
+template <bool Q4>
+__device__ __forceinline__ WalkCursor walk_cursor(const int8_t* __restrict__ Q, const __half* __restrict__ D, int K,
+                                                  int n_w, int g, int gi, int ti) {
+    const int nb = K / 32;
+    const int kb0 = g * kWalkG;
+    WalkCursor c;
+    c.row = n_w + gi;
+    c.rs = n_w + 2 * ti;
+    c.q = Q4 ? Q + (size_t)c.row * (K / 2) + kb0 * 16 + 4 * ti : Q + (size_t)c.row * K + kb0 * 32 + 8 * ti;
+    c.d = D + (size_t)c.rs * nb + kb0;
+    return c;
+}
+
+__device__ __forceinline__ uint32_t ld_stream_u32(const void* p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+// Block i of the group at cursor c into w.q[.][i].
+template <int NTW, bool Q4>
+__device__ __forceinline__ void walk_load_q(const WalkCursor& c, int K, int N, int i, WalkGroup<NTW, Q4>& w) {
+    const size_t tstride = Q4 ? (size_t)8 * (K / 2) : (size_t)8 * K;
+#pragma unroll
+    for (int t = 0; t < NTW; ++t) {
+        const int8_t* p = c.q + t * tstride + i * (Q4 ? 16 : 32);
+        const bool ok = c.row + 8 * t < N;
+        if (Q4) {
+            w.q[t][i][0] = ok ? ld_stream_u32(p) : 0u;
+        } else {
+            const uint2 v = ok ? ld_stream_u2(p) : make_uint2(0u, 0u);
+            w.q[t][i][0] = v.x;
+            w.q[t][i][Q4 ? 0 : 1] = v.y;
+        }
+    }
+}
+
+// The group's scales at cursor c into w.d0 / w.d1 (8-byte loads: K / 32
+// and the group's first block are multiples of 4).
+template <int NTW, bool Q4>
+__device__ __forceinline__ void walk_load_d(const WalkCursor& c, int K, int N, WalkGroup<NTW, Q4>& w) {
+    const int nb = K / 32;
+#pragma unroll
+    for (int t = 0; t < NTW; ++t) {
+        const __half* p = c.d + (size_t)8 * t * nb;
+        const int rs = c.rs + 8 * t;
+        const uint2 a = rs < N ? ld_stream_u2(p) : make_uint2(0u, 0u);
+        const uint2 b = rs + 1 < N ? ld_stream_u2(p + nb) : make_uint2(0u, 0u);
+        w.d0[t][0] = a.x;
+        w.d0[t][1] = a.y;
+        w.d1[t][0] = b.x;
+        w.d1[t][1] = b.y;
+    }
+}
+
+template <int MT, int NTW, class Epi, class Pro, bool LO = true, bool Q4 = false>
 __global__ void __launch_bounds__(kThreads) k_bgemm_q8_tiles(Pro pro, int B, int K, const int8_t* __restrict__ Q,
                                                              const __half* __restrict__ D, int N, Epi epi, int* err) {
     using namespace sm100;
+    static_assert(kWalkG == 4, "a group's scales are one 8-byte load per row");
     extern __shared__ __align__(16) unsigned char smem[];
     constexpr int kRows = MT * 16;
     constexpr int kRowsCta = kWarps * NTW * 8;
@@ -456,16 +513,27 @@ __global__ void __launch_bounds__(kThreads) k_bgemm_q8_tiles(Pro pro, int B, int
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gi = lane >> 2, ti = lane & 3;
     const int Bc = min(B, kRows);
-    const int nb = K / 32;
+    const int ng = K / (32 * kWalkG);  // groups per tile
     const int n_tiles = (N + kRowsCta - 1) / kRowsCta;
-    const int my_tiles = blockIdx.x < n_tiles ? (n_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-    const int total = my_tiles * nb;  // this warp's (tile, block) steps
-    auto step_n0 = [&](int s) { return (int)(blockIdx.x + (s / nb) * gridDim.x) * kRowsCta + warp * NTW * 8; };
+    const int wrow = warp * NTW * 8;   // the warp's first row within a tile
 
-    WeightBlock wq[DEPTH][NTW];
+    // The first kRing groups go out before the wait: weights do not depend
+    // on the previous kernel.
+    WalkGroup<NTW, Q4> wg[kWalkRing];
+    int l_tile = blockIdx.x, l_g = 0;  // the next group to load
 #pragma unroll
-    for (int i = 0; i < DEPTH; ++i)
-        if (i < total) load_block<NTW, Q4>(Q, D, N, K, step_n0(i), gi, ti, (i % nb) * 32, wq[i]);
+    for (int r = 0; r < kWalkRing; ++r) {
+        if (l_tile < n_tiles) {
+            const WalkCursor c = walk_cursor<Q4>(Q, D, K, l_tile * kRowsCta + wrow, l_g, gi, ti);
+#pragma unroll
+            for (int i = 0; i < kWalkG; ++i) walk_load_q<NTW, Q4>(c, K, N, i, wg[r]);
+            walk_load_d<NTW, Q4>(c, K, N, wg[r]);
+        }
+        if (++l_g == ng) {
+            l_g = 0;
+            l_tile += gridDim.x;
+        }
+    }
     pdl_launch_dependents();
     pdl_wait();  // the activation rows come from the previous kernel
     epi.start(0, 0, B);
@@ -483,54 +551,66 @@ __global__ void __launch_bounds__(kThreads) k_bgemm_q8_tiles(Pro pro, int B, int
 #pragma unroll
         for (int t = 0; t < NTW; ++t) acc[m][t][0] = acc[m][t][1] = acc[m][t][2] = acc[m][t][3] = 0.f;
     if (staged) {
-        for (int s0 = 0; s0 < total; s0 += DEPTH) {
+        int c_tile = blockIdx.x, c_g = 0;  // the group being multiplied
+        while (c_tile < n_tiles) {
 #pragma unroll
-            for (int i = 0; i < DEPTH; ++i) {
-                const int s = s0 + i;
-                if (s < total) {
-                    const int kb = s % nb;
-                    uint32_t bw[NTW][4];
-                    float dsc[NTW][2];
+            for (int r = 0; r < kWalkRing; ++r) {
+                if (c_tile < n_tiles) {
+                    const bool refill = l_tile < n_tiles;
+                    const WalkCursor lc = walk_cursor<Q4>(Q, D, K, l_tile * kRowsCta + wrow, l_g, gi, ti);
 #pragma unroll
-                    for (int t = 0; t < NTW; ++t) {
-                        const WeightBlock& wb = wq[i][t];
-                        if (Q4) {
-                            q4x8_to_h2(wb.q.x, bw[t]);
-                        } else {
-                            bw[t][0] = i8x2_to_h2(wb.q.x, 0x4140u);
-                            bw[t][1] = i8x2_to_h2(wb.q.x, 0x4342u);
-                            bw[t][2] = i8x2_to_h2(wb.q.y, 0x4140u);
-                            bw[t][3] = i8x2_to_h2(wb.q.y, 0x4342u);
-                        }
-                        dsc[t][0] = h_bits_to_f(wb.d0);
-                        dsc[t][1] = h_bits_to_f(wb.d1);
-                    }
-                    if (s + DEPTH < total)
-                        load_block<NTW, Q4>(Q, D, N, K, step_n0(s + DEPTH), gi, ti, ((s + DEPTH) % nb) * 32, wq[i]);
-#pragma unroll
-                    for (int m = 0; m < MT; ++m) {
-                        const __half* hr = ah + (m * 16 + gi) * ld + kb * 32 + 8 * ti;
-                        const __half* lr = al + (m * 16 + gi) * ld + kb * 32 + 8 * ti;
-                        const uint4 h0 = *reinterpret_cast<const uint4*>(hr);
-                        const uint4 h1 = *reinterpret_cast<const uint4*>(hr + 8 * ld);
-                        const uint4 l0 = LO ? *reinterpret_cast<const uint4*>(lr) : make_uint4(0u, 0u, 0u, 0u);
-                        const uint4 l1 = LO ? *reinterpret_cast<const uint4*>(lr + 8 * ld) : make_uint4(0u, 0u, 0u, 0u);
+                    for (int i = 0; i < kWalkG; ++i) {
+                        const int kb = c_g * kWalkG + i;
+                        uint32_t bw[NTW][4];
+                        float dsc[NTW][2];
 #pragma unroll
                         for (int t = 0; t < NTW; ++t) {
-                            float p[4] = {0.f, 0.f, 0.f, 0.f};
-                            mma16816(p, h0.x, h1.x, h0.y, h1.y, bw[t][0], bw[t][1]);
-                            if (LO) mma16816(p, l0.x, l1.x, l0.y, l1.y, bw[t][0], bw[t][1]);
-                            mma16816(p, h0.z, h1.z, h0.w, h1.w, bw[t][2], bw[t][3]);
-                            if (LO) mma16816(p, l0.z, l1.z, l0.w, l1.w, bw[t][2], bw[t][3]);
-                            acc[m][t][0] = fmaf(dsc[t][0], p[0], acc[m][t][0]);
-                            acc[m][t][1] = fmaf(dsc[t][1], p[1], acc[m][t][1]);
-                            acc[m][t][2] = fmaf(dsc[t][0], p[2], acc[m][t][2]);
-                            acc[m][t][3] = fmaf(dsc[t][1], p[3], acc[m][t][3]);
+                            if (Q4) {
+                                q4x8_to_h2(wg[r].q[t][i][0], bw[t]);
+                            } else {
+                                bw[t][0] = i8x2_to_h2(wg[r].q[t][i][0], 0x4140u);
+                                bw[t][1] = i8x2_to_h2(wg[r].q[t][i][0], 0x4342u);
+                                bw[t][2] = i8x2_to_h2(wg[r].q[t][i][Q4 ? 0 : 1], 0x4140u);
+                                bw[t][3] = i8x2_to_h2(wg[r].q[t][i][Q4 ? 0 : 1], 0x4342u);
+                            }
+                            const uint32_t w0 = wg[r].d0[t][i >> 1], w1 = wg[r].d1[t][i >> 1];
+                            dsc[t][0] = h_bits_to_f((i & 1) ? (w0 >> 16) : (w0 & 0xffffu));
+                            dsc[t][1] = h_bits_to_f((i & 1) ? (w1 >> 16) : (w1 & 0xffffu));
+                        }
+                        if (refill) {
+                            walk_load_q<NTW, Q4>(lc, K, N, i, wg[r]);
+                            if (i == kWalkG - 1) walk_load_d<NTW, Q4>(lc, K, N, wg[r]);
+                        }
+#pragma unroll
+                        for (int m = 0; m < MT; ++m) {
+                            const __half* hr = ah + (m * 16 + gi) * ld + kb * 32 + 8 * ti;
+                            const __half* lr = al + (m * 16 + gi) * ld + kb * 32 + 8 * ti;
+                            const uint4 h0 = *reinterpret_cast<const uint4*>(hr);
+                            const uint4 h1 = *reinterpret_cast<const uint4*>(hr + 8 * ld);
+                            const uint4 l0 = LO ? *reinterpret_cast<const uint4*>(lr) : make_uint4(0u, 0u, 0u, 0u);
+                            const uint4 l1 =
+                                LO ? *reinterpret_cast<const uint4*>(lr + 8 * ld) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                            for (int t = 0; t < NTW; ++t) {
+                                float p[4] = {0.f, 0.f, 0.f, 0.f};
+                                mma16816(p, h0.x, h1.x, h0.y, h1.y, bw[t][0], bw[t][1]);
+                                if (LO) mma16816(p, l0.x, l1.x, l0.y, l1.y, bw[t][0], bw[t][1]);
+                                mma16816(p, h0.z, h1.z, h0.w, h1.w, bw[t][2], bw[t][3]);
+                                if (LO) mma16816(p, l0.z, l1.z, l0.w, l1.w, bw[t][2], bw[t][3]);
+                                acc[m][t][0] = fmaf(dsc[t][0], p[0], acc[m][t][0]);
+                                acc[m][t][1] = fmaf(dsc[t][1], p[1], acc[m][t][1]);
+                                acc[m][t][2] = fmaf(dsc[t][0], p[2], acc[m][t][2]);
+                                acc[m][t][3] = fmaf(dsc[t][1], p[3], acc[m][t][3]);
+                            }
                         }
                     }
-                    if (kb == nb - 1) {
-                        // The tile's last block: its outputs, then a fresh tile.
-                        const int n0 = step_n0(s);
+                    if (++l_g == ng) {
+                        l_g = 0;
+                        l_tile += gridDim.x;
+                    }
+                    if (++c_g == ng) {
+                        // The tile's last group: its outputs, then a fresh tile.
+                        const int n0 = c_tile * kRowsCta + wrow;
 #pragma unroll
                         for (int m = 0; m < MT; ++m)
 #pragma unroll
@@ -543,6 +623,8 @@ __global__ void __launch_bounds__(kThreads) k_bgemm_q8_tiles(Pro pro, int B, int
                                 }
                                 acc[m][t][0] = acc[m][t][1] = acc[m][t][2] = acc[m][t][3] = 0.f;
                             }
+                        c_g = 0;
+                        c_tile += gridDim.x;
                     }
                 }
             }
