@@ -449,8 +449,9 @@ def run_prefill(args, wl, shape, weights, reps, world):
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "f16 tensor-core operands (activations of Q/K/V, o_proj and gate/up as f16 hi/lo pairs; "
-                     "attention q, k, p in f16 and v as an f16 hi/lo pair), f32 accumulation, f32 "
+            "dtype": "f16 tensor-core operands (activations of Q/K/V, o_proj and gate/up as f16 hi/lo pairs, "
+                     "down's as f16; attention q, k, p in f16 and v as an f16 hi/lo pair; the kept rows' LM "
+                     "head as f16 hi/lo rows against the f16 embedding), f32 accumulation, f32 "
                      "residual/softmax/KV" if tensor else "f32",
             "data": "synthetic (seeded random weights of the Qwen2.5-0.5B shape, uniform-random tokens)",
             "config": workload_config(wl, shape, world), "clocks": clocks.summary(),
